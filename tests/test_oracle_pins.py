@@ -1,0 +1,384 @@
+"""Pins of the FP64 oracle to things other than itself.
+
+Each test fixes one part of the oracle against hand-worked encodings of the
+number formats, brute force on tiny inputs, invariants of the method, or an
+independent library conversion, so that a dropped term, a wrong sign or index
+or a transposed operand fails at least one of them.  CPU only.
+"""
+
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import mla_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_table(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                rows.append(line.split())
+    return rows
+
+
+# ---------------------------------------------------------------- bfloat16
+
+
+@pytest.mark.parametrize(
+    "value,bits",
+    [
+        (1.0, 0x3F80),
+        (-2.0, 0xC000),
+        (3.0, 0x4040),
+        (0.1, 0x3DCD),  # 1.6 * 2**-4: mantissa 76.8 -> 77
+        (1.0 + 2.0**-8, 0x3F80),  # tie -> even
+        (1.0 + 3 * 2.0**-8, 0x3F82),  # tie -> even
+        (1.0 + 2.0**-8 + 2.0**-30, 0x3F81),  # just above the tie
+        ((2.0 - 2.0**-7) * 2.0**127, 0x7F7F),  # largest finite
+        (2.0**-133, 0x0001),  # smallest subnormal
+        (2.0**-134, 0x0000),  # tie with zero -> even
+        (3 * 2.0**-134, 0x0002),  # tie -> even
+        (-0.0, 0x8000),
+    ],
+)
+def test_bf16_hand_worked(value, bits):
+    assert int(O.f64_to_bf16_bits(np.array([value]))[0]) == bits
+
+
+def test_bf16_matches_torch_cast_on_binary32_values():
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal(200_000) * np.exp(rng.uniform(-30, 30, 200_000))).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = O.f64_to_bf16_bits(x.astype(np.float64))
+    assert np.array_equal(got, ref)
+
+
+def test_bf16_decode_roundtrip():
+    bits = np.arange(0, 1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = O.bf16_bits_to_f64(bits)
+    finite = np.isfinite(vals)
+    assert np.array_equal(O.f64_to_bf16_bits(vals[finite]), bits[finite])
+
+
+# ---------------------------------------------------------------- E4M3
+
+
+def test_e4m3_hand_worked_table():
+    for value, code in _read_table("e4m3_codes.txt"):
+        got = int(O.e4m3_satfinite(np.array([float(value)]))[0])
+        assert got == int(code, 16), (value, hex(got), code)
+
+
+def test_e4m3_decode_matches_torch_and_roundtrips():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float32).numpy()
+    got = O.e4m3_to_f64(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    fin = ~np.isnan(ref)
+    assert np.array_equal(got[fin], ref[fin].astype(np.float64))
+    assert np.array_equal(O.e4m3_satfinite(got[fin]), codes[fin])
+
+
+def test_e4m3_matches_torch_cast_in_range():
+    rng = np.random.default_rng(12)
+    x = (rng.standard_normal(200_000) * np.exp(rng.uniform(-12, 6.5, 200_000))).astype(np.float32)
+    x = x[np.abs(x) < 464.0]
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = O.e4m3_satfinite(x.astype(np.float64))
+    assert np.array_equal(got, ref)
+
+
+def test_e4m3_saturates_never_nan():
+    big = np.array([448.0, 463.99, 464.0, 500.0, 1e6, -1e6, -470.0])
+    codes = O.e4m3_satfinite(big)
+    assert set(codes.tolist()) <= {0x7E, 0xFE}
+
+
+# ---------------------------------------------------------------- pow2_ceil
+
+
+def _page_pow2_ceil(v32: np.ndarray) -> np.ndarray:
+    """The integer form printed with pow2_ceil: take the binary32 bits, keep the
+    exponent field, add one if any mantissa bit is set, shift back."""
+    bits = v32.astype(np.float32).view(np.uint32)
+    e = bits >> np.uint32(23)
+    e = e + (bits & np.uint32(0x7FFFFF) != 0).astype(np.uint32)
+    return (e << np.uint32(23)).view(np.float32).astype(np.float64)
+
+
+def test_pow2_ceil_table():
+    for kind, v, want in _read_table("pow2_ceil.txt"):
+        v, want = float(v), float(want)
+        got = O.pow2_ceil(np.float32(v)) if kind == "p2c" else O.ds_tile_scale(v)
+        assert float(got) == want, (kind, v, float(got), want)
+
+
+def test_pow2_ceil_matches_integer_form():
+    rng = np.random.default_rng(13)
+    v = np.exp2(rng.uniform(-120, 120, 300_000)).astype(np.float32)
+    v = np.concatenate([v, np.exp2(np.arange(-126, 127)).astype(np.float32)])
+    assert np.array_equal(O.pow2_ceil(v.astype(np.float64)), _page_pow2_ceil(v))
+
+
+def test_ds_tile_scale_uses_division_by_448():
+    # amax = 1.75 * 2**k gives exactly 2**(k-8) only with a correctly rounded
+    # division; every such scale must be the exact power of two.
+    for k in range(-10, 12):
+        assert float(O.ds_tile_scale(1.75 * 2.0**k)) == max(2.0 ** (k - 8), 2.0**-13)
+
+
+# ---------------------------------------------------------------- RMSNorm
+
+
+def test_rmsnorm_worked_example():
+    out = O.rmsnorm(np.array([[3.0, 4.0]]), np.ones(2), 0.0)
+    assert np.allclose(out, [[3 / math.sqrt(12.5), 4 / math.sqrt(12.5)]], rtol=0, atol=1e-15)
+    assert abs(out[0, 0] - 0.848528137423857) < 1e-14
+    assert abs(out[0, 1] - 1.131370849898476) < 1e-14
+
+
+def test_rmsnorm_gamma_and_eps():
+    out = O.rmsnorm(np.array([[3.0, 4.0]]), np.array([2.0, 0.5]), 0.0)
+    assert np.allclose(out, [[6 / math.sqrt(12.5), 2 / math.sqrt(12.5)]], atol=1e-15)
+    # eps is added to the mean of squares, not to the root
+    out = O.rmsnorm(np.array([[1.0, 1.0]]), np.ones(2), 3.0)
+    assert np.allclose(out, [[0.5, 0.5]], atol=1e-15)
+
+
+def test_rmsnorm_scale_invariance():
+    rng = np.random.default_rng(14)
+    x = rng.standard_normal((4, 1536))
+    g = 1 + 0.1 * rng.standard_normal(1536)
+    a = O.rmsnorm(x, g, 0.0)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    for c in (0.1, 3.0, 10.0):
+        # without eps the norm is exactly scale-free
+        assert np.max(np.abs(a - O.rmsnorm(c * x, g, 0.0)) / np.abs(a)) < 1e-13
+        # with eps the change is the closed-form factor sqrt((ms+eps)/(ms+eps/c^2))
+        b = O.rmsnorm(c * x, g, 1e-6)
+        ratio = np.sqrt((ms + 1e-6) / (ms + 1e-6 / c**2))
+        assert np.max(np.abs(b / O.rmsnorm(x, g, 1e-6) - ratio)) < 1e-13
+
+
+# ---------------------------------------------------------------- Q_B and W_UK
+
+
+def test_q_projection_brute_force():
+    rng = np.random.default_rng(15)
+    B, H = 2, 2
+    xq = rng.standard_normal((B, 1536))
+    w = rng.standard_normal((H * 192, 1536))
+    q, cond = O.q_projection(xq, w, H)
+    for b in range(B):
+        for h in range(H):
+            for p in (0, 1, 77, 127, 128, 150, 191):
+                s = 0.0
+                a = 0.0
+                for k in range(1536):
+                    s += xq[b, k] * w[h * 192 + p, k]
+                    a += abs(xq[b, k] * w[h * 192 + p, k])
+                assert abs(q[b, h, p] - s) <= 1e-12 * a
+                assert abs(cond[b, h, p] - a) <= 1e-12 * a
+
+
+def test_q_projection_one_hot_indexing():
+    H = 3
+    w = np.arange(H * 192 * 1536, dtype=np.float64).reshape(H * 192, 1536)
+    for k in (0, 5, 1535):
+        xq = np.zeros((1, 1536))
+        xq[0, k] = 1.0
+        q, _ = O.q_projection(xq, w, H)
+        for h in range(H):
+            for p in (0, 127, 128, 191):
+                assert q[0, h, p] == w[h * 192 + p, k]
+
+
+def test_absorb_brute_force_and_one_hot():
+    rng = np.random.default_rng(16)
+    B, H = 2, 2
+    qn = rng.standard_normal((B, H, 128))
+    w = rng.standard_normal((H, 128, 512))
+    lat, cond = O.absorb(qn, w)
+    for b in range(B):
+        for h in range(H):
+            for c in (0, 1, 255, 511):
+                s = sum(qn[b, h, p] * w[h, p, c] for p in range(128))
+                a = sum(abs(qn[b, h, p] * w[h, p, c]) for p in range(128))
+                assert abs(lat[b, h, c] - s) <= 1e-12 * a
+                assert abs(cond[b, h, c] - a) <= 1e-12 * a
+    e = np.zeros((1, H, 128))
+    e[0, 1, 37] = 1.0
+    lat, _ = O.absorb(e, w)
+    assert np.array_equal(lat[0, 1], w[1, 37])
+    assert np.all(lat[0, 0] == 0)
+
+
+def test_absorb_equals_unabsorbed_score():
+    """q_nope . (W_UK[h] @ c) == (absorbed q) . c for any latent vector c: the
+    absorbed query scores a latent KV row exactly as the unabsorbed query scores
+    the key it up-projects to."""
+    rng = np.random.default_rng(17)
+    H = 3
+    qn = rng.standard_normal((2, H, 128))
+    w = rng.standard_normal((H, 128, 512))
+    lat, _ = O.absorb(qn, w)
+    c = rng.standard_normal(512)
+    for b in range(2):
+        for h in range(H):
+            k_nope = w[h] @ c
+            lhs = qn[b, h] @ k_nope
+            rhs = lat[b, h] @ c
+            assert abs(lhs - rhs) <= 1e-12 * (np.abs(qn[b, h]) @ np.abs(w[h]) @ np.abs(c))
+
+
+# ---------------------------------------------------------------- KV rows
+
+
+def _bf16(vals):
+    return O.f64_to_bf16_bits(np.asarray(vals, dtype=np.float64))
+
+
+def _hand_inputs(layout, pages=2, page_size=4, slots=(5,), H=1):
+    B = len(slots)
+    row = 656 if layout == 1 else 576
+    rng = np.random.default_rng(18)
+    cache = rng.integers(0, 256, (pages, page_size, row), dtype=np.uint8)
+    return dict(
+        w_qb=_bf16(np.zeros((H * 192, 1536))),
+        w_uk=_bf16(np.zeros((H, 128, 512))),
+        gamma_q=_bf16(np.ones(1536)),
+        gamma_kv=_bf16(np.ones(512)),
+        q_a=_bf16(np.ones((B, 1536))),
+        kv_c=_bf16(np.ones((B, 512))),
+        k_pe=_bf16(np.full((B, 64), 2.0)),
+        slots=np.array(slots, dtype=np.int64),
+        cache=cache,
+        layout=layout,
+        k_scale=0.05,
+        eps=1e-6,
+    )
+
+
+def test_kv_row_per_tensor_worked():
+    # kv_c = 1 -> normed = bf16(1/sqrt(1 + 1e-6)) = 1.0; 1.0 / fp32(0.05) rounds
+    # to 20.0 -> E4M3 0x5A; k_pe 2.0 / 0.05 -> 40.0 -> 0x62.
+    inp = _hand_inputs(0)
+    out = O.decode_step(inp)
+    row = out["cache"][1, 1]  # slot 5, page size 4
+    assert np.all(row[:512] == 0x5A)
+    assert np.all(row[512:] == 0x62)
+    other = np.ones(inp["cache"].shape[:2], bool)
+    other[1, 1] = False
+    assert np.array_equal(out["cache"][other], inp["cache"][other])
+
+
+def test_kv_row_ds_worked():
+    # normed = 1.0 -> amax 1 -> 1/448 -> scale 2**-8; 1.0 * 256 -> E4M3 0x78;
+    # scale bits 0x3B800000 little-endian; k_pe BF16 2.0 = 0x4000 little-endian.
+    inp = _hand_inputs(1)
+    out = O.decode_step(inp)
+    row = out["cache"][1, 1]
+    assert np.all(row[:512] == 0x78)
+    assert list(row[512:528]) == [0x00, 0x00, 0x80, 0x3B] * 4
+    assert list(row[528:]) == [0x00, 0x40] * 64
+
+
+def test_kv_ds_scale_per_tile_and_k_pe_raw():
+    inp = _hand_inputs(1)
+    kv = np.ones((1, 512))
+    kv[0, 128:256] *= 8.0  # tile 1 larger
+    kv[0, 300] = 64.0  # one big value in tile 2
+    inp["kv_c"] = _bf16(kv)
+    kpe = np.linspace(-3, 3, 64)[None]
+    inp["k_pe"] = _bf16(kpe)
+    out = O.decode_step(inp)
+    row = out["cache"][1, 1]
+    scales = row[512:528].view("<f4").astype(np.float64)
+    n = out["kv_normed"][0]
+    for t in range(4):
+        want = O.pow2_ceil(max(np.float32(np.max(np.abs(n[128 * t:128 * t + 128])) / 448), np.float32(1e-4)))
+        assert scales[t] == want
+    assert scales[1] > scales[0] and scales[2] > scales[1]
+    assert np.array_equal(row[528:].view("<u2"), inp["k_pe"][0])
+    # the element holding a tile's amax maps near the top of the E4M3 range
+    assert O.e4m3_to_f64(row[300:301])[0] * scales[2] == pytest.approx(n[300], rel=2**-3)
+
+
+def test_slot_math_every_slot():
+    pages, ps = 3, 4
+    slots = list(range(pages * ps)) + [-1]
+    for layout in (0, 1):
+        inp = _hand_inputs(layout, pages=pages, page_size=ps, slots=slots)
+        kv = np.tile(np.linspace(0.5, 2.0, 512), (len(slots), 1)) * np.arange(1, len(slots) + 1)[:, None]
+        inp["kv_c"] = _bf16(kv)
+        out = O.decode_step(inp)
+        for b, s in enumerate(slots[:-1]):
+            one = dict(inp)
+            one.update(
+                kv_c=inp["kv_c"][b:b + 1], k_pe=inp["k_pe"][b:b + 1],
+                q_a=inp["q_a"][b:b + 1], slots=np.array([s]),
+            )
+            row = O.decode_step(one)["cache"][s // ps, s % ps]
+            assert np.array_equal(out["cache"][s // ps, s % ps], row)
+            if layout == 0:
+                # one byte the hand derivation fixes: normed = bf16 of the row/rms
+                assert row.shape == (576,)
+
+
+def test_negative_and_out_of_range_slots_are_skipped():
+    inp = _hand_inputs(0, pages=2, page_size=4, slots=(-1, 8, 100))
+    out = O.decode_step(inp)
+    assert np.array_equal(out["cache"], inp["cache"])
+    assert out["bad_slots"] == [1, 2]
+
+
+# ---------------------------------------------------------------- whole step
+
+
+def test_decode_step_constructed_example():
+    """A step whose every output follows by hand: q_a = 1 and gamma = 1 give
+    xq = bf16(1/sqrt(1+eps)) = 1; row p of every head is constant
+    (p+1) * 2**-12, so q[p] = bf16(0.375 (p+1)); W_UK[h, p, c] = 3 * 2**-8 when
+    p == c % 128, so q_latent[c] = bf16(3 * 2**-8 * q[c % 128]) (the rounded q)."""
+    H = 2
+    inp = _hand_inputs(0, H=H, slots=(2,))
+    w_qb = np.zeros((H * 192, 1536))
+    for h in range(H):
+        for p in range(192):
+            w_qb[h * 192 + p, :] = (p + 1) * 2.0**-12 * (1 + h)
+    w_uk = np.zeros((H, 128, 512))
+    for c in range(512):
+        w_uk[:, c % 128, c] = 3 * 2.0**-8
+    inp["w_qb"] = _bf16(w_qb)
+    inp["w_uk"] = _bf16(w_uk)
+    out = O.decode_step(inp)
+    assert np.all(out["q_c"] == 0x3F80)
+    for h in range(H):
+        q = O.round_to_bf16(0.375 * np.arange(1, 193) * (1 + h))
+        assert np.array_equal(O.bf16_bits_to_f64(out["q_pe"][0, h]), q[128:])
+        want = O.round_to_bf16(3 * 2.0**-8 * q[np.arange(512) % 128])
+        assert np.array_equal(O.bf16_bits_to_f64(out["q_latent"][0, h]), want)
+    # the unrounded q would give a different latent for some columns
+    qx = 0.375 * np.arange(1, 129)
+    assert np.any(O.round_to_bf16(3 * 2.0**-8 * qx) != O.round_to_bf16(3 * 2.0**-8 * O.round_to_bf16(qx)))
+
+
+def test_decode_step_shapes_on_a_workload():
+    from mla_query_projection_gb300 import synthetic as S
+
+    inp = S.workload_inputs("tiny_b1_h16_e4m3")
+    out = O.decode_step(inp)
+    assert out["q_c"].shape == (1, 1536)
+    assert out["q_pe"].shape == (1, 16, 64)
+    assert out["q_latent"].shape == (1, 16, 512)
+    assert out["cache"].shape == (8, 64, 576)
+    changed = np.any(out["cache"] != inp["cache"], axis=-1)
+    s = int(inp["slots"][0])
+    assert changed.sum() == 1 and changed[s // 64, s % 64]
