@@ -1,0 +1,169 @@
+/*
+ * mla_query.h - C ABI of the GB300 (sm_103a) decode-step MLA query library.
+ *
+ * One call of mla_query_decode runs the query side of one Multi-head Latent
+ * Attention decode step on one GPU, as the vLLM API page "mla.query" (module
+ * vllm/models/kimi_k3/nvidia/specialized_decode/cutedsl/mla/query.py, class
+ * MlaQuery) defines it:
+ *
+ *   1. q_a RMSNorm (class MlaQuery, method kernel):
+ *        xq[b,k] = bf16((q_a[b,k] * rr) * gamma_q[k]),
+ *        rr = 1/sqrt(sum_k q_a[b,k]^2 / 1536 + eps);          xq is also q_c.
+ *   2. Q_B projection (method kernel): for every head h and p < 192,
+ *        q[b,h,p] = bf16(sum_k xq[b,k] * W_QB[h*192+p, k])  (FP32 accumulate).
+ *   3. rope split: q_pe[b,h,i] = q[b,h,128+i], i < 64 (no rotation here).
+ *   4. W_UK absorption (method kernel):
+ *        q_latent[b,h,c] = bf16(sum_{p<128} q[b,h,p] * W_UK[h,p,c]).
+ *   5. KV insert (methods insert, kv_fp8, insert_ds; function pow2_ceil):
+ *        n = bf16((kv_c * rr_kv) * gamma_kv), rr_kv = 1/sqrt(sum kv_c^2/512 + eps),
+ *        written with k_pe into the paged FP8 cache row of slot_mapping[b].
+ *
+ * Conventions.  All tensors are caller-owned device memory unless stated.
+ * BF16 is IEEE bfloat16 stored as 16-bit words; arrays are row-major and
+ * dense unless a stride argument says otherwise.  Every pointer must be
+ * 16-byte aligned.  Calls are asynchronous on the given CUDA stream
+ * (a cudaStream_t passed as void*; NULL = the legacy default stream), never
+ * synchronise the host and never allocate.  Host-checkable argument errors
+ * return a negative code and launch nothing; errors only the device can see
+ * (a slot beyond the cache) set a sticky device flag read by
+ * mla_query_get_error.  No call ever traps the GPU.
+ */
+#ifndef MLA_QUERY_H
+#define MLA_QUERY_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MLA_API __attribute__((visibility("default")))
+#else
+#define MLA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define MLA_OK 0
+#define MLA_EINVAL (-1)       /* bad argument (null, size, alignment, layout) */
+#define MLA_ENOMEM (-2)       /* device allocation failed in create           */
+#define MLA_ECUDA (-3)        /* a CUDA runtime/driver call failed            */
+#define MLA_EUNSUPPORTED (-4) /* shape the library does not handle            */
+
+/* KV cache layouts (page "mla.query", methods insert and insert_ds). */
+#define MLA_KV_FP8_E4M3 0   /* 576-byte row: 512 E4M3 latent + 64 E4M3 k_pe,
+                               each value divided by k_scale                 */
+#define MLA_KV_FP8_DS_MLA 1 /* 656-byte row: 512 E4M3 latent scaled per 128
+                               columns by a power of two, 4 FP32 scales at
+                               byte 512, 64 raw BF16 k_pe at byte 528        */
+
+/* Bits of the device error flag (mla_query_get_error). */
+#define MLA_DEVERR_BAD_SLOT 1u /* a slot >= num_pages * page_size was skipped   */
+#define MLA_DEVERR_TIMEOUT 2u  /* an internal bounded wait gave up (results of
+                                  that call are not valid)                     */
+
+/* Compute paths (mla_query_set_path). */
+#define MLA_PATH_AUTO 0 /* pick by batch size                               */
+#define MLA_PATH_FMA 1  /* FP32 FMA dot products (batch <= 2)                */
+#define MLA_PATH_MMA 2  /* BF16 tensor-core tiles, FP32 accumulate           */
+
+#define MLA_MAX_BATCH 256 /* largest batch one decode call accepts           */
+#define MLA_MAX_HEADS 128 /* largest number of local heads                   */
+
+typedef struct mla_query* mla_query_t;
+
+/*
+ * mla_query_create - bind one layer's static weights (page "mla.query", class
+ * MlaQuery, constructor and the argument list of method kernel: w_qa (gamma_q),
+ * w_kva (gamma_kv), w_qb, w_uk, eps).
+ *
+ *   out       receives the handle (host pointer, must not be NULL).
+ *   num_heads local heads H, 1 <= H <= MLA_MAX_HEADS.
+ *   w_qb      device BF16 [H*192][1536], row h*192+p is Q_B row p of head h
+ *             (p < 128 nope, p >= 128 rope).
+ *   w_uk      device BF16 [H][128][512], element (h, p, c).
+ *   gamma_q   device BF16 [1536], gamma_kv device BF16 [512].
+ *   eps       RMSNorm epsilon used by both norms.
+ *
+ * The weights are borrowed, not copied: they must stay valid and unchanged
+ * until mla_query_destroy.  create allocates the handle's small device scratch
+ * (query hand-off buffer, counters, error flag) with cudaMalloc on the current
+ * device; the handle may only be used on that device.
+ * Returns MLA_OK, MLA_EINVAL, MLA_ENOMEM or MLA_ECUDA.
+ */
+MLA_API int mla_query_create(mla_query_t* out, int num_heads, const void* w_qb,
+                     const void* w_uk, const void* gamma_q,
+                     const void* gamma_kv, float eps);
+
+/*
+ * mla_query_decode - run one decode step (all five steps above) on `stream`.
+ *
+ *   batch         B tokens, 1 <= B <= MLA_MAX_BATCH.
+ *   q_a           device BF16 [B][q_a_stride] (first 1536 used);
+ *                 q_a_stride in elements, 0 means 1536; multiple of 8.
+ *   kv_c          device BF16 [B][kv_c_stride] (first 512), 0 means 512.
+ *   k_pe          device BF16 [B][k_pe_stride] (first 64), 0 means 64.
+ *                 (A fused [B][2112] q_a|kv_c|k_pe row is q_a = row,
+ *                 kv_c = row + 1536, k_pe = row + 2048, all strides 2112.)
+ *   slot_mapping  device int64 [B]; a slot < 0 skips the token's cache row
+ *                 (page "mla.query", method insert); a slot >= num_pages *
+ *                 page_size is skipped and sets MLA_DEVERR_BAD_SLOT.
+ *   kv_cache      device uint8 [num_pages][page_size][row], row = 576
+ *                 (MLA_KV_FP8_E4M3) or 656 (MLA_KV_FP8_DS_MLA) bytes; slot s
+ *                 lives at page s / page_size, offset s % page_size.
+ *   layout        MLA_KV_FP8_E4M3 or MLA_KV_FP8_DS_MLA.
+ *   k_scale       device FP32 [1]; the per-tensor layout divides by it
+ *                 (ignored by the ds layout, may then be NULL).
+ *   q_latent      device BF16 [B][H][512] output.
+ *   q_pe          device BF16 [B][H][64] output.
+ *   q_c           device BF16 [B][1536] output, or NULL to skip it.
+ *   stream        cudaStream_t as void*.
+ *
+ * Inputs are read, and outputs written, only after the previous kernel on
+ * the stream has completed (programmatic dependent launch: weights may be
+ * prefetched earlier).  Calls sharing one handle must be ordered on one
+ * stream: they share the handle's scratch.
+ * Returns MLA_OK, MLA_EINVAL, MLA_EUNSUPPORTED or MLA_ECUDA (launch error).
+ */
+MLA_API int mla_query_decode(mla_query_t h, int batch, const void* q_a,
+                     int64_t q_a_stride, const void* kv_c, int64_t kv_c_stride,
+                     const void* k_pe, int64_t k_pe_stride,
+                     const int64_t* slot_mapping, void* kv_cache,
+                     int64_t num_pages, int page_size, int layout,
+                     const float* k_scale, void* q_latent, void* q_pe,
+                     void* q_c, void* stream);
+
+/*
+ * mla_query_get_error - read and clear the handle's device error flag.
+ * Synchronises `stream` (host wait).  *device_flags receives the OR of the
+ * MLA_DEVERR_* bits raised since the last call (0 if none).
+ */
+MLA_API int mla_query_get_error(mla_query_t h, unsigned* device_flags, void* stream);
+
+/*
+ * mla_query_set_path - force a compute path (MLA_PATH_*) for later decode
+ * calls on this handle; MLA_PATH_AUTO restores the batch-size dispatch.
+ * A forced path that cannot serve a batch makes decode return
+ * MLA_EUNSUPPORTED.  For tests and tuning; results of every path agree within
+ * the library's stated tolerance.
+ */
+MLA_API int mla_query_set_path(mla_query_t h, int path);
+
+/*
+ * mla_query_path_for - the path (MLA_PATH_FMA / MLA_PATH_MMA) a decode call
+ * with `batch` tokens takes on this handle; negative on error.
+ */
+MLA_API int mla_query_path_for(mla_query_t h, int batch);
+
+/* mla_query_destroy - free the handle and its scratch (NULL is a no-op).
+ * The caller must ensure no decode on the handle is still in flight. */
+MLA_API void mla_query_destroy(mla_query_t h);
+
+/* mla_query_strerror - static text for a return code. */
+MLA_API const char* mla_query_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_QUERY_H */

@@ -1,1 +1,25 @@
-"""GB300-native decode-step MLA query path (placeholder; binding added with the library)."""
+"""GB300-native decode-step MLA query path.
+
+``binding`` holds the ctypes binding of ``libmla_query.so`` (the C ABI in
+``include/mla_query.h``); ``runner`` wraps it for torch tensors;
+``synthetic`` draws the seeded workloads.  Importing the package does not load
+the library; the first binding call does, and fails loudly if it is missing.
+"""
+
+from .binding import (  # noqa: F401
+    MLA_DEVERR_BAD_SLOT,
+    MLA_DEVERR_TIMEOUT,
+    MLA_KV_FP8_DS_MLA,
+    MLA_KV_FP8_E4M3,
+    MLA_OK,
+    MLA_PATH_AUTO,
+    MLA_PATH_FMA,
+    MLA_PATH_MMA,
+    MlaError,
+    mla_query_create,
+    mla_query_decode,
+    mla_query_destroy,
+    mla_query_get_error,
+    mla_query_path_for,
+    mla_query_set_path,
+)

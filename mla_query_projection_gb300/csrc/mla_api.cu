@@ -1,0 +1,246 @@
+// mla_api.cu - the C ABI (include/mla_query.h): argument checks, the handle
+// with its device scratch, the W_UK tensor map, and path dispatch.
+#include <cudaTypedefs.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "../../include/mla_query.h"
+#include "mla_internal.h"
+
+struct mla_query {
+  int device;
+  int heads;
+  int num_sms;
+  int path;  // MLA_PATH_*
+  const uint16_t* w_qb;
+  const uint16_t* w_uk;
+  const uint16_t* gamma_q;
+  const uint16_t* gamma_kv;
+  float eps;
+  CUtensorMap uk_map;
+  void* scratch;  // one cudaMalloc: err | finished | ready[] | qn[]
+  uint32_t* err;
+  uint32_t* finished;
+  uint32_t* ready;
+  uint16_t* qn;
+};
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// W_UK [H*128 rows][512 columns] BF16, boxes of 128 rows x 64 columns (128 B
+// rows, 128 B swizzle).
+int encode_uk_map(CUtensorMap* map, const void* w_uk, int heads) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return MLA_ECUDA;
+  cuuint64_t dims[2] = {(cuuint64_t)mla::kKvLora, (cuuint64_t)heads * mla::kNope};
+  cuuint64_t strides[1] = {(cuuint64_t)mla::kKvLora * 2};
+  cuuint32_t box[2] = {(cuuint32_t)mla::kUkCols, (cuuint32_t)mla::kNope};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w_uk), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MLA_OK : MLA_ECUDA;
+}
+
+int pick_path(const mla_query* h, int batch, bool* mma, int* nt) {
+  int path = h->path;
+  if (path == MLA_PATH_AUTO) path = batch <= 2 ? MLA_PATH_FMA : MLA_PATH_MMA;
+  if (path == MLA_PATH_FMA) {
+    if (batch > 2) return MLA_EUNSUPPORTED;
+    *mma = false;
+  } else if (path == MLA_PATH_MMA) {
+    *mma = true;
+  } else {
+    return MLA_EINVAL;
+  }
+  *nt = mla::tokens_per_cta(batch, *mma);
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_query_strerror(int code) {
+  switch (code) {
+    case MLA_OK: return "ok";
+    case MLA_EINVAL: return "invalid argument";
+    case MLA_ENOMEM: return "device allocation failed";
+    case MLA_ECUDA: return "CUDA call failed";
+    case MLA_EUNSUPPORTED: return "unsupported shape or path";
+    default: return "unknown error";
+  }
+}
+
+int mla_query_create(mla_query_t* out, int num_heads, const void* w_qb, const void* w_uk,
+                     const void* gamma_q, const void* gamma_kv, float eps) {
+  if (out == nullptr) return MLA_EINVAL;
+  *out = nullptr;
+  if (num_heads < 1 || num_heads > MLA_MAX_HEADS) return MLA_EINVAL;
+  if (w_qb == nullptr || w_uk == nullptr || gamma_q == nullptr || gamma_kv == nullptr)
+    return MLA_EINVAL;
+  if (!aligned16(w_qb) || !aligned16(w_uk) || !aligned16(gamma_q) || !aligned16(gamma_kv))
+    return MLA_EINVAL;
+  if (!(eps >= 0.0f)) return MLA_EINVAL;
+
+  mla_query* h = static_cast<mla_query*>(calloc(1, sizeof(mla_query)));
+  if (h == nullptr) return MLA_ENOMEM;
+  h->heads = num_heads;
+  h->w_qb = static_cast<const uint16_t*>(w_qb);
+  h->w_uk = static_cast<const uint16_t*>(w_uk);
+  h->gamma_q = static_cast<const uint16_t*>(gamma_q);
+  h->gamma_kv = static_cast<const uint16_t*>(gamma_kv);
+  h->eps = eps;
+  h->path = MLA_PATH_AUTO;
+  int rc = MLA_ECUDA;
+  if (cudaGetDevice(&h->device) != cudaSuccess) goto fail;
+  if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) !=
+      cudaSuccess)
+    goto fail;
+  if (mla::prepare_fused_kernels() != cudaSuccess) goto fail;
+  if ((rc = encode_uk_map(&h->uk_map, w_uk, num_heads)) != MLA_OK) goto fail;
+  {
+    const size_t head = 256;  // err, finished
+    const size_t ready_bytes = mla::scratch_ready_elems(num_heads) * sizeof(uint32_t);
+    const size_t qn_off = head + ((ready_bytes + 255) / 256) * 256;
+    const size_t bytes = qn_off + mla::scratch_qn_elems(num_heads) * sizeof(uint16_t);
+    if (cudaMalloc(&h->scratch, bytes) != cudaSuccess) {
+      rc = MLA_ENOMEM;
+      goto fail;
+    }
+    if (cudaMemset(h->scratch, 0, bytes) != cudaSuccess) goto fail;
+    uint8_t* base = static_cast<uint8_t*>(h->scratch);
+    h->err = reinterpret_cast<uint32_t*>(base);
+    h->finished = reinterpret_cast<uint32_t*>(base + 4);
+    h->ready = reinterpret_cast<uint32_t*>(base + head);
+    h->qn = reinterpret_cast<uint16_t*>(base + qn_off);
+  }
+  *out = h;
+  return MLA_OK;
+fail:
+  if (h->scratch) cudaFree(h->scratch);
+  free(h);
+  cudaGetLastError();
+  return rc;
+}
+
+int mla_query_decode(mla_query_t h, int batch, const void* q_a, int64_t q_a_stride,
+                     const void* kv_c, int64_t kv_c_stride, const void* k_pe,
+                     int64_t k_pe_stride, const int64_t* slot_mapping, void* kv_cache,
+                     int64_t num_pages, int page_size, int layout, const float* k_scale,
+                     void* q_latent, void* q_pe, void* q_c, void* stream) {
+  if (h == nullptr) return MLA_EINVAL;
+  if (batch < 1 || batch > MLA_MAX_BATCH) return MLA_EINVAL;
+  if (q_a == nullptr || kv_c == nullptr || k_pe == nullptr || slot_mapping == nullptr ||
+      kv_cache == nullptr || q_latent == nullptr || q_pe == nullptr)
+    return MLA_EINVAL;
+  if (layout != MLA_KV_FP8_E4M3 && layout != MLA_KV_FP8_DS_MLA) return MLA_EINVAL;
+  if (layout == MLA_KV_FP8_E4M3 && k_scale == nullptr) return MLA_EINVAL;
+  if (num_pages < 1 || page_size < 1) return MLA_EINVAL;
+  if (q_a_stride == 0) q_a_stride = mla::kQLora;
+  if (kv_c_stride == 0) kv_c_stride = mla::kKvLora;
+  if (k_pe_stride == 0) k_pe_stride = mla::kRope;
+  if (q_a_stride < mla::kQLora || kv_c_stride < mla::kKvLora || k_pe_stride < mla::kRope)
+    return MLA_EINVAL;
+  if ((q_a_stride | kv_c_stride | k_pe_stride) & 7) return MLA_EINVAL;
+  if (!aligned16(q_a) || !aligned16(kv_c) || !aligned16(k_pe) || !aligned16(kv_cache) ||
+      !aligned16(q_latent) || !aligned16(q_pe) || !aligned16(q_c) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) ||
+      (reinterpret_cast<uintptr_t>(k_scale) & 3u))
+    return MLA_EINVAL;
+
+  bool mma = false;
+  int nt = 1;
+  int rc = pick_path(h, batch, &mma, &nt);
+  if (rc != MLA_OK) return rc;
+
+  mla::DecodeArgs a;
+  a.w_qb = h->w_qb;
+  a.gamma_q = h->gamma_q;
+  a.gamma_kv = h->gamma_kv;
+  a.q_a = static_cast<const uint16_t*>(q_a);
+  a.kv_c = static_cast<const uint16_t*>(kv_c);
+  a.k_pe = static_cast<const uint16_t*>(k_pe);
+  a.q_a_stride = q_a_stride;
+  a.kv_c_stride = kv_c_stride;
+  a.k_pe_stride = k_pe_stride;
+  a.slots = slot_mapping;
+  a.cache = static_cast<uint8_t*>(kv_cache);
+  a.num_pages = num_pages;
+  a.page_size = page_size;
+  a.layout = layout;
+  a.k_scale = k_scale;
+  a.q_latent = static_cast<uint16_t*>(q_latent);
+  a.q_pe = static_cast<uint16_t*>(q_pe);
+  a.q_c = static_cast<uint16_t*>(q_c);
+  a.qn = h->qn;
+  a.ready = h->ready;
+  a.finished = h->finished;
+  a.err = h->err;
+  a.heads = h->heads;
+  a.batch = batch;
+  a.groups = (batch + nt - 1) / nt;
+  a.eps = h->eps;
+  if (a.groups > h->num_sms) return MLA_EUNSUPPORTED;
+
+  cudaError_t e =
+      mla::launch_fused(a, &h->uk_map, nt, mma, h->num_sms, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ECUDA;
+  }
+  return MLA_OK;
+}
+
+int mla_query_get_error(mla_query_t h, unsigned* device_flags, void* stream) {
+  if (h == nullptr || device_flags == nullptr) return MLA_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, h->err, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess ||
+      cudaMemsetAsync(h->err, 0, sizeof(uint32_t), s) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ECUDA;
+  }
+  *device_flags = v;
+  return MLA_OK;
+}
+
+int mla_query_set_path(mla_query_t h, int path) {
+  if (h == nullptr) return MLA_EINVAL;
+  if (path != MLA_PATH_AUTO && path != MLA_PATH_FMA && path != MLA_PATH_MMA) return MLA_EINVAL;
+  h->path = path;
+  return MLA_OK;
+}
+
+int mla_query_path_for(mla_query_t h, int batch) {
+  if (h == nullptr || batch < 1 || batch > MLA_MAX_BATCH) return MLA_EINVAL;
+  bool mma = false;
+  int nt = 1;
+  int rc = pick_path(h, batch, &mma, &nt);
+  if (rc != MLA_OK) return rc;
+  return mma ? MLA_PATH_MMA : MLA_PATH_FMA;
+}
+
+void mla_query_destroy(mla_query_t h) {
+  if (h == nullptr) return;
+  if (h->scratch) cudaFree(h->scratch);
+  free(h);
+}
+
+}  // extern "C"

@@ -1,0 +1,679 @@
+// mla_fused.cu - the fused decode-step kernel of the MLA query path.
+//
+// One persistent launch (one CTA per SM, `groups` token groups along grid.y)
+// computes, for the tokens of its group (page "mla.query", class MlaQuery,
+// methods kernel / tiled / insert / insert_ds / store_qc):
+//   q_a RMSNorm -> xq (q_c), Q_B rows -> q (BF16), rope rows -> q_pe,
+//   nope rows through W_UK -> q_latent, and the paged FP8 KV insert.
+//
+// GB300 design (not the page's cluster design):
+//  * Weight streaming.  Each CTA owns a byte-balanced share of three lists:
+//    the H*128 nope rows of W_QB, then a combined list per head of the eight
+//    64-column W_UK tiles and the 64 rope rows.  Rows arrive by 1-D bulk TMA
+//    (3 KiB each, padded smem pitch), W_UK tiles by 2-D tensor TMA with 128 B
+//    swizzle, into a ring of 16-row stages tracked by mbarriers.  The first
+//    stages are issued before the programmatic-dependent-launch wait, since
+//    weights do not depend on the previous kernel.
+//  * Nope hand-off.  All CTAs stream their nope rows first and publish the
+//    BF16 q values to a small global scratch; a per-(group, head) counter
+//    reaches 128 when a head is complete.  The W_UK tiles of a head come
+//    later in every CTA's order, so by then the counters are normally full;
+//    the wait is bounded and raises MLA_DEVERR_TIMEOUT instead of hanging.
+//    The last CTA to finish re-arms the counters for the next call.
+//  * Arithmetic.  FMA flavour (1-2 tokens): FP32 FMAs, one warp per row,
+//    x held in registers.  MMA flavour (8 or 16 tokens per CTA): BF16
+//    mma.sync m16n8k16 with the weight rows as the M side (tokens are N),
+//    K split over the 8 warps and reduced in a fixed order through smem; the
+//    absorption uses ldmatrix.trans on the swizzled W_UK tile as the M side.
+#include <cuda_bf16.h>
+
+#include "mla_device.cuh"
+#include "mla_internal.h"
+#include "../../include/mla_query.h"
+
+namespace mla {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kStageRows = 16;
+constexpr int kPitch = kRowBytes + 64;            // 3136 B: conflict-free MMA loads
+constexpr int kStageBytes = kStageRows * kPitch;  // 50176 = 49 KiB (1 KiB aligned)
+constexpr int kUkPerStage = 3;                    // 3 x 16 KiB W_UK tiles per stage
+constexpr int kQsPitch = kNope + 8;               // BF16 elements per staged q row (MMA)
+constexpr long long kWaitLimit = 2000000000LL;    // ~1 s of SM clock
+
+enum StageKind { kNopeRows = 0, kRopeRows = 1, kUkTiles = 2 };
+
+struct Stage {
+  int kind;
+  int first;  // nope index n (h*128+p), rope index r (h*64+p-128) or unit u (h*8+cb)
+  int count;
+};
+
+struct Work {
+  int n0, n1;  // nope indices
+  int c0, c1;  // combined items (per head: 8 W_UK units, then 64 rope rows)
+};
+
+__device__ __forceinline__ int first_item(int64_t x) {
+  const int64_t h = x / kItemBytesPerHead;
+  const int64_t local = x % kItemBytesPerHead;
+  const int64_t uk_bytes = (int64_t)kUkUnitsPerHead * kUkUnitBytes;
+  int64_t l;
+  if (local == 0) {
+    l = 0;
+  } else if (local <= uk_bytes) {
+    l = (local + kUkUnitBytes - 1) / kUkUnitBytes;
+  } else {
+    l = kUkUnitsPerHead + (local - uk_bytes + kRowBytes - 1) / kRowBytes;
+  }
+  return (int)(h * kItemsPerHead + l);
+}
+
+__device__ __forceinline__ Work cta_work(int i, int P, int H) {
+  Work w;
+  const int64_t N = (int64_t)H * kNope;
+  w.n0 = (int)(N * i / P);
+  w.n1 = (int)(N * (i + 1) / P);
+  const int64_t T = (int64_t)H * kItemBytesPerHead;
+  w.c0 = first_item(T * i / P);
+  w.c1 = first_item(T * (i + 1) / P);
+  return w;
+}
+
+__device__ __forceinline__ bool next_stage(int& pn, int& pc, const Work& w, Stage& s) {
+  if (pn < w.n1) {
+    s.kind = kNopeRows;
+    s.first = pn;
+    s.count = min(kStageRows, w.n1 - pn);
+    pn += s.count;
+    return true;
+  }
+  if (pc < w.c1) {
+    const int h = pc / kItemsPerHead, l = pc % kItemsPerHead;
+    if (l < kUkUnitsPerHead) {
+      s.kind = kUkTiles;
+      s.first = h * kUkUnitsPerHead + l;
+      s.count = min(min(kUkPerStage, kUkUnitsPerHead - l), w.c1 - pc);
+    } else {
+      s.kind = kRopeRows;
+      s.first = h * kRope + (l - kUkUnitsPerHead);
+      s.count = min(min(kStageRows, kItemsPerHead - l), w.c1 - pc);
+    }
+    pc += s.count;
+    return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ int stage_row(const Stage& s, int j) {
+  if (s.kind == kNopeRows) {
+    const int n = s.first + j;
+    return (n / kNope) * kHeadRows + (n % kNope);
+  }
+  const int r = s.first + j;
+  return (r / kRope) * kHeadRows + kNope + (r % kRope);
+}
+
+// Issue the copies of stage `s` into `buf` (called by all 32 lanes of warp 0).
+__device__ __forceinline__ void issue_stage(const Stage& s, uint8_t* buf, uint64_t* bar,
+                                            const DecodeArgs& a, const CUtensorMap* uk_map,
+                                            int lane) {
+  if (s.kind == kUkTiles) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar, (uint32_t)(s.count * kUkUnitBytes));
+      for (int j = 0; j < s.count; ++j) {
+        const int u = s.first + j;
+        tma_g2s_2d(buf + j * kUkUnitBytes, uk_map, (u % kUkUnitsPerHead) * kUkCols,
+                   (u / kUkUnitsPerHead) * kNope, bar);
+      }
+    }
+  } else {
+    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(s.count * kRowBytes));
+    __syncwarp();
+    if (lane < s.count) {
+      const int row = stage_row(s, lane);
+      bulk_g2s(buf + lane * kPitch, a.w_qb + (int64_t)row * kQLora, kRowBytes, bar);
+    }
+  }
+}
+
+// Paged FP8 KV insert of token b (page "mla.query", methods insert, kv_fp8,
+// insert_ds).  Called by the whole CTA; threads 0..71 work.
+__device__ void kv_insert(const DecodeArgs& a, int b, float* red2) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t slot = a.slots[b];
+  if (slot < 0) return;
+  const int64_t page = slot / a.page_size, off = slot % a.page_size;
+  if (page >= a.num_pages) {
+    if (tid == 0) atomicOr(a.err, MLA_DEVERR_BAD_SLOT);
+    return;
+  }
+  const bool ds = a.layout == MLA_KV_FP8_DS_MLA;
+  uint8_t* row = a.cache + (page * a.page_size + off) * (ds ? kRowDs : kRowE4m3);
+  float x[8];
+  if (tid < 64) {
+    const uint4 v = *reinterpret_cast<const uint4*>(a.kv_c + (int64_t)b * a.kv_c_stride + 8 * tid);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = bf16lo(w[i]);
+      x[2 * i + 1] = bf16hi(w[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss = fmaf(x[i], x[i], ss);
+    ss = warp_sum(ss);
+    if (lane == 0) red2[warp] = ss;
+  }
+  __syncthreads();
+  if (tid < 64) {
+    const float total = red2[0] + red2[1];
+    const float rr = __frsqrt_rn(__fadd_rn(__fmul_rn(total, 1.0f / 512.0f), a.eps));
+    const uint4 gv = *reinterpret_cast<const uint4*>(a.gamma_kv + 8 * tid);
+    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    float n[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      n[2 * i] = bf_round(__fmul_rn(__fmul_rn(x[2 * i], rr), bf16lo(gw[i])));
+      n[2 * i + 1] = bf_round(__fmul_rn(__fmul_rn(x[2 * i + 1], rr), bf16hi(gw[i])));
+    }
+    uint2 out;
+    if (!ds) {
+      const float ks = *a.k_scale;
+      out.x = (uint32_t)e4m3x2(__fdiv_rn(n[0], ks), __fdiv_rn(n[1], ks)) |
+              ((uint32_t)e4m3x2(__fdiv_rn(n[2], ks), __fdiv_rn(n[3], ks)) << 16);
+      out.y = (uint32_t)e4m3x2(__fdiv_rn(n[4], ks), __fdiv_rn(n[5], ks)) |
+              ((uint32_t)e4m3x2(__fdiv_rn(n[6], ks), __fdiv_rn(n[7], ks)) << 16);
+    } else {
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(n[i]));
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+      const float scale = pow2_ceil_f32(fmaxf(__fdiv_rn(amax, 448.0f), 1e-4f));
+      const float inv = __fdiv_rn(1.0f, scale);  // exact: a power of two
+      out.x = (uint32_t)e4m3x2(n[0] * inv, n[1] * inv) |
+              ((uint32_t)e4m3x2(n[2] * inv, n[3] * inv) << 16);
+      out.y = (uint32_t)e4m3x2(n[4] * inv, n[5] * inv) |
+              ((uint32_t)e4m3x2(n[6] * inv, n[7] * inv) << 16);
+      if ((lane & 15) == 0) *reinterpret_cast<float*>(row + kDsScales + 4 * (tid >> 4)) = scale;
+    }
+    *reinterpret_cast<uint2*>(row + 8 * tid) = out;
+  } else if (tid < 72) {
+    const int c = tid - 64;
+    const uint4 v = *reinterpret_cast<const uint4*>(a.k_pe + (int64_t)b * a.k_pe_stride + 8 * c);
+    if (ds) {
+      *reinterpret_cast<uint4*>(row + kDsRope + 16 * c) = v;
+    } else {
+      const float ks = *a.k_scale;
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint2 out;
+      out.x = (uint32_t)e4m3x2(__fdiv_rn(bf16lo(w[0]), ks), __fdiv_rn(bf16hi(w[0]), ks)) |
+              ((uint32_t)e4m3x2(__fdiv_rn(bf16lo(w[1]), ks), __fdiv_rn(bf16hi(w[1]), ks)) << 16);
+      out.y = (uint32_t)e4m3x2(__fdiv_rn(bf16lo(w[2]), ks), __fdiv_rn(bf16hi(w[2]), ks)) |
+              ((uint32_t)e4m3x2(__fdiv_rn(bf16lo(w[3]), ks), __fdiv_rn(bf16hi(w[3]), ks)) << 16);
+      *reinterpret_cast<uint2*>(row + kKvLora + 8 * c) = out;
+    }
+  }
+  __syncthreads();
+}
+
+template <int NT, bool MMA>
+struct Smem {
+  static constexpr int kStages = MMA ? 3 : 4;
+  static constexpr int kRing = kStages * kStageBytes;
+  static constexpr int kXq = NT * kPitch;
+  static constexpr int kQs = MMA ? NT * kQsPitch * 2 : NT * kNope * 4;
+  static constexpr int kRed = MMA ? kWarps * kStageRows * NT * 4 : kUkPerStage * 32 * NT * 2 * 4;
+  static constexpr int oXq = kRing;
+  static constexpr int oQs = oXq + kXq;
+  static constexpr int oRed = oQs + kQs;
+  static constexpr int oSs = oRed + kRed;                      // [NT][8] floats + [2]
+  static constexpr int oBar = oSs + (NT * 8 + 8) * 4;
+  static constexpr int oFlag = oBar + kStages * 8;
+  static constexpr int kBytes = oFlag + 16;
+  static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1 KiB
+};
+
+template <int NT, bool MMA>
+__global__ void __launch_bounds__(kThreads, 1)
+    mla_fused_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap uk_map) {
+  using S = Smem<NT, MMA>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* ring = smem;
+  uint8_t* xq = smem + S::oXq;
+  float* red = reinterpret_cast<float*>(smem + S::oRed);
+  float* ss_part = reinterpret_cast<float*>(smem + S::oSs);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::oBar);
+  int* flag = reinterpret_cast<int*>(smem + S::oFlag);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int P = gridDim.x, i = blockIdx.x, grp = blockIdx.y;
+  const int H = a.heads;
+  const Work w = cta_work(i, P, H);
+
+  if (tid == 0) {
+    for (int s = 0; s < S::kStages; ++s) mbar_init(&bars[s], 1);
+    mbar_fence_init();
+    prefetch_tensormap(&uk_map);
+  }
+  __syncthreads();
+
+  // Weights do not depend on the previous kernel: start streaming them now.
+  int prod_n = w.n0, prod_c = w.c0, issued = 0;
+  if (warp == 0) {
+    Stage st;
+    for (int s = 0; s < S::kStages && next_stage(prod_n, prod_c, w, st); ++s) {
+      issue_stage(st, ring + s * kStageBytes, &bars[s], a, &uk_map, lane);
+      ++issued;
+    }
+  }
+
+  pdl_wait();
+  pdl_launch_dependents();
+
+  // ---- q_a RMSNorm of this group's tokens -> xq (BF16, smem) ------------
+  const int tok0 = grp * NT;
+  {
+    uint4 xv[NT];
+    if (tid < 192) {
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        if (tok0 + t < a.batch)
+          xv[t] = *reinterpret_cast<const uint4*>(a.q_a + (int64_t)(tok0 + t) * a.q_a_stride +
+                                                  8 * tid);
+        else
+          xv[t] = make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const uint32_t ww[4] = {xv[t].x, xv[t].y, xv[t].z, xv[t].w};
+        float ss = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          ss = fmaf(bf16lo(ww[k]), bf16lo(ww[k]), ss);
+          ss = fmaf(bf16hi(ww[k]), bf16hi(ww[k]), ss);
+        }
+        ss = warp_sum(ss);
+        if (lane == 0) ss_part[t * 8 + warp] = ss;
+      }
+    }
+    __syncthreads();
+    if (tid < 192) {
+      const uint4 gv = *reinterpret_cast<const uint4*>(a.gamma_q + 8 * tid);
+      const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const float* sp = ss_part + t * 8;
+        const float total = ((((sp[0] + sp[1]) + sp[2]) + sp[3]) + sp[4]) + sp[5];
+        const float rr = __frsqrt_rn(__fadd_rn(__fdiv_rn(total, 1536.0f), a.eps));
+        const uint32_t ww[4] = {xv[t].x, xv[t].y, xv[t].z, xv[t].w};
+        uint4 o;
+        uint32_t* op = &o.x;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float lo = __fmul_rn(__fmul_rn(bf16lo(ww[k]), rr), bf16lo(gw[k]));
+          const float hi = __fmul_rn(__fmul_rn(bf16hi(ww[k]), rr), bf16hi(gw[k]));
+          op[k] = pack_bf16x2(lo, hi);
+        }
+        if (tok0 + t >= a.batch) o = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(xq + t * kPitch + 16 * tid) = o;
+      }
+    }
+    __syncthreads();
+  }
+
+  // q_c rows (page "mla.query", method store_qc): CTA 0 of the group.
+  if (i == 0 && a.q_c != nullptr && tid < 192) {
+    for (int t = 0; t < NT && tok0 + t < a.batch; ++t)
+      *reinterpret_cast<uint4*>(a.q_c + (int64_t)(tok0 + t) * kQLora + 8 * tid) =
+          *reinterpret_cast<const uint4*>(xq + t * kPitch + 16 * tid);
+  }
+
+  // KV insert: token t of the group goes to CTA t % P.
+  for (int t = i; t < NT; t += P)
+    if (tok0 + t < a.batch) kv_insert(a, tok0 + t, ss_part + NT * 8);
+
+  // FMA flavour: this lane's x values in registers (k = 256 c + 8 lane + e).
+  float xr[MMA ? 1 : NT][MMA ? 1 : 48];
+  if constexpr (!MMA) {
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int c = 0; c < 6; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(xq + t * kPitch + 2 * (256 * c + 8 * lane));
+        const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          xr[t][8 * c + 2 * k] = bf16lo(ww[k]);
+          xr[t][8 * c + 2 * k + 1] = bf16hi(ww[k]);
+        }
+      }
+  }
+
+  uint16_t* qn_g = a.qn + (int64_t)grp * NT * H * kNope;
+  uint32_t* ready_g = a.ready + grp * H;
+  bool timed_out = false;
+
+  int cons_n = w.n0, cons_c = w.c0, stuck = -1;
+  Stage st;
+  for (int s = 0; next_stage(cons_n, cons_c, w, st); ++s) {
+    const int slot = s % S::kStages;
+    uint8_t* buf = ring + slot * kStageBytes;
+    const bool got = mbar_wait_bounded(&bars[slot], (uint32_t)((s / S::kStages) & 1), kWaitLimit);
+    if (__syncthreads_or(got ? 0 : 1)) {
+      // a copy never landed: stop consuming, drain what is in flight below
+      timed_out = true;
+      stuck = s;
+      break;
+    }
+
+    if (st.kind == kUkTiles) {
+      // ---- absorption of one head's nope q through 1-3 W_UK tiles -------
+      const int h = st.first / kUkUnitsPerHead;
+      const int cb0 = st.first % kUkUnitsPerHead;
+      if (tid == 0) {
+        const long long t0 = clock64();
+        while (ld_acquire_gpu(ready_g + h) < (uint32_t)kNope) {
+          if (clock64() - t0 > kWaitLimit) {
+            timed_out = true;
+            break;
+          }
+          __nanosleep(64);
+        }
+      }
+      __syncthreads();
+      const uint16_t* src = qn_g + (int64_t)h * kNope;  // + t*H*128
+      if constexpr (MMA) {
+        uint16_t* qs = reinterpret_cast<uint16_t*>(smem + S::oQs);
+        for (int e = tid; e < NT * (kNope / 2); e += kThreads) {
+          const int t = e / (kNope / 2), c2 = e % (kNope / 2);
+          const uint32_t v = __ldcg(reinterpret_cast<const unsigned int*>(
+              src + (int64_t)t * H * kNope + 2 * c2));
+          *reinterpret_cast<uint32_t*>(qs + t * kQsPitch + 2 * c2) = v;
+        }
+      } else {
+        float* qs = reinterpret_cast<float*>(smem + S::oQs);
+        for (int e = tid; e < NT * (kNope / 2); e += kThreads) {
+          const int t = e / (kNope / 2), c2 = e % (kNope / 2);
+          const uint32_t v = __ldcg(reinterpret_cast<const unsigned int*>(
+              src + (int64_t)t * H * kNope + 2 * c2));
+          qs[t * kNope + 2 * c2] = bf16lo(v);
+          qs[t * kNope + 2 * c2 + 1] = bf16hi(v);
+        }
+      }
+      __syncthreads();
+
+      if constexpr (MMA) {
+        const uint16_t* qs = reinterpret_cast<const uint16_t*>(smem + S::oQs);
+        const int g = lane >> 2, q = lane & 3;
+        for (int pair = warp; pair < 4 * st.count; pair += kWarps) {
+          const int u = pair >> 2, mt = pair & 3;
+          const uint32_t tile = smem_u32(buf + u * kUkUnitBytes);
+          float acc[NT / 8][4];
+#pragma unroll
+          for (int nt = 0; nt < NT / 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+          for (int ks = 0; ks < kNope / 16; ++ks) {
+            const int m = lane >> 3;
+            const int p = 16 * ks + (lane & 7) + 8 * (m >> 1);
+            const int chunk = 2 * mt + (m & 1);
+            uint32_t af[4];
+            ldmatrix_x4_trans(af, tile + p * 128 + ((chunk ^ (p & 7)) << 4));
+#pragma unroll
+            for (int nt = 0; nt < NT / 8; ++nt) {
+              const uint16_t* qr = qs + (8 * nt + g) * kQsPitch + 16 * ks + 2 * q;
+              const uint32_t b0 = *reinterpret_cast<const uint32_t*>(qr);
+              const uint32_t b1 = *reinterpret_cast<const uint32_t*>(qr + 8);
+              mma_bf16_16816(acc[nt], af[0], af[1], af[2], af[3], b0, b1);
+            }
+          }
+          const int cbase = (cb0 + u) * kUkCols + 16 * mt + g;
+#pragma unroll
+          for (int nt = 0; nt < NT / 8; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int t = 8 * nt + 2 * q + (e & 1);
+              const int c = cbase + 8 * (e >> 1);
+              if (tok0 + t < a.batch)
+                a.q_latent[((int64_t)(tok0 + t) * H + h) * kKvLora + c] = f2bf_bits(acc[nt][e]);
+            }
+          }
+        }
+      } else {
+        const float* qs = reinterpret_cast<const float*>(smem + S::oQs);
+        const int u = tid >> 6, cp = tid & 31, ph = (tid >> 5) & 1;
+        float acc[NT][2];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = 0.f;
+        const bool active = u < st.count;
+        if (active) {
+          const uint8_t* tile = buf + u * kUkUnitBytes;
+#pragma unroll 8
+          for (int pp = 0; pp < 64; ++pp) {
+            const int p = 64 * ph + pp;
+            const uint32_t wv = *reinterpret_cast<const uint32_t*>(
+                tile + p * 128 + ((((cp >> 2) ^ (p & 7))) << 4) + (cp & 3) * 4);
+            const float w0 = bf16lo(wv), w1 = bf16hi(wv);
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+              acc[t][0] = fmaf(qs[t * kNope + p], w0, acc[t][0]);
+              acc[t][1] = fmaf(qs[t * kNope + p], w1, acc[t][1]);
+            }
+          }
+          if (ph == 1) {
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+              red[((u * 32 + cp) * NT + t) * 2] = acc[t][0];
+              red[((u * 32 + cp) * NT + t) * 2 + 1] = acc[t][1];
+            }
+          }
+        }
+        __syncthreads();
+        if (active && ph == 0) {
+          const int c = (cb0 + u) * kUkCols + 2 * cp;
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            if (tok0 + t < a.batch) {
+              const float v0 = acc[t][0] + red[((u * 32 + cp) * NT + t) * 2];
+              const float v1 = acc[t][1] + red[((u * 32 + cp) * NT + t) * 2 + 1];
+              *reinterpret_cast<uint32_t*>(a.q_latent + ((int64_t)(tok0 + t) * H + h) * kKvLora +
+                                           c) = pack_bf16x2(v0, v1);
+            }
+          }
+        }
+      }
+    } else {
+      // ---- Q_B rows (nope or rope) -------------------------------------
+      if constexpr (MMA) {
+        const int g = lane >> 2, q = lane & 3;
+        float acc[NT / 8][4];
+#pragma unroll
+        for (int nt = 0; nt < NT / 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 6; ++c) {
+          const int kb = 2 * (192 * warp + 32 * c + 8 * q);
+          const uint4 alo = *reinterpret_cast<const uint4*>(buf + g * kPitch + kb);
+          const uint4 ahi = *reinterpret_cast<const uint4*>(buf + (g + 8) * kPitch + kb);
+#pragma unroll
+          for (int nt = 0; nt < NT / 8; ++nt) {
+            const uint4 bx = *reinterpret_cast<const uint4*>(xq + (8 * nt + g) * kPitch + kb);
+            mma_bf16_16816(acc[nt], alo.x, ahi.x, alo.y, ahi.y, bx.x, bx.y);
+            mma_bf16_16816(acc[nt], alo.z, ahi.z, alo.w, ahi.w, bx.z, bx.w);
+          }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT / 8; ++nt) {
+          float* rw = red + warp * kStageRows * NT;
+          rw[g * NT + 8 * nt + 2 * q] = acc[nt][0];
+          rw[g * NT + 8 * nt + 2 * q + 1] = acc[nt][1];
+          rw[(g + 8) * NT + 8 * nt + 2 * q] = acc[nt][2];
+          rw[(g + 8) * NT + 8 * nt + 2 * q + 1] = acc[nt][3];
+        }
+        __syncthreads();
+        for (int e = tid; e < kStageRows * NT; e += kThreads) {
+          const int j = e / NT, t = e % NT;
+          if (j >= st.count) continue;
+          float v = 0.f;
+#pragma unroll
+          for (int ww = 0; ww < kWarps; ++ww) v += red[ww * kStageRows * NT + e];
+          const uint16_t bits = f2bf_bits(v);
+          if (st.kind == kNopeRows) {
+            const int n = st.first + j;
+            qn_g[((int64_t)t * H + n / kNope) * kNope + n % kNope] = bits;
+            __threadfence();
+          } else if (tok0 + t < a.batch) {
+            const int r = st.first + j;
+            a.q_pe[((int64_t)(tok0 + t) * H + r / kRope) * kRope + r % kRope] = bits;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+          const int j = warp + kWarps * rr;
+          if (j >= st.count) break;
+          const uint8_t* rowp = buf + j * kPitch;
+          float acc[NT][2];
+#pragma unroll
+          for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = 0.f;
+#pragma unroll
+          for (int c = 0; c < 6; ++c) {
+            const uint4 v = *reinterpret_cast<const uint4*>(rowp + 2 * (256 * c + 8 * lane));
+            const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float w0 = bf16lo(ww[k]), w1 = bf16hi(ww[k]);
+#pragma unroll
+              for (int t = 0; t < NT; ++t) {
+                acc[t][0] = fmaf(w0, xr[t][8 * c + 2 * k], acc[t][0]);
+                acc[t][1] = fmaf(w1, xr[t][8 * c + 2 * k + 1], acc[t][1]);
+              }
+            }
+          }
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            const float v = warp_sum(acc[t][0] + acc[t][1]);
+            if (lane == 0) {
+              const uint16_t bits = f2bf_bits(v);
+              if (st.kind == kNopeRows) {
+                const int n = st.first + j;
+                qn_g[((int64_t)t * H + n / kNope) * kNope + n % kNope] = bits;
+                __threadfence();
+              } else if (tok0 + t < a.batch) {
+                const int r = st.first + j;
+                a.q_pe[((int64_t)(tok0 + t) * H + r / kRope) * kRope + r % kRope] = bits;
+              }
+            }
+          }
+        }
+      }
+    }
+
+    __syncthreads();  // stage buffer and smem scratch free again
+    if (st.kind == kNopeRows && tid == 0) {
+      // publish the finished nope rows, per head
+      int j = 0;
+      while (j < st.count) {
+        const int h = (st.first + j) / kNope;
+        const int upto = min(st.count, (h + 1) * kNope - st.first);
+        red_release_gpu_add(ready_g + h, (uint32_t)(upto - j));
+        j = upto;
+      }
+    }
+    if (warp == 0) {
+      Stage nx;
+      if (next_stage(prod_n, prod_c, w, nx)) {
+        issue_stage(nx, buf, &bars[slot], a, &uk_map, lane);
+        ++issued;
+      }
+    }
+  }
+
+  // ---- end of call: flags, and the last CTA re-arms the counters ------
+  if (stuck >= 0 && tid == 0) {
+    // bounded second wait for the copies this CTA still has in flight
+    for (int s = stuck; s < issued; ++s)
+      (void)mbar_wait_bounded(&bars[s % S::kStages], (uint32_t)((s / S::kStages) & 1), kWaitLimit);
+  }
+  if (timed_out) atomicOr(a.err, MLA_DEVERR_TIMEOUT);
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const uint32_t total = gridDim.x * gridDim.y;
+    const uint32_t prev = atomicAdd(a.finished, 1u);
+    *flag = (prev == total - 1) ? 1 : 0;
+  }
+  __syncthreads();
+  if (*flag) {
+    for (int e = tid; e < a.groups * H; e += kThreads) a.ready[e] = 0u;
+    __syncthreads();
+    if (tid == 0) {
+      *a.finished = 0u;
+      __threadfence();
+    }
+  }
+  (void)issued;
+}
+
+template <int NT, bool MMA>
+cudaError_t launch_one(const DecodeArgs& a, const CUtensorMap* map, int num_sms,
+                       cudaStream_t stream) {
+  using S = Smem<NT, MMA>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(num_sms / a.groups), (unsigned)a.groups, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = S::kAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_fused_kernel<NT, MMA>, a, *map);
+}
+
+template <int NT, bool MMA>
+cudaError_t prepare_one() {
+  using S = Smem<NT, MMA>;
+  static_assert(S::kAlloc <= 232448, "shared memory budget");
+  return cudaFuncSetAttribute(mla_fused_kernel<NT, MMA>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, S::kAlloc);
+}
+
+}  // namespace
+
+int tokens_per_cta(int batch, bool mma) {
+  if (!mma) return batch <= 1 ? 1 : 2;
+  return batch <= 8 ? 8 : 16;
+}
+
+size_t scratch_qn_elems(int heads) { return (size_t)(MLA_MAX_BATCH + 16) * heads * kNope; }
+size_t scratch_ready_elems(int heads) { return (size_t)(MLA_MAX_BATCH / 8 + 2) * heads; }
+
+cudaError_t prepare_fused_kernels() {
+  cudaError_t e;
+  if ((e = prepare_one<1, false>()) != cudaSuccess) return e;
+  if ((e = prepare_one<2, false>()) != cudaSuccess) return e;
+  if ((e = prepare_one<8, true>()) != cudaSuccess) return e;
+  if ((e = prepare_one<16, true>()) != cudaSuccess) return e;
+  return cudaSuccess;
+}
+
+cudaError_t launch_fused(const DecodeArgs& a, const CUtensorMap* map, int nt, bool mma,
+                         int num_sms, cudaStream_t stream) {
+  if (!mma) {
+    if (nt == 1) return launch_one<1, false>(a, map, num_sms, stream);
+    if (nt == 2) return launch_one<2, false>(a, map, num_sms, stream);
+  } else {
+    if (nt == 8) return launch_one<8, true>(a, map, num_sms, stream);
+    if (nt == 16) return launch_one<16, true>(a, map, num_sms, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace mla

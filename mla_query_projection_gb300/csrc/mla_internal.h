@@ -1,0 +1,72 @@
+// mla_internal.h - host/device shared definitions of the MLA query library
+// (not part of the public C ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mla {
+
+// Geometry fixed by the method (page "mla.query", class MlaQuery).
+constexpr int kQLora = 1536;   // q_a width
+constexpr int kNope = 128;     // nope rows per head
+constexpr int kRope = 64;      // rope rows per head
+constexpr int kHeadRows = 192; // Q_B rows per head
+constexpr int kKvLora = 512;   // latent width
+constexpr int kRowE4m3 = 576;  // per-tensor cache row bytes
+constexpr int kRowDs = 656;    // fp8_ds_mla cache row bytes
+constexpr int kDsScales = 512; // byte offset of the four FP32 tile scales
+constexpr int kDsRope = 528;   // byte offset of the BF16 k_pe
+
+// Work units of the fused kernel.
+constexpr int kRowBytes = kQLora * 2;        // one Q_B row in global memory (3072 B)
+constexpr int kUkCols = 64;                  // latent columns per W_UK unit
+constexpr int kUkUnitsPerHead = kKvLora / kUkCols;  // 8
+constexpr int kUkUnitBytes = kNope * kUkCols * 2;   // 16 KiB
+// Combined per-head list of the second phase: 8 W_UK units then 64 rope rows.
+constexpr int kItemsPerHead = kUkUnitsPerHead + kRope;                       // 72
+constexpr int64_t kItemBytesPerHead = (int64_t)kUkUnitsPerHead * kUkUnitBytes +
+                                      (int64_t)kRope * kRowBytes;            // 327680
+
+struct DecodeArgs {
+  const uint16_t* w_qb;      // [H*192][1536]
+  const uint16_t* gamma_q;   // [1536]
+  const uint16_t* gamma_kv;  // [512]
+  const uint16_t* q_a;       // [B][q_a_stride]
+  const uint16_t* kv_c;      // [B][kv_c_stride]
+  const uint16_t* k_pe;      // [B][k_pe_stride]
+  int64_t q_a_stride, kv_c_stride, k_pe_stride;  // elements
+  const int64_t* slots;      // [B]
+  uint8_t* cache;            // [num_pages][page_size][row]
+  int64_t num_pages;
+  int page_size;
+  int layout;
+  const float* k_scale;      // [1] (per-tensor layout)
+  uint16_t* q_latent;        // [B][H][512]
+  uint16_t* q_pe;            // [B][H][64]
+  uint16_t* q_c;             // [B][1536] or null
+  // scratch (device)
+  uint16_t* qn;              // [groups][NT][H][128] BF16 nope values
+  uint32_t* ready;           // [groups][H] nope rows finished per head
+  uint32_t* finished;        // [1] CTAs finished (last one re-arms `ready`)
+  uint32_t* err;             // [1] MLA_DEVERR_* bits
+  int heads;
+  int batch;
+  int groups;                // token groups (grid.y)
+  float eps;
+};
+
+// Scratch sizes for `heads` heads at the largest batch.
+size_t scratch_qn_elems(int heads);
+size_t scratch_ready_elems(int heads);
+
+// Launch of the fused kernel; nt = tokens per CTA (template), mma = flavour.
+// Returns a cudaError_t.
+cudaError_t launch_fused(const DecodeArgs& a, const CUtensorMap* uk_map, int nt, bool mma,
+                         int num_sms, cudaStream_t stream);
+cudaError_t prepare_fused_kernels();
+
+int tokens_per_cta(int batch, bool mma);
+
+}  // namespace mla

@@ -1,0 +1,66 @@
+"""The C-ABI library: builds for sm_103a, loads without a GPU, exports every
+function the public header declares, and rejects bad arguments on the host
+before touching the device.  CPU only: no compute call is made."""
+
+import ctypes
+import os
+
+import pytest
+
+from mla_query_projection_gb300 import binding as B
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(B.LIB_PATH):
+        from mla_query_projection_gb300 import build
+
+        build.build()
+    return B.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = B.exported_symbols()
+    assert {"mla_query_create", "mla_query_decode", "mla_query_destroy"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/mla_query.h but not exported"
+
+
+def test_no_unexported_internal_symbols(lib):
+    # internal kernels and helpers stay hidden (only the C ABI is public)
+    with pytest.raises(AttributeError):
+        lib.launch_fused  # noqa: B018
+
+
+def test_strerror(lib):
+    assert B.strerror(B.MLA_OK) == "ok"
+    assert "invalid" in B.strerror(B.MLA_EINVAL)
+    assert B.strerror(12345) == "unknown error"
+
+
+def test_create_rejects_bad_arguments_on_host(lib):
+    h = ctypes.c_void_p()
+    assert lib.mla_query_create(None, 16, 16, 16, 16, 16, 1e-6) == B.MLA_EINVAL
+    # heads out of range
+    assert lib.mla_query_create(ctypes.byref(h), 0, 16, 16, 16, 16, 1e-6) == B.MLA_EINVAL
+    assert lib.mla_query_create(ctypes.byref(h), 129, 16, 16, 16, 16, 1e-6) == B.MLA_EINVAL
+    # null weight
+    assert lib.mla_query_create(ctypes.byref(h), 16, None, 16, 16, 16, 1e-6) == B.MLA_EINVAL
+    # misaligned weight
+    assert lib.mla_query_create(ctypes.byref(h), 16, 24, 16, 16, 16, 1e-6) == B.MLA_EINVAL
+    # negative eps
+    assert lib.mla_query_create(ctypes.byref(h), 16, 16, 16, 16, 16, -1.0) == B.MLA_EINVAL
+    assert h.value is None
+
+
+def test_decode_rejects_null_handle(lib):
+    rc = B.mla_query_decode(None, 1, 16, 0, 16, 0, 16, 0, 16, 16, 8, 64, 0, 16, 16, 16, None, None)
+    assert rc == B.MLA_EINVAL
+
+
+def test_other_entry_points_reject_null_handle(lib):
+    assert B.mla_query_set_path(None, B.MLA_PATH_FMA) == B.MLA_EINVAL
+    assert B.mla_query_path_for(None, 1) == B.MLA_EINVAL
+    with pytest.raises(B.MlaError):
+        B.mla_query_get_error(None)
+    B.mla_query_destroy(None)  # no-op

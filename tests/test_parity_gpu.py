@@ -1,0 +1,185 @@
+"""GPU parity: the CUDA path (through the C ABI) against the FP64 oracle, on
+the same seeded inputs, element by element.  Every test needs a GB300."""
+
+import numpy as np
+import pytest
+import torch
+
+from mla_query_projection_gb300 import binding as B
+from mla_query_projection_gb300 import synthetic as S
+from mla_query_projection_gb300.runner import DecodeStep
+from oracle import mla_oracle as O
+
+from .parity_util import check_bf16, check_step
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda_device():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    B.load()
+    torch.cuda.set_device(0)
+    yield
+
+
+def run_case(inp, path=B.MLA_PATH_AUTO, fused_row=False, q_c=True, repeat=1):
+    step = DecodeStep(inp, fused_row=fused_row, q_c=q_c)
+    assert step.set_path(path) == B.MLA_OK
+    for _ in range(repeat):
+        assert step.decode() == B.MLA_OK
+    out = step.results()
+    flags = step.error_flags()
+    step.close()
+    return out, flags
+
+
+def assert_parity(inp, report=None, **kw):
+    ref = O.decode_step(inp)
+    out, flags = run_case(inp, **kw)
+    want_flag = B.MLA_DEVERR_BAD_SLOT if ref["bad_slots"] else 0
+    assert flags == want_flag, f"device flags {flags}"
+    check_step(out, ref, inp, report=report, q_c=kw.get("q_c", True))
+    return out, ref
+
+
+@pytest.mark.parametrize("name", list(S.WORKLOADS))
+def test_named_workloads(name):
+    inp = S.workload_inputs(name)
+    rep = {}
+    assert_parity(inp, report=rep)
+    print(name, rep)
+
+
+@pytest.mark.parametrize("layout", [S.LAYOUT_E4M3, S.LAYOUT_DS_MLA])
+@pytest.mark.parametrize("heads", [64, 128])
+@pytest.mark.parametrize("batch", [1, 2, 4, 8, 16, 32, 64])
+def test_sweep(batch, heads, layout):
+    inp = S.make_inputs(**S.sweep_workload(batch, heads, layout))
+    assert_parity(inp)
+
+
+@pytest.mark.parametrize("batch", [3, 5, 7, 9, 15, 17, 31, 33, 63, 65, 100, 200, 256])
+def test_ragged_batches(batch):
+    layout = S.LAYOUT_DS_MLA if batch % 2 else S.LAYOUT_E4M3
+    inp = S.make_inputs(batch=batch, heads=16, layout=layout, pages=64, seed=100 + batch,
+                        outliers=0.01)
+    assert_parity(inp)
+
+
+@pytest.mark.parametrize("heads", [1, 2, 3, 5, 127, 128])
+@pytest.mark.parametrize("batch", [1, 2, 16])
+def test_head_counts(heads, batch):
+    inp = S.make_inputs(batch=batch, heads=heads, layout=S.LAYOUT_E4M3, pages=16, seed=200 + heads)
+    assert_parity(inp)
+
+
+@pytest.mark.parametrize("batch", [1, 2])
+def test_fma_and_mma_paths_agree(batch):
+    inp = S.make_inputs(batch=batch, heads=32, layout=S.LAYOUT_DS_MLA, pages=16, seed=300)
+    fma, ref = assert_parity(inp, path=B.MLA_PATH_FMA)
+    mma, _ = assert_parity(inp, path=B.MLA_PATH_MMA)
+    # the q_a RMSNorm is one code path: q_c is bit-identical across paths
+    assert np.array_equal(fma["q_c"], mma["q_c"])
+    assert np.array_equal(fma["cache"], mma["cache"])
+
+
+def test_fma_path_refuses_large_batch():
+    inp = S.make_inputs(batch=3, heads=4, layout=S.LAYOUT_E4M3, pages=4, seed=301)
+    step = DecodeStep(inp)
+    assert step.set_path(B.MLA_PATH_FMA) == B.MLA_OK
+    assert step.decode() == B.MLA_EUNSUPPORTED
+    step.close()
+
+
+@pytest.mark.parametrize("batch", [1, 8, 24])
+def test_fused_qkv_row_strides(batch):
+    inp = S.make_inputs(batch=batch, heads=16, layout=S.LAYOUT_E4M3, pages=8, seed=400 + batch)
+    assert_parity(inp, fused_row=True)
+
+
+def test_q_c_optional():
+    inp = S.make_inputs(batch=4, heads=8, layout=S.LAYOUT_E4M3, pages=8, seed=500)
+    assert_parity(inp, q_c=False)
+
+
+def test_negative_slots_skip_and_bad_slots_flag():
+    inp = S.make_inputs(batch=6, heads=8, layout=S.LAYOUT_DS_MLA, pages=4, seed=600)
+    cap = 4 * 64
+    inp["slots"] = np.array([-1, 3, cap, 17, cap + 1000, -5], dtype=np.int64)
+    out, ref = assert_parity(inp)
+    assert ref["bad_slots"] == [2, 4]
+
+
+def test_repeated_calls_rearm_and_match():
+    """Back-to-back calls on one handle: the hand-off counters re-arm (no
+    timeout flag) and every call gives the same bits."""
+    inp = S.make_inputs(batch=16, heads=64, layout=S.LAYOUT_E4M3, pages=64, seed=700)
+    step = DecodeStep(inp)
+    outs = []
+    for _ in range(5):
+        assert step.decode() == B.MLA_OK
+        outs.append(step.results())
+    assert step.error_flags() == 0
+    for o in outs[1:]:
+        for k in ("q_latent", "q_pe", "q_c"):
+            assert np.array_equal(o[k], outs[0][k])
+    step.close()
+
+
+def test_all_paths_deterministic_across_handles():
+    inp = S.make_inputs(batch=2, heads=16, layout=S.LAYOUT_E4M3, pages=8, seed=800)
+    a, _ = run_case(inp)
+    b, _ = run_case(inp)
+    for k in ("q_latent", "q_pe", "q_c", "cache"):
+        assert np.array_equal(a[k], b[k])
+
+
+def test_decode_argument_errors_on_device_buffers():
+    inp = S.make_inputs(batch=2, heads=4, layout=S.LAYOUT_E4M3, pages=4, seed=900)
+    st = DecodeStep(inp)
+    s = torch.cuda.current_stream()
+    args = [st.handle, 2, st.q_a, 0, st.kv_c, 0, st.k_pe, 0, st.slots, st.cache, st.num_pages,
+            st.page_size, st.layout, st.k_scale, st.q_latent, st.q_pe, st.q_c, s]
+
+    def call(**over):
+        a = list(args)
+        names = ["h", "batch", "q_a", "qs", "kv_c", "ks", "k_pe", "ps", "slots", "cache", "pages",
+                 "psize", "layout", "k_scale", "q_latent", "q_pe", "q_c", "stream"]
+        for k, v in over.items():
+            a[names.index(k)] = v
+        return B.mla_query_decode(*a)
+
+    assert call() == B.MLA_OK
+    assert call(batch=0) == B.MLA_EINVAL
+    assert call(batch=B.MLA_MAX_BATCH + 1) == B.MLA_EINVAL
+    assert call(q_a=None) == B.MLA_EINVAL
+    assert call(q_a=st.q_a.data_ptr() + 2) == B.MLA_EINVAL  # misaligned
+    assert call(qs=1530) == B.MLA_EINVAL  # stride below the row width
+    assert call(qs=1540) == B.MLA_EINVAL  # stride not a multiple of 8
+    assert call(layout=7) == B.MLA_EINVAL
+    assert call(k_scale=None) == B.MLA_EINVAL  # per-tensor layout needs k_scale
+    assert call(pages=0) == B.MLA_EINVAL
+    assert call() == B.MLA_OK
+    torch.cuda.synchronize()
+    assert st.error_flags() == 0
+    st.close()
+
+
+def test_weights_bound_at_create_are_read_each_call():
+    """The handle borrows the weights: changing them between calls changes
+    the result (no hidden copy)."""
+    inp = S.make_inputs(batch=1, heads=4, layout=S.LAYOUT_E4M3, pages=4, seed=1000)
+    st = DecodeStep(inp)
+    assert st.decode() == B.MLA_OK
+    first = st.results()
+    st.w_qb.mul_(2.0)
+    assert st.decode() == B.MLA_OK
+    second = st.results()
+    inp2 = dict(inp)
+    inp2["w_qb"] = (O.f64_to_bf16_bits(2.0 * O.bf16_bits_to_f64(inp["w_qb"])))
+    ref = O.decode_step(inp2)
+    check_bf16("q_pe", second["q_pe"], ref["q_pe"], ref["q_cond"][:, :, 128:])
+    assert not np.array_equal(first["q_pe"], second["q_pe"])
+    st.close()
