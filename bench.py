@@ -1,0 +1,509 @@
+"""Benchmark of the decode-step MLA query path on GB300.
+
+Default workload: one token (B=1), 64 local heads, per-tensor FP8 E4M3 KV cache
+of 1024 pages x 64 tokens ("latency_b1_h64_e4m3").  A step is one
+mla_query_decode call: q_a RMSNorm, Q_B projection, W_UK absorption and the
+paged KV insert for one batch of synthetic tokens.
+
+Timing: steps are captured in CUDA graphs and replayed; W warm-up steps, then
+exactly K timed steps between CUDA events on the launching stream, with a
+barrier and a device synchronise on both sides.  The weights rotate over
+enough independent sets that their total exceeds 3x the L2 cache, so every
+step streams its weights from HBM.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the FP64 CPU oracle
+on the same workload instead (bounded samples, host cores).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "µs per MLA-query decode step and HBM GB/s vs ~8 TB/s peak, B=1..64"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["mla_query_projection_gb300/csrc/mla_fused.cu",
+                  "mla_query_projection_gb300/csrc/mla_device.cuh"]
+
+
+def algorithmic_bytes(batch: int, heads: int, layout: int) -> int:
+    """Bytes one decode step must move: W_QB (H*192*1536*2) + W_UK (H*128*512*2)
+    + gammas (2*(1536+512)) + activations read (B*(1536+512+64)*2 + 8 slot)
+    + outputs written (B*H*(512+64)*2 + q_c B*1536*2) + cache rows (576/656)."""
+    row = 656 if layout == 1 else 576
+    return (heads * 192 * 1536 * 2 + heads * 128 * 512 * 2 + 2 * (1536 + 512)
+            + batch * ((1536 + 512 + 64) * 2 + 8) + batch * heads * (512 + 64) * 2
+            + batch * 1536 * 2 + batch * row)
+
+
+def algorithmic_flops(batch: int, heads: int) -> int:
+    return 2 * batch * heads * (192 * 1536 + 128 * 512)
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def read_peaks() -> tuple[float, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def read_traffic(workload: str) -> float | None:
+    """DRAM bytes per launch from the committed ncu summary of this workload,
+    if it was taken on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", f"mla_fused_{workload}.txt")
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    with open(p) as f:
+        for line in f:
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("kernel_sources_sha256_16") != kernel_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------- workloads
+
+WORKLOAD_DEFAULT = "latency_b1_h64_e4m3"
+
+
+def workload_cfg(name: str) -> dict:
+    from mla_query_projection_gb300 import synthetic as S
+
+    if name in S.WORKLOADS:
+        return dict(S.WORKLOADS[name])
+    # sweep point: sweep_b{B}_h{H}_{e4m3|ds}
+    parts = name.split("_")
+    if parts[0] == "sweep":
+        b, h = int(parts[1][1:]), int(parts[2][1:])
+        lay = S.LAYOUT_DS_MLA if parts[3] == "ds" else S.LAYOUT_E4M3
+        return S.sweep_workload(b, h, lay)
+    raise SystemExit(f"unknown workload {name}")
+
+
+# ---------------------------------------------------------------- GPU arm
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except FileNotFoundError:
+            self.proc = None
+            return
+        t0 = time.time()
+        while time.time() - t0 < 5.0:  # wait for the first sample
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.05)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                c = [x.strip() for x in line.split(",")]
+                if len(c) < 9:
+                    continue
+                try:
+                    sm.append(float(c[1]))
+                    smax.append(float(c[2]))
+                    power.append(float(c[3]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, c[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {
+            "sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(smax) if smax else None,
+            "reasons": sorted(reasons),
+            "samples": len(sm),
+            "power_w_max": max(power) if power else None,
+        }
+
+
+def gpu_arm(args, rank: int, world: int, local_rank: int) -> dict | None:
+    import numpy as np
+    import torch
+
+    from mla_query_projection_gb300 import binding as B
+    from mla_query_projection_gb300 import synthetic as S
+    from mla_query_projection_gb300.runner import bf16_tensor
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    cfg = workload_cfg(args.workload)
+    inp = S.make_inputs(**cfg)
+    Bn, H, layout = cfg["batch"], cfg["heads"], cfg["layout"]
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    wbytes = H * (192 * 1536 + 128 * 512) * 2
+    nsets = max(1, -(-3 * l2 // wbytes))
+
+    # Weight sets: set 0 from the seeded generator, the others drawn on the
+    # device from a seeded torch generator with the same distributions.
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234 + rank)
+    sets = []
+    for k in range(nsets):
+        if k == 0:
+            w = dict(w_qb=bf16_tensor(inp["w_qb"], dev), w_uk=bf16_tensor(inp["w_uk"], dev),
+                     gamma_q=bf16_tensor(inp["gamma_q"], dev),
+                     gamma_kv=bf16_tensor(inp["gamma_kv"], dev))
+        else:
+            w = dict(
+                w_qb=(torch.randn(H * 192, 1536, device=dev, generator=gen) * 0.02).bfloat16(),
+                w_uk=(torch.randn(H, 128, 512, device=dev, generator=gen) * 0.05).bfloat16(),
+                gamma_q=(1 + 0.1 * torch.randn(1536, device=dev, generator=gen)).bfloat16(),
+                gamma_kv=(1 + 0.1 * torch.randn(512, device=dev, generator=gen)).bfloat16())
+        w["handle"] = B.mla_query_create(H, w["w_qb"], w["w_uk"], w["gamma_q"], w["gamma_kv"],
+                                         float(inp["eps"]))
+        if args.path:
+            B.mla_query_set_path(w["handle"], args.path)
+        sets.append(w)
+
+    q_a = bf16_tensor(inp["q_a"], dev)
+    kv_c = bf16_tensor(inp["kv_c"], dev)
+    k_pe = bf16_tensor(inp["k_pe"], dev)
+    slots = torch.from_numpy(inp["slots"]).to(dev)
+    cache = torch.from_numpy(inp["cache"]).to(dev)
+    k_scale = torch.tensor([inp["k_scale"]], dtype=torch.float32, device=dev)
+    q_latent = torch.empty(Bn, H, 512, dtype=torch.bfloat16, device=dev)
+    q_pe = torch.empty(Bn, H, 64, dtype=torch.bfloat16, device=dev)
+    q_c = torch.empty(Bn, 1536, dtype=torch.bfloat16, device=dev)
+    pages, psize = cache.shape[0], cache.shape[1]
+
+    def decode(j, stream, qa=q_a, kvc=kv_c, kpe=k_pe, sl=slots, ql=q_latent, qp=q_pe, qc=q_c):
+        rc = B.mla_query_decode(sets[j % nsets]["handle"], Bn, qa, 0, kvc, 0, kpe, 0, sl, cache,
+                                pages, psize, layout, k_scale, ql, qp, qc, stream)
+        if rc != B.MLA_OK:
+            raise RuntimeError(f"mla_query_decode: {B.strerror(rc)}")
+
+    stream = torch.cuda.Stream(dev)
+    G = max(1, min(args.graph_steps, args.steps))
+    # graphs: G steps each (the step index inside a graph picks the weight set)
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            for j in range(2):  # eager warm-up of the capture stream
+                decode(j, stream)
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for j in range(n):
+                    decode(j, torch.cuda.current_stream())
+        return g
+
+    g_full = capture(G)
+    rem = args.steps % G
+    g_rem = capture(rem) if rem else None
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+
+    # warm-up (untimed)
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, -(-args.warmup // G))):
+            g_full.replay()
+    torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps // G):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1)
+    flags = B.mla_query_get_error(sets[0]["handle"], stream)
+    for w in sets[1:]:
+        flags |= B.mla_query_get_error(w["handle"], stream)
+    if flags:
+        raise RuntimeError(f"device error flags {flags} during the timed run")
+
+    # e2e: host (pinned) inputs -> device, decode, outputs -> host, every step.
+    K_e = max(1, min(args.steps, args.e2e_steps))
+    h_qa, h_kvc, h_kpe = q_a.cpu().pin_memory(), kv_c.cpu().pin_memory(), k_pe.cpu().pin_memory()
+    h_sl = slots.cpu().pin_memory()
+    o_ql = torch.empty_like(q_latent, device="cpu").pin_memory()
+    o_qp = torch.empty_like(q_pe, device="cpu").pin_memory()
+    o_qc = torch.empty_like(q_c, device="cpu").pin_memory()
+    d_qa, d_kvc, d_kpe, d_sl = (torch.empty_like(t) for t in (q_a, kv_c, k_pe, slots))
+
+    def e2e_step(j):
+        d_qa.copy_(h_qa, non_blocking=True)
+        d_kvc.copy_(h_kvc, non_blocking=True)
+        d_kpe.copy_(h_kpe, non_blocking=True)
+        d_sl.copy_(h_sl, non_blocking=True)
+        decode(j, stream, qa=d_qa, kvc=d_kvc, kpe=d_kpe, sl=d_sl)
+        o_ql.copy_(q_latent, non_blocking=True)
+        o_qp.copy_(q_pe, non_blocking=True)
+        o_qc.copy_(q_c, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for j in range(min(50, K_e)):
+            e2e_step(j)
+    torch.cuda.synchronize(dev)
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        f0.record(stream)
+        for j in range(K_e):
+            e2e_step(j)
+        f1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    ms_e2e = f0.elapsed_time(f1)
+    h2d = sum(t.numel() * t.element_size() for t in (h_qa, h_kvc, h_kpe, h_sl))
+    d2h = sum(t.numel() * t.element_size() for t in (o_ql, o_qp, o_qc))
+
+    for w in sets:
+        B.mla_query_destroy(w["handle"])
+
+    per_step_ms = ms / args.steps
+    per_step_e2e_ms = ms_e2e / K_e
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([per_step_ms, per_step_e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        per_step_ms, per_step_e2e_ms = float(t[0]), float(t[1])
+
+    return dict(per_step_ms=per_step_ms, per_step_e2e_ms=per_step_e2e_ms, h2d=h2d, d2h=d2h,
+                clocks=clocks, nsets=nsets, l2=l2, K_e=K_e, cfg=cfg)
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+_ORACLE_CHILD = r"""
+import json, sys, time
+sys.path.insert(0, sys.argv[1])
+import numpy as np
+from oracle import mla_oracle as O
+d = np.load(sys.argv[2])
+inp = {k: d[k] for k in d.files}
+for k in ("layout",):
+    inp[k] = int(inp[k])
+for k in ("k_scale", "eps"):
+    inp[k] = float(inp[k])
+budget, steps = float(sys.argv[3]), int(sys.argv[4])
+O.decode_step(inp)  # warm
+t0 = time.perf_counter(); n = 0
+while True:
+    O.decode_step(inp); n += 1
+    el = time.perf_counter() - t0
+    if (steps and n >= steps) or (not steps and el >= budget):
+        break
+print(json.dumps({"seconds": el, "samples": n}))
+"""
+
+
+def oracle_time(cfg: dict, sample_heads: int, budget_s: float, steps: int = 0) -> dict:
+    """Time the oracle (single-threaded BLAS) on `sample_heads` heads of the
+    workload's batch with an 8-page cache; returns seconds per sample."""
+    import numpy as np
+
+    from mla_query_projection_gb300 import synthetic as S
+
+    c = dict(cfg)
+    c.update(heads=sample_heads, pages=8)
+    inp = S.make_inputs(**c)
+    fd, path = tempfile.mkstemp(suffix=".npz")
+    os.close(fd)
+    np.savez(path, **{k: np.asarray(v) for k, v in inp.items()})
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        out = subprocess.run([sys.executable, "-c", _ORACLE_CHILD, ROOT, path, str(budget_s),
+                              str(steps)], capture_output=True, text=True, env=env, check=True)
+    finally:
+        os.unlink(path)
+    r = json.loads(out.stdout.strip().splitlines()[-1])
+    return dict(sec_per_sample=r["seconds"] / r["samples"], samples=r["samples"],
+                seconds=r["seconds"])
+
+
+def cpu_baseline(cfg: dict, budget_s: float) -> dict:
+    """Oracle us per full decode step, from two head counts (linear in H)."""
+    H = cfg["heads"]
+    h1, h2 = 1, min(H, 8)
+    t1 = oracle_time(cfg, h1, budget_s / 3)
+    t2 = oracle_time(cfg, h2, 2 * budget_s / 3) if h2 > h1 else t1
+    per_head = (t2["sec_per_sample"] - t1["sec_per_sample"]) / max(1, h2 - h1)
+    full = t1["sec_per_sample"] + per_head * (H - h1)
+    return {
+        "value": full * 1e6,
+        "unit": "us",
+        "cores": 1,
+        "kind": "oracle",
+        "sample": (f"FP64 numpy oracle, single-threaded BLAS, B={cfg['batch']} tokens on "
+                   f"{h1} and {h2} heads (8-page cache), {t1['samples']}+{t2['samples']} "
+                   f"samples in {t1['seconds'] + t2['seconds']:.1f} s, extrapolated linearly "
+                   f"to {H} heads"),
+    }
+
+
+# ---------------------------------------------------------------- main
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD_DEFAULT)
+    ap.add_argument("--graph-steps", type=int, default=100)
+    ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--path", type=int, default=0, help="force MLA_PATH_* (0 = auto)")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    cfg = workload_cfg(args.workload)
+    Bn, H, layout = cfg["batch"], cfg["heads"], cfg["layout"]
+    config = {"workload": args.workload, "batch": Bn, "heads": H,
+              "kv_layout": "fp8_ds_mla" if layout == 1 else "fp8_e4m3_per_tensor",
+              "pages": cfg["pages"], "page_size": 64}
+
+    if args.impl == "reference":
+        # The reference arm is the FP64 CPU oracle; rank 0 alone runs it.
+        if rank != 0:
+            return
+        t_full = oracle_time(cfg, min(H, 8), 2.0)["sec_per_sample"] * H / min(H, 8)
+        budget = 150.0
+        per_step_budget = budget / max(1, args.steps + args.warmup)
+        hs = max(1, min(H, int(H * per_step_budget / max(t_full, 1e-9))))
+        oracle_time(cfg, hs, 0.0, steps=min(args.warmup, 50))
+        r = oracle_time(cfg, hs, 0.0, steps=args.steps)
+        us = r["sec_per_sample"] * 1e6 * H / hs
+        line = {
+            "impl": "reference", "metric": METRIC, "value": us, "unit": "us",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": us / 1e3, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+            "cpu_baseline": {"value": us, "unit": "us", "cores": 1, "kind": "oracle",
+                             "sample": f"each step: the FP64 oracle on {hs} of {H} heads "
+                                       f"(B={Bn}, 8-page cache), scaled by {H}/{hs}"},
+            "e2e": {"value": us, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
+        print(json.dumps(line), flush=True)
+        return
+
+    import torch
+
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    r = gpu_arm(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+
+    per_step_us = r["per_step_ms"] * 1e3
+    value = per_step_us / world  # whole-job time per decode step (N replicas)
+    nbytes = algorithmic_bytes(Bn, H, layout)
+    achieved = nbytes / (per_step_us * 1e-6) / 1e9
+    peak, peak_src = read_peaks()
+    config.update({
+        "l2_policy": f"inputs larger than L2: {r['nsets']} rotating weight sets "
+                     f"({r['nsets'] * H * 720 * 1024 / 1e6:.0f} MB vs L2 {r['l2'] / 1e6:.0f} MB)",
+        "graph_steps": args.graph_steps, "parallelism": f"replicas{world}",
+    })
+    line = {
+        "metric": METRIC, "value": value, "unit": "us", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": r["per_step_ms"], "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config,
+        "tokens_per_s": Bn * world / (r["per_step_ms"] * 1e-3),
+        "hbm_gbs": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_src} (MEASURED_PEAKS hbm_gbs)",
+                     "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
+                     "algorithmic_bytes_per_launch": nbytes,
+                     "traffic": read_traffic(args.workload),
+                     "kernel": "mla_fused_kernel", "gflop_per_launch": algorithmic_flops(Bn, H) / 1e9},
+        "e2e": {"value": r["per_step_e2e_ms"] * 1e3 / world, "unit": "us",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+                "steps": r["K_e"], "note": "eager C-ABI calls with pinned host buffers"},
+        "gpu_launches": args.steps,
+        "clocks": r["clocks"],
+    }
+    if not args.no_cpu and world == 1:
+        line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_budget)
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

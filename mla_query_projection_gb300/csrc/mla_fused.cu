@@ -140,85 +140,87 @@ __device__ __forceinline__ void issue_stage(const Stage& s, uint8_t* buf, uint64
   }
 }
 
+__device__ __forceinline__ void named_barrier(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Paged FP8 KV insert of token b (page "mla.query", methods insert, kv_fp8,
-// insert_ds).  Called by the whole CTA; threads 0..71 work.
-__device__ void kv_insert(const DecodeArgs& a, int b, float* red2) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// insert_ds), run by the 64 threads of warps 6-7 (lt = 0..63) while warps 0-5
+// normalise q_a.  Thread lt owns latent columns 8*lt..8*lt+7; threads 0..7
+// also own k_pe values 8*lt..8*lt+7.  red2 holds the two warps' partial sums.
+__device__ void kv_insert(const DecodeArgs& a, int b, int lt, float* red2) {
+  const int lane = lt & 31, w = lt >> 5;
   const int64_t slot = a.slots[b];
+  const uint4 v = *reinterpret_cast<const uint4*>(a.kv_c + (int64_t)b * a.kv_c_stride + 8 * lt);
+  const uint4 gv = *reinterpret_cast<const uint4*>(a.gamma_kv + 8 * lt);
+  uint4 pe = make_uint4(0, 0, 0, 0);
+  if (lt < 8) pe = *reinterpret_cast<const uint4*>(a.k_pe + (int64_t)b * a.k_pe_stride + 8 * lt);
+  const bool ds = a.layout == MLA_KV_FP8_DS_MLA;
+  const float ks = ds ? 1.0f : *a.k_scale;
+  float x[8];
+  const uint32_t xw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = bf16lo(xw[i]);
+    x[2 * i + 1] = bf16hi(xw[i]);
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) ss = fmaf(x[i], x[i], ss);
+  ss = warp_sum(ss);
+  if (lane == 0) red2[w] = ss;
+  named_barrier(2, 64);
+  const float total = red2[0] + red2[1];
+  named_barrier(2, 64);  // red2 may be reused by the next token
   if (slot < 0) return;
   const int64_t page = slot / a.page_size, off = slot % a.page_size;
   if (page >= a.num_pages) {
-    if (tid == 0) atomicOr(a.err, MLA_DEVERR_BAD_SLOT);
+    if (lt == 0) atomicOr(a.err, MLA_DEVERR_BAD_SLOT);
     return;
   }
-  const bool ds = a.layout == MLA_KV_FP8_DS_MLA;
   uint8_t* row = a.cache + (page * a.page_size + off) * (ds ? kRowDs : kRowE4m3);
-  float x[8];
-  if (tid < 64) {
-    const uint4 v = *reinterpret_cast<const uint4*>(a.kv_c + (int64_t)b * a.kv_c_stride + 8 * tid);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    float ss = 0.f;
+  const float rr = __frsqrt_rn(__fadd_rn(__fmul_rn(total, 1.0f / 512.0f), a.eps));
+  const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+  float n[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      x[2 * i] = bf16lo(w[i]);
-      x[2 * i + 1] = bf16hi(w[i]);
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) ss = fmaf(x[i], x[i], ss);
-    ss = warp_sum(ss);
-    if (lane == 0) red2[warp] = ss;
+  for (int i = 0; i < 4; ++i) {
+    n[2 * i] = bf_round(__fmul_rn(__fmul_rn(x[2 * i], rr), bf16lo(gw[i])));
+    n[2 * i + 1] = bf_round(__fmul_rn(__fmul_rn(x[2 * i + 1], rr), bf16hi(gw[i])));
   }
-  __syncthreads();
-  if (tid < 64) {
-    const float total = red2[0] + red2[1];
-    const float rr = __frsqrt_rn(__fadd_rn(__fmul_rn(total, 1.0f / 512.0f), a.eps));
-    const uint4 gv = *reinterpret_cast<const uint4*>(a.gamma_kv + 8 * tid);
-    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-    float n[8];
+  uint2 out;
+  if (!ds) {
+    out.x = (uint32_t)e4m3x2(__fdiv_rn(n[0], ks), __fdiv_rn(n[1], ks)) |
+            ((uint32_t)e4m3x2(__fdiv_rn(n[2], ks), __fdiv_rn(n[3], ks)) << 16);
+    out.y = (uint32_t)e4m3x2(__fdiv_rn(n[4], ks), __fdiv_rn(n[5], ks)) |
+            ((uint32_t)e4m3x2(__fdiv_rn(n[6], ks), __fdiv_rn(n[7], ks)) << 16);
+  } else {
+    float amax = 0.f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      n[2 * i] = bf_round(__fmul_rn(__fmul_rn(x[2 * i], rr), bf16lo(gw[i])));
-      n[2 * i + 1] = bf_round(__fmul_rn(__fmul_rn(x[2 * i + 1], rr), bf16hi(gw[i])));
-    }
-    uint2 out;
-    if (!ds) {
-      const float ks = *a.k_scale;
-      out.x = (uint32_t)e4m3x2(__fdiv_rn(n[0], ks), __fdiv_rn(n[1], ks)) |
-              ((uint32_t)e4m3x2(__fdiv_rn(n[2], ks), __fdiv_rn(n[3], ks)) << 16);
-      out.y = (uint32_t)e4m3x2(__fdiv_rn(n[4], ks), __fdiv_rn(n[5], ks)) |
-              ((uint32_t)e4m3x2(__fdiv_rn(n[6], ks), __fdiv_rn(n[7], ks)) << 16);
-    } else {
-      float amax = 0.f;
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(n[i]));
 #pragma unroll
-      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(n[i]));
-#pragma unroll
-      for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-      const float scale = pow2_ceil_f32(fmaxf(__fdiv_rn(amax, 448.0f), 1e-4f));
-      const float inv = __fdiv_rn(1.0f, scale);  // exact: a power of two
-      out.x = (uint32_t)e4m3x2(n[0] * inv, n[1] * inv) |
-              ((uint32_t)e4m3x2(n[2] * inv, n[3] * inv) << 16);
-      out.y = (uint32_t)e4m3x2(n[4] * inv, n[5] * inv) |
-              ((uint32_t)e4m3x2(n[6] * inv, n[7] * inv) << 16);
-      if ((lane & 15) == 0) *reinterpret_cast<float*>(row + kDsScales + 4 * (tid >> 4)) = scale;
-    }
-    *reinterpret_cast<uint2*>(row + 8 * tid) = out;
-  } else if (tid < 72) {
-    const int c = tid - 64;
-    const uint4 v = *reinterpret_cast<const uint4*>(a.k_pe + (int64_t)b * a.k_pe_stride + 8 * c);
+    for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const float scale = pow2_ceil_f32(fmaxf(__fdiv_rn(amax, 448.0f), 1e-4f));
+    const float inv = __fdiv_rn(1.0f, scale);  // exact: a power of two
+    out.x = (uint32_t)e4m3x2(n[0] * inv, n[1] * inv) |
+            ((uint32_t)e4m3x2(n[2] * inv, n[3] * inv) << 16);
+    out.y = (uint32_t)e4m3x2(n[4] * inv, n[5] * inv) |
+            ((uint32_t)e4m3x2(n[6] * inv, n[7] * inv) << 16);
+    if ((lane & 15) == 0) *reinterpret_cast<float*>(row + kDsScales + 4 * (lt >> 4)) = scale;
+  }
+  *reinterpret_cast<uint2*>(row + 8 * lt) = out;
+  if (lt < 8) {
     if (ds) {
-      *reinterpret_cast<uint4*>(row + kDsRope + 16 * c) = v;
+      *reinterpret_cast<uint4*>(row + kDsRope + 16 * lt) = pe;
     } else {
-      const float ks = *a.k_scale;
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      uint2 out;
-      out.x = (uint32_t)e4m3x2(__fdiv_rn(bf16lo(w[0]), ks), __fdiv_rn(bf16hi(w[0]), ks)) |
-              ((uint32_t)e4m3x2(__fdiv_rn(bf16lo(w[1]), ks), __fdiv_rn(bf16hi(w[1]), ks)) << 16);
-      out.y = (uint32_t)e4m3x2(__fdiv_rn(bf16lo(w[2]), ks), __fdiv_rn(bf16hi(w[2]), ks)) |
-              ((uint32_t)e4m3x2(__fdiv_rn(bf16lo(w[3]), ks), __fdiv_rn(bf16hi(w[3]), ks)) << 16);
-      *reinterpret_cast<uint2*>(row + kKvLora + 8 * c) = out;
+      const uint32_t w2[4] = {pe.x, pe.y, pe.z, pe.w};
+      uint2 o2;
+      o2.x = (uint32_t)e4m3x2(__fdiv_rn(bf16lo(w2[0]), ks), __fdiv_rn(bf16hi(w2[0]), ks)) |
+             ((uint32_t)e4m3x2(__fdiv_rn(bf16lo(w2[1]), ks), __fdiv_rn(bf16hi(w2[1]), ks)) << 16);
+      o2.y = (uint32_t)e4m3x2(__fdiv_rn(bf16lo(w2[2]), ks), __fdiv_rn(bf16hi(w2[2]), ks)) |
+             ((uint32_t)e4m3x2(__fdiv_rn(bf16lo(w2[3]), ks), __fdiv_rn(bf16hi(w2[3]), ks)) << 16);
+      *reinterpret_cast<uint2*>(row + kKvLora + 8 * lt) = o2;
     }
   }
-  __syncthreads();
 }
 
 template <int NT, bool MMA>
@@ -277,67 +279,61 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();
   pdl_launch_dependents();
 
-  // ---- q_a RMSNorm of this group's tokens -> xq (BF16, smem) ------------
+  // ---- q_a RMSNorm of this group's tokens -> xq (warps 0-5), and the ----
+  // ---- paged KV insert of this CTA's tokens (warps 6-7), concurrently ---
   const int tok0 = grp * NT;
-  {
+  if (warp < 6) {
     uint4 xv[NT];
-    if (tid < 192) {
 #pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        if (tok0 + t < a.batch)
-          xv[t] = *reinterpret_cast<const uint4*>(a.q_a + (int64_t)(tok0 + t) * a.q_a_stride +
-                                                  8 * tid);
-        else
-          xv[t] = make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        const uint32_t ww[4] = {xv[t].x, xv[t].y, xv[t].z, xv[t].w};
-        float ss = 0.f;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          ss = fmaf(bf16lo(ww[k]), bf16lo(ww[k]), ss);
-          ss = fmaf(bf16hi(ww[k]), bf16hi(ww[k]), ss);
-        }
-        ss = warp_sum(ss);
-        if (lane == 0) ss_part[t * 8 + warp] = ss;
-      }
+    for (int t = 0; t < NT; ++t) {
+      if (tok0 + t < a.batch)
+        xv[t] = *reinterpret_cast<const uint4*>(a.q_a + (int64_t)(tok0 + t) * a.q_a_stride +
+                                                8 * tid);
+      else
+        xv[t] = make_uint4(0, 0, 0, 0);
     }
-    __syncthreads();
-    if (tid < 192) {
-      const uint4 gv = *reinterpret_cast<const uint4*>(a.gamma_q + 8 * tid);
-      const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    const uint4 gv = *reinterpret_cast<const uint4*>(a.gamma_q + 8 * tid);
 #pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        const float* sp = ss_part + t * 8;
-        const float total = ((((sp[0] + sp[1]) + sp[2]) + sp[3]) + sp[4]) + sp[5];
-        const float rr = __frsqrt_rn(__fadd_rn(__fdiv_rn(total, 1536.0f), a.eps));
-        const uint32_t ww[4] = {xv[t].x, xv[t].y, xv[t].z, xv[t].w};
-        uint4 o;
-        uint32_t* op = &o.x;
+    for (int t = 0; t < NT; ++t) {
+      const uint32_t ww[4] = {xv[t].x, xv[t].y, xv[t].z, xv[t].w};
+      float ss = 0.f;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float lo = __fmul_rn(__fmul_rn(bf16lo(ww[k]), rr), bf16lo(gw[k]));
-          const float hi = __fmul_rn(__fmul_rn(bf16hi(ww[k]), rr), bf16hi(gw[k]));
-          op[k] = pack_bf16x2(lo, hi);
-        }
-        if (tok0 + t >= a.batch) o = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(xq + t * kPitch + 16 * tid) = o;
+      for (int k = 0; k < 4; ++k) {
+        ss = fmaf(bf16lo(ww[k]), bf16lo(ww[k]), ss);
+        ss = fmaf(bf16hi(ww[k]), bf16hi(ww[k]), ss);
       }
+      ss = warp_sum(ss);
+      if (lane == 0) ss_part[t * 8 + warp] = ss;
     }
-    __syncthreads();
+    named_barrier(1, 192);
+    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const float* sp = ss_part + t * 8;
+      const float total = ((((sp[0] + sp[1]) + sp[2]) + sp[3]) + sp[4]) + sp[5];
+      const float rr = __frsqrt_rn(__fadd_rn(__fdiv_rn(total, 1536.0f), a.eps));
+      const uint32_t ww[4] = {xv[t].x, xv[t].y, xv[t].z, xv[t].w};
+      uint4 o;
+      o.x = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[0]), rr), bf16lo(gw[0])),
+                        __fmul_rn(__fmul_rn(bf16hi(ww[0]), rr), bf16hi(gw[0])));
+      o.y = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[1]), rr), bf16lo(gw[1])),
+                        __fmul_rn(__fmul_rn(bf16hi(ww[1]), rr), bf16hi(gw[1])));
+      o.z = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[2]), rr), bf16lo(gw[2])),
+                        __fmul_rn(__fmul_rn(bf16hi(ww[2]), rr), bf16hi(gw[2])));
+      o.w = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[3]), rr), bf16lo(gw[3])),
+                        __fmul_rn(__fmul_rn(bf16hi(ww[3]), rr), bf16hi(gw[3])));
+      if (tok0 + t >= a.batch) o = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(xq + t * kPitch + 16 * tid) = o;
+      // q_c rows (page "mla.query", method store_qc): CTA 0 of the group.
+      if (i == 0 && a.q_c != nullptr && tok0 + t < a.batch)
+        *reinterpret_cast<uint4*>(a.q_c + (int64_t)(tok0 + t) * kQLora + 8 * tid) = o;
+    }
+  } else {
+    // token t of the group is inserted by CTA t % P
+    for (int t = i; t < NT; t += P)
+      if (tok0 + t < a.batch) kv_insert(a, tok0 + t, tid - 192, ss_part + NT * 8);
   }
-
-  // q_c rows (page "mla.query", method store_qc): CTA 0 of the group.
-  if (i == 0 && a.q_c != nullptr && tid < 192) {
-    for (int t = 0; t < NT && tok0 + t < a.batch; ++t)
-      *reinterpret_cast<uint4*>(a.q_c + (int64_t)(tok0 + t) * kQLora + 8 * tid) =
-          *reinterpret_cast<const uint4*>(xq + t * kPitch + 16 * tid);
-  }
-
-  // KV insert: token t of the group goes to CTA t % P.
-  for (int t = i; t < NT; t += P)
-    if (tok0 + t < a.batch) kv_insert(a, tok0 + t, ss_part + NT * 8);
+  __syncthreads();
 
   // FMA flavour: this lane's x values in registers (k = 256 c + 8 lane + e).
   float xr[MMA ? 1 : NT][MMA ? 1 : 48];
@@ -526,7 +522,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (st.kind == kNopeRows) {
             const int n = st.first + j;
             qn_g[((int64_t)t * H + n / kNope) * kNope + n % kNope] = bits;
-            __threadfence();
           } else if (tok0 + t < a.batch) {
             const int r = st.first + j;
             a.q_pe[((int64_t)(tok0 + t) * H + r / kRope) * kRope + r % kRope] = bits;
@@ -563,7 +558,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (st.kind == kNopeRows) {
                 const int n = st.first + j;
                 qn_g[((int64_t)t * H + n / kNope) * kNope + n % kNope] = bits;
-                __threadfence();
               } else if (tok0 + t < a.batch) {
                 const int r = st.first + j;
                 a.q_pe[((int64_t)(tok0 + t) * H + r / kRope) * kRope + r % kRope] = bits;
@@ -576,7 +570,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     __syncthreads();  // stage buffer and smem scratch free again
     if (st.kind == kNopeRows && tid == 0) {
-      // publish the finished nope rows, per head
+      // Publish the finished nope rows, per head.  The CTA barrier above
+      // orders every thread's q stores before this thread's fence, and the
+      // fence (cumulative) makes them visible GPU-wide before the counter.
+      __threadfence();
       int j = 0;
       while (j < st.count) {
         const int h = (st.first + j) / kNope;

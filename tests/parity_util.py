@@ -1,11 +1,19 @@
 """Comparison of the CUDA path's outputs with the FP64 oracle's.
 
-Tolerances (the acceptance bar of the MLA query path):
+Tolerances (the acceptance bar of the MLA query path), with r the oracle's
+BF16-rounded value, g the GPU's, and S = sum_i |a_i * b_i| the magnitude of the
+terms of the dot product that produced the output (K terms):
   * BF16 outputs (q_c, q_pe, q_latent): at least 99.9% of elements within one
-    BF16 ulp, measured as a relative error of 2**-7 against the oracle's
-    BF16-rounded value, and relative error at most 1e-2 everywhere, where the
-    denominator is max(|ref|, 2**-8 * sum|terms|) so that outputs whose dot
-    product cancels to near zero are judged against the size of their terms.
+    BF16 ulp, i.e. |g - r| <= 2**-7 * |r| + K * 2**-24 * S.  The second term is
+    the worst-case error bound of a K-term FP32 summation (Higham's gamma_K
+    times S); without it, outputs whose dot product cancels to almost zero fail
+    on rounding error alone (observed: q_pe = -1.39e-5 from terms summing to
+    ~20 in magnitude).
+  * Everywhere: |g - r| <= 1e-2 * max(|r|, S).  Relative error of a cancelling
+    dot product is judged against the size of its terms: the absorption reads
+    BF16-rounded q values, and one q value rounded to the other side of a tie
+    (legitimate for any FP32 accumulation order) moves an output by up to one
+    BF16 ulp of that single term, 6.2e-2 of 2**-8 * S in one observed case.
   * FP8 cache bytes: at least 99.9% identical; the rest within one E4M3 code
     (codes compared as signed ordinals, so +0 and -0 are equal).
   * fp8_ds_mla power-of-two scales, k_pe bytes, slot/page placement and every
@@ -24,22 +32,27 @@ FRAC_WITHIN_ULP = 0.999
 FRAC_FP8_EXACT = 0.999
 
 
-def check_bf16(name, got_bits, ref_bits, cond=None, report=None):
+def check_bf16(name, got_bits, ref_bits, cond=None, k_terms=0, report=None):
     g = O.bf16_bits_to_f64(got_bits)
     r = O.bf16_bits_to_f64(ref_bits)
     assert g.shape == r.shape, (name, g.shape, r.shape)
     assert np.all(np.isfinite(g)), f"{name}: non-finite GPU output"
     err = np.abs(g - r)
-    within = err <= ULP_REL * np.abs(r)
-    denom = np.abs(r)
-    if cond is not None:
-        denom = np.maximum(denom, 2.0**-8 * cond)
+    if cond is None:
+        cond = np.zeros_like(r)
+    tol = ULP_REL * np.abs(r) + k_terms * 2.0**-24 * cond
+    within = err <= tol
+    denom = np.maximum(np.abs(r), cond)
     denom = np.where(denom == 0, 1.0, denom)
     rel = err / denom
     frac = float(np.mean(within)) if within.size else 1.0
-    exact = float(np.mean(got_bits == ref_bits)) if within.size else 1.0
     if report is not None:
-        report[name] = dict(within_ulp=frac, bit_exact=exact, max_rel=float(rel.max(initial=0.0)))
+        report[name] = dict(
+            within_tol=frac,
+            within_plain_ulp=float(np.mean(err <= ULP_REL * np.abs(r))) if r.size else 1.0,
+            bit_exact=float(np.mean(got_bits == ref_bits)) if r.size else 1.0,
+            max_rel=float(rel.max(initial=0.0)),
+        )
     assert frac >= FRAC_WITHIN_ULP, f"{name}: only {frac:.5f} within 1 BF16 ulp"
     assert rel.max(initial=0.0) <= MAX_REL, f"{name}: max rel {rel.max():.3e}"
 
@@ -79,7 +92,9 @@ def check_cache(got, ref, before, slots, page_size, layout, report=None):
 def check_step(gpu: dict, ref: dict, inp: dict, report=None, q_c=True):
     if q_c:
         check_bf16("q_c", gpu["q_c"], ref["q_c"], report=report)
-    check_bf16("q_pe", gpu["q_pe"], ref["q_pe"], ref["q_cond"][:, :, 128:], report=report)
-    check_bf16("q_latent", gpu["q_latent"], ref["q_latent"], ref["lat_cond"], report=report)
+    check_bf16("q_pe", gpu["q_pe"], ref["q_pe"], ref["q_cond"][:, :, 128:], k_terms=1536,
+               report=report)
+    check_bf16("q_latent", gpu["q_latent"], ref["q_latent"], ref["lat_cond"], k_terms=128,
+               report=report)
     check_cache(gpu["cache"], ref["cache"], inp["cache"], inp["slots"], inp["cache"].shape[1],
                 int(inp["layout"]), report=report)
