@@ -9,40 +9,44 @@
 // GB300 design (not the page's cluster design):
 //  * Weight streaming.  Each CTA owns a byte-balanced share of three lists:
 //    the H*128 nope rows of W_QB, then a combined list per head of the eight
-//    64-column W_UK tiles and the 64 rope rows.  Rows arrive by 1-D bulk TMA
-//    (3 KiB each, padded smem pitch), W_UK tiles by 2-D tensor TMA with 128 B
-//    swizzle, into a ring of 16-row stages tracked by mbarriers.  The first
-//    stages are issued before the programmatic-dependent-launch wait, since
-//    weights do not depend on the previous kernel.
+//    64-column W_UK tiles and the 64 rope rows.  A producer warp streams them
+//    into a ring of stages: rows by 1-D bulk TMA (3 KiB each, padded smem
+//    pitch), W_UK tiles by 2-D tensor TMA with 128 B swizzle; full/empty
+//    mbarriers pace it, so a slot is refilled as soon as the eight consumer
+//    warps release it.  Weights do not depend on the previous kernel, so the
+//    producer starts before the programmatic-dependent-launch wait.
 //  * Nope hand-off.  All CTAs stream their nope rows first and publish the
 //    BF16 q values to a small global scratch; a per-(group, head) counter
-//    reaches 128 when a head is complete.  The W_UK tiles of a head come
-//    later in every CTA's order, so by then the counters are normally full;
-//    the wait is bounded and raises MLA_DEVERR_TIMEOUT instead of hanging.
-//    The last CTA to finish re-arms the counters for the next call.
-//  * Arithmetic.  FMA flavour (1-2 tokens): FP32 FMAs, one warp per row,
-//    x held in registers.  MMA flavour (8 or 16 tokens per CTA): BF16
-//    mma.sync m16n8k16 with the weight rows as the M side (tokens are N),
-//    K split over the 8 warps and reduced in a fixed order through smem; the
-//    absorption uses ldmatrix.trans on the swizzled W_UK tile as the M side.
+//    reaches 128 when a head is complete (one release per head and writer).
+//    The W_UK tiles of a head come later in every CTA's order, so by then the
+//    counters are normally full; the wait is bounded and raises
+//    MLA_DEVERR_TIMEOUT instead of hanging.  The last CTA re-arms the counters.
+//  * Arithmetic.  FMA flavour (1-2 tokens, 8-row stages): FP32 FMAs, one warp
+//    per row, x in registers.  MMA flavour (8 or 16 tokens per CTA, 16-row
+//    stages): BF16 mma.sync m16n8k16 with the weight rows as the M side
+//    (tokens are N), K split over the eight consumer warps and reduced in a
+//    fixed order through smem; the absorption takes the swizzled W_UK tile as
+//    the M side through ldmatrix.trans.
 #include <cuda_bf16.h>
 
+#include "../../include/mla_query.h"
 #include "mla_device.cuh"
 #include "mla_internal.h"
-#include "../../include/mla_query.h"
 
 namespace mla {
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kStageRows = 16;
-constexpr int kPitch = kRowBytes + 64;            // 3136 B: conflict-free MMA loads
-constexpr int kStageBytes = kStageRows * kPitch;  // 50176 = 49 KiB (1 KiB aligned)
-constexpr int kUkPerStage = 3;                    // 3 x 16 KiB W_UK tiles per stage
-constexpr int kQsPitch = kNope + 8;               // BF16 elements per staged q row (MMA)
-constexpr long long kWaitLimit = 2000000000LL;    // ~1 s of SM clock
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;  // 256
+constexpr int kThreads = kConsumers + 32;        // + one producer warp
+constexpr int kPitch = kRowBytes + 64;           // 3136 B: conflict-free MMA loads
+constexpr long long kWaitLimit = 2000000000LL;   // ~1 s of SM clock
+
+// Named barriers (0 is __syncthreads).
+constexpr int kBarNorm = 1;       // warps 0-5: q_a RMSNorm
+constexpr int kBarInsert = 2;     // warps 6-7: KV insert
+constexpr int kBarConsumers = 3;  // warps 0-7
 
 enum StageKind { kNopeRows = 0, kRopeRows = 1, kUkTiles = 2 };
 
@@ -56,6 +60,17 @@ struct Work {
   int n0, n1;  // nope indices
   int c0, c1;  // combined items (per head: 8 W_UK units, then 64 rope rows)
 };
+
+template <bool MMA>
+struct Geo {
+  static constexpr int kStageRows = MMA ? 16 : 8;
+  static constexpr int kStageBytes = ((kStageRows * kPitch + 1023) / 1024) * 1024;
+  static constexpr int kUkPerStage = kStageBytes / kUkUnitBytes;  // 3 or 1
+};
+
+__device__ __forceinline__ void named_barrier(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 
 __device__ __forceinline__ int first_item(int64_t x) {
   const int64_t h = x / kItemBytesPerHead;
@@ -83,11 +98,13 @@ __device__ __forceinline__ Work cta_work(int i, int P, int H) {
   return w;
 }
 
+template <bool MMA>
 __device__ __forceinline__ bool next_stage(int& pn, int& pc, const Work& w, Stage& s) {
+  using G = Geo<MMA>;
   if (pn < w.n1) {
     s.kind = kNopeRows;
     s.first = pn;
-    s.count = min(kStageRows, w.n1 - pn);
+    s.count = min(G::kStageRows, w.n1 - pn);
     pn += s.count;
     return true;
   }
@@ -96,11 +113,11 @@ __device__ __forceinline__ bool next_stage(int& pn, int& pc, const Work& w, Stag
     if (l < kUkUnitsPerHead) {
       s.kind = kUkTiles;
       s.first = h * kUkUnitsPerHead + l;
-      s.count = min(min(kUkPerStage, kUkUnitsPerHead - l), w.c1 - pc);
+      s.count = min(min(G::kUkPerStage, kUkUnitsPerHead - l), w.c1 - pc);
     } else {
       s.kind = kRopeRows;
       s.first = h * kRope + (l - kUkUnitsPerHead);
-      s.count = min(min(kStageRows, kItemsPerHead - l), w.c1 - pc);
+      s.count = min(min(G::kStageRows, kItemsPerHead - l), w.c1 - pc);
     }
     pc += s.count;
     return true;
@@ -117,7 +134,7 @@ __device__ __forceinline__ int stage_row(const Stage& s, int j) {
   return (r / kRope) * kHeadRows + kNope + (r % kRope);
 }
 
-// Issue the copies of stage `s` into `buf` (called by all 32 lanes of warp 0).
+// Issue the copies of stage `s` into `buf` (all 32 lanes of the producer warp).
 __device__ __forceinline__ void issue_stage(const Stage& s, uint8_t* buf, uint64_t* bar,
                                             const DecodeArgs& a, const CUtensorMap* uk_map,
                                             int lane) {
@@ -138,10 +155,6 @@ __device__ __forceinline__ void issue_stage(const Stage& s, uint8_t* buf, uint64
       bulk_g2s(buf + lane * kPitch, a.w_qb + (int64_t)row * kQLora, kRowBytes, bar);
     }
   }
-}
-
-__device__ __forceinline__ void named_barrier(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // Paged FP8 KV insert of token b (page "mla.query", methods insert, kv_fp8,
@@ -169,9 +182,9 @@ __device__ void kv_insert(const DecodeArgs& a, int b, int lt, float* red2) {
   for (int i = 0; i < 8; ++i) ss = fmaf(x[i], x[i], ss);
   ss = warp_sum(ss);
   if (lane == 0) red2[w] = ss;
-  named_barrier(2, 64);
+  named_barrier(kBarInsert, 64);
   const float total = red2[0] + red2[1];
-  named_barrier(2, 64);  // red2 may be reused by the next token
+  named_barrier(kBarInsert, 64);  // red2 may be reused by the next token
   if (slot < 0) return;
   const int64_t page = slot / a.page_size, off = slot % a.page_size;
   if (page >= a.num_pages) {
@@ -223,19 +236,41 @@ __device__ void kv_insert(const DecodeArgs& a, int b, int lt, float* red2) {
   }
 }
 
+// Bounded wait of one lane until `ready` reaches `target`; false on timeout.
+__device__ __forceinline__ bool wait_ready(const uint32_t* ready, uint32_t target) {
+  if (ld_acquire_gpu(ready) >= target) return true;
+  const long long t0 = clock64();
+  while (ld_acquire_gpu(ready) < target) {
+    if (clock64() - t0 > kWaitLimit) return false;
+    __nanosleep(64);
+  }
+  return true;
+}
+
+// Publish `count` finished nope rows of head h.  Caller: one lane, after the
+// stores it covers (its own, or the CTA's behind a barrier); the fence is
+// cumulative, so those stores are visible GPU-wide before the counter moves.
+__device__ __forceinline__ void publish_rows(uint32_t* ready_g, int h, int count) {
+  __threadfence();
+  red_release_gpu_add(ready_g + h, (uint32_t)count);
+}
+
 template <int NT, bool MMA>
 struct Smem {
-  static constexpr int kStages = MMA ? 3 : 4;
-  static constexpr int kRing = kStages * kStageBytes;
+  using G = Geo<MMA>;
+  static constexpr int kStages = MMA ? (NT <= 8 ? 4 : 3) : 8;
+  static constexpr int kRing = kStages * G::kStageBytes;
   static constexpr int kXq = NT * kPitch;
-  static constexpr int kQs = MMA ? NT * kQsPitch * 2 : NT * kNope * 4;
-  static constexpr int kRed = MMA ? kWarps * kStageRows * NT * 4 : kUkPerStage * 32 * NT * 2 * 4;
+  // FMA: per-warp staged q of one head [warp][NT][128] FP32; MMA: split-K
+  // partial sums [warp][16 rows][NT] FP32.
+  static constexpr int kScratch =
+      MMA ? kConsumerWarps * 16 * NT * 4 : kConsumerWarps * NT * kNope * 4;
   static constexpr int oXq = kRing;
-  static constexpr int oQs = oXq + kXq;
-  static constexpr int oRed = oQs + kQs;
-  static constexpr int oSs = oRed + kRed;                      // [NT][8] floats + [2]
-  static constexpr int oBar = oSs + (NT * 8 + 8) * 4;
-  static constexpr int oFlag = oBar + kStages * 8;
+  static constexpr int oScratch = oXq + kXq;
+  static constexpr int oSs = oScratch + kScratch;  // [NT][8] + [8] floats
+  static constexpr int oFull = oSs + (NT * 8 + 8) * 4;
+  static constexpr int oEmpty = oFull + kStages * 8;
+  static constexpr int oFlag = oEmpty + kStages * 8;
   static constexpr int kBytes = oFlag + 16;
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1 KiB
 };
@@ -244,217 +279,232 @@ template <int NT, bool MMA>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_fused_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap uk_map) {
   using S = Smem<NT, MMA>;
+  using G = Geo<MMA>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* ring = smem;
   uint8_t* xq = smem + S::oXq;
-  float* red = reinterpret_cast<float*>(smem + S::oRed);
   float* ss_part = reinterpret_cast<float*>(smem + S::oSs);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::oBar);
-  int* flag = reinterpret_cast<int*>(smem + S::oFlag);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::oFull);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + S::oEmpty);
+  volatile int* flag = reinterpret_cast<volatile int*>(smem + S::oFlag);  // [1]: last CTA
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int P = gridDim.x, i = blockIdx.x, grp = blockIdx.y;
   const int H = a.heads;
   const Work w = cta_work(i, P, H);
+  const int tok0 = grp * NT;
+  uint16_t* qn_g = a.qn + (int64_t)grp * NT * H * kNope;
+  uint32_t* ready_g = a.ready + grp * H;
 
   if (tid == 0) {
-    for (int s = 0; s < S::kStages; ++s) mbar_init(&bars[s], 1);
+    for (int s = 0; s < S::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    flag[1] = 0;
     mbar_fence_init();
     prefetch_tensormap(&uk_map);
   }
   __syncthreads();
 
-  // Weights do not depend on the previous kernel: start streaming them now.
-  int prod_n = w.n0, prod_c = w.c0, issued = 0;
-  if (warp == 0) {
-    Stage st;
-    for (int s = 0; s < S::kStages && next_stage(prod_n, prod_c, w, st); ++s) {
-      issue_stage(st, ring + s * kStageBytes, &bars[s], a, &uk_map, lane);
-      ++issued;
-    }
-  }
-
-  pdl_wait();
-  pdl_launch_dependents();
-
-  // ---- q_a RMSNorm of this group's tokens -> xq (warps 0-5), and the ----
-  // ---- paged KV insert of this CTA's tokens (warps 6-7), concurrently ---
-  const int tok0 = grp * NT;
-  if (warp < 6) {
-    uint4 xv[NT];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      if (tok0 + t < a.batch)
-        xv[t] = *reinterpret_cast<const uint4*>(a.q_a + (int64_t)(tok0 + t) * a.q_a_stride +
-                                                8 * tid);
-      else
-        xv[t] = make_uint4(0, 0, 0, 0);
-    }
-    const uint4 gv = *reinterpret_cast<const uint4*>(a.gamma_q + 8 * tid);
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      const uint32_t ww[4] = {xv[t].x, xv[t].y, xv[t].z, xv[t].w};
-      float ss = 0.f;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        ss = fmaf(bf16lo(ww[k]), bf16lo(ww[k]), ss);
-        ss = fmaf(bf16hi(ww[k]), bf16hi(ww[k]), ss);
-      }
-      ss = warp_sum(ss);
-      if (lane == 0) ss_part[t * 8 + warp] = ss;
-    }
-    named_barrier(1, 192);
-    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      const float* sp = ss_part + t * 8;
-      const float total = ((((sp[0] + sp[1]) + sp[2]) + sp[3]) + sp[4]) + sp[5];
-      const float rr = __frsqrt_rn(__fadd_rn(__fdiv_rn(total, 1536.0f), a.eps));
-      const uint32_t ww[4] = {xv[t].x, xv[t].y, xv[t].z, xv[t].w};
-      uint4 o;
-      o.x = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[0]), rr), bf16lo(gw[0])),
-                        __fmul_rn(__fmul_rn(bf16hi(ww[0]), rr), bf16hi(gw[0])));
-      o.y = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[1]), rr), bf16lo(gw[1])),
-                        __fmul_rn(__fmul_rn(bf16hi(ww[1]), rr), bf16hi(gw[1])));
-      o.z = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[2]), rr), bf16lo(gw[2])),
-                        __fmul_rn(__fmul_rn(bf16hi(ww[2]), rr), bf16hi(gw[2])));
-      o.w = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[3]), rr), bf16lo(gw[3])),
-                        __fmul_rn(__fmul_rn(bf16hi(ww[3]), rr), bf16hi(gw[3])));
-      if (tok0 + t >= a.batch) o = make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(xq + t * kPitch + 16 * tid) = o;
-      // q_c rows (page "mla.query", method store_qc): CTA 0 of the group.
-      if (i == 0 && a.q_c != nullptr && tok0 + t < a.batch)
-        *reinterpret_cast<uint4*>(a.q_c + (int64_t)(tok0 + t) * kQLora + 8 * tid) = o;
-    }
-  } else {
-    // token t of the group is inserted by CTA t % P
-    for (int t = i; t < NT; t += P)
-      if (tok0 + t < a.batch) kv_insert(a, tok0 + t, tid - 192, ss_part + NT * 8);
-  }
-  __syncthreads();
-
-  // FMA flavour: this lane's x values in registers (k = 256 c + 8 lane + e).
-  float xr[MMA ? 1 : NT][MMA ? 1 : 48];
-  if constexpr (!MMA) {
-#pragma unroll
-    for (int t = 0; t < NT; ++t)
-#pragma unroll
-      for (int c = 0; c < 6; ++c) {
-        const uint4 v = *reinterpret_cast<const uint4*>(xq + t * kPitch + 2 * (256 * c + 8 * lane));
-        const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          xr[t][8 * c + 2 * k] = bf16lo(ww[k]);
-          xr[t][8 * c + 2 * k + 1] = bf16hi(ww[k]);
-        }
-      }
-  }
-
-  uint16_t* qn_g = a.qn + (int64_t)grp * NT * H * kNope;
-  uint32_t* ready_g = a.ready + grp * H;
   bool timed_out = false;
 
-  int cons_n = w.n0, cons_c = w.c0, stuck = -1;
-  Stage st;
-  for (int s = 0; next_stage(cons_n, cons_c, w, st); ++s) {
-    const int slot = s % S::kStages;
-    uint8_t* buf = ring + slot * kStageBytes;
-    const bool got = mbar_wait_bounded(&bars[slot], (uint32_t)((s / S::kStages) & 1), kWaitLimit);
-    if (__syncthreads_or(got ? 0 : 1)) {
-      // a copy never landed: stop consuming, drain what is in flight below
-      timed_out = true;
-      stuck = s;
-      break;
+  if (warp == kConsumerWarps) {
+    // ================= producer warp =================================
+    // Weights do not depend on the previous kernel: no PDL wait here.
+    int pn = w.n0, pc = w.c0, issued = 0;
+    Stage st;
+    while (next_stage<MMA>(pn, pc, w, st)) {
+      const int slot = issued % S::kStages;
+      if (issued >= S::kStages) {
+        const uint32_t par = (uint32_t)(((issued / S::kStages) - 1) & 1);
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait_bounded(&empty[slot], par, kWaitLimit) ? 1 : 0;
+        // On a timeout keep going (results are flagged invalid): every wait in
+        // this kernel is bounded, so it still ends; no warp leaves the stage
+        // sequence the others follow.
+        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) timed_out = true;
+      }
+      issue_stage(st, ring + slot * G::kStageBytes, &full[slot], a, &uk_map, lane);
+      ++issued;
+    }
+    // Every issued stage is consumed; after a timeout this bounded wait also
+    // covers copies that may still be landing before the CTA exits.
+    if (lane == 0) {
+      for (int s = max(0, issued - S::kStages); s < issued; ++s)
+        (void)mbar_wait_bounded(&full[s % S::kStages], (uint32_t)((s / S::kStages) & 1),
+                                kWaitLimit);
+    }
+  } else {
+    // ================= consumer warps 0-7 ============================
+    pdl_wait();
+    if (tid == 0) pdl_launch_dependents();
+
+    // ---- q_a RMSNorm -> xq (warps 0-5); KV insert (warps 6-7) -------
+    if (warp < 6) {
+      uint4 xv[NT];
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        if (tok0 + t < a.batch)
+          xv[t] = *reinterpret_cast<const uint4*>(a.q_a + (int64_t)(tok0 + t) * a.q_a_stride +
+                                                  8 * tid);
+        else
+          xv[t] = make_uint4(0, 0, 0, 0);
+      }
+      const uint4 gv = *reinterpret_cast<const uint4*>(a.gamma_q + 8 * tid);
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const uint32_t ww[4] = {xv[t].x, xv[t].y, xv[t].z, xv[t].w};
+        float ss = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          ss = fmaf(bf16lo(ww[k]), bf16lo(ww[k]), ss);
+          ss = fmaf(bf16hi(ww[k]), bf16hi(ww[k]), ss);
+        }
+        ss = warp_sum(ss);
+        if (lane == 0) ss_part[t * 8 + warp] = ss;
+      }
+      named_barrier(kBarNorm, 192);
+      const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const float* sp = ss_part + t * 8;
+        const float total = ((((sp[0] + sp[1]) + sp[2]) + sp[3]) + sp[4]) + sp[5];
+        const float rr = __frsqrt_rn(__fadd_rn(__fdiv_rn(total, 1536.0f), a.eps));
+        const uint32_t ww[4] = {xv[t].x, xv[t].y, xv[t].z, xv[t].w};
+        uint4 o;
+        o.x = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[0]), rr), bf16lo(gw[0])),
+                          __fmul_rn(__fmul_rn(bf16hi(ww[0]), rr), bf16hi(gw[0])));
+        o.y = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[1]), rr), bf16lo(gw[1])),
+                          __fmul_rn(__fmul_rn(bf16hi(ww[1]), rr), bf16hi(gw[1])));
+        o.z = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[2]), rr), bf16lo(gw[2])),
+                          __fmul_rn(__fmul_rn(bf16hi(ww[2]), rr), bf16hi(gw[2])));
+        o.w = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[3]), rr), bf16lo(gw[3])),
+                          __fmul_rn(__fmul_rn(bf16hi(ww[3]), rr), bf16hi(gw[3])));
+        if (tok0 + t >= a.batch) o = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(xq + t * kPitch + 16 * tid) = o;
+        // q_c rows (page "mla.query", method store_qc): CTA 0 of the group.
+        if (i == 0 && a.q_c != nullptr && tok0 + t < a.batch)
+          *reinterpret_cast<uint4*>(a.q_c + (int64_t)(tok0 + t) * kQLora + 8 * tid) = o;
+      }
+    } else {
+      // token t of the group is inserted by CTA t % P
+      for (int t = i; t < NT; t += P)
+        if (tok0 + t < a.batch) kv_insert(a, tok0 + t, tid - 192, ss_part + NT * 8);
+    }
+    named_barrier(kBarConsumers, kConsumers);
+
+    // FMA flavour: this lane's x values in registers (k = 256 c + 8 lane + e).
+    float xr[MMA ? 1 : NT][MMA ? 1 : 48];
+    if constexpr (!MMA) {
+#pragma unroll
+      for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int c = 0; c < 6; ++c) {
+          const uint4 v =
+              *reinterpret_cast<const uint4*>(xq + t * kPitch + 2 * (256 * c + 8 * lane));
+          const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            xr[t][8 * c + 2 * k] = bf16lo(ww[k]);
+            xr[t][8 * c + 2 * k + 1] = bf16hi(ww[k]);
+          }
+        }
     }
 
-    if (st.kind == kUkTiles) {
-      // ---- absorption of one head's nope q through 1-3 W_UK tiles -------
-      const int h = st.first / kUkUnitsPerHead;
-      const int cb0 = st.first % kUkUnitsPerHead;
-      if (tid == 0) {
-        const long long t0 = clock64();
-        while (ld_acquire_gpu(ready_g + h) < (uint32_t)kNope) {
-          if (clock64() - t0 > kWaitLimit) {
-            timed_out = true;
-            break;
-          }
-          __nanosleep(64);
-        }
-      }
-      __syncthreads();
-      const uint16_t* src = qn_g + (int64_t)h * kNope;  // + t*H*128
-      if constexpr (MMA) {
-        uint16_t* qs = reinterpret_cast<uint16_t*>(smem + S::oQs);
-        for (int e = tid; e < NT * (kNope / 2); e += kThreads) {
-          const int t = e / (kNope / 2), c2 = e % (kNope / 2);
-          const uint32_t v = __ldcg(reinterpret_cast<const unsigned int*>(
-              src + (int64_t)t * H * kNope + 2 * c2));
-          *reinterpret_cast<uint32_t*>(qs + t * kQsPitch + 2 * c2) = v;
-        }
-      } else {
-        float* qs = reinterpret_cast<float*>(smem + S::oQs);
-        for (int e = tid; e < NT * (kNope / 2); e += kThreads) {
-          const int t = e / (kNope / 2), c2 = e % (kNope / 2);
-          const uint32_t v = __ldcg(reinterpret_cast<const unsigned int*>(
-              src + (int64_t)t * H * kNope + 2 * c2));
-          qs[t * kNope + 2 * c2] = bf16lo(v);
-          qs[t * kNope + 2 * c2 + 1] = bf16hi(v);
-        }
-      }
-      __syncthreads();
+    // Nope rows finished but not yet published, for head pub_h (FMA: kept by
+    // lane 0 of each warp for its own rows; MMA: by thread 0 for the CTA).
+    int pub_h = -1, pub_n = 0;
 
-      if constexpr (MMA) {
-        const uint16_t* qs = reinterpret_cast<const uint16_t*>(smem + S::oQs);
-        const int g = lane >> 2, q = lane & 3;
-        for (int pair = warp; pair < 4 * st.count; pair += kWarps) {
-          const int u = pair >> 2, mt = pair & 3;
-          const uint32_t tile = smem_u32(buf + u * kUkUnitBytes);
-          float acc[NT / 8][4];
+    int cn = w.n0, cc = w.c0;
+    Stage st;
+    for (int s = 0; next_stage<MMA>(cn, cc, w, st); ++s) {
+      const int slot = s % S::kStages;
+      uint8_t* buf = ring + slot * G::kStageBytes;
+      if (!mbar_wait_bounded(&full[slot], (uint32_t)((s / S::kStages) & 1), kWaitLimit))
+        timed_out = true;  // keep the stage sequence; the call is flagged invalid
+      if (st.kind != kNopeRows && pub_h >= 0) {
+        // the nope phase is over: publish what is left
+        publish_rows(ready_g, pub_h, pub_n);
+        pub_h = -1;
+      }
+
+      if (st.kind == kUkTiles) {
+        // ---- absorption of one head's nope q through W_UK tiles -------
+        const int h = st.first / kUkUnitsPerHead;
+        const int cb0 = st.first % kUkUnitsPerHead;
+        int rdy = 1;
+        if (lane == 0) rdy = wait_ready(ready_g + h, (uint32_t)kNope) ? 1 : 0;
+        rdy = __shfl_sync(0xFFFFFFFFu, rdy, 0);
+        if (!rdy) timed_out = true;
+        const uint16_t* qsrc = qn_g + (int64_t)h * kNope;  // token t at + t*H*128
+        if constexpr (MMA) {
+          const int g = lane >> 2, q = lane & 3;
+          // B fragments (q^T, 8 tokens per n-tile) straight from L2.
+          uint32_t bf[NT / 8][kNope / 16][2];
 #pragma unroll
-          for (int nt = 0; nt < NT / 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+          for (int nt = 0; nt < NT / 8; ++nt)
 #pragma unroll
-          for (int ks = 0; ks < kNope / 16; ++ks) {
-            const int m = lane >> 3;
-            const int p = 16 * ks + (lane & 7) + 8 * (m >> 1);
-            const int chunk = 2 * mt + (m & 1);
-            uint32_t af[4];
-            ldmatrix_x4_trans(af, tile + p * 128 + ((chunk ^ (p & 7)) << 4));
+            for (int ks = 0; ks < kNope / 16; ++ks) {
+              const uint16_t* qr = qsrc + (int64_t)(8 * nt + g) * H * kNope + 16 * ks + 2 * q;
+              bf[nt][ks][0] = __ldcg(reinterpret_cast<const unsigned int*>(qr));
+              bf[nt][ks][1] = __ldcg(reinterpret_cast<const unsigned int*>(qr + 8));
+            }
+          for (int pair = warp; pair < 4 * st.count; pair += kConsumerWarps) {
+            const int u = pair >> 2, mt = pair & 3;
+            const uint32_t tile = smem_u32(buf + u * kUkUnitBytes);
+            float acc[NT / 8][4];
+#pragma unroll
+            for (int nt = 0; nt < NT / 8; ++nt)
+              acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < kNope / 16; ++ks) {
+              const int m = lane >> 3;
+              const int p = 16 * ks + (lane & 7) + 8 * (m >> 1);
+              const int chunk = 2 * mt + (m & 1);
+              uint32_t af[4];
+              ldmatrix_x4_trans(af, tile + p * 128 + ((chunk ^ (p & 7)) << 4));
+#pragma unroll
+              for (int nt = 0; nt < NT / 8; ++nt)
+                mma_bf16_16816(acc[nt], af[0], af[1], af[2], af[3], bf[nt][ks][0], bf[nt][ks][1]);
+            }
+            const int cbase = (cb0 + u) * kUkCols + 16 * mt + g;
 #pragma unroll
             for (int nt = 0; nt < NT / 8; ++nt) {
-              const uint16_t* qr = qs + (8 * nt + g) * kQsPitch + 16 * ks + 2 * q;
-              const uint32_t b0 = *reinterpret_cast<const uint32_t*>(qr);
-              const uint32_t b1 = *reinterpret_cast<const uint32_t*>(qr + 8);
-              mma_bf16_16816(acc[nt], af[0], af[1], af[2], af[3], b0, b1);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int t = 8 * nt + 2 * q + (e & 1);
+                const int c = cbase + 8 * (e >> 1);
+                if (tok0 + t < a.batch)
+                  a.q_latent[((int64_t)(tok0 + t) * H + h) * kKvLora + c] = f2bf_bits(acc[nt][e]);
+              }
             }
           }
-          const int cbase = (cb0 + u) * kUkCols + 16 * mt + g;
+        } else {
+          // One W_UK unit (64 columns); warp w owns columns 8w..8w+7.  Lane:
+          // column pair cp = lane & 3, rows p = pg + 8 k (pg = lane >> 2).
+          float* qs = reinterpret_cast<float*>(smem + S::oScratch) + warp * NT * kNope;
 #pragma unroll
-          for (int nt = 0; nt < NT / 8; ++nt) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int t = 8 * nt + 2 * q + (e & 1);
-              const int c = cbase + 8 * (e >> 1);
-              if (tok0 + t < a.batch)
-                a.q_latent[((int64_t)(tok0 + t) * H + h) * kKvLora + c] = f2bf_bits(acc[nt][e]);
-            }
+          for (int t = 0; t < NT; ++t) {
+            const uint2 v =
+                __ldcg(reinterpret_cast<const uint2*>(qsrc + (int64_t)t * H * kNope + 4 * lane));
+            qs[t * kNope + 4 * lane] = bf16lo(v.x);
+            qs[t * kNope + 4 * lane + 1] = bf16hi(v.x);
+            qs[t * kNope + 4 * lane + 2] = bf16lo(v.y);
+            qs[t * kNope + 4 * lane + 3] = bf16hi(v.y);
           }
-        }
-      } else {
-        const float* qs = reinterpret_cast<const float*>(smem + S::oQs);
-        const int u = tid >> 6, cp = tid & 31, ph = (tid >> 5) & 1;
-        float acc[NT][2];
+          __syncwarp();
+          const int cp = lane & 3, pg = lane >> 2;
+          float acc[NT][2];
 #pragma unroll
-        for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = 0.f;
-        const bool active = u < st.count;
-        if (active) {
-          const uint8_t* tile = buf + u * kUkUnitBytes;
-#pragma unroll 8
-          for (int pp = 0; pp < 64; ++pp) {
-            const int p = 64 * ph + pp;
+          for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = 0.f;
+#pragma unroll
+          for (int k = 0; k < kNope / 8; ++k) {
+            const int p = pg + 8 * k;
             const uint32_t wv = *reinterpret_cast<const uint32_t*>(
-                tile + p * 128 + ((((cp >> 2) ^ (p & 7))) << 4) + (cp & 3) * 4);
+                buf + p * 128 + ((warp ^ (p & 7)) << 4) + 4 * cp);
             const float w0 = bf16lo(wv), w1 = bf16hi(wv);
 #pragma unroll
             for (int t = 0; t < NT; ++t) {
@@ -462,31 +512,29 @@ __global__ void __launch_bounds__(kThreads, 1)
               acc[t][1] = fmaf(qs[t * kNope + p], w1, acc[t][1]);
             }
           }
-          if (ph == 1) {
 #pragma unroll
-            for (int t = 0; t < NT; ++t) {
-              red[((u * 32 + cp) * NT + t) * 2] = acc[t][0];
-              red[((u * 32 + cp) * NT + t) * 2 + 1] = acc[t][1];
+          for (int t = 0; t < NT; ++t)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              float v = acc[t][e];
+              v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
+              v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
+              v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
+              acc[t][e] = v;
             }
+          if (pg == 0) {
+            const int c = cb0 * kUkCols + 8 * warp + 2 * cp;
+#pragma unroll
+            for (int t = 0; t < NT; ++t)
+              if (tok0 + t < a.batch)
+                *reinterpret_cast<uint32_t*>(a.q_latent +
+                                             ((int64_t)(tok0 + t) * H + h) * kKvLora + c) =
+                    pack_bf16x2(acc[t][0], acc[t][1]);
           }
         }
-        __syncthreads();
-        if (active && ph == 0) {
-          const int c = (cb0 + u) * kUkCols + 2 * cp;
-#pragma unroll
-          for (int t = 0; t < NT; ++t) {
-            if (tok0 + t < a.batch) {
-              const float v0 = acc[t][0] + red[((u * 32 + cp) * NT + t) * 2];
-              const float v1 = acc[t][1] + red[((u * 32 + cp) * NT + t) * 2 + 1];
-              *reinterpret_cast<uint32_t*>(a.q_latent + ((int64_t)(tok0 + t) * H + h) * kKvLora +
-                                           c) = pack_bf16x2(v0, v1);
-            }
-          }
-        }
-      }
-    } else {
-      // ---- Q_B rows (nope or rope) -------------------------------------
-      if constexpr (MMA) {
+      } else if constexpr (MMA) {
+        // ---- Q_B rows, tensor cores, K split over the warps ----------
+        float* red = reinterpret_cast<float*>(smem + S::oScratch);
         const int g = lane >> 2, q = lane & 3;
         float acc[NT / 8][4];
 #pragma unroll
@@ -503,21 +551,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_bf16_16816(acc[nt], alo.z, ahi.z, alo.w, ahi.w, bx.z, bx.w);
           }
         }
+        // the weight slot is no longer read: release it to the producer
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        float* rw = red + warp * 16 * NT;
 #pragma unroll
         for (int nt = 0; nt < NT / 8; ++nt) {
-          float* rw = red + warp * kStageRows * NT;
           rw[g * NT + 8 * nt + 2 * q] = acc[nt][0];
           rw[g * NT + 8 * nt + 2 * q + 1] = acc[nt][1];
           rw[(g + 8) * NT + 8 * nt + 2 * q] = acc[nt][2];
           rw[(g + 8) * NT + 8 * nt + 2 * q + 1] = acc[nt][3];
         }
-        __syncthreads();
-        for (int e = tid; e < kStageRows * NT; e += kThreads) {
+        named_barrier(kBarConsumers, kConsumers);
+        for (int e = tid; e < 16 * NT; e += kConsumers) {
           const int j = e / NT, t = e % NT;
           if (j >= st.count) continue;
           float v = 0.f;
 #pragma unroll
-          for (int ww = 0; ww < kWarps; ++ww) v += red[ww * kStageRows * NT + e];
+          for (int ww = 0; ww < kConsumerWarps; ++ww) v += red[ww * 16 * NT + e];
           const uint16_t bits = f2bf_bits(v);
           if (st.kind == kNopeRows) {
             const int n = st.first + j;
@@ -527,11 +578,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             a.q_pe[((int64_t)(tok0 + t) * H + r / kRope) * kRope + r % kRope] = bits;
           }
         }
+        named_barrier(kBarConsumers, kConsumers);  // q stores done, red free
+        if (st.kind == kNopeRows && tid == 0) {
+          // count the CTA's finished rows per head; publish a head once the
+          // CTA has no more rows of it
+          for (int j = 0; j < st.count;) {
+            const int h = (st.first + j) / kNope;
+            const int upto = min(st.count, (h + 1) * kNope - st.first);
+            if (pub_h != h) {
+              if (pub_h >= 0) publish_rows(ready_g, pub_h, pub_n);
+              pub_h = h;
+              pub_n = 0;
+            }
+            pub_n += upto - j;
+            j = upto;
+          }
+          if (cn >= w.n1 || (pub_h + 1) * kNope <= cn) {
+            publish_rows(ready_g, pub_h, pub_n);
+            pub_h = -1;
+            pub_n = 0;
+          }
+        }
+        continue;  // slot already released
       } else {
-#pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-          const int j = warp + kWarps * rr;
-          if (j >= st.count) break;
+        // ---- Q_B rows, FP32 FMA: warp w owns row w of the stage ---------
+        const int j = warp;
+        if (j < st.count) {
           const uint8_t* rowp = buf + j * kPitch;
           float acc[NT][2];
 #pragma unroll
@@ -550,63 +622,53 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[slot]);
+          float v[NT];
 #pragma unroll
-          for (int t = 0; t < NT; ++t) {
-            const float v = warp_sum(acc[t][0] + acc[t][1]);
-            if (lane == 0) {
-              const uint16_t bits = f2bf_bits(v);
-              if (st.kind == kNopeRows) {
-                const int n = st.first + j;
-                qn_g[((int64_t)t * H + n / kNope) * kNope + n % kNope] = bits;
-              } else if (tok0 + t < a.batch) {
-                const int r = st.first + j;
-                a.q_pe[((int64_t)(tok0 + t) * H + r / kRope) * kRope + r % kRope] = bits;
+          for (int t = 0; t < NT; ++t) v[t] = warp_sum(acc[t][0] + acc[t][1]);
+          if (lane == 0) {
+            if (st.kind == kNopeRows) {
+              const int n = st.first + j;
+              const int h = n / kNope;
+#pragma unroll
+              for (int t = 0; t < NT; ++t)
+                qn_g[((int64_t)t * H + h) * kNope + n % kNope] = f2bf_bits(v[t]);
+              if (pub_h != h) {
+                if (pub_h >= 0) publish_rows(ready_g, pub_h, pub_n);
+                pub_h = h;
+                pub_n = 0;
               }
+              ++pub_n;
+            } else {
+              const int r = st.first + j;
+#pragma unroll
+              for (int t = 0; t < NT; ++t)
+                if (tok0 + t < a.batch)
+                  a.q_pe[((int64_t)(tok0 + t) * H + r / kRope) * kRope + r % kRope] =
+                      f2bf_bits(v[t]);
             }
           }
+          continue;  // slot already released
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
     }
-
-    __syncthreads();  // stage buffer and smem scratch free again
-    if (st.kind == kNopeRows && tid == 0) {
-      // Publish the finished nope rows, per head.  The CTA barrier above
-      // orders every thread's q stores before this thread's fence, and the
-      // fence (cumulative) makes them visible GPU-wide before the counter.
-      __threadfence();
-      int j = 0;
-      while (j < st.count) {
-        const int h = (st.first + j) / kNope;
-        const int upto = min(st.count, (h + 1) * kNope - st.first);
-        red_release_gpu_add(ready_g + h, (uint32_t)(upto - j));
-        j = upto;
-      }
-    }
-    if (warp == 0) {
-      Stage nx;
-      if (next_stage(prod_n, prod_c, w, nx)) {
-        issue_stage(nx, buf, &bars[slot], a, &uk_map, lane);
-        ++issued;
-      }
-    }
+    if (pub_h >= 0) publish_rows(ready_g, pub_h, pub_n);
   }
 
   // ---- end of call: flags, and the last CTA re-arms the counters ------
-  if (stuck >= 0 && tid == 0) {
-    // bounded second wait for the copies this CTA still has in flight
-    for (int s = stuck; s < issued; ++s)
-      (void)mbar_wait_bounded(&bars[s % S::kStages], (uint32_t)((s / S::kStages) & 1), kWaitLimit);
-  }
   if (timed_out) atomicOr(a.err, MLA_DEVERR_TIMEOUT);
   __syncthreads();
   if (tid == 0) {
     __threadfence();
     const uint32_t total = gridDim.x * gridDim.y;
     const uint32_t prev = atomicAdd(a.finished, 1u);
-    *flag = (prev == total - 1) ? 1 : 0;
+    flag[1] = (prev == total - 1) ? 1 : 0;
   }
   __syncthreads();
-  if (*flag) {
+  if (flag[1]) {
     for (int e = tid; e < a.groups * H; e += kThreads) a.ready[e] = 0u;
     __syncthreads();
     if (tid == 0) {
@@ -614,7 +676,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       __threadfence();
     }
   }
-  (void)issued;
 }
 
 template <int NT, bool MMA>
