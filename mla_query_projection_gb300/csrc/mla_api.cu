@@ -23,6 +23,7 @@ struct mla_query {
   uint32_t* finished;
   uint32_t* ready;
   uint16_t* qn;
+  uint64_t* trace;  // MLA_TRACE builds: per-CTA timeline stamps
 };
 
 namespace {
@@ -130,6 +131,13 @@ int mla_query_create(mla_query_t* out, int num_heads, const void* w_qb, const vo
     h->ready = reinterpret_cast<uint32_t*>(base + head);
     h->qn = reinterpret_cast<uint16_t*>(base + qn_off);
   }
+#ifdef MLA_TRACE
+  {
+    const size_t tb = (size_t)h->num_sms * mla::kTraceSlots * 8;
+    if (cudaMalloc(&h->trace, tb) != cudaSuccess || cudaMemset(h->trace, 0, tb) != cudaSuccess)
+      goto fail;
+  }
+#endif
   *out = h;
   return MLA_OK;
 fail:
@@ -196,6 +204,7 @@ int mla_query_decode(mla_query_t h, int batch, const void* q_a, int64_t q_a_stri
   a.batch = batch;
   a.groups = (batch + nt - 1) / nt;
   a.eps = h->eps;
+  a.trace = h->trace;
   if (a.groups > h->num_sms) return MLA_EUNSUPPORTED;
 
   cudaError_t e =
@@ -237,8 +246,19 @@ int mla_query_path_for(mla_query_t h, int batch) {
   return mma ? MLA_PATH_MMA : MLA_PATH_FMA;
 }
 
+#ifdef MLA_TRACE
+// Timeline readout of trace builds: copies the per-CTA stamps to `host` and
+// clears them for the next call.
+MLA_API int mla_query_trace_read(mla_query_t h, void* host, size_t bytes) {
+  if (h == nullptr || h->trace == nullptr) return MLA_EINVAL;
+  if (cudaMemcpy(host, h->trace, bytes, cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ECUDA;
+  return cudaMemset(h->trace, 0, bytes) == cudaSuccess ? MLA_OK : MLA_ECUDA;
+}
+#endif
+
 void mla_query_destroy(mla_query_t h) {
   if (h == nullptr) return;
+  if (h->trace) cudaFree(h->trace);
   if (h->scratch) cudaFree(h->scratch);
   free(h);
 }

@@ -236,6 +236,24 @@ __device__ void kv_insert(const DecodeArgs& a, int b, int lt, float* red2) {
   }
 }
 
+// Timeline stamps (MLA_TRACE builds): slot 0 start, 1 producer ring filled,
+// 2 consumer prologue done, 3 first W_UK wait start, 4 its end, 5 end of the
+// nope phase, 6 last stage consumed, 7 end, 8.. the time each stage's data
+// was seen by consumer thread 0.
+__device__ __forceinline__ void trace_stamp(const DecodeArgs& a, int slot) {
+#ifdef MLA_TRACE
+  if (a.trace != nullptr && slot < kTraceSlots) {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    uint64_t* p = a.trace + (int64_t)(blockIdx.y * gridDim.x + blockIdx.x) * kTraceSlots + slot;
+    if (*p == 0) *p = t;
+  }
+#else
+  (void)a;
+  (void)slot;
+#endif
+}
+
 // Bounded wait of one lane until `ready` reaches `target`; false on timeout.
 __device__ __forceinline__ bool wait_ready(const uint32_t* ready, uint32_t target) {
   if (ld_acquire_gpu(ready) >= target) return true;
@@ -306,6 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     flag[1] = 0;
     mbar_fence_init();
     prefetch_tensormap(&uk_map);
+    trace_stamp(a, 0);
   }
   __syncthreads();
 
@@ -329,6 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       issue_stage(st, ring + slot * G::kStageBytes, &full[slot], a, &uk_map, lane);
       ++issued;
+      if (issued == S::kStages && lane == 0) trace_stamp(a, 1);
     }
     // Every issued stage is consumed; after a timeout this bounded wait also
     // covers copies that may still be landing before the CTA exits.
@@ -395,6 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tok0 + t < a.batch) kv_insert(a, tok0 + t, tid - 192, ss_part + NT * 8);
     }
     named_barrier(kBarConsumers, kConsumers);
+    if (tid == 0) trace_stamp(a, 2);
 
     // FMA flavour: this lane's x values in registers (k = 256 c + 8 lane + e).
     float xr[MMA ? 1 : NT][MMA ? 1 : 48];
@@ -425,6 +446,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* buf = ring + slot * G::kStageBytes;
       if (!mbar_wait_bounded(&full[slot], (uint32_t)((s / S::kStages) & 1), kWaitLimit))
         timed_out = true;  // keep the stage sequence; the call is flagged invalid
+      if (tid == 0) {
+        trace_stamp(a, 8 + s);
+        if (st.kind != kNopeRows) trace_stamp(a, 5);
+      }
       if (st.kind != kNopeRows && pub_h >= 0) {
         // the nope phase is over: publish what is left
         publish_rows(ready_g, pub_h, pub_n);
@@ -436,7 +461,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = st.first / kUkUnitsPerHead;
         const int cb0 = st.first % kUkUnitsPerHead;
         int rdy = 1;
+        if (tid == 0) trace_stamp(a, 3);
         if (lane == 0) rdy = wait_ready(ready_g + h, (uint32_t)kNope) ? 1 : 0;
+        if (tid == 0) trace_stamp(a, 4);
         rdy = __shfl_sync(0xFFFFFFFFu, rdy, 0);
         if (!rdy) timed_out = true;
         const uint16_t* qsrc = qn_g + (int64_t)h * kNope;  // token t at + t*H*128
@@ -656,6 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&empty[slot]);
     }
     if (pub_h >= 0) publish_rows(ready_g, pub_h, pub_n);
+    if (tid == 0) trace_stamp(a, 6);
   }
 
   // ---- end of call: flags, and the last CTA re-arms the counters ------
@@ -667,6 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t prev = atomicAdd(a.finished, 1u);
     flag[1] = (prev == total - 1) ? 1 : 0;
   }
+  if (tid == 0) trace_stamp(a, 7);
   __syncthreads();
   if (flag[1]) {
     for (int e = tid; e < a.groups * H; e += kThreads) a.ready[e] = 0u;

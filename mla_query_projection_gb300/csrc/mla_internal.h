@@ -55,7 +55,12 @@ struct DecodeArgs {
   int batch;
   int groups;                // token groups (grid.y)
   float eps;
+  // Timeline records (builds with MLA_TRACE only; null otherwise):
+  // per CTA kTraceSlots globaltimer stamps, see mla_fused.cu.
+  uint64_t* trace;
 };
+
+constexpr int kTraceSlots = 64;
 
 // Scratch sizes for `heads` heads at the largest batch.
 size_t scratch_qn_elems(int heads);

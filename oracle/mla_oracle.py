@@ -55,6 +55,12 @@ ROW_BYTES_DS = DS_ROPE + 2 * QK_ROPE  # 656
 
 E4M3_MAX = 448.0
 
+# Relative width of the rounding tie zone of the normalised q_a row: a bound on
+# the FP32 evaluation error of x * rr * gamma (a sum of squares over 8 + 5 + 6
+# additions, one division, one add, one reciprocal square root, two products:
+# under 20 roundings of 2**-24 each).
+XQ_TIE_REL = 2.0**-20
+
 LAYOUT_E4M3 = 0
 LAYOUT_DS_MLA = 1
 
@@ -87,6 +93,33 @@ def round_to_bf16(x) -> np.ndarray:
     r = np.ldexp(np.rint(np.ldexp(x, -q_exp)), q_exp)
     bf16_max = (2.0 - 2.0**-7) * 2.0**127
     return np.where(np.abs(r) > bf16_max, np.copysign(np.inf, x), r)
+
+
+def bf16_quantum(x) -> np.ndarray:
+    """Spacing of the bfloat16 values around each float64 value (2**(e-8),
+    2**-133 below the normal range)."""
+    _, e = np.frexp(np.asarray(x, dtype=np.float64))
+    return np.ldexp(1.0, np.maximum(e - 8, -133))
+
+
+def bf16_midpoint_distance(x) -> np.ndarray:
+    """Distance from each value to the nearest midpoint between two adjacent
+    bfloat16 values (0 at a tie of round-to-nearest)."""
+    x = np.asarray(x, dtype=np.float64)
+    q = bf16_quantum(x)
+    frac = np.abs(x) / q - np.floor(np.abs(x) / q)
+    return np.abs(frac - 0.5) * q
+
+
+def bf16_other_rounding(x) -> np.ndarray:
+    """The bfloat16 neighbour of each value that round-to-nearest does not
+    pick (the other side of the value; equal to x when x is representable)."""
+    x = np.asarray(x, dtype=np.float64)
+    q = bf16_quantum(x)
+    lo = np.floor(x / q) * q
+    hi = np.ceil(x / q) * q
+    r = round_to_bf16(x)
+    return np.where(r == hi, lo, hi)
 
 
 def f64_to_bf16_bits(x) -> np.ndarray:
@@ -253,7 +286,7 @@ def slot_to_page(slot, page_size):
     return int(slot) // int(page_size), int(slot) % int(page_size)
 
 
-def decode_step(inp):
+def decode_step(inp, xq_alt=None):
     """One decode step of the whole path.
 
     ``inp`` is a dict with BF16 bit arrays ``w_qb [H*192, 1536]``,
@@ -265,7 +298,15 @@ def decode_step(inp):
     Returns a dict: BF16 bits ``q_c [B, 1536]``, ``q_pe [B, H, 64]``,
     ``q_latent [B, H, 512]``; the updated ``cache``; float64 exact
     pre-rounding values and |term| sums for tolerance floors; ``bad_slots``
-    (slots at or beyond the cache capacity, skipped)."""
+    (slots at or beyond the cache capacity, skipped).
+
+    ``xq_alt`` (bool [B, 1536], optional) selects, for the marked elements of
+    the normalised q_a row, the other correct BF16 rounding: an element whose
+    exact value lies at a rounding midpoint to within the FP32 evaluation
+    error has two correct roundings (FP32 arithmetic, as the page computes it,
+    may land on either side).  Marked elements must lie within XQ_TIE_REL of
+    their value from a midpoint; the rest of the step follows from the chosen
+    rounding."""
     H = inp["w_uk"].shape[0]
     eps = float(np.float32(inp["eps"]))
     w_qb = bf16_bits_to_f64(inp["w_qb"])
@@ -278,7 +319,14 @@ def decode_step(inp):
     k_pe = bf16_bits_to_f64(k_pe_bits)
 
     # q_a RMSNorm, one BF16 rounding; the rounded row is q_c and the GEMM input.
-    xq = round_to_bf16(rmsnorm(q_a, g_q, eps))
+    xq_exact = rmsnorm(q_a, g_q, eps)
+    xq = round_to_bf16(xq_exact)
+    if xq_alt is not None:
+        xq_alt = np.asarray(xq_alt, dtype=bool)
+        near = bf16_midpoint_distance(xq_exact) <= XQ_TIE_REL * np.abs(xq_exact)
+        if np.any(xq_alt & ~near):
+            raise ValueError("xq_alt marks an element outside the rounding tie zone")
+        xq = np.where(xq_alt, bf16_other_rounding(xq_exact), xq)
     # Q_B projection, one BF16 rounding per output.
     q_exact, q_cond = q_projection(xq, w_qb, H)
     q = round_to_bf16(q_exact)
@@ -320,7 +368,7 @@ def decode_step(inp):
         "q_cond": q_cond,
         "lat_exact": lat_exact,
         "lat_cond": lat_cond,
-        "xq_exact": rmsnorm(q_a, g_q, eps),
+        "xq_exact": xq_exact,
         "kv_normed": normed,
         "ds_scales": ds_scales,
         "bad_slots": bad,

@@ -18,6 +18,20 @@ terms of the dot product that produced the output (K terms):
     (codes compared as signed ordinals, so +0 and -0 are equal).
   * fp8_ds_mla power-of-two scales, k_pe bytes, slot/page placement and every
     cache byte outside the written rows: bit-exact.
+
+Rounding ties.  The path rounds FP32 intermediates to BF16 where the page
+does (the normalised q_a row, the Q_B outputs).  When an exact value lies at a
+rounding midpoint to within the FP32 evaluation error, both neighbours are
+correct results, and the choice moves everything downstream of it:
+  * q_c: every element must equal the oracle's rounding, or lie in the tie
+    zone (within 2**-20 of its value from a midpoint) and take the other
+    rounding; the oracle then computes the rest of the step for the rounding
+    the GPU took (``reference_for``).  Observed on GB300: q_c element -0.95117186
+    (1.5e-8 from the midpoint) rounded the other way moved ~6% of that token's
+    q_latent outputs by more than one ulp.
+  * q_latent: Q_B outputs whose exact value lies within 2**-22 * S of a
+    midpoint may round either way; each such q value widens the tolerance of
+    the outputs it feeds by one BF16 quantum of q times |W_UK[h, p, c]|.
 """
 
 from __future__ import annotations
@@ -32,7 +46,38 @@ FRAC_WITHIN_ULP = 0.999
 FRAC_FP8_EXACT = 0.999
 
 
-def check_bf16(name, got_bits, ref_bits, cond=None, k_terms=0, report=None):
+Q_TIE_REL_S = 2.0**-22
+
+
+def reference_for(inp, gpu_q_c=None):
+    """The oracle's step for the inputs; if the GPU's q_c takes the other
+    correct rounding of tie-zone elements, the oracle's step for that rounding."""
+    ref = O.decode_step(inp)
+    if gpu_q_c is None:
+        return ref
+    mism = np.asarray(gpu_q_c) != ref["q_c"]
+    if not mism.any():
+        return ref
+    near = O.bf16_midpoint_distance(ref["xq_exact"]) <= O.XQ_TIE_REL * np.abs(ref["xq_exact"])
+    bad = mism & ~near
+    assert not bad.any(), f"q_c differs outside the rounding tie zone at {np.argwhere(bad)[:5]}"
+    alt = O.decode_step(inp, xq_alt=mism)
+    assert np.array_equal(alt["q_c"], gpu_q_c), "q_c is neither rounding of a tie-zone element"
+    return alt
+
+
+def latent_slack(ref, inp):
+    """Tolerance added to q_latent for Q_B outputs whose rounding may go
+    either way (see the module docstring)."""
+    q_exact = ref["q_exact"][:, :, :128]
+    cond = ref["q_cond"][:, :, :128]
+    amb = O.bf16_midpoint_distance(q_exact) <= Q_TIE_REL_S * cond
+    step = np.where(amb, O.bf16_quantum(q_exact), 0.0)
+    w_uk = np.abs(O.bf16_bits_to_f64(inp["w_uk"]))
+    return np.einsum("bhp,hpc->bhc", step, w_uk)
+
+
+def check_bf16(name, got_bits, ref_bits, cond=None, k_terms=0, report=None, slack=None):
     g = O.bf16_bits_to_f64(got_bits)
     r = O.bf16_bits_to_f64(ref_bits)
     assert g.shape == r.shape, (name, g.shape, r.shape)
@@ -40,11 +85,13 @@ def check_bf16(name, got_bits, ref_bits, cond=None, k_terms=0, report=None):
     err = np.abs(g - r)
     if cond is None:
         cond = np.zeros_like(r)
-    tol = ULP_REL * np.abs(r) + k_terms * 2.0**-24 * cond
+    if slack is None:
+        slack = 0.0
+    tol = ULP_REL * np.abs(r) + k_terms * 2.0**-24 * cond + slack
     within = err <= tol
     denom = np.maximum(np.abs(r), cond)
     denom = np.where(denom == 0, 1.0, denom)
-    rel = err / denom
+    rel = np.maximum(err - slack, 0.0) / denom
     frac = float(np.mean(within)) if within.size else 1.0
     if report is not None:
         report[name] = dict(
@@ -95,6 +142,24 @@ def check_step(gpu: dict, ref: dict, inp: dict, report=None, q_c=True):
     check_bf16("q_pe", gpu["q_pe"], ref["q_pe"], ref["q_cond"][:, :, 128:], k_terms=1536,
                report=report)
     check_bf16("q_latent", gpu["q_latent"], ref["q_latent"], ref["lat_cond"], k_terms=128,
-               report=report)
+               report=report, slack=latent_slack(ref, inp))
     check_cache(gpu["cache"], ref["cache"], inp["cache"], inp["slots"], inp["cache"].shape[1],
                 int(inp["layout"]), report=report)
+
+
+def check_against_oracle(gpu: dict, inp: dict, report=None, q_c=True, dump_name=None):
+    """Oracle reference (tie-aware) and every check; on failure, saves the GPU
+    outputs under $MLA_PARITY_DUMP (if set) for offline analysis."""
+    import os
+
+    ref = reference_for(inp, gpu.get("q_c") if q_c else None)
+    try:
+        check_step(gpu, ref, inp, report=report, q_c=q_c)
+    except AssertionError:
+        d = os.environ.get("MLA_PARITY_DUMP")
+        if d and dump_name:
+            os.makedirs(d, exist_ok=True)
+            np.savez_compressed(os.path.join(d, f"{dump_name}.npz"),
+                                **{k: v for k, v in gpu.items() if k != "cache"})
+        raise
+    return ref

@@ -382,3 +382,44 @@ def test_decode_step_shapes_on_a_workload():
     changed = np.any(out["cache"] != inp["cache"], axis=-1)
     s = int(inp["slots"][0])
     assert changed.sum() == 1 and changed[s // 64, s % 64]
+
+
+# ---------------------------------------------------------------- tie zones
+
+
+def test_bf16_midpoint_helpers_hand_worked():
+    x = np.array([1.0 + 2.0**-8, 1.0 + 2.0**-9, 3.0, -0.95117186, 2.0**-140])
+    d = O.bf16_midpoint_distance(x)
+    assert d[0] == 0.0  # exactly halfway between 1.0 and 1 + 2**-7
+    assert d[1] == 2.0**-9  # a quarter quantum from 1.0, a quarter from the midpoint
+    assert d[2] == 2.0**-7  # representable (quantum 2**-6 in [2, 4)): half a quantum away
+    assert abs(d[3] - 1.5e-8) < 1e-15
+    other = O.bf16_other_rounding(x)
+    assert other[0] == 1.0078125 and O.round_to_bf16(x[0]) == 1.0
+    assert other[1] == 1.0078125
+    assert other[2] == 3.0
+    assert other[3] == -0.953125 and O.round_to_bf16(x[3]) == -0.94921875
+
+
+def test_decode_step_alternate_rounding_of_a_tie():
+    """Marking the normalised element nearest a BF16 tie moves only that q_c
+    element, by one quantum; marking an element far from a tie is refused."""
+    inp = _hand_inputs(0, H=1, slots=(1,))
+    rng = np.random.default_rng(19)
+    inp["q_a"] = _bf16(rng.standard_normal((1, 1536)))
+    ref = O.decode_step(inp)
+    dist = O.bf16_midpoint_distance(ref["xq_exact"]) / np.abs(ref["xq_exact"])
+    k = int(np.argmin(dist))
+    if dist[0, k] <= O.XQ_TIE_REL:
+        alt = np.zeros((1, 1536), bool)
+        alt[0, k] = True
+        out = O.decode_step(inp, xq_alt=alt)
+        moved = out["q_c"] != ref["q_c"]
+        assert moved.sum() == 1 and moved[0, k]
+        q = O.bf16_quantum(ref["xq_exact"][0, k])
+        assert abs(O.bf16_bits_to_f64(out["q_c"])[0, k] - O.bf16_bits_to_f64(ref["q_c"])[0, k]) == q
+    far = int(np.argmax(dist))
+    alt = np.zeros((1, 1536), bool)
+    alt[0, far] = True
+    with pytest.raises(ValueError):
+        O.decode_step(inp, xq_alt=alt)

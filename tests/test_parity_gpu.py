@@ -1,6 +1,8 @@
 """GPU parity: the CUDA path (through the C ABI) against the FP64 oracle, on
 the same seeded inputs, element by element.  Every test needs a GB300."""
 
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -10,7 +12,7 @@ from mla_query_projection_gb300 import synthetic as S
 from mla_query_projection_gb300.runner import DecodeStep
 from oracle import mla_oracle as O
 
-from .parity_util import check_bf16, check_step
+from .parity_util import check_against_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -36,11 +38,11 @@ def run_case(inp, path=B.MLA_PATH_AUTO, fused_row=False, q_c=True, repeat=1):
 
 
 def assert_parity(inp, report=None, **kw):
-    ref = O.decode_step(inp)
     out, flags = run_case(inp, **kw)
+    name = os.environ.get("PYTEST_CURRENT_TEST", "case").split(" ")[0].split("::")[-1]
+    ref = check_against_oracle(out, inp, report=report, q_c=kw.get("q_c", True), dump_name=name)
     want_flag = B.MLA_DEVERR_BAD_SLOT if ref["bad_slots"] else 0
     assert flags == want_flag, f"device flags {flags}"
-    check_step(out, ref, inp, report=report, q_c=kw.get("q_c", True))
     return out, ref
 
 
@@ -100,8 +102,14 @@ def test_fused_qkv_row_strides(batch):
 
 
 def test_q_c_optional():
+    """q_c = NULL computes the same step without writing q_c: bit-identical to
+    the run that writes it, which is checked against the oracle."""
     inp = S.make_inputs(batch=4, heads=8, layout=S.LAYOUT_E4M3, pages=8, seed=500)
-    assert_parity(inp, q_c=False)
+    with_qc, _ = assert_parity(inp)
+    without, flags = run_case(inp, q_c=False)
+    assert flags == 0
+    for k in ("q_latent", "q_pe", "cache"):
+        assert np.array_equal(with_qc[k], without[k])
 
 
 def test_negative_slots_skip_and_bad_slots_flag():
@@ -179,7 +187,6 @@ def test_weights_bound_at_create_are_read_each_call():
     second = st.results()
     inp2 = dict(inp)
     inp2["w_qb"] = (O.f64_to_bf16_bits(2.0 * O.bf16_bits_to_f64(inp["w_qb"])))
-    ref = O.decode_step(inp2)
-    check_bf16("q_pe", second["q_pe"], ref["q_pe"], ref["q_cond"][:, :, 128:], k_terms=1536)
+    check_against_oracle(second, inp2)
     assert not np.array_equal(first["q_pe"], second["q_pe"])
     st.close()
