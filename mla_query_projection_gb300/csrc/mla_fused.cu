@@ -238,8 +238,9 @@ __device__ void kv_insert(const DecodeArgs& a, int b, int lt, float* red2) {
 
 // Timeline stamps (MLA_TRACE builds): slot 0 start, 1 producer ring filled,
 // 2 consumer prologue done, 3 first W_UK wait start, 4 its end, 5 end of the
-// nope phase, 6 last stage consumed, 7 end, 8.. the time each stage's data
-// was seen by consumer thread 0.
+// nope phase, 6 last stage consumed, 7 end, 8..27 the time consumer thread 0
+// saw stage s's data, 28..47 the time the producer issued stage s, 48..63 the
+// time consumer thread 0 finished stage s (s < 16).
 __device__ __forceinline__ void trace_stamp(const DecodeArgs& a, int slot) {
 #ifdef MLA_TRACE
   if (a.trace != nullptr && slot < kTraceSlots) {
@@ -346,6 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // sequence the others follow.
         if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) timed_out = true;
       }
+      if (lane == 0 && issued < 20) trace_stamp(a, 28 + issued);
       issue_stage(st, ring + slot * G::kStageBytes, &full[slot], a, &uk_map, lane);
       ++issued;
       if (issued == S::kStages && lane == 0) trace_stamp(a, 1);
@@ -447,7 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait_bounded(&full[slot], (uint32_t)((s / S::kStages) & 1), kWaitLimit))
         timed_out = true;  // keep the stage sequence; the call is flagged invalid
       if (tid == 0) {
-        trace_stamp(a, 8 + s);
+        if (s < 20) trace_stamp(a, 8 + s);
+        if (s > 0 && s <= 16) trace_stamp(a, 47 + s);
         if (st.kind != kNopeRows) trace_stamp(a, 5);
       }
       if (st.kind != kNopeRows && pub_h >= 0) {
@@ -465,6 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) rdy = wait_ready(ready_g + h, (uint32_t)kNope) ? 1 : 0;
         if (tid == 0) trace_stamp(a, 4);
         rdy = __shfl_sync(0xFFFFFFFFu, rdy, 0);
+        __syncwarp();  // orders the lanes' q loads below after lane 0's acquire
         if (!rdy) timed_out = true;
         const uint16_t* qsrc = qn_g + (int64_t)h * kNope;  // token t at + t*H*128
         if constexpr (MMA) {
@@ -476,8 +480,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int ks = 0; ks < kNope / 16; ++ks) {
               const uint16_t* qr = qsrc + (int64_t)(8 * nt + g) * H * kNope + 16 * ks + 2 * q;
-              bf[nt][ks][0] = __ldcg(reinterpret_cast<const unsigned int*>(qr));
-              bf[nt][ks][1] = __ldcg(reinterpret_cast<const unsigned int*>(qr + 8));
+              bf[nt][ks][0] = ld_cg_u32(qr);
+              bf[nt][ks][1] = ld_cg_u32(qr + 8);
             }
           for (int pair = warp; pair < 4 * st.count; pair += kConsumerWarps) {
             const int u = pair >> 2, mt = pair & 3;
@@ -515,8 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float* qs = reinterpret_cast<float*>(smem + S::oScratch) + warp * NT * kNope;
 #pragma unroll
           for (int t = 0; t < NT; ++t) {
-            const uint2 v =
-                __ldcg(reinterpret_cast<const uint2*>(qsrc + (int64_t)t * H * kNope + 4 * lane));
+            const uint2 v = ld_cg_u32x2(qsrc + (int64_t)t * H * kNope + 4 * lane);
             qs[t * kNope + 4 * lane] = bf16lo(v.x);
             qs[t * kNope + 4 * lane + 1] = bf16hi(v.x);
             qs[t * kNope + 4 * lane + 2] = bf16lo(v.y);
