@@ -155,6 +155,46 @@ MLA_API int mla_query_set_path(mla_query_t h, int path);
  */
 MLA_API int mla_query_path_for(mla_query_t h, int batch);
 
+#define MLA_NOALLOC_MAX_BATCH 64 /* largest batch of mla_query_decode_noalloc */
+
+/*
+ * mla_query_decode_noalloc - the same decode step as mla_query_decode, for
+ * callers that must not allocate device memory: a serving runtime that
+ * reserves all GPU memory for its own pool at start-up, or a plugin loaded
+ * into a framework whose allocator owns the device, cannot let a library call
+ * cudaMalloc behind its back.  The pages define no such entry point; it has
+ * no counterpart there.
+ *
+ * No handle: the weights, eps and every per-call argument are passed
+ * directly (same meaning, layout and alignment rules as mla_query_create and
+ * mla_query_decode).  The kernel's scratch (q hand-off buffer and counters)
+ * is one fixed device array inside the library, about 2 MiB, that every GPU
+ * which loads the library holds until the process exits.  The call allocates
+ * nothing (no cudaMalloc, cudaFree or allocating library routine).
+ *
+ *   batch         1 <= B <= MLA_NOALLOC_MAX_BATCH (64); a larger batch
+ *                 returns MLA_EUNSUPPORTED; num_heads <= MLA_MAX_HEADS.
+ *   device_flags  optional caller-owned device word (4-byte aligned) into
+ *                 which the call ORs MLA_DEVERR_* bits; NULL to ignore them.
+ *
+ * The first call on a device sets that device up (looks up the array's
+ * device address, opts the kernels into their shared memory); make that first
+ * call before any stream capture.  Every call shares the one array, and each
+ * call clears its counters on `stream` before launching: calls that may
+ * overlap on the GPU (different streams, or threads without ordering) race on
+ * it and must not be issued; order them on one stream.
+ * Returns MLA_OK, MLA_EINVAL, MLA_EUNSUPPORTED or MLA_ECUDA.
+ */
+MLA_API int mla_query_decode_noalloc(int num_heads, const void* w_qb, const void* w_uk,
+                                     const void* gamma_q, const void* gamma_kv, float eps,
+                                     int batch, const void* q_a, int64_t q_a_stride,
+                                     const void* kv_c, int64_t kv_c_stride, const void* k_pe,
+                                     int64_t k_pe_stride, const int64_t* slot_mapping,
+                                     void* kv_cache, int64_t num_pages, int page_size,
+                                     int layout, const float* k_scale, void* q_latent,
+                                     void* q_pe, void* q_c, unsigned* device_flags,
+                                     void* stream);
+
 /* mla_query_destroy - free the handle and its scratch (NULL is a no-op).
  * The caller must ensure no decode on the handle is still in flight. */
 MLA_API void mla_query_destroy(mla_query_t h);

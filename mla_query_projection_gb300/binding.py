@@ -28,6 +28,7 @@ MLA_PATH_FMA = 1
 MLA_PATH_MMA = 2
 MLA_MAX_BATCH = 256
 MLA_MAX_HEADS = 128
+MLA_NOALLOC_MAX_BATCH = 64
 
 _lib = None
 
@@ -62,6 +63,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mla_query_set_path.restype = i32
     lib.mla_query_path_for.argtypes = [vp, i32]
     lib.mla_query_path_for.restype = i32
+    lib.mla_query_decode_noalloc.argtypes = [
+        i32, vp, vp, vp, vp, f32, i32, vp, i64, vp, i64, vp, i64, vp, vp, i64, i32, i32, vp, vp,
+        vp, vp, vp, vp,
+    ]
+    lib.mla_query_decode_noalloc.restype = i32
     lib.mla_query_destroy.argtypes = [vp]
     lib.mla_query_destroy.restype = None
     lib.mla_query_strerror.argtypes = [i32]
@@ -112,6 +118,22 @@ def mla_query_decode(
         handle, int(batch), _ptr(q_a), int(q_a_stride), _ptr(kv_c), int(kv_c_stride),
         _ptr(k_pe), int(k_pe_stride), _ptr(slot_mapping), _ptr(kv_cache), int(num_pages),
         int(page_size), int(layout), _ptr(k_scale), _ptr(q_latent), _ptr(q_pe), _ptr(q_c),
+        _stream(stream),
+    )
+
+
+def mla_query_decode_noalloc(
+    num_heads, w_qb, w_uk, gamma_q, gamma_kv, eps, batch, q_a, q_a_stride, kv_c, kv_c_stride,
+    k_pe, k_pe_stride, slot_mapping, kv_cache, num_pages, page_size, layout, k_scale, q_latent,
+    q_pe, q_c, device_flags, stream,
+) -> int:
+    """The handle-free decode for callers that must not allocate device
+    memory; returns the C return code."""
+    return load().mla_query_decode_noalloc(
+        int(num_heads), _ptr(w_qb), _ptr(w_uk), _ptr(gamma_q), _ptr(gamma_kv), float(eps),
+        int(batch), _ptr(q_a), int(q_a_stride), _ptr(kv_c), int(kv_c_stride), _ptr(k_pe),
+        int(k_pe_stride), _ptr(slot_mapping), _ptr(kv_cache), int(num_pages), int(page_size),
+        int(layout), _ptr(k_scale), _ptr(q_latent), _ptr(q_pe), _ptr(q_c), _ptr(device_flags),
         _stream(stream),
     )
 
