@@ -85,10 +85,14 @@ typedef struct mla_query* mla_query_t;
  *   gamma_q   device BF16 [1536], gamma_kv device BF16 [512].
  *   eps       RMSNorm epsilon used by both norms.
  *
- * The weights are borrowed, not copied: they must stay valid and unchanged
- * until mla_query_destroy.  create allocates the handle's small device scratch
- * (query hand-off buffer, counters, error flag) with cudaMalloc on the current
- * device; the handle may only be used on that device.
+ * W_QB and the gammas are borrowed, not copied: they must stay valid and
+ * unchanged until mla_query_destroy.  W_UK is copied once, here, into a
+ * library-owned layout of contiguous 64-column tiles (H * 128 KiB), so later
+ * changes to the caller's W_UK are not seen (create a new handle instead).
+ * create allocates that copy and the handle's small device scratch (query
+ * hand-off buffer, counters, error flag) with cudaMalloc on the current
+ * device, and synchronises the legacy default stream; the handle may only be
+ * used on that device.
  * Returns MLA_OK, MLA_EINVAL, MLA_ENOMEM or MLA_ECUDA.
  */
 MLA_API int mla_query_create(mla_query_t* out, int num_heads, const void* w_qb,

@@ -24,6 +24,7 @@ struct mla_query {
   uint32_t* ready;
   uint16_t* qn;
   uint64_t* trace;  // MLA_TRACE builds: per-CTA timeline stamps
+  uint8_t* w_uk_packed;  // library-owned repacked copy of W_UK
 };
 
 namespace {
@@ -131,6 +132,15 @@ int mla_query_create(mla_query_t* out, int num_heads, const void* w_qb, const vo
     h->ready = reinterpret_cast<uint32_t*>(base + head);
     h->qn = reinterpret_cast<uint16_t*>(base + qn_off);
   }
+  // W_UK copy in contiguous pre-swizzled units (one 1-D bulk copy per unit).
+  if (cudaMalloc(&h->w_uk_packed, (size_t)num_heads * mla::kUkUnitsPerHead * mla::kUkUnitBytes) !=
+      cudaSuccess) {
+    rc = MLA_ENOMEM;
+    goto fail;
+  }
+  if (mla::repack_w_uk(h->w_uk, h->w_uk_packed, num_heads, 0) != cudaSuccess ||
+      cudaStreamSynchronize(0) != cudaSuccess)
+    goto fail;
 #ifdef MLA_TRACE
   {
     const size_t tb = (size_t)h->num_sms * mla::kTraceSlots * 8;
@@ -142,6 +152,8 @@ int mla_query_create(mla_query_t* out, int num_heads, const void* w_qb, const vo
   return MLA_OK;
 fail:
   if (h->scratch) cudaFree(h->scratch);
+  if (h->w_uk_packed) cudaFree(h->w_uk_packed);
+  if (h->trace) cudaFree(h->trace);
   free(h);
   cudaGetLastError();
   return rc;
@@ -179,6 +191,7 @@ int mla_query_decode(mla_query_t h, int batch, const void* q_a, int64_t q_a_stri
 
   mla::DecodeArgs a;
   a.w_qb = h->w_qb;
+  a.w_uk_packed = h->w_uk_packed;
   a.gamma_q = h->gamma_q;
   a.gamma_kv = h->gamma_kv;
   a.q_a = static_cast<const uint16_t*>(q_a);
@@ -260,6 +273,7 @@ void mla_query_destroy(mla_query_t h) {
   if (h == nullptr) return;
   if (h->trace) cudaFree(h->trace);
   if (h->scratch) cudaFree(h->scratch);
+  if (h->w_uk_packed) cudaFree(h->w_uk_packed);
   free(h);
 }
 

@@ -139,7 +139,12 @@ __device__ __forceinline__ void issue_stage(const Stage& s, uint8_t* buf, uint64
                                             const DecodeArgs& a, const CUtensorMap* uk_map,
                                             int lane) {
   if (s.kind == kUkTiles) {
-    if (lane == 0) {
+    if (lane == 0 && a.w_uk_packed != nullptr) {
+      // consecutive units of one head are contiguous in the packed copy
+      mbar_arrive_expect_tx(bar, (uint32_t)(s.count * kUkUnitBytes));
+      bulk_g2s(buf, a.w_uk_packed + (int64_t)s.first * kUkUnitBytes,
+               (uint32_t)(s.count * kUkUnitBytes), bar);
+    } else if (lane == 0) {
       mbar_arrive_expect_tx(bar, (uint32_t)(s.count * kUkUnitBytes));
       for (int j = 0; j < s.count; ++j) {
         const int u = s.first + j;
@@ -744,6 +749,27 @@ int tokens_per_cta(int batch, bool mma) {
 
 size_t scratch_qn_elems(int heads) { return (size_t)(MLA_MAX_BATCH + 16) * heads * kNope; }
 size_t scratch_ready_elems(int heads) { return (size_t)(MLA_MAX_BATCH / 8 + 2) * heads; }
+
+__global__ void repack_w_uk_kernel(const uint16_t* __restrict__ w_uk, uint8_t* __restrict__ dst,
+                                   int heads) {
+  const int64_t n = (int64_t)heads * kUkUnitsPerHead * kNope * 8;  // 16-byte chunks
+  for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int j = (int)(e % 8);
+    const int p = (int)((e / 8) % kNope);
+    const int cb = (int)((e / (8 * kNope)) % kUkUnitsPerHead);
+    const int h = (int)(e / (8 * kNope * kUkUnitsPerHead));
+    const uint4 v = *reinterpret_cast<const uint4*>(
+        w_uk + ((int64_t)h * kNope + p) * kKvLora + cb * kUkCols + 8 * j);
+    *reinterpret_cast<uint4*>(dst + ((int64_t)(h * kUkUnitsPerHead + cb) * kNope + p) * 128 +
+                              16 * (j ^ (p & 7))) = v;
+  }
+}
+
+cudaError_t repack_w_uk(const uint16_t* w_uk, uint8_t* dst, int heads, cudaStream_t stream) {
+  repack_w_uk_kernel<<<256, 256, 0, stream>>>(w_uk, dst, heads);
+  return cudaGetLastError();
+}
 
 cudaError_t prepare_fused_kernels() {
   cudaError_t e;

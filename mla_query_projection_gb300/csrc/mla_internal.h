@@ -31,6 +31,10 @@ constexpr int64_t kItemBytesPerHead = (int64_t)kUkUnitsPerHead * kUkUnitBytes +
 
 struct DecodeArgs {
   const uint16_t* w_qb;      // [H*192][1536]
+  // W_UK repacked as contiguous pre-swizzled 64-column units (see
+  // repack_w_uk), or null to load the caller's [H][128][512] through the
+  // tensor map.
+  const uint8_t* w_uk_packed;
   const uint16_t* gamma_q;   // [1536]
   const uint16_t* gamma_kv;  // [512]
   const uint16_t* q_a;       // [B][q_a_stride]
@@ -71,6 +75,12 @@ size_t scratch_ready_elems(int heads);
 cudaError_t launch_fused(const DecodeArgs& a, const CUtensorMap* uk_map, int nt, bool mma,
                          int num_sms, cudaStream_t stream);
 cudaError_t prepare_fused_kernels();
+
+// Repack W_UK [H][128][512] BF16 into H*8 contiguous 16 KiB units: unit
+// (h, cb) holds columns 64*cb..64*cb+63 as 128 rows of 128 B, the 16-byte
+// chunk j of row p stored at chunk position j ^ (p % 8) (the layout a 2-D
+// tensor copy with 128-byte swizzle produces).  dst: H * 131072 bytes.
+cudaError_t repack_w_uk(const uint16_t* w_uk, uint8_t* dst, int heads, cudaStream_t stream);
 
 int tokens_per_cta(int batch, bool mma);
 
