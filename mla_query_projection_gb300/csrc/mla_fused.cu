@@ -18,9 +18,10 @@
 //  * Nope hand-off.  All CTAs stream their nope rows first and publish the
 //    BF16 q values to a small global scratch; a per-(group, head) counter
 //    reaches 128 when a head is complete (one release per head and writer).
-//    The W_UK tiles of a head come later in every CTA's order, so by then the
-//    counters are normally full; the wait is bounded and raises
-//    MLA_DEVERR_TIMEOUT instead of hanging.  The last CTA re-arms the counters.
+//    Every CTA streams its rope rows next and its W_UK tiles last, so by then
+//    the counters are normally full; each warp waits (bounded: a timeout
+//    raises MLA_DEVERR_TIMEOUT instead of hanging) and loads the head's q
+//    once per head.  The last CTA re-arms the counters.
 //  * Arithmetic.  FMA flavour (1-2 tokens, 8-row stages): FP32 FMAs, one warp
 //    per row, x in registers.  MMA flavour (8 or 16 tokens per CTA, 16-row
 //    stages): BF16 mma.sync m16n8k16 with the weight rows as the M side
@@ -98,28 +99,57 @@ __device__ __forceinline__ Work cta_work(int i, int P, int H) {
   return w;
 }
 
+// Stage order of one CTA: its nope rows, then its rope rows, then its W_UK
+// units (the absorption comes last, when every CTA's nope rows, written in
+// the first phase, are long complete).
+struct Cursor {
+  int pn;     // next nope index
+  int pc;     // next combined item
+  int phase;  // 0 nope rows, 1 rope rows, 2 W_UK units
+};
+
+__device__ __forceinline__ Cursor start_cursor(const Work& w) { return Cursor{w.n0, w.c0, 0}; }
+
 template <bool MMA>
-__device__ __forceinline__ bool next_stage(int& pn, int& pc, const Work& w, Stage& s) {
+__device__ __forceinline__ bool next_stage(Cursor& c, const Work& w, Stage& s) {
   using G = Geo<MMA>;
-  if (pn < w.n1) {
-    s.kind = kNopeRows;
-    s.first = pn;
-    s.count = min(G::kStageRows, w.n1 - pn);
-    pn += s.count;
-    return true;
+  if (c.phase == 0) {
+    if (c.pn < w.n1) {
+      s.kind = kNopeRows;
+      s.first = c.pn;
+      s.count = min(G::kStageRows, w.n1 - c.pn);
+      c.pn += s.count;
+      return true;
+    }
+    c.phase = 1;
+    c.pc = w.c0;
   }
-  if (pc < w.c1) {
-    const int h = pc / kItemsPerHead, l = pc % kItemsPerHead;
-    if (l < kUkUnitsPerHead) {
-      s.kind = kUkTiles;
-      s.first = h * kUkUnitsPerHead + l;
-      s.count = min(min(G::kUkPerStage, kUkUnitsPerHead - l), w.c1 - pc);
-    } else {
+  if (c.phase == 1) {
+    while (c.pc < w.c1) {
+      const int h = c.pc / kItemsPerHead, l = c.pc % kItemsPerHead;
+      if (l < kUkUnitsPerHead) {  // skip this head's W_UK units for now
+        c.pc = h * kItemsPerHead + kUkUnitsPerHead;
+        continue;
+      }
       s.kind = kRopeRows;
       s.first = h * kRope + (l - kUkUnitsPerHead);
-      s.count = min(min(G::kStageRows, kItemsPerHead - l), w.c1 - pc);
+      s.count = min(min(G::kStageRows, kItemsPerHead - l), w.c1 - c.pc);
+      c.pc += s.count;
+      return true;
     }
-    pc += s.count;
+    c.phase = 2;
+    c.pc = w.c0;
+  }
+  while (c.pc < w.c1) {
+    const int h = c.pc / kItemsPerHead, l = c.pc % kItemsPerHead;
+    if (l >= kUkUnitsPerHead) {  // rope rows were streamed in phase 1
+      c.pc = (h + 1) * kItemsPerHead;
+      continue;
+    }
+    s.kind = kUkTiles;
+    s.first = h * kUkUnitsPerHead + l;
+    s.count = min(min(G::kUkPerStage, kUkUnitsPerHead - l), w.c1 - c.pc);
+    c.pc += s.count;
     return true;
   }
   return false;
@@ -339,9 +369,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kConsumerWarps) {
     // ================= producer warp =================================
     // Weights do not depend on the previous kernel: no PDL wait here.
-    int pn = w.n0, pc = w.c0, issued = 0;
+    Cursor cur = start_cursor(w);
+    int issued = 0;
     Stage st;
-    while (next_stage<MMA>(pn, pc, w, st)) {
+    while (next_stage<MMA>(cur, w, st)) {
       const int slot = issued % S::kStages;
       if (issued >= S::kStages) {
         const uint32_t par = (uint32_t)(((issued / S::kStages) - 1) & 1);
@@ -446,9 +477,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // lane 0 of each warp for its own rows; MMA: by thread 0 for the CTA).
     int pub_h = -1, pub_n = 0;
 
-    int cn = w.n0, cc = w.c0;
+    // Head whose nope q this warp holds (FMA: staged in smem; MMA: as B
+    // fragments in registers) after its hand-off wait, or -1.
+    int cached_h = -1;
+    uint32_t bf[MMA ? NT / 8 : 1][kNope / 16][2];
+
+    Cursor cur = start_cursor(w);
     Stage st;
-    for (int s = 0; next_stage<MMA>(cn, cc, w, st); ++s) {
+    for (int s = 0; next_stage<MMA>(cur, w, st); ++s) {
       const int slot = s % S::kStages;
       uint8_t* buf = ring + slot * G::kStageBytes;
       if (!mbar_wait_bounded(&full[slot], (uint32_t)((s / S::kStages) & 1), kWaitLimit))
@@ -468,26 +504,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- absorption of one head's nope q through W_UK tiles -------
         const int h = st.first / kUkUnitsPerHead;
         const int cb0 = st.first % kUkUnitsPerHead;
-        int rdy = 1;
-        if (tid == 0) trace_stamp(a, 3);
-        if (lane == 0) rdy = wait_ready(ready_g + h, (uint32_t)kNope) ? 1 : 0;
-        if (tid == 0) trace_stamp(a, 4);
-        rdy = __shfl_sync(0xFFFFFFFFu, rdy, 0);
-        __syncwarp();  // orders the lanes' q loads below after lane 0's acquire
-        if (!rdy) timed_out = true;
+        const bool fresh = h != cached_h;  // warp-uniform
+        if (fresh) {
+          int rdy = 1;
+          if (tid == 0) trace_stamp(a, 3);
+          if (lane == 0) rdy = wait_ready(ready_g + h, (uint32_t)kNope) ? 1 : 0;
+          if (tid == 0) trace_stamp(a, 4);
+          rdy = __shfl_sync(0xFFFFFFFFu, rdy, 0);
+          __syncwarp();  // orders the lanes' q loads below after lane 0's acquire
+          if (!rdy) timed_out = true;
+          cached_h = h;
+        }
         const uint16_t* qsrc = qn_g + (int64_t)h * kNope;  // token t at + t*H*128
         if constexpr (MMA) {
           const int g = lane >> 2, q = lane & 3;
-          // B fragments (q^T, 8 tokens per n-tile) straight from L2.
-          uint32_t bf[NT / 8][kNope / 16][2];
+          if (fresh) {
+            // B fragments (q^T, 8 tokens per n-tile) straight from L2.
 #pragma unroll
-          for (int nt = 0; nt < NT / 8; ++nt)
+            for (int nt = 0; nt < NT / 8; ++nt)
 #pragma unroll
-            for (int ks = 0; ks < kNope / 16; ++ks) {
-              const uint16_t* qr = qsrc + (int64_t)(8 * nt + g) * H * kNope + 16 * ks + 2 * q;
-              bf[nt][ks][0] = ld_cg_u32(qr);
-              bf[nt][ks][1] = ld_cg_u32(qr + 8);
-            }
+              for (int ks = 0; ks < kNope / 16; ++ks) {
+                const uint16_t* qr = qsrc + (int64_t)(8 * nt + g) * H * kNope + 16 * ks + 2 * q;
+                bf[nt][ks][0] = ld_cg_u32(qr);
+                bf[nt][ks][1] = ld_cg_u32(qr + 8);
+              }
+          }
           for (int pair = warp; pair < 4 * st.count; pair += kConsumerWarps) {
             const int u = pair >> 2, mt = pair & 3;
             const uint32_t tile = smem_u32(buf + u * kUkUnitBytes);
@@ -522,15 +563,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           // One W_UK unit (64 columns); warp w owns columns 8w..8w+7.  Lane:
           // column pair cp = lane & 3, rows p = pg + 8 k (pg = lane >> 2).
           float* qs = reinterpret_cast<float*>(smem + S::oScratch) + warp * NT * kNope;
+          if (fresh) {
 #pragma unroll
-          for (int t = 0; t < NT; ++t) {
-            const uint2 v = ld_cg_u32x2(qsrc + (int64_t)t * H * kNope + 4 * lane);
-            qs[t * kNope + 4 * lane] = bf16lo(v.x);
-            qs[t * kNope + 4 * lane + 1] = bf16hi(v.x);
-            qs[t * kNope + 4 * lane + 2] = bf16lo(v.y);
-            qs[t * kNope + 4 * lane + 3] = bf16hi(v.y);
+            for (int t = 0; t < NT; ++t) {
+              const uint2 v = ld_cg_u32x2(qsrc + (int64_t)t * H * kNope + 4 * lane);
+              qs[t * kNope + 4 * lane] = bf16lo(v.x);
+              qs[t * kNope + 4 * lane + 1] = bf16hi(v.x);
+              qs[t * kNope + 4 * lane + 2] = bf16lo(v.y);
+              qs[t * kNope + 4 * lane + 3] = bf16hi(v.y);
+            }
+            __syncwarp();
           }
-          __syncwarp();
           const int cp = lane & 3, pg = lane >> 2;
           float acc[NT][2];
 #pragma unroll
@@ -628,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             pub_n += upto - j;
             j = upto;
           }
-          if (cn >= w.n1 || (pub_h + 1) * kNope <= cn) {
+          if (cur.pn >= w.n1 || (pub_h + 1) * kNope <= cur.pn) {
             publish_rows(ready_g, pub_h, pub_n);
             pub_h = -1;
             pub_n = 0;
