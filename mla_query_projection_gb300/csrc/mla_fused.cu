@@ -22,9 +22,9 @@
 //    the counters are normally full; each warp waits (bounded: a timeout
 //    raises MLA_DEVERR_TIMEOUT instead of hanging) and loads the head's q
 //    once per head.  The last CTA re-arms the counters.
-//  * Arithmetic.  FMA flavour (1-2 tokens, 8-row stages): FP32 FMAs, one warp
-//    per row, x in registers.  MMA flavour (8 or 16 tokens per CTA, 16-row
-//    stages): BF16 mma.sync m16n8k16 with the weight rows as the M side
+//  * Arithmetic (16-row stages of 49 KiB: fewer, larger stages stream faster).
+//    FMA flavour (1-2 tokens): FP32 FMAs, one warp per row, x in registers.
+//    MMA flavour (8 or 16 tokens per CTA): BF16 mma.sync m16n8k16 with the weight rows as the M side
 //    (tokens are N), K split over the eight consumer warps and reduced in a
 //    fixed order through smem; the absorption takes the swizzled W_UK tile as
 //    the M side through ldmatrix.trans.
@@ -64,7 +64,7 @@ struct Work {
 
 template <bool MMA>
 struct Geo {
-  static constexpr int kStageRows = MMA ? 16 : 8;
+  static constexpr int kStageRows = 16;
   static constexpr int kStageBytes = ((kStageRows * kPitch + 1023) / 1024) * 1024;
   static constexpr int kUkPerStage = kStageBytes / kUkUnitBytes;  // 3 or 1
 };
@@ -312,7 +312,7 @@ __device__ __forceinline__ void publish_rows(uint32_t* ready_g, int h, int count
 template <int NT, bool MMA>
 struct Smem {
   using G = Geo<MMA>;
-  static constexpr int kStages = MMA ? (NT <= 8 ? 4 : 3) : 8;
+  static constexpr int kStages = NT <= 8 ? 4 : 3;
   static constexpr int kRing = kStages * G::kStageBytes;
   static constexpr int kXq = NT * kPitch;
   // FMA: per-warp staged q of one head [warp][NT][128] FP32; MMA: split-K
@@ -560,8 +560,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         } else {
-          // One W_UK unit (64 columns); warp w owns columns 8w..8w+7.  Lane:
-          // column pair cp = lane & 3, rows p = pg + 8 k (pg = lane >> 2).
+          // W_UK units of 64 columns; in each, warp w owns columns 8w..8w+7.
+          // Lane: column pair cp = lane & 3, rows p = pg + 8 k (pg = lane >> 2).
           float* qs = reinterpret_cast<float*>(smem + S::oScratch) + warp * NT * kNope;
           if (fresh) {
 #pragma unroll
@@ -575,39 +575,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
           }
           const int cp = lane & 3, pg = lane >> 2;
-          float acc[NT][2];
+          for (int u = 0; u < st.count; ++u) {
+            const uint8_t* tile = buf + u * kUkUnitBytes;
+            float acc[NT][2];
 #pragma unroll
-          for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = 0.f;
+            for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = 0.f;
 #pragma unroll
-          for (int k = 0; k < kNope / 8; ++k) {
-            const int p = pg + 8 * k;
-            const uint32_t wv = *reinterpret_cast<const uint32_t*>(
-                buf + p * 128 + ((warp ^ (p & 7)) << 4) + 4 * cp);
-            const float w0 = bf16lo(wv), w1 = bf16hi(wv);
+            for (int k = 0; k < kNope / 8; ++k) {
+              const int p = pg + 8 * k;
+              const uint32_t wv = *reinterpret_cast<const uint32_t*>(
+                  tile + p * 128 + ((warp ^ (p & 7)) << 4) + 4 * cp);
+              const float w0 = bf16lo(wv), w1 = bf16hi(wv);
 #pragma unroll
-            for (int t = 0; t < NT; ++t) {
-              acc[t][0] = fmaf(qs[t * kNope + p], w0, acc[t][0]);
-              acc[t][1] = fmaf(qs[t * kNope + p], w1, acc[t][1]);
+              for (int t = 0; t < NT; ++t) {
+                acc[t][0] = fmaf(qs[t * kNope + p], w0, acc[t][0]);
+                acc[t][1] = fmaf(qs[t * kNope + p], w1, acc[t][1]);
+              }
             }
-          }
-#pragma unroll
-          for (int t = 0; t < NT; ++t)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              float v = acc[t][e];
-              v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
-              v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
-              v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
-              acc[t][e] = v;
-            }
-          if (pg == 0) {
-            const int c = cb0 * kUkCols + 8 * warp + 2 * cp;
 #pragma unroll
             for (int t = 0; t < NT; ++t)
-              if (tok0 + t < a.batch)
-                *reinterpret_cast<uint32_t*>(a.q_latent +
-                                             ((int64_t)(tok0 + t) * H + h) * kKvLora + c) =
-                    pack_bf16x2(acc[t][0], acc[t][1]);
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                float v = acc[t][e];
+                v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
+                v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
+                v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
+                acc[t][e] = v;
+              }
+            if (pg == 0) {
+              const int c = (cb0 + u) * kUkCols + 8 * warp + 2 * cp;
+#pragma unroll
+              for (int t = 0; t < NT; ++t)
+                if (tok0 + t < a.batch)
+                  *reinterpret_cast<uint32_t*>(a.q_latent +
+                                               ((int64_t)(tok0 + t) * H + h) * kKvLora + c) =
+                      pack_bf16x2(acc[t][0], acc[t][1]);
+            }
           }
         }
       } else if constexpr (MMA) {
@@ -679,39 +682,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;  // slot already released
       } else {
-        // ---- Q_B rows, FP32 FMA: warp w owns row w of the stage ---------
-        const int j = warp;
-        if (j < st.count) {
-          const uint8_t* rowp = buf + j * kPitch;
-          float acc[NT][2];
+        // ---- Q_B rows, FP32 FMA: warp w owns rows w and w + 8 -----------
+        float v[2][NT];
 #pragma unroll
-          for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = 0.f;
+        for (int rr = 0; rr < 2; ++rr) {
+          const int j = warp + kConsumerWarps * rr;
+          if (j < st.count) {
+            const uint8_t* rowp = buf + j * kPitch;
+            float acc[NT][2];
 #pragma unroll
-          for (int c = 0; c < 6; ++c) {
-            const uint4 v = *reinterpret_cast<const uint4*>(rowp + 2 * (256 * c + 8 * lane));
-            const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
+            for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = 0.f;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float w0 = bf16lo(ww[k]), w1 = bf16hi(ww[k]);
+            for (int c = 0; c < 6; ++c) {
+              const uint4 wv = *reinterpret_cast<const uint4*>(rowp + 2 * (256 * c + 8 * lane));
+              const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-              for (int t = 0; t < NT; ++t) {
-                acc[t][0] = fmaf(w0, xr[t][8 * c + 2 * k], acc[t][0]);
-                acc[t][1] = fmaf(w1, xr[t][8 * c + 2 * k + 1], acc[t][1]);
+              for (int k = 0; k < 4; ++k) {
+                const float w0 = bf16lo(ww[k]), w1 = bf16hi(ww[k]);
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                  acc[t][0] = fmaf(w0, xr[t][8 * c + 2 * k], acc[t][0]);
+                  acc[t][1] = fmaf(w1, xr[t][8 * c + 2 * k + 1], acc[t][1]);
+                }
               }
             }
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&empty[slot]);
-          float v[NT];
 #pragma unroll
-          for (int t = 0; t < NT; ++t) v[t] = warp_sum(acc[t][0] + acc[t][1]);
+            for (int t = 0; t < NT; ++t) v[rr][t] = acc[t][0] + acc[t][1];
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);  // the slot is no longer read
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+          const int j = warp + kConsumerWarps * rr;
+          if (j >= st.count) break;
+#pragma unroll
+          for (int t = 0; t < NT; ++t) v[rr][t] = warp_sum(v[rr][t]);
           if (lane == 0) {
             if (st.kind == kNopeRows) {
               const int n = st.first + j;
               const int h = n / kNope;
 #pragma unroll
               for (int t = 0; t < NT; ++t)
-                qn_g[((int64_t)t * H + h) * kNope + n % kNope] = f2bf_bits(v[t]);
+                qn_g[((int64_t)t * H + h) * kNope + n % kNope] = f2bf_bits(v[rr][t]);
               if (pub_h != h) {
                 if (pub_h >= 0) publish_rows(ready_g, pub_h, pub_n);
                 pub_h = h;
@@ -724,11 +737,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int t = 0; t < NT; ++t)
                 if (tok0 + t < a.batch)
                   a.q_pe[((int64_t)(tok0 + t) * H + r / kRope) * kRope + r % kRope] =
-                      f2bf_bits(v[t]);
+                      f2bf_bits(v[rr][t]);
             }
           }
-          continue;  // slot already released
         }
+        continue;  // slot already released
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
