@@ -57,102 +57,44 @@ struct Stage {
   int count;
 };
 
-struct Work {
-  int n0, n1;  // nope indices
-  int c0, c1;  // combined items (per head: 8 W_UK units, then 64 rope rows)
-};
-
 template <bool MMA>
 struct Geo {
   static constexpr int kStageRows = 16;
   static constexpr int kStageBytes = ((kStageRows * kPitch + 1023) / 1024) * 1024;
-  static constexpr int kUkPerStage = kStageBytes / kUkUnitBytes;  // 3 or 1
+  static constexpr int kUkPerStage = kStageBytes / kUkUnitBytes;  // 3
+  static_assert(kNope % kStageRows == 0 && kRope % kStageRows == 0, "stages within a head");
+  static_assert(kUkPerStage >= 3, "three W_UK units per stage");
 };
 
 __device__ __forceinline__ void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-__device__ __forceinline__ int first_item(int64_t x) {
-  const int64_t h = x / kItemBytesPerHead;
-  const int64_t local = x % kItemBytesPerHead;
-  const int64_t uk_bytes = (int64_t)kUkUnitsPerHead * kUkUnitBytes;
-  int64_t l;
-  if (local == 0) {
-    l = 0;
-  } else if (local <= uk_bytes) {
-    l = (local + kUkUnitBytes - 1) / kUkUnitBytes;
+// The stage list of one token group: H*8 stages of 16 nope rows, then H*4
+// stages of 16 rope rows, then H*3 stages of W_UK units (units 0-2, 3-5 and
+// 6-7 of each head).  Stages never straddle heads.  The absorption stages
+// come last, so whichever CTA takes one finds that head's nope rows long
+// published.
+__device__ __forceinline__ int total_stages(int H) { return 15 * H; }
+
+__device__ __forceinline__ Stage decode_stage(int idx, int H) {
+  Stage s;
+  const int n_nope = 8 * H, n_rope = 4 * H;
+  if (idx < n_nope) {
+    s.kind = kNopeRows;
+    s.first = 16 * idx;
+    s.count = 16;
+  } else if (idx < n_nope + n_rope) {
+    s.kind = kRopeRows;
+    s.first = 16 * (idx - n_nope);
+    s.count = 16;
   } else {
-    l = kUkUnitsPerHead + (local - uk_bytes + kRowBytes - 1) / kRowBytes;
-  }
-  return (int)(h * kItemsPerHead + l);
-}
-
-__device__ __forceinline__ Work cta_work(int i, int P, int H) {
-  Work w;
-  const int64_t N = (int64_t)H * kNope;
-  w.n0 = (int)(N * i / P);
-  w.n1 = (int)(N * (i + 1) / P);
-  const int64_t T = (int64_t)H * kItemBytesPerHead;
-  w.c0 = first_item(T * i / P);
-  w.c1 = first_item(T * (i + 1) / P);
-  return w;
-}
-
-// Stage order of one CTA: its nope rows, then its rope rows, then its W_UK
-// units (the absorption comes last, when every CTA's nope rows, written in
-// the first phase, are long complete).
-struct Cursor {
-  int pn;     // next nope index
-  int pc;     // next combined item
-  int phase;  // 0 nope rows, 1 rope rows, 2 W_UK units
-};
-
-__device__ __forceinline__ Cursor start_cursor(const Work& w) { return Cursor{w.n0, w.c0, 0}; }
-
-template <bool MMA>
-__device__ __forceinline__ bool next_stage(Cursor& c, const Work& w, Stage& s) {
-  using G = Geo<MMA>;
-  if (c.phase == 0) {
-    if (c.pn < w.n1) {
-      s.kind = kNopeRows;
-      s.first = c.pn;
-      s.count = min(G::kStageRows, w.n1 - c.pn);
-      c.pn += s.count;
-      return true;
-    }
-    c.phase = 1;
-    c.pc = w.c0;
-  }
-  if (c.phase == 1) {
-    while (c.pc < w.c1) {
-      const int h = c.pc / kItemsPerHead, l = c.pc % kItemsPerHead;
-      if (l < kUkUnitsPerHead) {  // skip this head's W_UK units for now
-        c.pc = h * kItemsPerHead + kUkUnitsPerHead;
-        continue;
-      }
-      s.kind = kRopeRows;
-      s.first = h * kRope + (l - kUkUnitsPerHead);
-      s.count = min(min(G::kStageRows, kItemsPerHead - l), w.c1 - c.pc);
-      c.pc += s.count;
-      return true;
-    }
-    c.phase = 2;
-    c.pc = w.c0;
-  }
-  while (c.pc < w.c1) {
-    const int h = c.pc / kItemsPerHead, l = c.pc % kItemsPerHead;
-    if (l >= kUkUnitsPerHead) {  // rope rows were streamed in phase 1
-      c.pc = (h + 1) * kItemsPerHead;
-      continue;
-    }
+    const int u = idx - n_nope - n_rope, h = u / 3, k = u % 3;
     s.kind = kUkTiles;
-    s.first = h * kUkUnitsPerHead + l;
-    s.count = min(min(G::kUkPerStage, kUkUnitsPerHead - l), w.c1 - c.pc);
-    c.pc += s.count;
-    return true;
+    s.first = h * kUkUnitsPerHead + 3 * k;
+    s.count = k == 2 ? 2 : 3;
   }
-  return false;
+  return s;
 }
 
 __device__ __forceinline__ int stage_row(const Stage& s, int j) {
@@ -324,7 +266,9 @@ struct Smem {
   static constexpr int oSs = oScratch + kScratch;  // [NT][8] + [8] floats
   static constexpr int oFull = oSs + (NT * 8 + 8) * 4;
   static constexpr int oEmpty = oFull + kStages * 8;
-  static constexpr int oFlag = oEmpty + kStages * 8;
+  static constexpr int oRbar = oEmpty + kStages * 8;  // 2 reduction barriers (MMA)
+  static constexpr int oDesc = oRbar + 16;            // stage index per ring slot
+  static constexpr int oFlag = oDesc + kStages * 4;
   static constexpr int kBytes = oFlag + 16;
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1 KiB
 };
@@ -342,12 +286,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* ss_part = reinterpret_cast<float*>(smem + S::oSs);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::oFull);
   uint64_t* empty = reinterpret_cast<uint64_t*>(smem + S::oEmpty);
+  uint64_t* rbar = reinterpret_cast<uint64_t*>(smem + S::oRbar);
+  volatile int* desc = reinterpret_cast<volatile int*>(smem + S::oDesc);
   volatile int* flag = reinterpret_cast<volatile int*>(smem + S::oFlag);  // [1]: last CTA
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int P = gridDim.x, i = blockIdx.x, grp = blockIdx.y;
   const int H = a.heads;
-  const Work w = cta_work(i, P, H);
+  const int total = total_stages(H);
   const int tok0 = grp * NT;
   uint16_t* qn_g = a.qn + (int64_t)grp * NT * H * kNope;
   uint32_t* ready_g = a.ready + grp * H;
@@ -356,7 +302,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < S::kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
+      desc[s] = -1;
     }
+    mbar_init(&rbar[0], kConsumerWarps);
+    mbar_init(&rbar[1], kConsumerWarps);
     flag[1] = 0;
     mbar_fence_init();
     prefetch_tensormap(&uk_map);
@@ -368,30 +317,63 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kConsumerWarps) {
     // ================= producer warp =================================
-    // Weights do not depend on the previous kernel: no PDL wait here.
-    Cursor cur = start_cursor(w);
-    int issued = 0;
-    Stage st;
-    while (next_stage<MMA>(cur, w, st)) {
-      const int slot = issued % S::kStages;
-      if (issued >= S::kStages) {
-        const uint32_t par = (uint32_t)(((issued / S::kStages) - 1) & 1);
+    // Stages k < kStages are assigned statically (stage k*P + i) and issued
+    // at once: weights do not depend on the previous kernel, and no scratch
+    // is touched.  Further stages are taken on demand from the group's
+    // counter, after the previous kernel (which re-arms it) has completed;
+    // faster SMs thus take more of the list.
+    int k = 0;
+    for (; k < S::kStages; ++k) {
+      const int idx = k * P + i;
+      if (idx >= total) break;
+      if (lane == 0) {
+        desc[k] = idx;
+        trace_stamp(a, 28 + k);
+      }
+      issue_stage(decode_stage(idx, H), ring + k * G::kStageBytes, &full[k], a, &uk_map, lane);
+    }
+    if (lane == 0) trace_stamp(a, 1);
+    pdl_wait();
+    const bool dynamic = k == S::kStages;
+    uint32_t grab = 0;
+    if (dynamic && lane == 0) grab = atomicAdd(a.work + grp, 1u);
+    while (true) {
+      const int slot = k % S::kStages;
+      if (k >= S::kStages) {
+        const uint32_t par = (uint32_t)(((k / S::kStages) - 1) & 1);
         int ok = 1;
         if (lane == 0) ok = mbar_wait_bounded(&empty[slot], par, kWaitLimit) ? 1 : 0;
         // On a timeout keep going (results are flagged invalid): every wait in
-        // this kernel is bounded, so it still ends; no warp leaves the stage
-        // sequence the others follow.
+        // this kernel is bounded, so it still ends.
         if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) timed_out = true;
       }
-      if (lane == 0 && issued < 20) trace_stamp(a, 28 + issued);
-      issue_stage(st, ring + slot * G::kStageBytes, &full[slot], a, &uk_map, lane);
-      ++issued;
-      if (issued == S::kStages && lane == 0) trace_stamp(a, 1);
+      int idx = -1;
+      if (dynamic) {
+        idx = S::kStages * P + (int)__shfl_sync(0xFFFFFFFFu, grab, 0);
+        if (idx >= total) idx = -1;
+      }
+      if (idx < 0) {
+        // end marker: the consumers stop at this slot
+        if (lane == 0) {
+          desc[slot] = -1;
+          mbar_arrive(&full[slot]);
+        }
+        break;
+      }
+      if (lane == 0) {
+        grab = atomicAdd(a.work + grp, 1u);  // the next grab is in flight meanwhile
+        desc[slot] = idx;
+        if (k < 20) trace_stamp(a, 28 + k);
+      }
+      issue_stage(decode_stage(idx, H), ring + slot * G::kStageBytes, &full[slot], a, &uk_map,
+                  lane);
+      ++k;
     }
     // Every issued stage is consumed; after a timeout this bounded wait also
-    // covers copies that may still be landing before the CTA exits.
+    // covers copies that may still be landing before the CTA exits.  (Stage
+    // k - kStages shared its slot with the end marker and is already done.)
     if (lane == 0) {
-      for (int s = max(0, issued - S::kStages); s < issued; ++s)
+      for (int s = max(0, k - S::kStages + 1); s < k; ++s)
         (void)mbar_wait_bounded(&full[s % S::kStages], (uint32_t)((s / S::kStages) & 1),
                                 kWaitLimit);
     }
@@ -473,29 +455,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
-    // Nope rows finished but not yet published, for head pub_h (FMA: kept by
+    // Nope rows stored but not yet published, for head pub_h (FMA: kept by
     // lane 0 of each warp for its own rows; MMA: by thread 0 for the CTA).
+    // They are published one stage later, before the next stores, when the
+    // fence finds them long written.
     int pub_h = -1, pub_n = 0;
+    int rsteps = 0;  // MMA row stages done: phase of the reduction barriers
 
     // Head whose nope q this warp holds (FMA: staged in smem; MMA: as B
     // fragments in registers) after its hand-off wait, or -1.
     int cached_h = -1;
     uint32_t bf[MMA ? NT / 8 : 1][kNope / 16][2];
 
-    Cursor cur = start_cursor(w);
-    Stage st;
-    for (int s = 0; next_stage<MMA>(cur, w, st); ++s) {
+    for (int s = 0; s <= total; ++s) {
       const int slot = s % S::kStages;
       uint8_t* buf = ring + slot * G::kStageBytes;
       if (!mbar_wait_bounded(&full[slot], (uint32_t)((s / S::kStages) & 1), kWaitLimit))
-        timed_out = true;  // keep the stage sequence; the call is flagged invalid
+        timed_out = true;  // the call is flagged invalid; every wait stays bounded
+      const int idx = desc[slot];
+      if (idx < 0 || idx >= total) break;  // end marker
+      const Stage st = decode_stage(idx, H);
       if (tid == 0) {
         if (s < 20) trace_stamp(a, 8 + s);
         if (s > 0 && s <= 16) trace_stamp(a, 47 + s);
         if (st.kind != kNopeRows) trace_stamp(a, 5);
       }
       if (st.kind != kNopeRows && pub_h >= 0) {
-        // the nope phase is over: publish what is left
         publish_rows(ready_g, pub_h, pub_n);
         pub_h = -1;
       }
@@ -643,10 +628,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           rw[(g + 8) * NT + 8 * nt + 2 * q] = acc[nt][2];
           rw[(g + 8) * NT + 8 * nt + 2 * q + 1] = acc[nt][3];
         }
-        named_barrier(kBarConsumers, kConsumers);
+        // partial sums of all warps written (bounded mbarrier wait)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&rbar[0]);
+        if (!mbar_wait_bounded(&rbar[0], (uint32_t)(rsteps & 1), kWaitLimit)) timed_out = true;
+        if (tid == 0 && pub_h >= 0) {  // the previous nope stage, before this one's stores
+          publish_rows(ready_g, pub_h, pub_n);
+          pub_h = -1;
+        }
         for (int e = tid; e < 16 * NT; e += kConsumers) {
           const int j = e / NT, t = e % NT;
-          if (j >= st.count) continue;
           float v = 0.f;
 #pragma unroll
           for (int ww = 0; ww < kConsumerWarps; ++ww) v += red[ww * 16 * NT + e];
@@ -659,26 +650,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             a.q_pe[((int64_t)(tok0 + t) * H + r / kRope) * kRope + r % kRope] = bits;
           }
         }
-        named_barrier(kBarConsumers, kConsumers);  // q stores done, red free
+        // q stores done, partial sums free again
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&rbar[1]);
+        if (!mbar_wait_bounded(&rbar[1], (uint32_t)(rsteps & 1), kWaitLimit)) timed_out = true;
+        ++rsteps;
         if (st.kind == kNopeRows && tid == 0) {
-          // count the CTA's finished rows per head; publish a head once the
-          // CTA has no more rows of it
-          for (int j = 0; j < st.count;) {
-            const int h = (st.first + j) / kNope;
-            const int upto = min(st.count, (h + 1) * kNope - st.first);
-            if (pub_h != h) {
-              if (pub_h >= 0) publish_rows(ready_g, pub_h, pub_n);
-              pub_h = h;
-              pub_n = 0;
-            }
-            pub_n += upto - j;
-            j = upto;
-          }
-          if (cur.pn >= w.n1 || (pub_h + 1) * kNope <= cur.pn) {
-            publish_rows(ready_g, pub_h, pub_n);
-            pub_h = -1;
-            pub_n = 0;
-          }
+          pub_h = st.first / kNope;
+          pub_n = st.count;
         }
         continue;  // slot already released
       } else {
@@ -722,15 +701,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (st.kind == kNopeRows) {
               const int n = st.first + j;
               const int h = n / kNope;
+              if (pub_h >= 0 && !(pub_h == h && rr == 1)) {
+                publish_rows(ready_g, pub_h, pub_n);  // an earlier stage's rows
+                pub_h = -1;
+              }
 #pragma unroll
               for (int t = 0; t < NT; ++t)
                 qn_g[((int64_t)t * H + h) * kNope + n % kNope] = f2bf_bits(v[rr][t]);
-              if (pub_h != h) {
-                if (pub_h >= 0) publish_rows(ready_g, pub_h, pub_n);
+              if (pub_h == h) {
+                ++pub_n;
+              } else {
                 pub_h = h;
-                pub_n = 0;
+                pub_n = 1;
               }
-              ++pub_n;
             } else {
               const int r = st.first + j;
 #pragma unroll
@@ -763,6 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (flag[1]) {
     for (int e = tid; e < a.groups * H; e += kThreads) a.ready[e] = 0u;
+    for (int e = tid; e < a.groups; e += kThreads) a.work[e] = 0u;
     __syncthreads();
     if (tid == 0) {
       *a.finished = 0u;
