@@ -243,12 +243,18 @@ __device__ __forceinline__ bool wait_ready(const uint32_t* ready, uint32_t targe
   return true;
 }
 
-// Publish `count` finished nope rows of head h.  Caller: one lane, after the
-// stores it covers (its own, or the CTA's behind a barrier); the fence is
-// cumulative, so those stores are visible GPU-wide before the counter moves.
-__device__ __forceinline__ void publish_rows(uint32_t* ready_g, int h, int count) {
+// Nope rows a warp (FMA: its own rows, two per stage) or the CTA (MMA: a
+// whole stage, via thread 0) stored but has not yet published: a list of
+// head indices in shared memory, each entry `rows` rows of that head.  One
+// lane publishes the whole list with a single fence when the CTA leaves its
+// nope stages, or when the list is full.
+constexpr int kPendMax = 16;
+
+__device__ __forceinline__ void flush_pending(int* list, int& n, int rows, uint32_t* ready_g) {
+  if (n == 0) return;
   __threadfence();
-  red_release_gpu_add(ready_g + h, (uint32_t)count);
+  for (int e = 0; e < n; ++e) red_release_gpu_add(ready_g + list[e], (uint32_t)rows);
+  n = 0;
 }
 
 template <int NT, bool MMA>
@@ -268,7 +274,8 @@ struct Smem {
   static constexpr int oEmpty = oFull + kStages * 8;
   static constexpr int oRbar = oEmpty + kStages * 8;  // 2 reduction barriers (MMA)
   static constexpr int oDesc = oRbar + 16;            // stage index per ring slot
-  static constexpr int oFlag = oDesc + kStages * 4;
+  static constexpr int oPend = oDesc + kStages * 4;    // [warp][kPendMax] pending heads
+  static constexpr int oFlag = oPend + kConsumerWarps * kPendMax * 4;
   static constexpr int kBytes = oFlag + 16;
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1 KiB
 };
@@ -455,11 +462,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
-    // Nope rows stored but not yet published, for head pub_h (FMA: kept by
-    // lane 0 of each warp for its own rows; MMA: by thread 0 for the CTA).
-    // They are published one stage later, before the next stores, when the
-    // fence finds them long written.
-    int pub_h = -1, pub_n = 0;
+    // Pending nope publications (see flush_pending): kept by lane 0 of each
+    // warp (FMA) or by thread 0 (MMA).
+    int* pend = reinterpret_cast<int*>(smem + S::oPend) + warp * kPendMax;
+    int npend = 0;
+    constexpr int kPendRows = MMA ? 16 : 2;
     int rsteps = 0;  // MMA row stages done: phase of the reduction barriers
 
     // Head whose nope q this warp holds (FMA: staged in smem; MMA: as B
@@ -480,10 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (s > 0 && s <= 16) trace_stamp(a, 47 + s);
         if (st.kind != kNopeRows) trace_stamp(a, 5);
       }
-      if (st.kind != kNopeRows && pub_h >= 0) {
-        publish_rows(ready_g, pub_h, pub_n);
-        pub_h = -1;
-      }
+      if (st.kind != kNopeRows) flush_pending(pend, npend, kPendRows, ready_g);
 
       if (st.kind == kUkTiles) {
         // ---- absorption of one head's nope q through W_UK tiles -------
@@ -632,10 +636,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&rbar[0]);
         if (!mbar_wait_bounded(&rbar[0], (uint32_t)(rsteps & 1), kWaitLimit)) timed_out = true;
-        if (tid == 0 && pub_h >= 0) {  // the previous nope stage, before this one's stores
-          publish_rows(ready_g, pub_h, pub_n);
-          pub_h = -1;
-        }
         for (int e = tid; e < 16 * NT; e += kConsumers) {
           const int j = e / NT, t = e % NT;
           float v = 0.f;
@@ -656,8 +656,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait_bounded(&rbar[1], (uint32_t)(rsteps & 1), kWaitLimit)) timed_out = true;
         ++rsteps;
         if (st.kind == kNopeRows && tid == 0) {
-          pub_h = st.first / kNope;
-          pub_n = st.count;
+          // every thread's q stores precede the barrier above
+          pend[npend++] = st.first / kNope;
+          if (npend == kPendMax) flush_pending(pend, npend, kPendRows, ready_g);
         }
         continue;  // slot already released
       } else {
@@ -701,18 +702,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (st.kind == kNopeRows) {
               const int n = st.first + j;
               const int h = n / kNope;
-              if (pub_h >= 0 && !(pub_h == h && rr == 1)) {
-                publish_rows(ready_g, pub_h, pub_n);  // an earlier stage's rows
-                pub_h = -1;
-              }
 #pragma unroll
               for (int t = 0; t < NT; ++t)
                 qn_g[((int64_t)t * H + h) * kNope + n % kNope] = f2bf_bits(v[rr][t]);
-              if (pub_h == h) {
-                ++pub_n;
-              } else {
-                pub_h = h;
-                pub_n = 1;
+              if (rr == 1) {  // both rows of this warp stored (one head per stage)
+                pend[npend++] = h;
+                if (npend == kPendMax) flush_pending(pend, npend, kPendRows, ready_g);
               }
             } else {
               const int r = st.first + j;
@@ -729,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
     }
-    if (pub_h >= 0) publish_rows(ready_g, pub_h, pub_n);
+    flush_pending(pend, npend, kPendRows, ready_g);
     if (tid == 0) trace_stamp(a, 6);
   }
 
