@@ -39,11 +39,15 @@ class MlaError(RuntimeError):
         self.code = code
 
 
-def load(path: str = LIB_PATH) -> ctypes.CDLL:
-    """Load the library once; raises if it has not been built."""
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load the library once; raises if it has not been built.  The path
+    defaults to the in-tree build; $MLA_QUERY_LIB selects another build of
+    the same sources (for example an instrumented one)."""
     global _lib
     if _lib is not None:
         return _lib
+    if path is None:
+        path = os.environ.get("MLA_QUERY_LIB", LIB_PATH)
     if not os.path.exists(path):
         raise RuntimeError(
             f"{path} not found: build it with `python -m mla_query_projection_gb300.build` "
