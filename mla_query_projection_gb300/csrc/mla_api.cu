@@ -21,7 +21,6 @@ struct mla_query {
   void* scratch;  // one cudaMalloc: err | finished | ready[] | qn[]
   uint32_t* err;
   uint32_t* finished;
-  uint32_t* work;
   uint32_t* ready;
   uint16_t* qn;
   uint64_t* trace;  // MLA_TRACE builds: per-CTA timeline stamps
@@ -130,7 +129,6 @@ int mla_query_create(mla_query_t* out, int num_heads, const void* w_qb, const vo
     uint8_t* base = static_cast<uint8_t*>(h->scratch);
     h->err = reinterpret_cast<uint32_t*>(base);
     h->finished = reinterpret_cast<uint32_t*>(base + 4);
-    h->work = reinterpret_cast<uint32_t*>(base + 8);  // [groups], groups <= 34
     h->ready = reinterpret_cast<uint32_t*>(base + head);
     h->qn = reinterpret_cast<uint16_t*>(base + qn_off);
   }
@@ -214,7 +212,6 @@ int mla_query_decode(mla_query_t h, int batch, const void* q_a, int64_t q_a_stri
   a.qn = h->qn;
   a.ready = h->ready;
   a.finished = h->finished;
-  a.work = h->work;
   a.err = h->err;
   a.heads = h->heads;
   a.batch = batch;

@@ -70,29 +70,31 @@ __device__ __forceinline__ void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-// The stage list of one token group: H*8 stages of 16 nope rows, then H*4
-// stages of 16 rope rows, then H*3 stages of W_UK units (units 0-2, 3-5 and
-// 6-7 of each head).  Stages never straddle heads.  The absorption stages
-// come last, so whichever CTA takes one finds that head's nope rows long
-// published.
+// The stage list of one token group: H*8 stages of 16 nope rows, then H*3
+// stages of W_UK units (units 0-2, 3-5 and 6-7 of each head), then H*4
+// stages of 16 rope rows.  Stages never straddle heads.  CTA i takes stages
+// i, i+P, i+2P, ...: every CTA streams nope rows first; by the time a CTA
+// reaches the absorption of head h, the nope rows of h were taken at least
+// a round earlier, and the rope rows it streams afterwards keep its copy
+// queue busy while it waits.
 __device__ __forceinline__ int total_stages(int H) { return 15 * H; }
 
 __device__ __forceinline__ Stage decode_stage(int idx, int H) {
   Stage s;
-  const int n_nope = 8 * H, n_rope = 4 * H;
+  const int n_nope = 8 * H, n_uk = 3 * H;
   if (idx < n_nope) {
     s.kind = kNopeRows;
     s.first = 16 * idx;
     s.count = 16;
-  } else if (idx < n_nope + n_rope) {
-    s.kind = kRopeRows;
-    s.first = 16 * (idx - n_nope);
-    s.count = 16;
-  } else {
-    const int u = idx - n_nope - n_rope, h = u / 3, k = u % 3;
+  } else if (idx < n_nope + n_uk) {
+    const int u = idx - n_nope, h = u / 3, k = u % 3;
     s.kind = kUkTiles;
     s.first = h * kUkUnitsPerHead + 3 * k;
     s.count = k == 2 ? 2 : 3;
+  } else {
+    s.kind = kRopeRows;
+    s.first = 16 * (idx - n_nope - n_uk);
+    s.count = 16;
   }
   return s;
 }
@@ -257,16 +259,41 @@ __device__ __forceinline__ void flush_pending(int* list, int& n, int rows, uint3
   n = 0;
 }
 
+// End of a CTA's nope stages: publish every pending row.  In the MMA
+// flavour thread 0 publishes for the CTA, so the consumer warps first meet
+// at `sync_bar` (used once per call): every warp's q stores precede it.
+template <bool MMA>
+__device__ __forceinline__ void leave_nope(int* pend, int& npend, int& last_h, uint64_t* sync_bar,
+                                           int lane, int tid, uint32_t* ready_g, bool& timed_out) {
+  if constexpr (MMA) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sync_bar);
+    if (!mbar_wait_bounded(sync_bar, 0u, kWaitLimit)) timed_out = true;
+    if (tid == 0 && last_h >= 0) {
+      pend[npend++] = last_h;
+      last_h = -1;
+    }
+    flush_pending(pend, npend, 16, ready_g);
+  } else {
+    (void)last_h;
+    (void)sync_bar;
+    (void)lane;
+    (void)tid;
+    (void)timed_out;
+    flush_pending(pend, npend, 2, ready_g);
+  }
+}
+
 template <int NT, bool MMA>
 struct Smem {
   using G = Geo<MMA>;
-  static constexpr int kStages = NT <= 8 ? 4 : 3;
+  static constexpr int kStages = MMA ? 3 : 4;
   static constexpr int kRing = kStages * G::kStageBytes;
   static constexpr int kXq = NT * kPitch;
   // FMA: per-warp staged q of one head [warp][NT][128] FP32; MMA: split-K
-  // partial sums [warp][16 rows][NT] FP32.
+  // partial sums [2 buffers][warp][16 rows][NT] FP32.
   static constexpr int kScratch =
-      MMA ? kConsumerWarps * 16 * NT * 4 : kConsumerWarps * NT * kNope * 4;
+      MMA ? 2 * kConsumerWarps * 16 * NT * 4 : kConsumerWarps * NT * kNope * 4;
   static constexpr int oXq = kRing;
   static constexpr int oScratch = oXq + kXq;
   static constexpr int oSs = oScratch + kScratch;  // [NT][8] + [8] floats
@@ -324,26 +351,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kConsumerWarps) {
     // ================= producer warp =================================
-    // Stages k < kStages are assigned statically (stage k*P + i) and issued
-    // at once: weights do not depend on the previous kernel, and no scratch
-    // is touched.  Further stages are taken on demand from the group's
-    // counter, after the previous kernel (which re-arms it) has completed;
-    // faster SMs thus take more of the list.
+    // Stage k of this CTA is stage k*P + i of the list.  Weights do not
+    // depend on the previous kernel and the producer touches no scratch, so
+    // it starts streaming without waiting for it.
     int k = 0;
-    for (; k < S::kStages; ++k) {
-      const int idx = k * P + i;
-      if (idx >= total) break;
-      if (lane == 0) {
-        desc[k] = idx;
-        trace_stamp(a, 28 + k);
-      }
-      issue_stage(decode_stage(idx, H), ring + k * G::kStageBytes, &full[k], a, &uk_map, lane);
-    }
-    if (lane == 0) trace_stamp(a, 1);
-    pdl_wait();
-    const bool dynamic = k == S::kStages;
-    uint32_t grab = 0;
-    if (dynamic && lane == 0) grab = atomicAdd(a.work + grp, 1u);
     while (true) {
       const int slot = k % S::kStages;
       if (k >= S::kStages) {
@@ -354,12 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // this kernel is bounded, so it still ends.
         if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) timed_out = true;
       }
-      int idx = -1;
-      if (dynamic) {
-        idx = S::kStages * P + (int)__shfl_sync(0xFFFFFFFFu, grab, 0);
-        if (idx >= total) idx = -1;
-      }
-      if (idx < 0) {
+      const int idx = k * P + i;
+      if (idx >= total) {
         // end marker: the consumers stop at this slot
         if (lane == 0) {
           desc[slot] = -1;
@@ -368,9 +375,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       if (lane == 0) {
-        grab = atomicAdd(a.work + grp, 1u);  // the next grab is in flight meanwhile
         desc[slot] = idx;
         if (k < 20) trace_stamp(a, 28 + k);
+        if (k == S::kStages) trace_stamp(a, 1);
       }
       issue_stage(decode_stage(idx, H), ring + slot * G::kStageBytes, &full[slot], a, &uk_map,
                   lane);
@@ -467,7 +474,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int* pend = reinterpret_cast<int*>(smem + S::oPend) + warp * kPendMax;
     int npend = 0;
     constexpr int kPendRows = MMA ? 16 : 2;
-    int rsteps = 0;  // MMA row stages done: phase of the reduction barriers
+    int last_h = -1;      // MMA: head of the last nope stage, listed after the next barrier
+    bool in_nope = true;  // still in this CTA's nope stages
+    int rsteps = 0;       // MMA row stages done: buffer and phase of the reduction
 
     // Head whose nope q this warp holds (FMA: staged in smem; MMA: as B
     // fragments in registers) after its hand-off wait, or -1.
@@ -487,7 +496,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (s > 0 && s <= 16) trace_stamp(a, 47 + s);
         if (st.kind != kNopeRows) trace_stamp(a, 5);
       }
-      if (st.kind != kNopeRows) flush_pending(pend, npend, kPendRows, ready_g);
+      if (in_nope && st.kind != kNopeRows) {
+        in_nope = false;
+        leave_nope<MMA>(pend, npend, last_h, &rbar[1], lane, tid, ready_g, timed_out);
+      }
 
       if (st.kind == kUkTiles) {
         // ---- absorption of one head's nope q through W_UK tiles -------
@@ -604,7 +616,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else if constexpr (MMA) {
         // ---- Q_B rows, tensor cores, K split over the warps ----------
-        float* red = reinterpret_cast<float*>(smem + S::oScratch);
+        // partial sums, double-buffered: one barrier per stage suffices
+        float* red = reinterpret_cast<float*>(smem + S::oScratch) + (rsteps & 1) * (kConsumerWarps * 16 * NT);
         const int g = lane >> 2, q = lane & 3;
         float acc[NT / 8][4];
 #pragma unroll
@@ -632,10 +645,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           rw[(g + 8) * NT + 8 * nt + 2 * q] = acc[nt][2];
           rw[(g + 8) * NT + 8 * nt + 2 * q + 1] = acc[nt][3];
         }
-        // partial sums of all warps written (bounded mbarrier wait)
+        // partial sums of all warps written (bounded mbarrier wait); also
+        // orders every warp's q stores of the previous stage before it
         __syncwarp();
         if (lane == 0) mbar_arrive(&rbar[0]);
         if (!mbar_wait_bounded(&rbar[0], (uint32_t)(rsteps & 1), kWaitLimit)) timed_out = true;
+        if (tid == 0 && last_h >= 0) {
+          pend[npend++] = last_h;
+          last_h = -1;
+          if (npend == kPendMax) flush_pending(pend, npend, kPendRows, ready_g);
+        }
         for (int e = tid; e < 16 * NT; e += kConsumers) {
           const int j = e / NT, t = e % NT;
           float v = 0.f;
@@ -650,16 +669,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             a.q_pe[((int64_t)(tok0 + t) * H + r / kRope) * kRope + r % kRope] = bits;
           }
         }
-        // q stores done, partial sums free again
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&rbar[1]);
-        if (!mbar_wait_bounded(&rbar[1], (uint32_t)(rsteps & 1), kWaitLimit)) timed_out = true;
         ++rsteps;
-        if (st.kind == kNopeRows && tid == 0) {
-          // every thread's q stores precede the barrier above
-          pend[npend++] = st.first / kNope;
-          if (npend == kPendMax) flush_pending(pend, npend, kPendRows, ready_g);
-        }
+        if (st.kind == kNopeRows && tid == 0) last_h = st.first / kNope;
         continue;  // slot already released
       } else {
         // ---- Q_B rows, FP32 FMA: warp w owns rows w and w + 8 -----------
@@ -724,7 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
     }
-    flush_pending(pend, npend, kPendRows, ready_g);
+    if (in_nope) leave_nope<MMA>(pend, npend, last_h, &rbar[1], lane, tid, ready_g, timed_out);
     if (tid == 0) trace_stamp(a, 6);
   }
 
@@ -741,7 +752,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (flag[1]) {
     for (int e = tid; e < a.groups * H; e += kThreads) a.ready[e] = 0u;
-    for (int e = tid; e < a.groups; e += kThreads) a.work[e] = 0u;
     __syncthreads();
     if (tid == 0) {
       *a.finished = 0u;

@@ -54,7 +54,6 @@ struct DecodeArgs {
   uint16_t* qn;              // [groups][NT][H][128] BF16 nope values
   uint32_t* ready;           // [groups][H] nope rows finished per head
   uint32_t* finished;        // [1] CTAs finished (last one re-arms the counters)
-  uint32_t* work;            // [groups] next dynamically assigned stage
   uint32_t* err;             // [1] MLA_DEVERR_* bits
   int heads;
   int batch;

@@ -19,7 +19,7 @@
 namespace {
 
 // Layout of the array: [0, 256) error word (unused when the caller passes
-// its own flag word), CTA counter and stage counters; [256, 256 + kReadyBytes) per-head
+// its own flag word) and CTA counter; [256, 256 + kReadyBytes) per-head
 // counters; then the q hand-off buffer [tokens][heads][128] BF16.
 constexpr size_t kHeaderBytes = 256;
 constexpr size_t kMaxGroups = MLA_NOALLOC_MAX_BATCH / 16;  // 16 tokens per CTA above 8
@@ -159,7 +159,6 @@ extern "C" MLA_API int mla_query_decode_noalloc(
   a.err = device_flags != nullptr ? reinterpret_cast<uint32_t*>(device_flags)
                                   : reinterpret_cast<uint32_t*>(base);
   a.finished = reinterpret_cast<uint32_t*>(base + 4);
-  a.work = reinterpret_cast<uint32_t*>(base + 8);
   a.ready = reinterpret_cast<uint32_t*>(base + kHeaderBytes);
   a.qn = reinterpret_cast<uint16_t*>(base + kHeaderBytes + kReadyBytes);
   a.heads = num_heads;
