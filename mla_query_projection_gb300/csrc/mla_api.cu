@@ -25,6 +25,8 @@ struct mla_query {
   uint16_t* qn;
   uint64_t* trace;  // MLA_TRACE builds: per-CTA timeline stamps
   uint8_t* w_uk_packed;  // library-owned repacked copy of W_UK
+  float* partial;        // absorbing kernel: FP32 partial absorptions
+  mla::AbsSplit split;   // absorbing kernel: per-CTA ranges
 };
 
 namespace {
@@ -132,6 +134,16 @@ int mla_query_create(mla_query_t* out, int num_heads, const void* w_qb, const vo
     h->ready = reinterpret_cast<uint32_t*>(base + head);
     h->qn = reinterpret_cast<uint16_t*>(base + qn_off);
   }
+  if (h->num_sms > mla::kMaxCtas) {
+    rc = MLA_EUNSUPPORTED;
+    goto fail;
+  }
+  mla::make_abs_split(num_heads, h->num_sms, &h->split);
+  if (cudaMalloc(&h->partial, (size_t)num_heads * 8 * 2 * mla::kKvLora * sizeof(float)) !=
+      cudaSuccess) {
+    rc = MLA_ENOMEM;
+    goto fail;
+  }
   // W_UK copy in contiguous pre-swizzled units (one 1-D bulk copy per unit).
   if (cudaMalloc(&h->w_uk_packed, (size_t)num_heads * mla::kUkUnitsPerHead * mla::kUkUnitBytes) !=
       cudaSuccess) {
@@ -152,6 +164,7 @@ int mla_query_create(mla_query_t* out, int num_heads, const void* w_qb, const vo
   return MLA_OK;
 fail:
   if (h->scratch) cudaFree(h->scratch);
+  if (h->partial) cudaFree(h->partial);
   if (h->w_uk_packed) cudaFree(h->w_uk_packed);
   if (h->trace) cudaFree(h->trace);
   free(h);
@@ -192,6 +205,8 @@ int mla_query_decode(mla_query_t h, int batch, const void* q_a, int64_t q_a_stri
   mla::DecodeArgs a;
   a.w_qb = h->w_qb;
   a.w_uk_packed = h->w_uk_packed;
+  a.w_uk = h->w_uk;
+  a.partial = h->partial;
   a.gamma_q = h->gamma_q;
   a.gamma_kv = h->gamma_kv;
   a.q_a = static_cast<const uint16_t*>(q_a);
@@ -220,8 +235,10 @@ int mla_query_decode(mla_query_t h, int batch, const void* q_a, int64_t q_a_stri
   a.trace = h->trace;
   if (a.groups > h->num_sms) return MLA_EUNSUPPORTED;
 
-  cudaError_t e =
-      mla::launch_fused(a, &h->uk_map, nt, mma, h->num_sms, static_cast<cudaStream_t>(stream));
+  cudaError_t e = mma ? mla::launch_fused(a, &h->uk_map, nt, mma, h->num_sms,
+                                          static_cast<cudaStream_t>(stream))
+                      : mla::launch_absorb(a, h->split, nt, h->num_sms,
+                                           static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {
     cudaGetLastError();
     return MLA_ECUDA;
@@ -274,6 +291,7 @@ void mla_query_destroy(mla_query_t h) {
   if (h->trace) cudaFree(h->trace);
   if (h->scratch) cudaFree(h->scratch);
   if (h->w_uk_packed) cudaFree(h->w_uk_packed);
+  if (h->partial) cudaFree(h->partial);
   free(h);
 }
 

@@ -760,6 +760,349 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ===========================================================================
+// Absorbing kernel (1-2 tokens): no hand-off between CTAs.
+//
+// A "task" is 16 consecutive nope rows of one head (48 KiB of W_QB) together
+// with the same 16 rows of that head's W_UK (16 KiB, contiguous in the
+// caller's [H][128][512] layout).  The CTA computes the 16 BF16 q values, then
+// their contribution to all 512 latent columns, and stores that FP32 partial
+// sum.  A per-head counter finds the last of a head's 8 tasks; that CTA's
+// finisher warp adds the 8 partials in task order and writes q_latent.  Rope
+// rows stream after a CTA's tasks and go straight to q_pe.  Each CTA owns a
+// contiguous run of tasks and of rope rows, balanced in bytes on the host.
+// ===========================================================================
+
+constexpr int kTaskRows = 16;
+constexpr int kTasksPerHead = kNope / kTaskRows;              // 8
+constexpr int kTaskUkBytes = kTaskRows * kKvLora * 2;         // 16 KiB
+constexpr int kTaskQbBytes = kTaskRows * kPitch;              // 50176
+constexpr int kTaskStage = kTaskQbBytes + kTaskUkBytes;       // 66560
+constexpr int kAbsStages = 3;
+constexpr int kAbsThreads = kConsumers + 64;                  // + producer + finisher
+constexpr int kSigRing = 4;                                   // consumer -> finisher signals
+
+template <int NT>
+struct AbsSmem {
+  static constexpr int kRing = kAbsStages * kTaskStage;
+  static constexpr int oXq = kRing;
+  static constexpr int oQ16 = oXq + NT * kPitch;                 // [2][NT][16] FP32
+  static constexpr int oSs = oQ16 + 2 * NT * kTaskRows * 4;      // [NT][8] + [8]
+  static constexpr int oFull = oSs + (NT * 8 + 8) * 4;
+  static constexpr int oEmpty = oFull + kAbsStages * 8;
+  static constexpr int oQbar = oEmpty + kAbsStages * 8;
+  static constexpr int oSig = oQbar + 8;
+  static constexpr int oFree = oSig + kSigRing * 8;
+  static constexpr int kBytes = oFree + kSigRing * 8;
+  static constexpr int kAlloc = kBytes + 128;
+};
+
+// This CTA's stages: tasks [t0, t1), then rope rows [r0, r1) in chunks of 16.
+struct AbsSeq {
+  int t0, t1, r0, r1;
+  __device__ int tasks() const { return t1 - t0; }
+  __device__ int stages() const { return (t1 - t0) + (r1 - r0 + kTaskRows - 1) / kTaskRows; }
+};
+
+__device__ __forceinline__ int rope_row(int r) {  // rope index -> W_QB row
+  return (r / kRope) * kHeadRows + kNope + (r % kRope);
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kAbsThreads, 1)
+    mla_absorb_kernel(const DecodeArgs a, const __grid_constant__ AbsSplit split) {
+  using S = AbsSmem<NT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                             ~static_cast<uintptr_t>(127));
+  uint8_t* ring = smem;
+  uint8_t* xq = smem + S::oXq;
+  float* q16 = reinterpret_cast<float*>(smem + S::oQ16);
+  float* ss_part = reinterpret_cast<float*>(smem + S::oSs);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::oFull);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + S::oEmpty);
+  uint64_t* qbar = reinterpret_cast<uint64_t*>(smem + S::oQbar);
+  uint64_t* sig = reinterpret_cast<uint64_t*>(smem + S::oSig);
+  uint64_t* sfree = reinterpret_cast<uint64_t*>(smem + S::oFree);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int i = blockIdx.x, P = gridDim.x;
+  const int H = a.heads;
+  const AbsSeq seq{split.task[i], split.task[i + 1], split.rope[i], split.rope[i + 1]};
+  const int nst = seq.stages();
+
+  if (tid == 0) {
+    for (int s = 0; s < kAbsStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    mbar_init(qbar, kConsumerWarps);
+    for (int s = 0; s < kSigRing; ++s) {
+      mbar_init(&sig[s], kConsumerWarps);
+      mbar_init(&sfree[s], 1);
+    }
+    mbar_fence_init();
+    trace_stamp(a, 0);
+  }
+  __syncthreads();
+  bool timed_out = false;
+
+  if (warp == kConsumerWarps) {
+    // ================= producer: weights only, no PDL wait ============
+    for (int k = 0; k < nst; ++k) {
+      const int slot = k % kAbsStages;
+      uint8_t* buf = ring + slot * kTaskStage;
+      if (k >= kAbsStages) {
+        int ok = 1;
+        if (lane == 0)
+          ok = mbar_wait_bounded(&empty[slot], (uint32_t)(((k / kAbsStages) - 1) & 1), kWaitLimit)
+                   ? 1 : 0;
+        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) timed_out = true;
+      }
+      if (lane == 0 && k < 20) trace_stamp(a, 28 + k);
+      if (k < seq.tasks()) {
+        const int tk = seq.t0 + k, h = tk / kTasksPerHead, p0 = (tk % kTasksPerHead) * kTaskRows;
+        if (lane == 0) mbar_arrive_expect_tx(&full[slot], kTaskRows * kRowBytes + kTaskUkBytes);
+        __syncwarp();
+        if (lane < kTaskRows)
+          bulk_g2s(buf + lane * kPitch, a.w_qb + ((int64_t)h * kHeadRows + p0 + lane) * kQLora,
+                   kRowBytes, &full[slot]);
+        else if (lane == kTaskRows)
+          bulk_g2s(buf + kTaskQbBytes, a.w_uk + ((int64_t)h * kNope + p0) * kKvLora,
+                   kTaskUkBytes, &full[slot]);
+      } else {
+        const int r = seq.r0 + (k - seq.tasks()) * kTaskRows;
+        const int n = min(kTaskRows, seq.r1 - r);
+        if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)(n * kRowBytes));
+        __syncwarp();
+        if (lane < n)
+          bulk_g2s(buf + lane * kPitch, a.w_qb + (int64_t)rope_row(r + lane) * kQLora, kRowBytes,
+                   &full[slot]);
+      }
+    }
+    if (lane == 0)
+      for (int k = max(0, nst - kAbsStages); k < nst; ++k)
+        (void)mbar_wait_bounded(&full[k % kAbsStages], (uint32_t)((k / kAbsStages) & 1),
+                                kWaitLimit);
+  } else if (warp == kConsumerWarps + 1) {
+    // ================= finisher: publish partials, close heads ========
+    pdl_wait();
+    for (int n = 0; n < seq.tasks(); ++n) {
+      const int tk = seq.t0 + n, h = tk / kTasksPerHead;
+      int last = 0;
+      if (lane == 0) {
+        if (!mbar_wait_bounded(&sig[n % kSigRing], (uint32_t)((n / kSigRing) & 1), kWaitLimit))
+          timed_out = true;
+        // the consumers' partial stores precede `sig`: make them visible GPU-wide
+        __threadfence();
+        last = atomicAdd(a.ready + h, 1u) == kTasksPerHead - 1;
+        mbar_arrive(&sfree[n % kSigRing]);
+        if (last) __threadfence();
+      }
+      last = __shfl_sync(0xFFFFFFFFu, last, 0);
+      __syncwarp();
+      if (last) {
+        // all 8 partials of head h are visible: add them in task order
+        const float* part = a.partial + (int64_t)h * kTasksPerHead * NT * kKvLora;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          for (int c4 = lane; c4 < kKvLora / 4; c4 += 32) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int pb = 0; pb < kTasksPerHead; ++pb) {
+              const float4 v = ld_cg_f32x4(part + ((int64_t)pb * NT + t) * kKvLora + 4 * c4);
+              acc.x += v.x;
+              acc.y += v.y;
+              acc.z += v.z;
+              acc.w += v.w;
+            }
+            if (t < a.batch) {
+              uint2 o;
+              o.x = pack_bf16x2(acc.x, acc.y);
+              o.y = pack_bf16x2(acc.z, acc.w);
+              *reinterpret_cast<uint2*>(a.q_latent + ((int64_t)t * H + h) * kKvLora + 4 * c4) = o;
+            }
+          }
+        }
+        if (lane == 0) a.ready[h] = 0u;  // re-armed for the next call
+      }
+    }
+  } else {
+    // ================= consumer warps 0-7 ============================
+    pdl_wait();
+    if (tid == 0) pdl_launch_dependents();
+    // q_a RMSNorm -> xq (warps 0-5); KV insert of token i (warps 6-7)
+    if (warp < 6) {
+      uint4 xv[NT];
+#pragma unroll
+      for (int t = 0; t < NT; ++t)
+        xv[t] = t < a.batch ? *reinterpret_cast<const uint4*>(a.q_a + (int64_t)t * a.q_a_stride +
+                                                               8 * tid)
+                            : make_uint4(0, 0, 0, 0);
+      const uint4 gv = *reinterpret_cast<const uint4*>(a.gamma_q + 8 * tid);
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const uint32_t ww[4] = {xv[t].x, xv[t].y, xv[t].z, xv[t].w};
+        float ss = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          ss = fmaf(bf16lo(ww[k]), bf16lo(ww[k]), ss);
+          ss = fmaf(bf16hi(ww[k]), bf16hi(ww[k]), ss);
+        }
+        ss = warp_sum(ss);
+        if (lane == 0) ss_part[t * 8 + warp] = ss;
+      }
+      named_barrier(kBarNorm, 192);
+      const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const float* sp = ss_part + t * 8;
+        const float total = ((((sp[0] + sp[1]) + sp[2]) + sp[3]) + sp[4]) + sp[5];
+        const float rr = __frsqrt_rn(__fadd_rn(__fdiv_rn(total, 1536.0f), a.eps));
+        const uint32_t ww[4] = {xv[t].x, xv[t].y, xv[t].z, xv[t].w};
+        uint4 o;
+        o.x = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[0]), rr), bf16lo(gw[0])),
+                          __fmul_rn(__fmul_rn(bf16hi(ww[0]), rr), bf16hi(gw[0])));
+        o.y = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[1]), rr), bf16lo(gw[1])),
+                          __fmul_rn(__fmul_rn(bf16hi(ww[1]), rr), bf16hi(gw[1])));
+        o.z = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[2]), rr), bf16lo(gw[2])),
+                          __fmul_rn(__fmul_rn(bf16hi(ww[2]), rr), bf16hi(gw[2])));
+        o.w = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[3]), rr), bf16lo(gw[3])),
+                          __fmul_rn(__fmul_rn(bf16hi(ww[3]), rr), bf16hi(gw[3])));
+        if (t >= a.batch) o = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(xq + t * kPitch + 16 * tid) = o;
+        if (i == 0 && a.q_c != nullptr && t < a.batch)
+          *reinterpret_cast<uint4*>(a.q_c + (int64_t)t * kQLora + 8 * tid) = o;
+      }
+    } else {
+      for (int t = i; t < NT; t += P)
+        if (t < a.batch) kv_insert(a, t, tid - 192, ss_part + NT * 8);
+    }
+    named_barrier(kBarConsumers, kConsumers);
+    if (tid == 0) trace_stamp(a, 2);
+
+    float xr[NT][48];
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int c = 0; c < 6; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(xq + t * kPitch + 2 * (256 * c + 8 * lane));
+        const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          xr[t][8 * c + 2 * k] = bf16lo(ww[k]);
+          xr[t][8 * c + 2 * k + 1] = bf16hi(ww[k]);
+        }
+      }
+
+    for (int k = 0; k < nst; ++k) {
+      const int slot = k % kAbsStages;
+      const uint8_t* buf = ring + slot * kTaskStage;
+      if (!mbar_wait_bounded(&full[slot], (uint32_t)((k / kAbsStages) & 1), kWaitLimit))
+        timed_out = true;
+      if (tid == 0 && k < 20) trace_stamp(a, 8 + k);
+      const bool task = k < seq.tasks();
+      // rows w and w + 8 of the stage: FP32 dot products with xq
+      const int nrows = task ? kTaskRows : min(kTaskRows, seq.r1 - (seq.r0 + (k - seq.tasks()) * kTaskRows));
+      float v[2][NT];
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const int j = warp + kConsumerWarps * rr;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) v[rr][t] = 0.f;
+        if (j < nrows) {
+          const uint8_t* rowp = buf + j * kPitch;
+          float acc[NT][2];
+#pragma unroll
+          for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = 0.f;
+#pragma unroll
+          for (int c = 0; c < 6; ++c) {
+            const uint4 wv = *reinterpret_cast<const uint4*>(rowp + 2 * (256 * c + 8 * lane));
+            const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const float w0 = bf16lo(ww[kk]), w1 = bf16hi(ww[kk]);
+#pragma unroll
+              for (int t = 0; t < NT; ++t) {
+                acc[t][0] = fmaf(w0, xr[t][8 * c + 2 * kk], acc[t][0]);
+                acc[t][1] = fmaf(w1, xr[t][8 * c + 2 * kk + 1], acc[t][1]);
+              }
+            }
+          }
+#pragma unroll
+          for (int t = 0; t < NT; ++t) v[rr][t] = warp_sum(acc[t][0] + acc[t][1]);
+        }
+      }
+      if (!task) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        if (lane == 0) {
+          const int r0 = seq.r0 + (k - seq.tasks()) * kTaskRows;
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            const int j = warp + kConsumerWarps * rr;
+            if (j < nrows) {
+              const int r = r0 + j;
+#pragma unroll
+              for (int t = 0; t < NT; ++t)
+                if (t < a.batch)
+                  a.q_pe[((int64_t)t * H + r / kRope) * kRope + r % kRope] = f2bf_bits(v[rr][t]);
+            }
+          }
+        }
+        continue;
+      }
+      // ---- task: share the 16 BF16-rounded q values, absorb them --------
+      const int n = k, tk = seq.t0 + k;
+      float* qb = q16 + (n & 1) * NT * kTaskRows;
+      if (lane == 0) {
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+          for (int t = 0; t < NT; ++t) qb[t * kTaskRows + warp + kConsumerWarps * rr] = bf_round(v[rr][t]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qbar);
+      if (!mbar_wait_bounded(qbar, (uint32_t)(n & 1), kWaitLimit)) timed_out = true;
+      // this lane: latent columns c, c + 1 with c = 64 w + 2 lane
+      const int c = 64 * warp + 2 * lane;
+      const uint8_t* uk = buf + kTaskQbBytes;
+      float acc[NT][2];
+#pragma unroll
+      for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = 0.f;
+#pragma unroll
+      for (int p = 0; p < kTaskRows; ++p) {
+        const uint32_t wv = *reinterpret_cast<const uint32_t*>(uk + p * (kKvLora * 2) + 2 * c);
+        const float w0 = bf16lo(wv), w1 = bf16hi(wv);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          acc[t][0] = fmaf(qb[t * kTaskRows + p], w0, acc[t][0]);
+          acc[t][1] = fmaf(qb[t * kTaskRows + p], w1, acc[t][1]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);  // W_QB and W_UK of the slot are read
+      float* part = a.partial + ((int64_t)tk * NT) * kKvLora;
+#pragma unroll
+      for (int t = 0; t < NT; ++t)
+        *reinterpret_cast<float2*>(part + (int64_t)t * kKvLora + c) = make_float2(acc[t][0], acc[t][1]);
+      // signal the finisher (its ring slot must have been consumed)
+      __syncwarp();
+      if (lane == 0) {
+        if (n >= kSigRing &&
+            !mbar_wait_bounded(&sfree[n % kSigRing], (uint32_t)(((n / kSigRing) - 1) & 1), kWaitLimit))
+          timed_out = true;
+        mbar_arrive(&sig[n % kSigRing]);
+      }
+    }
+    if (tid == 0) trace_stamp(a, 6);
+  }
+
+  if (timed_out) atomicOr(a.err, MLA_DEVERR_TIMEOUT);
+  __syncthreads();
+  if (tid == 0) trace_stamp(a, 7);
+}
+
 template <int NT, bool MMA>
 cudaError_t launch_one(const DecodeArgs& a, const CUtensorMap* map, int num_sms,
                        cudaStream_t stream) {
@@ -816,13 +1159,64 @@ cudaError_t repack_w_uk(const uint16_t* w_uk, uint8_t* dst, int heads, cudaStrea
   return cudaGetLastError();
 }
 
+void make_abs_split(int heads, int ctas, AbsSplit* sp) {
+  // tasks: even split; rope rows: fill each CTA up to an even share of bytes
+  const int64_t tasks = (int64_t)heads * kTasksPerHead, rope = (int64_t)heads * kRope;
+  const int64_t tb = kTaskRows * kRowBytes + kTaskUkBytes, rb = kRowBytes;
+  const int64_t total = tasks * tb + rope * rb;
+  int prev = 0;
+  for (int i = 0; i <= ctas; ++i) {
+    const int64_t t = tasks * i / ctas;
+    sp->task[i] = (uint16_t)t;
+    int64_t r = (total * i / ctas - t * tb + rb / 2) / rb;
+    if (r < prev) r = prev;
+    if (r > rope) r = rope;
+    if (i == ctas) r = rope;
+    sp->rope[i] = (uint16_t)r;
+    prev = (int)r;
+  }
+}
+
+template <int NT>
+cudaError_t launch_abs(const DecodeArgs& a, const AbsSplit& sp, int ctas, cudaStream_t stream) {
+  using S = AbsSmem<NT>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ctas, 1, 1);
+  cfg.blockDim = dim3(kAbsThreads, 1, 1);
+  cfg.dynamicSmemBytes = S::kAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_absorb_kernel<NT>, a, sp);
+}
+
+template <int NT>
+cudaError_t prepare_abs() {
+  using S = AbsSmem<NT>;
+  static_assert(S::kAlloc <= 232448, "shared memory budget");
+  return cudaFuncSetAttribute(mla_absorb_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              S::kAlloc);
+}
+
 cudaError_t prepare_fused_kernels() {
   cudaError_t e;
+  if ((e = prepare_abs<1>()) != cudaSuccess) return e;
+  if ((e = prepare_abs<2>()) != cudaSuccess) return e;
   if ((e = prepare_one<1, false>()) != cudaSuccess) return e;
   if ((e = prepare_one<2, false>()) != cudaSuccess) return e;
   if ((e = prepare_one<8, true>()) != cudaSuccess) return e;
   if ((e = prepare_one<16, true>()) != cudaSuccess) return e;
   return cudaSuccess;
+}
+
+cudaError_t launch_absorb(const DecodeArgs& a, const AbsSplit& sp, int nt, int ctas,
+                          cudaStream_t stream) {
+  if (nt == 1) return launch_abs<1>(a, sp, ctas, stream);
+  if (nt == 2) return launch_abs<2>(a, sp, ctas, stream);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_fused(const DecodeArgs& a, const CUtensorMap* map, int nt, bool mma,

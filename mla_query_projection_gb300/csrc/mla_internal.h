@@ -52,6 +52,8 @@ struct DecodeArgs {
   uint16_t* q_c;             // [B][1536] or null
   // scratch (device)
   uint16_t* qn;              // [groups][NT][H][128] BF16 nope values
+  const uint16_t* w_uk;      // [H][128][512] (absorbing kernel)
+  float* partial;            // [H*8 tasks][NT][512] FP32 partial absorptions
   uint32_t* ready;           // [groups][H] nope rows finished per head
   uint32_t* finished;        // [1] CTAs finished (last one re-arms the counters)
   uint32_t* err;             // [1] MLA_DEVERR_* bits
@@ -65,6 +67,17 @@ struct DecodeArgs {
 };
 
 constexpr int kTraceSlots = 64;
+
+// Per-CTA ranges of the absorbing kernel (tasks of 16 nope rows + W_UK rows,
+// then rope rows), computed on the host.
+constexpr int kMaxCtas = 256;
+struct AbsSplit {
+  uint16_t task[kMaxCtas + 1];
+  uint16_t rope[kMaxCtas + 1];
+};
+void make_abs_split(int heads, int ctas, AbsSplit* sp);
+cudaError_t launch_absorb(const DecodeArgs& a, const AbsSplit& sp, int nt, int ctas,
+                          cudaStream_t stream);
 
 // Scratch sizes for `heads` heads at the largest batch.
 size_t scratch_qn_elems(int heads);

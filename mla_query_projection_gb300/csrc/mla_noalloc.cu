@@ -139,6 +139,8 @@ extern "C" MLA_API int mla_query_decode_noalloc(
   mla::DecodeArgs a;
   a.w_qb = static_cast<const uint16_t*>(w_qb);
   a.w_uk_packed = nullptr;  // W_UK is read in place through the tensor map
+  a.w_uk = static_cast<const uint16_t*>(w_uk);
+  a.partial = nullptr;
   a.gamma_q = static_cast<const uint16_t*>(gamma_q);
   a.gamma_kv = static_cast<const uint16_t*>(gamma_kv);
   a.q_a = static_cast<const uint16_t*>(q_a);
