@@ -225,8 +225,7 @@ __device__ __forceinline__ void trace_stamp(const DecodeArgs& a, int slot) {
   if (a.trace != nullptr && slot < kTraceSlots) {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    uint64_t* p = a.trace + (int64_t)(blockIdx.y * gridDim.x + blockIdx.x) * kTraceSlots + slot;
-    if (*p == 0) *p = t;
+    a.trace[(int64_t)(blockIdx.y * gridDim.x + blockIdx.x) * kTraceSlots + slot] = t;
   }
 #else
   (void)a;
@@ -494,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tid == 0) {
         if (s < 20) trace_stamp(a, 8 + s);
         if (s > 0 && s <= 16) trace_stamp(a, 47 + s);
-        if (st.kind != kNopeRows) trace_stamp(a, 5);
+        if (st.kind != kNopeRows && in_nope) trace_stamp(a, 5);
       }
       if (in_nope && st.kind != kNopeRows) {
         in_nope = false;
