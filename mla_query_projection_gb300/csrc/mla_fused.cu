@@ -885,23 +885,38 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
                                 kWaitLimit);
   } else if (warp == kConsumerWarps + 1) {
     // ================= finisher: publish partials, close heads ========
+    // Takes every task whose partials are stored (up to the signal ring):
+    // one fence makes them visible GPU-wide, then one lane per task bumps
+    // that head's counter (one round trip for the batch).  A task that
+    // completes its head adds the head's 8 partials in task order.
     pdl_wait();
-    for (int n = 0; n < seq.tasks(); ++n) {
-      const int tk = seq.t0 + n, h = tk / kTasksPerHead;
-      int last = 0;
+    const int ntasks = seq.tasks();
+    for (int n = 0; n < ntasks;) {
+      int m = 0;
       if (lane == 0) {
         if (!mbar_wait_bounded(&sig[n % kSigRing], (uint32_t)((n / kSigRing) & 1), kWaitLimit))
           timed_out = true;
-        // the consumers' partial stores precede `sig`: make them visible GPU-wide
-        __threadfence();
-        last = atomicAdd(a.ready + h, 1u) == kTasksPerHead - 1;
-        mbar_arrive(&sfree[n % kSigRing]);
-        if (last) __threadfence();
+        m = 1;
+        while (m < kSigRing && n + m < ntasks &&
+               mbar_try_wait(&sig[(n + m) % kSigRing], (uint32_t)(((n + m) / kSigRing) & 1)))
+          ++m;
+        __threadfence();  // the consumers' partial stores precede `sig`
       }
-      last = __shfl_sync(0xFFFFFFFFu, last, 0);
+      m = __shfl_sync(0xFFFFFFFFu, m, 0);
+      int last = 0;
+      if (lane < m) {
+        const int h = (seq.t0 + n + lane) / kTasksPerHead;
+        last = atomicAdd(a.ready + h, 1u) == kTasksPerHead - 1;
+      }
       __syncwarp();
-      if (last) {
-        // all 8 partials of head h are visible: add them in task order
+      if (lane == 0)
+        for (int j = 0; j < m; ++j) mbar_arrive(&sfree[(n + j) % kSigRing]);
+      unsigned lastmask = __ballot_sync(0xFFFFFFFFu, last);
+      if (lastmask) __threadfence();  // acquire: the other tasks' partials are visible
+      while (lastmask) {
+        const int j = __ffs(lastmask) - 1;
+        lastmask &= lastmask - 1;
+        const int h = (seq.t0 + n + j) / kTasksPerHead;
         const float* part = a.partial + (int64_t)h * kTasksPerHead * NT * kKvLora;
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
@@ -925,6 +940,7 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
         }
         if (lane == 0) a.ready[h] = 0u;  // re-armed for the next call
       }
+      n += m;
     }
   } else {
     // ================= consumer warps 0-7 ============================
