@@ -68,10 +68,24 @@ def read_peaks() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def read_traffic(workload: str) -> float | None:
-    """DRAM bytes per launch from the committed ncu summary of this workload,
-    if it was taken on the current kernel sources."""
-    p = os.path.join(ROOT, "profiles", f"mla_fused_{workload}.txt")
+def kernel_for(path: int, batch: int) -> str:
+    """The kernel one decode step launches on the given path (MLA_PATH_FMA:
+    the absorbing kernel, one or two tokens per CTA; MLA_PATH_MMA: the
+    hand-off kernel, 8 or 16 tokens per CTA group)."""
+    if path == 1:
+        return f"mla_absorb_kernel<{1 if batch <= 1 else 2}>"
+    return f"mla_fused_kernel<{8 if batch <= 8 else 16},true>"
+
+
+def profile_name(kernel: str, workload: str) -> str:
+    base = kernel.split("<")[0]
+    return os.path.join(ROOT, "profiles", f"{base}_{workload}.txt")
+
+
+def read_traffic(kernel: str, workload: str) -> float | None:
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, if it was taken on the current kernel sources."""
+    p = profile_name(kernel, workload)
     if not os.path.exists(p):
         return None
     vals = {}
@@ -105,6 +119,33 @@ def workload_cfg(name: str) -> dict:
         lay = S.LAYOUT_DS_MLA if parts[3] == "ds" else S.LAYOUT_E4M3
         return S.sweep_workload(b, h, lay)
     raise SystemExit(f"unknown workload {name}")
+
+
+# ---------------------------------------------------------------- ranks
+
+
+def max_over_ranks(values, device=None) -> list[float]:
+    """Each value's maximum over all ranks: the slowest replica sets the time
+    of a step.  Without an initialised process group, the values themselves."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_us(per_step_us: float, world: int) -> float:
+    """Whole-job time per decode step when `world` replicas each run one step
+    in the same (max-over-ranks) time: N steps complete per per-step time."""
+    return per_step_us / world
+
+
+def runs_reference_arm(rank: int) -> bool:
+    """The oracle arm runs on rank 0 only; other ranks exit without work."""
+    return rank == 0
 
 
 # ---------------------------------------------------------------- GPU arm
@@ -276,6 +317,7 @@ def gpu_arm(args, rank: int, world: int, local_rank: int) -> dict | None:
     barrier()
     clocks = sampler.stop()
     ms = e0.elapsed_time(e1)
+    path = B.mla_query_path_for(sets[0]["handle"], Bn)
     flags = B.mla_query_get_error(sets[0]["handle"], stream)
     for w in sets[1:]:
         flags |= B.mla_query_get_error(w["handle"], stream)
@@ -323,17 +365,10 @@ def gpu_arm(args, rank: int, world: int, local_rank: int) -> dict | None:
     for w in sets:
         B.mla_query_destroy(w["handle"])
 
-    per_step_ms = ms / args.steps
-    per_step_e2e_ms = ms_e2e / K_e
-    if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([per_step_ms, per_step_e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        per_step_ms, per_step_e2e_ms = float(t[0]), float(t[1])
+    per_step_ms, per_step_e2e_ms = max_over_ranks([ms / args.steps, ms_e2e / K_e], dev)
 
     return dict(per_step_ms=per_step_ms, per_step_e2e_ms=per_step_e2e_ms, h2d=h2d, d2h=d2h,
-                clocks=clocks, nsets=nsets, l2=l2, K_e=K_e, cfg=cfg)
+                clocks=clocks, nsets=nsets, l2=l2, K_e=K_e, cfg=cfg, path=path)
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -434,7 +469,7 @@ def main():
 
     if args.impl == "reference":
         # The reference arm is the FP64 CPU oracle; rank 0 alone runs it.
-        if rank != 0:
+        if not runs_reference_arm(rank):
             return
         t_full = oracle_time(cfg, min(H, 8), 2.0)["sec_per_sample"] * H / min(H, 8)
         budget = 150.0
@@ -472,10 +507,11 @@ def main():
         return
 
     per_step_us = r["per_step_ms"] * 1e3
-    value = per_step_us / world  # whole-job time per decode step (N replicas)
+    value = whole_job_us(per_step_us, world)
     nbytes = algorithmic_bytes(Bn, H, layout)
     achieved = nbytes / (per_step_us * 1e-6) / 1e9
     peak, peak_src = read_peaks()
+    kernel = kernel_for(r["path"], Bn)
     config.update({
         "l2_policy": f"inputs larger than L2: {r['nsets']} rotating weight sets "
                      f"({r['nsets'] * H * 720 * 1024 / 1e6:.0f} MB vs L2 {r['l2'] / 1e6:.0f} MB)",
@@ -492,8 +528,8 @@ def main():
                      "frac": achieved / peak, "peak_source": f"{peak_src} (MEASURED_PEAKS hbm_gbs)",
                      "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
                      "algorithmic_bytes_per_launch": nbytes,
-                     "traffic": read_traffic(args.workload),
-                     "kernel": "mla_fused_kernel", "gflop_per_launch": algorithmic_flops(Bn, H) / 1e9},
+                     "traffic": read_traffic(kernel, args.workload),
+                     "kernel": kernel, "gflop_per_launch": algorithmic_flops(Bn, H) / 1e9},
         "e2e": {"value": r["per_step_e2e_ms"] * 1e3 / world, "unit": "us",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                 "steps": r["K_e"], "note": "eager C-ABI calls with pinned host buffers"},
