@@ -896,11 +896,13 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
       if (lane == 0) {
         if (!mbar_wait_bounded(&sig[n % kSigRing], (uint32_t)((n / kSigRing) & 1), kWaitLimit))
           timed_out = true;
+        trace_stamp(a, 51);
         m = 1;
         while (m < kSigRing && n + m < ntasks &&
                mbar_try_wait(&sig[(n + m) % kSigRing], (uint32_t)(((n + m) / kSigRing) & 1)))
           ++m;
         __threadfence();  // the consumers' partial stores precede `sig`
+        trace_stamp(a, 52);
       }
       m = __shfl_sync(0xFFFFFFFFu, m, 0);
       int last = 0;
@@ -912,7 +914,9 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
       if (lane == 0)
         for (int j = 0; j < m; ++j) mbar_arrive(&sfree[(n + j) % kSigRing]);
       unsigned lastmask = __ballot_sync(0xFFFFFFFFu, last);
+      if (lane == 0) trace_stamp(a, 48);
       if (lastmask) __threadfence();  // acquire: the other tasks' partials are visible
+      if (lastmask && lane == 0) trace_stamp(a, 53);
       while (lastmask) {
         const int j = __ffs(lastmask) - 1;
         lastmask &= lastmask - 1;
@@ -939,9 +943,11 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
           }
         }
         if (lane == 0) a.ready[h] = 0u;  // re-armed for the next call
+        if (lane == 0) trace_stamp(a, 49);
       }
       n += m;
     }
+    if (lane == 0) trace_stamp(a, 50);
   } else {
     // ================= consumer warps 0-7 ============================
     pdl_wait();
