@@ -63,8 +63,8 @@ extern "C" {
                                   that call are not valid)                     */
 
 /* Compute paths (mla_query_set_path). */
-#define MLA_PATH_AUTO 0 /* pick by batch size                               */
-#define MLA_PATH_FMA 1  /* FP32 FMA dot products (batch <= 2)                */
+#define MLA_PATH_AUTO 0 /* the default: MLA_PATH_MMA at every batch size    */
+#define MLA_PATH_FMA 1  /* FP32 FMA dot products (batch <= 2 only)           */
 #define MLA_PATH_MMA 2  /* BF16 tensor-core tiles, FP32 accumulate           */
 
 #define MLA_MAX_BATCH 256 /* largest batch one decode call accepts           */
@@ -146,7 +146,7 @@ MLA_API int mla_query_get_error(mla_query_t h, unsigned* device_flags, void* str
 
 /*
  * mla_query_set_path - force a compute path (MLA_PATH_*) for later decode
- * calls on this handle; MLA_PATH_AUTO restores the batch-size dispatch.
+ * calls on this handle; MLA_PATH_AUTO restores the default dispatch.
  * A forced path that cannot serve a batch makes decode return
  * MLA_EUNSUPPORTED.  For tests and tuning; results of every path agree within
  * the library's stated tolerance.

@@ -27,6 +27,8 @@ struct mla_query {
   uint8_t* w_uk_packed;  // library-owned repacked copy of W_UK
   float* partial;        // absorbing kernel: FP32 partial absorptions
   mla::AbsSplit split;   // absorbing kernel: per-CTA ranges
+  mla::PairSplit pair_split;  // paired absorbing kernel: per-pair heads, per-CTA rope
+  int pair_ctas;              // its grid (even), 0 if it cannot run on this device
 };
 
 namespace {
@@ -61,18 +63,33 @@ int encode_uk_map(CUtensorMap* map, const void* w_uk, int heads) {
   return r == CUDA_SUCCESS ? MLA_OK : MLA_ECUDA;
 }
 
-int pick_path(const mla_query* h, int batch, bool* mma, int* nt) {
+// The kernel a decode call launches:
+//   absorbing kernel, FP32 FMA flavour (1 or 2 tokens per CTA);
+//   absorbing kernel, tensor-core flavour (8 or 16 tokens per CTA, B <= 16);
+//   hand-off kernel, tensor cores, token groups of 8 or 16 (any B).
+enum class Kernel { kAbsorbFma, kAbsorbMma, kAbsorbPair, kHandoff };
+
+int pick_kernel(const mla_query* h, int batch, Kernel* k, int* nt) {
   int path = h->path;
-  if (path == MLA_PATH_AUTO) path = batch <= 2 ? MLA_PATH_FMA : MLA_PATH_MMA;
+  if (path == MLA_PATH_AUTO) path = MLA_PATH_MMA;  // tensor cores are faster from one token on
   if (path == MLA_PATH_FMA) {
     if (batch > 2) return MLA_EUNSUPPORTED;
-    *mma = false;
+    *k = Kernel::kAbsorbFma;
+    *nt = batch <= 1 ? 1 : 2;
   } else if (path == MLA_PATH_MMA) {
-    *mma = true;
+    if (batch <= 8 && h->pair_ctas > 0) {
+      *k = Kernel::kAbsorbPair;
+      *nt = 8;
+    } else if (batch <= 16) {
+      *k = Kernel::kAbsorbMma;
+      *nt = batch <= 8 ? 8 : 16;
+    } else {
+      *k = Kernel::kHandoff;
+      *nt = mla::tokens_per_cta(batch, true);
+    }
   } else {
     return MLA_EINVAL;
   }
-  *nt = mla::tokens_per_cta(batch, *mma);
   return MLA_OK;
 }
 
@@ -139,7 +156,12 @@ int mla_query_create(mla_query_t* out, int num_heads, const void* w_qb, const vo
     goto fail;
   }
   mla::make_abs_split(num_heads, h->num_sms, &h->split);
-  if (cudaMalloc(&h->partial, (size_t)num_heads * 8 * 2 * mla::kKvLora * sizeof(float)) !=
+  h->pair_ctas = h->num_sms & ~1;
+  if (!mla::make_pair_split(num_heads, h->pair_ctas, &h->pair_split) ||
+      !mla::pair_kernel_fits(h->pair_ctas))
+    h->pair_ctas = 0;
+  // FP32 partial absorptions of the absorbing kernels: [task][token < 16][512]
+  if (cudaMalloc(&h->partial, (size_t)num_heads * 8 * 16 * mla::kKvLora * sizeof(float)) !=
       cudaSuccess) {
     rc = MLA_ENOMEM;
     goto fail;
@@ -197,9 +219,9 @@ int mla_query_decode(mla_query_t h, int batch, const void* q_a, int64_t q_a_stri
       (reinterpret_cast<uintptr_t>(k_scale) & 3u))
     return MLA_EINVAL;
 
-  bool mma = false;
+  Kernel kern = Kernel::kAbsorbFma;
   int nt = 1;
-  int rc = pick_path(h, batch, &mma, &nt);
+  int rc = pick_kernel(h, batch, &kern, &nt);
   if (rc != MLA_OK) return rc;
 
   mla::DecodeArgs a;
@@ -235,10 +257,14 @@ int mla_query_decode(mla_query_t h, int batch, const void* q_a, int64_t q_a_stri
   a.trace = h->trace;
   if (a.groups > h->num_sms) return MLA_EUNSUPPORTED;
 
-  cudaError_t e = mma ? mla::launch_fused(a, &h->uk_map, nt, mma, h->num_sms,
-                                          static_cast<cudaStream_t>(stream))
-                      : mla::launch_absorb(a, h->split, nt, h->num_sms,
-                                           static_cast<cudaStream_t>(stream));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (kern == Kernel::kHandoff)
+    e = mla::launch_fused(a, &h->uk_map, nt, true, h->num_sms, st);
+  else if (kern == Kernel::kAbsorbPair)
+    e = mla::launch_pair(a, h->pair_split, h->pair_ctas, st);
+  else
+    e = mla::launch_absorb(a, h->split, nt, h->num_sms, st);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return MLA_ECUDA;
@@ -269,11 +295,11 @@ int mla_query_set_path(mla_query_t h, int path) {
 
 int mla_query_path_for(mla_query_t h, int batch) {
   if (h == nullptr || batch < 1 || batch > MLA_MAX_BATCH) return MLA_EINVAL;
-  bool mma = false;
+  Kernel kern = Kernel::kAbsorbFma;
   int nt = 1;
-  int rc = pick_path(h, batch, &mma, &nt);
+  int rc = pick_kernel(h, batch, &kern, &nt);
   if (rc != MLA_OK) return rc;
-  return mma ? MLA_PATH_MMA : MLA_PATH_FMA;
+  return kern == Kernel::kAbsorbFma ? MLA_PATH_FMA : MLA_PATH_MMA;
 }
 
 #ifdef MLA_TRACE

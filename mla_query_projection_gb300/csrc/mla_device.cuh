@@ -74,6 +74,30 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// L2 eviction policy under which the lines an access touches are the first
+// candidates for eviction (weights that are dead once copied to shared memory).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// bulk_g2s with an L2 cache policy for the lines it reads.
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], "
+      "%2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// Bulk prefetch of [src, src + bytes) from global memory into L2: no
+// completion, no shared memory; src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // 2-D tensor copy global -> shared through a tensor map (box set at encode).
 // x is the innermost coordinate (elements), y the row.
 __device__ __forceinline__ void tma_g2s_2d(void* dst, const CUtensorMap* map, int x, int y,
@@ -87,6 +111,34 @@ __device__ __forceinline__ void tma_g2s_2d(void* dst, const CUtensorMap* map, in
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---------------------------------------------------------------- clusters
+
+// Address, in the shared::cluster window, of the same shared-memory location
+// in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// Barrier over every thread of every CTA of the cluster (all threads call it).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// 16-byte store into another CTA's shared memory (shared::cluster address),
+// counted in bytes on that CTA's mbarrier `rbar` (shared::cluster address).
+__device__ __forceinline__ void st_async_v4(uint32_t raddr, float x, float y, float z, float w,
+                                            uint32_t rbar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, "
+      "[%5];" ::"r"(raddr),
+      "f"(x), "f"(y), "f"(z), "f"(w), "r"(rbar)
+      : "memory");
 }
 
 // ---------------------------------------------------------------- PDL

@@ -220,6 +220,18 @@ __device__ void kv_insert(const DecodeArgs& a, int b, int lt, float* red2) {
 // nope phase, 6 last stage consumed, 7 end, 8..27 the time consumer thread 0
 // saw stage s's data, 28..47 the time the producer issued stage s, 48..63 the
 // time consumer thread 0 finished stage s (s < 16).
+// Trace builds: add a cycle count to a per-CTA slot (one thread per CTA).
+__device__ __forceinline__ void trace_add(const DecodeArgs& a, int slot, long long v) {
+#ifdef MLA_TRACE
+  if (a.trace != nullptr && slot < kTraceSlots)
+    a.trace[(int64_t)(blockIdx.y * gridDim.x + blockIdx.x) * kTraceSlots + slot] += (uint64_t)v;
+#else
+  (void)a;
+  (void)slot;
+  (void)v;
+#endif
+}
+
 __device__ __forceinline__ void trace_stamp(const DecodeArgs& a, int slot) {
 #ifdef MLA_TRACE
   if (a.trace != nullptr && slot < kTraceSlots) {
@@ -778,8 +790,7 @@ constexpr int kTaskUkBytes = kTaskRows * kKvLora * 2;         // 16 KiB
 constexpr int kTaskQbBytes = kTaskRows * kPitch;              // 50176
 constexpr int kTaskStage = kTaskQbBytes + kTaskUkBytes;       // 66560
 constexpr int kAbsStages = 3;
-constexpr int kAbsThreads = kConsumers + 64;                  // + producer + finisher
-constexpr int kSigRing = 4;                                   // consumer -> finisher signals
+constexpr int kAbsThreads = kConsumers + 32;                  // + producer warp
 
 template <int NT>
 struct AbsSmem {
@@ -790,9 +801,7 @@ struct AbsSmem {
   static constexpr int oFull = oSs + (NT * 8 + 8) * 4;
   static constexpr int oEmpty = oFull + kAbsStages * 8;
   static constexpr int oQbar = oEmpty + kAbsStages * 8;
-  static constexpr int oSig = oQbar + 8;
-  static constexpr int oFree = oSig + kSigRing * 8;
-  static constexpr int kBytes = oFree + kSigRing * 8;
+  static constexpr int kBytes = oQbar + 8;
   static constexpr int kAlloc = kBytes + 128;
 };
 
@@ -805,6 +814,59 @@ struct AbsSeq {
 
 __device__ __forceinline__ int rope_row(int r) {  // rope index -> W_QB row
   return (r / kRope) * kHeadRows + kNope + (r % kRope);
+}
+
+// Prefetch stage k of a CTA's sequence into L2: a task's 16 W_QB rows and 16
+// W_UK rows are two contiguous runs, a rope chunk at most two (it may cross
+// into the next head).
+__device__ __forceinline__ void abs_prefetch_stage(const DecodeArgs& a, const AbsSeq& seq, int k) {
+  if (k < seq.tasks()) {
+    const int tk = seq.t0 + k, h = tk / kTasksPerHead, p0 = (tk % kTasksPerHead) * kTaskRows;
+    bulk_prefetch_l2(a.w_qb + ((int64_t)h * kHeadRows + p0) * kQLora, kTaskRows * kRowBytes);
+    bulk_prefetch_l2(a.w_uk + ((int64_t)h * kNope + p0) * kKvLora, kTaskUkBytes);
+  } else {
+    const int r = seq.r0 + (k - seq.tasks()) * kTaskRows;
+    const int n = min(kTaskRows, seq.r1 - r);
+    const int n1 = min(n, kRope - r % kRope);
+    bulk_prefetch_l2(a.w_qb + (int64_t)rope_row(r) * kQLora, (uint32_t)(n1 * kRowBytes));
+    if (n > n1)
+      bulk_prefetch_l2(a.w_qb + (int64_t)rope_row(r + n1) * kQLora, (uint32_t)((n - n1) * kRowBytes));
+  }
+}
+
+// Head closing of the absorbing kernels, launched right after them (its CTAs
+// may be resident early and wait, programmatic dependent launch):
+// q_latent[t][h][c] = BF16 of the 8 FP32 partials of head h, token t, added
+// in task order (partials laid out [task][token < NT][512]).  One thread per
+// (token, head, 4 columns).
+template <int NT>
+__global__ void __launch_bounds__(256) mla_close_kernel(const DecodeArgs a) {
+  // The next kernel may be scheduled at once (it streams static weights
+  // until its own wait, which covers this kernel's completion).
+  pdl_launch_dependents();
+  pdl_wait();  // the partials of the absorbing kernel
+  const int per_tok = a.heads * (kKvLora / 4);
+  const int items = a.batch * per_tok;
+  for (int it = blockIdx.x * blockDim.x + threadIdx.x; it < items; it += gridDim.x * blockDim.x) {
+    const int t = it / per_tok, r = it % per_tok, h = r / (kKvLora / 4), c4 = r % (kKvLora / 4);
+    const float* part = a.partial + ((int64_t)h * kTasksPerHead * NT + t) * kKvLora + 4 * c4;
+    float4 v[kTasksPerHead];
+#pragma unroll
+    for (int pb = 0; pb < kTasksPerHead; ++pb)
+      v[pb] = ld_cg_f32x4(part + (int64_t)pb * NT * kKvLora);
+    float4 acc = v[0];
+#pragma unroll
+    for (int pb = 1; pb < kTasksPerHead; ++pb) {
+      acc.x += v[pb].x;
+      acc.y += v[pb].y;
+      acc.z += v[pb].z;
+      acc.w += v[pb].w;
+    }
+    uint2 o;
+    o.x = pack_bf16x2(acc.x, acc.y);
+    o.y = pack_bf16x2(acc.z, acc.w);
+    *reinterpret_cast<uint2*>(a.q_latent + ((int64_t)t * a.heads + h) * kKvLora + 4 * c4) = o;
+  }
 }
 
 template <int NT>
@@ -821,8 +883,6 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::oFull);
   uint64_t* empty = reinterpret_cast<uint64_t*>(smem + S::oEmpty);
   uint64_t* qbar = reinterpret_cast<uint64_t*>(smem + S::oQbar);
-  uint64_t* sig = reinterpret_cast<uint64_t*>(smem + S::oSig);
-  uint64_t* sfree = reinterpret_cast<uint64_t*>(smem + S::oFree);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int i = blockIdx.x, P = gridDim.x;
@@ -836,11 +896,8 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
       mbar_init(&empty[s], kConsumerWarps);
     }
     mbar_init(qbar, kConsumerWarps);
-    for (int s = 0; s < kSigRing; ++s) {
-      mbar_init(&sig[s], kConsumerWarps);
-      mbar_init(&sfree[s], 1);
-    }
     mbar_fence_init();
+    pdl_launch_dependents();  // the head-closing kernel may be scheduled now
     trace_stamp(a, 0);
   }
   __syncthreads();
@@ -848,7 +905,16 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
 
   if (warp == kConsumerWarps) {
     // ================= producer: weights only, no PDL wait ============
+    // The first ring's worth of stages goes straight to shared memory; every
+    // later stage is prefetched into L2 at once, so HBM keeps streaming this
+    // CTA's weights while the ring is full (waiting for the previous kernel,
+    // the norm prologue).  Copies out of L2 mark their lines evict-first.
+    const uint64_t pol = l2_policy_evict_first();
     for (int k = 0; k < nst; ++k) {
+      if (k == kAbsStages) {
+        for (int kk = kAbsStages + lane; kk < nst; kk += 32) abs_prefetch_stage(a, seq, kk);
+        __syncwarp();
+      }
       const int slot = k % kAbsStages;
       uint8_t* buf = ring + slot * kTaskStage;
       if (k >= kAbsStages) {
@@ -864,94 +930,33 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
         if (lane == 0) mbar_arrive_expect_tx(&full[slot], kTaskRows * kRowBytes + kTaskUkBytes);
         __syncwarp();
         if (lane < kTaskRows)
-          bulk_g2s(buf + lane * kPitch, a.w_qb + ((int64_t)h * kHeadRows + p0 + lane) * kQLora,
-                   kRowBytes, &full[slot]);
+          bulk_g2s_hint(buf + lane * kPitch,
+                        a.w_qb + ((int64_t)h * kHeadRows + p0 + lane) * kQLora, kRowBytes,
+                        &full[slot], pol);
         else if (lane == kTaskRows)
-          bulk_g2s(buf + kTaskQbBytes, a.w_uk + ((int64_t)h * kNope + p0) * kKvLora,
-                   kTaskUkBytes, &full[slot]);
+          bulk_g2s_hint(buf + kTaskQbBytes, a.w_uk + ((int64_t)h * kNope + p0) * kKvLora,
+                        kTaskUkBytes, &full[slot], pol);
       } else {
         const int r = seq.r0 + (k - seq.tasks()) * kTaskRows;
         const int n = min(kTaskRows, seq.r1 - r);
         if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)(n * kRowBytes));
         __syncwarp();
         if (lane < n)
-          bulk_g2s(buf + lane * kPitch, a.w_qb + (int64_t)rope_row(r + lane) * kQLora, kRowBytes,
-                   &full[slot]);
+          bulk_g2s_hint(buf + lane * kPitch, a.w_qb + (int64_t)rope_row(r + lane) * kQLora,
+                        kRowBytes, &full[slot], pol);
       }
     }
     if (lane == 0)
       for (int k = max(0, nst - kAbsStages); k < nst; ++k)
         (void)mbar_wait_bounded(&full[k % kAbsStages], (uint32_t)((k / kAbsStages) & 1),
                                 kWaitLimit);
-  } else if (warp == kConsumerWarps + 1) {
-    // ================= finisher: publish partials, close heads ========
-    // Takes every task whose partials are stored (up to the signal ring):
-    // one fence makes them visible GPU-wide, then one lane per task bumps
-    // that head's counter (one round trip for the batch).  A task that
-    // completes its head adds the head's 8 partials in task order.
-    pdl_wait();
-    const int ntasks = seq.tasks();
-    for (int n = 0; n < ntasks;) {
-      int m = 0;
-      if (lane == 0) {
-        if (!mbar_wait_bounded(&sig[n % kSigRing], (uint32_t)((n / kSigRing) & 1), kWaitLimit))
-          timed_out = true;
-        trace_stamp(a, 51);
-        m = 1;
-        while (m < kSigRing && n + m < ntasks &&
-               mbar_try_wait(&sig[(n + m) % kSigRing], (uint32_t)(((n + m) / kSigRing) & 1)))
-          ++m;
-        __threadfence();  // the consumers' partial stores precede `sig`
-        trace_stamp(a, 52);
-      }
-      m = __shfl_sync(0xFFFFFFFFu, m, 0);
-      int last = 0;
-      if (lane < m) {
-        const int h = (seq.t0 + n + lane) / kTasksPerHead;
-        last = atomicAdd(a.ready + h, 1u) == kTasksPerHead - 1;
-      }
-      __syncwarp();
-      if (lane == 0)
-        for (int j = 0; j < m; ++j) mbar_arrive(&sfree[(n + j) % kSigRing]);
-      unsigned lastmask = __ballot_sync(0xFFFFFFFFu, last);
-      if (lane == 0) trace_stamp(a, 48);
-      if (lastmask) __threadfence();  // acquire: the other tasks' partials are visible
-      if (lastmask && lane == 0) trace_stamp(a, 53);
-      while (lastmask) {
-        const int j = __ffs(lastmask) - 1;
-        lastmask &= lastmask - 1;
-        const int h = (seq.t0 + n + j) / kTasksPerHead;
-        const float* part = a.partial + (int64_t)h * kTasksPerHead * NT * kKvLora;
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          for (int c4 = lane; c4 < kKvLora / 4; c4 += 32) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int pb = 0; pb < kTasksPerHead; ++pb) {
-              const float4 v = ld_cg_f32x4(part + ((int64_t)pb * NT + t) * kKvLora + 4 * c4);
-              acc.x += v.x;
-              acc.y += v.y;
-              acc.z += v.z;
-              acc.w += v.w;
-            }
-            if (t < a.batch) {
-              uint2 o;
-              o.x = pack_bf16x2(acc.x, acc.y);
-              o.y = pack_bf16x2(acc.z, acc.w);
-              *reinterpret_cast<uint2*>(a.q_latent + ((int64_t)t * H + h) * kKvLora + 4 * c4) = o;
-            }
-          }
-        }
-        if (lane == 0) a.ready[h] = 0u;  // re-armed for the next call
-        if (lane == 0) trace_stamp(a, 49);
-      }
-      n += m;
-    }
-    if (lane == 0) trace_stamp(a, 50);
   } else {
     // ================= consumer warps 0-7 ============================
+    // gamma_q is a static weight: loaded before the wait for the previous kernel
+    const uint4 gv = warp < 6 ? *reinterpret_cast<const uint4*>(a.gamma_q + 8 * tid)
+                              : make_uint4(0, 0, 0, 0);
     pdl_wait();
-    if (tid == 0) pdl_launch_dependents();
+    if (tid == 0) trace_stamp(a, 3);
     // q_a RMSNorm -> xq (warps 0-5); KV insert of token i (warps 6-7)
     if (warp < 6) {
       uint4 xv[NT];
@@ -960,7 +965,6 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
         xv[t] = t < a.batch ? *reinterpret_cast<const uint4*>(a.q_a + (int64_t)t * a.q_a_stride +
                                                                8 * tid)
                             : make_uint4(0, 0, 0, 0);
-      const uint4 gv = *reinterpret_cast<const uint4*>(a.gamma_q + 8 * tid);
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
         const uint32_t ww[4] = {xv[t].x, xv[t].y, xv[t].z, xv[t].w};
@@ -1075,6 +1079,7 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
       }
       // ---- task: share the 16 BF16-rounded q values, absorb them --------
       const int n = k, tk = seq.t0 + k;
+      (void)n;
       float* qb = q16 + (n & 1) * NT * kTaskRows;
       if (lane == 0) {
 #pragma unroll
@@ -1107,20 +1112,727 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
 #pragma unroll
       for (int t = 0; t < NT; ++t)
         *reinterpret_cast<float2*>(part + (int64_t)t * kKvLora + c) = make_float2(acc[t][0], acc[t][1]);
-      // signal the finisher (its ring slot must have been consumed)
-      __syncwarp();
-      if (lane == 0) {
-        if (n >= kSigRing &&
-            !mbar_wait_bounded(&sfree[n % kSigRing], (uint32_t)(((n / kSigRing) - 1) & 1), kWaitLimit))
-          timed_out = true;
-        mbar_arrive(&sig[n % kSigRing]);
-      }
     }
     if (tid == 0) trace_stamp(a, 6);
   }
 
   if (timed_out) atomicOr(a.err, MLA_DEVERR_TIMEOUT);
   __syncthreads();
+  if (tid == 0) trace_stamp(a, 7);
+}
+
+// ===========================================================================
+// Absorbing kernel on tensor cores (up to 16 tokens per CTA).
+//
+// The tasks, rope chunks, host split, finisher and head closing of the FMA
+// flavour above, with the arithmetic on mma.sync m16n8k16 (BF16 operands,
+// FP32 accumulate):
+//  * Q_B: a stage's 16 weight rows are the M side and the tokens the N side
+//    (8 per n-tile); warp w takes the K slice [192 w, 192 w + 192), and the
+//    eight split-K partial tiles are added in warp order after one barrier
+//    (two partial buffers alternate, so one barrier per stage suffices).
+//  * absorption: W_UK^T of the task (512 latent columns x 16 rows) is the M
+//    side, read with ldmatrix.trans from rows padded to 1040 B; the task's 16
+//    BF16-rounded q values of each token are the N side.  Warp w owns the
+//    latent columns [64 w, 64 w + 64).
+// The normalised q_a row never lives in shared memory: each lane builds the
+// B fragments of its K slice straight from q_a and keeps them in registers.
+// Both contractions use one k order for A and B: a lane's 8 consecutive K
+// values (one 16-byte load of a weight row and of its xq) feed two mma
+// k-steps, which only permutes the terms of each dot product.
+// ===========================================================================
+
+constexpr int kUkPitchM = kKvLora * 2 + 16;               // 1040 B: conflict-free ldmatrix
+constexpr int kTaskUkBytesM = kTaskRows * kUkPitchM;      // 16640
+constexpr int kTaskStageM = kTaskQbBytes + kTaskUkBytesM; // 66816
+constexpr int kRedTok = 24;  // floats per (warp, token) row of split-K partials (16 used)
+
+template <int NT>
+struct AbsMmaSmem {
+  static constexpr int kRing = kAbsStages * kTaskStageM;
+  static constexpr int kRedBuf = kConsumerWarps * NT * kRedTok;   // floats per buffer
+  static constexpr int oRed = kRing;                               // [2][warp][token][kRedTok]
+  static constexpr int oSs = oRed + 2 * kRedBuf * 4;               // [warp][NT] + [8] floats
+  static constexpr int oFull = oSs + (kConsumerWarps * NT + 8) * 4;
+  static constexpr int oEmpty = oFull + kAbsStages * 8;
+  static constexpr int oRbar = oEmpty + kAbsStages * 8;            // [2] split-K barriers
+  static constexpr int kBytes = oRbar + 16;
+  static constexpr int kAlloc = kBytes + 128;
+};
+
+template <int NT>
+__global__ void __launch_bounds__(kAbsThreads, 1)
+    mla_absorb_mma_kernel(const DecodeArgs a, const __grid_constant__ AbsSplit split) {
+  using S = AbsMmaSmem<NT>;
+  constexpr int NTL = NT / 8;  // n-tiles
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                             ~static_cast<uintptr_t>(127));
+  uint8_t* ring = smem;
+  float* redp = reinterpret_cast<float*>(smem + S::oRed);
+  float* ss_s = reinterpret_cast<float*>(smem + S::oSs);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::oFull);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + S::oEmpty);
+  uint64_t* rbar = reinterpret_cast<uint64_t*>(smem + S::oRbar);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int i = blockIdx.x, P = gridDim.x;
+  const int H = a.heads;
+  const AbsSeq seq{split.task[i], split.task[i + 1], split.rope[i], split.rope[i + 1]};
+  const int nst = seq.stages();
+
+  if (tid == 0) {
+    for (int s = 0; s < kAbsStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    mbar_init(&rbar[0], kConsumerWarps);
+    mbar_init(&rbar[1], kConsumerWarps);
+    mbar_fence_init();
+    pdl_launch_dependents();  // the head-closing kernel may be scheduled now
+    trace_stamp(a, 0);
+  }
+  __syncthreads();
+  bool timed_out = false;
+
+  if (warp == kConsumerWarps) {
+    // ================= producer: weights only, no PDL wait ============
+    // As in the FMA flavour; a task's W_UK rows land at a 1040-byte pitch.
+    const uint64_t pol = l2_policy_evict_first();
+    for (int k = 0; k < nst; ++k) {
+      if (k == kAbsStages) {
+        for (int kk = kAbsStages + lane; kk < nst; kk += 32) abs_prefetch_stage(a, seq, kk);
+        __syncwarp();
+      }
+      const int slot = k % kAbsStages;
+      uint8_t* buf = ring + slot * kTaskStageM;
+      if (k >= kAbsStages) {
+        int ok = 1;
+        if (lane == 0)
+          ok = mbar_wait_bounded(&empty[slot], (uint32_t)(((k / kAbsStages) - 1) & 1), kWaitLimit)
+                   ? 1 : 0;
+        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) timed_out = true;
+      }
+      if (lane == 0 && k < 20) trace_stamp(a, 28 + k);
+      if (k < seq.tasks()) {
+        const int tk = seq.t0 + k, h = tk / kTasksPerHead, p0 = (tk % kTasksPerHead) * kTaskRows;
+        if (lane == 0)
+          mbar_arrive_expect_tx(&full[slot], kTaskRows * kRowBytes + kTaskRows * kKvLora * 2);
+        __syncwarp();
+        if (lane < kTaskRows)
+          bulk_g2s_hint(buf + lane * kPitch,
+                        a.w_qb + ((int64_t)h * kHeadRows + p0 + lane) * kQLora, kRowBytes,
+                        &full[slot], pol);
+        else
+          bulk_g2s_hint(buf + kTaskQbBytes + (lane - kTaskRows) * kUkPitchM,
+                        a.w_uk + ((int64_t)h * kNope + p0 + lane - kTaskRows) * kKvLora,
+                        kKvLora * 2, &full[slot], pol);
+      } else {
+        const int r = seq.r0 + (k - seq.tasks()) * kTaskRows;
+        const int n = min(kTaskRows, seq.r1 - r);
+        if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)(n * kRowBytes));
+        __syncwarp();
+        if (lane < n)
+          bulk_g2s_hint(buf + lane * kPitch, a.w_qb + (int64_t)rope_row(r + lane) * kQLora,
+                        kRowBytes, &full[slot], pol);
+      }
+    }
+    if (lane == 0)
+      for (int k = max(0, nst - kAbsStages); k < nst; ++k)
+        (void)mbar_wait_bounded(&full[k % kAbsStages], (uint32_t)((k / kAbsStages) & 1),
+                                kWaitLimit);
+  } else {
+    // ================= consumer warps 0-7 ============================
+    const int g = lane >> 2, q = lane & 3;
+    // gamma_q of this lane's K slice: a static weight, loaded before the wait
+    uint4 gam[6];
+#pragma unroll
+    for (int c = 0; c < 6; ++c)
+      gam[c] = *reinterpret_cast<const uint4*>(a.gamma_q + 192 * warp + 32 * c + 8 * q);
+    pdl_wait();
+    if (tid == 0) trace_stamp(a, 3);
+    // q_a RMSNorm -> B fragments xb[nt][c] (token 8 nt + g, K 192 w + 32 c + 8 q + 0..7)
+    uint4 xb[NTL][6];
+#pragma unroll
+    for (int nt = 0; nt < NTL; ++nt) {
+      const int tok = 8 * nt + g;
+      float ss = 0.f;
+#pragma unroll
+      for (int c = 0; c < 6; ++c) {
+        xb[nt][c] = tok < a.batch
+                        ? *reinterpret_cast<const uint4*>(a.q_a + (int64_t)tok * a.q_a_stride +
+                                                          192 * warp + 32 * c + 8 * q)
+                        : make_uint4(0, 0, 0, 0);
+        const uint32_t ww[4] = {xb[nt][c].x, xb[nt][c].y, xb[nt][c].z, xb[nt][c].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          ss = fmaf(bf16lo(ww[e]), bf16lo(ww[e]), ss);
+          ss = fmaf(bf16hi(ww[e]), bf16hi(ww[e]), ss);
+        }
+      }
+      ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
+      ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 2);
+      if (q == 0) ss_s[warp * NT + tok] = ss;
+    }
+    named_barrier(kBarConsumers, kConsumers);
+#pragma unroll
+    for (int nt = 0; nt < NTL; ++nt) {
+      const int tok = 8 * nt + g;
+      float total = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) total += ss_s[w * NT + tok];
+      const float rr = __frsqrt_rn(__fadd_rn(__fdiv_rn(total, 1536.0f), a.eps));
+#pragma unroll
+      for (int c = 0; c < 6; ++c) {
+        const uint32_t ww[4] = {xb[nt][c].x, xb[nt][c].y, xb[nt][c].z, xb[nt][c].w};
+        const uint32_t gw[4] = {gam[c].x, gam[c].y, gam[c].z, gam[c].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          o[e] = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[e]), rr), bf16lo(gw[e])),
+                             __fmul_rn(__fmul_rn(bf16hi(ww[e]), rr), bf16hi(gw[e])));
+        xb[nt][c] = make_uint4(o[0], o[1], o[2], o[3]);
+        if (i == 0 && a.q_c != nullptr && tok < a.batch)
+          *reinterpret_cast<uint4*>(a.q_c + (int64_t)tok * kQLora + 192 * warp + 32 * c + 8 * q) =
+              xb[nt][c];
+      }
+    }
+    // KV insert of token i (and i + P, ...) by warps 6-7
+    if (warp >= 6)
+      for (int t = i; t < a.batch; t += P) kv_insert(a, t, tid - 192, ss_s + kConsumerWarps * NT);
+    if (tid == 0) trace_stamp(a, 2);
+
+#ifdef MLA_TRACE
+    long long ph[6] = {0, 0, 0, 0, 0, 0};
+    long long tc = clock64();
+#define MLA_PHASE(j)                   \
+  do {                                 \
+    const long long t2_ = clock64();   \
+    ph[j] += t2_ - tc;                 \
+    tc = t2_;                          \
+  } while (0)
+#else
+#define MLA_PHASE(j) \
+  do {               \
+  } while (0)
+#endif
+    for (int k = 0; k < nst; ++k) {
+      const int slot = k % kAbsStages;
+      const uint8_t* buf = ring + slot * kTaskStageM;
+      if (!mbar_wait_bounded(&full[slot], (uint32_t)((k / kAbsStages) & 1), kWaitLimit))
+        timed_out = true;
+      MLA_PHASE(0);
+      if (tid == 0 && k < 20) trace_stamp(a, 8 + k);
+      const bool task = k < seq.tasks();
+      // ---- Q_B rows of the stage over this warp's K slice ---------------
+      // Four independent accumulator chains (the 12 k-steps would otherwise
+      // wait on one another's results), added pairwise at the end.
+      float acc[NTL][4];
+      {
+        uint4 alo[6], ahi[6];
+#pragma unroll
+        for (int c = 0; c < 6; ++c) {
+          const int kb = 2 * (192 * warp + 32 * c + 8 * q);
+          alo[c] = *reinterpret_cast<const uint4*>(buf + g * kPitch + kb);
+          ahi[c] = *reinterpret_cast<const uint4*>(buf + (g + 8) * kPitch + kb);
+        }
+        float ch[NTL][4][4];
+#pragma unroll
+        for (int nt = 0; nt < NTL; ++nt)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) ch[nt][j][0] = ch[nt][j][1] = ch[nt][j][2] = ch[nt][j][3] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 6; ++c)
+#pragma unroll
+          for (int nt = 0; nt < NTL; ++nt) {
+            mma_bf16_16816(ch[nt][2 * (c & 1)], alo[c].x, ahi[c].x, alo[c].y, ahi[c].y,
+                           xb[nt][c].x, xb[nt][c].y);
+            mma_bf16_16816(ch[nt][2 * (c & 1) + 1], alo[c].z, ahi[c].z, alo[c].w, ahi[c].w,
+                           xb[nt][c].z, xb[nt][c].w);
+          }
+#pragma unroll
+        for (int nt = 0; nt < NTL; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            acc[nt][e] = (ch[nt][0][e] + ch[nt][1][e]) + (ch[nt][2][e] + ch[nt][3][e]);
+      }
+      if (!task) {  // a rope stage holds no W_UK: the slot is free now
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+      }
+      MLA_PHASE(1);
+      // ---- split-K partials -> shared, one barrier ----------------------
+      float* red = redp + (k & 1) * S::kRedBuf;
+      {
+        float* rw = red + warp * NT * kRedTok;
+#pragma unroll
+        for (int nt = 0; nt < NTL; ++nt) {
+          const int t0 = 8 * nt + 2 * q;
+          rw[t0 * kRedTok + g] = acc[nt][0];
+          rw[(t0 + 1) * kRedTok + g] = acc[nt][1];
+          rw[t0 * kRedTok + g + 8] = acc[nt][2];
+          rw[(t0 + 1) * kRedTok + g + 8] = acc[nt][3];
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rbar[k & 1]);
+      if (!mbar_wait_bounded(&rbar[k & 1], (uint32_t)((k >> 1) & 1), kWaitLimit)) timed_out = true;
+      MLA_PHASE(2);
+
+      if (!task) {
+        // ---- rope rows -> q_pe ------------------------------------------
+        const int r0 = seq.r0 + (k - seq.tasks()) * kTaskRows;
+        const int nrows = min(kTaskRows, seq.r1 - r0);
+        for (int e = tid; e < kTaskRows * NT; e += kConsumers) {
+          const int row = e & (kTaskRows - 1), tok = e >> 4;
+          if (row < nrows && tok < a.batch) {
+            float v = 0.f;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) v += red[(w * NT + tok) * kRedTok + row];
+            const int r = r0 + row;
+            a.q_pe[((int64_t)tok * H + r / kRope) * kRope + r % kRope] = f2bf_bits(v);
+          }
+        }
+        MLA_PHASE(5);
+        continue;
+      }
+      // ---- task: BF16 q of the 16 rows (B fragments of q^T), absorption --
+      uint32_t qb[NTL][2];
+#pragma unroll
+      for (int nt = 0; nt < NTL; ++nt) {
+        const int tok = 8 * nt + g;
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float* rr = red + (w * NT + tok) * kRedTok;
+          const float2 lo = *reinterpret_cast<const float2*>(rr + 2 * q);
+          const float2 hi = *reinterpret_cast<const float2*>(rr + 2 * q + 8);
+          s0 += lo.x;
+          s1 += lo.y;
+          s2 += hi.x;
+          s3 += hi.y;
+        }
+        qb[nt][0] = pack_bf16x2(s0, s1);
+        qb[nt][1] = pack_bf16x2(s2, s3);
+      }
+      const uint32_t uk = smem_u32(buf + kTaskQbBytes);
+      float d[4][NTL][4];
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        const int m = lane >> 3;
+        const int p = (lane & 7) + 8 * (m >> 1);
+        const int c = 64 * warp + 16 * mt + 8 * (m & 1);
+        uint32_t af[4];
+        ldmatrix_x4_trans(af, uk + p * kUkPitchM + 2 * c);
+#pragma unroll
+        for (int nt = 0; nt < NTL; ++nt) {
+          d[mt][nt][0] = d[mt][nt][1] = d[mt][nt][2] = d[mt][nt][3] = 0.f;
+          mma_bf16_16816(d[mt][nt], af[0], af[1], af[2], af[3], qb[nt][0], qb[nt][1]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);  // W_QB and W_UK of the slot are read
+      MLA_PHASE(3);
+      // FP32 partial absorption of this task: [task][token][512]
+      const int n = k, tk = seq.t0 + k;
+      (void)n;
+      float* part = a.partial + (int64_t)tk * NT * kKvLora;
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        const int c = 64 * warp + 16 * mt + g;
+#pragma unroll
+        for (int nt = 0; nt < NTL; ++nt) {
+          const int t0 = 8 * nt + 2 * q;
+          if (t0 < a.batch) {
+            part[(int64_t)t0 * kKvLora + c] = d[mt][nt][0];
+            part[(int64_t)t0 * kKvLora + c + 8] = d[mt][nt][2];
+          }
+          if (t0 + 1 < a.batch) {
+            part[(int64_t)(t0 + 1) * kKvLora + c] = d[mt][nt][1];
+            part[(int64_t)(t0 + 1) * kKvLora + c + 8] = d[mt][nt][3];
+          }
+        }
+      }
+      MLA_PHASE(4);
+    }
+#ifdef MLA_TRACE
+    if (lane == 0 && (warp == 0 || warp == 5))
+      for (int j = 0; j < 6; ++j) trace_add(a, (warp == 0 ? 56 : 22) + j, ph[j]);
+#endif
+#undef MLA_PHASE
+    if (tid == 0) trace_stamp(a, 6);
+  }
+
+  if (timed_out) atomicOr(a.err, MLA_DEVERR_TIMEOUT);
+  __syncthreads();
+  if (tid == 0) trace_stamp(a, 7);
+}
+
+// ===========================================================================
+// Paired absorbing kernel (tensor cores, up to 8 tokens): clusters of two CTAs.
+//
+// Both CTAs of a pair take the same heads; rank r streams nope tasks
+// 4r..4r+3 (rows 64r..64r+63) of each, with their W_UK rows, and accumulates
+// the head's absorption over its four tasks in registers.  After a head's
+// last task, the warps whose latent columns the other CTA owns (rank 0 owns
+// columns 0..255, rank 1 columns 256..511) send their FP32 sums into the
+// other CTA's shared memory (st.async, counted on its mbarrier).  After the
+// rope stages each CTA adds the two halves of its columns - rows 0..63 first,
+// then rows 64..127 - and writes q_latent.  No global scratch, no second
+// kernel, no wait on any CTA outside the pair.
+// ===========================================================================
+
+constexpr int kPairNT = 8;
+constexpr int kPairRecvBytes = 4 * 4 * 32 * 16;  // 4 warps x 4 m-tiles x 32 lanes x 16 B
+
+struct PairSmem {
+  static constexpr int NT = kPairNT;
+  static constexpr int kRing = kAbsStages * kTaskStageM;
+  static constexpr int kRedBuf = kConsumerWarps * NT * kRedTok;     // floats per buffer
+  static constexpr int oRed = kRing;                                 // [2][warp][token][kRedTok]
+  static constexpr int oRecv = oRed + 2 * kRedBuf * 4;               // [2 heads][kPairRecvBytes]
+  static constexpr int oSs = oRecv + 2 * kPairRecvBytes;             // [warp][NT] + [8] floats
+  static constexpr int oFull = oSs + (kConsumerWarps * NT + 8) * 4;
+  static constexpr int oEmpty = oFull + kAbsStages * 8;
+  static constexpr int oRbar = oEmpty + kAbsStages * 8;              // [2] split-K barriers
+  static constexpr int oRecvBar = oRbar + 16;                        // [2] received halves
+  static constexpr int kBytes = oRecvBar + 16;
+  static constexpr int kAlloc = kBytes + 128;
+};
+
+// This CTA's stages: 4 tasks per head of its pair, then rope rows [r0, r1).
+struct PairSeq {
+  int h0, nh, rank, r0, r1;
+  __device__ int tasks() const { return 4 * nh; }
+  __device__ int stages() const { return 4 * nh + (r1 - r0 + kTaskRows - 1) / kTaskRows; }
+  __device__ int head(int k) const { return h0 + k / 4; }
+  __device__ int p0(int k) const { return kTaskRows * (4 * rank + k % 4); }
+};
+
+__device__ __forceinline__ void pair_prefetch_stage(const DecodeArgs& a, const PairSeq& seq, int k) {
+  if (k < seq.tasks()) {
+    const int h = seq.head(k), p0 = seq.p0(k);
+    bulk_prefetch_l2(a.w_qb + ((int64_t)h * kHeadRows + p0) * kQLora, kTaskRows * kRowBytes);
+    bulk_prefetch_l2(a.w_uk + ((int64_t)h * kNope + p0) * kKvLora, kTaskUkBytes);
+  } else {
+    const int r = seq.r0 + (k - seq.tasks()) * kTaskRows;
+    const int n = min(kTaskRows, seq.r1 - r);
+    const int n1 = min(n, kRope - r % kRope);
+    bulk_prefetch_l2(a.w_qb + (int64_t)rope_row(r) * kQLora, (uint32_t)(n1 * kRowBytes));
+    if (n > n1)
+      bulk_prefetch_l2(a.w_qb + (int64_t)rope_row(r + n1) * kQLora, (uint32_t)((n - n1) * kRowBytes));
+  }
+}
+
+__global__ void __launch_bounds__(kAbsThreads, 1)
+    mla_absorb_pair_kernel(const DecodeArgs a, const __grid_constant__ PairSplit split) {
+  using S = PairSmem;
+  constexpr int NT = kPairNT;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                             ~static_cast<uintptr_t>(127));
+  uint8_t* ring = smem;
+  float* redp = reinterpret_cast<float*>(smem + S::oRed);
+  float* ss_s = reinterpret_cast<float*>(smem + S::oSs);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::oFull);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + S::oEmpty);
+  uint64_t* rbar = reinterpret_cast<uint64_t*>(smem + S::oRbar);
+  uint64_t* recvbar = reinterpret_cast<uint64_t*>(smem + S::oRecvBar);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int i = blockIdx.x, P = gridDim.x;
+  const int H = a.heads;
+  const int pair = i >> 1, rank = i & 1;  // cluster (2, 1, 1): rank = blockIdx.x % 2
+  const PairSeq seq{split.head[pair], split.head[pair + 1] - split.head[pair], rank,
+                    split.rope[i], split.rope[i + 1]};
+  const int nst = seq.stages();
+
+  if (tid == 0) {
+    for (int s = 0; s < kAbsStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    mbar_init(&rbar[0], kConsumerWarps);
+    mbar_init(&rbar[1], kConsumerWarps);
+    mbar_init(&recvbar[0], 1);
+    mbar_init(&recvbar[1], 1);
+    // The other CTA's sums of head j land in recv[j]: armed before the pair
+    // meets below, so no byte can arrive before its count is expected.
+    for (int j = 0; j < seq.nh; ++j) mbar_arrive_expect_tx(&recvbar[j], kPairRecvBytes);
+    mbar_fence_init();
+    pdl_launch_dependents();
+    trace_stamp(a, 0);
+  }
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers are initialised and armed
+  bool timed_out = false;
+
+  if (warp == kConsumerWarps) {
+    // ================= producer: weights only, no PDL wait ============
+    const uint64_t pol = l2_policy_evict_first();
+    for (int k = 0; k < nst; ++k) {
+      if (k == kAbsStages) {
+        for (int kk = kAbsStages + lane; kk < nst; kk += 32) pair_prefetch_stage(a, seq, kk);
+        __syncwarp();
+      }
+      const int slot = k % kAbsStages;
+      uint8_t* buf = ring + slot * kTaskStageM;
+      if (k >= kAbsStages) {
+        int ok = 1;
+        if (lane == 0)
+          ok = mbar_wait_bounded(&empty[slot], (uint32_t)(((k / kAbsStages) - 1) & 1), kWaitLimit)
+                   ? 1 : 0;
+        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) timed_out = true;
+      }
+      if (lane == 0 && k < 20) trace_stamp(a, 28 + k);
+      if (k < seq.tasks()) {
+        const int h = seq.head(k), p0 = seq.p0(k);
+        if (lane == 0)
+          mbar_arrive_expect_tx(&full[slot], kTaskRows * kRowBytes + kTaskRows * kKvLora * 2);
+        __syncwarp();
+        if (lane < kTaskRows)
+          bulk_g2s_hint(buf + lane * kPitch,
+                        a.w_qb + ((int64_t)h * kHeadRows + p0 + lane) * kQLora, kRowBytes,
+                        &full[slot], pol);
+        else
+          bulk_g2s_hint(buf + kTaskQbBytes + (lane - kTaskRows) * kUkPitchM,
+                        a.w_uk + ((int64_t)h * kNope + p0 + lane - kTaskRows) * kKvLora,
+                        kKvLora * 2, &full[slot], pol);
+      } else {
+        const int r = seq.r0 + (k - seq.tasks()) * kTaskRows;
+        const int n = min(kTaskRows, seq.r1 - r);
+        if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)(n * kRowBytes));
+        __syncwarp();
+        if (lane < n)
+          bulk_g2s_hint(buf + lane * kPitch, a.w_qb + (int64_t)rope_row(r + lane) * kQLora,
+                        kRowBytes, &full[slot], pol);
+      }
+    }
+    if (lane == 0)
+      for (int k = max(0, nst - kAbsStages); k < nst; ++k)
+        (void)mbar_wait_bounded(&full[k % kAbsStages], (uint32_t)((k / kAbsStages) & 1),
+                                kWaitLimit);
+  } else {
+    // ================= consumer warps 0-7 ============================
+    const int g = lane >> 2, q = lane & 3;
+    uint4 gam[6];
+#pragma unroll
+    for (int c = 0; c < 6; ++c)
+      gam[c] = *reinterpret_cast<const uint4*>(a.gamma_q + 192 * warp + 32 * c + 8 * q);
+    pdl_wait();
+    if (tid == 0) trace_stamp(a, 3);
+    // q_a RMSNorm -> B fragments xb[c] (token g, K 192 w + 32 c + 8 q + 0..7)
+    uint4 xb[6];
+    {
+      const int tok = g;
+      float ss = 0.f;
+#pragma unroll
+      for (int c = 0; c < 6; ++c) {
+        xb[c] = tok < a.batch ? *reinterpret_cast<const uint4*>(a.q_a + (int64_t)tok * a.q_a_stride +
+                                                               192 * warp + 32 * c + 8 * q)
+                              : make_uint4(0, 0, 0, 0);
+        const uint32_t ww[4] = {xb[c].x, xb[c].y, xb[c].z, xb[c].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          ss = fmaf(bf16lo(ww[e]), bf16lo(ww[e]), ss);
+          ss = fmaf(bf16hi(ww[e]), bf16hi(ww[e]), ss);
+        }
+      }
+      ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
+      ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 2);
+      if (q == 0) ss_s[warp * NT + tok] = ss;
+      named_barrier(kBarConsumers, kConsumers);
+      float total = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) total += ss_s[w * NT + tok];
+      const float rr = __frsqrt_rn(__fadd_rn(__fdiv_rn(total, 1536.0f), a.eps));
+#pragma unroll
+      for (int c = 0; c < 6; ++c) {
+        const uint32_t ww[4] = {xb[c].x, xb[c].y, xb[c].z, xb[c].w};
+        const uint32_t gw[4] = {gam[c].x, gam[c].y, gam[c].z, gam[c].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          o[e] = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[e]), rr), bf16lo(gw[e])),
+                             __fmul_rn(__fmul_rn(bf16hi(ww[e]), rr), bf16hi(gw[e])));
+        xb[c] = make_uint4(o[0], o[1], o[2], o[3]);
+        if (i == 0 && a.q_c != nullptr && tok < a.batch)
+          *reinterpret_cast<uint4*>(a.q_c + (int64_t)tok * kQLora + 192 * warp + 32 * c + 8 * q) =
+              xb[c];
+      }
+    }
+    if (warp >= 6)
+      for (int t = i; t < a.batch; t += P) kv_insert(a, t, tid - 192, ss_s + kConsumerWarps * NT);
+    if (tid == 0) trace_stamp(a, 2);
+
+    // Columns 64 w .. 64 w + 63 belong to rank 0 for w < 4, to rank 1 else.
+    const bool own = (warp < 4) == (rank == 0);
+    const uint32_t recv_local = smem_u32(smem + S::oRecv) +
+                                (uint32_t)((((warp & 3) * 4) * 32 + lane) * 16);
+    float dacc[4][4];   // this head's absorption over the tasks so far
+    float keep[2][4][4];  // owned sums of heads 0 and 1 of the pair
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) dacc[mt][e] = keep[0][mt][e] = keep[1][mt][e] = 0.f;
+
+    for (int k = 0; k < nst; ++k) {
+      const int slot = k % kAbsStages;
+      const uint8_t* buf = ring + slot * kTaskStageM;
+      if (!mbar_wait_bounded(&full[slot], (uint32_t)((k / kAbsStages) & 1), kWaitLimit))
+        timed_out = true;
+      if (tid == 0 && k < 20) trace_stamp(a, 8 + k);
+      const bool task = k < seq.tasks();
+      // ---- Q_B rows of the stage over this warp's K slice ---------------
+      float acc[4];
+      {
+        uint4 alo[6], ahi[6];
+#pragma unroll
+        for (int c = 0; c < 6; ++c) {
+          const int kb = 2 * (192 * warp + 32 * c + 8 * q);
+          alo[c] = *reinterpret_cast<const uint4*>(buf + g * kPitch + kb);
+          ahi[c] = *reinterpret_cast<const uint4*>(buf + (g + 8) * kPitch + kb);
+        }
+        float ch[4][4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) ch[j][0] = ch[j][1] = ch[j][2] = ch[j][3] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 6; ++c) {
+          mma_bf16_16816(ch[2 * (c & 1)], alo[c].x, ahi[c].x, alo[c].y, ahi[c].y, xb[c].x, xb[c].y);
+          mma_bf16_16816(ch[2 * (c & 1) + 1], alo[c].z, ahi[c].z, alo[c].w, ahi[c].w, xb[c].z,
+                         xb[c].w);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[e] = (ch[0][e] + ch[1][e]) + (ch[2][e] + ch[3][e]);
+      }
+      if (!task) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+      }
+      // ---- split-K partials -> shared, one barrier ----------------------
+      float* red = redp + (k & 1) * S::kRedBuf;
+      {
+        float* rw = red + warp * NT * kRedTok;
+        const int t0 = 2 * q;
+        rw[t0 * kRedTok + g] = acc[0];
+        rw[(t0 + 1) * kRedTok + g] = acc[1];
+        rw[t0 * kRedTok + g + 8] = acc[2];
+        rw[(t0 + 1) * kRedTok + g + 8] = acc[3];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rbar[k & 1]);
+      if (!mbar_wait_bounded(&rbar[k & 1], (uint32_t)((k >> 1) & 1), kWaitLimit)) timed_out = true;
+
+      if (!task) {
+        // ---- rope rows -> q_pe ------------------------------------------
+        const int r0 = seq.r0 + (k - seq.tasks()) * kTaskRows;
+        const int nrows = min(kTaskRows, seq.r1 - r0);
+        for (int e = tid; e < kTaskRows * NT; e += kConsumers) {
+          const int row = e & (kTaskRows - 1), tok = e >> 4;
+          if (row < nrows && tok < a.batch) {
+            float v = 0.f;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) v += red[(w * NT + tok) * kRedTok + row];
+            const int r = r0 + row;
+            a.q_pe[((int64_t)tok * H + r / kRope) * kRope + r % kRope] = f2bf_bits(v);
+          }
+        }
+        continue;
+      }
+      // ---- task: BF16 q of the 16 rows, absorption into dacc -------------
+      uint32_t qb0, qb1;
+      {
+        const int tok = g;
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float* rr = red + (w * NT + tok) * kRedTok;
+          const float2 lo = *reinterpret_cast<const float2*>(rr + 2 * q);
+          const float2 hi = *reinterpret_cast<const float2*>(rr + 2 * q + 8);
+          s0 += lo.x;
+          s1 += lo.y;
+          s2 += hi.x;
+          s3 += hi.y;
+        }
+        qb0 = pack_bf16x2(s0, s1);
+        qb1 = pack_bf16x2(s2, s3);
+      }
+      const int u = k & 3;  // task of the head: 0..3
+      if (u == 0) {
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) dacc[mt][0] = dacc[mt][1] = dacc[mt][2] = dacc[mt][3] = 0.f;
+      }
+      const uint32_t uk = smem_u32(buf + kTaskQbBytes);
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        const int m = lane >> 3;
+        const int p = (lane & 7) + 8 * (m >> 1);
+        const int c = 64 * warp + 16 * mt + 8 * (m & 1);
+        uint32_t af[4];
+        ldmatrix_x4_trans(af, uk + p * kUkPitchM + 2 * c);
+        mma_bf16_16816(dacc[mt], af[0], af[1], af[2], af[3], qb0, qb1);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);  // W_QB and W_UK of the slot are read
+      if (u == 3) {
+        const int j = k >> 2;  // head of the pair: 0 or 1
+        if (own) {
+#pragma unroll
+          for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if (j == 0) keep[0][mt][e] = dacc[mt][e];
+              else keep[1][mt][e] = dacc[mt][e];
+            }
+        } else {
+          // to the other CTA: same warp slot (w & 3), same lane, head slot j
+          const uint32_t peer = (uint32_t)(rank ^ 1);
+          const uint32_t rbar_remote = mapa_shared(smem_u32(&recvbar[j]), peer);
+#pragma unroll
+          for (int mt = 0; mt < 4; ++mt) {
+            const uint32_t laddr = recv_local + (uint32_t)(j * kPairRecvBytes + mt * 32 * 16);
+            st_async_v4(mapa_shared(laddr, peer), dacc[mt][0], dacc[mt][1], dacc[mt][2],
+                        dacc[mt][3], rbar_remote);
+          }
+        }
+      }
+    }
+    if (tid == 0) trace_stamp(a, 6);
+
+    // ---- owned columns: rows 0..63 (rank 0) + rows 64..127 (rank 1) ------
+    if (own) {
+      for (int j = 0; j < seq.nh; ++j) {
+        if (!mbar_wait_bounded(&recvbar[j], 0u, kWaitLimit)) timed_out = true;
+        const int h = seq.h0 + j;
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+          const float4 o = *reinterpret_cast<const float4*>(
+              smem + S::oRecv + j * kPairRecvBytes + ((((warp & 3) * 4 + mt) * 32 + lane) * 16));
+          const float pv[4] = {o.x, o.y, o.z, o.w};
+          float v[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float mine = j == 0 ? keep[0][mt][e] : keep[1][mt][e];
+            v[e] = rank == 0 ? mine + pv[e] : pv[e] + mine;
+          }
+          const int c = 64 * warp + 16 * mt + g, t0 = 2 * q;
+          if (t0 < a.batch) {
+            a.q_latent[((int64_t)t0 * H + h) * kKvLora + c] = f2bf_bits(v[0]);
+            a.q_latent[((int64_t)t0 * H + h) * kKvLora + c + 8] = f2bf_bits(v[2]);
+          }
+          if (t0 + 1 < a.batch) {
+            a.q_latent[((int64_t)(t0 + 1) * H + h) * kKvLora + c] = f2bf_bits(v[1]);
+            a.q_latent[((int64_t)(t0 + 1) * H + h) * kKvLora + c + 8] = f2bf_bits(v[3]);
+          }
+        }
+      }
+    }
+  }
+
+  if (timed_out) atomicOr(a.err, MLA_DEVERR_TIMEOUT);
+  __syncthreads();
+  // Neither CTA leaves while the other may still write into its shared memory.
+  cluster_sync();
   if (tid == 0) trace_stamp(a, 7);
 }
 
@@ -1199,6 +1911,22 @@ void make_abs_split(int heads, int ctas, AbsSplit* sp) {
 }
 
 template <int NT>
+cudaError_t launch_close(const DecodeArgs& a, int ctas, cudaStream_t stream) {
+  const int items = a.batch * a.heads * (kKvLora / 4);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)min((items + 255) / 256, 8 * ctas), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_close_kernel<NT>, a);
+}
+
+template <int NT>
 cudaError_t launch_abs(const DecodeArgs& a, const AbsSplit& sp, int ctas, cudaStream_t stream) {
   using S = AbsSmem<NT>;
   cudaLaunchConfig_t cfg = {};
@@ -1211,7 +1939,9 @@ cudaError_t launch_abs(const DecodeArgs& a, const AbsSplit& sp, int ctas, cudaSt
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_absorb_kernel<NT>, a, sp);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, mla_absorb_kernel<NT>, a, sp);
+  if (e != cudaSuccess) return e;
+  return launch_close<NT>(a, ctas, stream);
 }
 
 template <int NT>
@@ -1222,10 +1952,107 @@ cudaError_t prepare_abs() {
                               S::kAlloc);
 }
 
+template <int NT>
+cudaError_t launch_abs_mma(const DecodeArgs& a, const AbsSplit& sp, int ctas, cudaStream_t stream) {
+  using S = AbsMmaSmem<NT>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ctas, 1, 1);
+  cfg.blockDim = dim3(kAbsThreads, 1, 1);
+  cfg.dynamicSmemBytes = S::kAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, mla_absorb_mma_kernel<NT>, a, sp);
+  if (e != cudaSuccess) return e;
+  return launch_close<NT>(a, ctas, stream);
+}
+
+template <int NT>
+cudaError_t prepare_abs_mma() {
+  using S = AbsMmaSmem<NT>;
+  static_assert(S::kAlloc <= 232448, "shared memory budget");
+  return cudaFuncSetAttribute(mla_absorb_mma_kernel<NT>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, S::kAlloc);
+}
+
+bool make_pair_split(int heads, int ctas, PairSplit* sp) {
+  const int pairs = ctas / 2;
+  if (pairs < 1 || ctas > kMaxCtas) return false;
+  for (int c = 0; c <= pairs; ++c) sp->head[c] = (uint16_t)((int64_t)heads * c / pairs);
+  for (int c = 0; c < pairs; ++c)
+    if (sp->head[c + 1] - sp->head[c] > 2) return false;
+  // rope rows fill every CTA up to an even share of the bytes
+  const int64_t tb = (int64_t)4 * (kTaskRows * kRowBytes + kTaskUkBytes);  // one head's tasks
+  const int64_t rb = kRowBytes, rope = (int64_t)heads * kRope;
+  const int64_t total = (int64_t)heads * 2 * tb + rope * rb;
+  int64_t task_bytes = 0;
+  int prev = 0;
+  sp->rope[0] = 0;
+  for (int i = 0; i < ctas; ++i) {
+    task_bytes += (int64_t)(sp->head[i / 2 + 1] - sp->head[i / 2]) * tb;
+    int64_t r = (total * (i + 1) / ctas - task_bytes + rb / 2) / rb;
+    if (r < prev) r = prev;
+    if (r > rope) r = rope;
+    if (i == ctas - 1) r = rope;
+    sp->rope[i + 1] = (uint16_t)r;
+    prev = (int)r;
+  }
+  return true;
+}
+
+namespace {
+cudaLaunchConfig_t pair_config(int ctas, cudaStream_t stream, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ctas, 1, 1);
+  cfg.blockDim = dim3(kAbsThreads, 1, 1);
+  cfg.dynamicSmemBytes = PairSmem::kAlloc;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cfg;
+}
+}  // namespace
+
+bool pair_kernel_fits(int ctas) {
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = pair_config(ctas, nullptr, attr);
+  cfg.numAttrs = 1;  // the cluster shape only
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, mla_absorb_pair_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return clusters >= ctas / 2;
+}
+
+cudaError_t launch_pair(const DecodeArgs& a, const PairSplit& sp, int ctas, cudaStream_t stream) {
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = pair_config(ctas, stream, attr);
+  return cudaLaunchKernelEx(&cfg, mla_absorb_pair_kernel, a, sp);
+}
+
 cudaError_t prepare_fused_kernels() {
+  static_assert(PairSmem::kAlloc <= 232448, "shared memory budget");
+  {
+    cudaError_t e = cudaFuncSetAttribute(mla_absorb_pair_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         PairSmem::kAlloc);
+    if (e != cudaSuccess) return e;
+  }
   cudaError_t e;
   if ((e = prepare_abs<1>()) != cudaSuccess) return e;
   if ((e = prepare_abs<2>()) != cudaSuccess) return e;
+  if ((e = prepare_abs_mma<8>()) != cudaSuccess) return e;
+  if ((e = prepare_abs_mma<16>()) != cudaSuccess) return e;
   if ((e = prepare_one<1, false>()) != cudaSuccess) return e;
   if ((e = prepare_one<2, false>()) != cudaSuccess) return e;
   if ((e = prepare_one<8, true>()) != cudaSuccess) return e;
@@ -1237,6 +2064,8 @@ cudaError_t launch_absorb(const DecodeArgs& a, const AbsSplit& sp, int nt, int c
                           cudaStream_t stream) {
   if (nt == 1) return launch_abs<1>(a, sp, ctas, stream);
   if (nt == 2) return launch_abs<2>(a, sp, ctas, stream);
+  if (nt == 8) return launch_abs_mma<8>(a, sp, ctas, stream);
+  if (nt == 16) return launch_abs_mma<16>(a, sp, ctas, stream);
   return cudaErrorInvalidValue;
 }
 

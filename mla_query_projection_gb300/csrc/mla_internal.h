@@ -76,6 +76,19 @@ struct AbsSplit {
   uint16_t rope[kMaxCtas + 1];
 };
 void make_abs_split(int heads, int ctas, AbsSplit* sp);
+// Split of the paired absorbing kernel (clusters of two CTAs): the heads of
+// pair c are [head[c], head[c + 1]) (at most two), rank r of the pair takes
+// nope tasks 4r..4r+3 of each; rope rows [rope[i], rope[i + 1]) of CTA i.
+struct PairSplit {
+  uint16_t head[kMaxCtas / 2 + 1];
+  uint16_t rope[kMaxCtas + 1];
+};
+// Fills `sp` for `ctas` (even) CTAs; false if some pair would get more than
+// two heads.
+bool make_pair_split(int heads, int ctas, PairSplit* sp);
+// Whether `ctas` CTAs of the paired kernel can all be resident at once.
+bool pair_kernel_fits(int ctas);
+cudaError_t launch_pair(const DecodeArgs& a, const PairSplit& sp, int ctas, cudaStream_t stream);
 cudaError_t launch_absorb(const DecodeArgs& a, const AbsSplit& sp, int nt, int ctas,
                           cudaStream_t stream);
 
