@@ -156,10 +156,19 @@ int mla_query_create(mla_query_t* out, int num_heads, const void* w_qb, const vo
     goto fail;
   }
   mla::make_abs_split(num_heads, h->num_sms, &h->split);
+  // The paired kernel gives each CTA whole half-heads (256 KiB of weights per
+  // head); it is used only where that keeps the CTAs balanced, i.e. no CTA
+  // holds more than 10% above the average bytes per CTA.
   h->pair_ctas = h->num_sms & ~1;
-  if (!mla::make_pair_split(num_heads, h->pair_ctas, &h->pair_split) ||
-      !mla::pair_kernel_fits(h->pair_ctas))
-    h->pair_ctas = 0;
+  {
+    const int pairs = h->pair_ctas / 2;
+    const int64_t most = (int64_t)((num_heads + pairs - 1) / pairs) * 4 * 65536;
+    const int64_t avg = (int64_t)num_heads * (8 * 65536 + 64 * 3072) / h->pair_ctas;
+    if (pairs < 1 || 10 * most > 11 * avg ||
+        !mla::make_pair_split(num_heads, h->pair_ctas, &h->pair_split) ||
+        !mla::pair_kernel_fits(h->pair_ctas))
+      h->pair_ctas = 0;
+  }
   // FP32 partial absorptions of the absorbing kernels: [task][token < 16][512]
   if (cudaMalloc(&h->partial, (size_t)num_heads * 8 * 16 * mla::kKvLora * sizeof(float)) !=
       cudaSuccess) {

@@ -130,6 +130,14 @@ __device__ __forceinline__ void cluster_sync() {
       "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Cluster barrier without memory ordering: only keeps every CTA of the
+// cluster resident until all have arrived.
+__device__ __forceinline__ void cluster_sync_relaxed() {
+  asm volatile(
+      "barrier.cluster.arrive.relaxed.aligned;\n\t"
+      "barrier.cluster.wait.aligned;" ::: "memory");
+}
+
 // 16-byte store into another CTA's shared memory (shared::cluster address),
 // counted in bytes on that CTA's mbarrier `rbar` (shared::cluster address).
 __device__ __forceinline__ void st_async_v4(uint32_t raddr, float x, float y, float z, float w,

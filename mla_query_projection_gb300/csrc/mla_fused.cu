@@ -1800,30 +1800,40 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
     if (tid == 0) trace_stamp(a, 6);
 
     // ---- owned columns: rows 0..63 (rank 0) + rows 64..127 (rank 1) ------
+    // The BF16 results go back into this warp's 2 KiB receive slot as
+    // [token][64 columns], then out as 16-byte stores.
     if (own) {
       for (int j = 0; j < seq.nh; ++j) {
         if (!mbar_wait_bounded(&recvbar[j], 0u, kWaitLimit)) timed_out = true;
         const int h = seq.h0 + j;
+        uint8_t* slotp = smem + S::oRecv + j * kPairRecvBytes + (warp & 3) * (4 * 32 * 16);
+        float v[4][4];
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt) {
-          const float4 o = *reinterpret_cast<const float4*>(
-              smem + S::oRecv + j * kPairRecvBytes + ((((warp & 3) * 4 + mt) * 32 + lane) * 16));
+          const float4 o = *reinterpret_cast<const float4*>(slotp + (mt * 32 + lane) * 16);
           const float pv[4] = {o.x, o.y, o.z, o.w};
-          float v[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float mine = j == 0 ? keep[0][mt][e] : keep[1][mt][e];
-            v[e] = rank == 0 ? mine + pv[e] : pv[e] + mine;
+            v[mt][e] = rank == 0 ? mine + pv[e] : pv[e] + mine;
           }
-          const int c = 64 * warp + 16 * mt + g, t0 = 2 * q;
-          if (t0 < a.batch) {
-            a.q_latent[((int64_t)t0 * H + h) * kKvLora + c] = f2bf_bits(v[0]);
-            a.q_latent[((int64_t)t0 * H + h) * kKvLora + c + 8] = f2bf_bits(v[2]);
-          }
-          if (t0 + 1 < a.batch) {
-            a.q_latent[((int64_t)(t0 + 1) * H + h) * kKvLora + c] = f2bf_bits(v[1]);
-            a.q_latent[((int64_t)(t0 + 1) * H + h) * kKvLora + c + 8] = f2bf_bits(v[3]);
-          }
+        }
+        __syncwarp();
+        uint16_t* stage = reinterpret_cast<uint16_t*>(slotp);  // [8 tokens][64 columns]
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+          const int cl = 16 * mt + g, t0 = 2 * q;  // column within the warp's 64
+          stage[t0 * 64 + cl] = f2bf_bits(v[mt][0]);
+          stage[(t0 + 1) * 64 + cl] = f2bf_bits(v[mt][1]);
+          stage[t0 * 64 + cl + 8] = f2bf_bits(v[mt][2]);
+          stage[(t0 + 1) * 64 + cl + 8] = f2bf_bits(v[mt][3]);
+        }
+        __syncwarp();
+        for (int e = lane; e < a.batch * 8; e += 32) {  // 8 chunks of 16 B per token
+          const int t = e >> 3, ch = e & 7;
+          *reinterpret_cast<uint4*>(a.q_latent + ((int64_t)t * H + h) * kKvLora + 64 * warp +
+                                    8 * ch) =
+              *reinterpret_cast<const uint4*>(stage + t * 64 + 8 * ch);
         }
       }
     }
@@ -1831,8 +1841,9 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
 
   if (timed_out) atomicOr(a.err, MLA_DEVERR_TIMEOUT);
   __syncthreads();
-  // Neither CTA leaves while the other may still write into its shared memory.
-  cluster_sync();
+  // Neither CTA leaves while the other may still write into its shared memory
+  // (every owner waited for its received bytes above; this only holds both).
+  cluster_sync_relaxed();
   if (tid == 0) trace_stamp(a, 7);
 }
 
