@@ -1483,6 +1483,7 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
 // ===========================================================================
 
 constexpr int kPairNT = 8;
+constexpr int kPairPrefetch = 4;  // stages prefetched into L2 beyond the ring
 constexpr int kPairRecvBytes = 4 * 4 * 32 * 16;  // 4 warps x 4 m-tiles x 32 lanes x 16 B
 
 struct PairSmem {
@@ -1570,10 +1571,16 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
   if (warp == kConsumerWarps) {
     // ================= producer: weights only, no PDL wait ============
     const uint64_t pol = l2_policy_evict_first();
+    // L2 prefetch runs a window of kPairPrefetch stages ahead of the ring:
+    // enough to keep HBM busy while the ring is full, without holding a whole
+    // two-head share (about 450 KiB per CTA) in L2 at once.
     for (int k = 0; k < nst; ++k) {
       if (k == kAbsStages) {
-        for (int kk = kAbsStages + lane; kk < nst; kk += 32) pair_prefetch_stage(a, seq, kk);
+        for (int kk = kAbsStages + lane; kk < min(nst, kAbsStages + kPairPrefetch); kk += 32)
+          pair_prefetch_stage(a, seq, kk);
         __syncwarp();
+      } else if (k > kAbsStages && lane == 0 && k - 1 + kPairPrefetch < nst) {
+        pair_prefetch_stage(a, seq, k - 1 + kPairPrefetch);
       }
       const int slot = k % kAbsStages;
       uint8_t* buf = ring + slot * kTaskStageM;
