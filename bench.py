@@ -74,19 +74,16 @@ def kernel_for(path: int, batch: int) -> str:
     hand-off kernel, 8 or 16 tokens per CTA group)."""
     if path == 1:
         return f"mla_absorb_kernel<{1 if batch <= 1 else 2}>"
-    if batch <= 8:
-        return "mla_absorb_pair_kernel"
     if batch <= 16:
-        return "mla_absorb_mma_kernel<16>"
+        return f"mla_absorb_pair_kernel<{8 if batch <= 8 else 16}>"
     return f"mla_fused_kernel<{8 if batch <= 8 else 16},true>"
 
 
 def launches_per_step(path: int, batch: int) -> int:
-    """Kernels one decode call launches: the absorbing kernels that store FP32
-    partials (FMA path; tensor cores at 9-16 tokens) are followed by the
-    head-closing kernel; the paired kernel (up to 8 tokens) and the hand-off
-    kernel (above 16) run alone."""
-    return 2 if (path == 1 or 8 < batch <= 16) else 1
+    """Kernels one decode call launches: the FMA absorbing kernel is followed by
+    the head-closing kernel; the paired kernel (up to 16 tokens) and the
+    hand-off kernel (above 16) run alone."""
+    return 2 if path == 1 else 1
 
 
 def profile_name(kernel: str, workload: str) -> str:

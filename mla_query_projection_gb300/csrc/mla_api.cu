@@ -29,6 +29,7 @@ struct mla_query {
   mla::AbsSplit split;   // absorbing kernel: per-CTA ranges
   mla::PairSplit pair_split;  // paired absorbing kernel: per-pair heads, per-CTA rope
   int pair_ctas;              // its grid (even), 0 if it cannot run on this device
+  bool pair16;                // its 16-token flavour can run too
 };
 
 namespace {
@@ -80,6 +81,9 @@ int pick_kernel(const mla_query* h, int batch, Kernel* k, int* nt) {
     if (batch <= 8 && h->pair_ctas > 0) {
       *k = Kernel::kAbsorbPair;
       *nt = 8;
+    } else if (batch <= 16 && h->pair_ctas > 0 && h->pair16) {
+      *k = Kernel::kAbsorbPair;
+      *nt = 16;
     } else if (batch <= 16) {
       *k = Kernel::kAbsorbMma;
       *nt = batch <= 8 ? 8 : 16;
@@ -166,8 +170,9 @@ int mla_query_create(mla_query_t* out, int num_heads, const void* w_qb, const vo
     const int64_t avg = (int64_t)num_heads * (8 * 65536 + 64 * 3072) / h->pair_ctas;
     if (pairs < 1 || 10 * most > 11 * avg ||
         !mla::make_pair_split(num_heads, h->pair_ctas, &h->pair_split) ||
-        !mla::pair_kernel_fits(h->pair_ctas))
+        !mla::pair_kernel_fits(h->pair_ctas, 8))
       h->pair_ctas = 0;
+    h->pair16 = h->pair_ctas > 0 && mla::pair_kernel_fits(h->pair_ctas, 16);
   }
   // FP32 partial absorptions of the absorbing kernels: [task][token < 16][512]
   if (cudaMalloc(&h->partial, (size_t)num_heads * 8 * 16 * mla::kKvLora * sizeof(float)) !=
@@ -271,7 +276,7 @@ int mla_query_decode(mla_query_t h, int batch, const void* q_a, int64_t q_a_stri
   if (kern == Kernel::kHandoff)
     e = mla::launch_fused(a, &h->uk_map, nt, true, h->num_sms, st);
   else if (kern == Kernel::kAbsorbPair)
-    e = mla::launch_pair(a, h->pair_split, h->pair_ctas, st);
+    e = mla::launch_pair(a, h->pair_split, h->pair_ctas, nt, st);
   else
     e = mla::launch_absorb(a, h->split, nt, h->num_sms, st);
   if (e != cudaSuccess) {

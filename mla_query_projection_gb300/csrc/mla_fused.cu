@@ -1469,33 +1469,39 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
 }
 
 // ===========================================================================
-// Paired absorbing kernel (tensor cores, up to 8 tokens): clusters of two CTAs.
+// Paired absorbing kernel (tensor cores, up to 16 tokens): clusters of two CTAs.
 //
 // Both CTAs of a pair take the same heads; rank r streams nope tasks
 // 4r..4r+3 (rows 64r..64r+63) of each, with their W_UK rows, and accumulates
-// the head's absorption over its four tasks in registers.  After a head's
-// last task, the warps whose latent columns the other CTA owns (rank 0 owns
-// columns 0..255, rank 1 columns 256..511) send their FP32 sums into the
+// the head's absorption over its four tasks in the mma accumulators.  After a
+// head's last task, the warps whose latent columns the other CTA owns (rank 0
+// owns columns 0..255, rank 1 columns 256..511) send their FP32 sums into the
 // other CTA's shared memory (st.async, counted on its mbarrier).  After the
 // rope stages each CTA adds the two halves of its columns - rows 0..63 first,
 // then rows 64..127 - and writes q_latent.  No global scratch, no second
 // kernel, no wait on any CTA outside the pair.
+//
+// NT = 8 tokens: a 3-stage ring, the owned sums stay in registers.
+// NT = 16: a 2-stage ring (shared memory), the owned sums go to shared memory.
 // ===========================================================================
 
-constexpr int kPairNT = 8;
-constexpr int kPairPrefetch = 4;  // stages prefetched into L2 beyond the ring
-constexpr int kPairRecvBytes = 4 * 4 * 32 * 16;  // 4 warps x 4 m-tiles x 32 lanes x 16 B
+constexpr int kPairPrefetch = 1;  // stages prefetched into L2 beyond the ring
 
+template <int NT>
 struct PairSmem {
-  static constexpr int NT = kPairNT;
-  static constexpr int kRing = kAbsStages * kTaskStageM;
+  static constexpr int NTL = NT / 8;
+  static constexpr int kStages = NT == 8 ? 3 : 2;
+  static constexpr int kRecvBytes = 4 * 4 * NTL * 32 * 16;  // 4 warps x 4 m-tiles x n-tiles x 32 lanes x 16 B
+  static constexpr bool kKeepInSmem = NT > 8;
+  static constexpr int kRing = kStages * kTaskStageM;
   static constexpr int kRedBuf = kConsumerWarps * NT * kRedTok;     // floats per buffer
   static constexpr int oRed = kRing;                                 // [2][warp][token][kRedTok]
-  static constexpr int oRecv = oRed + 2 * kRedBuf * 4;               // [2 heads][kPairRecvBytes]
-  static constexpr int oSs = oRecv + 2 * kPairRecvBytes;             // [warp][NT] + [8] floats
+  static constexpr int oRecv = oRed + 2 * kRedBuf * 4;               // [2 heads][kRecvBytes]
+  static constexpr int oKeep = oRecv + 2 * kRecvBytes;               // [2 heads][kRecvBytes] (NT > 8)
+  static constexpr int oSs = oKeep + (kKeepInSmem ? 2 * kRecvBytes : 0);  // [warp][NT] + [8] floats
   static constexpr int oFull = oSs + (kConsumerWarps * NT + 8) * 4;
-  static constexpr int oEmpty = oFull + kAbsStages * 8;
-  static constexpr int oRbar = oEmpty + kAbsStages * 8;              // [2] split-K barriers
+  static constexpr int oEmpty = oFull + kStages * 8;
+  static constexpr int oRbar = oEmpty + kStages * 8;                 // [2] split-K barriers
   static constexpr int oRecvBar = oRbar + 16;                        // [2] received halves
   static constexpr int kBytes = oRecvBar + 16;
   static constexpr int kAlloc = kBytes + 128;
@@ -1525,10 +1531,12 @@ __device__ __forceinline__ void pair_prefetch_stage(const DecodeArgs& a, const P
   }
 }
 
+template <int NT>
 __global__ void __launch_bounds__(kAbsThreads, 1)
     mla_absorb_pair_kernel(const DecodeArgs a, const __grid_constant__ PairSplit split) {
-  using S = PairSmem;
-  constexpr int NT = kPairNT;
+  using S = PairSmem<NT>;
+  constexpr int NTL = S::NTL;
+  constexpr int ST = S::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
                                              ~static_cast<uintptr_t>(127));
@@ -1549,7 +1557,7 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
   const int nst = seq.stages();
 
   if (tid == 0) {
-    for (int s = 0; s < kAbsStages; ++s) {
+    for (int s = 0; s < ST; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
     }
@@ -1559,7 +1567,7 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
     mbar_init(&recvbar[1], 1);
     // The other CTA's sums of head j land in recv[j]: armed before the pair
     // meets below, so no byte can arrive before its count is expected.
-    for (int j = 0; j < seq.nh; ++j) mbar_arrive_expect_tx(&recvbar[j], kPairRecvBytes);
+    for (int j = 0; j < seq.nh; ++j) mbar_arrive_expect_tx(&recvbar[j], S::kRecvBytes);
     mbar_fence_init();
     pdl_launch_dependents();
     trace_stamp(a, 0);
@@ -1570,25 +1578,25 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
 
   if (warp == kConsumerWarps) {
     // ================= producer: weights only, no PDL wait ============
+    // L2 prefetch runs kPairPrefetch stages ahead of the ring: HBM keeps
+    // streaming while the ring is full, without a whole two-head share
+    // (about 450 KiB per CTA) sitting in L2 at once (measured: a window of one
+    // stage beats deeper ones at 128 heads, 14.9 us against 16.9 us for four).
     const uint64_t pol = l2_policy_evict_first();
-    // L2 prefetch runs a window of kPairPrefetch stages ahead of the ring:
-    // enough to keep HBM busy while the ring is full, without holding a whole
-    // two-head share (about 450 KiB per CTA) in L2 at once.
     for (int k = 0; k < nst; ++k) {
-      if (k == kAbsStages) {
-        for (int kk = kAbsStages + lane; kk < min(nst, kAbsStages + kPairPrefetch); kk += 32)
+      if (k == ST) {
+        for (int kk = ST + lane; kk < min(nst, ST + kPairPrefetch); kk += 32)
           pair_prefetch_stage(a, seq, kk);
         __syncwarp();
-      } else if (k > kAbsStages && lane == 0 && k - 1 + kPairPrefetch < nst) {
+      } else if (k > ST && lane == 0 && k - 1 + kPairPrefetch < nst) {
         pair_prefetch_stage(a, seq, k - 1 + kPairPrefetch);
       }
-      const int slot = k % kAbsStages;
+      const int slot = k % ST;
       uint8_t* buf = ring + slot * kTaskStageM;
-      if (k >= kAbsStages) {
+      if (k >= ST) {
         int ok = 1;
         if (lane == 0)
-          ok = mbar_wait_bounded(&empty[slot], (uint32_t)(((k / kAbsStages) - 1) & 1), kWaitLimit)
-                   ? 1 : 0;
+          ok = mbar_wait_bounded(&empty[slot], (uint32_t)(((k / ST) - 1) & 1), kWaitLimit) ? 1 : 0;
         if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) timed_out = true;
       }
       if (lane == 0 && k < 20) trace_stamp(a, 28 + k);
@@ -1616,9 +1624,8 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
       }
     }
     if (lane == 0)
-      for (int k = max(0, nst - kAbsStages); k < nst; ++k)
-        (void)mbar_wait_bounded(&full[k % kAbsStages], (uint32_t)((k / kAbsStages) & 1),
-                                kWaitLimit);
+      for (int k = max(0, nst - ST); k < nst; ++k)
+        (void)mbar_wait_bounded(&full[k % ST], (uint32_t)((k / ST) & 1), kWaitLimit);
   } else {
     // ================= consumer warps 0-7 ============================
     const int g = lane >> 2, q = lane & 3;
@@ -1628,17 +1635,19 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
       gam[c] = *reinterpret_cast<const uint4*>(a.gamma_q + 192 * warp + 32 * c + 8 * q);
     pdl_wait();
     if (tid == 0) trace_stamp(a, 3);
-    // q_a RMSNorm -> B fragments xb[c] (token g, K 192 w + 32 c + 8 q + 0..7)
-    uint4 xb[6];
-    {
-      const int tok = g;
+    // q_a RMSNorm -> B fragments xb[nt][c] (token 8 nt + g, K 192 w + 32 c + 8 q + 0..7)
+    uint4 xb[NTL][6];
+#pragma unroll
+    for (int nt = 0; nt < NTL; ++nt) {
+      const int tok = 8 * nt + g;
       float ss = 0.f;
 #pragma unroll
       for (int c = 0; c < 6; ++c) {
-        xb[c] = tok < a.batch ? *reinterpret_cast<const uint4*>(a.q_a + (int64_t)tok * a.q_a_stride +
-                                                               192 * warp + 32 * c + 8 * q)
-                              : make_uint4(0, 0, 0, 0);
-        const uint32_t ww[4] = {xb[c].x, xb[c].y, xb[c].z, xb[c].w};
+        xb[nt][c] = tok < a.batch
+                        ? *reinterpret_cast<const uint4*>(a.q_a + (int64_t)tok * a.q_a_stride +
+                                                          192 * warp + 32 * c + 8 * q)
+                        : make_uint4(0, 0, 0, 0);
+        const uint32_t ww[4] = {xb[nt][c].x, xb[nt][c].y, xb[nt][c].z, xb[nt][c].w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           ss = fmaf(bf16lo(ww[e]), bf16lo(ww[e]), ss);
@@ -1648,24 +1657,28 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
       ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
       ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 2);
       if (q == 0) ss_s[warp * NT + tok] = ss;
-      named_barrier(kBarConsumers, kConsumers);
+    }
+    named_barrier(kBarConsumers, kConsumers);
+#pragma unroll
+    for (int nt = 0; nt < NTL; ++nt) {
+      const int tok = 8 * nt + g;
       float total = 0.f;
 #pragma unroll
       for (int w = 0; w < kConsumerWarps; ++w) total += ss_s[w * NT + tok];
       const float rr = __frsqrt_rn(__fadd_rn(__fdiv_rn(total, 1536.0f), a.eps));
 #pragma unroll
       for (int c = 0; c < 6; ++c) {
-        const uint32_t ww[4] = {xb[c].x, xb[c].y, xb[c].z, xb[c].w};
+        const uint32_t ww[4] = {xb[nt][c].x, xb[nt][c].y, xb[nt][c].z, xb[nt][c].w};
         const uint32_t gw[4] = {gam[c].x, gam[c].y, gam[c].z, gam[c].w};
         uint32_t o[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e)
           o[e] = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[e]), rr), bf16lo(gw[e])),
                              __fmul_rn(__fmul_rn(bf16hi(ww[e]), rr), bf16hi(gw[e])));
-        xb[c] = make_uint4(o[0], o[1], o[2], o[3]);
+        xb[nt][c] = make_uint4(o[0], o[1], o[2], o[3]);
         if (i == 0 && a.q_c != nullptr && tok < a.batch)
           *reinterpret_cast<uint4*>(a.q_c + (int64_t)tok * kQLora + 192 * warp + 32 * c + 8 * q) =
-              xb[c];
+              xb[nt][c];
       }
     }
     if (warp >= 6)
@@ -1673,25 +1686,28 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
     if (tid == 0) trace_stamp(a, 2);
 
     // Columns 64 w .. 64 w + 63 belong to rank 0 for w < 4, to rank 1 else.
+    // A warp's slot of a per-head buffer: [m-tile][n-tile][lane][16 B].
     const bool own = (warp < 4) == (rank == 0);
-    const uint32_t recv_local = smem_u32(smem + S::oRecv) +
-                                (uint32_t)((((warp & 3) * 4) * 32 + lane) * 16);
-    float dacc[4][4];   // this head's absorption over the tasks so far
-    float keep[2][4][4];  // owned sums of heads 0 and 1 of the pair
+    const int slot_off = (warp & 3) * (4 * NTL * 32 * 16);
+    float dacc[4][NTL][4];   // this head's absorption over the tasks so far
+    float keep[2][4][4];     // NT = 8: owned sums of heads 0 and 1 of the pair
 #pragma unroll
     for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) dacc[mt][e] = keep[0][mt][e] = keep[1][mt][e] = 0.f;
+      for (int e = 0; e < 4; ++e) {
+        keep[0][mt][e] = keep[1][mt][e] = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < NTL; ++nt) dacc[mt][nt][e] = 0.f;
+      }
 
     for (int k = 0; k < nst; ++k) {
-      const int slot = k % kAbsStages;
+      const int slot = k % ST;
       const uint8_t* buf = ring + slot * kTaskStageM;
-      if (!mbar_wait_bounded(&full[slot], (uint32_t)((k / kAbsStages) & 1), kWaitLimit))
-        timed_out = true;
+      if (!mbar_wait_bounded(&full[slot], (uint32_t)((k / ST) & 1), kWaitLimit)) timed_out = true;
       if (tid == 0 && k < 20) trace_stamp(a, 8 + k);
       const bool task = k < seq.tasks();
       // ---- Q_B rows of the stage over this warp's K slice ---------------
-      float acc[4];
+      float acc[NTL][4];
       {
         uint4 alo[6], ahi[6];
 #pragma unroll
@@ -1700,17 +1716,25 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
           alo[c] = *reinterpret_cast<const uint4*>(buf + g * kPitch + kb);
           ahi[c] = *reinterpret_cast<const uint4*>(buf + (g + 8) * kPitch + kb);
         }
-        float ch[4][4];
+        float ch[NTL][4][4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) ch[j][0] = ch[j][1] = ch[j][2] = ch[j][3] = 0.f;
+        for (int nt = 0; nt < NTL; ++nt)
 #pragma unroll
-        for (int c = 0; c < 6; ++c) {
-          mma_bf16_16816(ch[2 * (c & 1)], alo[c].x, ahi[c].x, alo[c].y, ahi[c].y, xb[c].x, xb[c].y);
-          mma_bf16_16816(ch[2 * (c & 1) + 1], alo[c].z, ahi[c].z, alo[c].w, ahi[c].w, xb[c].z,
-                         xb[c].w);
-        }
+          for (int j = 0; j < 4; ++j) ch[nt][j][0] = ch[nt][j][1] = ch[nt][j][2] = ch[nt][j][3] = 0.f;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[e] = (ch[0][e] + ch[1][e]) + (ch[2][e] + ch[3][e]);
+        for (int c = 0; c < 6; ++c)
+#pragma unroll
+          for (int nt = 0; nt < NTL; ++nt) {
+            mma_bf16_16816(ch[nt][2 * (c & 1)], alo[c].x, ahi[c].x, alo[c].y, ahi[c].y,
+                           xb[nt][c].x, xb[nt][c].y);
+            mma_bf16_16816(ch[nt][2 * (c & 1) + 1], alo[c].z, ahi[c].z, alo[c].w, ahi[c].w,
+                           xb[nt][c].z, xb[nt][c].w);
+          }
+#pragma unroll
+        for (int nt = 0; nt < NTL; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            acc[nt][e] = (ch[nt][0][e] + ch[nt][1][e]) + (ch[nt][2][e] + ch[nt][3][e]);
       }
       if (!task) {
         __syncwarp();
@@ -1720,11 +1744,14 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
       float* red = redp + (k & 1) * S::kRedBuf;
       {
         float* rw = red + warp * NT * kRedTok;
-        const int t0 = 2 * q;
-        rw[t0 * kRedTok + g] = acc[0];
-        rw[(t0 + 1) * kRedTok + g] = acc[1];
-        rw[t0 * kRedTok + g + 8] = acc[2];
-        rw[(t0 + 1) * kRedTok + g + 8] = acc[3];
+#pragma unroll
+        for (int nt = 0; nt < NTL; ++nt) {
+          const int t0 = 8 * nt + 2 * q;
+          rw[t0 * kRedTok + g] = acc[nt][0];
+          rw[(t0 + 1) * kRedTok + g] = acc[nt][1];
+          rw[t0 * kRedTok + g + 8] = acc[nt][2];
+          rw[(t0 + 1) * kRedTok + g + 8] = acc[nt][3];
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&rbar[k & 1]);
@@ -1747,9 +1774,10 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
         continue;
       }
       // ---- task: BF16 q of the 16 rows, absorption into dacc -------------
-      uint32_t qb0, qb1;
-      {
-        const int tok = g;
+      uint32_t qb[NTL][2];
+#pragma unroll
+      for (int nt = 0; nt < NTL; ++nt) {
+        const int tok = 8 * nt + g;
         float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) {
@@ -1761,13 +1789,16 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
           s2 += hi.x;
           s3 += hi.y;
         }
-        qb0 = pack_bf16x2(s0, s1);
-        qb1 = pack_bf16x2(s2, s3);
+        qb[nt][0] = pack_bf16x2(s0, s1);
+        qb[nt][1] = pack_bf16x2(s2, s3);
       }
       const int u = k & 3;  // task of the head: 0..3
       if (u == 0) {
 #pragma unroll
-        for (int mt = 0; mt < 4; ++mt) dacc[mt][0] = dacc[mt][1] = dacc[mt][2] = dacc[mt][3] = 0.f;
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+          for (int nt = 0; nt < NTL; ++nt)
+            dacc[mt][nt][0] = dacc[mt][nt][1] = dacc[mt][nt][2] = dacc[mt][nt][3] = 0.f;
       }
       const uint32_t uk = smem_u32(buf + kTaskQbBytes);
 #pragma unroll
@@ -1777,64 +1808,91 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
         const int c = 64 * warp + 16 * mt + 8 * (m & 1);
         uint32_t af[4];
         ldmatrix_x4_trans(af, uk + p * kUkPitchM + 2 * c);
-        mma_bf16_16816(dacc[mt], af[0], af[1], af[2], af[3], qb0, qb1);
+#pragma unroll
+        for (int nt = 0; nt < NTL; ++nt)
+          mma_bf16_16816(dacc[mt][nt], af[0], af[1], af[2], af[3], qb[nt][0], qb[nt][1]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);  // W_QB and W_UK of the slot are read
       if (u == 3) {
         const int j = k >> 2;  // head of the pair: 0 or 1
         if (own) {
+          if constexpr (S::kKeepInSmem) {
+            uint8_t* kp = smem + S::oKeep + j * S::kRecvBytes + slot_off;
 #pragma unroll
-          for (int mt = 0; mt < 4; ++mt)
+            for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              if (j == 0) keep[0][mt][e] = dacc[mt][e];
-              else keep[1][mt][e] = dacc[mt][e];
-            }
+              for (int nt = 0; nt < NTL; ++nt)
+                *reinterpret_cast<float4*>(kp + ((mt * NTL + nt) * 32 + lane) * 16) =
+                    make_float4(dacc[mt][nt][0], dacc[mt][nt][1], dacc[mt][nt][2], dacc[mt][nt][3]);
+          } else {
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                if (j == 0) keep[0][mt][e] = dacc[mt][0][e];
+                else keep[1][mt][e] = dacc[mt][0][e];
+              }
+          }
         } else {
           // to the other CTA: same warp slot (w & 3), same lane, head slot j
           const uint32_t peer = (uint32_t)(rank ^ 1);
           const uint32_t rbar_remote = mapa_shared(smem_u32(&recvbar[j]), peer);
+          const uint32_t base = smem_u32(smem + S::oRecv + j * S::kRecvBytes + slot_off);
 #pragma unroll
-          for (int mt = 0; mt < 4; ++mt) {
-            const uint32_t laddr = recv_local + (uint32_t)(j * kPairRecvBytes + mt * 32 * 16);
-            st_async_v4(mapa_shared(laddr, peer), dacc[mt][0], dacc[mt][1], dacc[mt][2],
-                        dacc[mt][3], rbar_remote);
-          }
+          for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NTL; ++nt)
+              st_async_v4(mapa_shared(base + (uint32_t)(((mt * NTL + nt) * 32 + lane) * 16), peer),
+                          dacc[mt][nt][0], dacc[mt][nt][1], dacc[mt][nt][2], dacc[mt][nt][3],
+                          rbar_remote);
         }
       }
     }
     if (tid == 0) trace_stamp(a, 6);
 
     // ---- owned columns: rows 0..63 (rank 0) + rows 64..127 (rank 1) ------
-    // The BF16 results go back into this warp's 2 KiB receive slot as
+    // The BF16 results go back into this warp's receive slot as
     // [token][64 columns], then out as 16-byte stores.
     if (own) {
       for (int j = 0; j < seq.nh; ++j) {
         if (!mbar_wait_bounded(&recvbar[j], 0u, kWaitLimit)) timed_out = true;
         const int h = seq.h0 + j;
-        uint8_t* slotp = smem + S::oRecv + j * kPairRecvBytes + (warp & 3) * (4 * 32 * 16);
-        float v[4][4];
+        uint8_t* slotp = smem + S::oRecv + j * S::kRecvBytes + slot_off;
+        float v[4][NTL][4];
 #pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
-          const float4 o = *reinterpret_cast<const float4*>(slotp + (mt * 32 + lane) * 16);
-          const float pv[4] = {o.x, o.y, o.z, o.w};
+        for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float mine = j == 0 ? keep[0][mt][e] : keep[1][mt][e];
-            v[mt][e] = rank == 0 ? mine + pv[e] : pv[e] + mine;
+          for (int nt = 0; nt < NTL; ++nt) {
+            const float4 o = *reinterpret_cast<const float4*>(slotp + ((mt * NTL + nt) * 32 + lane) * 16);
+            const float pv[4] = {o.x, o.y, o.z, o.w};
+            float mine[4];
+            if constexpr (S::kKeepInSmem) {
+              const float4 kv = *reinterpret_cast<const float4*>(
+                  smem + S::oKeep + j * S::kRecvBytes + slot_off + ((mt * NTL + nt) * 32 + lane) * 16);
+              mine[0] = kv.x;
+              mine[1] = kv.y;
+              mine[2] = kv.z;
+              mine[3] = kv.w;
+            } else {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) mine[e] = j == 0 ? keep[0][mt][e] : keep[1][mt][e];
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[mt][nt][e] = rank == 0 ? mine[e] + pv[e] : pv[e] + mine[e];
           }
-        }
         __syncwarp();
-        uint16_t* stage = reinterpret_cast<uint16_t*>(slotp);  // [8 tokens][64 columns]
+        uint16_t* stage = reinterpret_cast<uint16_t*>(slotp);  // [NT tokens][64 columns]
 #pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
-          const int cl = 16 * mt + g, t0 = 2 * q;  // column within the warp's 64
-          stage[t0 * 64 + cl] = f2bf_bits(v[mt][0]);
-          stage[(t0 + 1) * 64 + cl] = f2bf_bits(v[mt][1]);
-          stage[t0 * 64 + cl + 8] = f2bf_bits(v[mt][2]);
-          stage[(t0 + 1) * 64 + cl + 8] = f2bf_bits(v[mt][3]);
-        }
+        for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+          for (int nt = 0; nt < NTL; ++nt) {
+            const int cl = 16 * mt + g, t0 = 8 * nt + 2 * q;  // column within the warp's 64
+            stage[t0 * 64 + cl] = f2bf_bits(v[mt][nt][0]);
+            stage[(t0 + 1) * 64 + cl] = f2bf_bits(v[mt][nt][1]);
+            stage[t0 * 64 + cl + 8] = f2bf_bits(v[mt][nt][2]);
+            stage[(t0 + 1) * 64 + cl + 8] = f2bf_bits(v[mt][nt][3]);
+          }
         __syncwarp();
         for (int e = lane; e < a.batch * 8; e += 32) {  // 8 chunks of 16 B per token
           const int t = e >> 3, ch = e & 7;
@@ -2022,11 +2080,12 @@ bool make_pair_split(int heads, int ctas, PairSplit* sp) {
 }
 
 namespace {
+template <int NT>
 cudaLaunchConfig_t pair_config(int ctas, cudaStream_t stream, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)ctas, 1, 1);
   cfg.blockDim = dim3(kAbsThreads, 1, 1);
-  cfg.dynamicSmemBytes = PairSmem::kAlloc;
+  cfg.dynamicSmemBytes = PairSmem<NT>::kAlloc;
   cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -2040,30 +2099,47 @@ cudaLaunchConfig_t pair_config(int ctas, cudaStream_t stream, cudaLaunchAttribut
 }
 }  // namespace
 
-bool pair_kernel_fits(int ctas) {
+template <int NT>
+bool pair_fits(int ctas) {
   cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = pair_config(ctas, nullptr, attr);
+  cudaLaunchConfig_t cfg = pair_config<NT>(ctas, nullptr, attr);
   cfg.numAttrs = 1;  // the cluster shape only
   int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, mla_absorb_pair_kernel, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&clusters, mla_absorb_pair_kernel<NT>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return false;
   }
   return clusters >= ctas / 2;
 }
 
-cudaError_t launch_pair(const DecodeArgs& a, const PairSplit& sp, int ctas, cudaStream_t stream) {
+bool pair_kernel_fits(int ctas, int nt) {
+  return nt == 8 ? pair_fits<8>(ctas) : nt == 16 ? pair_fits<16>(ctas) : false;
+}
+
+cudaError_t launch_pair(const DecodeArgs& a, const PairSplit& sp, int ctas, int nt,
+                        cudaStream_t stream) {
   cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = pair_config(ctas, stream, attr);
-  return cudaLaunchKernelEx(&cfg, mla_absorb_pair_kernel, a, sp);
+  if (nt == 8) {
+    cudaLaunchConfig_t cfg = pair_config<8>(ctas, stream, attr);
+    return cudaLaunchKernelEx(&cfg, mla_absorb_pair_kernel<8>, a, sp);
+  }
+  if (nt == 16) {
+    cudaLaunchConfig_t cfg = pair_config<16>(ctas, stream, attr);
+    return cudaLaunchKernelEx(&cfg, mla_absorb_pair_kernel<16>, a, sp);
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t prepare_fused_kernels() {
-  static_assert(PairSmem::kAlloc <= 232448, "shared memory budget");
+  static_assert(PairSmem<8>::kAlloc <= 232448, "shared memory budget");
+  static_assert(PairSmem<16>::kAlloc <= 232448, "shared memory budget");
   {
-    cudaError_t e = cudaFuncSetAttribute(mla_absorb_pair_kernel,
+    cudaError_t e = cudaFuncSetAttribute(mla_absorb_pair_kernel<8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         PairSmem::kAlloc);
+                                         PairSmem<8>::kAlloc);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(mla_absorb_pair_kernel<16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, PairSmem<16>::kAlloc);
     if (e != cudaSuccess) return e;
   }
   cudaError_t e;

@@ -86,9 +86,11 @@ struct PairSplit {
 // Fills `sp` for `ctas` (even) CTAs; false if some pair would get more than
 // two heads.
 bool make_pair_split(int heads, int ctas, PairSplit* sp);
-// Whether `ctas` CTAs of the paired kernel can all be resident at once.
-bool pair_kernel_fits(int ctas);
-cudaError_t launch_pair(const DecodeArgs& a, const PairSplit& sp, int ctas, cudaStream_t stream);
+// Whether `ctas` CTAs of the paired kernel (nt = 8 or 16 tokens) can all be
+// resident at once.
+bool pair_kernel_fits(int ctas, int nt);
+cudaError_t launch_pair(const DecodeArgs& a, const PairSplit& sp, int ctas, int nt,
+                        cudaStream_t stream);
 cudaError_t launch_absorb(const DecodeArgs& a, const AbsSplit& sp, int nt, int ctas,
                           cudaStream_t stream);
 
