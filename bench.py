@@ -70,20 +70,17 @@ def read_peaks() -> tuple[float, str]:
 
 def kernel_for(path: int, batch: int) -> str:
     """The kernel one decode step launches on the given path (MLA_PATH_FMA:
-    the absorbing kernel, one or two tokens per CTA; MLA_PATH_MMA: the
-    hand-off kernel, 8 or 16 tokens per CTA group)."""
+    the FP32-FMA absorbing kernel, one or two tokens per CTA; MLA_PATH_MMA:
+    the paired tensor-core kernel, 8 or 16 tokens per launch)."""
     if path == 1:
         return f"mla_absorb_kernel<{1 if batch <= 1 else 2}>"
-    if batch <= 16:
-        return f"mla_absorb_pair_kernel<{8 if batch <= 8 else 16}>"
-    return f"mla_fused_kernel<{8 if batch <= 8 else 16},true>"
+    return f"mla_absorb_pair_kernel<{8 if batch <= 8 else 16}>"
 
 
 def launches_per_step(path: int, batch: int) -> int:
     """Kernels one decode call launches: the FMA absorbing kernel is followed by
-    the head-closing kernel; the paired kernel (up to 16 tokens) and the
-    hand-off kernel (above 16) run alone."""
-    return 2 if path == 1 else 1
+    the head-closing kernel; the paired kernel runs once per 16 tokens."""
+    return 2 if path == 1 else -(-batch // 16)
 
 
 def profile_name(kernel: str, workload: str) -> str:

@@ -81,8 +81,8 @@ int pick_kernel(const mla_query* h, int batch, Kernel* k, int* nt) {
     if (batch <= 8 && h->pair_ctas > 0) {
       *k = Kernel::kAbsorbPair;
       *nt = 8;
-    } else if (batch <= 16 && h->pair_ctas > 0 && h->pair16) {
-      *k = Kernel::kAbsorbPair;
+    } else if (h->pair_ctas > 0 && h->pair16) {
+      *k = Kernel::kAbsorbPair;  // above 16 tokens: one launch per 16 tokens
       *nt = 16;
     } else if (batch <= 16) {
       *k = Kernel::kAbsorbMma;
@@ -275,8 +275,27 @@ int mla_query_decode(mla_query_t h, int batch, const void* q_a, int64_t q_a_stri
   cudaError_t e;
   if (kern == Kernel::kHandoff)
     e = mla::launch_fused(a, &h->uk_map, nt, true, h->num_sms, st);
-  else if (kern == Kernel::kAbsorbPair)
+  else if (kern == Kernel::kAbsorbPair && batch <= 16)
     e = mla::launch_pair(a, h->pair_split, h->pair_ctas, nt, st);
+  else if (kern == Kernel::kAbsorbPair) {
+    // Batches above 16: the 16-token paired kernel once per slice of 16
+    // tokens, every per-token pointer offset to the slice.  Each launch
+    // streams the weights again; each slice inserts its own KV rows.
+    e = cudaSuccess;
+    for (int t0 = 0; t0 < batch && e == cudaSuccess; t0 += 16) {
+      mla::DecodeArgs s16 = a;
+      s16.batch = batch - t0 < 16 ? batch - t0 : 16;
+      s16.groups = 1;
+      s16.q_a = a.q_a + (int64_t)t0 * a.q_a_stride;
+      s16.kv_c = a.kv_c + (int64_t)t0 * a.kv_c_stride;
+      s16.k_pe = a.k_pe + (int64_t)t0 * a.k_pe_stride;
+      s16.slots = a.slots + t0;
+      s16.q_latent = a.q_latent + (int64_t)t0 * h->heads * mla::kKvLora;
+      s16.q_pe = a.q_pe + (int64_t)t0 * h->heads * mla::kRope;
+      s16.q_c = a.q_c != nullptr ? a.q_c + (int64_t)t0 * mla::kQLora : nullptr;
+      e = mla::launch_pair(s16, h->pair_split, h->pair_ctas, s16.batch <= 8 ? 8 : 16, st);
+    }
+  }
   else
     e = mla::launch_absorb(a, h->split, nt, h->num_sms, st);
   if (e != cudaSuccess) {
