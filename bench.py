@@ -71,16 +71,22 @@ def read_peaks() -> tuple[float, str]:
 def kernel_for(path: int, batch: int) -> str:
     """The kernel one decode step launches on the given path (MLA_PATH_FMA:
     the FP32-FMA absorbing kernel, one or two tokens per CTA; MLA_PATH_MMA:
-    the paired tensor-core kernel, 8 or 16 tokens per launch)."""
+    the paired tensor-core kernel, 8 or 16 tokens per launch, or above 32
+    tokens the wide tcgen05 kernel, 64 tokens per launch)."""
     if path == 1:
         return f"mla_absorb_kernel<{1 if batch <= 1 else 2}>"
+    if batch > 32:
+        return "mla_wide_kernel"
     return f"mla_absorb_pair_kernel<{8 if batch <= 8 else 16}>"
 
 
 def launches_per_step(path: int, batch: int) -> int:
     """Kernels one decode call launches: the FMA absorbing kernel is followed by
-    the head-closing kernel; the paired kernel runs once per 16 tokens."""
-    return 2 if path == 1 else -(-batch // 16)
+    the head-closing kernel; the paired kernel runs once per 16 tokens up to 32
+    tokens, the wide tcgen05 kernel once per 64 tokens above."""
+    if path == 1:
+        return 2
+    return -(-batch // 64) if batch > 32 else -(-batch // 16)
 
 
 def profile_name(kernel: str, workload: str) -> str:

@@ -30,6 +30,10 @@ struct mla_query {
   mla::PairSplit pair_split;  // paired absorbing kernel: per-pair heads, per-CTA rope
   int pair_ctas;              // its grid (even), 0 if it cannot run on this device
   bool pair16;                // its 16-token flavour can run too
+  uint16_t* w_ukt;            // wide kernel: library-owned W_UK^T [H][512][128]
+  CUtensorMap wide_maps[3];   // W_QB (64 x 128 and 64 x 64 boxes), W_UK^T (64 x 128)
+  mla::WideSplit wide_split;  // per-pair heads and rope units
+  int wide_ctas;              // its grid (even), 0 if it cannot run on this device
 };
 
 namespace {
@@ -64,11 +68,26 @@ int encode_uk_map(CUtensorMap* map, const void* w_uk, int heads) {
   return r == CUDA_SUCCESS ? MLA_OK : MLA_ECUDA;
 }
 
+// A 2-D BF16 tensor map [rows][cols] (row-major), boxes of box_rows x 64
+// columns (128 B rows, 128 B swizzle).
+int encode_bf16_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return MLA_ECUDA;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MLA_OK : MLA_ECUDA;
+}
+
 // The kernel a decode call launches:
 //   absorbing kernel, FP32 FMA flavour (1 or 2 tokens per CTA);
 //   absorbing kernel, tensor-core flavour (8 or 16 tokens per CTA, B <= 16);
 //   hand-off kernel, tensor cores, token groups of 8 or 16 (any B).
-enum class Kernel { kAbsorbFma, kAbsorbMma, kAbsorbPair, kHandoff };
+enum class Kernel { kAbsorbFma, kAbsorbMma, kAbsorbPair, kWide, kHandoff };
 
 int pick_kernel(const mla_query* h, int batch, Kernel* k, int* nt) {
   int path = h->path;
@@ -81,6 +100,12 @@ int pick_kernel(const mla_query* h, int batch, Kernel* k, int* nt) {
     if (batch <= 8 && h->pair_ctas > 0) {
       *k = Kernel::kAbsorbPair;
       *nt = 8;
+    } else if (batch <= 16 && h->pair_ctas > 0 && h->pair16) {
+      *k = Kernel::kAbsorbPair;
+      *nt = 16;
+    } else if (batch > 32 && h->wide_ctas > 0) {
+      *k = Kernel::kWide;  // one launch per 64 tokens
+      *nt = mla::wide_tokens();
     } else if (h->pair_ctas > 0 && h->pair16) {
       *k = Kernel::kAbsorbPair;  // above 16 tokens: one launch per 16 tokens
       *nt = 16;
@@ -189,6 +214,25 @@ int mla_query_create(mla_query_t* out, int num_heads, const void* w_qb, const vo
   if (mla::repack_w_uk(h->w_uk, h->w_uk_packed, num_heads, 0) != cudaSuccess ||
       cudaStreamSynchronize(0) != cudaSuccess)
     goto fail;
+  // Wide kernel (17 tokens and more): W_UK^T copy, tensor maps, pair split.
+  if (cudaMalloc(&h->w_ukt, (size_t)num_heads * mla::kKvLora * mla::kNope * 2) != cudaSuccess) {
+    rc = MLA_ENOMEM;
+    goto fail;
+  }
+  if (mla::prepare_wide_kernel() != cudaSuccess ||
+      mla::transpose_w_uk(h->w_uk, h->w_ukt, num_heads, 0) != cudaSuccess ||
+      cudaStreamSynchronize(0) != cudaSuccess)
+    goto fail;
+  h->wide_ctas = h->num_sms & ~1;
+  if (encode_bf16_map(&h->wide_maps[0], w_qb, (int64_t)num_heads * mla::kHeadRows, mla::kQLora,
+                      128) != MLA_OK ||
+      encode_bf16_map(&h->wide_maps[1], w_qb, (int64_t)num_heads * mla::kHeadRows, mla::kQLora,
+                      64) != MLA_OK ||
+      encode_bf16_map(&h->wide_maps[2], h->w_ukt, (int64_t)num_heads * mla::kKvLora, mla::kNope,
+                      128) != MLA_OK ||
+      !mla::make_wide_split(num_heads, h->wide_ctas, &h->wide_split) ||
+      !mla::wide_kernel_fits(h->wide_ctas))
+    h->wide_ctas = 0;
 #ifdef MLA_TRACE
   {
     const size_t tb = (size_t)h->num_sms * mla::kTraceSlots * 8;
@@ -202,6 +246,7 @@ fail:
   if (h->scratch) cudaFree(h->scratch);
   if (h->partial) cudaFree(h->partial);
   if (h->w_uk_packed) cudaFree(h->w_uk_packed);
+  if (h->w_ukt) cudaFree(h->w_ukt);
   if (h->trace) cudaFree(h->trace);
   free(h);
   cudaGetLastError();
@@ -275,7 +320,24 @@ int mla_query_decode(mla_query_t h, int batch, const void* q_a, int64_t q_a_stri
   cudaError_t e;
   if (kern == Kernel::kHandoff)
     e = mla::launch_fused(a, &h->uk_map, nt, true, h->num_sms, st);
-  else if (kern == Kernel::kAbsorbPair && batch <= 16)
+  else if (kern == Kernel::kWide) {
+    // one launch per slice of 64 tokens, every per-token pointer offset
+    e = cudaSuccess;
+    const int tw = mla::wide_tokens();
+    for (int t0 = 0; t0 < batch && e == cudaSuccess; t0 += tw) {
+      mla::DecodeArgs s64 = a;
+      s64.batch = batch - t0 < tw ? batch - t0 : tw;
+      s64.groups = 1;
+      s64.q_a = a.q_a + (int64_t)t0 * a.q_a_stride;
+      s64.kv_c = a.kv_c + (int64_t)t0 * a.kv_c_stride;
+      s64.k_pe = a.k_pe + (int64_t)t0 * a.k_pe_stride;
+      s64.slots = a.slots + t0;
+      s64.q_latent = a.q_latent + (int64_t)t0 * h->heads * mla::kKvLora;
+      s64.q_pe = a.q_pe + (int64_t)t0 * h->heads * mla::kRope;
+      s64.q_c = a.q_c != nullptr ? a.q_c + (int64_t)t0 * mla::kQLora : nullptr;
+      e = mla::launch_wide(s64, h->wide_split, h->wide_maps, h->wide_ctas, st);
+    }
+  } else if (kern == Kernel::kAbsorbPair && batch <= 16)
     e = mla::launch_pair(a, h->pair_split, h->pair_ctas, nt, st);
   else if (kern == Kernel::kAbsorbPair) {
     // Batches above 16: the 16-token paired kernel once per slice of 16
@@ -350,6 +412,7 @@ void mla_query_destroy(mla_query_t h) {
   if (h->trace) cudaFree(h->trace);
   if (h->scratch) cudaFree(h->scratch);
   if (h->w_uk_packed) cudaFree(h->w_uk_packed);
+  if (h->w_ukt) cudaFree(h->w_ukt);
   if (h->partial) cudaFree(h->partial);
   free(h);
 }

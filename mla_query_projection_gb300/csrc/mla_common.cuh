@@ -1,0 +1,138 @@
+// mla_common.cuh - device pieces shared by the MLA query kernels: launch
+// geometry constants, named barriers, timeline stamps of trace builds and the
+// paged FP8 KV insert (page "mla.query", methods insert, kv_fp8, insert_ds).
+#pragma once
+
+#include "../../include/mla_query.h"
+#include "mla_device.cuh"
+#include "mla_internal.h"
+
+namespace mla {
+namespace {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;  // 256
+constexpr int kThreads = kConsumers + 32;        // + one producer warp
+constexpr int kPitch = kRowBytes + 64;           // 3136 B: conflict-free MMA loads
+constexpr long long kWaitLimit = 2000000000LL;   // ~1 s of SM clock
+
+// Named barriers (0 is __syncthreads).
+constexpr int kBarNorm = 1;       // warps 0-5: q_a RMSNorm
+constexpr int kBarInsert = 2;     // warps 6-7: KV insert
+constexpr int kBarConsumers = 3;  // warps 0-7
+
+__device__ __forceinline__ void named_barrier(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Timeline stamps (MLA_TRACE builds): slot 0 start, 1 producer ring filled,
+// 2 consumer prologue done, 3 first W_UK wait start, 4 its end, 5 end of the
+// nope phase, 6 last stage consumed, 7 end, 8..27 the time consumer thread 0
+// saw stage s's data, 28..47 the time the producer issued stage s, 48..63 the
+// time consumer thread 0 finished stage s (s < 16).
+// Trace builds: add a cycle count to a per-CTA slot (one thread per CTA).
+__device__ __forceinline__ void trace_add(const DecodeArgs& a, int slot, long long v) {
+#ifdef MLA_TRACE
+  if (a.trace != nullptr && slot < kTraceSlots)
+    a.trace[(int64_t)(blockIdx.y * gridDim.x + blockIdx.x) * kTraceSlots + slot] += (uint64_t)v;
+#else
+  (void)a;
+  (void)slot;
+  (void)v;
+#endif
+}
+
+__device__ __forceinline__ void trace_stamp(const DecodeArgs& a, int slot) {
+#ifdef MLA_TRACE
+  if (a.trace != nullptr && slot < kTraceSlots) {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    a.trace[(int64_t)(blockIdx.y * gridDim.x + blockIdx.x) * kTraceSlots + slot] = t;
+  }
+#else
+  (void)a;
+  (void)slot;
+#endif
+}
+
+// Paged FP8 KV insert of token b (page "mla.query", methods insert, kv_fp8,
+// insert_ds), run by the 64 threads of warps 6-7 (lt = 0..63) while warps 0-5
+// normalise q_a.  Thread lt owns latent columns 8*lt..8*lt+7; threads 0..7
+// also own k_pe values 8*lt..8*lt+7.  red2 holds the two warps' partial sums.
+__device__ void kv_insert(const DecodeArgs& a, int b, int lt, float* red2) {
+  const int lane = lt & 31, w = lt >> 5;
+  const int64_t slot = a.slots[b];
+  const uint4 v = *reinterpret_cast<const uint4*>(a.kv_c + (int64_t)b * a.kv_c_stride + 8 * lt);
+  const uint4 gv = *reinterpret_cast<const uint4*>(a.gamma_kv + 8 * lt);
+  uint4 pe = make_uint4(0, 0, 0, 0);
+  if (lt < 8) pe = *reinterpret_cast<const uint4*>(a.k_pe + (int64_t)b * a.k_pe_stride + 8 * lt);
+  const bool ds = a.layout == MLA_KV_FP8_DS_MLA;
+  const float ks = ds ? 1.0f : *a.k_scale;
+  float x[8];
+  const uint32_t xw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = bf16lo(xw[i]);
+    x[2 * i + 1] = bf16hi(xw[i]);
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) ss = fmaf(x[i], x[i], ss);
+  ss = warp_sum(ss);
+  if (lane == 0) red2[w] = ss;
+  named_barrier(kBarInsert, 64);
+  const float total = red2[0] + red2[1];
+  named_barrier(kBarInsert, 64);  // red2 may be reused by the next token
+  if (slot < 0) return;
+  const int64_t page = slot / a.page_size, off = slot % a.page_size;
+  if (page >= a.num_pages) {
+    if (lt == 0) atomicOr(a.err, MLA_DEVERR_BAD_SLOT);
+    return;
+  }
+  uint8_t* row = a.cache + (page * a.page_size + off) * (ds ? kRowDs : kRowE4m3);
+  const float rr = __frsqrt_rn(__fadd_rn(__fmul_rn(total, 1.0f / 512.0f), a.eps));
+  const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+  float n[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    n[2 * i] = bf_round(__fmul_rn(__fmul_rn(x[2 * i], rr), bf16lo(gw[i])));
+    n[2 * i + 1] = bf_round(__fmul_rn(__fmul_rn(x[2 * i + 1], rr), bf16hi(gw[i])));
+  }
+  uint2 out;
+  if (!ds) {
+    out.x = (uint32_t)e4m3x2(__fdiv_rn(n[0], ks), __fdiv_rn(n[1], ks)) |
+            ((uint32_t)e4m3x2(__fdiv_rn(n[2], ks), __fdiv_rn(n[3], ks)) << 16);
+    out.y = (uint32_t)e4m3x2(__fdiv_rn(n[4], ks), __fdiv_rn(n[5], ks)) |
+            ((uint32_t)e4m3x2(__fdiv_rn(n[6], ks), __fdiv_rn(n[7], ks)) << 16);
+  } else {
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(n[i]));
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const float scale = pow2_ceil_f32(fmaxf(__fdiv_rn(amax, 448.0f), 1e-4f));
+    const float inv = __fdiv_rn(1.0f, scale);  // exact: a power of two
+    out.x = (uint32_t)e4m3x2(n[0] * inv, n[1] * inv) |
+            ((uint32_t)e4m3x2(n[2] * inv, n[3] * inv) << 16);
+    out.y = (uint32_t)e4m3x2(n[4] * inv, n[5] * inv) |
+            ((uint32_t)e4m3x2(n[6] * inv, n[7] * inv) << 16);
+    if ((lane & 15) == 0) *reinterpret_cast<float*>(row + kDsScales + 4 * (lt >> 4)) = scale;
+  }
+  *reinterpret_cast<uint2*>(row + 8 * lt) = out;
+  if (lt < 8) {
+    if (ds) {
+      *reinterpret_cast<uint4*>(row + kDsRope + 16 * lt) = pe;
+    } else {
+      const uint32_t w2[4] = {pe.x, pe.y, pe.z, pe.w};
+      uint2 o2;
+      o2.x = (uint32_t)e4m3x2(__fdiv_rn(bf16lo(w2[0]), ks), __fdiv_rn(bf16hi(w2[0]), ks)) |
+             ((uint32_t)e4m3x2(__fdiv_rn(bf16lo(w2[1]), ks), __fdiv_rn(bf16hi(w2[1]), ks)) << 16);
+      o2.y = (uint32_t)e4m3x2(__fdiv_rn(bf16lo(w2[2]), ks), __fdiv_rn(bf16hi(w2[2]), ks)) |
+             ((uint32_t)e4m3x2(__fdiv_rn(bf16lo(w2[3]), ks), __fdiv_rn(bf16hi(w2[3]), ks)) << 16);
+      *reinterpret_cast<uint2*>(row + kKvLora + 8 * lt) = o2;
+    }
+  }
+}
+
+}  // namespace
+}  // namespace mla

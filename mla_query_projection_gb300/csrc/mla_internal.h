@@ -89,6 +89,22 @@ bool make_pair_split(int heads, int ctas, PairSplit* sp);
 // Whether `ctas` CTAs of the paired kernel (nt = 8 or 16 tokens) can all be
 // resident at once.
 bool pair_kernel_fits(int ctas, int nt);
+// Wide kernel (17-64 tokens, tcgen05, clusters of two CTAs splitting K): the
+// heads of pair c are [head[c], head[c + 1]) (at most two), its rope units
+// the heads [rope[c], rope[c + 1]).
+struct WideSplit {
+  uint16_t head[kMaxCtas / 2 + 1];
+  uint16_t rope[kMaxCtas / 2 + 1];
+};
+int wide_tokens();
+cudaError_t prepare_wide_kernel();
+bool wide_kernel_fits(int ctas);
+bool make_wide_split(int heads, int ctas, WideSplit* sp);
+// ukt[h][c][p] = w_uk[h][p][c] (the M x K operand of the absorption GEMM)
+cudaError_t transpose_w_uk(const uint16_t* w_uk, uint16_t* ukt, int heads, cudaStream_t stream);
+// maps[0]: W_QB, 64 x 128 boxes; maps[1]: W_QB, 64 x 64 boxes; maps[2]: W_UK^T, 64 x 128 boxes
+cudaError_t launch_wide(const DecodeArgs& a, const WideSplit& sp, const CUtensorMap* maps,
+                        int ctas, cudaStream_t stream);
 cudaError_t launch_pair(const DecodeArgs& a, const PairSplit& sp, int ctas, int nt,
                         cudaStream_t stream);
 cudaError_t launch_absorb(const DecodeArgs& a, const AbsSplit& sp, int nt, int ctas,

@@ -1,0 +1,561 @@
+// mla_wide.cu - the decode step for wide batches (17 to 64 tokens per launch)
+// on the 5th-generation tensor cores (tcgen05, accumulators in TMEM).
+//
+// What it computes is the step of page "mla.query", class MlaQuery (methods
+// kernel / tiled / insert / insert_ds / store_qc): q_a RMSNorm -> xq (q_c),
+// Q_B rows -> q (BF16, FP32 accumulate), rope rows -> q_pe, nope rows through
+// W_UK -> q_latent, and the paged FP8 KV insert.
+//
+// GB300 design.  A thread-block cluster of two CTAs splits K = 1536 in halves:
+// each CTA keeps its half of the normalised xq of all 64 tokens resident in
+// shared memory (the B operand, 96 KiB) and streams only its half of every
+// weight row, so each weight byte enters the GPU once for all the tokens.
+//  * Units of a pair (the same list on both CTAs): for each of its heads (at
+//    most two) NOPE (the head's 128 nope rows: one M = 128 tile, N = 64
+//    tokens, K = 768) then ABS (the absorption of that head), and then a
+//    byte-balancing share of ROPE units (one head's 64 rope rows).
+//  * A producer warp streams 2-D tensor-map boxes of 64 K-columns (128 B,
+//    swizzled) by TMA into a 4-slot ring; one thread issues tcgen05.mma from
+//    the ring and the resident xq, accumulating in TMEM, and commits each slot
+//    back to the producer.
+//  * The two K-half partial sums of a NOPE or ROPE tile are exchanged through
+//    distributed shared memory (st.async): rank r finishes tokens 32r..32r+31,
+//    adding the half of K 0..767 first.  For NOPE it writes the BF16 q as the
+//    B operand of the absorption (tokens x 128 rows, swizzled), which a second
+//    GEMM multiplies by W_UK^T (a copy made at create, [h][c][p]) into TMEM;
+//    the epilogue writes q_latent.
+// Every wait is bounded (MLA_DEVERR_TIMEOUT instead of a hang).
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "../../include/mla_query.h"
+#include "mla_common.cuh"
+#include "mla_device.cuh"
+#include "mla_internal.h"
+
+namespace mla {
+
+namespace {
+
+constexpr int kWideTok = 64;                 // tokens per launch (N of the Q_B GEMM)
+constexpr int kWideHalfTok = 32;             // tokens each CTA of the pair finishes
+constexpr int kWideKHalf = kQLora / 2;       // 768
+constexpr int kWideAtoms = kWideKHalf / 64;  // 12 K atoms of 64 columns (128 B)
+constexpr int kWideSlots = 4;
+constexpr int kWideBox = 128 * 128;          // one 128-row x 128 B box (16 KiB)
+constexpr int kWideThreads = 256;
+constexpr int kWideTmemCols = 256;           // D_qb x2 (64 each) + D_abs (4 x 32)
+
+enum WideUnit { kUnitNope = 0, kUnitAbs = 1, kUnitRope = 2 };
+
+struct WideSmem {
+  static constexpr int oXq = 0;                                  // [12][64 rows][128 B]
+  static constexpr int oRing = oXq + kWideAtoms * kWideTok * 128;   // 98304
+  static constexpr int oQt = oRing + kWideSlots * kWideBox;         // [2][32 rows][128 B]
+  static constexpr int oRecv = oQt + 2 * kWideHalfTok * 128;        // [2][128][32] FP32
+  static constexpr int oSs = oRecv + 2 * 128 * kWideHalfTok * 4;    // own [64], peer [64], red [8]
+  static constexpr int oBar = oSs + (2 * kWideTok + 8) * 4;
+  // barriers: full[4] empty[4] dready[2] dfree[2] qready absready absfree
+  //           recvfull[2] sendok[2] ssbar xqready tslot
+  static constexpr int kBars = 4 + 4 + 2 + 2 + 3 + 2 + 2 + 1 + 1;
+  static constexpr int oTslot = oBar + kBars * 8;
+  static constexpr int kBytes = oTslot + 16;
+  static constexpr int kAlloc = kBytes + 1024;  // base aligned up to 1 KiB (swizzle atoms)
+};
+
+// K-major SWIZZLE_128B shared-memory matrix descriptor (tcgen05): start
+// address, leading offset unused (1), 1024 B between 8-row groups, version 1.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor: BF16 x BF16 -> FP32, both K-major, M x N.
+__host__ __device__ constexpr uint32_t umma_idesc(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t idesc,
+                                     uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(da), "l"(db), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every tcgen05.mma this thread issued so far completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 lanes x 16 columns of FP32 from TMEM (lane base and column in `taddr`).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// Arrive on the mbarrier at `remote` (a shared::cluster address in the other
+// CTA of the pair).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote)
+               : "memory");
+}
+
+// Offset of element (row, col) of a K-major 128 B-swizzled block (col < 64).
+__device__ __forceinline__ int sw128(int row, int col) {
+  return row * 128 + ((((col >> 3) ^ row) & 7) << 4) + (col & 7) * 2;
+}
+
+// Units of pair c: for each head h in [head[c], head[c+1]) NOPE(h), ABS(h);
+// then ROPE(h) for h in [rope[c], rope[c+1]).
+struct WideSeq {
+  int h0, nh, r0, nr;
+  __device__ int units() const { return 2 * nh + nr; }
+  __device__ int kind(int u) const { return u < 2 * nh ? (u & 1) : kUnitRope; }
+  __device__ int head(int u) const { return u < 2 * nh ? h0 + (u >> 1) : r0 + (u - 2 * nh); }
+  __device__ int boxes(int u) const { return kind(u) == kUnitAbs ? 8 : kWideAtoms; }
+};
+
+__global__ void __launch_bounds__(kWideThreads, 1)
+    mla_wide_kernel(const DecodeArgs a, const __grid_constant__ WideSplit split,
+                    const __grid_constant__ CUtensorMap map_qb,
+                    const __grid_constant__ CUtensorMap map_qb64,
+                    const __grid_constant__ CUtensorMap map_ukt) {
+  using S = WideSmem;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::oBar);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + 4;
+  uint64_t* dready = bars + 8;
+  uint64_t* dfree = bars + 10;
+  uint64_t* qready = bars + 12;
+  uint64_t* absready = bars + 13;
+  uint64_t* absfree = bars + 14;
+  uint64_t* recvfull = bars + 15;
+  uint64_t* sendok = bars + 17;
+  uint64_t* ssbar = bars + 19;
+  uint64_t* xqready = bars + 20;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + S::oTslot);
+  float* ss_own = reinterpret_cast<float*>(smem + S::oSs);
+  float* ss_peer = ss_own + kWideTok;
+  float* red2 = ss_peer + kWideTok;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int i = blockIdx.x, P = gridDim.x;
+  const int pair = i >> 1, rank = i & 1;  // cluster (2, 1, 1)
+  const uint32_t peer = (uint32_t)(rank ^ 1);
+  const int H = a.heads;
+  const WideSeq seq{split.head[pair], split.head[pair + 1] - split.head[pair], split.rope[pair],
+                    split.rope[pair + 1] - split.rope[pair]};
+  const int nu = seq.units();
+
+  if (tid == 0) {
+    for (int s = 0; s < kWideSlots; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&dready[b], 1);
+      mbar_init(&dfree[b], 128);
+      mbar_init(&recvfull[b], 1);
+      mbar_init(&sendok[b], 1);
+    }
+    mbar_init(qready, 1);
+    mbar_init(absready, 1);
+    mbar_init(absfree, 128);
+    mbar_init(ssbar, 1);
+    mbar_init(xqready, 1);
+    // the other CTA's bytes: its sums of squares, and its first two tile halves
+    mbar_arrive_expect_tx(ssbar, kWideTok * 4);
+    mbar_arrive_expect_tx(&recvfull[0], 128 * kWideHalfTok * 4);
+    mbar_arrive_expect_tx(&recvfull[1], 128 * kWideHalfTok * 4);
+    mbar_fence_init();
+    pdl_launch_dependents();
+    prefetch_tensormap(&map_qb);
+    prefetch_tensormap(&map_qb64);
+    prefetch_tensormap(&map_ukt);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tslot)),
+                 "r"(kWideTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cluster_sync();  // both CTAs' barriers initialised and armed
+  const uint32_t tmem = *tslot;
+  bool timed_out = false;
+
+  if (warp == 0) {
+    // ================= producer: weight boxes, no PDL wait =============
+    if (lane == 0) {
+      int k = 0;  // box counter over all units
+      for (int u = 0; u < nu; ++u) {
+        const int kind = seq.kind(u), h = seq.head(u), nb = seq.boxes(u);
+        for (int bx = 0; bx < nb; ++bx, ++k) {
+          const int slot = k % kWideSlots;
+          if (k >= kWideSlots &&
+              !mbar_wait_bounded(&empty[slot], (uint32_t)(((k / kWideSlots) - 1) & 1), kWaitLimit))
+            timed_out = true;
+          uint8_t* dst = smem + S::oRing + slot * kWideBox;
+          if (kind == kUnitNope) {
+            mbar_arrive_expect_tx(&full[slot], kWideBox);
+            tma_g2s_2d(dst, &map_qb, 64 * (kWideAtoms * rank + bx), kHeadRows * h, &full[slot]);
+          } else if (kind == kUnitRope) {
+            mbar_arrive_expect_tx(&full[slot], kWideBox / 2);
+            tma_g2s_2d(dst, &map_qb64, 64 * (kWideAtoms * rank + bx), kHeadRows * h + kNope,
+                       &full[slot]);
+          } else {  // W_UK^T rows [512 h + 128 ct, +128), p atom pa
+            const int ct = bx >> 1, pa = bx & 1;
+            mbar_arrive_expect_tx(&full[slot], kWideBox);
+            tma_g2s_2d(dst, &map_ukt, 64 * pa, kKvLora * h + 128 * ct, &full[slot]);
+          }
+        }
+      }
+      // every issued box is consumed before the CTA may leave
+      for (int kk = k - kWideSlots > 0 ? k - kWideSlots : 0; kk < k; ++kk)
+        (void)mbar_wait_bounded(&empty[kk % kWideSlots], (uint32_t)((kk / kWideSlots) & 1),
+                                kWaitLimit);
+    }
+  } else if (warp == 1) {
+    // ================= MMA issuer ==================================
+    if (lane == 0) {
+      if (!mbar_wait_bounded(xqready, 0u, kWaitLimit)) timed_out = true;
+      tc_fence_after();
+      const uint32_t xq0 = smem_u32(smem + S::oXq), ring0 = smem_u32(smem + S::oRing),
+                     qt0 = smem_u32(smem + S::oQt);
+      int k = 0, nq = 0, na = 0;  // boxes, Q_B tiles, absorptions so far
+      for (int u = 0; u < nu; ++u) {
+        const int kind = seq.kind(u), nb = seq.boxes(u);
+        uint32_t dcol;
+        if (kind == kUnitAbs) {
+          // the q tile of this head is written; the previous absorption read out
+          if (!mbar_wait_bounded(qready, (uint32_t)(na & 1), kWaitLimit)) timed_out = true;
+          if (na > 0 && !mbar_wait_bounded(absfree, (uint32_t)((na - 1) & 1), kWaitLimit))
+            timed_out = true;
+          tc_fence_after();
+          dcol = 128;
+        } else {
+          const int b = nq & 1;
+          if (nq >= 2 && !mbar_wait_bounded(&dfree[b], (uint32_t)(((nq >> 1) - 1) & 1), kWaitLimit))
+            timed_out = true;
+          tc_fence_after();
+          dcol = 64 * b;
+        }
+        for (int bx = 0; bx < nb; ++bx, ++k) {
+          const int slot = k % kWideSlots;
+          if (!mbar_wait_bounded(&full[slot], (uint32_t)((k / kWideSlots) & 1), kWaitLimit))
+            timed_out = true;
+          tc_fence_after();
+          const uint32_t abase = ring0 + slot * kWideBox;
+          if (kind == kUnitAbs) {
+            const int ct = bx >> 1, pa = bx & 1;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma(tmem + dcol + kWideHalfTok * ct, umma_desc(abase + 32 * kk),
+                   umma_desc(qt0 + pa * (kWideHalfTok * 128) + 32 * kk),
+                   umma_idesc(128, kWideHalfTok), (pa | kk) != 0);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma(tmem + dcol, umma_desc(abase + 32 * kk),
+                   umma_desc(xq0 + bx * (kWideTok * 128) + 32 * kk), umma_idesc(128, kWideTok),
+                   (bx | kk) != 0);
+          }
+          umma_commit(&empty[slot]);  // the slot is free once these MMAs are done
+        }
+        if (kind == kUnitAbs) {
+          umma_commit(absready);
+          ++na;
+        } else {
+          umma_commit(&dready[nq & 1]);
+          ++nq;
+        }
+      }
+    }
+  } else {
+    // ================= warps 2-7: q_a RMSNorm of this K half -> xq =====
+    const int pw = warp - 2;  // 0..5
+    const int kbase = kWideKHalf * rank;
+    pdl_wait();
+    // raw q_a of token t into the swizzled xq atoms; sums of squares per token
+    for (int t = pw; t < kWideTok; t += 6) {
+      float ss = 0.f;
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        const int c = lane + 32 * j;  // 16-byte chunk 0..95 of the half row
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (t < a.batch)
+          v = *reinterpret_cast<const uint4*>(a.q_a + (int64_t)t * a.q_a_stride + kbase + 8 * c);
+        const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          ss = fmaf(bf16lo(ww[e]), bf16lo(ww[e]), ss);
+          ss = fmaf(bf16hi(ww[e]), bf16hi(ww[e]), ss);
+        }
+        const int col = 8 * c;  // column within the half
+        *reinterpret_cast<uint4*>(smem + S::oXq + (col >> 6) * (kWideTok * 128) +
+                                  sw128(t, col & 63)) = v;
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) ss_own[t] = ss;
+    }
+    named_barrier(4, 192);
+    // the other CTA needs this half's sums: 64 floats into its ss_peer
+    if (pw == 0 && lane < kWideTok / 4) {
+      const float4 v = *reinterpret_cast<const float4*>(ss_own + 4 * lane);
+      st_async_v4(mapa_shared(smem_u32(ss_peer + 4 * lane), peer), v.x, v.y, v.z, v.w,
+                  mapa_shared(smem_u32(ssbar), peer));
+    }
+    if (!mbar_wait_bounded(ssbar, 0u, kWaitLimit)) timed_out = true;
+    // normalise in place: xq = bf16((x * rr) * gamma_q), K half 0 summed first
+    for (int t = pw; t < kWideTok; t += 6) {
+      const float total = rank == 0 ? ss_own[t] + ss_peer[t] : ss_peer[t] + ss_own[t];
+      const float rr = __frsqrt_rn(__fadd_rn(__fdiv_rn(total, 1536.0f), a.eps));
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        const int c = lane + 32 * j, col = 8 * c;
+        uint4* px = reinterpret_cast<uint4*>(smem + S::oXq + (col >> 6) * (kWideTok * 128) +
+                                             sw128(t, col & 63));
+        uint4 o = make_uint4(0, 0, 0, 0);
+        if (t < a.batch) {
+          const uint4 v = *px;
+          const uint4 gv = *reinterpret_cast<const uint4*>(a.gamma_q + kbase + col);
+          const uint32_t ww[4] = {v.x, v.y, v.z, v.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+          uint32_t r[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            r[e] = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[e]), rr), bf16lo(gw[e])),
+                               __fmul_rn(__fmul_rn(bf16hi(ww[e]), rr), bf16hi(gw[e])));
+          o = make_uint4(r[0], r[1], r[2], r[3]);
+          if (a.q_c != nullptr && pair == 0)  // the first pair writes q_c
+            *reinterpret_cast<uint4*>(a.q_c + (int64_t)t * kQLora + kbase + col) = o;
+        }
+        *px = o;
+      }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // xq feeds the tensor cores
+    named_barrier(4, 192);
+    if (tid == 64) mbar_arrive(xqready);
+    // KV insert of token i (and i + P, ...) by warps 2-3
+    if (warp < 4)
+      for (int t = i; t < a.batch; t += P) kv_insert(a, t, tid - 64, red2);
+
+    if (warp >= 4) {
+      // ================= epilogue: TMEM lanes 0..127 ===================
+      const int m = tid - 128;  // row of the tile = TMEM lane
+      const uint32_t lane_base = (uint32_t)(32 * (warp - 4)) << 16;
+      const int my0 = kWideHalfTok * rank, peer0 = kWideHalfTok * (rank ^ 1);
+      int nq = 0, na = 0;
+      for (int u = 0; u < nu; ++u) {
+        const int kind = seq.kind(u), h = seq.head(u);
+        if (kind == kUnitAbs) {
+          if (!mbar_wait_bounded(absready, (uint32_t)(na & 1), kWaitLimit)) timed_out = true;
+          tc_fence_after();
+          const int64_t tstep = (int64_t)H * kKvLora;  // one token further in q_latent
+          const int nt_here = min(kWideHalfTok, a.batch - my0);
+#pragma unroll 1
+          for (int ct = 0; ct < 4; ++ct) {
+            float v[32];
+            tmem_ld16(tmem + lane_base + 128 + kWideHalfTok * ct, *reinterpret_cast<float(*)[16]>(v));
+            tmem_ld16(tmem + lane_base + 128 + kWideHalfTok * ct + 16,
+                      *reinterpret_cast<float(*)[16]>(v + 16));
+            uint16_t* d = a.q_latent + ((int64_t)my0 * H + h) * kKvLora + 128 * ct + m;
+#pragma unroll
+            for (int tl = 0; tl < kWideHalfTok; ++tl, d += tstep)
+              if (tl < nt_here) *d = f2bf_bits(v[tl]);
+          }
+          tc_fence_before();
+          mbar_arrive(absfree);
+          ++na;
+          continue;
+        }
+        // ---- a Q_B tile: this K half for 64 tokens -> exchange -> q --------
+        const int b = nq & 1;
+        if (!mbar_wait_bounded(&dready[b], (uint32_t)((nq >> 1) & 1), kWaitLimit)) timed_out = true;
+        tc_fence_after();
+        float q[kWideHalfTok];
+        // the other CTA's tokens of this row go into its receive buffer b
+        tmem_ld16(tmem + lane_base + 64 * b + peer0, *reinterpret_cast<float(*)[16]>(q));
+        tmem_ld16(tmem + lane_base + 64 * b + peer0 + 16, *reinterpret_cast<float(*)[16]>(q + 16));
+        if (nq >= 2 && !mbar_wait_bounded(&sendok[b], (uint32_t)(((nq >> 1) - 1) & 1), kWaitLimit))
+          timed_out = true;
+        {
+          const uint32_t rb = mapa_shared(smem_u32(&recvfull[b]), peer);
+          const uint32_t dst = smem_u32(smem + S::oRecv + (b * 128 + m) * kWideHalfTok * 4);
+#pragma unroll
+          for (int j = 0; j < kWideHalfTok; j += 4)
+            st_async_v4(mapa_shared(dst + 4 * j, peer), q[j], q[j + 1], q[j + 2], q[j + 3], rb);
+        }
+        // this CTA's tokens: its K half plus the other CTA's, K 0..767 first
+        tmem_ld16(tmem + lane_base + 64 * b + my0, *reinterpret_cast<float(*)[16]>(q));
+        tmem_ld16(tmem + lane_base + 64 * b + my0 + 16, *reinterpret_cast<float(*)[16]>(q + 16));
+        tc_fence_before();
+        mbar_arrive(&dfree[b]);
+        if (!mbar_wait_bounded(&recvfull[b], (uint32_t)((nq >> 1) & 1), kWaitLimit)) timed_out = true;
+        const float* rcv =
+            reinterpret_cast<const float*>(smem + S::oRecv + (b * 128 + m) * kWideHalfTok * 4);
+#pragma unroll
+        for (int j = 0; j < kWideHalfTok; ++j) q[j] = rank == 0 ? q[j] + rcv[j] : rcv[j] + q[j];
+        // buffer b is read: re-arm it for its next use, then let the other CTA send
+        named_barrier(5, 128);
+        if (m == 0) {
+          mbar_arrive_expect_tx(&recvfull[b], 128 * kWideHalfTok * 4);
+          mbar_arrive_remote(mapa_shared(smem_u32(&sendok[b]), peer));
+        }
+        if (kind == kUnitNope) {
+          // the previous absorption's MMAs are done reading the q tile
+          if (na > 0 && !mbar_wait_bounded(absready, (uint32_t)((na - 1) & 1), kWaitLimit))
+            timed_out = true;
+          // q^T tile: [token 0..31][row m] BF16, K-major swizzled, two atoms
+          uint8_t* qt = smem + S::oQt + (m >> 6) * (kWideHalfTok * 128);
+#pragma unroll
+          for (int tl = 0; tl < kWideHalfTok; ++tl)
+            *reinterpret_cast<uint16_t*>(qt + sw128(tl, m & 63)) = f2bf_bits(q[tl]);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          named_barrier(5, 128);
+          if (m == 0) mbar_arrive(qready);
+        } else if (m < kRope) {
+          const int nt_here = min(kWideHalfTok, a.batch - my0);
+          uint16_t* d = a.q_pe + ((int64_t)my0 * H + h) * kRope + m;
+#pragma unroll
+          for (int tl = 0; tl < kWideHalfTok; ++tl, d += (int64_t)H * kRope)
+            if (tl < nt_here) *d = f2bf_bits(q[tl]);
+        }
+        ++nq;
+      }
+    }
+  }
+
+  if (timed_out) atomicOr(a.err, MLA_DEVERR_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kWideTmemCols)
+                 : "memory");
+  }
+  // neither CTA leaves while the other may still write into its shared memory
+  cluster_sync_relaxed();
+}
+
+__global__ void transpose_w_uk_kernel(const uint16_t* __restrict__ w_uk, uint16_t* __restrict__ ukt,
+                                      int heads) {
+  // ukt[h][c][p] = w_uk[h][p][c]
+  const int64_t n = (int64_t)heads * kNope * kKvLora;
+  for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int p = (int)(e % kNope);
+    const int c = (int)((e / kNope) % kKvLora);
+    const int64_t h = e / ((int64_t)kNope * kKvLora);
+    ukt[e] = w_uk[(h * kNope + p) * kKvLora + c];
+  }
+}
+
+cudaLaunchConfig_t wide_config(int ctas, cudaStream_t stream, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ctas, 1, 1);
+  cfg.blockDim = dim3(kWideThreads, 1, 1);
+  cfg.dynamicSmemBytes = WideSmem::kAlloc;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cfg;
+}
+
+}  // namespace
+
+int wide_tokens() { return kWideTok; }
+
+cudaError_t prepare_wide_kernel() {
+  static_assert(WideSmem::kAlloc <= 232448, "shared memory budget");
+  return cudaFuncSetAttribute(mla_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              WideSmem::kAlloc);
+}
+
+bool wide_kernel_fits(int ctas) {
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = wide_config(ctas, nullptr, attr);
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, mla_wide_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return clusters >= ctas / 2;
+}
+
+bool make_wide_split(int heads, int ctas, WideSplit* sp) {
+  const int pairs = ctas / 2;
+  if (pairs < 1 || ctas > kMaxCtas) return false;
+  for (int c = 0; c <= pairs; ++c) sp->head[c] = (uint16_t)((int64_t)heads * c / pairs);
+  for (int c = 0; c < pairs; ++c)
+    if (sp->head[c + 1] - sp->head[c] > 2) return false;
+  // ROPE units (96 KiB per CTA each) fill every pair up to an even share of
+  // the bytes; a head's NOPE + ABS units are 320 KiB per CTA.
+  const int64_t hb = 20, rb = 6;  // in units of 16 KiB
+  const int64_t total = (int64_t)heads * (hb + rb);
+  int64_t head_bytes = 0;
+  int prev = 0;
+  sp->rope[0] = 0;
+  for (int c = 0; c < pairs; ++c) {
+    head_bytes += (int64_t)(sp->head[c + 1] - sp->head[c]) * hb;
+    int64_t r = (total * (c + 1) / pairs - head_bytes + rb / 2) / rb;
+    if (r < prev) r = prev;
+    if (r > heads) r = heads;
+    if (c == pairs - 1) r = heads;
+    sp->rope[c + 1] = (uint16_t)r;
+    prev = (int)r;
+  }
+  return true;
+}
+
+cudaError_t transpose_w_uk(const uint16_t* w_uk, uint16_t* ukt, int heads, cudaStream_t stream) {
+  transpose_w_uk_kernel<<<256, 256, 0, stream>>>(w_uk, ukt, heads);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wide(const DecodeArgs& a, const WideSplit& sp, const CUtensorMap* maps,
+                        int ctas, cudaStream_t stream) {
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = wide_config(ctas, stream, attr);
+  return cudaLaunchKernelEx(&cfg, mla_wide_kernel, a, sp, maps[0], maps[1], maps[2]);
+}
+
+}  // namespace mla
