@@ -41,7 +41,8 @@ constexpr int kWideTok = 64;                 // tokens per launch (N of the Q_B 
 constexpr int kWideHalfTok = 32;             // tokens each CTA of the pair finishes
 constexpr int kWideKHalf = kQLora / 2;       // 768
 constexpr int kWideAtoms = kWideKHalf / 64;  // 12 K atoms of 64 columns (128 B)
-constexpr int kWideSlots = 4;
+constexpr int kWideSlots = 5;
+constexpr int kWidePrefetch = 4;             // boxes prefetched into L2 beyond the ring
 constexpr int kWideBox = 128 * 128;          // one 128-row x 128 B box (16 KiB)
 constexpr int kWideThreads = 256;
 constexpr int kWideTmemCols = 256;           // D_qb x2 (64 each) + D_abs (4 x 32)
@@ -51,13 +52,14 @@ enum WideUnit { kUnitNope = 0, kUnitAbs = 1, kUnitRope = 2 };
 struct WideSmem {
   static constexpr int oXq = 0;                                  // [12][64 rows][128 B]
   static constexpr int oRing = oXq + kWideAtoms * kWideTok * 128;   // 98304
-  static constexpr int oQt = oRing + kWideSlots * kWideBox;         // [2][32 rows][128 B]
-  static constexpr int oRecv = oQt + 2 * kWideHalfTok * 128;        // [2][128][32] FP32
+  static constexpr int kQtBytes = 2 * kWideHalfTok * 128;          // one head: 2 atoms
+  static constexpr int oQt = oRing + kWideSlots * kWideBox;         // [2 heads][2][32 rows][128 B]
+  static constexpr int oRecv = oQt + 2 * kQtBytes;                  // [2][128][32] FP32
   static constexpr int oSs = oRecv + 2 * 128 * kWideHalfTok * 4;    // own [64], peer [64], red [8]
   static constexpr int oBar = oSs + (2 * kWideTok + 8) * 4;
-  // barriers: full[4] empty[4] dready[2] dfree[2] qready absready absfree
-  //           recvfull[2] sendok[2] ssbar xqready tslot
-  static constexpr int kBars = 4 + 4 + 2 + 2 + 3 + 2 + 2 + 1 + 1;
+  // barriers: full[5] empty[5] dready[2] dfree[2] qready[2] absready absfree
+  //           recvfull[2] sendok[2] ssbar xqready
+  static constexpr int kBars = 2 * kWideSlots + 2 + 2 + 2 + 2 + 2 + 2 + 1 + 1;
   static constexpr int oTslot = oBar + kBars * 8;
   static constexpr int kBytes = oTslot + 16;
   static constexpr int kAlloc = kBytes + 1024;  // base aligned up to 1 KiB (swizzle atoms)
@@ -130,13 +132,28 @@ __device__ __forceinline__ int sw128(int row, int col) {
   return row * 128 + ((((col >> 3) ^ row) & 7) << 4) + (col & 7) * 2;
 }
 
-// Units of pair c: for each head h in [head[c], head[c+1]) NOPE(h), ABS(h);
-// then ROPE(h) for h in [rope[c], rope[c+1]).
+// Units of pair c, heads [h0, h0 + nh) (nh <= 2) and rope units [r0, r0 + nr):
+// NOPE of every head, then ABS of every head, then the ROPE units - except
+// that a one-head pair puts one ROPE unit between its NOPE and its ABS.  Each
+// ABS thus follows an independent Q_B tile that keeps the tensor cores busy
+// while the epilogue exchanges and rounds the head's q.
 struct WideSeq {
   int h0, nh, r0, nr;
+  __device__ int ins() const { return (nh == 1 && nr > 0) ? 1 : 0; }
   __device__ int units() const { return 2 * nh + nr; }
-  __device__ int kind(int u) const { return u < 2 * nh ? (u & 1) : kUnitRope; }
-  __device__ int head(int u) const { return u < 2 * nh ? h0 + (u >> 1) : r0 + (u - 2 * nh); }
+  __device__ int kind(int u) const {
+    if (u < nh) return kUnitNope;
+    if (u < nh + ins()) return kUnitRope;
+    if (u < 2 * nh + ins()) return kUnitAbs;
+    return kUnitRope;
+  }
+  // head of a NOPE/ABS unit, or head whose rope rows a ROPE unit takes
+  __device__ int head(int u) const {
+    if (u < nh) return h0 + u;
+    if (u < nh + ins()) return r0;
+    if (u < 2 * nh + ins()) return h0 + (u - nh - ins());
+    return r0 + (u - 2 * nh);
+  }
   __device__ int boxes(int u) const { return kind(u) == kUnitAbs ? 8 : kWideAtoms; }
 };
 
@@ -151,16 +168,16 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::oBar);
   uint64_t* full = bars;
-  uint64_t* empty = bars + 4;
-  uint64_t* dready = bars + 8;
-  uint64_t* dfree = bars + 10;
-  uint64_t* qready = bars + 12;
-  uint64_t* absready = bars + 13;
-  uint64_t* absfree = bars + 14;
-  uint64_t* recvfull = bars + 15;
-  uint64_t* sendok = bars + 17;
-  uint64_t* ssbar = bars + 19;
-  uint64_t* xqready = bars + 20;
+  uint64_t* empty = bars + kWideSlots;
+  uint64_t* dready = bars + 2 * kWideSlots;
+  uint64_t* dfree = dready + 2;
+  uint64_t* qready = dfree + 2;
+  uint64_t* absready = qready + 2;
+  uint64_t* absfree = absready + 1;
+  uint64_t* recvfull = absfree + 1;
+  uint64_t* sendok = recvfull + 2;
+  uint64_t* ssbar = sendok + 2;
+  uint64_t* xqready = ssbar + 1;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + S::oTslot);
   float* ss_own = reinterpret_cast<float*>(smem + S::oSs);
   float* ss_peer = ss_own + kWideTok;
@@ -186,7 +203,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       mbar_init(&recvfull[b], 1);
       mbar_init(&sendok[b], 1);
     }
-    mbar_init(qready, 1);
+    mbar_init(&qready[0], 1);
+    mbar_init(&qready[1], 1);
     mbar_init(absready, 1);
     mbar_init(absfree, 128);
     mbar_init(ssbar, 1);
@@ -212,17 +230,45 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   __syncthreads();
   tc_fence_after();
   cluster_sync();  // both CTAs' barriers initialised and armed
+  if (tid == 0) trace_stamp(a, 0);
   const uint32_t tmem = *tslot;
   bool timed_out = false;
 
   if (warp == 0) {
     // ================= producer: weight boxes, no PDL wait =============
     if (lane == 0) {
+      // L2 prefetch kWidePrefetch boxes beyond the ring: a cursor (pu, pb)
+      // that runs ahead of the box being issued
+      int pu = 0, pb = 0, ahead = 0;
+      auto prefetch_next = [&](bool issue) {
+        while (pu < nu && pb >= seq.boxes(pu)) {
+          ++pu;
+          pb = 0;
+        }
+        if (pu >= nu) return;
+        const int kind = seq.kind(pu), h = seq.head(pu);
+        if (!issue) {
+          ++pb;
+          return;
+        }
+        if (kind == kUnitNope)
+          tma_prefetch_2d(&map_qb, 64 * (kWideAtoms * rank + pb), kHeadRows * h);
+        else if (kind == kUnitRope)
+          tma_prefetch_2d(&map_qb64, 64 * (kWideAtoms * rank + pb), kHeadRows * h + kNope);
+        else
+          tma_prefetch_2d(&map_ukt, 64 * (pb & 1), kKvLora * h + 128 * (pb >> 1));
+        ++pb;
+      };
       int k = 0;  // box counter over all units
       for (int u = 0; u < nu; ++u) {
         const int kind = seq.kind(u), h = seq.head(u), nb = seq.boxes(u);
         for (int bx = 0; bx < nb; ++bx, ++k) {
           const int slot = k % kWideSlots;
+          // keep the prefetch cursor kWideSlots + kWidePrefetch boxes ahead
+          while (ahead < k + kWideSlots + kWidePrefetch) {
+            prefetch_next(ahead >= kWideSlots);  // the first ring fill needs none
+            ++ahead;
+          }
           if (k >= kWideSlots &&
               !mbar_wait_bounded(&empty[slot], (uint32_t)(((k / kWideSlots) - 1) & 1), kWaitLimit))
             timed_out = true;
@@ -259,7 +305,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         uint32_t dcol;
         if (kind == kUnitAbs) {
           // the q tile of this head is written; the previous absorption read out
-          if (!mbar_wait_bounded(qready, (uint32_t)(na & 1), kWaitLimit)) timed_out = true;
+          if (!mbar_wait_bounded(&qready[na], 0u, kWaitLimit)) timed_out = true;
           if (na > 0 && !mbar_wait_bounded(absfree, (uint32_t)((na - 1) & 1), kWaitLimit))
             timed_out = true;
           tc_fence_after();
@@ -282,7 +328,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               umma(tmem + dcol + kWideHalfTok * ct, umma_desc(abase + 32 * kk),
-                   umma_desc(qt0 + pa * (kWideHalfTok * 128) + 32 * kk),
+                   umma_desc(qt0 + na * S::kQtBytes + pa * (kWideHalfTok * 128) + 32 * kk),
                    umma_idesc(128, kWideHalfTok), (pa | kk) != 0);
           } else {
 #pragma unroll
@@ -300,6 +346,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           umma_commit(&dready[nq & 1]);
           ++nq;
         }
+        if (u < 16) trace_stamp(a, 8 + u);  // unit u's MMAs issued
       }
     }
   } else {
@@ -307,24 +354,36 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     const int pw = warp - 2;  // 0..5
     const int kbase = kWideKHalf * rank;
     pdl_wait();
-    // raw q_a of token t into the swizzled xq atoms; sums of squares per token
+    if (tid == 64) trace_stamp(a, 3);
+    // raw q_a of this K half into the swizzled xq atoms: 16-byte async copies,
+    // all in flight at once (rows of tokens beyond the batch are zeroed)
+    for (int e = tid - 64; e < kWideTok * (kWideKHalf / 8); e += 192) {
+      const int t = e / (kWideKHalf / 8), c = e % (kWideKHalf / 8), col = 8 * c;
+      uint8_t* dst = smem + S::oXq + (col >> 6) * (kWideTok * 128) + sw128(t, col & 63);
+      if (t < a.batch) {
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)),
+                     "l"(a.q_a + (int64_t)t * a.q_a_stride + kbase + col)
+                     : "memory");
+      } else {
+        *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+      }
+    }
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+    named_barrier(4, 192);
+    // sums of squares per token over this half
     for (int t = pw; t < kWideTok; t += 6) {
       float ss = 0.f;
 #pragma unroll
       for (int j = 0; j < 3; ++j) {
-        const int c = lane + 32 * j;  // 16-byte chunk 0..95 of the half row
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (t < a.batch)
-          v = *reinterpret_cast<const uint4*>(a.q_a + (int64_t)t * a.q_a_stride + kbase + 8 * c);
+        const int col = 8 * (lane + 32 * j);
+        const uint4 v = *reinterpret_cast<const uint4*>(smem + S::oXq + (col >> 6) * (kWideTok * 128) +
+                                                        sw128(t, col & 63));
         const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           ss = fmaf(bf16lo(ww[e]), bf16lo(ww[e]), ss);
           ss = fmaf(bf16hi(ww[e]), bf16hi(ww[e]), ss);
         }
-        const int col = 8 * c;  // column within the half
-        *reinterpret_cast<uint4*>(smem + S::oXq + (col >> 6) * (kWideTok * 128) +
-                                  sw128(t, col & 63)) = v;
       }
       ss = warp_sum(ss);
       if (lane == 0) ss_own[t] = ss;
@@ -338,6 +397,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     }
     if (!mbar_wait_bounded(ssbar, 0u, kWaitLimit)) timed_out = true;
     // normalise in place: xq = bf16((x * rr) * gamma_q), K half 0 summed first
+    uint4 gam[3];
+#pragma unroll
+    for (int j = 0; j < 3; ++j)
+      gam[j] = *reinterpret_cast<const uint4*>(a.gamma_q + kbase + 8 * (lane + 32 * j));
     for (int t = pw; t < kWideTok; t += 6) {
       const float total = rank == 0 ? ss_own[t] + ss_peer[t] : ss_peer[t] + ss_own[t];
       const float rr = __frsqrt_rn(__fadd_rn(__fdiv_rn(total, 1536.0f), a.eps));
@@ -349,7 +412,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         uint4 o = make_uint4(0, 0, 0, 0);
         if (t < a.batch) {
           const uint4 v = *px;
-          const uint4 gv = *reinterpret_cast<const uint4*>(a.gamma_q + kbase + col);
+          const uint4 gv = gam[j];
           const uint32_t ww[4] = {v.x, v.y, v.z, v.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
           uint32_t r[4];
 #pragma unroll
@@ -365,7 +428,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // xq feeds the tensor cores
     named_barrier(4, 192);
-    if (tid == 64) mbar_arrive(xqready);
+    if (tid == 64) {
+      mbar_arrive(xqready);
+      trace_stamp(a, 2);
+    }
     // KV insert of token i (and i + P, ...) by warps 2-3
     if (warp < 4)
       for (int t = i; t < a.batch; t += P) kv_insert(a, t, tid - 64, red2);
@@ -397,6 +463,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           tc_fence_before();
           mbar_arrive(absfree);
           ++na;
+          if (m == 0 && u < 16) trace_stamp(a, 28 + u);  // unit u's epilogue done
           continue;
         }
         // ---- a Q_B tile: this K half for 64 tokens -> exchange -> q --------
@@ -433,17 +500,16 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           mbar_arrive_remote(mapa_shared(smem_u32(&sendok[b]), peer));
         }
         if (kind == kUnitNope) {
-          // the previous absorption's MMAs are done reading the q tile
-          if (na > 0 && !mbar_wait_bounded(absready, (uint32_t)((na - 1) & 1), kWaitLimit))
-            timed_out = true;
-          // q^T tile: [token 0..31][row m] BF16, K-major swizzled, two atoms
-          uint8_t* qt = smem + S::oQt + (m >> 6) * (kWideHalfTok * 128);
+          // q^T tile of head j of the pair: [token 0..31][row m] BF16,
+          // K-major swizzled, two atoms (each head has its own tile)
+          const int j = h - seq.h0;
+          uint8_t* qt = smem + S::oQt + j * S::kQtBytes + (m >> 6) * (kWideHalfTok * 128);
 #pragma unroll
           for (int tl = 0; tl < kWideHalfTok; ++tl)
             *reinterpret_cast<uint16_t*>(qt + sw128(tl, m & 63)) = f2bf_bits(q[tl]);
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           named_barrier(5, 128);
-          if (m == 0) mbar_arrive(qready);
+          if (m == 0) mbar_arrive(&qready[j]);
         } else if (m < kRope) {
           const int nt_here = min(kWideHalfTok, a.batch - my0);
           uint16_t* d = a.q_pe + ((int64_t)my0 * H + h) * kRope + m;
@@ -452,7 +518,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             if (tl < nt_here) *d = f2bf_bits(q[tl]);
         }
         ++nq;
+        if (m == 0 && u < 16) trace_stamp(a, 28 + u);  // unit u's epilogue done
       }
+      if (m == 0) trace_stamp(a, 6);
     }
   }
 
@@ -467,6 +535,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   }
   // neither CTA leaves while the other may still write into its shared memory
   cluster_sync_relaxed();
+  if (tid == 0) trace_stamp(a, 7);
 }
 
 __global__ void transpose_w_uk_kernel(const uint16_t* __restrict__ w_uk, uint16_t* __restrict__ ukt,
