@@ -83,10 +83,11 @@ def kernel_for(path: int, batch: int) -> str:
 def launches_per_step(path: int, batch: int) -> int:
     """Kernels one decode call launches: the FMA absorbing kernel is followed by
     the head-closing kernel; the paired kernel runs once per 16 tokens up to 32
-    tokens, the wide tcgen05 kernel once per 64 tokens above."""
+    tokens, above that the wide tcgen05 kernel (after its normalising kernel)
+    once per 64 tokens."""
     if path == 1:
         return 2
-    return -(-batch // 64) if batch > 32 else -(-batch // 16)
+    return 2 * -(-batch // 64) if batch > 32 else -(-batch // 16)
 
 
 def profile_name(kernel: str, workload: str) -> str:

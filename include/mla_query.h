@@ -85,14 +85,17 @@ typedef struct mla_query* mla_query_t;
  *   gamma_q   device BF16 [1536], gamma_kv device BF16 [512].
  *   eps       RMSNorm epsilon used by both norms.
  *
- * W_QB and the gammas are borrowed, not copied: they must stay valid and
- * unchanged until mla_query_destroy.  W_UK is copied once, here, into a
- * library-owned layout of contiguous 64-column tiles (H * 128 KiB), so later
- * changes to the caller's W_UK are not seen (create a new handle instead).
- * create allocates that copy and the handle's small device scratch (query
- * hand-off buffer, counters, error flag) with cudaMalloc on the current
- * device, and synchronises the legacy default stream; the handle may only be
- * used on that device.
+ * W_QB, W_UK and the gammas are borrowed: they must stay valid and unchanged
+ * until mla_query_destroy.  Batches of up to 32 tokens read W_QB, W_UK and
+ * the gammas in place.  create also copies the weights once into
+ * library-owned tiled layouts - W_UK in contiguous 64-column units (H * 128
+ * KiB) for the allocation-free hand-off path, and W_QB (H * 576 KiB) and
+ * W_UK^T (H * 128 KiB) in swizzled 16 KiB tiles for batches above 32 - so a
+ * changed weight would be seen by some batch sizes and not by others (create
+ * a new handle instead).  create allocates those copies and the handle's
+ * device scratch (partials, counters, error flag) with cudaMalloc on the
+ * current device, and synchronises the legacy default stream; the handle may
+ * only be used on that device.
  * Returns MLA_OK, MLA_EINVAL, MLA_ENOMEM or MLA_ECUDA.
  */
 MLA_API int mla_query_create(mla_query_t* out, int num_heads, const void* w_qb,

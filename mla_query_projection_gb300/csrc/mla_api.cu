@@ -30,8 +30,9 @@ struct mla_query {
   mla::PairSplit pair_split;  // paired absorbing kernel: per-pair heads, per-CTA rope
   int pair_ctas;              // its grid (even), 0 if it cannot run on this device
   bool pair16;                // its 16-token flavour can run too
-  uint16_t* w_ukt;            // wide kernel: library-owned W_UK^T [H][512][128]
-  CUtensorMap wide_maps[3];   // W_QB (64 x 128 and 64 x 64 boxes), W_UK^T (64 x 128)
+  uint8_t* wide_qb;           // wide kernel: library-owned W_QB tiles
+  uint8_t* wide_ukt;          // wide kernel: library-owned W_UK^T tiles
+  uint8_t* wide_xq;           // wide kernel: normalised xq in tile layout
   mla::WideSplit wide_split;  // per-pair heads and rope units
   int wide_ctas;              // its grid (even), 0 if it cannot run on this device
 };
@@ -63,21 +64,6 @@ int encode_uk_map(CUtensorMap* map, const void* w_uk, int heads) {
   cuuint32_t box[2] = {(cuuint32_t)mla::kUkCols, (cuuint32_t)mla::kNope};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w_uk), dims,
-                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? MLA_OK : MLA_ECUDA;
-}
-
-// A 2-D BF16 tensor map [rows][cols] (row-major), boxes of box_rows x 64
-// columns (128 B rows, 128 B swizzle).
-int encode_bf16_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-  if (enc == nullptr) return MLA_ECUDA;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MLA_OK : MLA_ECUDA;
@@ -215,22 +201,22 @@ int mla_query_create(mla_query_t* out, int num_heads, const void* w_qb, const vo
       cudaStreamSynchronize(0) != cudaSuccess)
     goto fail;
   // Wide kernel (17 tokens and more): W_UK^T copy, tensor maps, pair split.
-  if (cudaMalloc(&h->w_ukt, (size_t)num_heads * mla::kKvLora * mla::kNope * 2) != cudaSuccess) {
+  if (cudaMalloc(&h->wide_xq, mla::wide_xq_bytes()) != cudaSuccess) {
+    rc = MLA_ENOMEM;
+    goto fail;
+  }
+  if (cudaMalloc(&h->wide_qb, mla::wide_qb_bytes(num_heads)) != cudaSuccess ||
+      cudaMalloc(&h->wide_ukt, mla::wide_ukt_bytes(num_heads)) != cudaSuccess) {
     rc = MLA_ENOMEM;
     goto fail;
   }
   if (mla::prepare_wide_kernel() != cudaSuccess ||
-      mla::transpose_w_uk(h->w_uk, h->w_ukt, num_heads, 0) != cudaSuccess ||
+      mla::pack_wide_weights(h->w_qb, h->w_uk, h->wide_qb, h->wide_ukt, num_heads, 0) !=
+          cudaSuccess ||
       cudaStreamSynchronize(0) != cudaSuccess)
     goto fail;
   h->wide_ctas = h->num_sms & ~1;
-  if (encode_bf16_map(&h->wide_maps[0], w_qb, (int64_t)num_heads * mla::kHeadRows, mla::kQLora,
-                      128) != MLA_OK ||
-      encode_bf16_map(&h->wide_maps[1], w_qb, (int64_t)num_heads * mla::kHeadRows, mla::kQLora,
-                      64) != MLA_OK ||
-      encode_bf16_map(&h->wide_maps[2], h->w_ukt, (int64_t)num_heads * mla::kKvLora, mla::kNope,
-                      128) != MLA_OK ||
-      !mla::make_wide_split(num_heads, h->wide_ctas, &h->wide_split) ||
+  if (!mla::make_wide_split(num_heads, h->wide_ctas, &h->wide_split) ||
       !mla::wide_kernel_fits(h->wide_ctas))
     h->wide_ctas = 0;
 #ifdef MLA_TRACE
@@ -246,7 +232,9 @@ fail:
   if (h->scratch) cudaFree(h->scratch);
   if (h->partial) cudaFree(h->partial);
   if (h->w_uk_packed) cudaFree(h->w_uk_packed);
-  if (h->w_ukt) cudaFree(h->w_ukt);
+  if (h->wide_qb) cudaFree(h->wide_qb);
+  if (h->wide_ukt) cudaFree(h->wide_ukt);
+  if (h->wide_xq) cudaFree(h->wide_xq);
   if (h->trace) cudaFree(h->trace);
   free(h);
   cudaGetLastError();
@@ -314,6 +302,9 @@ int mla_query_decode(mla_query_t h, int batch, const void* q_a, int64_t q_a_stri
   a.groups = (batch + nt - 1) / nt;
   a.eps = h->eps;
   a.trace = h->trace;
+  a.wide_xq = h->wide_xq;
+  a.wide_qb = h->wide_qb;
+  a.wide_ukt = h->wide_ukt;
   if (a.groups > h->num_sms) return MLA_EUNSUPPORTED;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -335,7 +326,7 @@ int mla_query_decode(mla_query_t h, int batch, const void* q_a, int64_t q_a_stri
       s64.q_latent = a.q_latent + (int64_t)t0 * h->heads * mla::kKvLora;
       s64.q_pe = a.q_pe + (int64_t)t0 * h->heads * mla::kRope;
       s64.q_c = a.q_c != nullptr ? a.q_c + (int64_t)t0 * mla::kQLora : nullptr;
-      e = mla::launch_wide(s64, h->wide_split, h->wide_maps, h->wide_ctas, st);
+      e = mla::launch_wide(s64, h->wide_split, h->wide_ctas, st);
     }
   } else if (kern == Kernel::kAbsorbPair && batch <= 16)
     e = mla::launch_pair(a, h->pair_split, h->pair_ctas, nt, st);
@@ -412,7 +403,9 @@ void mla_query_destroy(mla_query_t h) {
   if (h->trace) cudaFree(h->trace);
   if (h->scratch) cudaFree(h->scratch);
   if (h->w_uk_packed) cudaFree(h->w_uk_packed);
-  if (h->w_ukt) cudaFree(h->w_ukt);
+  if (h->wide_qb) cudaFree(h->wide_qb);
+  if (h->wide_ukt) cudaFree(h->wide_ukt);
+  if (h->wide_xq) cudaFree(h->wide_xq);
   if (h->partial) cudaFree(h->partial);
   free(h);
 }

@@ -61,6 +61,13 @@ struct DecodeArgs {
   int batch;
   int groups;                // token groups (grid.y)
   float eps;
+  // Wide kernel: normalised xq of up to 64 tokens, laid out as the wide CTAs'
+  // swizzled shared-memory tiles ([2 K halves][12 atoms][64 rows][128 B]).
+  uint8_t* wide_xq;
+  // Wide kernel: W_QB and W_UK^T copied at create into 16 KiB tiles in the
+  // swizzled shared-memory layout (see pack_wide_weights).
+  const uint8_t* wide_qb;
+  const uint8_t* wide_ukt;
   // Timeline records (builds with MLA_TRACE only; null otherwise):
   // per CTA kTraceSlots globaltimer stamps, see mla_fused.cu.
   uint64_t* trace;
@@ -100,11 +107,13 @@ int wide_tokens();
 cudaError_t prepare_wide_kernel();
 bool wide_kernel_fits(int ctas);
 bool make_wide_split(int heads, int ctas, WideSplit* sp);
-// ukt[h][c][p] = w_uk[h][p][c] (the M x K operand of the absorption GEMM)
-cudaError_t transpose_w_uk(const uint16_t* w_uk, uint16_t* ukt, int heads, cudaStream_t stream);
-// maps[0]: W_QB, 64 x 128 boxes; maps[1]: W_QB, 64 x 64 boxes; maps[2]: W_UK^T, 64 x 128 boxes
-cudaError_t launch_wide(const DecodeArgs& a, const WideSplit& sp, const CUtensorMap* maps,
-                        int ctas, cudaStream_t stream);
+// Tiled copies of the weights for the wide kernel (bytes, and the packing).
+size_t wide_qb_bytes(int heads);
+size_t wide_ukt_bytes(int heads);
+cudaError_t pack_wide_weights(const uint16_t* w_qb, const uint16_t* w_uk, uint8_t* qb_tiles,
+                              uint8_t* ukt_tiles, int heads, cudaStream_t stream);
+cudaError_t launch_wide(const DecodeArgs& a, const WideSplit& sp, int ctas, cudaStream_t stream);
+size_t wide_xq_bytes();
 cudaError_t launch_pair(const DecodeArgs& a, const PairSplit& sp, int ctas, int nt,
                         cudaStream_t stream);
 cudaError_t launch_absorb(const DecodeArgs& a, const AbsSplit& sp, int nt, int ctas,

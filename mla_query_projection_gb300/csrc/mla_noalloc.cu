@@ -168,6 +168,9 @@ extern "C" MLA_API int mla_query_decode_noalloc(
   a.groups = groups;
   a.eps = eps;
   a.trace = nullptr;
+  a.wide_xq = nullptr;
+  a.wide_qb = nullptr;
+  a.wide_ukt = nullptr;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The array keeps the previous call's contents: the counters must start at

@@ -13,11 +13,12 @@
 //  * Units of a pair (the same list on both CTAs): for each of its heads (at
 //    most two) NOPE (the head's 128 nope rows: one M = 128 tile, N = 64
 //    tokens, K = 768) then ABS (the absorption of that head), and then a
-//    byte-balancing share of ROPE units (one head's 64 rope rows).
-//  * A producer warp streams 2-D tensor-map boxes of 64 K-columns (128 B,
-//    swizzled) by TMA into a 4-slot ring; one thread issues tcgen05.mma from
-//    the ring and the resident xq, accumulating in TMEM, and commits each slot
-//    back to the producer.
+//    byte-balancing share of ROPE units (the 64 rope rows of two heads).
+//  * The weights are copied at create into 16 KiB tiles (128 rows x 64
+//    K-columns, already in the swizzled shared-memory layout), so a producer
+//    warp streams each tile with one 1-D bulk TMA copy into a 5-slot ring;
+//    one thread issues tcgen05.mma from the ring and the resident xq,
+//    accumulating in TMEM, and commits each slot back to the producer.
 //  * The two K-half partial sums of a NOPE or ROPE tile are exchanged through
 //    distributed shared memory (st.async): rank r finishes tokens 32r..32r+31,
 //    adding the half of K 0..767 first.  For NOPE it writes the BF16 q as the
@@ -42,7 +43,7 @@ constexpr int kWideHalfTok = 32;             // tokens each CTA of the pair fini
 constexpr int kWideKHalf = kQLora / 2;       // 768
 constexpr int kWideAtoms = kWideKHalf / 64;  // 12 K atoms of 64 columns (128 B)
 constexpr int kWideSlots = 5;
-constexpr int kWidePrefetch = 4;             // boxes prefetched into L2 beyond the ring
+constexpr int kWidePrefetch = 12;            // boxes prefetched into L2 beyond the ring
 constexpr int kWideBox = 128 * 128;          // one 128-row x 128 B box (16 KiB)
 constexpr int kWideThreads = 256;
 constexpr int kWideTmemCols = 256;           // D_qb x2 (64 each) + D_abs (4 x 32)
@@ -147,7 +148,7 @@ struct WideSeq {
     if (u < 2 * nh + ins()) return kUnitAbs;
     return kUnitRope;
   }
-  // head of a NOPE/ABS unit, or head whose rope rows a ROPE unit takes
+  // head of a NOPE/ABS unit, or rope unit (heads 2 r, 2 r + 1) of a ROPE unit
   __device__ int head(int u) const {
     if (u < nh) return h0 + u;
     if (u < nh + ins()) return r0;
@@ -157,11 +158,21 @@ struct WideSeq {
   __device__ int boxes(int u) const { return kind(u) == kUnitAbs ? 8 : kWideAtoms; }
 };
 
+// Tile addresses in the packed copies (pack_wide_weights): NOPE tile
+// (h, K half, atom), ROPE tile (rope unit, K half, atom), W_UK^T tile
+// (h, 128-column tile ct, 64-row atom pa).
+__device__ __forceinline__ const uint8_t* wide_tile(const DecodeArgs& a, int kind, int h,
+                                                    int half, int bx) {
+  if (kind == kUnitNope)
+    return a.wide_qb + ((size_t)(h * 2 + half) * kWideAtoms + bx) * kWideBox;
+  if (kind == kUnitRope)
+    return a.wide_qb + ((size_t)a.heads * 2 * kWideAtoms + (size_t)(h * 2 + half) * kWideAtoms + bx) *
+                           kWideBox;
+  return a.wide_ukt + ((size_t)h * 8 + bx) * kWideBox;  // bx = 2 ct + pa
+}
+
 __global__ void __launch_bounds__(kWideThreads, 1)
-    mla_wide_kernel(const DecodeArgs a, const __grid_constant__ WideSplit split,
-                    const __grid_constant__ CUtensorMap map_qb,
-                    const __grid_constant__ CUtensorMap map_qb64,
-                    const __grid_constant__ CUtensorMap map_ukt) {
+    mla_wide_kernel(const DecodeArgs a, const __grid_constant__ WideSplit split) {
   using S = WideSmem;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -179,9 +190,6 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   uint64_t* ssbar = sendok + 2;
   uint64_t* xqready = ssbar + 1;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + S::oTslot);
-  float* ss_own = reinterpret_cast<float*>(smem + S::oSs);
-  float* ss_peer = ss_own + kWideTok;
-  float* red2 = ss_peer + kWideTok;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int i = blockIdx.x, P = gridDim.x;
@@ -209,15 +217,11 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     mbar_init(absfree, 128);
     mbar_init(ssbar, 1);
     mbar_init(xqready, 1);
-    // the other CTA's bytes: its sums of squares, and its first two tile halves
-    mbar_arrive_expect_tx(ssbar, kWideTok * 4);
+    // the other CTA's bytes: its first two tile halves
     mbar_arrive_expect_tx(&recvfull[0], 128 * kWideHalfTok * 4);
     mbar_arrive_expect_tx(&recvfull[1], 128 * kWideHalfTok * 4);
     mbar_fence_init();
     pdl_launch_dependents();
-    prefetch_tensormap(&map_qb);
-    prefetch_tensormap(&map_qb64);
-    prefetch_tensormap(&map_ukt);
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -235,8 +239,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   bool timed_out = false;
 
   if (warp == 0) {
-    // ================= producer: weight boxes, no PDL wait =============
+    // ================= producer: weight tiles, no PDL wait =============
     if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_first();
       // L2 prefetch kWidePrefetch boxes beyond the ring: a cursor (pu, pb)
       // that runs ahead of the box being issued
       int pu = 0, pb = 0, ahead = 0;
@@ -246,17 +251,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           pb = 0;
         }
         if (pu >= nu) return;
-        const int kind = seq.kind(pu), h = seq.head(pu);
-        if (!issue) {
-          ++pb;
-          return;
-        }
-        if (kind == kUnitNope)
-          tma_prefetch_2d(&map_qb, 64 * (kWideAtoms * rank + pb), kHeadRows * h);
-        else if (kind == kUnitRope)
-          tma_prefetch_2d(&map_qb64, 64 * (kWideAtoms * rank + pb), kHeadRows * h + kNope);
-        else
-          tma_prefetch_2d(&map_ukt, 64 * (pb & 1), kKvLora * h + 128 * (pb >> 1));
+        if (issue) bulk_prefetch_l2(wide_tile(a, seq.kind(pu), seq.head(pu), rank, pb), kWideBox);
         ++pb;
       };
       int k = 0;  // box counter over all units
@@ -273,18 +268,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
               !mbar_wait_bounded(&empty[slot], (uint32_t)(((k / kWideSlots) - 1) & 1), kWaitLimit))
             timed_out = true;
           uint8_t* dst = smem + S::oRing + slot * kWideBox;
-          if (kind == kUnitNope) {
-            mbar_arrive_expect_tx(&full[slot], kWideBox);
-            tma_g2s_2d(dst, &map_qb, 64 * (kWideAtoms * rank + bx), kHeadRows * h, &full[slot]);
-          } else if (kind == kUnitRope) {
-            mbar_arrive_expect_tx(&full[slot], kWideBox / 2);
-            tma_g2s_2d(dst, &map_qb64, 64 * (kWideAtoms * rank + bx), kHeadRows * h + kNope,
-                       &full[slot]);
-          } else {  // W_UK^T rows [512 h + 128 ct, +128), p atom pa
-            const int ct = bx >> 1, pa = bx & 1;
-            mbar_arrive_expect_tx(&full[slot], kWideBox);
-            tma_g2s_2d(dst, &map_ukt, 64 * pa, kKvLora * h + 128 * ct, &full[slot]);
-          }
+          mbar_arrive_expect_tx(&full[slot], kWideBox);
+          bulk_g2s_hint(dst, wide_tile(a, kind, h, rank, bx), kWideBox, &full[slot], pol);
         }
       }
       // every issued box is consumed before the CTA may leave
@@ -296,6 +281,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     // ================= MMA issuer ==================================
     if (lane == 0) {
       if (!mbar_wait_bounded(xqready, 0u, kWaitLimit)) timed_out = true;
+      trace_stamp(a, 2);
       tc_fence_after();
       const uint32_t xq0 = smem_u32(smem + S::oXq), ring0 = smem_u32(smem + S::oRing),
                      qt0 = smem_u32(smem + S::oQt);
@@ -350,91 +336,18 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       }
     }
   } else {
-    // ================= warps 2-7: q_a RMSNorm of this K half -> xq =====
-    const int pw = warp - 2;  // 0..5
-    const int kbase = kWideKHalf * rank;
+    // ================= warps 2-7: this K half of xq, then the epilogue ==
+    // The normalising kernel launched just before wrote xq in this tile's
+    // layout; twelve bulk copies (one per 64-column atom) bring this half in.
     pdl_wait();
-    if (tid == 64) trace_stamp(a, 3);
-    // raw q_a of this K half into the swizzled xq atoms: 16-byte async copies,
-    // all in flight at once (rows of tokens beyond the batch are zeroed)
-    for (int e = tid - 64; e < kWideTok * (kWideKHalf / 8); e += 192) {
-      const int t = e / (kWideKHalf / 8), c = e % (kWideKHalf / 8), col = 8 * c;
-      uint8_t* dst = smem + S::oXq + (col >> 6) * (kWideTok * 128) + sw128(t, col & 63);
-      if (t < a.batch) {
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)),
-                     "l"(a.q_a + (int64_t)t * a.q_a_stride + kbase + col)
-                     : "memory");
-      } else {
-        *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-      }
-    }
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-    named_barrier(4, 192);
-    // sums of squares per token over this half
-    for (int t = pw; t < kWideTok; t += 6) {
-      float ss = 0.f;
-#pragma unroll
-      for (int j = 0; j < 3; ++j) {
-        const int col = 8 * (lane + 32 * j);
-        const uint4 v = *reinterpret_cast<const uint4*>(smem + S::oXq + (col >> 6) * (kWideTok * 128) +
-                                                        sw128(t, col & 63));
-        const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          ss = fmaf(bf16lo(ww[e]), bf16lo(ww[e]), ss);
-          ss = fmaf(bf16hi(ww[e]), bf16hi(ww[e]), ss);
-        }
-      }
-      ss = warp_sum(ss);
-      if (lane == 0) ss_own[t] = ss;
-    }
-    named_barrier(4, 192);
-    // the other CTA needs this half's sums: 64 floats into its ss_peer
-    if (pw == 0 && lane < kWideTok / 4) {
-      const float4 v = *reinterpret_cast<const float4*>(ss_own + 4 * lane);
-      st_async_v4(mapa_shared(smem_u32(ss_peer + 4 * lane), peer), v.x, v.y, v.z, v.w,
-                  mapa_shared(smem_u32(ssbar), peer));
-    }
-    if (!mbar_wait_bounded(ssbar, 0u, kWaitLimit)) timed_out = true;
-    // normalise in place: xq = bf16((x * rr) * gamma_q), K half 0 summed first
-    uint4 gam[3];
-#pragma unroll
-    for (int j = 0; j < 3; ++j)
-      gam[j] = *reinterpret_cast<const uint4*>(a.gamma_q + kbase + 8 * (lane + 32 * j));
-    for (int t = pw; t < kWideTok; t += 6) {
-      const float total = rank == 0 ? ss_own[t] + ss_peer[t] : ss_peer[t] + ss_own[t];
-      const float rr = __frsqrt_rn(__fadd_rn(__fdiv_rn(total, 1536.0f), a.eps));
-#pragma unroll
-      for (int j = 0; j < 3; ++j) {
-        const int c = lane + 32 * j, col = 8 * c;
-        uint4* px = reinterpret_cast<uint4*>(smem + S::oXq + (col >> 6) * (kWideTok * 128) +
-                                             sw128(t, col & 63));
-        uint4 o = make_uint4(0, 0, 0, 0);
-        if (t < a.batch) {
-          const uint4 v = *px;
-          const uint4 gv = gam[j];
-          const uint32_t ww[4] = {v.x, v.y, v.z, v.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
-          uint32_t r[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            r[e] = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[e]), rr), bf16lo(gw[e])),
-                               __fmul_rn(__fmul_rn(bf16hi(ww[e]), rr), bf16hi(gw[e])));
-          o = make_uint4(r[0], r[1], r[2], r[3]);
-          if (a.q_c != nullptr && pair == 0)  // the first pair writes q_c
-            *reinterpret_cast<uint4*>(a.q_c + (int64_t)t * kQLora + kbase + col) = o;
-        }
-        *px = o;
-      }
-    }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // xq feeds the tensor cores
-    named_barrier(4, 192);
     if (tid == 64) {
-      mbar_arrive(xqready);
-      trace_stamp(a, 2);
+      trace_stamp(a, 3);
+      mbar_arrive_expect_tx(xqready, kWideAtoms * kWideTok * 128);
+      const uint8_t* src = a.wide_xq + (size_t)rank * kWideAtoms * kWideTok * 128;
+      for (int at = 0; at < kWideAtoms; ++at)
+        bulk_g2s(smem + S::oXq + at * (kWideTok * 128), src + at * (kWideTok * 128),
+                 kWideTok * 128, xqready);
     }
-    // KV insert of token i (and i + P, ...) by warps 2-3
-    if (warp < 4)
-      for (int t = i; t < a.batch; t += P) kv_insert(a, t, tid - 64, red2);
 
     if (warp >= 4) {
       // ================= epilogue: TMEM lanes 0..127 ===================
@@ -510,9 +423,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           named_barrier(5, 128);
           if (m == 0) mbar_arrive(&qready[j]);
-        } else if (m < kRope) {
+        } else if (2 * h + (m >> 6) < H) {  // rows 0..63: head 2h, 64..127: head 2h + 1
+          const int hr = 2 * h + (m >> 6);
           const int nt_here = min(kWideHalfTok, a.batch - my0);
-          uint16_t* d = a.q_pe + ((int64_t)my0 * H + h) * kRope + m;
+          uint16_t* d = a.q_pe + ((int64_t)my0 * H + hr) * kRope + (m & 63);
 #pragma unroll
           for (int tl = 0; tl < kWideHalfTok; ++tl, d += (int64_t)H * kRope)
             if (tl < nt_here) *d = f2bf_bits(q[tl]);
@@ -538,16 +452,100 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   if (tid == 0) trace_stamp(a, 7);
 }
 
-__global__ void transpose_w_uk_kernel(const uint16_t* __restrict__ w_uk, uint16_t* __restrict__ ukt,
-                                      int heads) {
-  // ukt[h][c][p] = w_uk[h][p][c]
-  const int64_t n = (int64_t)heads * kNope * kKvLora;
+// RMSNorm of the q_a rows of up to 64 tokens for the wide kernel (page
+// "mla.query": xq = bf16((q_a * rr) * gamma_q), rr = 1/sqrt(sum q_a^2 / 1536 +
+// eps)), written as q_c and into the wide CTAs' swizzled tile layout (rows of
+// tokens beyond the batch as zeros), plus the paged KV insert of each token.
+// One CTA of 192 threads per token: thread j takes columns 8j..8j+7.
+__global__ void __launch_bounds__(192) mla_wide_norm_kernel(const DecodeArgs a) {
+  __shared__ float part[6];
+  __shared__ float red2[2];
+  const int t = blockIdx.x, j = threadIdx.x, lane = j & 31, warp = j >> 5;
+  pdl_launch_dependents();  // the wide kernel streams weights meanwhile
+  pdl_wait();
+  uint4 o = make_uint4(0, 0, 0, 0);
+  if (t < a.batch) {
+    const uint4 v = *reinterpret_cast<const uint4*>(a.q_a + (int64_t)t * a.q_a_stride + 8 * j);
+    const uint4 gv = *reinterpret_cast<const uint4*>(a.gamma_q + 8 * j);
+    const uint32_t ww[4] = {v.x, v.y, v.z, v.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      ss = fmaf(bf16lo(ww[e]), bf16lo(ww[e]), ss);
+      ss = fmaf(bf16hi(ww[e]), bf16hi(ww[e]), ss);
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) part[warp] = ss;
+    __syncthreads();
+    const float total = ((((part[0] + part[1]) + part[2]) + part[3]) + part[4]) + part[5];
+    const float rr = __frsqrt_rn(__fadd_rn(__fdiv_rn(total, 1536.0f), a.eps));
+    uint32_t r[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      r[e] = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[e]), rr), bf16lo(gw[e])),
+                         __fmul_rn(__fmul_rn(bf16hi(ww[e]), rr), bf16hi(gw[e])));
+    o = make_uint4(r[0], r[1], r[2], r[3]);
+    if (a.q_c != nullptr) *reinterpret_cast<uint4*>(a.q_c + (int64_t)t * kQLora + 8 * j) = o;
+  }
+  // chunk j: K half j / 96, atom (j % 96) / 8, 16-byte chunk j % 8 of row t
+  const int half = j / 96, cc = j % 96, at = cc >> 3, c = cc & 7;
+  *reinterpret_cast<uint4*>(a.wide_xq + ((size_t)(half * kWideAtoms + at) * kWideTok) * 128 +
+                            t * 128 + ((c ^ (t & 7)) << 4)) = o;
+  if (t < a.batch && warp < 2) kv_insert(a, t, j, red2);
+}
+
+// Tiled copies for the wide kernel, each 16-byte chunk (row r, 8 K-columns
+// from 8 j) at r * 128 + ((j ^ (r % 8)) * 16) of its 16 KiB tile: the K-major
+// 128-byte-swizzled layout the kernel's shared-memory descriptors read.
+//   W_QB tiles: NOPE (h, half, atom) = rows 192 h .. 192 h + 127, columns
+//   768 half + 64 atom ..; then ROPE (unit u, half, atom) = rope rows of head
+//   2u (tile rows 0..63) and 2u + 1 (rows 64..127, zeros past the last head).
+//   W_UK^T tiles (h, ct, pa): row r = latent column 128 ct + r, K = W_UK row
+//   64 pa + k.
+__global__ void pack_wide_qb_kernel(const uint16_t* __restrict__ w_qb, uint8_t* __restrict__ out,
+                                    int heads) {
+  const int ropes = (heads + 1) / 2;
+  const int64_t tiles = (int64_t)(heads + ropes) * 2 * kWideAtoms;
+  const int64_t n = tiles * 128 * 8;  // 16-byte chunks
   for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n;
        e += (int64_t)gridDim.x * blockDim.x) {
-    const int p = (int)(e % kNope);
-    const int c = (int)((e / kNope) % kKvLora);
-    const int64_t h = e / ((int64_t)kNope * kKvLora);
-    ukt[e] = w_uk[(h * kNope + p) * kKvLora + c];
+    const int j = (int)(e & 7), r = (int)((e >> 3) & 127);
+    const int64_t tile = e >> 10;
+    const int at = (int)(tile % kWideAtoms), half = (int)((tile / kWideAtoms) & 1);
+    const int64_t unit = tile / (2 * kWideAtoms);
+    int64_t row = -1;
+    if (unit < heads) {
+      row = unit * kHeadRows + r;
+    } else {
+      const int64_t hd = 2 * (unit - heads) + (r >> 6);
+      if (hd < heads) row = hd * kHeadRows + kNope + (r & 63);
+    }
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (row >= 0)
+      v = *reinterpret_cast<const uint4*>(w_qb + row * kQLora + kWideKHalf * half + 64 * at + 8 * j);
+    *reinterpret_cast<uint4*>(out + tile * kWideBox + r * 128 + ((j ^ (r & 7)) << 4)) = v;
+  }
+}
+
+__global__ void pack_wide_ukt_kernel(const uint16_t* __restrict__ w_uk, uint8_t* __restrict__ out,
+                                     int heads) {
+  const int64_t n = (int64_t)heads * 8 * 128 * 8;  // 16-byte chunks
+  for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int j = (int)(e & 7), r = (int)((e >> 3) & 127);
+    const int64_t tile = e >> 10;
+    const int pa = (int)(tile & 1), ct = (int)((tile >> 1) & 3);
+    const int64_t h = tile >> 3;
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int p0 = 64 * pa + 8 * j + 2 * i;
+      const uint32_t lo = w_uk[(h * kNope + p0) * kKvLora + 128 * ct + r];
+      const uint32_t hi = w_uk[(h * kNope + p0 + 1) * kKvLora + 128 * ct + r];
+      w[i] = lo | (hi << 16);
+    }
+    *reinterpret_cast<uint4*>(out + tile * kWideBox + r * 128 + ((j ^ (r & 7)) << 4)) =
+        make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
@@ -596,10 +594,12 @@ bool make_wide_split(int heads, int ctas, WideSplit* sp) {
   for (int c = 0; c <= pairs; ++c) sp->head[c] = (uint16_t)((int64_t)heads * c / pairs);
   for (int c = 0; c < pairs; ++c)
     if (sp->head[c + 1] - sp->head[c] > 2) return false;
-  // ROPE units (96 KiB per CTA each) fill every pair up to an even share of
-  // the bytes; a head's NOPE + ABS units are 320 KiB per CTA.
-  const int64_t hb = 20, rb = 6;  // in units of 16 KiB
-  const int64_t total = (int64_t)heads * (hb + rb);
+  // ROPE units (two heads' rope rows, 192 KiB per CTA each) fill every pair
+  // up to an even share of the bytes; a head's NOPE + ABS units are 320 KiB
+  // per CTA.
+  const int ropes = (heads + 1) / 2;
+  const int64_t hb = 20, rb = 12;  // in units of 16 KiB
+  const int64_t total = (int64_t)heads * hb + (int64_t)ropes * rb;
   int64_t head_bytes = 0;
   int prev = 0;
   sp->rope[0] = 0;
@@ -607,24 +607,45 @@ bool make_wide_split(int heads, int ctas, WideSplit* sp) {
     head_bytes += (int64_t)(sp->head[c + 1] - sp->head[c]) * hb;
     int64_t r = (total * (c + 1) / pairs - head_bytes + rb / 2) / rb;
     if (r < prev) r = prev;
-    if (r > heads) r = heads;
-    if (c == pairs - 1) r = heads;
+    if (r > ropes) r = ropes;
+    if (c == pairs - 1) r = ropes;
     sp->rope[c + 1] = (uint16_t)r;
     prev = (int)r;
   }
   return true;
 }
 
-cudaError_t transpose_w_uk(const uint16_t* w_uk, uint16_t* ukt, int heads, cudaStream_t stream) {
-  transpose_w_uk_kernel<<<256, 256, 0, stream>>>(w_uk, ukt, heads);
+size_t wide_qb_bytes(int heads) {
+  return (size_t)(heads + (heads + 1) / 2) * 2 * kWideAtoms * kWideBox;
+}
+size_t wide_ukt_bytes(int heads) { return (size_t)heads * 8 * kWideBox; }
+
+cudaError_t pack_wide_weights(const uint16_t* w_qb, const uint16_t* w_uk, uint8_t* qb_tiles,
+                              uint8_t* ukt_tiles, int heads, cudaStream_t stream) {
+  pack_wide_qb_kernel<<<512, 256, 0, stream>>>(w_qb, qb_tiles, heads);
+  pack_wide_ukt_kernel<<<512, 256, 0, stream>>>(w_uk, ukt_tiles, heads);
   return cudaGetLastError();
 }
 
-cudaError_t launch_wide(const DecodeArgs& a, const WideSplit& sp, const CUtensorMap* maps,
-                        int ctas, cudaStream_t stream) {
+size_t wide_xq_bytes() { return (size_t)2 * kWideAtoms * kWideTok * 128; }
+
+cudaError_t launch_wide(const DecodeArgs& a, const WideSplit& sp, int ctas, cudaStream_t stream) {
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kWideTok, 1, 1);
+    cfg.blockDim = dim3(192, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, mla_wide_norm_kernel, a);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = wide_config(ctas, stream, attr);
-  return cudaLaunchKernelEx(&cfg, mla_wide_kernel, a, sp, maps[0], maps[1], maps[2]);
+  return cudaLaunchKernelEx(&cfg, mla_wide_kernel, a, sp);
 }
 
 }  // namespace mla

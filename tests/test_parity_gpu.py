@@ -176,8 +176,8 @@ def test_decode_argument_errors_on_device_buffers():
 
 
 def test_weights_bound_at_create_are_read_each_call():
-    """The handle borrows the weights: changing them between calls changes
-    the result (no hidden copy)."""
+    """Small batches read the borrowed W_QB in place: changing it between
+    calls changes the result."""
     inp = S.make_inputs(batch=1, heads=4, layout=S.LAYOUT_E4M3, pages=4, seed=1000)
     st = DecodeStep(inp)
     assert st.decode() == B.MLA_OK
