@@ -33,8 +33,10 @@ sys.path.insert(0, ROOT)
 METRIC = "µs per MLA-query decode step and HBM GB/s vs ~8 TB/s peak, B=1..64"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["mla_query_projection_gb300/csrc/mla_fused.cu",
-                  "mla_query_projection_gb300/csrc/mla_device.cuh"]
+KERNEL_SOURCES = ["mla_query_projection_gb300/csrc/mla_common.cuh",
+                  "mla_query_projection_gb300/csrc/mla_device.cuh",
+                  "mla_query_projection_gb300/csrc/mla_fused.cu",
+                  "mla_query_projection_gb300/csrc/mla_wide.cu"]
 
 
 def algorithmic_bytes(batch: int, heads: int, layout: int) -> int:
@@ -71,23 +73,23 @@ def read_peaks() -> tuple[float, str]:
 def kernel_for(path: int, batch: int) -> str:
     """The kernel one decode step launches on the given path (MLA_PATH_FMA:
     the FP32-FMA absorbing kernel, one or two tokens per CTA; MLA_PATH_MMA:
-    the paired tensor-core kernel, 8 or 16 tokens per launch, or above 32
+    the paired tensor-core kernel, 8 or 16 tokens per launch, or above 16
     tokens the wide tcgen05 kernel, 64 tokens per launch)."""
     if path == 1:
         return f"mla_absorb_kernel<{1 if batch <= 1 else 2}>"
-    if batch > 32:
+    if batch > 16:
         return "mla_wide_kernel"
     return f"mla_absorb_pair_kernel<{8 if batch <= 8 else 16}>"
 
 
 def launches_per_step(path: int, batch: int) -> int:
     """Kernels one decode call launches: the FMA absorbing kernel is followed by
-    the head-closing kernel; the paired kernel runs once per 16 tokens up to 32
-    tokens, above that the wide tcgen05 kernel (after its normalising kernel)
-    once per 64 tokens."""
+    the head-closing kernel; the paired kernel runs once up to 16 tokens, above
+    that the wide tcgen05 kernel (after its normalising kernel) once per 64
+    tokens."""
     if path == 1:
         return 2
-    return 2 * -(-batch // 64) if batch > 32 else -(-batch // 16)
+    return 2 * -(-batch // 64) if batch > 16 else 1
 
 
 def profile_name(kernel: str, workload: str) -> str:

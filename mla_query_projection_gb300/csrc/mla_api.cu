@@ -89,7 +89,7 @@ int pick_kernel(const mla_query* h, int batch, Kernel* k, int* nt) {
     } else if (batch <= 16 && h->pair_ctas > 0 && h->pair16) {
       *k = Kernel::kAbsorbPair;
       *nt = 16;
-    } else if (batch > 32 && h->wide_ctas > 0) {
+    } else if (batch > 16 && h->wide_ctas > 0) {
       *k = Kernel::kWide;  // one launch per 64 tokens
       *nt = mla::wide_tokens();
     } else if (h->pair_ctas > 0 && h->pair16) {
