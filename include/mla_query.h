@@ -141,6 +141,28 @@ MLA_API int mla_query_decode(mla_query_t h, int batch, const void* q_a,
                      void* q_c, void* stream);
 
 /*
+ * mla_query_decode_fp8q - the same decode step with per-tensor FP8 query
+ * outputs (page "mla.query", method kernel, the FP8 query epilogue used with
+ * the per-tensor FP8 cache for dense MLA): each q_latent and q_pe element is
+ * the OCP E4M3 code (round to nearest even, saturating to +-448) of
+ * bf16(v) * q_scale_inv, the product rounded to binary32.
+ *
+ *   q_scale_inv   device FP32 [1] (must not be NULL).
+ *   q_latent_fp8  device uint8 [B][H][512] output.
+ *   q_pe_fp8      device uint8 [B][H][64] output.
+ *   Every other argument, the ordering and the errors as mla_query_decode;
+ *   q_c stays BF16.  Returns MLA_EUNSUPPORTED where only the hand-off kernel
+ *   could serve the batch (not on a GB300).
+ */
+MLA_API int mla_query_decode_fp8q(mla_query_t h, int batch, const void* q_a,
+                          int64_t q_a_stride, const void* kv_c, int64_t kv_c_stride,
+                          const void* k_pe, int64_t k_pe_stride,
+                          const int64_t* slot_mapping, void* kv_cache,
+                          int64_t num_pages, int page_size, int layout,
+                          const float* k_scale, const float* q_scale_inv,
+                          void* q_latent_fp8, void* q_pe_fp8, void* q_c, void* stream);
+
+/*
  * mla_query_get_error - read and clear the handle's device error flag.
  * Synchronises `stream` (host wait).  *device_flags receives the OR of the
  * MLA_DEVERR_* bits raised since the last call (0 if none).

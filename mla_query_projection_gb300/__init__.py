@@ -18,6 +18,7 @@ from .binding import (  # noqa: F401
     MlaError,
     mla_query_create,
     mla_query_decode,
+    mla_query_decode_fp8q,
     mla_query_destroy,
     mla_query_get_error,
     mla_query_path_for,

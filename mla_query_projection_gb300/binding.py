@@ -61,6 +61,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         vp, i32, vp, i64, vp, i64, vp, i64, vp, vp, i64, i32, i32, vp, vp, vp, vp, vp,
     ]
     lib.mla_query_decode.restype = i32
+    lib.mla_query_decode_fp8q.argtypes = [
+        vp, i32, vp, i64, vp, i64, vp, i64, vp, vp, i64, i32, i32, vp, vp, vp, vp, vp, vp,
+    ]
+    lib.mla_query_decode_fp8q.restype = i32
     lib.mla_query_get_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint), vp]
     lib.mla_query_get_error.restype = i32
     lib.mla_query_set_path.argtypes = [vp, i32]
@@ -123,6 +127,20 @@ def mla_query_decode(
         _ptr(k_pe), int(k_pe_stride), _ptr(slot_mapping), _ptr(kv_cache), int(num_pages),
         int(page_size), int(layout), _ptr(k_scale), _ptr(q_latent), _ptr(q_pe), _ptr(q_c),
         _stream(stream),
+    )
+
+
+def mla_query_decode_fp8q(
+    handle, batch, q_a, q_a_stride, kv_c, kv_c_stride, k_pe, k_pe_stride, slot_mapping,
+    kv_cache, num_pages, page_size, layout, k_scale, q_scale_inv, q_latent_fp8, q_pe_fp8, q_c,
+    stream,
+) -> int:
+    """The decode step with per-tensor FP8 query outputs; returns the C return code."""
+    return load().mla_query_decode_fp8q(
+        handle, int(batch), _ptr(q_a), int(q_a_stride), _ptr(kv_c), int(kv_c_stride),
+        _ptr(k_pe), int(k_pe_stride), _ptr(slot_mapping), _ptr(kv_cache), int(num_pages),
+        int(page_size), int(layout), _ptr(k_scale), _ptr(q_scale_inv), _ptr(q_latent_fp8),
+        _ptr(q_pe_fp8), _ptr(q_c), _stream(stream),
     )
 
 

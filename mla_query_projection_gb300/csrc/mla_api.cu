@@ -241,11 +241,17 @@ fail:
   return rc;
 }
 
-int mla_query_decode(mla_query_t h, int batch, const void* q_a, int64_t q_a_stride,
-                     const void* kv_c, int64_t kv_c_stride, const void* k_pe,
-                     int64_t k_pe_stride, const int64_t* slot_mapping, void* kv_cache,
-                     int64_t num_pages, int page_size, int layout, const float* k_scale,
-                     void* q_latent, void* q_pe, void* q_c, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The decode step behind both entry points: BF16 query outputs, or
+// (q_scale_inv != nullptr) per-tensor FP8 ones.
+int decode_impl(mla_query_t h, int batch, const void* q_a, int64_t q_a_stride, const void* kv_c,
+                int64_t kv_c_stride, const void* k_pe, int64_t k_pe_stride,
+                const int64_t* slot_mapping, void* kv_cache, int64_t num_pages, int page_size,
+                int layout, const float* k_scale, const float* q_scale_inv, void* q_latent,
+                void* q_pe, void* q_c, void* stream) {
   if (h == nullptr) return MLA_EINVAL;
   if (batch < 1 || batch > MLA_MAX_BATCH) return MLA_EINVAL;
   if (q_a == nullptr || kv_c == nullptr || k_pe == nullptr || slot_mapping == nullptr ||
@@ -263,13 +269,15 @@ int mla_query_decode(mla_query_t h, int batch, const void* q_a, int64_t q_a_stri
   if (!aligned16(q_a) || !aligned16(kv_c) || !aligned16(k_pe) || !aligned16(kv_cache) ||
       !aligned16(q_latent) || !aligned16(q_pe) || !aligned16(q_c) ||
       (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) ||
-      (reinterpret_cast<uintptr_t>(k_scale) & 3u))
+      (reinterpret_cast<uintptr_t>(k_scale) & 3u) ||
+      (reinterpret_cast<uintptr_t>(q_scale_inv) & 3u))
     return MLA_EINVAL;
 
   Kernel kern = Kernel::kAbsorbFma;
   int nt = 1;
   int rc = pick_kernel(h, batch, &kern, &nt);
   if (rc != MLA_OK) return rc;
+  if (q_scale_inv != nullptr && kern == Kernel::kHandoff) return MLA_EUNSUPPORTED;
 
   mla::DecodeArgs a;
   a.w_qb = h->w_qb;
@@ -302,12 +310,15 @@ int mla_query_decode(mla_query_t h, int batch, const void* q_a, int64_t q_a_stri
   a.groups = (batch + nt - 1) / nt;
   a.eps = h->eps;
   a.trace = h->trace;
+  a.q_scale_inv = q_scale_inv;
   a.wide_xq = h->wide_xq;
   a.wide_qb = h->wide_qb;
   a.wide_ukt = h->wide_ukt;
   if (a.groups > h->num_sms) return MLA_EUNSUPPORTED;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // bytes per q_latent / q_pe element: BF16, or E4M3 with the FP8 query
+  const int64_t qbytes = q_scale_inv != nullptr ? 1 : 2;
   cudaError_t e;
   if (kern == Kernel::kHandoff)
     e = mla::launch_fused(a, &h->uk_map, nt, true, h->num_sms, st);
@@ -323,8 +334,10 @@ int mla_query_decode(mla_query_t h, int batch, const void* q_a, int64_t q_a_stri
       s64.kv_c = a.kv_c + (int64_t)t0 * a.kv_c_stride;
       s64.k_pe = a.k_pe + (int64_t)t0 * a.k_pe_stride;
       s64.slots = a.slots + t0;
-      s64.q_latent = a.q_latent + (int64_t)t0 * h->heads * mla::kKvLora;
-      s64.q_pe = a.q_pe + (int64_t)t0 * h->heads * mla::kRope;
+      s64.q_latent = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(a.q_latent) +
+                                                 (int64_t)t0 * h->heads * mla::kKvLora * qbytes);
+      s64.q_pe = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(a.q_pe) +
+                                             (int64_t)t0 * h->heads * mla::kRope * qbytes);
       s64.q_c = a.q_c != nullptr ? a.q_c + (int64_t)t0 * mla::kQLora : nullptr;
       e = mla::launch_wide(s64, h->wide_split, h->wide_ctas, st);
     }
@@ -343,8 +356,10 @@ int mla_query_decode(mla_query_t h, int batch, const void* q_a, int64_t q_a_stri
       s16.kv_c = a.kv_c + (int64_t)t0 * a.kv_c_stride;
       s16.k_pe = a.k_pe + (int64_t)t0 * a.k_pe_stride;
       s16.slots = a.slots + t0;
-      s16.q_latent = a.q_latent + (int64_t)t0 * h->heads * mla::kKvLora;
-      s16.q_pe = a.q_pe + (int64_t)t0 * h->heads * mla::kRope;
+      s16.q_latent = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(a.q_latent) +
+                                                 (int64_t)t0 * h->heads * mla::kKvLora * qbytes);
+      s16.q_pe = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(a.q_pe) +
+                                             (int64_t)t0 * h->heads * mla::kRope * qbytes);
       s16.q_c = a.q_c != nullptr ? a.q_c + (int64_t)t0 * mla::kQLora : nullptr;
       e = mla::launch_pair(s16, h->pair_split, h->pair_ctas, s16.batch <= 8 ? 8 : 16, st);
     }
@@ -356,6 +371,32 @@ int mla_query_decode(mla_query_t h, int batch, const void* q_a, int64_t q_a_stri
     return MLA_ECUDA;
   }
   return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_query_decode(mla_query_t h, int batch, const void* q_a, int64_t q_a_stride,
+                     const void* kv_c, int64_t kv_c_stride, const void* k_pe,
+                     int64_t k_pe_stride, const int64_t* slot_mapping, void* kv_cache,
+                     int64_t num_pages, int page_size, int layout, const float* k_scale,
+                     void* q_latent, void* q_pe, void* q_c, void* stream) {
+  return decode_impl(h, batch, q_a, q_a_stride, kv_c, kv_c_stride, k_pe, k_pe_stride,
+                     slot_mapping, kv_cache, num_pages, page_size, layout, k_scale, nullptr,
+                     q_latent, q_pe, q_c, stream);
+}
+
+int mla_query_decode_fp8q(mla_query_t h, int batch, const void* q_a, int64_t q_a_stride,
+                          const void* kv_c, int64_t kv_c_stride, const void* k_pe,
+                          int64_t k_pe_stride, const int64_t* slot_mapping, void* kv_cache,
+                          int64_t num_pages, int page_size, int layout, const float* k_scale,
+                          const float* q_scale_inv, void* q_latent_fp8, void* q_pe_fp8,
+                          void* q_c, void* stream) {
+  if (q_scale_inv == nullptr) return MLA_EINVAL;
+  return decode_impl(h, batch, q_a, q_a_stride, kv_c, kv_c_stride, k_pe, k_pe_stride,
+                     slot_mapping, kv_cache, num_pages, page_size, layout, k_scale, q_scale_inv,
+                     q_latent_fp8, q_pe_fp8, q_c, stream);
 }
 
 int mla_query_get_error(mla_query_t h, unsigned* device_flags, void* stream) {

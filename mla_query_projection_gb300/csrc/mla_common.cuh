@@ -55,6 +55,41 @@ __device__ __forceinline__ void trace_stamp(const DecodeArgs& a, int slot) {
 #endif
 }
 
+// One query output element (q_latent or q_pe) at index idx of its tensor:
+// BF16 bits, or with the per-tensor FP8 query (a.q_scale_inv set) the E4M3
+// code of bf16(v) * qsi, the product rounded to binary32 (qsi = *q_scale_inv,
+// loaded once by the caller with load_qsi).
+__device__ __forceinline__ float load_qsi(const DecodeArgs& a) {
+  return a.q_scale_inv != nullptr ? *a.q_scale_inv : 1.0f;
+}
+__device__ __forceinline__ uint8_t q_fp8(float v, float qsi) {
+  return (uint8_t)(e4m3x2(__fmul_rn(bf_round(v), qsi), 0.0f) & 0xFFu);
+}
+__device__ __forceinline__ void put_q(const DecodeArgs& a, uint16_t* base, int64_t idx, float v,
+                                      float qsi) {
+  if (a.q_scale_inv == nullptr)
+    base[idx] = f2bf_bits(v);
+  else
+    reinterpret_cast<uint8_t*>(base)[idx] = q_fp8(v, qsi);
+}
+// The first n of the N values v[] go to base[i0 + t * step], t = 0..n-1, in the
+// output type; the type is chosen once for the whole run.
+template <int N>
+__device__ __forceinline__ void put_q_run(const DecodeArgs& a, uint16_t* base, int64_t i0,
+                                          int64_t step, const float (&v)[N], int n, float qsi) {
+  if (a.q_scale_inv == nullptr) {
+    uint16_t* d = base + i0;
+#pragma unroll
+    for (int t = 0; t < N; ++t, d += step)
+      if (t < n) *d = f2bf_bits(v[t]);
+  } else {
+    uint8_t* d = reinterpret_cast<uint8_t*>(base) + i0;
+#pragma unroll
+    for (int t = 0; t < N; ++t, d += step)
+      if (t < n) *d = q_fp8(v[t], qsi);
+  }
+}
+
 // Paged FP8 KV insert of token b (page "mla.query", methods insert, kv_fp8,
 // insert_ds), run by the 64 threads of warps 6-7 (lt = 0..63) while warps 0-5
 // normalise q_a.  Thread lt owns latent columns 8*lt..8*lt+7; threads 0..7

@@ -743,10 +743,18 @@ __global__ void __launch_bounds__(256) mla_close_kernel(const DecodeArgs a) {
       acc.z += v[pb].z;
       acc.w += v[pb].w;
     }
-    uint2 o;
-    o.x = pack_bf16x2(acc.x, acc.y);
-    o.y = pack_bf16x2(acc.z, acc.w);
-    *reinterpret_cast<uint2*>(a.q_latent + ((int64_t)t * a.heads + h) * kKvLora + 4 * c4) = o;
+    const int64_t idx = ((int64_t)t * a.heads + h) * kKvLora + 4 * c4;
+    if (a.q_scale_inv == nullptr) {
+      uint2 o;
+      o.x = pack_bf16x2(acc.x, acc.y);
+      o.y = pack_bf16x2(acc.z, acc.w);
+      *reinterpret_cast<uint2*>(a.q_latent + idx) = o;
+    } else {
+      const float qsi = *a.q_scale_inv;
+      *reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(a.q_latent) + idx) =
+          (uint32_t)q_fp8(acc.x, qsi) | ((uint32_t)q_fp8(acc.y, qsi) << 8) |
+          ((uint32_t)q_fp8(acc.z, qsi) << 16) | ((uint32_t)q_fp8(acc.w, qsi) << 24);
+    }
   }
 }
 
@@ -952,7 +960,8 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
 #pragma unroll
               for (int t = 0; t < NT; ++t)
                 if (t < a.batch)
-                  a.q_pe[((int64_t)t * H + r / kRope) * kRope + r % kRope] = f2bf_bits(v[rr][t]);
+                  put_q(a, a.q_pe, ((int64_t)t * H + r / kRope) * kRope + r % kRope, v[rr][t],
+                        load_qsi(a));
             }
           }
         }
@@ -1271,7 +1280,7 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) v += red[(w * NT + tok) * kRedTok + row];
             const int r = r0 + row;
-            a.q_pe[((int64_t)tok * H + r / kRope) * kRope + r % kRope] = f2bf_bits(v);
+            put_q(a, a.q_pe, ((int64_t)tok * H + r / kRope) * kRope + r % kRope, v, load_qsi(a));
           }
         }
         MLA_PHASE(5);
@@ -1649,7 +1658,7 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) v += red[(w * NT + tok) * kRedTok + row];
             const int r = r0 + row;
-            a.q_pe[((int64_t)tok * H + r / kRope) * kRope + r % kRope] = f2bf_bits(v);
+            put_q(a, a.q_pe, ((int64_t)tok * H + r / kRope) * kRope + r % kRope, v, load_qsi(a));
           }
         }
         continue;
@@ -1763,23 +1772,45 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
             for (int e = 0; e < 4; ++e) v[mt][nt][e] = rank == 0 ? mine[e] + pv[e] : pv[e] + mine[e];
           }
         __syncwarp();
-        uint16_t* stage = reinterpret_cast<uint16_t*>(slotp);  // [NT tokens][64 columns]
+        if (a.q_scale_inv == nullptr) {
+          uint16_t* stage = reinterpret_cast<uint16_t*>(slotp);  // [NT tokens][64 columns]
 #pragma unroll
-        for (int mt = 0; mt < 4; ++mt)
+          for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
-          for (int nt = 0; nt < NTL; ++nt) {
-            const int cl = 16 * mt + g, t0 = 8 * nt + 2 * q;  // column within the warp's 64
-            stage[t0 * 64 + cl] = f2bf_bits(v[mt][nt][0]);
-            stage[(t0 + 1) * 64 + cl] = f2bf_bits(v[mt][nt][1]);
-            stage[t0 * 64 + cl + 8] = f2bf_bits(v[mt][nt][2]);
-            stage[(t0 + 1) * 64 + cl + 8] = f2bf_bits(v[mt][nt][3]);
+            for (int nt = 0; nt < NTL; ++nt) {
+              const int cl = 16 * mt + g, t0 = 8 * nt + 2 * q;  // column within the warp's 64
+              stage[t0 * 64 + cl] = f2bf_bits(v[mt][nt][0]);
+              stage[(t0 + 1) * 64 + cl] = f2bf_bits(v[mt][nt][1]);
+              stage[t0 * 64 + cl + 8] = f2bf_bits(v[mt][nt][2]);
+              stage[(t0 + 1) * 64 + cl + 8] = f2bf_bits(v[mt][nt][3]);
+            }
+          __syncwarp();
+          for (int e = lane; e < a.batch * 8; e += 32) {  // 8 chunks of 16 B per token
+            const int t = e >> 3, ch = e & 7;
+            *reinterpret_cast<uint4*>(a.q_latent + ((int64_t)t * H + h) * kKvLora + 64 * warp +
+                                      8 * ch) =
+                *reinterpret_cast<const uint4*>(stage + t * 64 + 8 * ch);
           }
-        __syncwarp();
-        for (int e = lane; e < a.batch * 8; e += 32) {  // 8 chunks of 16 B per token
-          const int t = e >> 3, ch = e & 7;
-          *reinterpret_cast<uint4*>(a.q_latent + ((int64_t)t * H + h) * kKvLora + 64 * warp +
-                                    8 * ch) =
-              *reinterpret_cast<const uint4*>(stage + t * 64 + 8 * ch);
+        } else {
+          const float qsi = *a.q_scale_inv;
+          uint8_t* stage = slotp;  // [NT tokens][64 columns] E4M3
+#pragma unroll
+          for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NTL; ++nt) {
+              const int cl = 16 * mt + g, t0 = 8 * nt + 2 * q;
+              stage[t0 * 64 + cl] = q_fp8(v[mt][nt][0], qsi);
+              stage[(t0 + 1) * 64 + cl] = q_fp8(v[mt][nt][1], qsi);
+              stage[t0 * 64 + cl + 8] = q_fp8(v[mt][nt][2], qsi);
+              stage[(t0 + 1) * 64 + cl + 8] = q_fp8(v[mt][nt][3], qsi);
+            }
+          __syncwarp();
+          uint8_t* ql8 = reinterpret_cast<uint8_t*>(a.q_latent);
+          for (int e = lane; e < a.batch * 4; e += 32) {  // 4 chunks of 16 B per token
+            const int t = e >> 2, ch = e & 3;
+            *reinterpret_cast<uint4*>(ql8 + ((int64_t)t * H + h) * kKvLora + 64 * warp + 16 * ch) =
+                *reinterpret_cast<const uint4*>(stage + t * 64 + 16 * ch);
+          }
         }
       }
     }

@@ -61,6 +61,10 @@ struct DecodeArgs {
   int batch;
   int groups;                // token groups (grid.y)
   float eps;
+  // Per-tensor FP8 query outputs (page "mla.query", method kernel, the FP8
+  // query epilogue): q_latent and q_pe hold E4M3 codes of
+  // bf16(v) * *q_scale_inv; nullptr for BF16 outputs.
+  const float* q_scale_inv;
   // Wide kernel: normalised xq of up to 64 tokens, laid out as the wide CTAs'
   // swizzled shared-memory tiles ([2 K halves][12 atoms][64 rows][128 B]).
   uint8_t* wide_xq;

@@ -168,6 +168,7 @@ extern "C" MLA_API int mla_query_decode_noalloc(
   a.groups = groups;
   a.eps = eps;
   a.trace = nullptr;
+  a.q_scale_inv = nullptr;
   a.wide_xq = nullptr;
   a.wide_qb = nullptr;
   a.wide_ukt = nullptr;

@@ -354,6 +354,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       const int m = tid - 128;  // row of the tile = TMEM lane
       const uint32_t lane_base = (uint32_t)(32 * (warp - 4)) << 16;
       const int my0 = kWideHalfTok * rank, peer0 = kWideHalfTok * (rank ^ 1);
+      const float qsi = load_qsi(a);
       int nq = 0, na = 0;
       for (int u = 0; u < nu; ++u) {
         const int kind = seq.kind(u), h = seq.head(u);
@@ -368,10 +369,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             tmem_ld16(tmem + lane_base + 128 + kWideHalfTok * ct, *reinterpret_cast<float(*)[16]>(v));
             tmem_ld16(tmem + lane_base + 128 + kWideHalfTok * ct + 16,
                       *reinterpret_cast<float(*)[16]>(v + 16));
-            uint16_t* d = a.q_latent + ((int64_t)my0 * H + h) * kKvLora + 128 * ct + m;
-#pragma unroll
-            for (int tl = 0; tl < kWideHalfTok; ++tl, d += tstep)
-              if (tl < nt_here) *d = f2bf_bits(v[tl]);
+            put_q_run(a, a.q_latent, ((int64_t)my0 * H + h) * kKvLora + 128 * ct + m, tstep, v,
+                      nt_here, qsi);
           }
           tc_fence_before();
           mbar_arrive(absfree);
@@ -426,10 +425,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         } else if (2 * h + (m >> 6) < H) {  // rows 0..63: head 2h, 64..127: head 2h + 1
           const int hr = 2 * h + (m >> 6);
           const int nt_here = min(kWideHalfTok, a.batch - my0);
-          uint16_t* d = a.q_pe + ((int64_t)my0 * H + hr) * kRope + (m & 63);
-#pragma unroll
-          for (int tl = 0; tl < kWideHalfTok; ++tl, d += (int64_t)H * kRope)
-            if (tl < nt_here) *d = f2bf_bits(q[tl]);
+          put_q_run(a, a.q_pe, ((int64_t)my0 * H + hr) * kRope + (m & 63), (int64_t)H * kRope, q,
+                    nt_here, qsi);
         }
         ++nq;
         if (m == 0 && u < 16) trace_stamp(a, 28 + u);  // unit u's epilogue done

@@ -249,6 +249,16 @@ def kv_row_e4m3(normed_bf16, k_pe, k_scale):
     return row
 
 
+def query_fp8(bf16_bits, q_scale_inv) -> np.ndarray:
+    """Per-tensor FP8 query element (page "mla.query", method ``kernel``, the
+    FP8 query epilogue of the per-tensor cache): the BF16-rounded output value
+    times ``q_scale_inv``, the product rounded to binary32 (a binary32
+    multiplication; the float64 product of a BF16 and a binary32 value is
+    exact), then cast to E4M3 with saturation."""
+    qsi = float(np.float32(q_scale_inv))
+    return e4m3_satfinite(round_to_f32(bf16_bits_to_f64(bf16_bits) * qsi))
+
+
 def ds_tile_scale(amax):
     """Scale of one 128-column tile of the ``fp8_ds_mla`` row: the binary32
     quotient ``amax / 448``, floored at binary32 1e-4, then ``pow2_ceil``.
@@ -296,7 +306,9 @@ def decode_step(inp, xq_alt=None):
     (0 per-tensor E4M3, 1 fp8_ds_mla); float ``k_scale`` and ``eps``.
 
     Returns a dict: BF16 bits ``q_c [B, 1536]``, ``q_pe [B, H, 64]``,
-    ``q_latent [B, H, 512]``; the updated ``cache``; float64 exact
+    ``q_latent [B, H, 512]`` (with a ``q_scale_inv`` entry in ``inp``, also
+    the FP8 query outputs ``q_latent_fp8`` and ``q_pe_fp8``, see query_fp8);
+    the updated ``cache``; float64 exact
     pre-rounding values and |term| sums for tolerance floors; ``bad_slots``
     (slots at or beyond the cache capacity, skipped).
 
@@ -359,7 +371,7 @@ def decode_step(inp, xq_alt=None):
             row = kv_row_e4m3(normed[b], k_pe[b], inp["k_scale"])
         cache[page, off, :] = row
 
-    return {
+    out = {
         "q_c": f64_to_bf16_bits(xq),
         "q_pe": f64_to_bf16_bits(q_pe),
         "q_latent": f64_to_bf16_bits(q_latent),
@@ -373,3 +385,8 @@ def decode_step(inp, xq_alt=None):
         "ds_scales": ds_scales,
         "bad_slots": bad,
     }
+    # FP8 query outputs (a ``q_scale_inv`` entry in ``inp`` asks for them)
+    if "q_scale_inv" in inp:
+        out["q_latent_fp8"] = query_fp8(out["q_latent"], inp["q_scale_inv"])
+        out["q_pe_fp8"] = query_fp8(out["q_pe"], inp["q_scale_inv"])
+    return out

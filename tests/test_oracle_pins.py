@@ -13,6 +13,7 @@ import numpy as np
 import pytest
 import torch
 
+from mla_query_projection_gb300 import synthetic as S
 from oracle import mla_oracle as O
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -423,3 +424,50 @@ def test_decode_step_alternate_rounding_of_a_tie():
     alt[0, far] = True
     with pytest.raises(ValueError):
         O.decode_step(inp, xq_alt=alt)
+
+
+# --------------------------------------------------------------- FP8 query
+# Page "mla.query", method kernel (FP8 query epilogue): fp8(bf16(v) * q_scale_inv).
+
+
+@pytest.mark.parametrize(
+    "value,qsi,code",
+    [
+        (1.0, 2.0, 0x40),      # 2.0
+        (0.5, 0.25, 0x20),     # 0.125 = 2^-3: exponent field 4
+        (-1.5, 1.0, 0xBC),     # -1.5: sign, exponent 7, mantissa 100
+        (300.0, 2.0, 0x7E),    # 600 saturates to 448
+        (-300.0, 2.0, 0xFE),
+        (1.0625, 1.0, 0x38),   # tie between 1.0 and 1.125: to even
+        (1.1875, 1.0, 0x3A),   # tie between 1.125 and 1.25: to even
+        (0.0, 5.0, 0x00),
+    ],
+)
+def test_query_fp8_hand_worked(value, qsi, code):
+    bits = O.f64_to_bf16_bits(np.array([value]))
+    assert int(O.query_fp8(bits, qsi)[0]) == code
+
+
+def test_query_fp8_rounds_the_output_to_bf16_first():
+    """The scale multiplies the BF16 output, not the exact value: a value just
+    above a BF16 midpoint scales to a different FP8 code than its rounding."""
+    # exact 1.0 + 2^-8 + tiny rounds (BF16, 8 bits) to 1.0078125; times 1.0 the
+    # FP8 code then follows the rounded value 1.0078125 -> 0x38 (nearest 1.0)
+    bits = O.f64_to_bf16_bits(np.array([1.0 + 2.0**-8 + 2.0**-20]))
+    assert float(O.bf16_bits_to_f64(bits)[0]) == 1.0078125
+    assert int(O.query_fp8(bits, 1.0)[0]) == 0x38
+    assert int(O.query_fp8(bits, 8.0)[0]) == 0x50  # 8.0625 -> 8 (0x50)
+
+
+def test_decode_step_fp8_query_outputs_follow_the_bf16_outputs():
+    inp = S.make_inputs(batch=2, heads=2, layout=S.LAYOUT_E4M3, pages=4, seed=77)
+    inp["q_scale_inv"] = 4.0
+    out = O.decode_step(inp)
+    assert out["q_latent_fp8"].shape == out["q_latent"].shape
+    assert out["q_pe_fp8"].shape == out["q_pe"].shape
+    # each code decodes to the E4M3 value nearest 4 x the BF16 output
+    for k in ("q_latent", "q_pe"):
+        want = 4.0 * O.bf16_bits_to_f64(out[k])
+        got = O.e4m3_to_f64(out[k + "_fp8"])
+        step = np.abs(got) * 2.0**-3 + 2.0**-9
+        assert np.all(np.abs(got - np.clip(want, -448, 448)) <= step)
