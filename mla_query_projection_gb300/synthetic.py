@@ -23,7 +23,8 @@ import numpy as np
 
 LAYOUT_E4M3 = 0
 LAYOUT_DS_MLA = 1
-ROW_BYTES = {LAYOUT_E4M3: 576, LAYOUT_DS_MLA: 656}
+LAYOUT_NVFP4_DS_MLA = 2
+ROW_BYTES = {LAYOUT_E4M3: 576, LAYOUT_DS_MLA: 656, LAYOUT_NVFP4_DS_MLA: 352}
 PAGE_SIZE = 64
 
 # The named workloads: (batch, heads, layout, pages, options).

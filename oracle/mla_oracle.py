@@ -21,6 +21,9 @@ What it computes follows the vLLM API page "mla.query" (module
 * ``insert_ds`` section and ``pow2_ceil`` function: the ``fp8_ds_mla`` row keeps
   one power-of-two scale per 128-column tile,
   ``exp2(ceil(log2(max(amax / 448, 1e-4))))``, and stores k_pe as raw BF16.
+* ``insert_nvfp4`` section: the ``nvfp4_ds_mla`` row keeps one E4M3 scale
+  ``max(amax / 6, 2**-9)`` per 16-value block, stores the values as E2M1 of
+  ``x * (1 / scale)`` and k_pe as unscaled E4M3.
 
 Every quantity is kept in float64; values are rounded only where the page
 rounds them (the ``BFloat16(...)`` casts, the FP32 quotient and the FP8 casts).
@@ -55,6 +58,16 @@ ROW_BYTES_DS = DS_ROPE + 2 * QK_ROPE  # 656
 
 E4M3_MAX = 448.0
 
+# ``nvfp4_ds_mla`` row: 512 E2M1 values packed two to a byte, one E4M3 scale
+# per 16-value block, then the 64 k_pe values as E4M3.  The offsets are not
+# printed on the page; reading taken: the three parts packed in that order.
+NVFP4_BLOCK = 16
+NVFP4_SCALES = KV_LORA // 2  # 256: byte offset of the 32 block scales
+NVFP4_ROPE = NVFP4_SCALES + KV_LORA // NVFP4_BLOCK  # 288: byte offset of E4M3 k_pe
+ROW_BYTES_NVFP4 = NVFP4_ROPE + QK_ROPE  # 352
+E2M1_MAX = 6.0
+NVFP4_SCALE_FLOOR = 2.0**-9  # the smallest positive E4M3 value
+
 # Relative width of the rounding tie zone of the normalised q_a row: a bound on
 # the FP32 evaluation error of x * rr * gamma (a sum of squares over 8 + 5 + 6
 # additions, one division, one add, one reciprocal square root, two products:
@@ -63,6 +76,9 @@ XQ_TIE_REL = 2.0**-20
 
 LAYOUT_E4M3 = 0
 LAYOUT_DS_MLA = 1
+LAYOUT_NVFP4_DS_MLA = 2
+ROW_BYTES = {LAYOUT_E4M3: ROW_BYTES_E4M3, LAYOUT_DS_MLA: ROW_BYTES_DS,
+             LAYOUT_NVFP4_DS_MLA: ROW_BYTES_NVFP4}
 
 
 # ---------------------------------------------------------------------------
@@ -171,6 +187,41 @@ def e4m3_to_f64(codes) -> np.ndarray:
     val = np.where(E == 0, m / 8.0 * 2.0**-6, (1.0 + m / 8.0) * np.ldexp(1.0, E - 7))
     val = np.where((E == 15) & (m == 7), np.nan, val)
     return s * val
+
+
+def e2m1_satfinite(v) -> np.ndarray:
+    """float64 -> OCP FP4 E2M1 code (uint8, low 4 bits), round to nearest even,
+    saturating.
+
+    E2M1: sign, 2 exponent bits with bias 1, 1 mantissa bit; normal values
+    (1 + m/2) * 2**(E - 1) for E = 1..3 (1, 1.5, 2, 3, 4, 6), subnormals
+    (m/2) for E = 0 (0, 0.5); no infinities or NaN, so the largest magnitude
+    is 6.  Reading taken: the cast saturates to +-6 and keeps the sign of a
+    zero, as the E4M3 cast does."""
+    v = np.asarray(v, dtype=np.float64)
+    if not np.all(np.isfinite(v)):
+        raise ValueError("e2m1_satfinite: non-finite input")
+    _, e = np.frexp(v)
+    q_exp = np.maximum(e - 2, -1)  # 2 significant bits; subnormal quantum 2**-1
+    r = np.ldexp(np.rint(np.ldexp(v, -q_exp)), q_exp)
+    r = np.clip(r, -E2M1_MAX, E2M1_MAX)
+    sign = np.signbit(r).astype(np.uint8) << np.uint8(3)
+    a = np.abs(r)
+    normal = a >= 1.0
+    m2, e2 = np.frexp(np.where(normal, a, 1.0))  # a = m2 * 2**e2, m2 in [0.5, 1)
+    exp_field = np.where(normal, e2 - 1 + 1, 0)
+    mant = np.where(normal, np.rint((m2 * 2.0 - 1.0) * 2.0), np.rint(a / 0.5))
+    code = (exp_field.astype(np.int64) << 1) | mant.astype(np.int64)
+    return (code.astype(np.uint8) | sign).astype(np.uint8)
+
+
+def e2m1_to_f64(codes) -> np.ndarray:
+    """OCP FP4 E2M1 code (low 4 bits) -> float64."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64) & 0xF
+    s = np.where(c & 0x8, -1.0, 1.0)
+    E = (c >> 1) & 0x3
+    m = c & 0x1
+    return s * np.where(E == 0, m * 0.5, (1.0 + m / 2.0) * np.ldexp(1.0, E - 1))
 
 
 def pow2_ceil(v) -> np.ndarray:
@@ -290,6 +341,53 @@ def kv_row_ds(normed_bf16, k_pe_bits):
     return row, scales
 
 
+def nvfp4_block_scale(amax):
+    """E4M3 scale of one 16-value block of the ``nvfp4_ds_mla`` row (page
+    "mla.query", ``insert_nvfp4``): ``sf = max(amax / 6, 2**-9)`` with the
+    binary32 quotient, cast to E4M3.  Returns (E4M3 code, its value, the
+    binary32 reciprocal of that value).  Reading taken: the values are scaled
+    by the reciprocal of the stored (E4M3-rounded) scale, so that code times
+    scale is what a reader of the row decodes."""
+    sf = np.maximum(round_to_f32(np.asarray(amax, dtype=np.float64) / E2M1_MAX),
+                    NVFP4_SCALE_FLOOR)
+    code = e4m3_satfinite(sf)
+    value = e4m3_to_f64(code)
+    return code, value, round_to_f32(1.0 / value)
+
+
+def nvfp4_scale_byte(block):
+    """Byte offset, within the row, of the scale of 16-value block ``block``
+    (0..31): the page stores the scales four-way interleaved, block s at
+    ``NVFP4_SCALES + 8 * (s % 4) + s // 4``."""
+    return NVFP4_SCALES + 8 * (block % 4) + block // 4
+
+
+def kv_row_nvfp4(normed_bf16, k_pe):
+    """``nvfp4_ds_mla`` row (352 bytes): page "mla.query", ``insert_nvfp4``.
+
+    Each 16-value block of the BF16 normed latent row gets an E4M3 scale
+    (nvfp4_block_scale over the block's amax) and its values are stored as
+    E2M1 of the binary32 product ``n * (1 / sf)``; k_pe is stored as E4M3 of
+    its BF16 value, with no scale.  Bytes 0..255: E2M1 codes, value 2k in the
+    low half of byte k and value 2k + 1 in the high half (reading taken: the
+    page's packing helper is not printed; this is the order of the FP4 formats
+    that hold two values per byte).  Bytes 256..287: the 32 scales, placed by
+    nvfp4_scale_byte.  Bytes 288..351: k_pe."""
+    n = np.asarray(normed_bf16, dtype=np.float64)
+    row = np.empty(ROW_BYTES_NVFP4, dtype=np.uint8)
+    codes = np.empty(KV_LORA, dtype=np.uint8)
+    scales = np.empty(KV_LORA // NVFP4_BLOCK, dtype=np.float64)
+    for s in range(KV_LORA // NVFP4_BLOCK):
+        seg = n[s * NVFP4_BLOCK:(s + 1) * NVFP4_BLOCK]
+        code, value, inv = nvfp4_block_scale(np.max(np.abs(seg)))
+        scales[s] = value
+        row[nvfp4_scale_byte(s)] = code
+        codes[s * NVFP4_BLOCK:(s + 1) * NVFP4_BLOCK] = e2m1_satfinite(round_to_f32(seg * inv))
+    row[:NVFP4_SCALES] = codes[0::2] | (codes[1::2] << np.uint8(4))
+    row[NVFP4_ROPE:] = e4m3_satfinite(np.asarray(k_pe, dtype=np.float64))
+    return row, scales
+
+
 def slot_to_page(slot, page_size):
     """Paged-cache address of a slot: ``(slot // page_size, slot % page_size)``
     (page "mla.query", ``insert``).  Only called for slot >= 0."""
@@ -303,7 +401,8 @@ def decode_step(inp, xq_alt=None):
     ``w_uk [H, 128, 512]``, ``gamma_q [1536]``, ``gamma_kv [512]``,
     ``q_a [B, 1536]``, ``kv_c [B, 512]``, ``k_pe [B, 64]``; ``slots`` int64 [B];
     ``cache`` uint8 [pages, page_size, row_bytes] (not modified); ``layout``
-    (0 per-tensor E4M3, 1 fp8_ds_mla); float ``k_scale`` and ``eps``.
+    (0 per-tensor E4M3, 1 fp8_ds_mla, 2 nvfp4_ds_mla); float ``k_scale`` and
+    ``eps``.
 
     Returns a dict: BF16 bits ``q_c [B, 1536]``, ``q_pe [B, H, 64]``,
     ``q_latent [B, H, 512]`` (with a ``q_scale_inv`` entry in ``inp``, also
@@ -352,7 +451,9 @@ def decode_step(inp, xq_alt=None):
     cache = np.array(inp["cache"], dtype=np.uint8, copy=True)
     pages, page_size, row_bytes = cache.shape
     layout = int(inp["layout"])
-    want = ROW_BYTES_DS if layout == LAYOUT_DS_MLA else ROW_BYTES_E4M3
+    if layout not in ROW_BYTES:
+        raise ValueError(f"unknown cache layout {layout}")
+    want = ROW_BYTES[layout]
     if row_bytes != want:
         raise ValueError(f"cache rows are {row_bytes} B, layout needs {want}")
     bad = []
@@ -366,6 +467,9 @@ def decode_step(inp, xq_alt=None):
             continue
         if layout == LAYOUT_DS_MLA:
             row, sc = kv_row_ds(normed[b], k_pe_bits[b])
+            ds_scales[b] = sc
+        elif layout == LAYOUT_NVFP4_DS_MLA:
+            row, sc = kv_row_nvfp4(normed[b], k_pe[b])
             ds_scales[b] = sc
         else:
             row = kv_row_e4m3(normed[b], k_pe[b], inp["k_scale"])

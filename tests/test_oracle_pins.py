@@ -248,7 +248,7 @@ def _bf16(vals):
 
 def _hand_inputs(layout, pages=2, page_size=4, slots=(5,), H=1):
     B = len(slots)
-    row = 656 if layout == 1 else 576
+    row = O.ROW_BYTES[layout]
     rng = np.random.default_rng(18)
     cache = rng.integers(0, 256, (pages, page_size, row), dtype=np.uint8)
     return dict(
@@ -315,7 +315,7 @@ def test_kv_ds_scale_per_tile_and_k_pe_raw():
 def test_slot_math_every_slot():
     pages, ps = 3, 4
     slots = list(range(pages * ps)) + [-1]
-    for layout in (0, 1):
+    for layout in (0, 1, 2):
         inp = _hand_inputs(layout, pages=pages, page_size=ps, slots=slots)
         kv = np.tile(np.linspace(0.5, 2.0, 512), (len(slots), 1)) * np.arange(1, len(slots) + 1)[:, None]
         inp["kv_c"] = _bf16(kv)
@@ -471,3 +471,150 @@ def test_decode_step_fp8_query_outputs_follow_the_bf16_outputs():
         got = O.e4m3_to_f64(out[k + "_fp8"])
         step = np.abs(got) * 2.0**-3 + 2.0**-9
         assert np.all(np.abs(got - np.clip(want, -448, 448)) <= step)
+
+
+# ---------------------------------------------------------------- nvfp4_ds_mla
+
+
+E2M1_MAGNITUDES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]  # codes 0..7
+
+
+def test_e2m1_hand_worked_table():
+    for value, code in _read_table("e2m1_codes.txt"):
+        got = int(O.e2m1_satfinite(np.array([float(value)]))[0])
+        assert got == int(code, 16), (value, hex(got), code)
+
+
+def test_e2m1_decode_and_roundtrip():
+    codes = np.arange(16, dtype=np.uint8)
+    want = np.array(E2M1_MAGNITUDES + [-m for m in E2M1_MAGNITUDES])
+    got = O.e2m1_to_f64(codes)
+    assert np.array_equal(got, want)
+    assert np.array_equal(np.signbit(got[8:]), np.ones(8, bool))  # code 8 is -0
+    assert np.array_equal(O.e2m1_satfinite(got), codes)
+
+
+def test_e2m1_is_the_nearest_value_ties_to_even():
+    """Brute force over the eight magnitudes: the nearest one, the one with
+    mantissa bit 0 (an even code) on a tie, 6 beyond the range."""
+    rng = np.random.default_rng(31)
+    x = np.concatenate([rng.uniform(-8, 8, 20_000), np.arange(-32, 33) / 4.0])
+    mags = np.array(E2M1_MAGNITUDES)
+    got = O.e2m1_satfinite(x)
+    for v, c in zip(x, got):
+        d = np.abs(mags - min(abs(v), 6.0))
+        best = np.flatnonzero(d == d.min())
+        k = best[0] if len(best) == 1 else best[best % 2 == 0][0]
+        assert (int(c) & 7) == k, (v, int(c))
+        assert (int(c) >> 3) == (1 if np.signbit(v) else 0), (v, int(c))
+
+
+@pytest.mark.parametrize(
+    "amax, code, value",
+    [
+        (6.0, 0x38, 1.0),  # 6 / 6 = 1: E4M3 E=7, m=0
+        (3.0, 0x30, 0.5),  # 0.5: E=6
+        (0.0, 0x01, 2.0**-9),  # floor 2**-9: the smallest E4M3 subnormal
+        (6 * 2.0**-10, 0x01, 2.0**-9),  # 2**-10 is below the floor
+        (7.0, 0x39, 1.125),  # 1.1667 -> nearer 1.125 (m=1) than 1.25
+        (6.375, 0x38, 1.0),  # 1.0625: tie 1.0 / 1.125 -> even (m=0)
+        (1.0, 0x23, 0.171875),  # 1/6 = 1.333 * 2**-3 -> m=3 (1.375): E=4
+        (2688.0, 0x7E, 448.0),  # 448: the largest finite E4M3
+        (1e5, 0x7E, 448.0),  # saturates
+    ],
+)
+def test_nvfp4_block_scale_hand_worked(amax, code, value):
+    c, v, inv = O.nvfp4_block_scale(amax)
+    assert int(c) == code and float(v) == value
+    assert float(inv) == float(np.float32(1.0) / np.float32(value))
+
+
+def test_nvfp4_values_use_the_stored_scale():
+    """Block amax 7: the stored scale is 1.125 (not 7/6), and 2.875 / 1.125 =
+    2.556 rounds to E2M1 3 (code 5), where 2.875 / (7/6) = 2.464 would give 2.
+    7 / 1.125 = 6.22 saturates to 6 (code 7)."""
+    n = np.zeros(512)
+    n[0], n[1] = 7.0, 2.875
+    row, scales = O.kv_row_nvfp4(n, np.zeros(64))
+    assert row[0] == 0x57  # value 0 in the low half, value 1 in the high half
+    assert row[O.NVFP4_SCALES] == 0x39 and scales[0] == 1.125
+    assert np.all(row[8:256] == 0x00)  # zero blocks: zero codes
+    assert np.all(row[O.NVFP4_SCALES + 1:O.NVFP4_SCALES + 8] == 0x01)  # blocks 4, 8, ..: floor
+
+
+def test_kv_row_nvfp4_worked():
+    # kv_c = 1 -> normed 1.0 -> amax 1 -> scale code 0x23 (0.171875), reciprocal
+    # 5.8181820 -> 1.0 * 5.818 rounds to E2M1 6 (code 7) -> byte 0x77; k_pe 2.0
+    # stored unscaled -> E4M3 0x40.
+    inp = _hand_inputs(2)
+    out = O.decode_step(inp)
+    row = out["cache"][1, 1]
+    assert row.shape == (352,)
+    assert np.all(row[:256] == 0x77)
+    assert np.all(row[256:288] == 0x23)
+    assert np.all(row[288:] == 0x40)
+
+
+def test_nvfp4_nibble_order_and_scale_placement():
+    """Block s of 16 values has amax 6 * 2**-(s % 7) * (1 + (s // 8) / 8), so its
+    scale is exactly 2**-(s % 7) * (1 + (s // 8) / 8), a normal E4M3 value:
+    code ((7 - s % 7) << 3) | (s // 8).  The scale of block s sits at byte
+    256 + 8 * (s % 4) + s // 4; every scale byte is written once.  Within a
+    block, values [6, -3, 1.5, 0.5, 4, 0, ...] times the scale give codes
+    7, 0xD, 3, 1, 6, 0: bytes 0xD7, 0x13, 0x06."""
+    n = np.zeros(512)
+    pattern = np.array([6.0, -3.0, 1.5, 0.5, 4.0] + [0.0] * 11)
+    for s in range(32):
+        n[16 * s:16 * s + 16] = pattern * 2.0 ** -(s % 7) * (1 + (s // 8) / 8)
+    row, _ = O.kv_row_nvfp4(n, np.zeros(64))
+    placed = sorted(O.nvfp4_scale_byte(s) for s in range(32))
+    assert placed == list(range(256, 288))
+    assert O.nvfp4_scale_byte(5) == 265
+    for s in range(32):
+        assert row[256 + 8 * (s % 4) + s // 4] == ((7 - s % 7) << 3) | (s // 8), s
+        assert list(row[8 * s:8 * s + 3]) == [0xD7, 0x13, 0x06], s
+        assert np.all(row[8 * s + 3:8 * s + 8] == 0)
+
+
+def test_nvfp4_dequantised_row_error_bound():
+    """E2M1 code times the stored scale is within half an E2M1 step of the
+    scaled value: |n - deq| <= sf * max(0.25, |n / sf| / 4), the slack of the
+    top step (4..6, step 2) also covering saturation (|n / sf| <= 6 * 17/16
+    after the scale's E4M3 rounding).  The bound holds while every scale is a
+    normal E4M3 value below 448, as for RMS-normalised rows (|n| <= sqrt(512)
+    times gamma)."""
+    rng = np.random.default_rng(32)
+    for trial in range(50):
+        n = O.round_to_bf16(rng.standard_normal(512) * np.exp(rng.uniform(-1.5, 1.5)))
+        n[rng.random(512) < 0.01] *= 20.0
+        row, scales = O.kv_row_nvfp4(n, np.zeros(64))
+        assert scales.min() >= 2.0**-6 and scales.max() < 448.0
+        codes = np.empty(512, np.uint8)
+        codes[0::2] = row[:256] & 0xF
+        codes[1::2] = row[:256] >> 4
+        sf = np.repeat(scales, 16)
+        deq = O.e2m1_to_f64(codes) * sf
+        bound = sf * np.maximum(0.25, np.abs(n / sf) / 4) * (1 + 2.0**-20)
+        assert np.all(np.abs(n - deq) <= bound), trial
+        # the decoded scale bytes are the returned scales
+        for s in range(32):
+            assert O.e4m3_to_f64(row[O.nvfp4_scale_byte(s):O.nvfp4_scale_byte(s) + 1])[0] == scales[s]
+
+
+def test_nvfp4_power_of_two_scaling_moves_only_the_scales():
+    """Scaling the row by 2**k (scales stay normal E4M3 and above the floor)
+    multiplies every scale by 2**k and leaves every E2M1 code unchanged."""
+    rng = np.random.default_rng(33)
+    n = O.round_to_bf16(rng.standard_normal(512) * 4.0)
+    base, sb = O.kv_row_nvfp4(n, np.zeros(64))
+    for k in (-3, -1, 2, 5):
+        row, sk = O.kv_row_nvfp4(n * 2.0**k, np.zeros(64))
+        assert np.array_equal(row[:256], base[:256]), k
+        assert np.array_equal(sk, sb * 2.0**k), k
+
+
+def test_nvfp4_k_pe_is_unscaled_e4m3():
+    kpe = O.round_to_bf16(np.linspace(-500, 500, 64))
+    row, _ = O.kv_row_nvfp4(np.ones(512), kpe)
+    ref = torch.from_numpy(kpe.astype(np.float32)).clamp(-448, 448).to(torch.float8_e4m3fn)
+    assert np.array_equal(row[288:], ref.view(torch.uint8).numpy())
