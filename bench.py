@@ -42,8 +42,9 @@ KERNEL_SOURCES = ["mla_query_projection_gb300/csrc/mla_common.cuh",
 def algorithmic_bytes(batch: int, heads: int, layout: int) -> int:
     """Bytes one decode step must move: W_QB (H*192*1536*2) + W_UK (H*128*512*2)
     + gammas (2*(1536+512)) + activations read (B*(1536+512+64)*2 + 8 slot)
-    + outputs written (B*H*(512+64)*2 + q_c B*1536*2) + cache rows (576/656)."""
-    row = 656 if layout == 1 else 576
+    + outputs written (B*H*(512+64)*2 + q_c B*1536*2) + cache rows (576, 656
+    or 352 bytes by layout)."""
+    row = {0: 576, 1: 656, 2: 352}[layout]
     return (heads * 192 * 1536 * 2 + heads * 128 * 512 * 2 + 2 * (1536 + 512)
             + batch * ((1536 + 512 + 64) * 2 + 8) + batch * heads * (512 + 64) * 2
             + batch * 1536 * 2 + batch * row)
@@ -127,11 +128,12 @@ def workload_cfg(name: str) -> dict:
 
     if name in S.WORKLOADS:
         return dict(S.WORKLOADS[name])
-    # sweep point: sweep_b{B}_h{H}_{e4m3|ds}
+    # sweep point: sweep_b{B}_h{H}_{e4m3|ds|nvfp4}
     parts = name.split("_")
     if parts[0] == "sweep":
         b, h = int(parts[1][1:]), int(parts[2][1:])
-        lay = S.LAYOUT_DS_MLA if parts[3] == "ds" else S.LAYOUT_E4M3
+        lay = {"e4m3": S.LAYOUT_E4M3, "ds": S.LAYOUT_DS_MLA,
+               "nvfp4": S.LAYOUT_NVFP4_DS_MLA}[parts[3]]
         return S.sweep_workload(b, h, lay)
     raise SystemExit(f"unknown workload {name}")
 

@@ -50,12 +50,19 @@ extern "C" {
 #define MLA_ECUDA (-3)        /* a CUDA runtime/driver call failed            */
 #define MLA_EUNSUPPORTED (-4) /* shape the library does not handle            */
 
-/* KV cache layouts (page "mla.query", methods insert and insert_ds). */
+/* KV cache layouts (page "mla.query", methods insert, insert_ds and
+   insert_nvfp4). */
 #define MLA_KV_FP8_E4M3 0   /* 576-byte row: 512 E4M3 latent + 64 E4M3 k_pe,
                                each value divided by k_scale                 */
 #define MLA_KV_FP8_DS_MLA 1 /* 656-byte row: 512 E4M3 latent scaled per 128
                                columns by a power of two, 4 FP32 scales at
                                byte 512, 64 raw BF16 k_pe at byte 528        */
+#define MLA_KV_NVFP4_DS_MLA 2 /* 352-byte row: 512 E2M1 latent, two to a byte
+                               (value 2k in the low half of byte k), scaled
+                               per 16 values by the E4M3 scale
+                               max(amax / 6, 2^-9); the 32 scales at byte
+                               256, block s at 256 + 8 * (s % 4) + s / 4;
+                               64 unscaled E4M3 k_pe at byte 288          */
 
 /* Bits of the device error flag (mla_query_get_error). */
 #define MLA_DEVERR_BAD_SLOT 1u /* a slot >= num_pages * page_size was skipped   */
@@ -116,11 +123,12 @@ MLA_API int mla_query_create(mla_query_t* out, int num_heads, const void* w_qb,
  *                 (page "mla.query", method insert); a slot >= num_pages *
  *                 page_size is skipped and sets MLA_DEVERR_BAD_SLOT.
  *   kv_cache      device uint8 [num_pages][page_size][row], row = 576
- *                 (MLA_KV_FP8_E4M3) or 656 (MLA_KV_FP8_DS_MLA) bytes; slot s
- *                 lives at page s / page_size, offset s % page_size.
- *   layout        MLA_KV_FP8_E4M3 or MLA_KV_FP8_DS_MLA.
+ *                 (MLA_KV_FP8_E4M3), 656 (MLA_KV_FP8_DS_MLA) or 352
+ *                 (MLA_KV_NVFP4_DS_MLA) bytes; slot s lives at page
+ *                 s / page_size, offset s % page_size.
+ *   layout        MLA_KV_FP8_E4M3, MLA_KV_FP8_DS_MLA or MLA_KV_NVFP4_DS_MLA.
  *   k_scale       device FP32 [1]; the per-tensor layout divides by it
- *                 (ignored by the ds layout, may then be NULL).
+ *                 (ignored by the two ds layouts, may then be NULL).
  *   q_latent      device BF16 [B][H][512] output.
  *   q_pe          device BF16 [B][H][64] output.
  *   q_c           device BF16 [B][1536] output, or NULL to skip it.

@@ -11,6 +11,7 @@ from .binding import (  # noqa: F401
     MLA_DEVERR_TIMEOUT,
     MLA_KV_FP8_DS_MLA,
     MLA_KV_FP8_E4M3,
+    MLA_KV_NVFP4_DS_MLA,
     MLA_OK,
     MLA_PATH_AUTO,
     MLA_PATH_FMA,

@@ -21,6 +21,7 @@ MLA_ECUDA = -3
 MLA_EUNSUPPORTED = -4
 MLA_KV_FP8_E4M3 = 0
 MLA_KV_FP8_DS_MLA = 1
+MLA_KV_NVFP4_DS_MLA = 2
 MLA_DEVERR_BAD_SLOT = 1
 MLA_DEVERR_TIMEOUT = 2
 MLA_PATH_AUTO = 0

@@ -257,7 +257,8 @@ int decode_impl(mla_query_t h, int batch, const void* q_a, int64_t q_a_stride, c
   if (q_a == nullptr || kv_c == nullptr || k_pe == nullptr || slot_mapping == nullptr ||
       kv_cache == nullptr || q_latent == nullptr || q_pe == nullptr)
     return MLA_EINVAL;
-  if (layout != MLA_KV_FP8_E4M3 && layout != MLA_KV_FP8_DS_MLA) return MLA_EINVAL;
+  if (layout != MLA_KV_FP8_E4M3 && layout != MLA_KV_FP8_DS_MLA && layout != MLA_KV_NVFP4_DS_MLA)
+    return MLA_EINVAL;
   if (layout == MLA_KV_FP8_E4M3 && k_scale == nullptr) return MLA_EINVAL;
   if (num_pages < 1 || page_size < 1) return MLA_EINVAL;
   if (q_a_stride == 0) q_a_stride = mla::kQLora;

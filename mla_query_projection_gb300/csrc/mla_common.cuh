@@ -90,10 +90,10 @@ __device__ __forceinline__ void put_q_run(const DecodeArgs& a, uint16_t* base, i
   }
 }
 
-// Paged FP8 KV insert of token b (page "mla.query", methods insert, kv_fp8,
-// insert_ds), run by the 64 threads of warps 6-7 (lt = 0..63) while warps 0-5
-// normalise q_a.  Thread lt owns latent columns 8*lt..8*lt+7; threads 0..7
-// also own k_pe values 8*lt..8*lt+7.  red2 holds the two warps' partial sums.
+// Paged KV insert of token b (page "mla.query", methods insert, kv_fp8,
+// insert_ds, insert_nvfp4), run by 64 threads (lt = 0..63, two whole warps).
+// Thread lt owns latent columns 8*lt..8*lt+7; threads 0..7 also own k_pe
+// values 8*lt..8*lt+7.  red2 holds the two warps' partial sums.
 __device__ void kv_insert(const DecodeArgs& a, int b, int lt, float* red2) {
   const int lane = lt & 31, w = lt >> 5;
   const int64_t slot = a.slots[b];
@@ -102,7 +102,8 @@ __device__ void kv_insert(const DecodeArgs& a, int b, int lt, float* red2) {
   uint4 pe = make_uint4(0, 0, 0, 0);
   if (lt < 8) pe = *reinterpret_cast<const uint4*>(a.k_pe + (int64_t)b * a.k_pe_stride + 8 * lt);
   const bool ds = a.layout == MLA_KV_FP8_DS_MLA;
-  const float ks = ds ? 1.0f : *a.k_scale;
+  const bool nv = a.layout == MLA_KV_NVFP4_DS_MLA;
+  const float ks = (ds || nv) ? 1.0f : *a.k_scale;
   float x[8];
   const uint32_t xw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -124,7 +125,7 @@ __device__ void kv_insert(const DecodeArgs& a, int b, int lt, float* red2) {
     if (lt == 0) atomicOr(a.err, MLA_DEVERR_BAD_SLOT);
     return;
   }
-  uint8_t* row = a.cache + (page * a.page_size + off) * (ds ? kRowDs : kRowE4m3);
+  uint8_t* row = a.cache + (page * a.page_size + off) * (ds ? kRowDs : nv ? kRowNvfp4 : kRowE4m3);
   const float rr = __frsqrt_rn(__fadd_rn(__fmul_rn(total, 1.0f / 512.0f), a.eps));
   const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
   float n[8];
@@ -132,6 +133,35 @@ __device__ void kv_insert(const DecodeArgs& a, int b, int lt, float* red2) {
   for (int i = 0; i < 4; ++i) {
     n[2 * i] = bf_round(__fmul_rn(__fmul_rn(x[2 * i], rr), bf16lo(gw[i])));
     n[2 * i + 1] = bf_round(__fmul_rn(__fmul_rn(x[2 * i + 1], rr), bf16hi(gw[i])));
+  }
+  if (nv) {
+    // one 16-value block per thread pair: E4M3 scale of max(amax / 6, 2^-9),
+    // values as E2M1 of n * (1 / scale) with the stored (rounded) scale
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(n[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    const float sf = fmaxf(__fdiv_rn(amax, 6.0f), 0x1p-9f);
+    const uint32_t code = e4m3x2(sf, 0.0f) & 0xFFu;
+    const float inv = __fdiv_rn(1.0f, e4m3_value(code));
+    float y[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(n[i], inv);
+    *reinterpret_cast<uint32_t*>(row + 4 * lt) = e2m1x8(y);
+    if ((lt & 1) == 0) {
+      const int s = lt >> 1;
+      row[kNvScales + 8 * (s & 3) + (s >> 2)] = (uint8_t)code;
+    }
+    if (lt < 8) {
+      const uint32_t w2[4] = {pe.x, pe.y, pe.z, pe.w};
+      uint2 o2;
+      o2.x = (uint32_t)e4m3x2(bf16lo(w2[0]), bf16hi(w2[0])) |
+             ((uint32_t)e4m3x2(bf16lo(w2[1]), bf16hi(w2[1])) << 16);
+      o2.y = (uint32_t)e4m3x2(bf16lo(w2[2]), bf16hi(w2[2])) |
+             ((uint32_t)e4m3x2(bf16lo(w2[3]), bf16hi(w2[3])) << 16);
+      *reinterpret_cast<uint2*>(row + kNvRope + 8 * lt) = o2;
+    }
+    return;
   }
   uint2 out;
   if (!ds) {

@@ -224,6 +224,28 @@ __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
   return r;
 }
 
+// Eight binary32 values -> eight OCP FP4 E2M1 codes (round to nearest even,
+// saturating to +-6), value 2k in the low half of byte k.
+__device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8]) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return r;
+}
+
+// Value of a non-negative, finite OCP FP8 E4M3 code (the low 7 bits): exponent
+// field E with bias 7 and mantissa m of 3 bits; (m / 8) * 2^-6 when E == 0.
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+  const uint32_t E = (code >> 3) & 15u, m = code & 7u;
+  return E == 0 ? (float)m * 0x1p-9f : __uint_as_float(((E + 120u) << 23) | (m << 20));
+}
+
 // exp2(ceil(log2(v))) of a positive normal binary32: keep the exponent field
 // and step it up by one when any fraction bit is set.
 __device__ __forceinline__ float pow2_ceil_f32(float v) {

@@ -18,6 +18,9 @@ constexpr int kRowE4m3 = 576;  // per-tensor cache row bytes
 constexpr int kRowDs = 656;    // fp8_ds_mla cache row bytes
 constexpr int kDsScales = 512; // byte offset of the four FP32 tile scales
 constexpr int kDsRope = 528;   // byte offset of the BF16 k_pe
+constexpr int kRowNvfp4 = 352;  // nvfp4_ds_mla cache row bytes
+constexpr int kNvScales = 256;  // byte offset of the 32 E4M3 block scales
+constexpr int kNvRope = 288;    // byte offset of the E4M3 k_pe
 
 // Work units of the fused kernel.
 constexpr int kRowBytes = kQLora * 2;        // one Q_B row in global memory (3072 B)

@@ -18,6 +18,8 @@ terms of the dot product that produced the output (K terms):
     (codes compared as signed ordinals, so +0 and -0 are equal).
   * fp8_ds_mla power-of-two scales, k_pe bytes, slot/page placement and every
     cache byte outside the written rows: bit-exact.
+  * nvfp4_ds_mla rows: E4M3 block scales and E4M3 k_pe bit-exact; E2M1 codes
+    at least 99.9% identical, the rest within one code.
 
 Rounding ties.  The path rounds FP32 intermediates to BF16 where the page
 does (the normalised q_a row, the Q_B outputs).  When an exact value lies at a
@@ -110,6 +112,12 @@ def e4m3_ordinal(codes):
     return np.where(c & 0x80, -mag, mag)
 
 
+def e2m1_ordinal(codes):
+    c = codes.astype(np.int64)
+    mag = c & 0x7
+    return np.where(c & 0x8, -mag, mag)
+
+
 def check_cache(got, ref, before, slots, page_size, layout, report=None):
     """Compare the whole cache: written rows by tolerance, everything else exact."""
     assert got.shape == ref.shape
@@ -123,6 +131,20 @@ def check_cache(got, ref, before, slots, page_size, layout, report=None):
     if not written.any():
         return
     g, r = got[written], ref[written]
+    if layout == O.LAYOUT_NVFP4_DS_MLA:
+        assert np.array_equal(g[:, O.NVFP4_SCALES:], r[:, O.NVFP4_SCALES:]), \
+            "nvfp4 block scales / k_pe differ"
+        gv, rv = g[:, :O.NVFP4_SCALES], r[:, :O.NVFP4_SCALES]
+        gc = np.concatenate([gv & 0xF, gv >> 4], axis=1)
+        rc = np.concatenate([rv & 0xF, rv >> 4], axis=1)
+        frac = float(np.mean(gc == rc))
+        dist = np.abs(e2m1_ordinal(gc) - e2m1_ordinal(rc))
+        if report is not None:
+            report["cache_fp4_exact"] = frac
+            report["cache_fp4_max_code_dist"] = int(dist.max(initial=0))
+        assert frac >= FRAC_FP8_EXACT, f"only {frac:.5f} of E2M1 codes identical"
+        assert dist.max(initial=0) <= 1, f"E2M1 codes up to {dist.max()} apart"
+        return
     if layout == O.LAYOUT_DS_MLA:
         assert np.array_equal(g[:, O.DS_SCALES:], r[:, O.DS_SCALES:]), "ds scales / k_pe differ"
         g, r = g[:, :O.DS_SCALES], r[:, :O.DS_SCALES]

@@ -26,6 +26,21 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, n), f"{n} declared in include/mla_query.h but not exported"
 
 
+def test_binding_constants_match_the_header():
+    """Every numeric #define of include/mla_query.h has the same value in the
+    binding (layouts, paths, error codes, device flags, limits)."""
+    import re
+
+    hdr = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "mla_query.h")
+    with open(hdr) as f:
+        text = f.read()
+    found = re.findall(r"#define\s+(MLA_[A-Z0-9_]+)\s+\(?(-?\d+)u?\)?", text)
+    assert len(found) >= 15
+    for name, value in found:
+        assert getattr(B, name) == int(value), name
+    assert B.MLA_KV_NVFP4_DS_MLA == 2
+
+
 def test_no_unexported_internal_symbols(lib):
     # internal kernels and helpers stay hidden (only the C ABI is public)
     with pytest.raises(AttributeError):

@@ -43,6 +43,8 @@ def _bits(t):
         (70, 16, S.LAYOUT_DS_MLA, B.MLA_PATH_AUTO), # wide kernel, two 64-token slices
         (4, 16, S.LAYOUT_E4M3, B.MLA_PATH_AUTO),    # partials + closing kernel (small H)
         (2, 32, S.LAYOUT_E4M3, B.MLA_PATH_FMA),     # FP32-FMA absorbing kernel
+        (8, 64, S.LAYOUT_NVFP4_DS_MLA, B.MLA_PATH_AUTO),   # FP8 query + nvfp4_ds_mla rows
+        (40, 32, S.LAYOUT_NVFP4_DS_MLA, B.MLA_PATH_AUTO),  # the same on the wide kernel
     ],
 )
 def test_fp8_query_codes_follow_the_bf16_outputs(batch, heads, layout, path):

@@ -62,6 +62,34 @@ def test_sweep(batch, heads, layout):
     assert_parity(inp)
 
 
+@pytest.mark.parametrize("heads", [64, 128])
+@pytest.mark.parametrize("batch", [1, 2, 8, 16, 17, 64, 70])
+def test_nvfp4_ds_mla_rows(batch, heads):
+    """The nvfp4_ds_mla cache layout on every kernel the batch selects
+    (paired 8 and 16 tokens, wide, wide in two slices), 1% kv_c outliers."""
+    inp = S.make_inputs(**S.sweep_workload(batch, heads, S.LAYOUT_NVFP4_DS_MLA))
+    rep = {}
+    assert_parity(inp, report=rep)
+    print(batch, heads, rep)
+
+
+@pytest.mark.parametrize("path", [B.MLA_PATH_FMA, B.MLA_PATH_MMA])
+def test_nvfp4_zero_rows_and_bad_slots(path):
+    """kv_c rows of zeros normalise to zeros: every block takes the scale floor
+    2**-9 (E4M3 0x01) and code 0; a skipped and an out-of-range slot leave
+    their rows alone."""
+    inp = S.make_inputs(batch=2, heads=16, layout=S.LAYOUT_NVFP4_DS_MLA, pages=4, seed=650)
+    inp["kv_c"][0, :] = 0
+    out, ref = assert_parity(inp, path=path)
+    s = int(inp["slots"][0])
+    row = out["cache"][s // 64, s % 64]
+    assert np.all(row[:256] == 0) and np.all(row[256:288] == 0x01)
+    inp = S.make_inputs(batch=4, heads=8, layout=S.LAYOUT_NVFP4_DS_MLA, pages=4, seed=651)
+    inp["slots"] = np.array([-1, 7, 4 * 64, 200], dtype=np.int64)
+    out, ref = assert_parity(inp)
+    assert ref["bad_slots"] == [2]
+
+
 @pytest.mark.parametrize("batch", [3, 5, 7, 9, 15, 17, 31, 33, 63, 65, 100, 200, 256])
 def test_ragged_batches(batch):
     layout = S.LAYOUT_DS_MLA if batch % 2 else S.LAYOUT_E4M3
@@ -97,7 +125,8 @@ def test_fma_path_refuses_large_batch():
 
 @pytest.mark.parametrize("batch", [1, 8, 24])
 def test_fused_qkv_row_strides(batch):
-    inp = S.make_inputs(batch=batch, heads=16, layout=S.LAYOUT_E4M3, pages=8, seed=400 + batch)
+    layout = S.LAYOUT_NVFP4_DS_MLA if batch == 8 else S.LAYOUT_E4M3
+    inp = S.make_inputs(batch=batch, heads=16, layout=layout, pages=8, seed=400 + batch)
     assert_parity(inp, fused_row=True)
 
 

@@ -46,7 +46,8 @@ def _bits(t):
 
 @pytest.mark.parametrize(
     "batch,heads,layout",
-    [(1, 64, S.LAYOUT_E4M3), (8, 128, S.LAYOUT_E4M3), (33, 32, S.LAYOUT_DS_MLA)],
+    [(1, 64, S.LAYOUT_E4M3), (8, 128, S.LAYOUT_E4M3), (33, 32, S.LAYOUT_DS_MLA),
+     (5, 16, S.LAYOUT_NVFP4_DS_MLA)],
 )
 def test_noalloc_matches_oracle_twice(batch, heads, layout):
     inp = S.make_inputs(batch=batch, heads=heads, layout=layout, pages=64, seed=1200 + batch)
