@@ -12,9 +12,13 @@ Workload recipe (the shapes and value distributions of the MLA query workloads):
   (distinct slots); the cache is pre-filled with random bytes.
   Options: ``row_scale`` multiplies each q_a and each kv_c row by its own factor
   drawn log-uniform in [0.1, 10]; ``outliers`` multiplies a Bernoulli(p) subset
-  of kv_c values by 1e3.
+  of kv_c values by 1e3; ``hidden`` also draws the down-projection that makes
+  the fused q_a | kv_c | k_pe row: hidden rows [B, 7168] ~ N(0, 1) and its
+  weight W_QKV_A [2112, 7168] ~ N(0, 0.012) (0.012 ~ 1/sqrt(7168), so the
+  projected row has about unit variance, like the drawn activations).
 Draw order is fixed: W_QB, W_UK, gamma_q, gamma_kv, q_a, kv_c, k_pe, slots,
-outlier mask, row scales, cache pre-fill.
+outlier mask, row scales, cache pre-fill, then (``hidden``) W_QKV_A and the
+hidden rows.
 """
 
 from __future__ import annotations
@@ -37,7 +41,13 @@ WORKLOADS = {
     "tensorcore_b64_h128_ds": dict(
         batch=64, heads=128, layout=LAYOUT_DS_MLA, pages=4096, seed=3, outliers=0.01
     ),
+    # the step from the hidden row: down-projection 7168 -> 2112, then the path
+    "hidden_b1_h64_e4m3": dict(
+        batch=1, heads=64, layout=LAYOUT_E4M3, pages=1024, seed=5, hidden=True
+    ),
 }
+QKV_ROW = 2112
+HIDDEN = 7168
 
 
 def sweep_workload(batch: int, heads: int, layout: int, seed: int = 4) -> dict:
@@ -71,6 +81,7 @@ def make_inputs(
     outliers: float = 0.0,
     page_size: int = PAGE_SIZE,
     prefill: bool = True,
+    hidden: bool = False,
 ) -> dict:
     """All inputs of one decode step, as numpy arrays of raw bits.
 
@@ -112,7 +123,20 @@ def make_inputs(
         heads=heads,
         batch=batch,
     )
+    if hidden:
+        out.update(qkv_a_weights(rng), hidden=hidden_rows(batch, rng))
     return out
+
+
+def qkv_a_weights(rng: np.random.Generator, n: int = QKV_ROW, k: int = HIDDEN) -> dict:
+    """W_QKV_A [n, k] ~ N(0, 0.012), BF16 bits."""
+    w = rng.standard_normal((n, k), dtype=np.float32) * np.float32(0.012)
+    return dict(w_qkv_a=to_bf16_bits(w))
+
+
+def hidden_rows(batch: int, rng: np.random.Generator, k: int = HIDDEN) -> np.ndarray:
+    """Hidden rows [batch, k] ~ N(0, 1), BF16 bits."""
+    return to_bf16_bits(rng.standard_normal((batch, k), dtype=np.float32))
 
 
 def workload_inputs(name: str, **override) -> dict:

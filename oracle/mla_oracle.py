@@ -65,6 +65,11 @@ NVFP4_BLOCK = 16
 NVFP4_SCALES = KV_LORA // 2  # 256: byte offset of the 32 block scales
 NVFP4_ROPE = NVFP4_SCALES + KV_LORA // NVFP4_BLOCK  # 288: byte offset of E4M3 k_pe
 ROW_BYTES_NVFP4 = NVFP4_ROPE + QK_ROPE  # 352
+
+# The fused row q_a | kv_c | k_pe that the path reads, and the hidden width
+# of the down-projection producing it.
+QKV_ROW = Q_LORA + KV_LORA + QK_ROPE  # 2112
+HIDDEN = 7168
 E2M1_MAX = 6.0
 NVFP4_SCALE_FLOOR = 2.0**-9  # the smallest positive E4M3 value
 
@@ -386,6 +391,24 @@ def kv_row_nvfp4(normed_bf16, k_pe):
     row[:NVFP4_SCALES] = codes[0::2] | (codes[1::2] << np.uint8(4))
     row[NVFP4_ROPE:] = e4m3_satfinite(np.asarray(k_pe, dtype=np.float64))
     return row, scales
+
+
+def qkv_a_projection(x_bits, w_bits):
+    """The down-projection that produces the fused qkv row the path reads:
+    ``y[b, n] = bf16(sum_k x[b, k] * W[n, k])`` (page "ws_gemm", class
+    ``WsGemm``: ``y[M, N] = x[M, K] @ W[N, K]^T`` with BF16 operands, FP32
+    accumulation and BF16 outputs).  With W = the stacked q_a / kv_a
+    projections [2112, 7168], row b of y is the ``qkv`` row of page
+    "mla.query" (``kernel``): q_a at columns 0..1535, kv_c at 1536..2047,
+    k_pe at 2048..2111.
+
+    ``x_bits`` uint16 BF16 [B, K], ``w_bits`` uint16 BF16 [N, K].  Returns
+    (BF16 bits of y [B, N], exact float64 sums, sums of |terms|)."""
+    x = bf16_bits_to_f64(x_bits)
+    w = bf16_bits_to_f64(w_bits)
+    exact = x @ w.T
+    cond = np.abs(x) @ np.abs(w).T
+    return f64_to_bf16_bits(exact), exact, cond
 
 
 def slot_to_page(slot, page_size):

@@ -618,3 +618,45 @@ def test_nvfp4_k_pe_is_unscaled_e4m3():
     row, _ = O.kv_row_nvfp4(np.ones(512), kpe)
     ref = torch.from_numpy(kpe.astype(np.float32)).clamp(-448, 448).to(torch.float8_e4m3fn)
     assert np.array_equal(row[288:], ref.view(torch.uint8).numpy())
+
+
+# ---------------------------------------------------------------- qkv_a projection
+
+
+def test_qkv_a_projection_brute_force():
+    rng = np.random.default_rng(41)
+    B, N, K = 3, 5, 37
+    x = _bf16(rng.standard_normal((B, K)))
+    w = _bf16(rng.standard_normal((N, K)) * 0.1)
+    y, exact, cond = O.qkv_a_projection(x, w)
+    xf, wf = O.bf16_bits_to_f64(x), O.bf16_bits_to_f64(w)
+    for b in range(B):
+        for n in range(N):
+            s = a = 0.0
+            for k in range(K):
+                s += xf[b, k] * wf[n, k]
+                a += abs(xf[b, k] * wf[n, k])
+            assert abs(exact[b, n] - s) <= 1e-12 * a
+            assert abs(cond[b, n] - a) <= 1e-12 * a
+            assert y[b, n] == _bf16([s])[0]
+
+
+def test_qkv_a_projection_one_hot_and_orientation():
+    """x = e_k picks column k of W for every output row: y[b, n] = W[n, k]
+    (W is [N, K], rows are outputs); a transposed operand would fail."""
+    N, K = 6, 10
+    w = _bf16(np.arange(N * K, dtype=np.float64).reshape(N, K) / 64.0)
+    for k in (0, 3, 9):
+        x = np.zeros((1, K))
+        x[0, k] = 1.0
+        y, _, _ = O.qkv_a_projection(_bf16(x), w)
+        assert np.array_equal(y[0], w[:, k])
+
+
+def test_qkv_a_projection_rounds_once():
+    """Terms whose exact sum is 1 + 2**-9 (below the BF16 midpoint 1 + 2**-8)
+    give 1.0; 1 + 3 * 2**-9 (above it) gives 1 + 2**-7."""
+    w = _bf16([[1.0, 2.0**-9, 0.0], [1.0, 2.0**-9, 2.0**-8]])
+    y, exact, _ = O.qkv_a_projection(_bf16([[1.0, 1.0, 1.0]]), w)
+    assert exact[0, 0] == 1 + 2.0**-9 and y[0, 0] == _bf16([1.0])[0]
+    assert exact[0, 1] == 1 + 3 * 2.0**-9 and y[0, 1] == _bf16([1 + 2.0**-7])[0]
