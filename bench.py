@@ -36,22 +36,29 @@ FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["mla_query_projection_gb300/csrc/mla_common.cuh",
                   "mla_query_projection_gb300/csrc/mla_device.cuh",
                   "mla_query_projection_gb300/csrc/mla_fused.cu",
-                  "mla_query_projection_gb300/csrc/mla_wide.cu"]
+                  "mla_query_projection_gb300/csrc/mla_wide.cu",
+                  "mla_query_projection_gb300/csrc/mla_qkv_a.cu"]
 
 
-def algorithmic_bytes(batch: int, heads: int, layout: int) -> int:
+def algorithmic_bytes(batch: int, heads: int, layout: int, hidden: bool = False) -> int:
     """Bytes one decode step must move: W_QB (H*192*1536*2) + W_UK (H*128*512*2)
     + gammas (2*(1536+512)) + activations read (B*(1536+512+64)*2 + 8 slot)
     + outputs written (B*H*(512+64)*2 + q_c B*1536*2) + cache rows (576, 656
-    or 352 bytes by layout)."""
+    or 352 bytes by layout).  A step from the hidden row adds the qkv_a
+    projection: W_QKV_A (2112*7168*2), the hidden rows (B*7168*2) and the
+    fused row it writes (B*2112*2)."""
     row = {0: 576, 1: 656, 2: 352}[layout]
-    return (heads * 192 * 1536 * 2 + heads * 128 * 512 * 2 + 2 * (1536 + 512)
-            + batch * ((1536 + 512 + 64) * 2 + 8) + batch * heads * (512 + 64) * 2
-            + batch * 1536 * 2 + batch * row)
+    n = (heads * 192 * 1536 * 2 + heads * 128 * 512 * 2 + 2 * (1536 + 512)
+         + batch * ((1536 + 512 + 64) * 2 + 8) + batch * heads * (512 + 64) * 2
+         + batch * 1536 * 2 + batch * row)
+    if hidden:
+        n += QKV_ROW * HIDDEN * 2 + batch * HIDDEN * 2 + batch * QKV_ROW * 2
+    return n
 
 
-def algorithmic_flops(batch: int, heads: int) -> int:
-    return 2 * batch * heads * (192 * 1536 + 128 * 512)
+def algorithmic_flops(batch: int, heads: int, hidden: bool = False) -> int:
+    f = 2 * batch * heads * (192 * 1536 + 128 * 512)
+    return f + (2 * batch * QKV_ROW * HIDDEN if hidden else 0)
 
 
 def kernel_hash() -> str:
@@ -71,6 +78,9 @@ def read_peaks() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
+QKV_ROW, HIDDEN = 2112, 7168
+
+
 def kernel_for(path: int, batch: int) -> str:
     """The kernel one decode step launches on the given path (MLA_PATH_FMA:
     the FP32-FMA absorbing kernel, one or two tokens per CTA; MLA_PATH_MMA:
@@ -83,14 +93,16 @@ def kernel_for(path: int, batch: int) -> str:
     return f"mla_absorb_pair_kernel<{8 if batch <= 8 else 16}>"
 
 
-def launches_per_step(path: int, batch: int) -> int:
+def launches_per_step(path: int, batch: int, hidden: bool = False) -> int:
     """Kernels one decode call launches: the FMA absorbing kernel is followed by
     the head-closing kernel; the paired kernel runs once up to 16 tokens, above
     that the wide tcgen05 kernel (after its normalising kernel) once per 64
-    tokens."""
+    tokens.  A step from the hidden row first runs the qkv_a projection once
+    per 8 tokens."""
+    pre = -(-batch // 8) if hidden else 0
     if path == 1:
-        return 2
-    return 2 * -(-batch // 64) if batch > 16 else 1
+        return pre + 2
+    return pre + (2 * -(-batch // 64) if batch > 16 else 1)
 
 
 def profile_name(kernel: str, workload: str) -> str:
@@ -244,8 +256,9 @@ def gpu_arm(args, rank: int, world: int, local_rank: int) -> dict | None:
     cfg = workload_cfg(args.workload)
     inp = S.make_inputs(**cfg)
     Bn, H, layout = cfg["batch"], cfg["heads"], cfg["layout"]
+    hidden = bool(cfg.get("hidden", False))
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    wbytes = H * (192 * 1536 + 128 * 512) * 2
+    wbytes = H * (192 * 1536 + 128 * 512) * 2 + (QKV_ROW * HIDDEN * 2 if hidden else 0)
     nsets = max(1, -(-3 * l2 // wbytes))
 
     # Weight sets: set 0 from the seeded generator, the others drawn on the
@@ -266,6 +279,11 @@ def gpu_arm(args, rank: int, world: int, local_rank: int) -> dict | None:
                 gamma_kv=(1 + 0.1 * torch.randn(512, device=dev, generator=gen)).bfloat16())
         w["handle"] = B.mla_query_create(H, w["w_qb"], w["w_uk"], w["gamma_q"], w["gamma_kv"],
                                          float(inp["eps"]))
+        if hidden:
+            w["w_qkv_a"] = (bf16_tensor(inp["w_qkv_a"], dev) if k == 0 else
+                            (torch.randn(QKV_ROW, HIDDEN, device=dev, generator=gen)
+                             * 0.012).bfloat16())
+            w["qkv_a"] = B.mla_qkv_a_create(QKV_ROW, HIDDEN, w["w_qkv_a"])
         if args.path:
             B.mla_query_set_path(w["handle"], args.path)
         sets.append(w)
@@ -280,9 +298,20 @@ def gpu_arm(args, rank: int, world: int, local_rank: int) -> dict | None:
     q_pe = torch.empty(Bn, H, 64, dtype=torch.bfloat16, device=dev)
     q_c = torch.empty(Bn, 1536, dtype=torch.bfloat16, device=dev)
     pages, psize = cache.shape[0], cache.shape[1]
+    if hidden:
+        # the step from the hidden row: the projection writes the fused row
+        # the decode step reads
+        x_hidden = bf16_tensor(inp["hidden"], dev)
+        y_row = torch.empty(Bn, QKV_ROW, dtype=torch.bfloat16, device=dev)
 
     def decode(j, stream, qa=q_a, kvc=kv_c, kpe=k_pe, sl=slots, ql=q_latent, qp=q_pe, qc=q_c):
-        rc = B.mla_query_decode(sets[j % nsets]["handle"], Bn, qa, 0, kvc, 0, kpe, 0, sl, cache,
+        st = 0
+        if hidden:
+            rc = B.mla_qkv_a_run(sets[j % nsets]["qkv_a"], Bn, x_hidden, 0, y_row, QKV_ROW, stream)
+            if rc != B.MLA_OK:
+                raise RuntimeError(f"mla_qkv_a_run: {B.strerror(rc)}")
+            qa, kvc, kpe, st = y_row, y_row[:, 1536:], y_row[:, 2048:], QKV_ROW
+        rc = B.mla_query_decode(sets[j % nsets]["handle"], Bn, qa, st, kvc, st, kpe, st, sl, cache,
                                 pages, psize, layout, k_scale, ql, qp, qc, stream)
         if rc != B.MLA_OK:
             raise RuntimeError(f"mla_query_decode: {B.strerror(rc)}")
@@ -335,9 +364,11 @@ def gpu_arm(args, rank: int, world: int, local_rank: int) -> dict | None:
     clocks = sampler.stop()
     ms = e0.elapsed_time(e1)
     path = B.mla_query_path_for(sets[0]["handle"], Bn)
-    flags = B.mla_query_get_error(sets[0]["handle"], stream)
-    for w in sets[1:]:
+    flags = 0
+    for w in sets:
         flags |= B.mla_query_get_error(w["handle"], stream)
+        if hidden:
+            flags |= B.mla_qkv_a_get_error(w["qkv_a"], stream)
     if flags:
         raise RuntimeError(f"device error flags {flags} during the timed run")
 
@@ -346,16 +377,21 @@ def gpu_arm(args, rank: int, world: int, local_rank: int) -> dict | None:
     # inputs as fused q_a|kv_c|k_pe rows (stride 2112) followed by the slots,
     # the outputs as q_latent|q_pe|q_c back to back.
     K_e = max(1, min(args.steps, args.e2e_steps))
-    row = 1536 + 512 + 64
+    row = HIDDEN if hidden else QKV_ROW  # the step's input row: hidden, or q_a|kv_c|k_pe
     in_rows = Bn * row * 2
     in_bytes = in_rows + Bn * 8
     h_in = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
-    fused = torch.cat([q_a.cpu(), kv_c.cpu(), k_pe.cpu()], dim=1).contiguous()
+    if hidden:
+        fused = x_hidden.cpu().contiguous()
+    else:
+        fused = torch.cat([q_a.cpu(), kv_c.cpu(), k_pe.cpu()], dim=1).contiguous()
     h_in[:in_rows].copy_(fused.view(torch.uint8).reshape(-1))
     h_in[in_rows:].copy_(slots.cpu().view(torch.uint8).reshape(-1))
     d_in = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
     d_rows = d_in[:in_rows].view(torch.bfloat16).view(Bn, row)
     d_sl = d_in[in_rows:].view(torch.int64)
+    if hidden:
+        e_row = torch.empty(Bn, QKV_ROW, dtype=torch.bfloat16, device=dev)
     o_sizes = [Bn * H * 512 * 2, Bn * H * 64 * 2, Bn * 1536 * 2]
     d_out = torch.empty(sum(o_sizes), dtype=torch.uint8, device=dev)
     e_ql = d_out[:o_sizes[0]].view(torch.bfloat16)
@@ -365,9 +401,16 @@ def gpu_arm(args, rank: int, world: int, local_rank: int) -> dict | None:
 
     def e2e_step(j):
         d_in.copy_(h_in, non_blocking=True)
-        rc = B.mla_query_decode(sets[j % nsets]["handle"], Bn, d_rows, row, d_rows[:, 1536:], row,
-                                d_rows[:, 2048:], row, d_sl, cache, pages, psize, layout, k_scale,
-                                e_ql, e_qp, e_qc, stream)
+        r_in = d_rows
+        if hidden:
+            rc = B.mla_qkv_a_run(sets[j % nsets]["qkv_a"], Bn, d_rows, HIDDEN, e_row, QKV_ROW,
+                                 stream)
+            if rc != B.MLA_OK:
+                raise RuntimeError(f"mla_qkv_a_run: {B.strerror(rc)}")
+            r_in = e_row
+        rc = B.mla_query_decode(sets[j % nsets]["handle"], Bn, r_in, QKV_ROW, r_in[:, 1536:],
+                                QKV_ROW, r_in[:, 2048:], QKV_ROW, d_sl, cache, pages, psize,
+                                layout, k_scale, e_ql, e_qp, e_qc, stream)
         if rc != B.MLA_OK:
             raise RuntimeError(f"mla_query_decode: {B.strerror(rc)}")
         h_out.copy_(d_out, non_blocking=True)
@@ -393,11 +436,13 @@ def gpu_arm(args, rank: int, world: int, local_rank: int) -> dict | None:
 
     for w in sets:
         B.mla_query_destroy(w["handle"])
+        if hidden:
+            B.mla_qkv_a_destroy(w["qkv_a"])
 
     per_step_ms, per_step_e2e_ms = max_over_ranks([ms / args.steps, ms_e2e / K_e], dev)
 
     return dict(per_step_ms=per_step_ms, per_step_e2e_ms=per_step_e2e_ms, h2d=h2d, d2h=d2h,
-                clocks=clocks, nsets=nsets, l2=l2, K_e=K_e, cfg=cfg, path=path)
+                clocks=clocks, nsets=nsets, l2=l2, K_e=K_e, cfg=cfg, path=path, wbytes=wbytes)
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -414,10 +459,14 @@ for k in ("layout",):
 for k in ("k_scale", "eps"):
     inp[k] = float(inp[k])
 budget, steps = float(sys.argv[3]), int(sys.argv[4])
-O.decode_step(inp)  # warm
+def step():
+    if "hidden" in inp:  # the step from the hidden row starts with the projection
+        O.qkv_a_projection(inp["hidden"], inp["w_qkv_a"])
+    O.decode_step(inp)
+step()  # warm
 t0 = time.perf_counter(); n = 0
 while True:
-    O.decode_step(inp); n += 1
+    step(); n += 1
     el = time.perf_counter() - t0
     if (steps and n >= steps) or (not steps and el >= budget):
         break
@@ -492,9 +541,12 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     cfg = workload_cfg(args.workload)
     Bn, H, layout = cfg["batch"], cfg["heads"], cfg["layout"]
+    hidden = bool(cfg.get("hidden", False))
     config = {"workload": args.workload, "batch": Bn, "heads": H,
-              "kv_layout": "fp8_ds_mla" if layout == 1 else "fp8_e4m3_per_tensor",
+              "kv_layout": {0: "fp8_e4m3_per_tensor", 1: "fp8_ds_mla", 2: "nvfp4_ds_mla"}[layout],
               "pages": cfg["pages"], "page_size": 64}
+    if hidden:
+        config["input"] = f"hidden rows [{Bn}, {HIDDEN}] through the qkv_a projection"
 
     if args.impl == "reference":
         # The reference arm is the FP64 CPU oracle; rank 0 alone runs it.
@@ -537,13 +589,15 @@ def main():
 
     per_step_us = r["per_step_ms"] * 1e3
     value = whole_job_us(per_step_us, world)
-    nbytes = algorithmic_bytes(Bn, H, layout)
+    nbytes = algorithmic_bytes(Bn, H, layout, hidden)
     achieved = nbytes / (per_step_us * 1e-6) / 1e9
     peak, peak_src = read_peaks()
     kernel = kernel_for(r["path"], Bn)
+    if hidden:
+        kernel = "mla_qkv_a_kernel+" + kernel
     config.update({
         "l2_policy": f"inputs larger than L2: {r['nsets']} rotating weight sets "
-                     f"({r['nsets'] * H * 720 * 1024 / 1e6:.0f} MB vs L2 {r['l2'] / 1e6:.0f} MB)",
+                     f"({r['nsets'] * r['wbytes'] / 1e6:.0f} MB vs L2 {r['l2'] / 1e6:.0f} MB)",
         "graph_steps": args.graph_steps, "parallelism": f"replicas{world}",
     })
     line = {
@@ -558,12 +612,12 @@ def main():
                      "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
                      "algorithmic_bytes_per_launch": nbytes,
                      "traffic": read_traffic(kernel, args.workload),
-                     "kernel": kernel, "gflop_per_launch": algorithmic_flops(Bn, H) / 1e9},
+                     "kernel": kernel, "gflop_per_launch": algorithmic_flops(Bn, H, hidden) / 1e9},
         "e2e": {"value": r["per_step_e2e_ms"] * 1e3 / world, "unit": "us",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                 "steps": r["K_e"],
                 "note": "eager: one pinned H2D copy, the C-ABI decode, one pinned D2H copy per step"},
-        "gpu_launches": args.steps * launches_per_step(r["path"], Bn),
+        "gpu_launches": args.steps * launches_per_step(r["path"], Bn, hidden),
         "clocks": r["clocks"],
     }
     if not args.no_cpu and world == 1:

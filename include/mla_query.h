@@ -239,6 +239,61 @@ MLA_API void mla_query_destroy(mla_query_t h);
 /* mla_query_strerror - static text for a return code. */
 MLA_API const char* mla_query_strerror(int code);
 
+/* ---------------------------------------------------------------------------
+ * The qkv_a down-projection: the step that produces the fused row the decode
+ * step reads (page "ws_gemm", class WsGemm: y[M, N] = x[M, K] @ W[N, K]^T,
+ * BF16 operands, FP32 accumulation, BF16 outputs; page "mla.query", method
+ * kernel: the qkv row holds q_a at columns 0..1535, kv_c at 1536..2047 and
+ * k_pe at 2048..2111).  With W = the stacked q_a / kv_a projections
+ * [2112][7168], y[b] can be handed to mla_query_decode as a fused row
+ * (q_a = y, kv_c = y + 1536, k_pe = y + 2048, all strides 2112); run on the
+ * same stream, the decode's weight streaming overlaps this call's tail.
+ * ------------------------------------------------------------------------- */
+typedef struct mla_qkv_a* mla_qkv_a_t;
+
+/*
+ * mla_qkv_a_create - bind the projection weight.
+ *
+ *   out  receives the handle.
+ *   n    output columns (rows of W), 1 <= n; n / SMs rounded up must be at
+ *        most 15 (n <= 2280 on 152 SMs).
+ *   k    input columns, a multiple of 512, 512 <= k <= 7168.
+ *   w    device BF16 [n][k], row-major, 16-byte aligned.  Borrowed: read in
+ *        place at every call, so it must stay valid and unchanged until
+ *        mla_qkv_a_destroy.
+ *
+ * Allocates a 4-byte device error word.  Returns MLA_OK, MLA_EINVAL (null or
+ * misaligned pointer, bad n or k), MLA_EUNSUPPORTED (n or k beyond the limits
+ * above), MLA_ENOMEM or MLA_ECUDA.
+ */
+MLA_API int mla_qkv_a_create(mla_qkv_a_t* out, int n, int k, const void* w);
+
+/*
+ * mla_qkv_a_run - y[b][j] = bf16(sum_i x[b][i] * W[j][i]) for b < batch, on
+ * `stream`, asynchronously (no host sync, no allocation).
+ *
+ *   batch     1 <= batch <= MLA_MAX_BATCH; one launch per 8 tokens.
+ *   x         device BF16 [batch][x_stride] (first k used), 16-byte aligned;
+ *             x_stride in elements, 0 means k; a multiple of 8.
+ *   y         device BF16 [batch][y_stride] output (first n written);
+ *             y_stride in elements, 0 means n.
+ *   stream    cudaStream_t as void*.
+ *
+ * W is streamed before the previous kernel on the stream completes
+ * (programmatic dependent launch); x is read, and y written, only after it.
+ * Returns MLA_OK, MLA_EINVAL or MLA_ECUDA (launch error).
+ */
+MLA_API int mla_qkv_a_run(mla_qkv_a_t h, int batch, const void* x, int64_t x_stride, void* y,
+                          int64_t y_stride, void* stream);
+
+/* mla_qkv_a_get_error - read and clear the handle's device error word
+ * (MLA_DEVERR_TIMEOUT if a bounded wait gave up); synchronises `stream`. */
+MLA_API int mla_qkv_a_get_error(mla_qkv_a_t h, unsigned* device_flags, void* stream);
+
+/* mla_qkv_a_destroy - free the handle (NULL is a no-op).  No call on it may
+ * still be in flight. */
+MLA_API void mla_qkv_a_destroy(mla_qkv_a_t h);
+
 #ifdef __cplusplus
 }
 #endif

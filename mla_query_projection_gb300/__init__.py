@@ -24,4 +24,8 @@ from .binding import (  # noqa: F401
     mla_query_get_error,
     mla_query_path_for,
     mla_query_set_path,
+    mla_qkv_a_create,
+    mla_qkv_a_destroy,
+    mla_qkv_a_get_error,
+    mla_qkv_a_run,
 )

@@ -81,6 +81,14 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.mla_query_destroy.restype = None
     lib.mla_query_strerror.argtypes = [i32]
     lib.mla_query_strerror.restype = ctypes.c_char_p
+    lib.mla_qkv_a_create.argtypes = [ctypes.POINTER(vp), i32, i32, vp]
+    lib.mla_qkv_a_create.restype = i32
+    lib.mla_qkv_a_run.argtypes = [vp, i32, vp, i64, vp, i64, vp]
+    lib.mla_qkv_a_run.restype = i32
+    lib.mla_qkv_a_get_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint), vp]
+    lib.mla_qkv_a_get_error.restype = i32
+    lib.mla_qkv_a_destroy.argtypes = [vp]
+    lib.mla_qkv_a_destroy.restype = None
     _lib = lib
     return lib
 
@@ -181,6 +189,34 @@ def mla_query_destroy(handle) -> None:
     load().mla_query_destroy(handle)
 
 
+def mla_qkv_a_create(n, k, w) -> int:
+    """Handle of the qkv_a down-projection y = x @ W^T (W [n][k] BF16 on the
+    device, borrowed); raises MlaError on failure."""
+    h = ctypes.c_void_p()
+    rc = load().mla_qkv_a_create(ctypes.byref(h), int(n), int(k), _ptr(w))
+    if rc != MLA_OK:
+        raise MlaError(rc, "mla_qkv_a_create")
+    return h.value
+
+
+def mla_qkv_a_run(handle, batch, x, x_stride, y, y_stride, stream) -> int:
+    return load().mla_qkv_a_run(
+        handle, int(batch), _ptr(x), int(x_stride), _ptr(y), int(y_stride), _stream(stream)
+    )
+
+
+def mla_qkv_a_get_error(handle, stream=None) -> int:
+    v = ctypes.c_uint(0)
+    rc = load().mla_qkv_a_get_error(handle, ctypes.byref(v), _stream(stream))
+    if rc != MLA_OK:
+        raise MlaError(rc, "mla_qkv_a_get_error")
+    return v.value
+
+
+def mla_qkv_a_destroy(handle) -> None:
+    load().mla_qkv_a_destroy(handle)
+
+
 def exported_symbols() -> list[str]:
     """Function names the public header declares."""
     import re
@@ -188,4 +224,4 @@ def exported_symbols() -> list[str]:
     hdr = os.path.join(os.path.dirname(HERE), "include", "mla_query.h")
     with open(hdr) as f:
         text = f.read()
-    return sorted(set(re.findall(r"\b(mla_query_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(mla_(?:query|qkv_a)_[a-z_0-9]+)\s*\(", text)))

@@ -26,10 +26,12 @@ class DecodeStep:
     """Device copies of one workload's inputs and outputs plus a handle.
 
     ``fused_row=True`` packs q_a | kv_c | k_pe into one [B, 2112] row (strided
-    inputs, the layout of a fused qkv activation)."""
+    inputs, the layout of a fused qkv activation).  ``hidden=True`` makes that
+    row on the device instead: every ``decode`` first runs the qkv_a
+    down-projection of ``inp["hidden"]`` through ``inp["w_qkv_a"]`` into it."""
 
     def __init__(self, inp: dict, device="cuda:0", fused_row: bool = False, q_c: bool = True,
-                 weights: dict | None = None):
+                 weights: dict | None = None, hidden: bool = False):
         self.device = torch.device(device)
         dev = self.device
         self.batch = int(inp["q_a"].shape[0])
@@ -45,6 +47,13 @@ class DecodeStep:
             self.gamma_q = bf16_tensor(wsrc["gamma_q"], dev)
             self.gamma_kv = bf16_tensor(wsrc["gamma_kv"], dev)
         Bn, H = self.batch, self.heads
+        self.qkv_a = None
+        if hidden:
+            self.w_qkv_a = bf16_tensor(inp["w_qkv_a"], dev)
+            self.hidden = bf16_tensor(inp["hidden"], dev)
+            n, k = self.w_qkv_a.shape
+            self.qkv_a = B.mla_qkv_a_create(n, k, self.w_qkv_a)
+            fused_row = True
         if fused_row:
             row = np.zeros((Bn, 2112), dtype=np.uint16)
             row[:, :1536] = inp["q_a"]
@@ -70,6 +79,11 @@ class DecodeStep:
 
     def decode(self, stream=None, batch=None) -> int:
         s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        if self.qkv_a is not None:
+            rc = B.mla_qkv_a_run(self.qkv_a, self.batch if batch is None else batch, self.hidden, 0,
+                                 self.row, 2112, s)
+            if rc != B.MLA_OK:
+                return rc
         return B.mla_query_decode(
             self.handle, self.batch if batch is None else batch,
             self.q_a, self.strides[0], self.kv_c, self.strides[1], self.k_pe, self.strides[2],
@@ -92,6 +106,8 @@ class DecodeStep:
         }
         if self.q_c is not None:
             out["q_c"] = bf16_bits(self.q_c)
+        if self.qkv_a is not None:
+            out["qkv_row"] = bf16_bits(self.row)
         return out
 
     def close(self):
@@ -99,6 +115,9 @@ class DecodeStep:
             torch.cuda.synchronize(self.device)
             B.mla_query_destroy(self.handle)
             self.handle = None
+        if self.qkv_a is not None:
+            B.mla_qkv_a_destroy(self.qkv_a)
+            self.qkv_a = None
 
     def __del__(self):
         try:

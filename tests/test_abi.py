@@ -79,3 +79,18 @@ def test_other_entry_points_reject_null_handle(lib):
     with pytest.raises(B.MlaError):
         B.mla_query_get_error(None)
     B.mla_query_destroy(None)  # no-op
+
+
+def test_qkv_a_rejects_bad_arguments_on_host(lib):
+    """The down-projection's host checks run before any device call."""
+    h = ctypes.c_void_p()
+    assert lib.mla_qkv_a_create(None, 2112, 7168, 16) == B.MLA_EINVAL
+    assert lib.mla_qkv_a_create(ctypes.byref(h), 2112, 7168, None) == B.MLA_EINVAL
+    assert lib.mla_qkv_a_create(ctypes.byref(h), 2112, 7168, 24) == B.MLA_EINVAL  # misaligned
+    assert lib.mla_qkv_a_create(ctypes.byref(h), 0, 7168, 16) == B.MLA_EINVAL
+    assert lib.mla_qkv_a_create(ctypes.byref(h), 2112, 7000, 16) == B.MLA_EINVAL  # k % 512
+    assert lib.mla_qkv_a_create(ctypes.byref(h), 2112, 256, 16) == B.MLA_EINVAL  # k < 512
+    assert lib.mla_qkv_a_create(ctypes.byref(h), 2112, 8192, 16) == B.MLA_EUNSUPPORTED
+    assert h.value is None
+    assert lib.mla_qkv_a_run(None, 1, 16, 0, 16, 0, None) == B.MLA_EINVAL
+    lib.mla_qkv_a_destroy(None)
