@@ -170,6 +170,65 @@ MLA_API int mla_query_decode_fp8q(mla_query_t h, int batch, const void* q_a,
                           const float* k_scale, const float* q_scale_inv,
                           void* q_latent_fp8, void* q_pe_fp8, void* q_c, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Gathered query rows (page "mla.query", class MlaQuery, methods publish and
+ * gathered: under decode context parallelism each rank writes its query into
+ * head block `rank` of a [B][q_heads][576] buffer armed with a sentinel, and
+ * the attention side polls until no element is the sentinel).  On one GPU the
+ * ranks are decode calls ordered on a stream; each writes its heads' rows in
+ * place, and the wait is the same bounded check.
+ *
+ * A query row is 576 elements: q_latent (512) then q_pe (64), BF16 (2 bytes)
+ * or, with q_scale_inv, E4M3 (1 byte).  The sentinel is all ones in every
+ * element (a NaN pattern in both types, never written by the decode).
+ * ------------------------------------------------------------------------- */
+#define MLA_MAX_ROW_HEADS 1024           /* q_heads limit of a row buffer    */
+#define MLA_ROWS_WAIT_MAX_NS 2000000000  /* longest wait mla_query_rows_wait accepts */
+
+/*
+ * mla_query_decode_rows - the decode step with the query written as rows:
+ * q_rows[t][head_offset + h][0..511] = q_latent[t][h], [512..575] = q_pe[t][h].
+ *
+ *   Arguments up to k_scale as mla_query_decode.
+ *   q_scale_inv  device FP32 [1] for E4M3 rows (as mla_query_decode_fp8q),
+ *                or NULL for BF16 rows.
+ *   q_rows       device [batch][q_heads][576] elements, 16-byte aligned.
+ *   q_heads      heads per token in the buffer, <= MLA_MAX_ROW_HEADS (for
+ *                example ranks * H, or a padded count the attention kernel
+ *                wants); head_offset + H <= q_heads.
+ *   head_offset  first head of this call's rows (rank * H).
+ *   q_c, stream  as mla_query_decode.
+ * Rows of other heads are not touched.  Returns as mla_query_decode, and
+ * MLA_EUNSUPPORTED where only the hand-off kernel could run the batch.
+ */
+MLA_API int mla_query_decode_rows(mla_query_t h, int batch, const void* q_a,
+                                  int64_t q_a_stride, const void* kv_c, int64_t kv_c_stride,
+                                  const void* k_pe, int64_t k_pe_stride,
+                                  const int64_t* slot_mapping, void* kv_cache,
+                                  int64_t num_pages, int page_size, int layout,
+                                  const float* k_scale, const float* q_scale_inv, void* q_rows,
+                                  int q_heads, int head_offset, void* q_c, void* stream);
+
+/*
+ * mla_query_rows_arm - set every element of q_rows [batch][q_heads][576]
+ * (elem_bytes 1 or 2 per element) to the sentinel, on `stream`.
+ * Returns MLA_OK, MLA_EINVAL or MLA_ECUDA.
+ */
+MLA_API int mla_query_rows_arm(void* q_rows, int batch, int q_heads, int elem_bytes,
+                               void* stream);
+
+/*
+ * mla_query_rows_wait - on `stream`, poll heads 0..wait_heads-1 of every token
+ * of q_rows [batch][q_heads][576] (wait_heads = ranks * H; heads beyond it,
+ * padding, are not polled) until no element is the sentinel.  If some
+ * element still is after limit_ns nanoseconds (0 <= limit_ns <=
+ * MLA_ROWS_WAIT_MAX_NS), the kernel sets MLA_DEVERR_TIMEOUT in the handle's
+ * device flags (mla_query_get_error) and returns; the context stays usable.
+ * Asynchronous.  Returns MLA_OK, MLA_EINVAL or MLA_ECUDA.
+ */
+MLA_API int mla_query_rows_wait(mla_query_t h, const void* q_rows, int batch, int q_heads,
+                                int wait_heads, int elem_bytes, int64_t limit_ns, void* stream);
+
 /*
  * mla_query_get_error - read and clear the handle's device error flag.
  * Synchronises `stream` (host wait).  *device_flags receives the OR of the

@@ -20,6 +20,9 @@ from .binding import (  # noqa: F401
     mla_query_create,
     mla_query_decode,
     mla_query_decode_fp8q,
+    mla_query_decode_rows,
+    mla_query_rows_arm,
+    mla_query_rows_wait,
     mla_query_destroy,
     mla_query_get_error,
     mla_query_path_for,

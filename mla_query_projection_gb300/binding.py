@@ -30,6 +30,8 @@ MLA_PATH_MMA = 2
 MLA_MAX_BATCH = 256
 MLA_MAX_HEADS = 128
 MLA_NOALLOC_MAX_BATCH = 64
+MLA_MAX_ROW_HEADS = 1024
+MLA_ROWS_WAIT_MAX_NS = 2000000000
 
 _lib = None
 
@@ -81,6 +83,14 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.mla_query_destroy.restype = None
     lib.mla_query_strerror.argtypes = [i32]
     lib.mla_query_strerror.restype = ctypes.c_char_p
+    lib.mla_query_decode_rows.argtypes = [
+        vp, i32, vp, i64, vp, i64, vp, i64, vp, vp, i64, i32, i32, vp, vp, vp, i32, i32, vp, vp,
+    ]
+    lib.mla_query_decode_rows.restype = i32
+    lib.mla_query_rows_arm.argtypes = [vp, i32, i32, i32, vp]
+    lib.mla_query_rows_arm.restype = i32
+    lib.mla_query_rows_wait.argtypes = [vp, vp, i32, i32, i32, i32, i64, vp]
+    lib.mla_query_rows_wait.restype = i32
     lib.mla_qkv_a_create.argtypes = [ctypes.POINTER(vp), i32, i32, vp]
     lib.mla_qkv_a_create.restype = i32
     lib.mla_qkv_a_run.argtypes = [vp, i32, vp, i64, vp, i64, vp]
@@ -187,6 +197,31 @@ def mla_query_path_for(handle, batch) -> int:
 
 def mla_query_destroy(handle) -> None:
     load().mla_query_destroy(handle)
+
+
+def mla_query_decode_rows(
+    handle, batch, q_a, q_a_stride, kv_c, kv_c_stride, k_pe, k_pe_stride, slot_mapping,
+    kv_cache, num_pages, page_size, layout, k_scale, q_scale_inv, q_rows, q_heads, head_offset,
+    q_c, stream,
+) -> int:
+    return load().mla_query_decode_rows(
+        handle, int(batch), _ptr(q_a), int(q_a_stride), _ptr(kv_c), int(kv_c_stride), _ptr(k_pe),
+        int(k_pe_stride), _ptr(slot_mapping), _ptr(kv_cache), int(num_pages), int(page_size),
+        int(layout), _ptr(k_scale), _ptr(q_scale_inv), _ptr(q_rows), int(q_heads),
+        int(head_offset), _ptr(q_c), _stream(stream),
+    )
+
+
+def mla_query_rows_arm(q_rows, batch, q_heads, elem_bytes, stream) -> int:
+    return load().mla_query_rows_arm(_ptr(q_rows), int(batch), int(q_heads), int(elem_bytes),
+                                     _stream(stream))
+
+
+def mla_query_rows_wait(handle, q_rows, batch, q_heads, wait_heads, elem_bytes, limit_ns,
+                        stream) -> int:
+    return load().mla_query_rows_wait(handle, _ptr(q_rows), int(batch), int(q_heads),
+                                      int(wait_heads), int(elem_bytes), int(limit_ns),
+                                      _stream(stream))
 
 
 def mla_qkv_a_create(n, k, w) -> int:

@@ -247,11 +247,18 @@ namespace {
 
 // The decode step behind both entry points: BF16 query outputs, or
 // (q_scale_inv != nullptr) per-tensor FP8 ones.
+// Addressing of the q outputs, in output elements: token and head strides of
+// q_latent and of q_pe (see DecodeArgs).  All zero: contiguous [B][H][512] and
+// [B][H][64].
+struct QStrides {
+  int64_t ql_ts, ql_hs, qp_ts, qp_hs;
+};
+
 int decode_impl(mla_query_t h, int batch, const void* q_a, int64_t q_a_stride, const void* kv_c,
                 int64_t kv_c_stride, const void* k_pe, int64_t k_pe_stride,
                 const int64_t* slot_mapping, void* kv_cache, int64_t num_pages, int page_size,
                 int layout, const float* k_scale, const float* q_scale_inv, void* q_latent,
-                void* q_pe, void* q_c, void* stream) {
+                void* q_pe, void* q_c, void* stream, QStrides qs = {0, 0, 0, 0}) {
   if (h == nullptr) return MLA_EINVAL;
   if (batch < 1 || batch > MLA_MAX_BATCH) return MLA_EINVAL;
   if (q_a == nullptr || kv_c == nullptr || k_pe == nullptr || slot_mapping == nullptr ||
@@ -278,7 +285,11 @@ int decode_impl(mla_query_t h, int batch, const void* q_a, int64_t q_a_stride, c
   int nt = 1;
   int rc = pick_kernel(h, batch, &kern, &nt);
   if (rc != MLA_OK) return rc;
-  if (q_scale_inv != nullptr && kern == Kernel::kHandoff) return MLA_EUNSUPPORTED;
+  const bool contiguous = qs.ql_ts == 0;
+  if ((q_scale_inv != nullptr || !contiguous) && kern == Kernel::kHandoff) return MLA_EUNSUPPORTED;
+  if (contiguous)
+    qs = {(int64_t)h->heads * mla::kKvLora, mla::kKvLora, (int64_t)h->heads * mla::kRope,
+          mla::kRope};
 
   mla::DecodeArgs a;
   a.w_qb = h->w_qb;
@@ -301,6 +312,10 @@ int decode_impl(mla_query_t h, int batch, const void* q_a, int64_t q_a_stride, c
   a.k_scale = k_scale;
   a.q_latent = static_cast<uint16_t*>(q_latent);
   a.q_pe = static_cast<uint16_t*>(q_pe);
+  a.ql_ts = qs.ql_ts;
+  a.ql_hs = qs.ql_hs;
+  a.qp_ts = qs.qp_ts;
+  a.qp_hs = qs.qp_hs;
   a.q_c = static_cast<uint16_t*>(q_c);
   a.qn = h->qn;
   a.ready = h->ready;
@@ -336,9 +351,9 @@ int decode_impl(mla_query_t h, int batch, const void* q_a, int64_t q_a_stride, c
       s64.k_pe = a.k_pe + (int64_t)t0 * a.k_pe_stride;
       s64.slots = a.slots + t0;
       s64.q_latent = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(a.q_latent) +
-                                                 (int64_t)t0 * h->heads * mla::kKvLora * qbytes);
+                                                 (int64_t)t0 * a.ql_ts * qbytes);
       s64.q_pe = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(a.q_pe) +
-                                             (int64_t)t0 * h->heads * mla::kRope * qbytes);
+                                             (int64_t)t0 * a.qp_ts * qbytes);
       s64.q_c = a.q_c != nullptr ? a.q_c + (int64_t)t0 * mla::kQLora : nullptr;
       e = mla::launch_wide(s64, h->wide_split, h->wide_ctas, st);
     }
@@ -358,9 +373,9 @@ int decode_impl(mla_query_t h, int batch, const void* q_a, int64_t q_a_stride, c
       s16.k_pe = a.k_pe + (int64_t)t0 * a.k_pe_stride;
       s16.slots = a.slots + t0;
       s16.q_latent = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(a.q_latent) +
-                                                 (int64_t)t0 * h->heads * mla::kKvLora * qbytes);
+                                                 (int64_t)t0 * a.ql_ts * qbytes);
       s16.q_pe = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(a.q_pe) +
-                                             (int64_t)t0 * h->heads * mla::kRope * qbytes);
+                                             (int64_t)t0 * a.qp_ts * qbytes);
       s16.q_c = a.q_c != nullptr ? a.q_c + (int64_t)t0 * mla::kQLora : nullptr;
       e = mla::launch_pair(s16, h->pair_split, h->pair_ctas, s16.batch <= 8 ? 8 : 16, st);
     }
@@ -398,6 +413,52 @@ int mla_query_decode_fp8q(mla_query_t h, int batch, const void* q_a, int64_t q_a
   return decode_impl(h, batch, q_a, q_a_stride, kv_c, kv_c_stride, k_pe, k_pe_stride,
                      slot_mapping, kv_cache, num_pages, page_size, layout, k_scale, q_scale_inv,
                      q_latent_fp8, q_pe_fp8, q_c, stream);
+}
+
+int mla_query_decode_rows(mla_query_t h, int batch, const void* q_a, int64_t q_a_stride,
+                          const void* kv_c, int64_t kv_c_stride, const void* k_pe,
+                          int64_t k_pe_stride, const int64_t* slot_mapping, void* kv_cache,
+                          int64_t num_pages, int page_size, int layout, const float* k_scale,
+                          const float* q_scale_inv, void* q_rows, int q_heads, int head_offset,
+                          void* q_c, void* stream) {
+  if (h == nullptr || q_rows == nullptr) return MLA_EINVAL;
+  if (head_offset < 0 || q_heads < 1 || q_heads > mla::kMaxRowHeads ||
+      head_offset + h->heads > q_heads)
+    return MLA_EINVAL;
+  const int64_t e = q_scale_inv != nullptr ? 1 : 2;  // bytes per element
+  uint8_t* base = static_cast<uint8_t*>(q_rows) + (int64_t)head_offset * mla::kRowElems * e;
+  const int64_t ts = (int64_t)q_heads * mla::kRowElems;
+  return decode_impl(h, batch, q_a, q_a_stride, kv_c, kv_c_stride, k_pe, k_pe_stride,
+                     slot_mapping, kv_cache, num_pages, page_size, layout, k_scale, q_scale_inv,
+                     base, base + mla::kKvLora * e, q_c, stream,
+                     QStrides{ts, mla::kRowElems, ts, mla::kRowElems});
+}
+
+int mla_query_rows_arm(void* q_rows, int batch, int q_heads, int elem_bytes, void* stream) {
+  if (q_rows == nullptr || batch < 1 || batch > MLA_MAX_BATCH || q_heads < 1 ||
+      q_heads > mla::kMaxRowHeads || (elem_bytes != 1 && elem_bytes != 2) || !aligned16(q_rows))
+    return MLA_EINVAL;
+  const size_t bytes = (size_t)batch * q_heads * mla::kRowElems * elem_bytes;
+  if (cudaMemsetAsync(q_rows, 0xFF, bytes, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ECUDA;
+  }
+  return MLA_OK;
+}
+
+int mla_query_rows_wait(mla_query_t h, const void* q_rows, int batch, int q_heads,
+                        int wait_heads, int elem_bytes, int64_t limit_ns, void* stream) {
+  if (h == nullptr || q_rows == nullptr || batch < 1 || batch > MLA_MAX_BATCH || q_heads < 1 ||
+      q_heads > mla::kMaxRowHeads || wait_heads < 1 || wait_heads > q_heads ||
+      (elem_bytes != 1 && elem_bytes != 2) || !aligned16(q_rows) || limit_ns < 0 ||
+      limit_ns > MLA_ROWS_WAIT_MAX_NS)
+    return MLA_EINVAL;
+  if (mla::launch_rows_wait(q_rows, batch, q_heads, wait_heads, elem_bytes, limit_ns, h->err,
+                            h->num_sms, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ECUDA;
+  }
+  return MLA_OK;
 }
 
 int mla_query_get_error(mla_query_t h, unsigned* device_flags, void* stream) {

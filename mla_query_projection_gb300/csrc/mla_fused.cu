@@ -743,7 +743,7 @@ __global__ void __launch_bounds__(256) mla_close_kernel(const DecodeArgs a) {
       acc.z += v[pb].z;
       acc.w += v[pb].w;
     }
-    const int64_t idx = ((int64_t)t * a.heads + h) * kKvLora + 4 * c4;
+    const int64_t idx = (int64_t)t * a.ql_ts + (int64_t)h * a.ql_hs + 4 * c4;
     if (a.q_scale_inv == nullptr) {
       uint2 o;
       o.x = pack_bf16x2(acc.x, acc.y);
@@ -960,8 +960,8 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
 #pragma unroll
               for (int t = 0; t < NT; ++t)
                 if (t < a.batch)
-                  put_q(a, a.q_pe, ((int64_t)t * H + r / kRope) * kRope + r % kRope, v[rr][t],
-                        load_qsi(a));
+                  put_q(a, a.q_pe, (int64_t)t * a.qp_ts + (int64_t)(r / kRope) * a.qp_hs + r % kRope,
+                        v[rr][t], load_qsi(a));
             }
           }
         }
@@ -1280,7 +1280,8 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) v += red[(w * NT + tok) * kRedTok + row];
             const int r = r0 + row;
-            put_q(a, a.q_pe, ((int64_t)tok * H + r / kRope) * kRope + r % kRope, v, load_qsi(a));
+            put_q(a, a.q_pe, (int64_t)tok * a.qp_ts + (int64_t)(r / kRope) * a.qp_hs + r % kRope, v,
+                  load_qsi(a));
           }
         }
         MLA_PHASE(5);
@@ -1658,7 +1659,8 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) v += red[(w * NT + tok) * kRedTok + row];
             const int r = r0 + row;
-            put_q(a, a.q_pe, ((int64_t)tok * H + r / kRope) * kRope + r % kRope, v, load_qsi(a));
+            put_q(a, a.q_pe, (int64_t)tok * a.qp_ts + (int64_t)(r / kRope) * a.qp_hs + r % kRope, v,
+                  load_qsi(a));
           }
         }
         continue;
@@ -1787,8 +1789,8 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
           __syncwarp();
           for (int e = lane; e < a.batch * 8; e += 32) {  // 8 chunks of 16 B per token
             const int t = e >> 3, ch = e & 7;
-            *reinterpret_cast<uint4*>(a.q_latent + ((int64_t)t * H + h) * kKvLora + 64 * warp +
-                                      8 * ch) =
+            *reinterpret_cast<uint4*>(a.q_latent + (int64_t)t * a.ql_ts + (int64_t)h * a.ql_hs +
+                                      64 * warp + 8 * ch) =
                 *reinterpret_cast<const uint4*>(stage + t * 64 + 8 * ch);
           }
         } else {
@@ -1808,7 +1810,8 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
           uint8_t* ql8 = reinterpret_cast<uint8_t*>(a.q_latent);
           for (int e = lane; e < a.batch * 4; e += 32) {  // 4 chunks of 16 B per token
             const int t = e >> 2, ch = e & 3;
-            *reinterpret_cast<uint4*>(ql8 + ((int64_t)t * H + h) * kKvLora + 64 * warp + 16 * ch) =
+            *reinterpret_cast<uint4*>(ql8 + (int64_t)t * a.ql_ts + (int64_t)h * a.ql_hs + 64 * warp +
+                                      16 * ch) =
                 *reinterpret_cast<const uint4*>(stage + t * 64 + 16 * ch);
           }
         }

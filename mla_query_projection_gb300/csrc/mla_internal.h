@@ -18,6 +18,8 @@ constexpr int kRowE4m3 = 576;  // per-tensor cache row bytes
 constexpr int kRowDs = 656;    // fp8_ds_mla cache row bytes
 constexpr int kDsScales = 512; // byte offset of the four FP32 tile scales
 constexpr int kDsRope = 528;   // byte offset of the BF16 k_pe
+constexpr int kRowElems = 576;   // a gathered query row: 512 latent + 64 rope
+constexpr int kMaxRowHeads = 1024;  // heads per token of a gathered query buffer
 constexpr int kRowNvfp4 = 352;  // nvfp4_ds_mla cache row bytes
 constexpr int kNvScales = 256;  // byte offset of the 32 E4M3 block scales
 constexpr int kNvRope = 288;    // byte offset of the E4M3 k_pe
@@ -50,8 +52,14 @@ struct DecodeArgs {
   int page_size;
   int layout;
   const float* k_scale;      // [1] (per-tensor layout)
-  uint16_t* q_latent;        // [B][H][512]
-  uint16_t* q_pe;            // [B][H][64]
+  uint16_t* q_latent;        // [B][H][512] by default, see ql_ts / ql_hs
+  uint16_t* q_pe;            // [B][H][64] by default, see qp_ts / qp_hs
+  // Output element (t, h, i) of q_latent is q_latent[t * ql_ts + h * ql_hs + i],
+  // of q_pe q_pe[t * qp_ts + h * qp_hs + i], in output elements (BF16, or
+  // bytes for FP8 queries).  Contiguous outputs: H*512, 512, H*64, 64; the
+  // gathered query rows [B][q_heads][576]: q_heads*576, 576 for both, with
+  // q_pe = q_latent + 512.
+  int64_t ql_ts, ql_hs, qp_ts, qp_hs;
   uint16_t* q_c;             // [B][1536] or null
   // scratch (device)
   uint16_t* qn;              // [groups][NT][H][128] BF16 nope values
@@ -119,6 +127,12 @@ size_t wide_qb_bytes(int heads);
 size_t wide_ukt_bytes(int heads);
 cudaError_t pack_wide_weights(const uint16_t* w_qb, const uint16_t* w_uk, uint8_t* qb_tiles,
                               uint8_t* ukt_tiles, int heads, cudaStream_t stream);
+// Bounded poll of a gathered query buffer [batch][q_heads][576] (mla_gather.cu):
+// returns once no element of the first wait_heads rows of every token is the
+// all-ones sentinel, or sets MLA_DEVERR_TIMEOUT in *err after limit_ns.
+cudaError_t launch_rows_wait(const void* rows, int batch, int q_heads, int wait_heads,
+                             int elem_bytes, int64_t limit_ns, uint32_t* err, int num_sms,
+                             cudaStream_t stream);
 cudaError_t launch_wide(const DecodeArgs& a, const WideSplit& sp, int ctas, cudaStream_t stream);
 size_t wide_xq_bytes();
 cudaError_t launch_pair(const DecodeArgs& a, const PairSplit& sp, int ctas, int nt,

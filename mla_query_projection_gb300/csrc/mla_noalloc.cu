@@ -158,6 +158,10 @@ extern "C" MLA_API int mla_query_decode_noalloc(
   a.k_scale = k_scale;
   a.q_latent = static_cast<uint16_t*>(q_latent);
   a.q_pe = static_cast<uint16_t*>(q_pe);
+  a.ql_ts = (int64_t)num_heads * mla::kKvLora;
+  a.ql_hs = mla::kKvLora;
+  a.qp_ts = (int64_t)num_heads * mla::kRope;
+  a.qp_hs = mla::kRope;
   a.q_c = static_cast<uint16_t*>(q_c);
   a.err = device_flags != nullptr ? reinterpret_cast<uint32_t*>(device_flags)
                                   : reinterpret_cast<uint32_t*>(base);

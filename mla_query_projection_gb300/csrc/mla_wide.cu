@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         if (kind == kUnitAbs) {
           if (!mbar_wait_bounded(absready, (uint32_t)(na & 1), kWaitLimit)) timed_out = true;
           tc_fence_after();
-          const int64_t tstep = (int64_t)H * kKvLora;  // one token further in q_latent
+          const int64_t tstep = a.ql_ts;  // one token further in q_latent
           const int nt_here = min(kWideHalfTok, a.batch - my0);
 #pragma unroll 1
           for (int ct = 0; ct < 4; ++ct) {
@@ -369,8 +369,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             tmem_ld16(tmem + lane_base + 128 + kWideHalfTok * ct, *reinterpret_cast<float(*)[16]>(v));
             tmem_ld16(tmem + lane_base + 128 + kWideHalfTok * ct + 16,
                       *reinterpret_cast<float(*)[16]>(v + 16));
-            put_q_run(a, a.q_latent, ((int64_t)my0 * H + h) * kKvLora + 128 * ct + m, tstep, v,
-                      nt_here, qsi);
+            put_q_run(a, a.q_latent, (int64_t)my0 * a.ql_ts + (int64_t)h * a.ql_hs + 128 * ct + m,
+                      tstep, v, nt_here, qsi);
           }
           tc_fence_before();
           mbar_arrive(absfree);
@@ -425,8 +425,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         } else if (2 * h + (m >> 6) < H) {  // rows 0..63: head 2h, 64..127: head 2h + 1
           const int hr = 2 * h + (m >> 6);
           const int nt_here = min(kWideHalfTok, a.batch - my0);
-          put_q_run(a, a.q_pe, ((int64_t)my0 * H + hr) * kRope + (m & 63), (int64_t)H * kRope, q,
-                    nt_here, qsi);
+          put_q_run(a, a.q_pe, (int64_t)my0 * a.qp_ts + (int64_t)hr * a.qp_hs + (m & 63), a.qp_ts,
+                    q, nt_here, qsi);
         }
         ++nq;
         if (m == 0 && u < 16) trace_stamp(a, 28 + u);  // unit u's epilogue done

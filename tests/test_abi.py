@@ -94,3 +94,17 @@ def test_qkv_a_rejects_bad_arguments_on_host(lib):
     assert h.value is None
     assert lib.mla_qkv_a_run(None, 1, 16, 0, 16, 0, None) == B.MLA_EINVAL
     lib.mla_qkv_a_destroy(None)
+
+
+def test_gathered_rows_reject_bad_arguments_on_host(lib):
+    """Host checks of the gathered-row entry points, before any device call."""
+    # null handle / buffer
+    assert B.mla_query_rows_wait(None, 16, 1, 64, 64, 1, 1000, None) == B.MLA_EINVAL
+    assert B.mla_query_rows_arm(None, 1, 64, 1, None) == B.MLA_EINVAL
+    assert B.mla_query_rows_arm(16, 0, 64, 1, None) == B.MLA_EINVAL  # batch
+    assert B.mla_query_rows_arm(16, 1, 0, 1, None) == B.MLA_EINVAL  # q_heads
+    assert B.mla_query_rows_arm(16, 1, B.MLA_MAX_ROW_HEADS + 1, 1, None) == B.MLA_EINVAL
+    assert B.mla_query_rows_arm(16, 1, 64, 4, None) == B.MLA_EINVAL  # element size
+    assert B.mla_query_rows_arm(24, 1, 64, 1, None) == B.MLA_EINVAL  # misaligned
+    assert B.mla_query_decode_rows(None, 1, 16, 0, 16, 0, 16, 0, 16, 16, 1, 64, 0, 16, None, 16,
+                                   64, 0, None, None) == B.MLA_EINVAL
