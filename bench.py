@@ -33,11 +33,25 @@ sys.path.insert(0, ROOT)
 METRIC = "µs per MLA-query decode step and HBM GB/s vs ~8 TB/s peak, B=1..64"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["mla_query_projection_gb300/csrc/mla_common.cuh",
-                  "mla_query_projection_gb300/csrc/mla_device.cuh",
-                  "mla_query_projection_gb300/csrc/mla_fused.cu",
-                  "mla_query_projection_gb300/csrc/mla_wide.cu",
-                  "mla_query_projection_gb300/csrc/mla_qkv_a.cu"]
+_CSRC = "mla_query_projection_gb300/csrc/"
+# The files that define each kernel family: an ncu summary stays valid while
+# they are unchanged.
+KERNEL_SOURCES = {
+    "fused": [_CSRC + f for f in ("mla_common.cuh", "mla_device.cuh", "mla_internal.h",
+                                  "mla_fused.cu")],
+    "wide": [_CSRC + f for f in ("mla_common.cuh", "mla_device.cuh", "mla_internal.h",
+                                 "mla_wide.cu")],
+    "qkv_a": [_CSRC + f for f in ("mla_device.cuh", "mla_qkv_a.cu")],
+}
+
+
+def kernel_sources(kernel: str) -> list[str]:
+    """Source files of the kernel(s) named ("a+b" for a chain of launches)."""
+    out = []
+    for k in kernel.split("+"):
+        fam = "qkv_a" if "qkv_a" in k else "wide" if "wide" in k else "fused"
+        out += [f for f in KERNEL_SOURCES[fam] if f not in out]
+    return out
 
 
 def algorithmic_bytes(batch: int, heads: int, layout: int, hidden: bool = False) -> int:
@@ -61,9 +75,9 @@ def algorithmic_flops(batch: int, heads: int, hidden: bool = False) -> int:
     return f + (2 * batch * QKV_ROW * HIDDEN if hidden else 0)
 
 
-def kernel_hash() -> str:
+def kernel_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
+    for p in kernel_sources(kernel):
         with open(os.path.join(ROOT, p), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -122,7 +136,7 @@ def read_traffic(kernel: str, workload: str) -> float | None:
             if ":" in line and not line.startswith("#"):
                 k, v = line.split(":", 1)
                 vals[k.strip()] = v.strip()
-    if vals.get("kernel_sources_sha256_16") != kernel_hash():
+    if vals.get("kernel_sources_sha256_16") != kernel_hash(kernel):
         return None
     try:
         return float(vals["dram_bytes_per_launch"])
