@@ -16,9 +16,15 @@
 //    byte-balancing share of ROPE units (the 64 rope rows of two heads).
 //  * The weights are copied at create into 16 KiB tiles (128 rows x 64
 //    K-columns, already in the swizzled shared-memory layout), so a producer
-//    warp streams each tile with one 1-D bulk TMA copy into a 5-slot ring;
+//    thread streams each tile with one 16 KiB 1-D bulk TMA copy into a 5-slot
+//    ring (one large copy per tile: the copies one thread issues complete
+//    one after another, so a 16 KiB copy keeps an SM near its share of HBM
+//    bandwidth, and L2 prefetches would queue behind the copies);
 //    one thread issues tcgen05.mma from the ring and the resident xq,
-//    accumulating in TMEM, and commits each slot back to the producer.
+//    accumulating in TMEM, and commits each slot back to the producer.  Its
+//    shared-memory descriptors are precomputed once and advanced by adding
+//    the 16-byte-unit offset of the slot and k step, so an MMA costs about
+//    as much to issue as the tensor core takes to run it.
 //  * The two K-half partial sums of a NOPE or ROPE tile are exchanged through
 //    distributed shared memory (st.async): rank r finishes tokens 32r..32r+31,
 //    adding the half of K 0..767 first.  For NOPE it writes the BF16 q as the
@@ -43,10 +49,9 @@ constexpr int kWideHalfTok = 32;             // tokens each CTA of the pair fini
 constexpr int kWideKHalf = kQLora / 2;       // 768
 constexpr int kWideAtoms = kWideKHalf / 64;  // 12 K atoms of 64 columns (128 B)
 constexpr int kWideSlots = 5;
-constexpr int kWidePrefetch = 12;            // boxes prefetched into L2 beyond the ring
 constexpr int kWideBox = 128 * 128;          // one 128-row x 128 B box (16 KiB)
 constexpr int kWideThreads = 256;
-constexpr int kWideTmemCols = 256;           // D_qb x2 (64 each) + D_abs (4 x 32)
+constexpr int kWideTmemCols = 512;           // D_qb x2 (64 each) + D_abs x2 (4 x 32 each)
 
 enum WideUnit { kUnitNope = 0, kUnitAbs = 1, kUnitRope = 2 };
 
@@ -58,9 +63,9 @@ struct WideSmem {
   static constexpr int oRecv = oQt + 2 * kQtBytes;                  // [2][128][32] FP32
   static constexpr int oSs = oRecv + 2 * 128 * kWideHalfTok * 4;    // own [64], peer [64], red [8]
   static constexpr int oBar = oSs + (2 * kWideTok + 8) * 4;
-  // barriers: full[5] empty[5] dready[2] dfree[2] qready[2] absready absfree
+  // barriers: full[5] empty[5] dready[2] dfree[2] qready[2] absready[2] absfree[2]
   //           recvfull[2] sendok[2] ssbar xqready
-  static constexpr int kBars = 2 * kWideSlots + 2 + 2 + 2 + 2 + 2 + 2 + 1 + 1;
+  static constexpr int kBars = 2 * kWideSlots + 2 + 2 + 2 + 2 + 2 + 2 + 2 + 1 + 1;
   static constexpr int oTslot = oBar + kBars * 8;
   static constexpr int kBytes = oTslot + 16;
   static constexpr int kAlloc = kBytes + 1024;  // base aligned up to 1 KiB (swizzle atoms)
@@ -183,9 +188,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   uint64_t* dready = bars + 2 * kWideSlots;
   uint64_t* dfree = dready + 2;
   uint64_t* qready = dfree + 2;
-  uint64_t* absready = qready + 2;
-  uint64_t* absfree = absready + 1;
-  uint64_t* recvfull = absfree + 1;
+  uint64_t* absready = qready + 2;  // one absorption accumulator per head of the pair
+  uint64_t* absfree = absready + 2;
+  uint64_t* recvfull = absfree + 2;
   uint64_t* sendok = recvfull + 2;
   uint64_t* ssbar = sendok + 2;
   uint64_t* xqready = ssbar + 1;
@@ -213,8 +218,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     }
     mbar_init(&qready[0], 1);
     mbar_init(&qready[1], 1);
-    mbar_init(absready, 1);
-    mbar_init(absfree, 128);
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(&absready[j], 1);
+      mbar_init(&absfree[j], 128);
+    }
     mbar_init(ssbar, 1);
     mbar_init(xqready, 1);
     // the other CTA's bytes: its first two tile halves
@@ -242,34 +249,22 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     // ================= producer: weight tiles, no PDL wait =============
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
-      // L2 prefetch kWidePrefetch boxes beyond the ring: a cursor (pu, pb)
-      // that runs ahead of the box being issued
-      int pu = 0, pb = 0, ahead = 0;
-      auto prefetch_next = [&](bool issue) {
-        while (pu < nu && pb >= seq.boxes(pu)) {
-          ++pu;
-          pb = 0;
-        }
-        if (pu >= nu) return;
-        if (issue) bulk_prefetch_l2(wide_tile(a, seq.kind(pu), seq.head(pu), rank, pb), kWideBox);
-        ++pb;
-      };
-      int k = 0;  // box counter over all units
+      int slot = 0;
+      uint32_t phase = 0;  // parity of the slot's next empty phase to wait for
+      int k = 0;           // box counter over all units
       for (int u = 0; u < nu; ++u) {
         const int kind = seq.kind(u), h = seq.head(u), nb = seq.boxes(u);
         for (int bx = 0; bx < nb; ++bx, ++k) {
-          const int slot = k % kWideSlots;
-          // keep the prefetch cursor kWideSlots + kWidePrefetch boxes ahead
-          while (ahead < k + kWideSlots + kWidePrefetch) {
-            prefetch_next(ahead >= kWideSlots);  // the first ring fill needs none
-            ++ahead;
-          }
-          if (k >= kWideSlots &&
-              !mbar_wait_bounded(&empty[slot], (uint32_t)(((k / kWideSlots) - 1) & 1), kWaitLimit))
+          if (k >= kWideSlots && !mbar_wait_bounded(&empty[slot], phase, kWaitLimit))
             timed_out = true;
-          uint8_t* dst = smem + S::oRing + slot * kWideBox;
           mbar_arrive_expect_tx(&full[slot], kWideBox);
-          bulk_g2s_hint(dst, wide_tile(a, kind, h, rank, bx), kWideBox, &full[slot], pol);
+          bulk_g2s_hint(smem + S::oRing + slot * kWideBox, wide_tile(a, kind, h, rank, bx), kWideBox,
+                        &full[slot], pol);
+          if (bx == 0 && u < 4) trace_stamp(a, 24 + u);  // unit u's first box issued
+          if (++slot == kWideSlots) {
+            slot = 0;
+            if (k >= kWideSlots) phase ^= 1u;
+          }
         }
       }
       // every issued box is consumed before the CTA may leave
@@ -283,19 +278,27 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       if (!mbar_wait_bounded(xqready, 0u, kWaitLimit)) timed_out = true;
       trace_stamp(a, 2);
       tc_fence_after();
-      const uint32_t xq0 = smem_u32(smem + S::oXq), ring0 = smem_u32(smem + S::oRing),
-                     qt0 = smem_u32(smem + S::oQt);
-      int k = 0, nq = 0, na = 0;  // boxes, Q_B tiles, absorptions so far
+      // Descriptors of the ring, the resident xq and the q tiles; an operand
+      // at byte offset o from one of them is its descriptor plus o / 16 (the
+      // start-address field, which no offset here carries out of).
+      const uint64_t dring = umma_desc(smem_u32(smem + S::oRing));
+      const uint64_t dxq = umma_desc(smem_u32(smem + S::oXq));
+      const uint64_t dqt = umma_desc(smem_u32(smem + S::oQt));
+      constexpr uint32_t idq = umma_idesc(128, kWideTok), ida = umma_idesc(128, kWideHalfTok);
+      int nq = 0, na = 0;  // Q_B tiles, absorptions so far
+      int slot = 0;
+      uint32_t fphase = 0;  // parity of the slot's next full phase
       for (int u = 0; u < nu; ++u) {
         const int kind = seq.kind(u), nb = seq.boxes(u);
         uint32_t dcol;
         if (kind == kUnitAbs) {
           // the q tile of this head is written; the previous absorption read out
           if (!mbar_wait_bounded(&qready[na], 0u, kWaitLimit)) timed_out = true;
-          if (na > 0 && !mbar_wait_bounded(absfree, (uint32_t)((na - 1) & 1), kWaitLimit))
+          if (na >= 2 &&
+              !mbar_wait_bounded(&absfree[na & 1], (uint32_t)(((na >> 1) - 1) & 1), kWaitLimit))
             timed_out = true;
           tc_fence_after();
-          dcol = 128;
+          dcol = 128 + 128 * (na & 1);
         } else {
           const int b = nq & 1;
           if (nq >= 2 && !mbar_wait_bounded(&dfree[b], (uint32_t)(((nq >> 1) - 1) & 1), kWaitLimit))
@@ -303,30 +306,36 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           tc_fence_after();
           dcol = 64 * b;
         }
-        for (int bx = 0; bx < nb; ++bx, ++k) {
-          const int slot = k % kWideSlots;
-          if (!mbar_wait_bounded(&full[slot], (uint32_t)((k / kWideSlots) & 1), kWaitLimit))
-            timed_out = true;
+        for (int bx = 0; bx < nb; ++bx) {
+          if (!mbar_wait_bounded(&full[slot], fphase, kWaitLimit)) timed_out = true;
           tc_fence_after();
-          const uint32_t abase = ring0 + slot * kWideBox;
+          const uint64_t da = dring + (uint64_t)(slot * (kWideBox >> 4));
           if (kind == kUnitAbs) {
+            // W_UK^T rows 128 ct.., q^T atom pa (nope rows 64 pa..64 pa + 63)
             const int ct = bx >> 1, pa = bx & 1;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma(tmem + dcol + kWideHalfTok * ct, umma_desc(abase + 32 * kk),
-                   umma_desc(qt0 + na * S::kQtBytes + pa * (kWideHalfTok * 128) + 32 * kk),
-                   umma_idesc(128, kWideHalfTok), (pa | kk) != 0);
+            const uint64_t db =
+                dqt + (uint64_t)(na * (S::kQtBytes >> 4) + pa * ((kWideHalfTok * 128) >> 4));
+            const uint32_t dt = tmem + dcol + kWideHalfTok * ct;
+            umma(dt, da, db, ida, (uint32_t)pa);
+            umma(dt, da + 2, db + 2, ida, 1u);
+            umma(dt, da + 4, db + 4, ida, 1u);
+            umma(dt, da + 6, db + 6, ida, 1u);
           } else {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma(tmem + dcol, umma_desc(abase + 32 * kk),
-                   umma_desc(xq0 + bx * (kWideTok * 128) + 32 * kk), umma_idesc(128, kWideTok),
-                   (bx | kk) != 0);
+            const uint64_t db = dxq + (uint64_t)(bx * ((kWideTok * 128) >> 4));
+            const uint32_t dt = tmem + dcol;
+            umma(dt, da, db, idq, (uint32_t)bx);
+            umma(dt, da + 2, db + 2, idq, 1u);
+            umma(dt, da + 4, db + 4, idq, 1u);
+            umma(dt, da + 6, db + 6, idq, 1u);
           }
           umma_commit(&empty[slot]);  // the slot is free once these MMAs are done
+          if (++slot == kWideSlots) {
+            slot = 0;
+            fphase ^= 1u;
+          }
         }
         if (kind == kUnitAbs) {
-          umma_commit(absready);
+          umma_commit(&absready[na & 1]);
           ++na;
         } else {
           umma_commit(&dready[nq & 1]);
@@ -340,13 +349,18 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     // The normalising kernel launched just before wrote xq in this tile's
     // layout; twelve bulk copies (one per 64-column atom) bring this half in.
     pdl_wait();
-    if (tid == 64) {
-      trace_stamp(a, 3);
-      mbar_arrive_expect_tx(xqready, kWideAtoms * kWideTok * 128);
-      const uint8_t* src = a.wide_xq + (size_t)rank * kWideAtoms * kWideTok * 128;
-      for (int at = 0; at < kWideAtoms; ++at)
-        bulk_g2s(smem + S::oXq + at * (kWideTok * 128), src + at * (kWideTok * 128),
-                 kWideTok * 128, xqready);
+    if (warp == 2) {
+      // one 8 KiB atom per lane: copies issued by different threads proceed
+      // side by side
+      if (lane == 0) {
+        trace_stamp(a, 3);
+        mbar_arrive_expect_tx(xqready, kWideAtoms * kWideTok * 128);
+      }
+      __syncwarp();
+      if (lane < kWideAtoms) {
+        const uint8_t* src = a.wide_xq + ((size_t)rank * kWideAtoms + lane) * (kWideTok * 128);
+        bulk_g2s(smem + S::oXq + lane * (kWideTok * 128), src, kWideTok * 128, xqready);
+      }
     }
 
     if (warp >= 4) {
@@ -359,21 +373,24 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       for (int u = 0; u < nu; ++u) {
         const int kind = seq.kind(u), h = seq.head(u);
         if (kind == kUnitAbs) {
-          if (!mbar_wait_bounded(absready, (uint32_t)(na & 1), kWaitLimit)) timed_out = true;
+          const int ab = na & 1;
+          if (!mbar_wait_bounded(&absready[ab], (uint32_t)((na >> 1) & 1), kWaitLimit))
+            timed_out = true;
           tc_fence_after();
           const int64_t tstep = a.ql_ts;  // one token further in q_latent
           const int nt_here = min(kWideHalfTok, a.batch - my0);
 #pragma unroll 1
           for (int ct = 0; ct < 4; ++ct) {
             float v[32];
-            tmem_ld16(tmem + lane_base + 128 + kWideHalfTok * ct, *reinterpret_cast<float(*)[16]>(v));
-            tmem_ld16(tmem + lane_base + 128 + kWideHalfTok * ct + 16,
+            tmem_ld16(tmem + lane_base + 128 + 128 * ab + kWideHalfTok * ct,
+                      *reinterpret_cast<float(*)[16]>(v));
+            tmem_ld16(tmem + lane_base + 128 + 128 * ab + kWideHalfTok * ct + 16,
                       *reinterpret_cast<float(*)[16]>(v + 16));
             put_q_run(a, a.q_latent, (int64_t)my0 * a.ql_ts + (int64_t)h * a.ql_hs + 128 * ct + m,
                       tstep, v, nt_here, qsi);
           }
           tc_fence_before();
-          mbar_arrive(absfree);
+          mbar_arrive(&absfree[ab]);
           ++na;
           if (m == 0 && u < 16) trace_stamp(a, 28 + u);  // unit u's epilogue done
           continue;
