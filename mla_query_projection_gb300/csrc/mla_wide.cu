@@ -27,10 +27,13 @@
 //    as much to issue as the tensor core takes to run it.
 //  * The two K-half partial sums of a NOPE or ROPE tile are exchanged through
 //    distributed shared memory (st.async): rank r finishes tokens 32r..32r+31,
-//    adding the half of K 0..767 first.  For NOPE it writes the BF16 q as the
-//    B operand of the absorption (tokens x 128 rows, swizzled), which a second
-//    GEMM multiplies by W_UK^T (a copy made at create, [h][c][p]) into TMEM;
-//    the epilogue writes q_latent.
+//    adding the half of K 0..767 first.  For NOPE it writes the BF16 q of its
+//    32 tokens into the B operand of the absorption (64 tokens x 128 rows,
+//    swizzled) and copies those rows into the other CTA's, so both hold the
+//    q of all 64 tokens; each CTA then multiplies its half of W_UK^T (a copy
+//    made at create, [h][c][p]: latent columns 256 r..256 r + 255) by it into
+//    TMEM, and the epilogue writes those columns of q_latent.  Every W_UK
+//    byte is streamed once.
 // Every wait is bounded (MLA_DEVERR_TIMEOUT instead of a hang).
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -58,14 +61,14 @@ enum WideUnit { kUnitNope = 0, kUnitAbs = 1, kUnitRope = 2 };
 struct WideSmem {
   static constexpr int oXq = 0;                                  // [12][64 rows][128 B]
   static constexpr int oRing = oXq + kWideAtoms * kWideTok * 128;   // 98304
-  static constexpr int kQtBytes = 2 * kWideHalfTok * 128;          // one head: 2 atoms
-  static constexpr int oQt = oRing + kWideSlots * kWideBox;         // [2 heads][2][32 rows][128 B]
-  static constexpr int oRecv = oQt + 2 * kQtBytes;                  // [2][128][32] FP32
-  static constexpr int oSs = oRecv + 2 * 128 * kWideHalfTok * 4;    // own [64], peer [64], red [8]
-  static constexpr int oBar = oSs + (2 * kWideTok + 8) * 4;
+  static constexpr int kQtAtom = kWideTok * 128;                   // 64 token rows of 128 B
+  static constexpr int kQtBytes = 2 * kQtAtom;                      // one head: 2 atoms
+  static constexpr int oQt = oRing + kWideSlots * kWideBox;         // [2 heads][2][64 rows][128 B]
+  static constexpr int oRecv = oQt + 2 * kQtBytes;                  // [128][32] FP32
+  static constexpr int oBar = oRecv + 128 * kWideHalfTok * 4;
   // barriers: full[5] empty[5] dready[2] dfree[2] qready[2] absready[2] absfree[2]
-  //           recvfull[2] sendok[2] ssbar xqready
-  static constexpr int kBars = 2 * kWideSlots + 2 + 2 + 2 + 2 + 2 + 2 + 2 + 1 + 1;
+  //           recvfull sendok xqready
+  static constexpr int kBars = 2 * kWideSlots + 2 + 2 + 2 + 2 + 2 + 1 + 1 + 1;
   static constexpr int oTslot = oBar + kBars * 8;
   static constexpr int kBytes = oTslot + 16;
   static constexpr int kAlloc = kBytes + 1024;  // base aligned up to 1 KiB (swizzle atoms)
@@ -160,12 +163,13 @@ struct WideSeq {
     if (u < 2 * nh + ins()) return h0 + (u - nh - ins());
     return r0 + (u - 2 * nh);
   }
-  __device__ int boxes(int u) const { return kind(u) == kUnitAbs ? 8 : kWideAtoms; }
+  __device__ int boxes(int u) const { return kind(u) == kUnitAbs ? 4 : kWideAtoms; }
 };
 
 // Tile addresses in the packed copies (pack_wide_weights): NOPE tile
 // (h, K half, atom), ROPE tile (rope unit, K half, atom), W_UK^T tile
-// (h, 128-column tile ct, 64-row atom pa).
+// (h, 128-column tile ct, 64-row atom pa); the CTA of rank `half` takes the
+// W_UK^T tiles of latent columns 256 half.. (ct = 2 half + bx / 2, pa = bx % 2).
 __device__ __forceinline__ const uint8_t* wide_tile(const DecodeArgs& a, int kind, int h,
                                                     int half, int bx) {
   if (kind == kUnitNope)
@@ -173,7 +177,7 @@ __device__ __forceinline__ const uint8_t* wide_tile(const DecodeArgs& a, int kin
   if (kind == kUnitRope)
     return a.wide_qb + ((size_t)a.heads * 2 * kWideAtoms + (size_t)(h * 2 + half) * kWideAtoms + bx) *
                            kWideBox;
-  return a.wide_ukt + ((size_t)h * 8 + bx) * kWideBox;  // bx = 2 ct + pa
+  return a.wide_ukt + ((size_t)h * 8 + 4 * half + bx) * kWideBox;  // 2 ct + pa
 }
 
 __global__ void __launch_bounds__(kWideThreads, 1)
@@ -190,10 +194,9 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   uint64_t* qready = dfree + 2;
   uint64_t* absready = qready + 2;  // one absorption accumulator per head of the pair
   uint64_t* absfree = absready + 2;
-  uint64_t* recvfull = absfree + 2;
-  uint64_t* sendok = recvfull + 2;
-  uint64_t* ssbar = sendok + 2;
-  uint64_t* xqready = ssbar + 1;
+  uint64_t* recvfull = absfree + 2;  // the other CTA's partials landed (one buffer)
+  uint64_t* sendok = recvfull + 1;    // the other CTA has read what this one sent
+  uint64_t* xqready = sendok + 1;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + S::oTslot);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -213,20 +216,20 @@ __global__ void __launch_bounds__(kWideThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(&dready[b], 1);
       mbar_init(&dfree[b], 128);
-      mbar_init(&recvfull[b], 1);
-      mbar_init(&sendok[b], 1);
+      // q tile of head b: this CTA's rows (one arrival) and the other CTA's
+      // (its bulk copies, counted in bytes; armed here)
+      mbar_init(&qready[b], 2);
+      mbar_arrive_expect_tx(&qready[b], S::kQtBytes / 2);
     }
-    mbar_init(&qready[0], 1);
-    mbar_init(&qready[1], 1);
+    mbar_init(recvfull, 1);
+    mbar_init(sendok, 1);
     for (int j = 0; j < 2; ++j) {
       mbar_init(&absready[j], 1);
       mbar_init(&absfree[j], 128);
     }
-    mbar_init(ssbar, 1);
     mbar_init(xqready, 1);
-    // the other CTA's bytes: its first two tile halves
-    mbar_arrive_expect_tx(&recvfull[0], 128 * kWideHalfTok * 4);
-    mbar_arrive_expect_tx(&recvfull[1], 128 * kWideHalfTok * 4);
+    // the other CTA's bytes: its first tile half
+    mbar_arrive_expect_tx(recvfull, 128 * kWideHalfTok * 4);
     mbar_fence_init();
     pdl_launch_dependents();
   }
@@ -284,7 +287,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       const uint64_t dring = umma_desc(smem_u32(smem + S::oRing));
       const uint64_t dxq = umma_desc(smem_u32(smem + S::oXq));
       const uint64_t dqt = umma_desc(smem_u32(smem + S::oQt));
-      constexpr uint32_t idq = umma_idesc(128, kWideTok), ida = umma_idesc(128, kWideHalfTok);
+      constexpr uint32_t idq = umma_idesc(128, kWideTok);
       int nq = 0, na = 0;  // Q_B tiles, absorptions so far
       int slot = 0;
       uint32_t fphase = 0;  // parity of the slot's next full phase
@@ -311,15 +314,15 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           tc_fence_after();
           const uint64_t da = dring + (uint64_t)(slot * (kWideBox >> 4));
           if (kind == kUnitAbs) {
-            // W_UK^T rows 128 ct.., q^T atom pa (nope rows 64 pa..64 pa + 63)
+            // W_UK^T rows 128 ct.. of this CTA's half, q^T atom pa (nope rows
+            // 64 pa..64 pa + 63) of all 64 tokens
             const int ct = bx >> 1, pa = bx & 1;
-            const uint64_t db =
-                dqt + (uint64_t)(na * (S::kQtBytes >> 4) + pa * ((kWideHalfTok * 128) >> 4));
-            const uint32_t dt = tmem + dcol + kWideHalfTok * ct;
-            umma(dt, da, db, ida, (uint32_t)pa);
-            umma(dt, da + 2, db + 2, ida, 1u);
-            umma(dt, da + 4, db + 4, ida, 1u);
-            umma(dt, da + 6, db + 6, ida, 1u);
+            const uint64_t db = dqt + (uint64_t)(na * (S::kQtBytes >> 4) + pa * (S::kQtAtom >> 4));
+            const uint32_t dt = tmem + dcol + kWideTok * ct;
+            umma(dt, da, db, idq, (uint32_t)pa);
+            umma(dt, da + 2, db + 2, idq, 1u);
+            umma(dt, da + 4, db + 4, idq, 1u);
+            umma(dt, da + 6, db + 6, idq, 1u);
           } else {
             const uint64_t db = dxq + (uint64_t)(bx * ((kWideTok * 128) >> 4));
             const uint32_t dt = tmem + dcol;
@@ -377,17 +380,20 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           if (!mbar_wait_bounded(&absready[ab], (uint32_t)((na >> 1) & 1), kWaitLimit))
             timed_out = true;
           tc_fence_after();
-          const int64_t tstep = a.ql_ts;  // one token further in q_latent
-          const int nt_here = min(kWideHalfTok, a.batch - my0);
+          // latent column 256 rank + 128 ct + m of all 64 tokens, 32 at a time
 #pragma unroll 1
-          for (int ct = 0; ct < 4; ++ct) {
+          for (int part = 0; part < 4; ++part) {
+            const int ct = part >> 1, t0 = kWideHalfTok * (part & 1);
             float v[32];
-            tmem_ld16(tmem + lane_base + 128 + 128 * ab + kWideHalfTok * ct,
+            tmem_ld16(tmem + lane_base + 128 + 128 * ab + kWideTok * ct + t0,
                       *reinterpret_cast<float(*)[16]>(v));
-            tmem_ld16(tmem + lane_base + 128 + 128 * ab + kWideHalfTok * ct + 16,
+            tmem_ld16(tmem + lane_base + 128 + 128 * ab + kWideTok * ct + t0 + 16,
                       *reinterpret_cast<float(*)[16]>(v + 16));
-            put_q_run(a, a.q_latent, (int64_t)my0 * a.ql_ts + (int64_t)h * a.ql_hs + 128 * ct + m,
-                      tstep, v, nt_here, qsi);
+            const int nt_here = min(kWideHalfTok, a.batch - t0);
+            if (nt_here > 0)
+              put_q_run(a, a.q_latent,
+                        (int64_t)t0 * a.ql_ts + (int64_t)h * a.ql_hs + 256 * rank + 128 * ct + m,
+                        a.ql_ts, v, nt_here, qsi);
           }
           tc_fence_before();
           mbar_arrive(&absfree[ab]);
@@ -403,11 +409,12 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         // the other CTA's tokens of this row go into its receive buffer b
         tmem_ld16(tmem + lane_base + 64 * b + peer0, *reinterpret_cast<float(*)[16]>(q));
         tmem_ld16(tmem + lane_base + 64 * b + peer0 + 16, *reinterpret_cast<float(*)[16]>(q + 16));
-        if (nq >= 2 && !mbar_wait_bounded(&sendok[b], (uint32_t)(((nq >> 1) - 1) & 1), kWaitLimit))
+        // the other CTA has read what this one sent for the previous tile
+        if (nq >= 1 && !mbar_wait_bounded(sendok, (uint32_t)((nq - 1) & 1), kWaitLimit))
           timed_out = true;
         {
-          const uint32_t rb = mapa_shared(smem_u32(&recvfull[b]), peer);
-          const uint32_t dst = smem_u32(smem + S::oRecv + (b * 128 + m) * kWideHalfTok * 4);
+          const uint32_t rb = mapa_shared(smem_u32(recvfull), peer);
+          const uint32_t dst = smem_u32(smem + S::oRecv + m * kWideHalfTok * 4);
 #pragma unroll
           for (int j = 0; j < kWideHalfTok; j += 4)
             st_async_v4(mapa_shared(dst + 4 * j, peer), q[j], q[j + 1], q[j + 2], q[j + 3], rb);
@@ -417,28 +424,36 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         tmem_ld16(tmem + lane_base + 64 * b + my0 + 16, *reinterpret_cast<float(*)[16]>(q + 16));
         tc_fence_before();
         mbar_arrive(&dfree[b]);
-        if (!mbar_wait_bounded(&recvfull[b], (uint32_t)((nq >> 1) & 1), kWaitLimit)) timed_out = true;
-        const float* rcv =
-            reinterpret_cast<const float*>(smem + S::oRecv + (b * 128 + m) * kWideHalfTok * 4);
+        if (!mbar_wait_bounded(recvfull, (uint32_t)(nq & 1), kWaitLimit)) timed_out = true;
+        const float* rcv = reinterpret_cast<const float*>(smem + S::oRecv + m * kWideHalfTok * 4);
 #pragma unroll
         for (int j = 0; j < kWideHalfTok; ++j) q[j] = rank == 0 ? q[j] + rcv[j] : rcv[j] + q[j];
-        // buffer b is read: re-arm it for its next use, then let the other CTA send
+        // the buffer is read: re-arm it for its next use, then let the other CTA send
         named_barrier(5, 128);
         if (m == 0) {
-          mbar_arrive_expect_tx(&recvfull[b], 128 * kWideHalfTok * 4);
-          mbar_arrive_remote(mapa_shared(smem_u32(&sendok[b]), peer));
+          mbar_arrive_expect_tx(recvfull, 128 * kWideHalfTok * 4);
+          mbar_arrive_remote(mapa_shared(smem_u32(sendok), peer));
         }
         if (kind == kUnitNope) {
-          // q^T tile of head j of the pair: [token 0..31][row m] BF16,
-          // K-major swizzled, two atoms (each head has its own tile)
+          // q^T tile of head j of the pair: [token 0..63][row m] BF16,
+          // K-major swizzled, two atoms (each head has its own tile); this
+          // CTA writes its 32 token rows and copies them into the other CTA's
           const int j = h - seq.h0;
-          uint8_t* qt = smem + S::oQt + j * S::kQtBytes + (m >> 6) * (kWideHalfTok * 128);
+          uint8_t* qt = smem + S::oQt + j * S::kQtBytes;
+          uint8_t* qa = qt + (m >> 6) * S::kQtAtom;
 #pragma unroll
           for (int tl = 0; tl < kWideHalfTok; ++tl)
-            *reinterpret_cast<uint16_t*>(qt + sw128(tl, m & 63)) = f2bf_bits(q[tl]);
+            *reinterpret_cast<uint16_t*>(qa + sw128(my0 + tl, m & 63)) = f2bf_bits(q[tl]);
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           named_barrier(5, 128);
-          if (m == 0) mbar_arrive(&qready[j]);
+          if (m == 0) {
+            const uint32_t rq = mapa_shared(smem_u32(&qready[j]), peer);
+            for (int at = 0; at < 2; ++at) {
+              uint8_t* rows = qt + at * S::kQtAtom + my0 * 128;  // 32 rows of 128 B
+              bulk_s2s_cluster(mapa_shared(smem_u32(rows), peer), rows, kWideHalfTok * 128, rq);
+            }
+            mbar_arrive(&qready[j]);
+          }
         } else if (2 * h + (m >> 6) < H) {  // rows 0..63: head 2h, 64..127: head 2h + 1
           const int hr = 2 * h + (m >> 6);
           const int nt_here = min(kWideHalfTok, a.batch - my0);
@@ -609,10 +624,10 @@ bool make_wide_split(int heads, int ctas, WideSplit* sp) {
   for (int c = 0; c < pairs; ++c)
     if (sp->head[c + 1] - sp->head[c] > 2) return false;
   // ROPE units (two heads' rope rows, 192 KiB per CTA each) fill every pair
-  // up to an even share of the bytes; a head's NOPE + ABS units are 320 KiB
-  // per CTA.
+  // up to an even share of the bytes; a head's NOPE + ABS units are 256 KiB
+  // per CTA (its nope rows' K half and its half of W_UK^T).
   const int ropes = (heads + 1) / 2;
-  const int64_t hb = 20, rb = 12;  // in units of 16 KiB
+  const int64_t hb = 16, rb = 12;  // in units of 16 KiB
   const int64_t total = (int64_t)heads * hb + (int64_t)ropes * rb;
   int64_t head_bytes = 0;
   int prev = 0;
