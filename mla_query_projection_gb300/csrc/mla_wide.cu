@@ -414,10 +414,14 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           timed_out = true;
         {
           const uint32_t rb = mapa_shared(smem_u32(recvfull), peer);
+          // row m of the other CTA's receive buffer; 16-byte chunk c (tokens
+          // 4c..4c+3) at position c ^ (m % 8), so that reading a row chunk by
+          // chunk is free of bank conflicts
           const uint32_t dst = smem_u32(smem + S::oRecv + m * kWideHalfTok * 4);
 #pragma unroll
-          for (int j = 0; j < kWideHalfTok; j += 4)
-            st_async_v4(mapa_shared(dst + 4 * j, peer), q[j], q[j + 1], q[j + 2], q[j + 3], rb);
+          for (int c = 0; c < kWideHalfTok / 4; ++c)
+            st_async_v4(mapa_shared(dst + 16 * (c ^ (m & 7)), peer), q[4 * c], q[4 * c + 1],
+                        q[4 * c + 2], q[4 * c + 3], rb);
         }
         // this CTA's tokens: its K half plus the other CTA's, K 0..767 first
         tmem_ld16(tmem + lane_base + 64 * b + my0, *reinterpret_cast<float(*)[16]>(q));
@@ -425,9 +429,15 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         tc_fence_before();
         mbar_arrive(&dfree[b]);
         if (!mbar_wait_bounded(recvfull, (uint32_t)(nq & 1), kWaitLimit)) timed_out = true;
-        const float* rcv = reinterpret_cast<const float*>(smem + S::oRecv + m * kWideHalfTok * 4);
+        const float4* rcv = reinterpret_cast<const float4*>(smem + S::oRecv + m * kWideHalfTok * 4);
 #pragma unroll
-        for (int j = 0; j < kWideHalfTok; ++j) q[j] = rank == 0 ? q[j] + rcv[j] : rcv[j] + q[j];
+        for (int c = 0; c < kWideHalfTok / 4; ++c) {
+          const float4 r = rcv[c ^ (m & 7)];
+          const float rv[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            q[4 * c + e] = rank == 0 ? q[4 * c + e] + rv[e] : rv[e] + q[4 * c + e];
+        }
         // the buffer is read: re-arm it for its next use, then let the other CTA send
         named_barrier(5, 128);
         if (m == 0) {
