@@ -142,26 +142,23 @@ __device__ __forceinline__ int sw128(int row, int col) {
 }
 
 // Units of pair c, heads [h0, h0 + nh) (nh <= 2) and rope units [r0, r0 + nr):
-// NOPE of every head, then ABS of every head, then the ROPE units - except
-// that a one-head pair puts one ROPE unit between its NOPE and its ABS.  Each
-// ABS thus follows an independent Q_B tile that keeps the tensor cores busy
-// while the epilogue exchanges and rounds the head's q.
+// NOPE of every head, then the ROPE units, then ABS of every head.  The Q_B
+// tiles in between give the epilogue time to finish each head's q before its
+// absorption needs it, and the step ends on absorptions, whose epilogue needs
+// nothing from the other CTA.
 struct WideSeq {
   int h0, nh, r0, nr;
-  __device__ int ins() const { return (nh == 1 && nr > 0) ? 1 : 0; }
   __device__ int units() const { return 2 * nh + nr; }
   __device__ int kind(int u) const {
     if (u < nh) return kUnitNope;
-    if (u < nh + ins()) return kUnitRope;
-    if (u < 2 * nh + ins()) return kUnitAbs;
-    return kUnitRope;
+    if (u < nh + nr) return kUnitRope;
+    return kUnitAbs;
   }
   // head of a NOPE/ABS unit, or rope unit (heads 2 r, 2 r + 1) of a ROPE unit
   __device__ int head(int u) const {
     if (u < nh) return h0 + u;
-    if (u < nh + ins()) return r0;
-    if (u < 2 * nh + ins()) return h0 + (u - nh - ins());
-    return r0 + (u - 2 * nh);
+    if (u < nh + nr) return r0 + (u - nh);
+    return h0 + (u - nh - nr);
   }
   __device__ int boxes(int u) const { return kind(u) == kUnitAbs ? 4 : kWideAtoms; }
 };
