@@ -114,19 +114,21 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// 32 lanes x 16 columns of FP32 from TMEM (lane base and column in `taddr`).
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
+// 32 lanes x 32 columns of FP32 from TMEM in one load and one wait.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-      "%15}, [%16];"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
 
 // Arrive on the mbarrier at `remote` (a shared::cluster address in the other
@@ -382,10 +384,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           for (int part = 0; part < 4; ++part) {
             const int ct = part >> 1, t0 = kWideHalfTok * (part & 1);
             float v[32];
-            tmem_ld16(tmem + lane_base + 128 + 128 * ab + kWideTok * ct + t0,
-                      *reinterpret_cast<float(*)[16]>(v));
-            tmem_ld16(tmem + lane_base + 128 + 128 * ab + kWideTok * ct + t0 + 16,
-                      *reinterpret_cast<float(*)[16]>(v + 16));
+            tmem_ld32(tmem + lane_base + 128 + 128 * ab + kWideTok * ct + t0, v);
             const int nt_here = min(kWideHalfTok, a.batch - t0);
             if (nt_here > 0)
               put_q_run(a, a.q_latent,
@@ -404,8 +403,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         tc_fence_after();
         float q[kWideHalfTok];
         // the other CTA's tokens of this row go into its receive buffer b
-        tmem_ld16(tmem + lane_base + 64 * b + peer0, *reinterpret_cast<float(*)[16]>(q));
-        tmem_ld16(tmem + lane_base + 64 * b + peer0 + 16, *reinterpret_cast<float(*)[16]>(q + 16));
+        tmem_ld32(tmem + lane_base + 64 * b + peer0, q);
         // the other CTA has read what this one sent for the previous tile
         if (nq >= 1 && !mbar_wait_bounded(sendok, (uint32_t)((nq - 1) & 1), kWaitLimit))
           timed_out = true;
@@ -421,8 +419,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                         q[4 * c + 2], q[4 * c + 3], rb);
         }
         // this CTA's tokens: its K half plus the other CTA's, K 0..767 first
-        tmem_ld16(tmem + lane_base + 64 * b + my0, *reinterpret_cast<float(*)[16]>(q));
-        tmem_ld16(tmem + lane_base + 64 * b + my0 + 16, *reinterpret_cast<float(*)[16]>(q + 16));
+        tmem_ld32(tmem + lane_base + 64 * b + my0, q);
         tc_fence_before();
         mbar_arrive(&dfree[b]);
         if (!mbar_wait_bounded(recvfull, (uint32_t)(nq & 1), kWaitLimit)) timed_out = true;
