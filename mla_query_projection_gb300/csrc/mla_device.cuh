@@ -74,19 +74,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
-// 1-D bulk copy from this CTA's shared memory to the shared memory of a CTA
-// of the cluster (dst and the mbarrier given as shared::cluster addresses),
-// completion counted on that mbarrier in bytes.  16-byte aligned, bytes a
-// multiple of 16.
-__device__ __forceinline__ void bulk_s2s_cluster(uint32_t dst, const void* src, uint32_t bytes,
-                                                 uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "r"(smem_u32(src)), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
 // L2 eviction policy under which the lines an access touches are the first
 // candidates for eviction (weights that are dead once copied to shared memory).
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {

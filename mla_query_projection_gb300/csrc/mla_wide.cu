@@ -131,6 +131,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// 1-D bulk copy from this CTA's shared memory to the shared memory of a CTA
+// of the cluster (dst and the mbarrier given as shared::cluster addresses),
+// completion counted on that mbarrier in bytes.  16-byte aligned, bytes a
+// multiple of 16.
+__device__ __forceinline__ void bulk_s2s_cluster(uint32_t dst, const void* src, uint32_t bytes,
+                                                 uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "r"(smem_u32(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // Arrive on the mbarrier at `remote` (a shared::cluster address in the other
 // CTA of the pair).
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t remote) {
