@@ -386,52 +386,93 @@ def gpu_arm(args, rank: int, world: int, local_rank: int) -> dict | None:
     if flags:
         raise RuntimeError(f"device error flags {flags} during the timed run")
 
-    # e2e: host (pinned) inputs -> device, decode, outputs -> host, every step.
-    # One staging buffer each way, as a serving loop would keep them: the
-    # inputs as fused q_a|kv_c|k_pe rows (stride 2112) followed by the slots,
-    # the outputs as q_latent|q_pe|q_c back to back.
+    # e2e: every step copies its inputs from pinned host memory to the device,
+    # runs the decode through the C ABI and copies its outputs back to pinned
+    # host memory, as a serving loop would: two staging buffers each way and
+    # three streams (copy in, compute, copy out) ordered by events, so that
+    # step j+1's upload and step j-1's download overlap step j's decode.  The
+    # inputs are the fused q_a|kv_c|k_pe rows (stride 2112; the hidden rows for
+    # the step from the hidden row) followed by the slots, the outputs
+    # q_latent|q_pe|q_c back to back.  Steps are captured in CUDA graphs of up
+    # to 50 steps, like the device-only run.
     K_e = max(1, min(args.steps, args.e2e_steps))
     row = HIDDEN if hidden else QKV_ROW  # the step's input row: hidden, or q_a|kv_c|k_pe
     in_rows = Bn * row * 2
     in_bytes = in_rows + Bn * 8
-    h_in = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
     if hidden:
         fused = x_hidden.cpu().contiguous()
     else:
         fused = torch.cat([q_a.cpu(), kv_c.cpu(), k_pe.cpu()], dim=1).contiguous()
-    h_in[:in_rows].copy_(fused.view(torch.uint8).reshape(-1))
-    h_in[in_rows:].copy_(slots.cpu().view(torch.uint8).reshape(-1))
-    d_in = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
-    d_rows = d_in[:in_rows].view(torch.bfloat16).view(Bn, row)
-    d_sl = d_in[in_rows:].view(torch.int64)
-    if hidden:
-        e_row = torch.empty(Bn, QKV_ROW, dtype=torch.bfloat16, device=dev)
     o_sizes = [Bn * H * 512 * 2, Bn * H * 64 * 2, Bn * 1536 * 2]
-    d_out = torch.empty(sum(o_sizes), dtype=torch.uint8, device=dev)
-    e_ql = d_out[:o_sizes[0]].view(torch.bfloat16)
-    e_qp = d_out[o_sizes[0]:o_sizes[0] + o_sizes[1]].view(torch.bfloat16)
-    e_qc = d_out[o_sizes[0] + o_sizes[1]:].view(torch.bfloat16)
-    h_out = torch.empty(sum(o_sizes), dtype=torch.uint8).pin_memory()
+    NBUF = 2
+    bufs = []
+    for _ in range(NBUF):
+        h_in = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+        h_in[:in_rows].copy_(fused.view(torch.uint8).reshape(-1))
+        h_in[in_rows:].copy_(slots.cpu().view(torch.uint8).reshape(-1))
+        d_in = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
+        d_out = torch.empty(sum(o_sizes), dtype=torch.uint8, device=dev)
+        bufs.append(dict(
+            h_in=h_in, d_in=d_in, d_out=d_out,
+            rows=d_in[:in_rows].view(torch.bfloat16).view(Bn, row),
+            sl=d_in[in_rows:].view(torch.int64),
+            ql=d_out[:o_sizes[0]].view(torch.bfloat16),
+            qp=d_out[o_sizes[0]:o_sizes[0] + o_sizes[1]].view(torch.bfloat16),
+            qc=d_out[o_sizes[0] + o_sizes[1]:].view(torch.bfloat16),
+            h_out=torch.empty(sum(o_sizes), dtype=torch.uint8).pin_memory(),
+            row=torch.empty(Bn, QKV_ROW, dtype=torch.bfloat16, device=dev) if hidden else None,
+            ev_in=torch.cuda.Event(), ev_done=torch.cuda.Event(), ev_out=torch.cuda.Event(),
+        ))
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
-    def e2e_step(j):
-        d_in.copy_(h_in, non_blocking=True)
-        r_in = d_rows
+    def e2e_step(j, first):
+        bf = bufs[j % NBUF]
+        if not first:
+            s_in.wait_event(bf["ev_done"])  # the decode that read this buffer is done
+        with torch.cuda.stream(s_in):
+            bf["d_in"].copy_(bf["h_in"], non_blocking=True)
+            bf["ev_in"].record(s_in)
+        stream.wait_event(bf["ev_in"])
+        if not first:
+            stream.wait_event(bf["ev_out"])  # this buffer's last outputs are downloaded
+        r_in = bf["rows"]
         if hidden:
-            rc = B.mla_qkv_a_run(sets[j % nsets]["qkv_a"], Bn, d_rows, HIDDEN, e_row, QKV_ROW,
-                                 stream)
+            rc = B.mla_qkv_a_run(sets[j % nsets]["qkv_a"], Bn, bf["rows"], HIDDEN, bf["row"],
+                                 QKV_ROW, stream)
             if rc != B.MLA_OK:
                 raise RuntimeError(f"mla_qkv_a_run: {B.strerror(rc)}")
-            r_in = e_row
+            r_in = bf["row"]
         rc = B.mla_query_decode(sets[j % nsets]["handle"], Bn, r_in, QKV_ROW, r_in[:, 1536:],
-                                QKV_ROW, r_in[:, 2048:], QKV_ROW, d_sl, cache, pages, psize,
-                                layout, k_scale, e_ql, e_qp, e_qc, stream)
+                                QKV_ROW, r_in[:, 2048:], QKV_ROW, bf["sl"], cache, pages, psize,
+                                layout, k_scale, bf["ql"], bf["qp"], bf["qc"], stream)
         if rc != B.MLA_OK:
             raise RuntimeError(f"mla_query_decode: {B.strerror(rc)}")
-        h_out.copy_(d_out, non_blocking=True)
+        bf["ev_done"].record(stream)
+        s_out.wait_event(bf["ev_done"])
+        with torch.cuda.stream(s_out):
+            bf["h_out"].copy_(bf["d_out"], non_blocking=True)
+            bf["ev_out"].record(s_out)
 
+    def capture_e2e(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            for j in range(2 * NBUF):  # eager warm-up of every stream and buffer
+                e2e_step(j, j < NBUF)
+            torch.cuda.synchronize(dev)
+            with torch.cuda.graph(g, stream=stream):
+                s_in.wait_stream(stream)
+                s_out.wait_stream(stream)
+                for j in range(n):
+                    e2e_step(j, j < NBUF)
+                stream.wait_stream(s_in)
+                stream.wait_stream(s_out)
+        return g
+
+    G_e = min(K_e, 50)
+    ge_full = capture_e2e(G_e)
+    ge_rem = capture_e2e(K_e % G_e) if K_e % G_e else None
     with torch.cuda.stream(stream):
-        for j in range(min(50, K_e)):
-            e2e_step(j)
+        ge_full.replay()
     torch.cuda.synchronize(dev)
     f0 = torch.cuda.Event(enable_timing=True)
     f1 = torch.cuda.Event(enable_timing=True)
@@ -439,8 +480,10 @@ def gpu_arm(args, rank: int, world: int, local_rank: int) -> dict | None:
     torch.cuda.synchronize(dev)
     with torch.cuda.stream(stream):
         f0.record(stream)
-        for j in range(K_e):
-            e2e_step(j)
+        for _ in range(K_e // G_e):
+            ge_full.replay()
+        if ge_rem is not None:
+            ge_rem.replay()
         f1.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
@@ -630,7 +673,10 @@ def main():
         "e2e": {"value": r["per_step_e2e_ms"] * 1e3 / world, "unit": "us",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                 "steps": r["K_e"],
-                "note": "eager: one pinned H2D copy, the C-ABI decode, one pinned D2H copy per step"},
+                "note": ("every step: one pinned H2D copy of its inputs, the C-ABI decode, one "
+                         "pinned D2H copy of its outputs; two staging buffers each way and "
+                         "three streams, so step j+1's upload and step j-1's download overlap "
+                         "step j's decode; captured in CUDA graphs of up to 50 steps")},
         "gpu_launches": args.steps * launches_per_step(r["path"], Bn, hidden),
         "clocks": r["clocks"],
     }
