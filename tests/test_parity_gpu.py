@@ -105,6 +105,16 @@ def test_head_counts(heads, batch):
     assert_parity(inp)
 
 
+@pytest.mark.parametrize("heads", [1, 3, 5, 127])
+@pytest.mark.parametrize("batch", [24, 64])
+def test_wide_kernel_head_counts(heads, batch):
+    """The wide tcgen05 kernel with odd head counts: pairs without a head, a
+    last two-head rope unit whose second head does not exist."""
+    inp = S.make_inputs(batch=batch, heads=heads, layout=S.LAYOUT_DS_MLA, pages=16,
+                        seed=250 + heads + batch)
+    assert_parity(inp)
+
+
 @pytest.mark.parametrize("batch", [1, 2])
 def test_fma_and_mma_paths_agree(batch):
     inp = S.make_inputs(batch=batch, heads=32, layout=S.LAYOUT_DS_MLA, pages=16, seed=300)
