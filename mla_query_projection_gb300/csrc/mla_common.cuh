@@ -90,50 +90,16 @@ __device__ __forceinline__ void put_q_run(const DecodeArgs& a, uint16_t* base, i
   }
 }
 
-// Paged KV insert of token b (page "mla.query", methods insert, kv_fp8,
-// insert_ds, insert_nvfp4), run by 64 threads (lt = 0..63, two whole warps).
-// Thread lt owns latent columns 8*lt..8*lt+7; threads 0..7 also own k_pe
-// values 8*lt..8*lt+7.  red2 holds the two warps' partial sums.
-__device__ void kv_insert(const DecodeArgs& a, int b, int lt, float* red2) {
-  const int lane = lt & 31, w = lt >> 5;
-  const int64_t slot = a.slots[b];
-  const uint4 v = *reinterpret_cast<const uint4*>(a.kv_c + (int64_t)b * a.kv_c_stride + 8 * lt);
-  const uint4 gv = *reinterpret_cast<const uint4*>(a.gamma_kv + 8 * lt);
-  uint4 pe = make_uint4(0, 0, 0, 0);
-  if (lt < 8) pe = *reinterpret_cast<const uint4*>(a.k_pe + (int64_t)b * a.k_pe_stride + 8 * lt);
-  const bool ds = a.layout == MLA_KV_FP8_DS_MLA;
-  const bool nv = a.layout == MLA_KV_NVFP4_DS_MLA;
-  const float ks = (ds || nv) ? 1.0f : *a.k_scale;
-  float x[8];
-  const uint32_t xw[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    x[2 * i] = bf16lo(xw[i]);
-    x[2 * i + 1] = bf16hi(xw[i]);
-  }
-  float ss = 0.f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) ss = fmaf(x[i], x[i], ss);
-  ss = warp_sum(ss);
-  if (lane == 0) red2[w] = ss;
-  named_barrier(kBarInsert, 64);
-  const float total = red2[0] + red2[1];
-  named_barrier(kBarInsert, 64);  // red2 may be reused by the next token
-  if (slot < 0) return;
-  const int64_t page = slot / a.page_size, off = slot % a.page_size;
-  if (page >= a.num_pages) {
-    if (lt == 0) atomicOr(a.err, MLA_DEVERR_BAD_SLOT);
-    return;
-  }
-  uint8_t* row = a.cache + (page * a.page_size + off) * (ds ? kRowDs : nv ? kRowNvfp4 : kRowE4m3);
-  const float rr = __frsqrt_rn(__fadd_rn(__fmul_rn(total, 1.0f / 512.0f), a.eps));
-  const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-  float n[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    n[2 * i] = bf_round(__fmul_rn(__fmul_rn(x[2 * i], rr), bf16lo(gw[i])));
-    n[2 * i + 1] = bf_round(__fmul_rn(__fmul_rn(x[2 * i + 1], rr), bf16hi(gw[i])));
-  }
+// The cache bytes of latent columns 8 lt..8 lt + 7 of a token's row (its
+// normalised BF16 values n) and, for lt < 8, of its k_pe values 8 lt..8 lt + 7,
+// in the row's layout (page "mla.query", methods insert, kv_fp8, insert_ds,
+// insert_nvfp4).  The fp8_ds_mla tile amax and the nvfp4 block amax are
+// reduced across the lanes that share them (16 and 2 consecutive lanes), so
+// the whole warp calls this together, with lt % 32 equal to the lane.
+__device__ __forceinline__ void kv_store_group(const DecodeArgs& a, uint8_t* row,
+                                               const float (&n)[8], uint4 pe, int lt, bool ds,
+                                               bool nv, float ks) {
+  const int lane = lt & 31;
   if (nv) {
     // one 16-value block per thread pair: E4M3 scale of max(amax / 6, 2^-9),
     // values as E2M1 of n * (1 / scale) with the stored (rounded) scale
@@ -196,6 +162,104 @@ __device__ void kv_insert(const DecodeArgs& a, int b, int lt, float* red2) {
              ((uint32_t)e4m3x2(__fdiv_rn(bf16lo(w2[3]), ks), __fdiv_rn(bf16hi(w2[3]), ks)) << 16);
       *reinterpret_cast<uint2*>(row + kKvLora + 8 * lt) = o2;
     }
+  }
+}
+
+// Sum of squares of 8 BF16 values in one FMA chain.
+__device__ __forceinline__ float kv_group_ss(uint4 v, float (&x)[8]) {
+  const uint32_t xw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = bf16lo(xw[i]);
+    x[2 * i + 1] = bf16hi(xw[i]);
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) ss = fmaf(x[i], x[i], ss);
+  return ss;
+}
+
+// The cache row of a slot, or null (a negative slot skips the row; a slot
+// beyond the cache skips it and sets MLA_DEVERR_BAD_SLOT).
+__device__ __forceinline__ uint8_t* kv_row(const DecodeArgs& a, int64_t slot, bool flag) {
+  if (slot < 0) return nullptr;
+  const int64_t page = slot / a.page_size, off = slot % a.page_size;
+  if (page >= a.num_pages) {
+    if (flag) atomicOr(a.err, MLA_DEVERR_BAD_SLOT);
+    return nullptr;
+  }
+  const bool ds = a.layout == MLA_KV_FP8_DS_MLA, nv = a.layout == MLA_KV_NVFP4_DS_MLA;
+  return a.cache + (page * a.page_size + off) * (ds ? kRowDs : nv ? kRowNvfp4 : kRowE4m3);
+}
+
+// Normalised BF16 values of 8 columns: bf16((x * rr) * gamma).
+__device__ __forceinline__ void kv_group_norm(const float (&x)[8], uint4 gv, float rr,
+                                              float (&n)[8]) {
+  const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    n[2 * i] = bf_round(__fmul_rn(__fmul_rn(x[2 * i], rr), bf16lo(gw[i])));
+    n[2 * i + 1] = bf_round(__fmul_rn(__fmul_rn(x[2 * i + 1], rr), bf16hi(gw[i])));
+  }
+}
+
+// Paged KV insert of token b (page "mla.query", methods insert, kv_fp8,
+// insert_ds, insert_nvfp4), run by 64 threads (lt = 0..63, two whole warps).
+// Thread lt owns latent columns 8*lt..8*lt+7; threads 0..7 also own k_pe
+// values 8*lt..8*lt+7.  red2 holds the two warps' partial sums.
+__device__ void kv_insert(const DecodeArgs& a, int b, int lt, float* red2) {
+  const int lane = lt & 31, w = lt >> 5;
+  const int64_t slot = a.slots[b];
+  const uint4 v = *reinterpret_cast<const uint4*>(a.kv_c + (int64_t)b * a.kv_c_stride + 8 * lt);
+  const uint4 gv = *reinterpret_cast<const uint4*>(a.gamma_kv + 8 * lt);
+  uint4 pe = make_uint4(0, 0, 0, 0);
+  if (lt < 8) pe = *reinterpret_cast<const uint4*>(a.k_pe + (int64_t)b * a.k_pe_stride + 8 * lt);
+  const bool ds = a.layout == MLA_KV_FP8_DS_MLA;
+  const bool nv = a.layout == MLA_KV_NVFP4_DS_MLA;
+  const float ks = (ds || nv) ? 1.0f : *a.k_scale;
+  float x[8];
+  float ss = warp_sum(kv_group_ss(v, x));
+  if (lane == 0) red2[w] = ss;
+  named_barrier(kBarInsert, 64);
+  const float total = red2[0] + red2[1];
+  named_barrier(kBarInsert, 64);  // red2 may be reused by the next token
+  uint8_t* row = kv_row(a, slot, lt == 0);
+  if (row == nullptr) return;
+  const float rr = __frsqrt_rn(__fadd_rn(__fmul_rn(total, 1.0f / 512.0f), a.eps));
+  float n[8];
+  kv_group_norm(x, gv, rr, n);
+  kv_store_group(a, row, n, pe, lt, ds, nv, ks);
+}
+
+// The same insert run by one warp: lane l takes the columns of threads l and
+// l + 32 of the 64-thread insert, and the sums are formed in the same order
+// (each group's FMA chain, each group reduced across the warp, group 0 plus
+// group 1), so the bytes written are the same.
+__device__ void kv_insert_warp(const DecodeArgs& a, int b, int lane) {
+  const int64_t slot = a.slots[b];
+  const uint16_t* kv = a.kv_c + (int64_t)b * a.kv_c_stride;
+  uint4 v[2], gv[2];
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    v[g] = *reinterpret_cast<const uint4*>(kv + 8 * (lane + 32 * g));
+    gv[g] = *reinterpret_cast<const uint4*>(a.gamma_kv + 8 * (lane + 32 * g));
+  }
+  uint4 pe = make_uint4(0, 0, 0, 0);
+  if (lane < 8) pe = *reinterpret_cast<const uint4*>(a.k_pe + (int64_t)b * a.k_pe_stride + 8 * lane);
+  const bool ds = a.layout == MLA_KV_FP8_DS_MLA;
+  const bool nv = a.layout == MLA_KV_NVFP4_DS_MLA;
+  const float ks = (ds || nv) ? 1.0f : *a.k_scale;
+  float x[2][8];
+  const float s0 = warp_sum(kv_group_ss(v[0], x[0]));
+  const float s1 = warp_sum(kv_group_ss(v[1], x[1]));
+  uint8_t* row = kv_row(a, slot, lane == 0);
+  if (row == nullptr) return;
+  const float rr = __frsqrt_rn(__fadd_rn(__fmul_rn(s0 + s1, 1.0f / 512.0f), a.eps));
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    float n[8];
+    kv_group_norm(x[g], gv[g], rr, n);
+    kv_store_group(a, row, n, g == 0 ? pe : make_uint4(0, 0, 0, 0), lane + 32 * g, ds, nv, ks);
   }
 }
 

@@ -672,6 +672,13 @@ constexpr int kTaskQbBytes = kTaskRows * kPitch;              // 50176
 constexpr int kTaskStage = kTaskQbBytes + kTaskUkBytes;       // 66560
 constexpr int kAbsStages = 3;
 constexpr int kAbsThreads = kConsumers + 32;                  // + producer warp
+// The 16-token paired kernel has a KV insert warp besides: its consumers'
+// longer prologue would otherwise carry the insert (measured at H = 64: 11.6
+// against 11.0 us); the 8-token kernel's consumers are faster without it.
+template <int NT>
+constexpr int pair_threads() {
+  return NT == 16 ? kAbsThreads + 32 : kAbsThreads;
+}
 
 template <int NT>
 struct AbsSmem {
@@ -1423,7 +1430,7 @@ __device__ __forceinline__ void pair_prefetch_stage(const DecodeArgs& a, const P
 }
 
 template <int NT>
-__global__ void __launch_bounds__(kAbsThreads, 1)
+__global__ void __launch_bounds__(pair_threads<NT>(), 1)
     mla_absorb_pair_kernel(const DecodeArgs a, const __grid_constant__ PairSplit split) {
   using S = PairSmem<NT>;
   constexpr int NTL = S::NTL;
@@ -1517,6 +1524,12 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
     if (lane == 0)
       for (int k = max(0, nst - ST); k < nst; ++k)
         (void)mbar_wait_bounded(&full[k % ST], (uint32_t)((k / ST) & 1), kWaitLimit);
+  } else if (warp == kConsumerWarps + 1) {
+    // ================= KV insert warp (16 tokens) ====================
+    // The CTA's KV rows (kv_c and k_pe are inputs: after the PDL wait), off
+    // the consumers' and the producer's paths.
+    pdl_wait();
+    for (int t = i; t < a.batch; t += P) kv_insert_warp(a, t, lane);
   } else {
     // ================= consumer warps 0-7 ============================
     const int g = lane >> 2, q = lane & 3;
@@ -1572,7 +1585,7 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
               xb[nt][c];
       }
     }
-    if (warp >= 6)
+    if (NT == 8 && warp >= 6)
       for (int t = i; t < a.batch; t += P) kv_insert(a, t, tid - 192, ss_s + kConsumerWarps * NT);
     if (tid == 0) trace_stamp(a, 2);
 
@@ -1999,7 +2012,7 @@ template <int NT>
 cudaLaunchConfig_t pair_config(int ctas, cudaStream_t stream, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)ctas, 1, 1);
-  cfg.blockDim = dim3(kAbsThreads, 1, 1);
+  cfg.blockDim = dim3(pair_threads<NT>(), 1, 1);
   cfg.dynamicSmemBytes = PairSmem<NT>::kAlloc;
   cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
