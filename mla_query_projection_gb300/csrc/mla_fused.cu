@@ -782,7 +782,6 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int i = blockIdx.x, P = gridDim.x;
-  const int H = a.heads;
   const AbsSeq seq{split.task[i], split.task[i + 1], split.rope[i], split.rope[i + 1]};
   const int nst = seq.stages();
 
@@ -1074,7 +1073,6 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int i = blockIdx.x, P = gridDim.x;
-  const int H = a.heads;
   const AbsSeq seq{split.task[i], split.task[i + 1], split.rope[i], split.rope[i + 1]};
   const int nst = seq.stages();
 
@@ -1448,7 +1446,6 @@ __global__ void __launch_bounds__(pair_threads<NT>(), 1)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int i = blockIdx.x, P = gridDim.x;
-  const int H = a.heads;
   const int pair = i >> 1, rank = i & 1;  // cluster (2, 1, 1): rank = blockIdx.x % 2
   const PairSeq seq{split.head[pair], split.head[pair + 1] - split.head[pair], rank,
                     split.rope[i], split.rope[i + 1]};

@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + S::oTslot);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int i = blockIdx.x, P = gridDim.x;
+  const int i = blockIdx.x;
   const int pair = i >> 1, rank = i & 1;  // cluster (2, 1, 1)
   const uint32_t peer = (uint32_t)(rank ^ 1);
   const int H = a.heads;
