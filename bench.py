@@ -95,28 +95,25 @@ def read_peaks() -> tuple[float, str]:
 QKV_ROW, HIDDEN = 2112, 7168
 
 
-def kernel_for(path: int, batch: int) -> str:
-    """The kernel one decode step launches on the given path (MLA_PATH_FMA:
-    the FP32-FMA absorbing kernel, one or two tokens per CTA; MLA_PATH_MMA:
-    the paired tensor-core kernel, 8 or 16 tokens per launch, or above 16
-    tokens the wide tcgen05 kernel, 64 tokens per launch)."""
-    if path == 1:
-        return f"mla_absorb_kernel<{1 if batch <= 1 else 2}>"
-    if batch > 16:
-        return "mla_wide_kernel"
-    return f"mla_absorb_pair_kernel<{8 if batch <= 8 else 16}>"
+def dominant_kernel(kernels: str) -> str:
+    """The kernel whose ncu summary a step's traffic comes from: of the kernels
+    a decode launches ("a+b", as mla_query_kernel_for names them), the wide
+    kernel, else the first."""
+    names = kernels.split("+")
+    return next((k for k in names if k.endswith("wide_kernel")), names[0])
 
 
-def launches_per_step(path: int, batch: int, hidden: bool = False) -> int:
-    """Kernels one decode call launches: the FMA absorbing kernel is followed by
-    the head-closing kernel; the paired kernel runs once up to 16 tokens, above
-    that the wide tcgen05 kernel (after its normalising kernel) once per 64
-    tokens.  A step from the hidden row first runs the qkv_a projection once
-    per 8 tokens."""
-    pre = -(-batch // 8) if hidden else 0
-    if path == 1:
-        return pre + 2
-    return pre + (2 * -(-batch // 64) if batch > 16 else 1)
+def launches_per_step(kernels: str, batch: int, hidden: bool = False) -> int:
+    """Kernels one step launches: those a decode names, once per 64 tokens on
+    the wide path and once per 16 tokens when the 16-token paired kernel
+    serves more than 16; a step from the hidden row first runs the qkv_a
+    projection once per 8 tokens."""
+    n = len(kernels.split("+"))
+    if "wide_kernel" in kernels:
+        n *= -(-batch // 64)
+    elif batch > 16:
+        n *= -(-batch // 16)
+    return n + (-(-batch // 8) if hidden else 0)
 
 
 def profile_name(kernel: str, workload: str) -> str:
@@ -378,6 +375,7 @@ def gpu_arm(args, rank: int, world: int, local_rank: int) -> dict | None:
     clocks = sampler.stop()
     ms = e0.elapsed_time(e1)
     path = B.mla_query_path_for(sets[0]["handle"], Bn)
+    kernels = B.mla_query_kernel_for(sets[0]["handle"], Bn)
     flags = 0
     for w in sets:
         flags |= B.mla_query_get_error(w["handle"], stream)
@@ -499,7 +497,8 @@ def gpu_arm(args, rank: int, world: int, local_rank: int) -> dict | None:
     per_step_ms, per_step_e2e_ms = max_over_ranks([ms / args.steps, ms_e2e / K_e], dev)
 
     return dict(per_step_ms=per_step_ms, per_step_e2e_ms=per_step_e2e_ms, h2d=h2d, d2h=d2h,
-                clocks=clocks, nsets=nsets, l2=l2, K_e=K_e, cfg=cfg, path=path, wbytes=wbytes)
+                clocks=clocks, nsets=nsets, l2=l2, K_e=K_e, cfg=cfg, path=path, wbytes=wbytes,
+                kernels=kernels)
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -649,7 +648,7 @@ def main():
     nbytes = algorithmic_bytes(Bn, H, layout, hidden)
     achieved = nbytes / (per_step_us * 1e-6) / 1e9
     peak, peak_src = read_peaks()
-    kernel = kernel_for(r["path"], Bn)
+    kernel = dominant_kernel(r["kernels"])
     if hidden:
         kernel = "mla_qkv_a_kernel+" + kernel
     config.update({
@@ -677,7 +676,8 @@ def main():
                          "pinned D2H copy of its outputs; two staging buffers each way and "
                          "three streams, so step j+1's upload and step j-1's download overlap "
                          "step j's decode; captured in CUDA graphs of up to 50 steps")},
-        "gpu_launches": args.steps * launches_per_step(r["path"], Bn, hidden),
+        "gpu_launches": args.steps * launches_per_step(r["kernels"], Bn, hidden),
+        "kernels": r["kernels"],
         "clocks": r["clocks"],
     }
     if not args.no_cpu and world == 1:

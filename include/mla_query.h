@@ -291,6 +291,12 @@ MLA_API int mla_query_decode_noalloc(int num_heads, const void* w_qb, const void
                                      void* q_pe, void* q_c, unsigned* device_flags,
                                      void* stream);
 
+/* mla_query_kernel_for - static text naming the kernels one decode of
+ * `batch` tokens launches on this handle and its path, "+" between kernels
+ * launched in sequence (a diagnostic: the split by batch size, head count and
+ * path).  NULL for a null handle or a batch outside 1..MLA_MAX_BATCH. */
+MLA_API const char* mla_query_kernel_for(mla_query_t h, int batch);
+
 /* mla_query_destroy - free the handle and its scratch (NULL is a no-op).
  * The caller must ensure no decode on the handle is still in flight. */
 MLA_API void mla_query_destroy(mla_query_t h);

@@ -25,6 +25,7 @@ from .binding import (  # noqa: F401
     mla_query_rows_wait,
     mla_query_destroy,
     mla_query_get_error,
+    mla_query_kernel_for,
     mla_query_path_for,
     mla_query_set_path,
     mla_qkv_a_create,

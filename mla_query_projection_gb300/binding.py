@@ -81,6 +81,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.mla_query_decode_noalloc.restype = i32
     lib.mla_query_destroy.argtypes = [vp]
     lib.mla_query_destroy.restype = None
+    lib.mla_query_kernel_for.argtypes = [vp, i32]
+    lib.mla_query_kernel_for.restype = ctypes.c_char_p
     lib.mla_query_strerror.argtypes = [i32]
     lib.mla_query_strerror.restype = ctypes.c_char_p
     lib.mla_query_decode_rows.argtypes = [
@@ -193,6 +195,12 @@ def mla_query_set_path(handle, path) -> int:
 
 def mla_query_path_for(handle, batch) -> int:
     return load().mla_query_path_for(handle, int(batch))
+
+
+def mla_query_kernel_for(handle, batch) -> str | None:
+    """Names of the kernels a decode of `batch` tokens launches ("a+b")."""
+    r = load().mla_query_kernel_for(handle, int(batch))
+    return r.decode() if r is not None else None
 
 
 def mla_query_destroy(handle) -> None:

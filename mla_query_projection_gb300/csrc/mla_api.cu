@@ -491,6 +491,22 @@ int mla_query_path_for(mla_query_t h, int batch) {
   return kern == Kernel::kAbsorbFma ? MLA_PATH_FMA : MLA_PATH_MMA;
 }
 
+const char* mla_query_kernel_for(mla_query_t h, int batch) {
+  if (h == nullptr || batch < 1 || batch > MLA_MAX_BATCH) return nullptr;
+  Kernel kern = Kernel::kAbsorbFma;
+  int nt = 1;
+  if (pick_kernel(h, batch, &kern, &nt) != MLA_OK) return nullptr;
+  switch (kern) {
+    case Kernel::kAbsorbFma: return nt == 1 ? "mla_absorb_kernel<1>+mla_close_kernel<1>"
+                                            : "mla_absorb_kernel<2>+mla_close_kernel<2>";
+    case Kernel::kAbsorbMma: return nt == 8 ? "mla_absorb_mma_kernel<8>" : "mla_absorb_mma_kernel<16>";
+    case Kernel::kAbsorbPair: return nt == 8 ? "mla_absorb_pair_kernel<8>" : "mla_absorb_pair_kernel<16>";
+    case Kernel::kWide: return "mla_wide_norm_kernel+mla_wide_kernel";
+    case Kernel::kHandoff: return "mla_fused_kernel";
+  }
+  return nullptr;
+}
+
 #ifdef MLA_TRACE
 // Timeline readout of trace builds: copies the per-CTA stamps to `host` and
 // clears them for the next call.

@@ -722,21 +722,13 @@ __device__ __forceinline__ void abs_prefetch_stage(const DecodeArgs& a, const Ab
   }
 }
 
-// Head closing of the absorbing kernels, launched right after them (its CTAs
-// may be resident early and wait, programmatic dependent launch):
-// q_latent[t][h][c] = BF16 of the 8 FP32 partials of head h, token t, added
-// in task order (partials laid out [task][token < NT][512]).  One thread per
-// (token, head, 4 columns).
+// Latent columns 4 c4..4 c4 + 3 of head h, token t: the head's 8 FP32
+// partials (laid out [task][token < NT][512]) added in task order and rounded
+// once (BF16, or with a per-tensor query scale the E4M3 code of the BF16
+// value).
 template <int NT>
-__global__ void __launch_bounds__(256) mla_close_kernel(const DecodeArgs a) {
-  // The next kernel may be scheduled at once (it streams static weights
-  // until its own wait, which covers this kernel's completion).
-  pdl_launch_dependents();
-  pdl_wait();  // the partials of the absorbing kernel
-  const int per_tok = a.heads * (kKvLora / 4);
-  const int items = a.batch * per_tok;
-  for (int it = blockIdx.x * blockDim.x + threadIdx.x; it < items; it += gridDim.x * blockDim.x) {
-    const int t = it / per_tok, r = it % per_tok, h = r / (kKvLora / 4), c4 = r % (kKvLora / 4);
+__device__ __forceinline__ void close_item(const DecodeArgs& a, int h, int t, int c4) {
+  {
     const float* part = a.partial + ((int64_t)h * kTasksPerHead * NT + t) * kKvLora + 4 * c4;
     float4 v[kTasksPerHead];
 #pragma unroll
@@ -762,6 +754,23 @@ __global__ void __launch_bounds__(256) mla_close_kernel(const DecodeArgs a) {
           (uint32_t)q_fp8(acc.x, qsi) | ((uint32_t)q_fp8(acc.y, qsi) << 8) |
           ((uint32_t)q_fp8(acc.z, qsi) << 16) | ((uint32_t)q_fp8(acc.w, qsi) << 24);
     }
+  }
+}
+
+// Head closing of the FP32-FMA absorbing kernel, launched right after it
+// (its CTAs may be resident early and wait, programmatic dependent launch).
+// One thread per (token, head, 4 columns).
+template <int NT>
+__global__ void __launch_bounds__(256) mla_close_kernel(const DecodeArgs a) {
+  // The next kernel may be scheduled at once (it streams static weights
+  // until its own wait, which covers this kernel's completion).
+  pdl_launch_dependents();
+  pdl_wait();  // the partials of the absorbing kernel
+  const int per_tok = a.heads * (kKvLora / 4);
+  const int items = a.batch * per_tok;
+  for (int it = blockIdx.x * blockDim.x + threadIdx.x; it < items; it += gridDim.x * blockDim.x) {
+    const int t = it / per_tok, r = it % per_tok;
+    close_item<NT>(a, r / (kKvLora / 4), t, r % (kKvLora / 4));
   }
 }
 
@@ -1052,7 +1061,8 @@ struct AbsMmaSmem {
   static constexpr int oFull = oSs + (kConsumerWarps * NT + 8) * 4;
   static constexpr int oEmpty = oFull + kAbsStages * 8;
   static constexpr int oRbar = oEmpty + kAbsStages * 8;            // [2] split-K barriers
-  static constexpr int kBytes = oRbar + 16;
+  static constexpr int oClose = oRbar + 16;                        // head this CTA closes, or -1
+  static constexpr int kBytes = oClose + 16;
   static constexpr int kAlloc = kBytes + 128;
 };
 
@@ -1349,6 +1359,28 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
           }
         }
       }
+      // The CTA that stores a head's last partial closes the head: it adds
+      // the 8 partials in task order (no second kernel).  A per-head counter
+      // in the handle's scratch counts the stored tasks; the closer resets
+      // it for the next call.
+      __threadfence();
+      named_barrier(kBarConsumers, kConsumers);
+      int* close_s = reinterpret_cast<int*>(smem + S::oClose);
+      if (tid == 0) {
+        const int h = tk / kTasksPerHead;
+        int ch = -1;
+        if (atomicAdd(&a.ready[h], 1u) + 1 == (uint32_t)kTasksPerHead) {
+          __threadfence();
+          a.ready[h] = 0;
+          ch = h;
+        }
+        *close_s = ch;
+      }
+      named_barrier(kBarConsumers, kConsumers);
+      const int ch = *close_s;
+      if (ch >= 0)
+        for (int it = tid; it < a.batch * (kKvLora / 4); it += kConsumers)
+          close_item<NT>(a, ch, it / (kKvLora / 4), it % (kKvLora / 4));
       MLA_PHASE(4);
     }
 #ifdef MLA_TRACE
@@ -1966,9 +1998,7 @@ cudaError_t launch_abs_mma(const DecodeArgs& a, const AbsSplit& sp, int ctas, cu
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, mla_absorb_mma_kernel<NT>, a, sp);
-  if (e != cudaSuccess) return e;
-  return launch_close<NT>(a, ctas, stream);
+  return cudaLaunchKernelEx(&cfg, mla_absorb_mma_kernel<NT>, a, sp);
 }
 
 template <int NT>

@@ -108,3 +108,7 @@ def test_gathered_rows_reject_bad_arguments_on_host(lib):
     assert B.mla_query_rows_arm(24, 1, 64, 1, None) == B.MLA_EINVAL  # misaligned
     assert B.mla_query_decode_rows(None, 1, 16, 0, 16, 0, 16, 0, 16, 16, 1, 64, 0, 16, None, 16,
                                    64, 0, None, None) == B.MLA_EINVAL
+
+
+def test_kernel_for_rejects_a_null_handle(lib):
+    assert B.mla_query_kernel_for(None, 1) is None

@@ -175,6 +175,44 @@ def test_repeated_calls_rearm_and_match():
     step.close()
 
 
+def test_small_head_count_repeated_calls_close_every_head():
+    """Small head counts run the partials kernel, whose last CTA per head adds
+    the head's partials: the per-head counters must re-arm, so repeated calls
+    give the same bits and no timeout flag."""
+    inp = S.make_inputs(batch=4, heads=16, layout=S.LAYOUT_E4M3, pages=8, seed=710)
+    st = DecodeStep(inp)
+    assert B.mla_query_kernel_for(st.handle, 4) == "mla_absorb_mma_kernel<8>"
+    outs = []
+    for _ in range(4):
+        assert st.decode() == B.MLA_OK
+        outs.append(st.results())
+    assert st.error_flags() == 0
+    check_against_oracle(outs[0], inp)
+    for o in outs[1:]:
+        for k in ("q_latent", "q_pe", "q_c"):
+            assert np.array_equal(o[k], outs[0][k])
+    st.close()
+
+
+@pytest.mark.parametrize(
+    "batch,heads,path,want",
+    [
+        (1, 64, B.MLA_PATH_AUTO, "mla_absorb_pair_kernel<8>"),
+        (12, 64, B.MLA_PATH_AUTO, "mla_absorb_pair_kernel<16>"),
+        (40, 64, B.MLA_PATH_AUTO, "mla_wide_norm_kernel+mla_wide_kernel"),
+        (1, 16, B.MLA_PATH_AUTO, "mla_absorb_mma_kernel<8>"),
+        (2, 16, B.MLA_PATH_FMA, "mla_absorb_kernel<2>+mla_close_kernel<2>"),
+    ],
+)
+def test_kernel_for_names_the_split(batch, heads, path, want):
+    inp = S.make_inputs(batch=1, heads=heads, layout=S.LAYOUT_E4M3, pages=2, seed=720)
+    st = DecodeStep(inp)
+    assert st.set_path(path) == B.MLA_OK
+    assert B.mla_query_kernel_for(st.handle, batch) == want
+    assert B.mla_query_kernel_for(st.handle, 0) is None
+    st.close()
+
+
 def test_all_paths_deterministic_across_handles():
     inp = S.make_inputs(batch=2, heads=16, layout=S.LAYOUT_E4M3, pages=8, seed=800)
     a, _ = run_case(inp)
