@@ -402,7 +402,7 @@ def gpu_arm(args, rank: int, world: int, local_rank: int) -> dict | None:
     else:
         fused = torch.cat([q_a.cpu(), kv_c.cpu(), k_pe.cpu()], dim=1).contiguous()
     o_sizes = [Bn * H * 512 * 2, Bn * H * 64 * 2, Bn * 1536 * 2]
-    NBUF = 2
+    NBUF = args.e2e_bufs
     bufs = []
     for _ in range(NBUF):
         h_in = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
@@ -586,6 +586,8 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD_DEFAULT)
     ap.add_argument("--graph-steps", type=int, default=100)
     ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--e2e-bufs", type=int, default=2,
+                    help="staging buffers each way in the end-to-end loop")
     ap.add_argument("--path", type=int, default=0, help="force MLA_PATH_* (0 = auto)")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu", action="store_true")
