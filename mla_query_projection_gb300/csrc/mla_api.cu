@@ -210,15 +210,16 @@ int mla_query_create(mla_query_t* out, int num_heads, const void* w_qb, const vo
     rc = MLA_ENOMEM;
     goto fail;
   }
-  if (mla::prepare_wide_kernel() != cudaSuccess ||
-      mla::pack_wide_weights(h->w_qb, h->w_uk, h->wide_qb, h->wide_ukt, num_heads, 0) !=
-          cudaSuccess ||
-      cudaStreamSynchronize(0) != cudaSuccess)
-    goto fail;
+  if (mla::prepare_wide_kernel() != cudaSuccess) goto fail;
+  // the split decides the rope tiles' shape, so it comes before the packing
   h->wide_ctas = h->num_sms & ~1;
   if (!mla::make_wide_split(num_heads, h->wide_ctas, &h->wide_split) ||
       !mla::wide_kernel_fits(h->wide_ctas))
     h->wide_ctas = 0;
+  if (mla::pack_wide_weights(h->w_qb, h->w_uk, h->wide_qb, h->wide_ukt, num_heads,
+                             h->wide_split.single, 0) != cudaSuccess ||
+      cudaStreamSynchronize(0) != cudaSuccess)
+    goto fail;
 #ifdef MLA_TRACE
   {
     const size_t tb = (size_t)h->num_sms * mla::kTraceSlots * 8;

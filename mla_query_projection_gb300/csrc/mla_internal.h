@@ -113,10 +113,14 @@ bool make_pair_split(int heads, int ctas, PairSplit* sp);
 bool pair_kernel_fits(int ctas, int nt);
 // Wide kernel (17-64 tokens, tcgen05, clusters of two CTAs splitting K): the
 // heads of pair c are [head[c], head[c + 1]) (at most two), its rope units
-// the heads [rope[c], rope[c + 1]).
+// [rope[c], rope[c + 1]).  A rope unit is the rope rows of two heads (2u,
+// 2u + 1: one 128-row tile), or with `single` set the rope rows of one head
+// (a 64-row tile): finer units, which even out the pairs where two-head units
+// cannot (64 heads on 76 pairs).
 struct WideSplit {
   uint16_t head[kMaxCtas / 2 + 1];
   uint16_t rope[kMaxCtas / 2 + 1];
+  int single;
 };
 int wide_tokens();
 cudaError_t prepare_wide_kernel();
@@ -126,7 +130,7 @@ bool make_wide_split(int heads, int ctas, WideSplit* sp);
 size_t wide_qb_bytes(int heads);
 size_t wide_ukt_bytes(int heads);
 cudaError_t pack_wide_weights(const uint16_t* w_qb, const uint16_t* w_uk, uint8_t* qb_tiles,
-                              uint8_t* ukt_tiles, int heads, cudaStream_t stream);
+                              uint8_t* ukt_tiles, int heads, int single, cudaStream_t stream);
 // Bounded poll of a gathered query buffer [batch][q_heads][576] (mla_gather.cu):
 // returns once no element of the first wait_heads rows of every token is the
 // all-ones sentinel, or sets MLA_DEVERR_TIMEOUT in *err after limit_ns.

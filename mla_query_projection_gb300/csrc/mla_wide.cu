@@ -13,7 +13,9 @@
 //  * Units of a pair (the same list on both CTAs): for each of its heads (at
 //    most two) NOPE (the head's 128 nope rows: one M = 128 tile, N = 64
 //    tokens, K = 768) then ABS (the absorption of that head), and then a
-//    byte-balancing share of ROPE units (the 64 rope rows of two heads).
+//    byte-balancing share of ROPE units: the 64 rope rows of two heads (one
+//    M = 128 tile), or of one head (an M = 64 tile, six boxes per CTA) where
+//    those finer units balance the pairs better (64 heads on 76 pairs).
 //  * The weights are copied at create into 16 KiB tiles (128 rows x 64
 //    K-columns, already in the swizzled shared-memory layout), so a producer
 //    thread streams each tile with one 16 KiB 1-D bulk TMA copy into a 5-slot
@@ -51,6 +53,7 @@ constexpr int kWideTok = 64;                 // tokens per launch (N of the Q_B 
 constexpr int kWideHalfTok = 32;             // tokens each CTA of the pair finishes
 constexpr int kWideKHalf = kQLora / 2;       // 768
 constexpr int kWideAtoms = kWideKHalf / 64;  // 12 K atoms of 64 columns (128 B)
+constexpr int kWideSingleBoxes = kWideAtoms / 2;  // one head's rope rows: 6 boxes of 2 atoms
 constexpr int kWideSlots = 5;
 constexpr int kWideBox = 128 * 128;          // one 128-row x 128 B box (16 KiB)
 constexpr int kWideThreads = 256;
@@ -162,7 +165,7 @@ __device__ __forceinline__ int sw128(int row, int col) {
 // absorption needs it, and the step ends on absorptions, whose epilogue needs
 // nothing from the other CTA.
 struct WideSeq {
-  int h0, nh, r0, nr;
+  int h0, nh, r0, nr, single;
   __device__ int units() const { return 2 * nh + nr; }
   __device__ int kind(int u) const {
     if (u < nh) return kUnitNope;
@@ -175,19 +178,24 @@ struct WideSeq {
     if (u < nh + nr) return r0 + (u - nh);
     return h0 + (u - nh - nr);
   }
-  __device__ int boxes(int u) const { return kind(u) == kUnitAbs ? 4 : kWideAtoms; }
+  __device__ int boxes(int u) const {
+    const int k = kind(u);
+    return k == kUnitAbs ? 4 : k == kUnitRope && single ? kWideSingleBoxes : kWideAtoms;
+  }
 };
 
 // Tile addresses in the packed copies (pack_wide_weights): NOPE tile
-// (h, K half, atom), ROPE tile (rope unit, K half, atom), W_UK^T tile
-// (h, 128-column tile ct, 64-row atom pa); the CTA of rank `half` takes the
-// W_UK^T tiles of latent columns 256 half.. (ct = 2 half + bx / 2, pa = bx % 2).
+// (h, K half, atom), ROPE tile (rope unit, K half, atom) or, for single-head
+// rope units, (head, K half, pair of atoms), W_UK^T tile (h, 128-column tile
+// ct, 64-row atom pa); the CTA of rank `half` takes the W_UK^T tiles of
+// latent columns 256 half.. (ct = 2 half + bx / 2, pa = bx % 2).
 __device__ __forceinline__ const uint8_t* wide_tile(const DecodeArgs& a, int kind, int h,
-                                                    int half, int bx) {
+                                                    int half, int bx, int single) {
   if (kind == kUnitNope)
     return a.wide_qb + ((size_t)(h * 2 + half) * kWideAtoms + bx) * kWideBox;
   if (kind == kUnitRope)
-    return a.wide_qb + ((size_t)a.heads * 2 * kWideAtoms + (size_t)(h * 2 + half) * kWideAtoms + bx) *
+    return a.wide_qb + ((size_t)a.heads * 2 * kWideAtoms +
+                        (size_t)(h * 2 + half) * (single ? kWideSingleBoxes : kWideAtoms) + bx) *
                            kWideBox;
   return a.wide_ukt + ((size_t)h * 8 + 4 * half + bx) * kWideBox;  // 2 ct + pa
 }
@@ -217,7 +225,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   const uint32_t peer = (uint32_t)(rank ^ 1);
   const int H = a.heads;
   const WideSeq seq{split.head[pair], split.head[pair + 1] - split.head[pair], split.rope[pair],
-                    split.rope[pair + 1] - split.rope[pair]};
+                    split.rope[pair + 1] - split.rope[pair], split.single};
   const int nu = seq.units();
 
   if (tid == 0) {
@@ -273,8 +281,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           if (k >= kWideSlots && !mbar_wait_bounded(&empty[slot], phase, kWaitLimit))
             timed_out = true;
           mbar_arrive_expect_tx(&full[slot], kWideBox);
-          bulk_g2s_hint(smem + S::oRing + slot * kWideBox, wide_tile(a, kind, h, rank, bx), kWideBox,
-                        &full[slot], pol);
+          bulk_g2s_hint(smem + S::oRing + slot * kWideBox, wide_tile(a, kind, h, rank, bx, seq.single),
+                        kWideBox, &full[slot], pol);
           if (bx == 0 && u < 4) trace_stamp(a, 24 + u);  // unit u's first box issued
           if (++slot == kWideSlots) {
             slot = 0;
@@ -300,6 +308,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       const uint64_t dxq = umma_desc(smem_u32(smem + S::oXq));
       const uint64_t dqt = umma_desc(smem_u32(smem + S::oQt));
       constexpr uint32_t idq = umma_idesc(128, kWideTok);
+      constexpr uint32_t idq64 = umma_idesc(64, kWideTok);
       int nq = 0, na = 0;  // Q_B tiles, absorptions so far
       int slot = 0;
       uint32_t fphase = 0;  // parity of the slot's next full phase
@@ -335,6 +344,21 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             umma(dt, da + 2, db + 2, idq, 1u);
             umma(dt, da + 4, db + 4, idq, 1u);
             umma(dt, da + 6, db + 6, idq, 1u);
+          } else if (kind == kUnitRope && seq.single) {
+            // one head's 64 rope rows, K atoms 2 bx and 2 bx + 1 (8 KiB
+            // each): M = 64, rows in TMEM lanes 32 (r / 16) + r % 16
+            const uint64_t db = dxq + (uint64_t)(2 * bx * ((kWideTok * 128) >> 4));
+            const uint64_t da1 = da + (uint64_t)((64 * 128) >> 4);
+            const uint64_t db1 = db + (uint64_t)((kWideTok * 128) >> 4);
+            const uint32_t dt = tmem + dcol;
+            umma(dt, da, db, idq64, (uint32_t)bx);
+            umma(dt, da + 2, db + 2, idq64, 1u);
+            umma(dt, da + 4, db + 4, idq64, 1u);
+            umma(dt, da + 6, db + 6, idq64, 1u);
+            umma(dt, da1, db1, idq64, 1u);
+            umma(dt, da1 + 2, db1 + 2, idq64, 1u);
+            umma(dt, da1 + 4, db1 + 4, idq64, 1u);
+            umma(dt, da1 + 6, db1 + 6, idq64, 1u);
           } else {
             const uint64_t db = dxq + (uint64_t)(bx * ((kWideTok * 128) >> 4));
             const uint32_t dt = tmem + dcol;
@@ -471,6 +495,14 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             }
             mbar_arrive(&qready[j]);
           }
+        } else if (seq.single) {
+          // head h: row 16 (m / 32) + m % 32 in TMEM lanes with m % 32 < 16
+          if ((m & 31) < 16) {
+            const int nt_here = min(kWideHalfTok, a.batch - my0);
+            put_q_run(a, a.q_pe,
+                      (int64_t)my0 * a.qp_ts + (int64_t)h * a.qp_hs + 16 * (m >> 5) + (m & 15),
+                      a.qp_ts, q, nt_here, qsi);
+          }
         } else if (2 * h + (m >> 6) < H) {  // rows 0..63: head 2h, 64..127: head 2h + 1
           const int hr = 2 * h + (m >> 6);
           const int nt_here = min(kWideHalfTok, a.batch - my0);
@@ -549,26 +581,37 @@ __global__ void __launch_bounds__(192) mla_wide_norm_kernel(const DecodeArgs a) 
 //   W_UK^T tiles (h, ct, pa): row r = latent column 128 ct + r, K = W_UK row
 //   64 pa + k.
 __global__ void pack_wide_qb_kernel(const uint16_t* __restrict__ w_qb, uint8_t* __restrict__ out,
-                                    int heads) {
+                                    int heads, int single) {
   const int ropes = (heads + 1) / 2;
-  const int64_t tiles = (int64_t)(heads + ropes) * 2 * kWideAtoms;
+  const int64_t nope_tiles = (int64_t)heads * 2 * kWideAtoms;
+  const int64_t tiles = nope_tiles + (single ? (int64_t)heads * 2 * kWideSingleBoxes
+                                             : (int64_t)ropes * 2 * kWideAtoms);
   const int64_t n = tiles * 128 * 8;  // 16-byte chunks
   for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n;
        e += (int64_t)gridDim.x * blockDim.x) {
     const int j = (int)(e & 7), r = (int)((e >> 3) & 127);
     const int64_t tile = e >> 10;
-    const int at = (int)(tile % kWideAtoms), half = (int)((tile / kWideAtoms) & 1);
-    const int64_t unit = tile / (2 * kWideAtoms);
     int64_t row = -1;
-    if (unit < heads) {
-      row = unit * kHeadRows + r;
+    int col = 0;  // first K column of the chunk
+    if (tile < nope_tiles) {
+      const int at = (int)(tile % kWideAtoms), half = (int)((tile / kWideAtoms) & 1);
+      row = (tile / (2 * kWideAtoms)) * kHeadRows + r;
+      col = kWideKHalf * half + 64 * at;
+    } else if (single) {
+      // (head, half, box): rows 0..63 = its rope rows at K atom 2 box,
+      // rows 64..127 of the tile = the same rows at K atom 2 box + 1
+      const int64_t t = tile - nope_tiles;
+      const int bx = (int)(t % kWideSingleBoxes), half = (int)((t / kWideSingleBoxes) & 1);
+      row = (t / (2 * kWideSingleBoxes)) * kHeadRows + kNope + (r & 63);
+      col = kWideKHalf * half + 64 * (2 * bx + (r >> 6));
     } else {
-      const int64_t hd = 2 * (unit - heads) + (r >> 6);
+      const int at = (int)(tile % kWideAtoms), half = (int)((tile / kWideAtoms) & 1);
+      const int64_t hd = 2 * (tile / (2 * kWideAtoms) - heads) + (r >> 6);
       if (hd < heads) row = hd * kHeadRows + kNope + (r & 63);
+      col = kWideKHalf * half + 64 * at;
     }
     uint4 v = make_uint4(0, 0, 0, 0);
-    if (row >= 0)
-      v = *reinterpret_cast<const uint4*>(w_qb + row * kQLora + kWideKHalf * half + 64 * at + 8 * j);
+    if (row >= 0) v = *reinterpret_cast<const uint4*>(w_qb + row * kQLora + col + 8 * j);
     *reinterpret_cast<uint4*>(out + tile * kWideBox + r * 128 + ((j ^ (r & 7)) << 4)) = v;
   }
 }
@@ -634,30 +677,57 @@ bool wide_kernel_fits(int ctas) {
   return clusters >= ctas / 2;
 }
 
-bool make_wide_split(int heads, int ctas, WideSplit* sp) {
-  const int pairs = ctas / 2;
-  if (pairs < 1 || ctas > kMaxCtas) return false;
+namespace {
+
+// Relative time of a single-head rope box (eight M = 64 MMAs on 16 KiB)
+// against a 128-row box (four M = 128 MMAs), as a fraction.
+constexpr int kSingleCostNum = 5, kSingleCostDen = 4;
+
+// Fills the split for one rope unit shape; returns the most loaded CTA's
+// estimated time in 128-row boxes x kSingleCostDen, or -1 if some pair would
+// get more than two heads.
+int64_t fill_wide_split(int heads, int pairs, int single, WideSplit* sp) {
+  sp->single = single;
   for (int c = 0; c <= pairs; ++c) sp->head[c] = (uint16_t)((int64_t)heads * c / pairs);
   for (int c = 0; c < pairs; ++c)
-    if (sp->head[c + 1] - sp->head[c] > 2) return false;
-  // ROPE units (two heads' rope rows, 192 KiB per CTA each) fill every pair
-  // up to an even share of the bytes; a head's NOPE + ABS units are 256 KiB
-  // per CTA (its nope rows' K half and its half of W_UK^T).
-  const int ropes = (heads + 1) / 2;
-  const int64_t hb = 16, rb = 12;  // in units of 16 KiB
+    if (sp->head[c + 1] - sp->head[c] > 2) return -1;
+  // ROPE units (two heads' rope rows, 12 boxes of 16 KiB per CTA, or one
+  // head's, 6 boxes) fill every pair up to an even share of the bytes; a
+  // head's NOPE + ABS units are 16 boxes per CTA (its nope rows' K half and
+  // its half of W_UK^T).
+  const int ropes = single ? heads : (heads + 1) / 2;
+  const int64_t hb = 16, rb = single ? kWideSingleBoxes : kWideAtoms;
   const int64_t total = (int64_t)heads * hb + (int64_t)ropes * rb;
-  int64_t head_bytes = 0;
+  int64_t head_bytes = 0, most = 0;
   int prev = 0;
   sp->rope[0] = 0;
   for (int c = 0; c < pairs; ++c) {
-    head_bytes += (int64_t)(sp->head[c + 1] - sp->head[c]) * hb;
+    const int nh = sp->head[c + 1] - sp->head[c];
+    head_bytes += (int64_t)nh * hb;
     int64_t r = (total * (c + 1) / pairs - head_bytes + rb / 2) / rb;
     if (r < prev) r = prev;
     if (r > ropes) r = ropes;
     if (c == pairs - 1) r = ropes;
     sp->rope[c + 1] = (uint16_t)r;
+    const int64_t cost = (int64_t)nh * hb * kSingleCostDen +
+                         (r - prev) * rb * (single ? kSingleCostNum : kSingleCostDen);
+    if (cost > most) most = cost;
     prev = (int)r;
   }
+  return most;
+}
+
+}  // namespace
+
+bool make_wide_split(int heads, int ctas, WideSplit* sp) {
+  const int pairs = ctas / 2;
+  sp->single = 0;
+  if (pairs < 1 || ctas > kMaxCtas) return false;
+  WideSplit one;
+  const int64_t two_cost = fill_wide_split(heads, pairs, 0, sp);
+  const int64_t one_cost = fill_wide_split(heads, pairs, 1, &one);
+  if (two_cost < 0) return false;
+  if (one_cost >= 0 && one_cost < two_cost) *sp = one;
   return true;
 }
 
@@ -667,8 +737,8 @@ size_t wide_qb_bytes(int heads) {
 size_t wide_ukt_bytes(int heads) { return (size_t)heads * 8 * kWideBox; }
 
 cudaError_t pack_wide_weights(const uint16_t* w_qb, const uint16_t* w_uk, uint8_t* qb_tiles,
-                              uint8_t* ukt_tiles, int heads, cudaStream_t stream) {
-  pack_wide_qb_kernel<<<512, 256, 0, stream>>>(w_qb, qb_tiles, heads);
+                              uint8_t* ukt_tiles, int heads, int single, cudaStream_t stream) {
+  pack_wide_qb_kernel<<<512, 256, 0, stream>>>(w_qb, qb_tiles, heads, single);
   pack_wide_ukt_kernel<<<512, 256, 0, stream>>>(w_uk, ukt_tiles, heads);
   return cudaGetLastError();
 }

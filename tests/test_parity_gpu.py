@@ -98,6 +98,24 @@ def test_ragged_batches(batch):
     assert_parity(inp)
 
 
+def test_empty_and_oversize_batches_write_nothing():
+    """An empty step (B = 0), a negative batch and one above MLA_MAX_BATCH
+    are host errors: the call returns MLA_EINVAL, launches nothing and leaves
+    every output and cache byte as it was; a valid call afterwards meets the
+    oracle."""
+    inp = S.make_inputs(batch=3, heads=4, layout=S.LAYOUT_E4M3, pages=4, seed=661)
+    step = DecodeStep(inp)
+    before = step.results()
+    for b in (0, -3, B.MLA_MAX_BATCH + 1):
+        assert step.decode(batch=b) == B.MLA_EINVAL, b
+    after = step.results()
+    for k in before:
+        assert np.array_equal(before[k], after[k]), k
+    assert step.error_flags() == 0
+    step.close()
+    assert_parity(inp)
+
+
 @pytest.mark.parametrize("heads", [1, 2, 3, 5, 127, 128])
 @pytest.mark.parametrize("batch", [1, 2, 16])
 def test_head_counts(heads, batch):
@@ -105,11 +123,12 @@ def test_head_counts(heads, batch):
     assert_parity(inp)
 
 
-@pytest.mark.parametrize("heads", [1, 3, 5, 127])
+@pytest.mark.parametrize("heads", [1, 3, 5, 61, 64, 113, 127])
 @pytest.mark.parametrize("batch", [24, 64])
 def test_wide_kernel_head_counts(heads, batch):
     """The wide tcgen05 kernel with odd head counts: pairs without a head, a
-    last two-head rope unit whose second head does not exist."""
+    last two-head rope unit whose second head does not exist; and head counts
+    whose split takes single-head rope units (64-row tiles: 61, 64, 113)."""
     inp = S.make_inputs(batch=batch, heads=heads, layout=S.LAYOUT_DS_MLA, pages=16,
                         seed=250 + heads + batch)
     assert_parity(inp)
