@@ -38,9 +38,9 @@ _CSRC = "mla_query_projection_gb300/csrc/"
 # they are unchanged.
 KERNEL_SOURCES = {
     "fused": [_CSRC + f for f in ("mla_common.cuh", "mla_device.cuh", "mla_internal.h",
-                                  "mla_fused.cu")],
+                                  "mla_fused.cu", "mla_split.cpp")],
     "wide": [_CSRC + f for f in ("mla_common.cuh", "mla_device.cuh", "mla_internal.h",
-                                 "mla_wide.cu")],
+                                 "mla_wide.cu", "mla_split.cpp")],
     "qkv_a": [_CSRC + f for f in ("mla_device.cuh", "mla_qkv_a.cu")],
 }
 

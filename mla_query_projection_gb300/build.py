@@ -54,7 +54,7 @@ def _compile(src: str) -> tuple[str, str]:
 def build(verbose: bool = False) -> str:
     """Compile and link; returns the path of the shared library."""
     os.makedirs(BUILD, exist_ok=True)
-    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
         results = list(ex.map(_compile, srcs))
     objs = [o for o, _ in results]

@@ -665,9 +665,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 // contiguous run of tasks and of rope rows, balanced in bytes on the host.
 // ===========================================================================
 
-constexpr int kTaskRows = 16;
-constexpr int kTasksPerHead = kNope / kTaskRows;              // 8
-constexpr int kTaskUkBytes = kTaskRows * kKvLora * 2;         // 16 KiB
 constexpr int kTaskQbBytes = kTaskRows * kPitch;              // 50176
 constexpr int kTaskStage = kTaskQbBytes + kTaskUkBytes;       // 66560
 constexpr int kAbsStages = 3;
@@ -1925,24 +1922,6 @@ cudaError_t repack_w_uk(const uint16_t* w_uk, uint8_t* dst, int heads, cudaStrea
   return cudaGetLastError();
 }
 
-void make_abs_split(int heads, int ctas, AbsSplit* sp) {
-  // tasks: even split; rope rows: fill each CTA up to an even share of bytes
-  const int64_t tasks = (int64_t)heads * kTasksPerHead, rope = (int64_t)heads * kRope;
-  const int64_t tb = kTaskRows * kRowBytes + kTaskUkBytes, rb = kRowBytes;
-  const int64_t total = tasks * tb + rope * rb;
-  int prev = 0;
-  for (int i = 0; i <= ctas; ++i) {
-    const int64_t t = tasks * i / ctas;
-    sp->task[i] = (uint16_t)t;
-    int64_t r = (total * i / ctas - t * tb + rb / 2) / rb;
-    if (r < prev) r = prev;
-    if (r > rope) r = rope;
-    if (i == ctas) r = rope;
-    sp->rope[i] = (uint16_t)r;
-    prev = (int)r;
-  }
-}
-
 template <int NT>
 cudaError_t launch_close(const DecodeArgs& a, int ctas, cudaStream_t stream) {
   const int items = a.batch * a.heads * (kKvLora / 4);
@@ -2007,31 +1986,6 @@ cudaError_t prepare_abs_mma() {
   static_assert(S::kAlloc <= 232448, "shared memory budget");
   return cudaFuncSetAttribute(mla_absorb_mma_kernel<NT>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, S::kAlloc);
-}
-
-bool make_pair_split(int heads, int ctas, PairSplit* sp) {
-  const int pairs = ctas / 2;
-  if (pairs < 1 || ctas > kMaxCtas) return false;
-  for (int c = 0; c <= pairs; ++c) sp->head[c] = (uint16_t)((int64_t)heads * c / pairs);
-  for (int c = 0; c < pairs; ++c)
-    if (sp->head[c + 1] - sp->head[c] > 2) return false;
-  // rope rows fill every CTA up to an even share of the bytes
-  const int64_t tb = (int64_t)4 * (kTaskRows * kRowBytes + kTaskUkBytes);  // one head's tasks
-  const int64_t rb = kRowBytes, rope = (int64_t)heads * kRope;
-  const int64_t total = (int64_t)heads * 2 * tb + rope * rb;
-  int64_t task_bytes = 0;
-  int prev = 0;
-  sp->rope[0] = 0;
-  for (int i = 0; i < ctas; ++i) {
-    task_bytes += (int64_t)(sp->head[i / 2 + 1] - sp->head[i / 2]) * tb;
-    int64_t r = (total * (i + 1) / ctas - task_bytes + rb / 2) / rb;
-    if (r < prev) r = prev;
-    if (r > rope) r = rope;
-    if (i == ctas - 1) r = rope;
-    sp->rope[i + 1] = (uint16_t)r;
-    prev = (int)r;
-  }
-  return true;
 }
 
 namespace {

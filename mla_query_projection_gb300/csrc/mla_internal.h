@@ -34,6 +34,20 @@ constexpr int kItemsPerHead = kUkUnitsPerHead + kRope;                       // 
 constexpr int64_t kItemBytesPerHead = (int64_t)kUkUnitsPerHead * kUkUnitBytes +
                                       (int64_t)kRope * kRowBytes;            // 327680
 
+// Tasks of the absorbing kernels: 16 nope rows of one head (their Q_B rows
+// and the matching W_UK rows).
+constexpr int kTaskRows = 16;
+constexpr int kTasksPerHead = kNope / kTaskRows;       // 8
+constexpr int kTaskUkBytes = kTaskRows * kKvLora * 2;  // 16 KiB
+
+// Units of the wide kernel in 16 KiB boxes per CTA of a pair: a head (its
+// nope rows' K half, 12 boxes, and its half of W_UK^T, 4), a two-head rope
+// unit (one box per 64-column K atom of a half), a single-head rope unit
+// (one box per two atoms).
+constexpr int kWideHeadBoxes = 16;
+constexpr int kWideRopeBoxes = 12;
+constexpr int kWideSingleBoxes = 6;
+
 struct DecodeArgs {
   const uint16_t* w_qb;      // [H*192][1536]
   // W_UK repacked as contiguous pre-swizzled 64-column units (see

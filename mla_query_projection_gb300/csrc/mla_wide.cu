@@ -53,7 +53,8 @@ constexpr int kWideTok = 64;                 // tokens per launch (N of the Q_B 
 constexpr int kWideHalfTok = 32;             // tokens each CTA of the pair finishes
 constexpr int kWideKHalf = kQLora / 2;       // 768
 constexpr int kWideAtoms = kWideKHalf / 64;  // 12 K atoms of 64 columns (128 B)
-constexpr int kWideSingleBoxes = kWideAtoms / 2;  // one head's rope rows: 6 boxes of 2 atoms
+static_assert(kWideAtoms == kWideRopeBoxes && kWideAtoms / 2 == kWideSingleBoxes,
+              "rope unit boxes");
 constexpr int kWideSlots = 5;
 constexpr int kWideBox = 128 * 128;          // one 128-row x 128 B box (16 KiB)
 constexpr int kWideThreads = 256;
@@ -675,60 +676,6 @@ bool wide_kernel_fits(int ctas) {
     return false;
   }
   return clusters >= ctas / 2;
-}
-
-namespace {
-
-// Relative time of a single-head rope box (eight M = 64 MMAs on 16 KiB)
-// against a 128-row box (four M = 128 MMAs), as a fraction.
-constexpr int kSingleCostNum = 5, kSingleCostDen = 4;
-
-// Fills the split for one rope unit shape; returns the most loaded CTA's
-// estimated time in 128-row boxes x kSingleCostDen, or -1 if some pair would
-// get more than two heads.
-int64_t fill_wide_split(int heads, int pairs, int single, WideSplit* sp) {
-  sp->single = single;
-  for (int c = 0; c <= pairs; ++c) sp->head[c] = (uint16_t)((int64_t)heads * c / pairs);
-  for (int c = 0; c < pairs; ++c)
-    if (sp->head[c + 1] - sp->head[c] > 2) return -1;
-  // ROPE units (two heads' rope rows, 12 boxes of 16 KiB per CTA, or one
-  // head's, 6 boxes) fill every pair up to an even share of the bytes; a
-  // head's NOPE + ABS units are 16 boxes per CTA (its nope rows' K half and
-  // its half of W_UK^T).
-  const int ropes = single ? heads : (heads + 1) / 2;
-  const int64_t hb = 16, rb = single ? kWideSingleBoxes : kWideAtoms;
-  const int64_t total = (int64_t)heads * hb + (int64_t)ropes * rb;
-  int64_t head_bytes = 0, most = 0;
-  int prev = 0;
-  sp->rope[0] = 0;
-  for (int c = 0; c < pairs; ++c) {
-    const int nh = sp->head[c + 1] - sp->head[c];
-    head_bytes += (int64_t)nh * hb;
-    int64_t r = (total * (c + 1) / pairs - head_bytes + rb / 2) / rb;
-    if (r < prev) r = prev;
-    if (r > ropes) r = ropes;
-    if (c == pairs - 1) r = ropes;
-    sp->rope[c + 1] = (uint16_t)r;
-    const int64_t cost = (int64_t)nh * hb * kSingleCostDen +
-                         (r - prev) * rb * (single ? kSingleCostNum : kSingleCostDen);
-    if (cost > most) most = cost;
-    prev = (int)r;
-  }
-  return most;
-}
-
-}  // namespace
-
-bool make_wide_split(int heads, int ctas, WideSplit* sp) {
-  const int pairs = ctas / 2;
-  sp->single = 0;
-  if (pairs < 1 || ctas > kMaxCtas) return false;
-  WideSplit one;
-  const int64_t two_cost = fill_wide_split(heads, pairs, 0, sp);
-  const int64_t one_cost = fill_wide_split(heads, pairs, 1, &one);
-  if (two_cost < 0) return false;
-  if (one_cost >= 0 && one_cost < two_cost) *sp = one;
-  return true;
 }
 
 size_t wide_qb_bytes(int heads) {

@@ -1,0 +1,37 @@
+// Prints the create-time work splits of mla_split.cpp for test_splits.py:
+// one line per (split, heads, CTAs), all integers.
+//   abs  H C  task[0..C] rope[0..C]
+//   pair H C ok  head[0..C/2] rope[0..C]
+//   wide H C ok single  head[0..C/2] rope[0..C/2]
+#include <cstdio>
+
+#include "mla_internal.h"
+#include "mla_query.h"
+
+int main() {
+  const int ctas_list[] = {2, 4, 6, 20, 132, 148, 150, 152, 256};
+  for (int ctas : ctas_list) {
+    const int pairs = ctas / 2;
+    for (int h = 1; h <= MLA_MAX_HEADS; ++h) {
+      static mla::AbsSplit as;
+      mla::make_abs_split(h, ctas, &as);
+      std::printf("abs %d %d", h, ctas);
+      for (int i = 0; i <= ctas; ++i) std::printf(" %d", as.task[i]);
+      for (int i = 0; i <= ctas; ++i) std::printf(" %d", as.rope[i]);
+      std::printf("\n");
+      static mla::PairSplit ps;
+      const bool pok = mla::make_pair_split(h, ctas, &ps);
+      std::printf("pair %d %d %d", h, ctas, pok ? 1 : 0);
+      for (int c = 0; c <= pairs; ++c) std::printf(" %d", pok ? ps.head[c] : 0);
+      for (int i = 0; i <= ctas; ++i) std::printf(" %d", pok ? ps.rope[i] : 0);
+      std::printf("\n");
+      static mla::WideSplit ws;
+      const bool wok = mla::make_wide_split(h, ctas, &ws);
+      std::printf("wide %d %d %d %d", h, ctas, wok ? 1 : 0, wok ? ws.single : 0);
+      for (int c = 0; c <= pairs; ++c) std::printf(" %d", wok ? ws.head[c] : 0);
+      for (int c = 0; c <= pairs; ++c) std::printf(" %d", wok ? ws.rope[c] : 0);
+      std::printf("\n");
+    }
+  }
+  return 0;
+}

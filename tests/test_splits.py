@@ -1,0 +1,110 @@
+"""Host logic: the create-time work splits of the absorbing kernels
+(mla_split.cpp), for every head count 1..128 and several CTA counts.
+
+A decode step (page "mla.query", class MlaQuery) streams each weight byte
+once, so it lasts as long as its most loaded CTA.  Each split must hand out
+every head, task and rope row exactly once, in contiguous runs, never give a
+cluster pair more than two heads, and keep every CTA within one rope unit of
+the larger of the even share and its own head or task bytes.  The splits are
+compiled from the library's source with a small driver (tests/split_driver.cpp);
+no GPU is needed."""
+
+import os
+import shutil
+import subprocess
+
+import pytest
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+CSRC = os.path.join(ROOT, "mla_query_projection_gb300", "csrc")
+CUDA_INC = "/usr/local/cuda/include"
+
+TASK = 16 * 1536 * 2 + 16 * 512 * 2  # one task: 16 Q_B rows and their 16 W_UK rows
+ROW = 1536 * 2                       # one rope row of W_QB
+HEAD_BOXES, ROPE_BOXES, SINGLE_BOXES = 16, 12, 6  # wide kernel, 16 KiB boxes per CTA
+
+
+@pytest.fixture(scope="module")
+def splits(tmp_path_factory):
+    cxx = shutil.which("g++")
+    if cxx is None or not os.path.exists(os.path.join(CUDA_INC, "cuda_runtime.h")):
+        pytest.skip("needs g++ and the CUDA headers")
+    exe = str(tmp_path_factory.mktemp("splits") / "split_driver")
+    subprocess.run([cxx, "-std=c++17", "-O1", "-I", CSRC, "-I", os.path.join(ROOT, "include"),
+                    "-I", CUDA_INC, os.path.join(HERE, "split_driver.cpp"),
+                    os.path.join(CSRC, "mla_split.cpp"), "-o", exe], check=True)
+    out = subprocess.run([exe], check=True, capture_output=True, text=True).stdout
+    rows = {"abs": [], "pair": [], "wide": []}
+    for line in out.splitlines():
+        f = line.split()
+        rows[f[0]].append((int(f[1]), int(f[2]), [int(x) for x in f[3:]]))
+    assert all(len(v) == 9 * 128 for v in rows.values())
+    return rows
+
+
+def runs(bounds, total):
+    """Contiguous runs [bounds[i], bounds[i+1]) covering [0, total) once."""
+    assert bounds[0] == 0 and bounds[-1] == total, (bounds[0], bounds[-1], total)
+    assert all(b <= c for b, c in zip(bounds, bounds[1:]))
+    return [c - b for b, c in zip(bounds, bounds[1:])]
+
+
+def test_absorbing_split(splits):
+    for heads, ctas, v in splits["abs"]:
+        tasks = runs(v[:ctas + 1], 8 * heads)
+        rope = runs(v[ctas + 1:], 64 * heads)
+        assert max(tasks) - min(tasks) <= 1, (heads, ctas)  # tasks evenly
+        mean = (8 * heads * TASK + 64 * heads * ROW) / ctas
+        for t, r in zip(tasks, rope):
+            assert t * TASK + r * ROW < max(mean, t * TASK) + ROW, (heads, ctas)
+
+
+def test_paired_split(splits):
+    for heads, ctas, v in splits["pair"]:
+        pairs = ctas // 2
+        ok, head, rope = v[0], v[1:pairs + 2], v[pairs + 2:]
+        # refused exactly when some pair would need a third head
+        assert ok == (heads <= 2 * pairs), (heads, ctas)
+        if not ok:
+            continue
+        nh = runs(head, heads)
+        assert max(nh) <= 2
+        rows = runs(rope, 64 * heads)
+        mean = (heads * 8 * TASK + 64 * heads * ROW) / ctas
+        for i, r in enumerate(rows):
+            own = nh[i // 2] * 4 * TASK  # each CTA takes 4 of a head's 8 tasks
+            assert own + r * ROW < max(mean, own) + ROW, (heads, ctas, i)
+
+
+def test_wide_split(splits):
+    for heads, ctas, v in splits["wide"]:
+        pairs = ctas // 2
+        ok, single, head, rope = v[0], v[1], v[2:pairs + 3], v[pairs + 3:]
+        assert ok == (heads <= 2 * pairs), (heads, ctas)
+        if not ok:
+            continue
+        nh = runs(head, heads)
+        assert max(nh) <= 2
+        ropes = heads if single else (heads + 1) // 2  # one head's or two heads' rope rows
+        units = runs(rope, ropes)
+        rb = SINGLE_BOXES if single else ROPE_BOXES
+        mean = (HEAD_BOXES * heads + rb * ropes) / pairs
+        for n, u in zip(nh, units):
+            own = n * HEAD_BOXES
+            assert own + u * rb < max(mean, own) + rb, (heads, ctas)
+
+
+def test_wide_split_shapes_on_76_pairs(splits):
+    """The cases the wide kernel's measurements rest on (152 CTAs): 64 heads
+    take single-head rope units (at most 22 boxes per CTA, against 28 with
+    two-head units); 127 and 128 heads keep two-head units (at most 44)."""
+    got = {h: v for h, c, v in splits["wide"] if c == 152}
+    for heads, single, most in ((64, 1, 22), (127, 0, 44), (128, 0, 44), (16, 0, 16)):
+        v = got[heads]
+        head, rope = v[2:79], v[79:]
+        nh = runs(head, heads)
+        units = runs(rope, heads if v[1] else (heads + 1) // 2)
+        rb = SINGLE_BOXES if v[1] else ROPE_BOXES
+        assert v[1] == single, heads
+        assert max(n * HEAD_BOXES + u * rb for n, u in zip(nh, units)) == most, heads
