@@ -73,11 +73,17 @@ HIDDEN = 7168
 E2M1_MAX = 6.0
 NVFP4_SCALE_FLOOR = 2.0**-9  # the smallest positive E4M3 value
 
-# Relative width of the rounding tie zone of the normalised q_a row: a bound on
-# the FP32 evaluation error of x * rr * gamma (a sum of squares over 8 + 5 + 6
-# additions, one division, one add, one reciprocal square root, two products:
-# under 20 roundings of 2**-24 each).
-XQ_TIE_REL = 2.0**-20
+# Relative width of the rounding tie zone of the normalised q_a row: a bound
+# on the FP32 evaluation error of x * rr * gamma over every way the row is
+# computed.  The sum of squares has positive terms, so a sum whose longest
+# path from a term to the result passes d roundings is within d * 2**-24 of
+# its value.  The longest such path: a 48-term FMA chain per lane (6 chunks of
+# 8 values), 2 shuffle additions over a lane quad, 7 additions over the 8
+# warps: d = 57.  Then the division by 1536 and the eps addition (2 more),
+# halved by the square root, plus the reciprocal square root and the two
+# products: (57 + 2) / 2 + 3 = 32.5 roundings of 2**-24.  33 * 2**-24 covers
+# it (second-order terms are below 2**-40).
+XQ_TIE_REL = 33 * 2.0**-24
 
 LAYOUT_E4M3 = 0
 LAYOUT_DS_MLA = 1

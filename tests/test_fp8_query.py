@@ -4,7 +4,11 @@ The FP8 variant runs the same kernels with a different epilogue (page
 "mla.query", method kernel: q_latent and q_pe stored as E4M3 codes of
 bf16(v) * q_scale_inv).  So its codes must equal, bit for bit, the oracle's
 FP8 conversion (query_fp8) applied to the same kernels' BF16 outputs, which are
-themselves checked against the oracle here.
+themselves checked against the oracle here; and they must meet the FP8 bar
+against the oracle's own FP8 outputs (at least 99.9% of codes identical, the
+rest within one code of the codes the oracle allows: its own, or for q_latent
+elements fed by a nope Q_B value of ambiguous rounding, the codes of that
+rounding's range).
 """
 
 import numpy as np
@@ -16,7 +20,7 @@ from mla_query_projection_gb300 import synthetic as S
 from mla_query_projection_gb300.runner import DecodeStep
 from oracle import mla_oracle as O
 
-from .parity_util import check_against_oracle
+from .parity_util import check_against_oracle, check_fp8_query, latent_slack
 
 pytestmark = pytest.mark.gpu
 
@@ -55,7 +59,7 @@ def test_fp8_query_codes_follow_the_bf16_outputs(batch, heads, layout, path):
     # BF16 run, checked against the oracle
     assert st.decode() == B.MLA_OK
     bf = st.results()
-    check_against_oracle(bf, inp)
+    ref = check_against_oracle(bf, inp)
     # FP8 run on the same inputs and a fresh copy of the cache
     dev = st.q_a.device
     qsi = torch.tensor([3.0], dtype=torch.float32, device=dev)
@@ -72,6 +76,13 @@ def test_fp8_query_codes_follow_the_bf16_outputs(batch, heads, layout, path):
     assert st.error_flags() == 0
     np.testing.assert_array_equal(ql8.cpu().numpy(), O.query_fp8(bf["q_latent"], 3.0))
     np.testing.assert_array_equal(qp8.cpu().numpy(), O.query_fp8(bf["q_pe"], 3.0))
+    # directly against the oracle's FP8 outputs (the oracle's step for the
+    # q_c rounding the GPU took, with q_scale_inv = 3)
+    rep = {}
+    check_fp8_query("q_latent_fp8", ql8.cpu().numpy(), ref["q_latent"], 3.0, rep,
+                    slack=latent_slack(ref, inp))
+    check_fp8_query("q_pe_fp8", qp8.cpu().numpy(), ref["q_pe"], 3.0, rep)
+    print(batch, heads, rep)
     np.testing.assert_array_equal(_bits(qc), bf["q_c"])
     np.testing.assert_array_equal(cache.cpu().numpy(), bf["cache"])
     st.close()

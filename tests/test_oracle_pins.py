@@ -280,6 +280,29 @@ def test_kv_row_per_tensor_worked():
     assert np.array_equal(out["cache"][other], inp["cache"][other])
 
 
+def test_kv_row_per_tensor_divides_by_k_scale():
+    """The per-tensor row divides by k_scale; multiplying by the binary32
+    reciprocal gives a different byte here.  k_scale = 7 and the value
+    91 * 2**-10 (BF16, seven significant bits): the quotient is exactly
+    13 * 2**-10 = 6.5 * 2**-9, halfway between the E4M3 subnormals 6 * 2**-9
+    (0x06) and 7 * 2**-9 (0x07); ties go to the even code, 0x06.  The binary32
+    reciprocal of 7 is 9586981 * 2**-26 > 1/7, so the product lands above the
+    midpoint and would round to 0x07.  With k_scale = 0.05 both forms give the
+    same bytes on every BF16 value, so the workloads' scale cannot tell them
+    apart; this case does."""
+    v = 91 * 2.0**-10
+    assert O.round_to_bf16(v) == v
+    assert np.float32(1.0) / np.float32(7.0) == np.float32(9586981 * 2.0**-26)
+    normed = np.full(512, v)
+    k_pe = np.full(64, -v)
+    row = O.kv_row_e4m3(normed, k_pe, 7.0)
+    assert np.all(row[:512] == 0x06)
+    assert np.all(row[512:] == 0x86)
+    # the other reading would have given 0x07: this pin tells the two apart
+    prod = float(np.float32(v) * (np.float32(1.0) / np.float32(7.0)))
+    assert O.e4m3_satfinite(prod) == 0x07
+
+
 def test_kv_row_ds_worked():
     # normed = 1.0 -> amax 1 -> 1/448 -> scale 2**-8; 1.0 * 256 -> E4M3 0x78;
     # scale bits 0x3B800000 little-endian; k_pe BF16 2.0 = 0x4000 little-endian.

@@ -286,3 +286,20 @@ def test_weights_bound_at_create_are_read_each_call():
     check_against_oracle(second, inp2)
     assert not np.array_equal(first["q_pe"], second["q_pe"])
     st.close()
+
+
+def test_per_tensor_insert_divides_by_k_scale():
+    """k_pe goes into the per-tensor row divided by k_scale, with no norm.
+    With k_scale = 7 and k_pe = 91 * 2**-10 the quotient 13 * 2**-10 is an
+    E4M3 tie that rounds to the even code 0x06; multiplying by the binary32
+    reciprocal of 7 would give 0x07.  The oracle pins the same case."""
+    inp = S.make_inputs(batch=2, heads=4, layout=S.LAYOUT_E4M3, pages=4, seed=1100)
+    v = O.f64_to_bf16_bits(np.array([91 * 2.0**-10, -91 * 2.0**-10]))
+    inp["k_pe"][0, :] = v[0]
+    inp["k_pe"][1, :] = v[1]
+    inp["k_scale"] = 7.0
+    out, ref = assert_parity(inp)
+    for b, want in ((0, 0x06), (1, 0x86)):
+        s = int(inp["slots"][b])
+        row = out["cache"][s // 64, s % 64]
+        assert np.all(row[512:] == want), (b, row[512:520])

@@ -55,7 +55,7 @@ def _run(w, x, x_pad=0, y_pad=0, repeat=1):
 
 def _check(y, w, x, report=None):
     ref, exact, cond = O.qkv_a_projection(x, w)
-    check_bf16("y", y, ref, cond, k_terms=w.shape[1], report=report)
+    check_bf16("y", y, ref, cond, report=report)
 
 
 @pytest.mark.parametrize(
