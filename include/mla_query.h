@@ -271,11 +271,17 @@ MLA_API int mla_query_path_for(mla_query_t h, int batch);
  *   batch         1 <= B <= MLA_NOALLOC_MAX_BATCH (64); a larger batch
  *                 returns MLA_EUNSUPPORTED; num_heads <= MLA_MAX_HEADS.
  *   device_flags  optional caller-owned device word (4-byte aligned) into
- *                 which the call ORs MLA_DEVERR_* bits; NULL to ignore them.
+ *                 which the call ORs MLA_DEVERR_* bits.  NULL discards them:
+ *                 a bad slot then goes unreported, and so does a hand-off
+ *                 wait that ran out (its CTAs wait on one another through
+ *                 global memory, for up to about a second when other work
+ *                 holds the SMs), after which q_latent is not valid.  Pass a
+ *                 word where the outputs must be trusted.
  *
  * The first call on a device sets that device up (looks up the array's
  * device address, opts the kernels into their shared memory); make that first
- * call before any stream capture.  Every call shares the one array, and each
+ * call before any stream capture.  The address is kept until the process
+ * exits: do not call this entry point on a device after cudaDeviceReset.  Every call shares the one array, and each
  * call clears its counters on `stream` before launching: calls that may
  * overlap on the GPU (different streams, or threads without ordering) race on
  * it and must not be issued; order them on one stream.

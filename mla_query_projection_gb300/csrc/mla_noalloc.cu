@@ -32,7 +32,10 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 // Per-device set-up, done by the first call on each device (with that device
 // current): the device address of the array and the kernels' shared-memory
 // opt-in.  In host code g_noalloc_scratch is only a stand-in symbol; the
-// kernel must be given the address cudaGetSymbolAddress returns.
+// kernel must be given the address cudaGetSymbolAddress returns.  The address
+// is kept for the life of the process, so the entry point must not be used
+// on a device after cudaDeviceReset (the module, and the array with it, would
+// be loaded again at another address).
 constexpr int kMaxDevices = 64;
 struct DeviceState {
   bool ready = false;
@@ -132,6 +135,11 @@ extern "C" MLA_API int mla_query_decode_noalloc(
   const bool mma = batch > 2;
   const int nt = mla::tokens_per_cta(batch, mma);
   const int groups = (batch + nt - 1) / nt;
+  // The kernel writes the q hand-off rows of every token slot of every group
+  // (padding slots past the batch included) and one counter per group and
+  // head: both must fit the array as sized above.
+  if (groups > (int)kMaxGroups || (int64_t)groups * nt > MLA_NOALLOC_MAX_BATCH)
+    return MLA_EUNSUPPORTED;
 
   CUtensorMap uk_map;
   if ((rc = encode_uk_map_noalloc(&uk_map, w_uk, num_heads)) != MLA_OK) return rc;
@@ -179,9 +187,10 @@ extern "C" MLA_API int mla_query_decode_noalloc(
   a.wide_ukt = nullptr;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // The array keeps the previous call's contents: the counters must start at
-  // zero (the q buffer is fully rewritten before it is read).
-  if (cudaMemsetAsync(base + 4, 0, kHeaderBytes - 4 + kReadyBytes, s) != cudaSuccess) {
+  // The array keeps the previous call's contents: the error word and the
+  // counters must start at zero (the q buffer is fully rewritten before it is
+  // read).
+  if (cudaMemsetAsync(base, 0, kHeaderBytes + kReadyBytes, s) != cudaSuccess) {
     cudaGetLastError();
     return MLA_ECUDA;
   }
