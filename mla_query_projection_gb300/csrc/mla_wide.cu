@@ -56,9 +56,20 @@ constexpr int kWideAtoms = kWideKHalf / 64;  // 12 K atoms of 64 columns (128 B)
 static_assert(kWideAtoms == kWideRopeBoxes && kWideAtoms / 2 == kWideSingleBoxes,
               "rope unit boxes");
 constexpr int kWideSlots = 5;
+// Boxes past the ring that a CTA prefetches into L2 when it starts, before
+// the programmatic-dependent-launch wait: the ring fills in about 2 us, and
+// the MMAs cannot start before the normalising kernel has run and xq has
+// landed, so without them the CTA's share of HBM would idle meanwhile.
+#ifndef MLA_WIDE_PREFETCH
+#define MLA_WIDE_PREFETCH 8
+#endif
+constexpr int kWidePrefetch = MLA_WIDE_PREFETCH;
 constexpr int kWideBox = 128 * 128;          // one 128-row x 128 B box (16 KiB)
 constexpr int kWideThreads = 256;
-constexpr int kWideTmemCols = 512;           // D_qb x2 (64 each) + D_abs x2 (4 x 32 each)
+// TMEM columns: Q_B tiles [2 buffers][2 K-quarter partials][64 tokens] at
+// 0..255, absorptions [2 heads][2 column tiles][64 tokens] at 256..511.
+constexpr int kWideTmemCols = 512;
+constexpr int kWideAbsCol = 256;
 
 enum WideUnit { kUnitNope = 0, kUnitAbs = 1, kUnitRope = 2 };
 
@@ -133,6 +144,16 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// The two K-quarter partials of a Q_B tile (columns c and c + 64), added in
+// FP32: first quarter first.
+__device__ __forceinline__ void tmem_ld_pair(uint32_t taddr, float (&v)[32]) {
+  float w[32];
+  tmem_ld32(taddr, v);
+  tmem_ld32(taddr + kWideTok, w);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __fadd_rn(v[j], w[j]);
 }
 
 // 1-D bulk copy from this CTA's shared memory to the shared memory of a CTA
@@ -269,32 +290,38 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   const uint32_t tmem = *tslot;
   bool timed_out = false;
 
-  if (warp == 0) {
-    // ================= producer: weight tiles, no PDL wait =============
+  if (warp == 0 || warp == 3) {
+    // ================= producers: weight tiles, no PDL wait ============
+    // Two issuing threads in different warps, boxes alternating between
+    // them: copies one thread issues complete one after another, and two
+    // issuers stream about 45 GB/s per SM against 35 for one (16 KiB
+    // copies, measured).  Box k goes to slot k % kWideSlots; its issuer
+    // waits for the consumption of box k - kWideSlots in that slot, which
+    // only box k's own issuer can be waiting for, so no slot runs more than
+    // one phase ahead of a wait on it.
     if (lane == 0) {
+      const int me = warp == 0 ? 0 : 1;
       const uint64_t pol = l2_policy_evict_first();
-      int slot = 0;
-      uint32_t phase = 0;  // parity of the slot's next empty phase to wait for
-      int k = 0;           // box counter over all units
+      int k = 0;  // box counter over all units
       for (int u = 0; u < nu; ++u) {
         const int kind = seq.kind(u), h = seq.head(u), nb = seq.boxes(u);
         for (int bx = 0; bx < nb; ++bx, ++k) {
-          if (k >= kWideSlots && !mbar_wait_bounded(&empty[slot], phase, kWaitLimit))
+          if ((k & 1) != me) continue;
+          const int slot = k % kWideSlots;
+          if (k >= kWideSlots &&
+              !mbar_wait_bounded(&empty[slot], (uint32_t)(((k / kWideSlots) - 1) & 1), kWaitLimit))
             timed_out = true;
           mbar_arrive_expect_tx(&full[slot], kWideBox);
           bulk_g2s_hint(smem + S::oRing + slot * kWideBox, wide_tile(a, kind, h, rank, bx, seq.single),
                         kWideBox, &full[slot], pol);
           if (bx == 0 && u < 4) trace_stamp(a, 24 + u);  // unit u's first box issued
-          if (++slot == kWideSlots) {
-            slot = 0;
-            if (k >= kWideSlots) phase ^= 1u;
-          }
         }
       }
-      // every issued box is consumed before the CTA may leave
+      // every box this thread issued is consumed before the CTA may leave
       for (int kk = k - kWideSlots > 0 ? k - kWideSlots : 0; kk < k; ++kk)
-        (void)mbar_wait_bounded(&empty[kk % kWideSlots], (uint32_t)((kk / kWideSlots) & 1),
-                                kWaitLimit);
+        if ((kk & 1) == me)
+          (void)mbar_wait_bounded(&empty[kk % kWideSlots], (uint32_t)((kk / kWideSlots) & 1),
+                                  kWaitLimit);
     }
   } else if (warp == 1) {
     // ================= MMA issuer ==================================
@@ -323,14 +350,19 @@ __global__ void __launch_bounds__(kWideThreads, 1)
               !mbar_wait_bounded(&absfree[na & 1], (uint32_t)(((na >> 1) - 1) & 1), kWaitLimit))
             timed_out = true;
           tc_fence_after();
-          dcol = 128 + 128 * (na & 1);
+          dcol = kWideAbsCol + 128 * (na & 1);
         } else {
           const int b = nq & 1;
           if (nq >= 2 && !mbar_wait_bounded(&dfree[b], (uint32_t)(((nq >> 1) - 1) & 1), kWaitLimit))
             timed_out = true;
           tc_fence_after();
-          dcol = 64 * b;
+          dcol = 128 * b;
         }
+        // A Q_B tile accumulates its K half in two partials (the first and
+        // the second half of its boxes, 24 k16 steps each), which the
+        // epilogue adds in FP32: the tensor core's accumulation error grows
+        // with the length of the chain.
+        const int half_nb = nb / 2;
         for (int bx = 0; bx < nb; ++bx) {
           if (!mbar_wait_bounded(&full[slot], fphase, kWaitLimit)) timed_out = true;
           tc_fence_after();
@@ -351,8 +383,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             const uint64_t db = dxq + (uint64_t)(2 * bx * ((kWideTok * 128) >> 4));
             const uint64_t da1 = da + (uint64_t)((64 * 128) >> 4);
             const uint64_t db1 = db + (uint64_t)((kWideTok * 128) >> 4);
-            const uint32_t dt = tmem + dcol;
-            umma(dt, da, db, idq64, (uint32_t)bx);
+            const uint32_t dt = tmem + dcol + kWideTok * (bx >= half_nb);
+            umma(dt, da, db, idq64, (uint32_t)(bx % half_nb));
             umma(dt, da + 2, db + 2, idq64, 1u);
             umma(dt, da + 4, db + 4, idq64, 1u);
             umma(dt, da + 6, db + 6, idq64, 1u);
@@ -362,8 +394,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             umma(dt, da1 + 6, db1 + 6, idq64, 1u);
           } else {
             const uint64_t db = dxq + (uint64_t)(bx * ((kWideTok * 128) >> 4));
-            const uint32_t dt = tmem + dcol;
-            umma(dt, da, db, idq, (uint32_t)bx);
+            const uint32_t dt = tmem + dcol + kWideTok * (bx >= half_nb);
+            umma(dt, da, db, idq, (uint32_t)(bx % half_nb));
             umma(dt, da + 2, db + 2, idq, 1u);
             umma(dt, da + 4, db + 4, idq, 1u);
             umma(dt, da + 6, db + 6, idq, 1u);
@@ -385,7 +417,17 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       }
     }
   } else {
-    // ================= warps 2-7: this K half of xq, then the epilogue ==
+    // ================= warps 2, 4-7: this K half of xq, then the epilogue
+    if (warp == 2 && lane == 0 && kWidePrefetch > 0) {
+      // the boxes just past the ring, into L2 (weights: no PDL wait)
+      int k = 0;
+      for (int u = 0; u < nu && k < kWideSlots + kWidePrefetch; ++u) {
+        const int kind = seq.kind(u), h = seq.head(u), nb = seq.boxes(u);
+        for (int bx = 0; bx < nb && k < kWideSlots + kWidePrefetch; ++bx, ++k)
+          if (k >= kWideSlots)
+            bulk_prefetch_l2(wide_tile(a, kind, h, rank, bx, seq.single), kWideBox);
+      }
+    }
     // The normalising kernel launched just before wrote xq in this tile's
     // layout; twelve bulk copies (one per 64-column atom) bring this half in.
     pdl_wait();
@@ -422,7 +464,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           for (int part = 0; part < 4; ++part) {
             const int ct = part >> 1, t0 = kWideHalfTok * (part & 1);
             float v[32];
-            tmem_ld32(tmem + lane_base + 128 + 128 * ab + kWideTok * ct + t0, v);
+            tmem_ld32(tmem + lane_base + kWideAbsCol + 128 * ab + kWideTok * ct + t0, v);
             const int nt_here = min(kWideHalfTok, a.batch - t0);
             if (nt_here > 0)
               put_q_run(a, a.q_latent,
@@ -441,7 +483,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         tc_fence_after();
         float q[kWideHalfTok];
         // the other CTA's tokens of this row go into its receive buffer b
-        tmem_ld32(tmem + lane_base + 64 * b + peer0, q);
+        tmem_ld_pair(tmem + lane_base + 128 * b + peer0, q);
         // the other CTA has read what this one sent for the previous tile
         if (nq >= 1 && !mbar_wait_bounded(sendok, (uint32_t)((nq - 1) & 1), kWaitLimit))
           timed_out = true;
@@ -457,7 +499,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                         q[4 * c + 2], q[4 * c + 3], rb);
         }
         // this CTA's tokens: its K half plus the other CTA's, K 0..767 first
-        tmem_ld32(tmem + lane_base + 64 * b + my0, q);
+        tmem_ld_pair(tmem + lane_base + 128 * b + my0, q);
         tc_fence_before();
         mbar_arrive(&dfree[b]);
         if (!mbar_wait_bounded(recvfull, (uint32_t)(nq & 1), kWaitLimit)) timed_out = true;
