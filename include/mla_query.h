@@ -93,13 +93,12 @@ typedef struct mla_query* mla_query_t;
  *   eps       RMSNorm epsilon used by both norms.
  *
  * W_QB, W_UK and the gammas are borrowed: they must stay valid and unchanged
- * until mla_query_destroy.  Batches of up to 32 tokens read W_QB, W_UK and
- * the gammas in place.  create also copies the weights once into
- * library-owned tiled layouts - W_UK in contiguous 64-column units (H * 128
- * KiB) for the allocation-free hand-off path, and W_QB (H * 576 KiB) and
- * W_UK^T (H * 128 KiB) in swizzled 16 KiB tiles for batches above 32 - so a
- * changed weight would be seen by some batch sizes and not by others (create
- * a new handle instead).  create allocates those copies and the handle's
+ * until mla_query_destroy.  Batches of up to 16 tokens read W_QB, W_UK and
+ * the gammas in place at every call.  Batches above 16 run the wide kernel,
+ * which reads copies of W_QB (H * 576 KiB) and W_UK^T (H * 128 KiB) that
+ * create makes once, in swizzled 16 KiB tiles; they read only the gammas in
+ * place.  So a weight changed after create is seen by batches of up to 16
+ * tokens and not by larger ones: create a new handle to change weights.  create allocates those copies and the handle's
  * device scratch (partials, counters, error flag) with cudaMalloc on the
  * current device, and synchronises the legacy default stream; the handle may
  * only be used on that device.

@@ -303,3 +303,25 @@ def test_per_tensor_insert_divides_by_k_scale():
         s = int(inp["slots"][b])
         row = out["cache"][s // 64, s % 64]
         assert np.all(row[512:] == want), (b, row[512:520])
+
+
+def test_batches_above_16_read_the_create_time_copy():
+    """Batches above 16 tokens run the wide kernel, which reads the W_QB and
+    W_UK^T tiles copied at create: changing W_QB in place afterwards leaves
+    their results as they were (still the oracle's for the weights at create),
+    while a batch of up to 16 tokens reads the changed W_QB."""
+    inp = S.make_inputs(batch=24, heads=8, layout=S.LAYOUT_E4M3, pages=8, seed=1010)
+    st = DecodeStep(inp)
+    assert B.mla_query_kernel_for(st.handle, 24) == "mla_wide_norm_kernel+mla_wide_kernel"
+    assert st.decode() == B.MLA_OK
+    first = st.results()
+    check_against_oracle(first, inp)
+    st.w_qb.mul_(2.0)
+    assert st.decode() == B.MLA_OK
+    second = st.results()
+    for k in ("q_latent", "q_pe", "q_c"):
+        assert np.array_equal(first[k], second[k]), k
+    assert st.decode(batch=4) == B.MLA_OK  # four tokens: W_QB read in place
+    small = st.results()
+    assert not np.array_equal(small["q_pe"][:4], first["q_pe"][:4])
+    st.close()
