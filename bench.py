@@ -47,6 +47,8 @@ KERNEL_SOURCES = {
     "wide": [_CSRC + f for f in ("mla_common.cuh", "mla_device.cuh", "mla_internal.h",
                                  "mla_wide.cu", "mla_split.cpp")],
     "qkv_a": [_CSRC + f for f in ("mla_device.cuh", "mla_qkv_a.cu")],
+    "small": [_CSRC + f for f in ("mla_common.cuh", "mla_device.cuh", "mla_internal.h",
+                                  "mla_small.cu", "mla_split.cpp")],
 }
 
 
@@ -54,7 +56,8 @@ def kernel_sources(kernel: str) -> list[str]:
     """Source files of the kernel(s) named ("a+b" for a chain of launches)."""
     out = []
     for k in kernel.split("+"):
-        fam = "qkv_a" if "qkv_a" in k else "wide" if "wide" in k else "fused"
+        fam = ("qkv_a" if "qkv_a" in k else "wide" if "wide" in k
+               else "small" if "small" in k else "fused")
         out += [f for f in KERNEL_SOURCES[fam] if f not in out]
     return out
 

@@ -70,8 +70,11 @@ extern "C" {
                                   that call are not valid)                     */
 
 /* Compute paths (mla_query_set_path). */
-#define MLA_PATH_AUTO 0 /* the default: MLA_PATH_MMA at every batch size    */
-#define MLA_PATH_FMA 1  /* FP32 FMA dot products (batch <= 2 only)           */
+#define MLA_PATH_AUTO 0 /* the default: MLA_PATH_MMA at every batch size
+                           (measured faster than the FMA kernel from one
+                           token on)                                       */
+#define MLA_PATH_FMA 1  /* FP32 FMA dot products: the small-batch kernel
+                           (batch <= 2 only; MLA_EUNSUPPORTED above)       */
 #define MLA_PATH_MMA 2  /* BF16 tensor-core tiles, FP32 accumulate           */
 
 #define MLA_MAX_BATCH 256 /* largest batch one decode call accepts           */
@@ -98,10 +101,18 @@ typedef struct mla_query* mla_query_t;
  * which reads copies of W_QB (H * 576 KiB) and W_UK^T (H * 128 KiB) that
  * create makes once, in swizzled 16 KiB tiles; they read only the gammas in
  * place.  So a weight changed after create is seen by batches of up to 16
- * tokens and not by larger ones: create a new handle to change weights.  create allocates those copies and the handle's
- * device scratch (partials, counters, error flag) with cudaMalloc on the
- * current device, and synchronises the legacy default stream; the handle may
- * only be used on that device.
+ * tokens and not by larger ones: create a new handle to change weights.
+ *
+ * Device memory: create allocates, with cudaMalloc on the current device,
+ * only what the kernels its dispatch can reach need for this head count on
+ * this device: the error flag and counters (under 20 KiB); the wide kernel's
+ * weight tiles (H * 704 KiB) and normalised-row buffer (192 KiB); where the
+ * paired kernel cannot serve every batch of up to 16 tokens (small head
+ * counts), the partials kernel's FP32 buffer (H * 256 KiB); and only on a
+ * device where neither the wide nor the 16-token paired kernel can run, the
+ * hand-off kernel's packed W_UK (H * 128 KiB) and q buffer.  On a GB300 at
+ * 64 or 128 heads that is the wide tiles and 192 KiB.  create synchronises
+ * the legacy default stream; the handle may only be used on that device.
  * Returns MLA_OK, MLA_EINVAL, MLA_ENOMEM or MLA_ECUDA.
  */
 MLA_API int mla_query_create(mla_query_t* out, int num_heads, const void* w_qb,

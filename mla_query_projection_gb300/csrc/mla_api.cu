@@ -1,6 +1,7 @@
 // mla_api.cu - the C ABI (include/mla_query.h): argument checks, the handle
 // with its device scratch, the W_UK tensor map, and path dispatch.
 #include <cudaTypedefs.h>
+#include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -35,6 +36,8 @@ struct mla_query {
   uint8_t* wide_xq;           // wide kernel: normalised xq in tile layout
   mla::WideSplit wide_split;  // per-pair heads and rope units
   int wide_ctas;              // its grid (even), 0 if it cannot run on this device
+  mla::SmallSplit small_split;  // small-batch FMA kernel: cluster size, heads, rope rows
+  int small_ctas;               // its grid, 0 if it cannot run on this device
 };
 
 namespace {
@@ -73,14 +76,20 @@ int encode_uk_map(CUtensorMap* map, const void* w_uk, int heads) {
 //   absorbing kernel, FP32 FMA flavour (1 or 2 tokens per CTA);
 //   absorbing kernel, tensor-core flavour (8 or 16 tokens per CTA, B <= 16);
 //   hand-off kernel, tensor cores, token groups of 8 or 16 (any B).
-enum class Kernel { kAbsorbFma, kAbsorbMma, kAbsorbPair, kWide, kHandoff };
+enum class Kernel { kSmall, kAbsorbMma, kAbsorbPair, kWide, kHandoff };
 
+// The default path takes tensor cores from one token on: measured on GB300
+// against the FP32-FMA small-batch kernel (B = 1: 8.19 against 10.6 us at 64
+// heads, 14.7 against 17.2 at 128, 5.43 against 5.56 at 16; B = 2: 8.19
+// against 14.1 us at 64 heads).  Both paths stream every weight byte once;
+// after the programmatic-dependent-launch wait a step is bound by its
+// consumers, and the per-row FMA work there is slower than the MMA tiles.
 int pick_kernel(const mla_query* h, int batch, Kernel* k, int* nt) {
   int path = h->path;
-  if (path == MLA_PATH_AUTO) path = MLA_PATH_MMA;  // tensor cores are faster from one token on
+  if (path == MLA_PATH_AUTO) path = MLA_PATH_MMA;
   if (path == MLA_PATH_FMA) {
-    if (batch > 2) return MLA_EUNSUPPORTED;
-    *k = Kernel::kAbsorbFma;
+    if (batch > 2 || h->small_ctas == 0) return MLA_EUNSUPPORTED;
+    *k = Kernel::kSmall;
     *nt = batch <= 1 ? 1 : 2;
   } else if (path == MLA_PATH_MMA) {
     if (batch <= 8 && h->pair_ctas > 0) {
@@ -148,29 +157,40 @@ int mla_query_create(mla_query_t* out, int num_heads, const void* w_qb, const vo
   if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) !=
       cudaSuccess)
     goto fail;
-  if (mla::prepare_fused_kernels() != cudaSuccess) goto fail;
+  if (mla::prepare_fused_kernels() != cudaSuccess || mla::prepare_small_kernels() != cudaSuccess)
+    goto fail;
   if ((rc = encode_uk_map(&h->uk_map, w_uk, num_heads)) != MLA_OK) goto fail;
-  {
-    const size_t head = 256;  // err, finished
-    const size_t ready_bytes = mla::scratch_ready_elems(num_heads) * sizeof(uint32_t);
-    const size_t qn_off = head + ((ready_bytes + 255) / 256) * 256;
-    const size_t bytes = qn_off + mla::scratch_qn_elems(num_heads) * sizeof(uint16_t);
-    if (cudaMalloc(&h->scratch, bytes) != cudaSuccess) {
-      rc = MLA_ENOMEM;
-      goto fail;
-    }
-    if (cudaMemset(h->scratch, 0, bytes) != cudaSuccess) goto fail;
-    uint8_t* base = static_cast<uint8_t*>(h->scratch);
-    h->err = reinterpret_cast<uint32_t*>(base);
-    h->finished = reinterpret_cast<uint32_t*>(base + 4);
-    h->ready = reinterpret_cast<uint32_t*>(base + head);
-    h->qn = reinterpret_cast<uint16_t*>(base + qn_off);
-  }
   if (h->num_sms > mla::kMaxCtas) {
     rc = MLA_EUNSUPPORTED;
     goto fail;
   }
   mla::make_abs_split(num_heads, h->num_sms, &h->split);
+  // The small-batch FMA kernel: the cluster size whose split puts the fewest
+  // bytes on the most loaded CTA.
+  // Each grid is sized so that all its clusters can be resident at once
+  // (the occupancy counts both CTAs an SM can hold; a grid takes at most one
+  // CTA per SM, leaving the other slot to the next step).
+  {
+    int most[3];
+    for (int k = 0; k < 3; ++k) {
+      const int c = 2 << k;
+      const int m1 = mla::small_kernel_max_clusters(c, 1), m2 = mla::small_kernel_max_clusters(c, 2);
+      most[k] = m1 < m2 ? m1 : m2;
+      if (most[k] <= 0) most[k] = -1;  // cannot run: no cluster of this size
+    }
+    h->small_ctas = 0;
+    mla::SmallSplit trial;
+    trial.cluster = 0;
+    const int ctas = mla::choose_small_split(num_heads, h->num_sms, most, &trial);
+    if (ctas > 0) {
+      h->small_split = trial;
+      h->small_ctas = ctas;
+    }
+#ifdef MLA_DEBUG_SPLIT
+    fprintf(stderr, "small split: heads %d sms %d max clusters %d %d %d -> ctas %d cluster %d\n",
+            num_heads, h->num_sms, most[0], most[1], most[2], h->small_ctas, trial.cluster);
+#endif
+  }
   // The paired kernel gives each CTA whole half-heads (256 KiB of weights per
   // head); it is used only where that keeps the CTAs balanced, i.e. no CTA
   // holds more than 10% above the average bytes per CTA.
@@ -185,41 +205,68 @@ int mla_query_create(mla_query_t* out, int num_heads, const void* w_qb, const vo
       h->pair_ctas = 0;
     h->pair16 = h->pair_ctas > 0 && mla::pair_kernel_fits(h->pair_ctas, 16);
   }
-  // FP32 partial absorptions of the absorbing kernels: [task][token < 16][512]
-  if (cudaMalloc(&h->partial, (size_t)num_heads * 8 * 16 * mla::kKvLora * sizeof(float)) !=
-      cudaSuccess) {
-    rc = MLA_ENOMEM;
-    goto fail;
-  }
-  // W_UK copy in contiguous pre-swizzled units (one 1-D bulk copy per unit).
-  if (cudaMalloc(&h->w_uk_packed, (size_t)num_heads * mla::kUkUnitsPerHead * mla::kUkUnitBytes) !=
-      cudaSuccess) {
-    rc = MLA_ENOMEM;
-    goto fail;
-  }
-  if (mla::repack_w_uk(h->w_uk, h->w_uk_packed, num_heads, 0) != cudaSuccess ||
-      cudaStreamSynchronize(0) != cudaSuccess)
-    goto fail;
-  // Wide kernel (17 tokens and more): W_UK^T copy, tensor maps, pair split.
-  if (cudaMalloc(&h->wide_xq, mla::wide_xq_bytes()) != cudaSuccess) {
-    rc = MLA_ENOMEM;
-    goto fail;
-  }
-  if (cudaMalloc(&h->wide_qb, mla::wide_qb_bytes(num_heads)) != cudaSuccess ||
-      cudaMalloc(&h->wide_ukt, mla::wide_ukt_bytes(num_heads)) != cudaSuccess) {
-    rc = MLA_ENOMEM;
-    goto fail;
-  }
+  // Wide kernel (17 tokens and more): its split decides the rope tiles' shape.
   if (mla::prepare_wide_kernel() != cudaSuccess) goto fail;
-  // the split decides the rope tiles' shape, so it comes before the packing
   h->wide_ctas = h->num_sms & ~1;
   if (!mla::make_wide_split(num_heads, h->wide_ctas, &h->wide_split) ||
       !mla::wide_kernel_fits(h->wide_ctas))
     h->wide_ctas = 0;
-  if (mla::pack_wide_weights(h->w_qb, h->w_uk, h->wide_qb, h->wide_ukt, num_heads,
-                             h->wide_split.single, 0) != cudaSuccess ||
-      cudaStreamSynchronize(0) != cudaSuccess)
-    goto fail;
+  {
+    // Device memory for the kernels the dispatch can reach with this head
+    // count on this device, and nothing else: the partials kernel where the
+    // paired kernel cannot serve every batch of up to 16 tokens, the wide
+    // kernel's tiled weight copies where it runs, and the hand-off kernel's
+    // packed W_UK and q buffer only where neither the wide nor the 16-token
+    // paired kernel covers batches above 16.
+    const bool partials = h->pair_ctas == 0 || !h->pair16;
+    const bool handoff = h->wide_ctas == 0 && !(h->pair_ctas > 0 && h->pair16);
+    const bool wide = h->wide_ctas > 0;
+    const size_t head = 256;  // err, finished
+    const size_t ready_bytes = mla::scratch_ready_elems(num_heads) * sizeof(uint32_t);
+    const size_t qn_off = head + ((ready_bytes + 255) / 256) * 256;
+    const size_t bytes =
+        qn_off + (handoff ? mla::scratch_qn_elems(num_heads) * sizeof(uint16_t) : 0);
+    if (cudaMalloc(&h->scratch, bytes) != cudaSuccess) {
+      rc = MLA_ENOMEM;
+      goto fail;
+    }
+    if (cudaMemset(h->scratch, 0, bytes) != cudaSuccess) goto fail;
+    uint8_t* base = static_cast<uint8_t*>(h->scratch);
+    h->err = reinterpret_cast<uint32_t*>(base);
+    h->finished = reinterpret_cast<uint32_t*>(base + 4);
+    h->ready = reinterpret_cast<uint32_t*>(base + head);
+    h->qn = handoff ? reinterpret_cast<uint16_t*>(base + qn_off) : nullptr;
+    // FP32 partial absorptions of the partials kernel: [task][token < 16][512]
+    if (partials &&
+        cudaMalloc(&h->partial, (size_t)num_heads * 8 * 16 * mla::kKvLora * sizeof(float)) !=
+            cudaSuccess) {
+      rc = MLA_ENOMEM;
+      goto fail;
+    }
+    // W_UK copy in contiguous pre-swizzled units (one 1-D bulk copy per unit)
+    if (handoff) {
+      if (cudaMalloc(&h->w_uk_packed,
+                     (size_t)num_heads * mla::kUkUnitsPerHead * mla::kUkUnitBytes) != cudaSuccess) {
+        rc = MLA_ENOMEM;
+        goto fail;
+      }
+      if (mla::repack_w_uk(h->w_uk, h->w_uk_packed, num_heads, 0) != cudaSuccess ||
+          cudaStreamSynchronize(0) != cudaSuccess)
+        goto fail;
+    }
+    if (wide) {
+      if (cudaMalloc(&h->wide_xq, mla::wide_xq_bytes()) != cudaSuccess ||
+          cudaMalloc(&h->wide_qb, mla::wide_qb_bytes(num_heads)) != cudaSuccess ||
+          cudaMalloc(&h->wide_ukt, mla::wide_ukt_bytes(num_heads)) != cudaSuccess) {
+        rc = MLA_ENOMEM;
+        goto fail;
+      }
+      if (mla::pack_wide_weights(h->w_qb, h->w_uk, h->wide_qb, h->wide_ukt, num_heads,
+                                 h->wide_split.single, 0) != cudaSuccess ||
+          cudaStreamSynchronize(0) != cudaSuccess)
+        goto fail;
+    }
+  }
 #ifdef MLA_TRACE
   {
     const size_t tb = (size_t)h->num_sms * mla::kTraceSlots * 8;
@@ -282,7 +329,7 @@ int decode_impl(mla_query_t h, int batch, const void* q_a, int64_t q_a_stride, c
       (reinterpret_cast<uintptr_t>(q_scale_inv) & 3u))
     return MLA_EINVAL;
 
-  Kernel kern = Kernel::kAbsorbFma;
+  Kernel kern = Kernel::kSmall;
   int nt = 1;
   int rc = pick_kernel(h, batch, &kern, &nt);
   if (rc != MLA_OK) return rc;
@@ -337,7 +384,9 @@ int decode_impl(mla_query_t h, int batch, const void* q_a, int64_t q_a_stride, c
   // bytes per q_latent / q_pe element: BF16, or E4M3 with the FP8 query
   const int64_t qbytes = q_scale_inv != nullptr ? 1 : 2;
   cudaError_t e;
-  if (kern == Kernel::kHandoff)
+  if (kern == Kernel::kSmall)
+    e = mla::launch_small(a, h->small_split, h->small_ctas, nt, st);
+  else if (kern == Kernel::kHandoff)
     e = mla::launch_fused(a, &h->uk_map, nt, true, h->num_sms, st);
   else if (kern == Kernel::kWide) {
     // one launch per slice of 64 tokens, every per-token pointer offset
@@ -485,21 +534,26 @@ int mla_query_set_path(mla_query_t h, int path) {
 
 int mla_query_path_for(mla_query_t h, int batch) {
   if (h == nullptr || batch < 1 || batch > MLA_MAX_BATCH) return MLA_EINVAL;
-  Kernel kern = Kernel::kAbsorbFma;
+  Kernel kern = Kernel::kSmall;
   int nt = 1;
   int rc = pick_kernel(h, batch, &kern, &nt);
   if (rc != MLA_OK) return rc;
-  return kern == Kernel::kAbsorbFma ? MLA_PATH_FMA : MLA_PATH_MMA;
+  return kern == Kernel::kSmall ? MLA_PATH_FMA : MLA_PATH_MMA;
 }
 
 const char* mla_query_kernel_for(mla_query_t h, int batch) {
   if (h == nullptr || batch < 1 || batch > MLA_MAX_BATCH) return nullptr;
-  Kernel kern = Kernel::kAbsorbFma;
+  Kernel kern = Kernel::kSmall;
   int nt = 1;
   if (pick_kernel(h, batch, &kern, &nt) != MLA_OK) return nullptr;
   switch (kern) {
-    case Kernel::kAbsorbFma: return nt == 1 ? "mla_absorb_kernel<1>+mla_close_kernel<1>"
-                                            : "mla_absorb_kernel<2>+mla_close_kernel<2>";
+    case Kernel::kSmall: {
+      static const char* names[2][3] = {
+          {"mla_small_kernel<1,2>", "mla_small_kernel<1,4>", "mla_small_kernel<1,8>"},
+          {"mla_small_kernel<2,2>", "mla_small_kernel<2,4>", "mla_small_kernel<2,8>"}};
+      const int c = h->small_split.cluster;
+      return names[nt - 1][c == 2 ? 0 : c == 4 ? 1 : 2];
+    }
     case Kernel::kAbsorbMma: return nt == 8 ? "mla_absorb_mma_kernel<8>" : "mla_absorb_mma_kernel<16>";
     case Kernel::kAbsorbPair: return nt == 8 ? "mla_absorb_pair_kernel<8>" : "mla_absorb_pair_kernel<16>";
     case Kernel::kWide: return "mla_wide_norm_kernel+mla_wide_kernel";

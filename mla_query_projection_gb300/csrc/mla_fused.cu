@@ -653,20 +653,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ===========================================================================
-// Absorbing kernel (1-2 tokens): no hand-off between CTAs.
+// Absorbing kernels: tasks, with no hand-off between CTAs.
 //
 // A "task" is 16 consecutive nope rows of one head (48 KiB of W_QB) together
 // with the same 16 rows of that head's W_UK (16 KiB, contiguous in the
 // caller's [H][128][512] layout).  The CTA computes the 16 BF16 q values, then
 // their contribution to all 512 latent columns, and stores that FP32 partial
-// sum.  A per-head counter finds the last of a head's 8 tasks; that CTA's
-// finisher warp adds the 8 partials in task order and writes q_latent.  Rope
-// rows stream after a CTA's tasks and go straight to q_pe.  Each CTA owns a
-// contiguous run of tasks and of rope rows, balanced in bytes on the host.
+// sum.  A per-head counter finds the last of a head's 8 tasks; that CTA adds
+// the 8 partials in task order and writes q_latent.  Rope rows stream after a
+// CTA's tasks and go straight to q_pe.  Each CTA owns a contiguous run of
+// tasks and of rope rows, balanced in bytes on the host.
 // ===========================================================================
 
 constexpr int kTaskQbBytes = kTaskRows * kPitch;              // 50176
-constexpr int kTaskStage = kTaskQbBytes + kTaskUkBytes;       // 66560
 constexpr int kAbsStages = 3;
 constexpr int kAbsThreads = kConsumers + 32;                  // + producer warp
 // The 16-token paired kernel has a KV insert warp besides: its consumers'
@@ -676,19 +675,6 @@ template <int NT>
 constexpr int pair_threads() {
   return NT == 16 ? kAbsThreads + 32 : kAbsThreads;
 }
-
-template <int NT>
-struct AbsSmem {
-  static constexpr int kRing = kAbsStages * kTaskStage;
-  static constexpr int oXq = kRing;
-  static constexpr int oQ16 = oXq + NT * kPitch;                 // [2][NT][16] FP32
-  static constexpr int oSs = oQ16 + 2 * NT * kTaskRows * 4;      // [NT][8] + [8]
-  static constexpr int oFull = oSs + (NT * 8 + 8) * 4;
-  static constexpr int oEmpty = oFull + kAbsStages * 8;
-  static constexpr int oQbar = oEmpty + kAbsStages * 8;
-  static constexpr int kBytes = oQbar + 8;
-  static constexpr int kAlloc = kBytes + 128;
-};
 
 // This CTA's stages: tasks [t0, t1), then rope rows [r0, r1) in chunks of 16.
 struct AbsSeq {
@@ -754,281 +740,11 @@ __device__ __forceinline__ void close_item(const DecodeArgs& a, int h, int t, in
   }
 }
 
-// Head closing of the FP32-FMA absorbing kernel, launched right after it
-// (its CTAs may be resident early and wait, programmatic dependent launch).
-// One thread per (token, head, 4 columns).
-template <int NT>
-__global__ void __launch_bounds__(256) mla_close_kernel(const DecodeArgs a) {
-  // The next kernel may be scheduled at once (it streams static weights
-  // until its own wait, which covers this kernel's completion).
-  pdl_launch_dependents();
-  pdl_wait();  // the partials of the absorbing kernel
-  const int per_tok = a.heads * (kKvLora / 4);
-  const int items = a.batch * per_tok;
-  for (int it = blockIdx.x * blockDim.x + threadIdx.x; it < items; it += gridDim.x * blockDim.x) {
-    const int t = it / per_tok, r = it % per_tok;
-    close_item<NT>(a, r / (kKvLora / 4), t, r % (kKvLora / 4));
-  }
-}
-
-template <int NT>
-__global__ void __launch_bounds__(kAbsThreads, 1)
-    mla_absorb_kernel(const DecodeArgs a, const __grid_constant__ AbsSplit split) {
-  using S = AbsSmem<NT>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
-                                             ~static_cast<uintptr_t>(127));
-  uint8_t* ring = smem;
-  uint8_t* xq = smem + S::oXq;
-  float* q16 = reinterpret_cast<float*>(smem + S::oQ16);
-  float* ss_part = reinterpret_cast<float*>(smem + S::oSs);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::oFull);
-  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + S::oEmpty);
-  uint64_t* qbar = reinterpret_cast<uint64_t*>(smem + S::oQbar);
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int i = blockIdx.x, P = gridDim.x;
-  const AbsSeq seq{split.task[i], split.task[i + 1], split.rope[i], split.rope[i + 1]};
-  const int nst = seq.stages();
-
-  if (tid == 0) {
-    for (int s = 0; s < kAbsStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
-    }
-    mbar_init(qbar, kConsumerWarps);
-    mbar_fence_init();
-    pdl_launch_dependents();  // the head-closing kernel may be scheduled now
-    trace_stamp(a, 0);
-  }
-  __syncthreads();
-  bool timed_out = false;
-
-  if (warp == kConsumerWarps) {
-    // ================= producer: weights only, no PDL wait ============
-    // The first ring's worth of stages goes straight to shared memory; every
-    // later stage is prefetched into L2 at once, so HBM keeps streaming this
-    // CTA's weights while the ring is full (waiting for the previous kernel,
-    // the norm prologue).  Copies out of L2 mark their lines evict-first.
-    const uint64_t pol = l2_policy_evict_first();
-    for (int k = 0; k < nst; ++k) {
-      if (k == kAbsStages) {
-        for (int kk = kAbsStages + lane; kk < nst; kk += 32) abs_prefetch_stage(a, seq, kk);
-        __syncwarp();
-      }
-      const int slot = k % kAbsStages;
-      uint8_t* buf = ring + slot * kTaskStage;
-      if (k >= kAbsStages) {
-        int ok = 1;
-        if (lane == 0)
-          ok = mbar_wait_bounded(&empty[slot], (uint32_t)(((k / kAbsStages) - 1) & 1), kWaitLimit)
-                   ? 1 : 0;
-        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) timed_out = true;
-      }
-      if (lane == 0 && k < 20) trace_stamp(a, 28 + k);
-      if (k < seq.tasks()) {
-        const int tk = seq.t0 + k, h = tk / kTasksPerHead, p0 = (tk % kTasksPerHead) * kTaskRows;
-        if (lane == 0) mbar_arrive_expect_tx(&full[slot], kTaskRows * kRowBytes + kTaskUkBytes);
-        __syncwarp();
-        if (lane < kTaskRows)
-          bulk_g2s_hint(buf + lane * kPitch,
-                        a.w_qb + ((int64_t)h * kHeadRows + p0 + lane) * kQLora, kRowBytes,
-                        &full[slot], pol);
-        else if (lane == kTaskRows)
-          bulk_g2s_hint(buf + kTaskQbBytes, a.w_uk + ((int64_t)h * kNope + p0) * kKvLora,
-                        kTaskUkBytes, &full[slot], pol);
-      } else {
-        const int r = seq.r0 + (k - seq.tasks()) * kTaskRows;
-        const int n = min(kTaskRows, seq.r1 - r);
-        if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)(n * kRowBytes));
-        __syncwarp();
-        if (lane < n)
-          bulk_g2s_hint(buf + lane * kPitch, a.w_qb + (int64_t)rope_row(r + lane) * kQLora,
-                        kRowBytes, &full[slot], pol);
-      }
-    }
-    if (lane == 0)
-      for (int k = max(0, nst - kAbsStages); k < nst; ++k)
-        (void)mbar_wait_bounded(&full[k % kAbsStages], (uint32_t)((k / kAbsStages) & 1),
-                                kWaitLimit);
-  } else {
-    // ================= consumer warps 0-7 ============================
-    // gamma_q is a static weight: loaded before the wait for the previous kernel
-    const uint4 gv = warp < 6 ? *reinterpret_cast<const uint4*>(a.gamma_q + 8 * tid)
-                              : make_uint4(0, 0, 0, 0);
-    pdl_wait();
-    if (tid == 0) trace_stamp(a, 3);
-    // q_a RMSNorm -> xq (warps 0-5); KV insert of token i (warps 6-7)
-    if (warp < 6) {
-      uint4 xv[NT];
-#pragma unroll
-      for (int t = 0; t < NT; ++t)
-        xv[t] = t < a.batch ? *reinterpret_cast<const uint4*>(a.q_a + (int64_t)t * a.q_a_stride +
-                                                               8 * tid)
-                            : make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        const uint32_t ww[4] = {xv[t].x, xv[t].y, xv[t].z, xv[t].w};
-        float ss = 0.f;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          ss = fmaf(bf16lo(ww[k]), bf16lo(ww[k]), ss);
-          ss = fmaf(bf16hi(ww[k]), bf16hi(ww[k]), ss);
-        }
-        ss = warp_sum(ss);
-        if (lane == 0) ss_part[t * 8 + warp] = ss;
-      }
-      named_barrier(kBarNorm, 192);
-      const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        const float* sp = ss_part + t * 8;
-        const float total = ((((sp[0] + sp[1]) + sp[2]) + sp[3]) + sp[4]) + sp[5];
-        const float rr = __frsqrt_rn(__fadd_rn(__fdiv_rn(total, 1536.0f), a.eps));
-        const uint32_t ww[4] = {xv[t].x, xv[t].y, xv[t].z, xv[t].w};
-        uint4 o;
-        o.x = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[0]), rr), bf16lo(gw[0])),
-                          __fmul_rn(__fmul_rn(bf16hi(ww[0]), rr), bf16hi(gw[0])));
-        o.y = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[1]), rr), bf16lo(gw[1])),
-                          __fmul_rn(__fmul_rn(bf16hi(ww[1]), rr), bf16hi(gw[1])));
-        o.z = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[2]), rr), bf16lo(gw[2])),
-                          __fmul_rn(__fmul_rn(bf16hi(ww[2]), rr), bf16hi(gw[2])));
-        o.w = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[3]), rr), bf16lo(gw[3])),
-                          __fmul_rn(__fmul_rn(bf16hi(ww[3]), rr), bf16hi(gw[3])));
-        if (t >= a.batch) o = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(xq + t * kPitch + 16 * tid) = o;
-        if (i == 0 && a.q_c != nullptr && t < a.batch)
-          *reinterpret_cast<uint4*>(a.q_c + (int64_t)t * kQLora + 8 * tid) = o;
-      }
-    } else {
-      for (int t = i; t < NT; t += P)
-        if (t < a.batch) kv_insert(a, t, tid - 192, ss_part + NT * 8);
-    }
-    named_barrier(kBarConsumers, kConsumers);
-    if (tid == 0) trace_stamp(a, 2);
-
-    float xr[NT][48];
-#pragma unroll
-    for (int t = 0; t < NT; ++t)
-#pragma unroll
-      for (int c = 0; c < 6; ++c) {
-        const uint4 v = *reinterpret_cast<const uint4*>(xq + t * kPitch + 2 * (256 * c + 8 * lane));
-        const uint32_t ww[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          xr[t][8 * c + 2 * k] = bf16lo(ww[k]);
-          xr[t][8 * c + 2 * k + 1] = bf16hi(ww[k]);
-        }
-      }
-
-    for (int k = 0; k < nst; ++k) {
-      const int slot = k % kAbsStages;
-      const uint8_t* buf = ring + slot * kTaskStage;
-      if (!mbar_wait_bounded(&full[slot], (uint32_t)((k / kAbsStages) & 1), kWaitLimit))
-        timed_out = true;
-      if (tid == 0 && k < 20) trace_stamp(a, 8 + k);
-      const bool task = k < seq.tasks();
-      // rows w and w + 8 of the stage: FP32 dot products with xq
-      const int nrows = task ? kTaskRows : min(kTaskRows, seq.r1 - (seq.r0 + (k - seq.tasks()) * kTaskRows));
-      float v[2][NT];
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const int j = warp + kConsumerWarps * rr;
-#pragma unroll
-        for (int t = 0; t < NT; ++t) v[rr][t] = 0.f;
-        if (j < nrows) {
-          const uint8_t* rowp = buf + j * kPitch;
-          float acc[NT][2];
-#pragma unroll
-          for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = 0.f;
-#pragma unroll
-          for (int c = 0; c < 6; ++c) {
-            const uint4 wv = *reinterpret_cast<const uint4*>(rowp + 2 * (256 * c + 8 * lane));
-            const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const float w0 = bf16lo(ww[kk]), w1 = bf16hi(ww[kk]);
-#pragma unroll
-              for (int t = 0; t < NT; ++t) {
-                acc[t][0] = fmaf(w0, xr[t][8 * c + 2 * kk], acc[t][0]);
-                acc[t][1] = fmaf(w1, xr[t][8 * c + 2 * kk + 1], acc[t][1]);
-              }
-            }
-          }
-#pragma unroll
-          for (int t = 0; t < NT; ++t) v[rr][t] = warp_sum(acc[t][0] + acc[t][1]);
-        }
-      }
-      if (!task) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
-        if (lane == 0) {
-          const int r0 = seq.r0 + (k - seq.tasks()) * kTaskRows;
-#pragma unroll
-          for (int rr = 0; rr < 2; ++rr) {
-            const int j = warp + kConsumerWarps * rr;
-            if (j < nrows) {
-              const int r = r0 + j;
-#pragma unroll
-              for (int t = 0; t < NT; ++t)
-                if (t < a.batch)
-                  put_q(a, a.q_pe, (int64_t)t * a.qp_ts + (int64_t)(r / kRope) * a.qp_hs + r % kRope,
-                        v[rr][t], load_qsi(a));
-            }
-          }
-        }
-        continue;
-      }
-      // ---- task: share the 16 BF16-rounded q values, absorb them --------
-      const int n = k, tk = seq.t0 + k;
-      (void)n;
-      float* qb = q16 + (n & 1) * NT * kTaskRows;
-      if (lane == 0) {
-#pragma unroll
-        for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-          for (int t = 0; t < NT; ++t) qb[t * kTaskRows + warp + kConsumerWarps * rr] = bf_round(v[rr][t]);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(qbar);
-      if (!mbar_wait_bounded(qbar, (uint32_t)(n & 1), kWaitLimit)) timed_out = true;
-      // this lane: latent columns c, c + 1 with c = 64 w + 2 lane
-      const int c = 64 * warp + 2 * lane;
-      const uint8_t* uk = buf + kTaskQbBytes;
-      float acc[NT][2];
-#pragma unroll
-      for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = 0.f;
-#pragma unroll
-      for (int p = 0; p < kTaskRows; ++p) {
-        const uint32_t wv = *reinterpret_cast<const uint32_t*>(uk + p * (kKvLora * 2) + 2 * c);
-        const float w0 = bf16lo(wv), w1 = bf16hi(wv);
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          acc[t][0] = fmaf(qb[t * kTaskRows + p], w0, acc[t][0]);
-          acc[t][1] = fmaf(qb[t * kTaskRows + p], w1, acc[t][1]);
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[slot]);  // W_QB and W_UK of the slot are read
-      float* part = a.partial + ((int64_t)tk * NT) * kKvLora;
-#pragma unroll
-      for (int t = 0; t < NT; ++t)
-        *reinterpret_cast<float2*>(part + (int64_t)t * kKvLora + c) = make_float2(acc[t][0], acc[t][1]);
-    }
-    if (tid == 0) trace_stamp(a, 6);
-  }
-
-  if (timed_out) atomicOr(a.err, MLA_DEVERR_TIMEOUT);
-  __syncthreads();
-  if (tid == 0) trace_stamp(a, 7);
-}
-
 // ===========================================================================
 // Absorbing kernel on tensor cores (up to 16 tokens per CTA).
 //
-// The tasks, rope chunks, host split, finisher and head closing of the FMA
-// flavour above, with the arithmetic on mma.sync m16n8k16 (BF16 operands,
-// FP32 accumulate):
+// The tasks, rope chunks, host split and head closing above, with the
+// arithmetic on mma.sync m16n8k16 (BF16 operands, FP32 accumulate):
 //  * Q_B: a stage's 16 weight rows are the M side and the tokens the N side
 //    (8 per n-tile); warp w takes the K slice [192 w, 192 w + 192), and the
 //    eight split-K partial tiles are added in warp order after one barrier
@@ -1923,48 +1639,6 @@ cudaError_t repack_w_uk(const uint16_t* w_uk, uint8_t* dst, int heads, cudaStrea
 }
 
 template <int NT>
-cudaError_t launch_close(const DecodeArgs& a, int ctas, cudaStream_t stream) {
-  const int items = a.batch * a.heads * (kKvLora / 4);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)min((items + 255) / 256, 8 * ctas), 1, 1);
-  cfg.blockDim = dim3(256, 1, 1);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_close_kernel<NT>, a);
-}
-
-template <int NT>
-cudaError_t launch_abs(const DecodeArgs& a, const AbsSplit& sp, int ctas, cudaStream_t stream) {
-  using S = AbsSmem<NT>;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)ctas, 1, 1);
-  cfg.blockDim = dim3(kAbsThreads, 1, 1);
-  cfg.dynamicSmemBytes = S::kAlloc;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, mla_absorb_kernel<NT>, a, sp);
-  if (e != cudaSuccess) return e;
-  return launch_close<NT>(a, ctas, stream);
-}
-
-template <int NT>
-cudaError_t prepare_abs() {
-  using S = AbsSmem<NT>;
-  static_assert(S::kAlloc <= 232448, "shared memory budget");
-  return cudaFuncSetAttribute(mla_absorb_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              S::kAlloc);
-}
-
-template <int NT>
 cudaError_t launch_abs_mma(const DecodeArgs& a, const AbsSplit& sp, int ctas, cudaStream_t stream) {
   using S = AbsMmaSmem<NT>;
   cudaLaunchConfig_t cfg = {};
@@ -2052,8 +1726,6 @@ cudaError_t prepare_fused_kernels() {
     if (e != cudaSuccess) return e;
   }
   cudaError_t e;
-  if ((e = prepare_abs<1>()) != cudaSuccess) return e;
-  if ((e = prepare_abs<2>()) != cudaSuccess) return e;
   if ((e = prepare_abs_mma<8>()) != cudaSuccess) return e;
   if ((e = prepare_abs_mma<16>()) != cudaSuccess) return e;
   if ((e = prepare_one<1, false>()) != cudaSuccess) return e;
@@ -2065,8 +1737,6 @@ cudaError_t prepare_fused_kernels() {
 
 cudaError_t launch_absorb(const DecodeArgs& a, const AbsSplit& sp, int nt, int ctas,
                           cudaStream_t stream) {
-  if (nt == 1) return launch_abs<1>(a, sp, ctas, stream);
-  if (nt == 2) return launch_abs<2>(a, sp, ctas, stream);
   if (nt == 8) return launch_abs_mma<8>(a, sp, ctas, stream);
   if (nt == 16) return launch_abs_mma<16>(a, sp, ctas, stream);
   return cudaErrorInvalidValue;

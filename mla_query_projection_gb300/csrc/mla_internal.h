@@ -125,6 +125,33 @@ bool make_pair_split(int heads, int ctas, PairSplit* sp);
 // Whether `ctas` CTAs of the paired kernel (nt = 8 or 16 tokens) can all be
 // resident at once.
 bool pair_kernel_fits(int ctas, int nt);
+// Small-batch FMA kernel (1-2 tokens, clusters of `cluster` CTAs, two CTAs
+// of consecutive steps resident per SM): the heads of cluster g are
+// [head[g], head[g + 1]) (at most two), rank r of the cluster takes nope rows
+// [r * 128 / cluster, (r + 1) * 128 / cluster) of each of them with their
+// W_UK rows, and CTA i the rope rows [rope[i], rope[i + 1]).
+struct SmallSplit {
+  int cluster;
+  uint16_t head[kMaxCtas / 2 + 1];
+  uint16_t rope[kMaxCtas + 1];
+};
+// Fills `sp` for `ctas` CTAs (a multiple of `cluster`, 2, 4 or 8); false if
+// some cluster would get more than two heads.
+bool make_small_split(int heads, int ctas, int cluster, SmallSplit* sp);
+// Weight bytes of the most loaded CTA of a split.
+int64_t small_split_max_bytes(int heads, int ctas, const SmallSplit& sp);
+// Chooses the cluster size (fewest bytes on the most loaded CTA) and fills
+// `sp`; returns the grid, or 0 if no cluster size can serve `heads`.  A grid
+// has at most num_sms / C clusters of C, and at most max_clusters[k] for
+// C = 2 << k (how many can be resident at once; 0 = no limit, negative = that
+// cluster size cannot run).
+int choose_small_split(int heads, int num_sms, const int* max_clusters, SmallSplit* sp);
+// Clusters of `cluster` CTAs of the small-batch kernel (nt tokens) that can
+// be resident at once on this device (0 on error).
+int small_kernel_max_clusters(int cluster, int nt);
+cudaError_t prepare_small_kernels();
+cudaError_t launch_small(const DecodeArgs& a, const SmallSplit& sp, int ctas, int nt,
+                         cudaStream_t stream);
 // Wide kernel (17-64 tokens, tcgen05, clusters of two CTAs splitting K): the
 // heads of pair c are [head[c], head[c + 1]) (at most two), its rope units
 // [rope[c], rope[c + 1]).  A rope unit is the rope rows of two heads (2u,

@@ -1,0 +1,552 @@
+// mla_small.cu - the decode step for one or two tokens on FP32 FMAs, shaped
+// so that the CTAs of consecutive steps share each SM.
+//
+// What it computes is the step of page "mla.query", class MlaQuery (method
+// kernel, the small-batch path, and insert / insert_ds / insert_nvfp4 /
+// store_qc): q_a RMSNorm -> xq (q_c), Q_B rows -> q (BF16, FP32 accumulate),
+// rope rows -> q_pe, nope rows through W_UK -> q_latent, and the KV insert.
+//
+// GB300 design.  With one or two tokens a weight element feeds one or two
+// FMAs, so the projection is no dense contraction: plain FP32 FMAs keep up
+// with the stream, and the kernel is shaped around the stream instead.
+//  * Two CTAs per SM.  A CTA holds a 96 KiB ring (three 32 KiB stages) and
+//    about 105 KiB of shared memory in all, so the CTA of the next step fits
+//    beside it.  The page's class docstring loads the static weights before
+//    the programmatic-dependent-launch wait; here that means the next step's
+//    producer fills its ring while this step computes its last stages,
+//    stores its outputs and exits, instead of after.
+//  * Clusters of C CTAs (2, 4 or 8) own whole heads (at most two per
+//    cluster); rank r takes nope rows [r 128/C, (r+1) 128/C) of each head and
+//    the same rows of W_UK, and rope rows fill every CTA to an even byte
+//    share.  A stage is 8 consecutive Q_B rows (24 KiB, contiguous in
+//    global memory) plus, for nope rows, their 8 W_UK rows (8 KiB): two 1-D
+//    bulk copies.
+//  * Warp w computes row w of a stage: each lane dots 48 of the row's 1536
+//    values with the normalised xq it keeps in registers (BF16 pairs), then
+//    the warp adds the lanes.  The 8 BF16-rounded nope q values go through
+//    shared memory to all 256 threads, and thread t adds their products with
+//    W_UK columns 2t, 2t + 1 into its FP32 absorption sums.
+//  * After a head's last stage each thread sends the sums of columns another
+//    rank owns (rank r owns columns [r 512/C, (r+1) 512/C)) into that CTA's
+//    shared memory (st.async, counted on its mbarrier); each owner adds the
+//    C partials in rank order (row order of the head) and writes q_latent.
+// Every wait is bounded (MLA_DEVERR_TIMEOUT instead of a hang).
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "../../include/mla_query.h"
+#include "mla_common.cuh"
+#include "mla_device.cuh"
+#include "mla_internal.h"
+
+namespace mla {
+
+namespace {
+
+constexpr int kSmRows = 8;                         // Q_B rows per stage: one per consumer warp
+constexpr int kSmQbBytes = kSmRows * kRowBytes;    // 24 KiB
+constexpr int kSmUkBytes = kSmRows * kKvLora * 2;  // 8 KiB
+constexpr int kSmStage = kSmQbBytes + kSmUkBytes;  // 32 KiB
+#ifndef MLA_SMALL_SLOTS
+#define MLA_SMALL_SLOTS 3
+#endif
+constexpr int kSmSlots = MLA_SMALL_SLOTS;
+#ifndef MLA_SMALL_PREFETCH
+#define MLA_SMALL_PREFETCH 0
+#endif
+constexpr bool kSmPrefetch = MLA_SMALL_PREFETCH != 0;
+constexpr int kSmThreads = kConsumers + 32;        // 8 consumer warps + the producer warp
+
+template <int NT, int C>
+struct SmallSmem {
+  static constexpr int kCols = kKvLora / C;            // latent columns a rank owns
+  static constexpr int kStagesPerHead = kNope / C / kSmRows;
+  static constexpr int kRecvHead = C * kCols * NT * 4;  // [rank][column][token] FP32
+  static constexpr int kRecvBytesIn = (C - 1) * kCols * NT * 4;  // what the peers send
+  static constexpr int oRing = 0;
+  static constexpr int oRecv = kSmSlots * kSmStage;     // [2 heads][kRecvHead]
+  static constexpr int oQv = oRecv + 2 * kRecvHead;     // [2][8 rows][NT] FP32
+  static constexpr int oFull = oQv + 2 * kSmRows * NT * 4;
+  static constexpr int oEmpty = oFull + kSmSlots * 8;
+  static constexpr int oRbar = oEmpty + kSmSlots * 8;   // [2] received partials
+  static constexpr int oQbar = oRbar + 16;              // [2] q values of a stage written
+  // two tokens: their xq rows in shared memory [NT][1536] BF16 (one token
+  // keeps its 48 values a lane in registers)
+  static constexpr int kXsBytes = NT > 1 ? NT * kRowBytes : 0;
+  static constexpr int oXs = oQbar + 16;
+  static constexpr int kBytes = oXs + kXsBytes;
+  static constexpr int kAlloc = kBytes + 128;
+  static_assert(kStagesPerHead * kSmRows * C == kNope, "stages per head");
+  static_assert(kSmSlots != 3 || 2 * (kAlloc + 1024) <= 233472, "two CTAs per SM");
+  static_assert(kSmSlots != 3 || kAlloc <= 120 * 1024, "the one-per-SM occupancy query asks for more");
+};
+
+// This CTA's stages: the nope stages of each head of its cluster, then its
+// rope rows in stages of up to 8.
+template <int C>
+struct SmallSeq {
+  static constexpr int kPerHead = kNope / C / kSmRows;
+  int h0, nh, rank, r0, r1;
+  __device__ int nope() const { return kPerHead * nh; }
+  __device__ int stages() const { return nope() + (r1 - r0 + kSmRows - 1) / kSmRows; }
+  __device__ int head(int k) const { return h0 + k / kPerHead; }
+  __device__ int p0(int k) const { return (kNope / C) * rank + kSmRows * (k % kPerHead); }
+};
+
+__device__ __forceinline__ int small_rope_row(int r) {  // rope index -> W_QB row
+  return (r / kRope) * kHeadRows + kNope + (r % kRope);
+}
+
+// Stage k of a CTA into L2 (no shared memory, no completion): its 8 Q_B
+// rows and, for nope rows, their 8 W_UK rows; rope rows may span two heads.
+template <int C>
+__device__ __forceinline__ void small_prefetch_stage(const DecodeArgs& a, const SmallSeq<C>& seq,
+                                                     int k) {
+  if (k < seq.nope()) {
+    const int h = seq.head(k), p0 = seq.p0(k);
+    bulk_prefetch_l2(a.w_qb + ((int64_t)h * kHeadRows + p0) * kQLora, kSmQbBytes);
+    bulk_prefetch_l2(a.w_uk + ((int64_t)h * kNope + p0) * kKvLora, kSmUkBytes);
+  } else {
+    const int r = seq.r0 + (k - seq.nope()) * kSmRows;
+    const int n = min(kSmRows, seq.r1 - r);
+    const int n1 = min(n, kRope - r % kRope);
+    bulk_prefetch_l2(a.w_qb + (int64_t)small_rope_row(r) * kQLora, (uint32_t)(n1 * kRowBytes));
+    if (n > n1)
+      bulk_prefetch_l2(a.w_qb + (int64_t)small_rope_row(r + n1) * kQLora,
+                       (uint32_t)((n - n1) * kRowBytes));
+  }
+}
+
+__device__ __forceinline__ void st_async_v2(uint32_t raddr, float x, float y, uint32_t rbar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
+          raddr),
+      "f"(x), "f"(y), "r"(rbar)
+      : "memory");
+}
+
+// FP32 dot products of one 8-value chunk of a Q_B row with the same chunk of
+// each token's xq (BF16 pairs): pair e of the chunk goes to accumulator e, so
+// four independent FMA chains run side by side.
+template <int NT>
+__device__ __forceinline__ void dot_chunk(const uint4 w, const uint4 (&x)[NT], float (&s)[NT][4]) {
+  const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    const uint32_t xx[4] = {x[t].x, x[t].y, x[t].z, x[t].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      s[t][e] = fmaf(bf16lo(ww[e]), bf16lo(xx[e]), s[t][e]);
+      s[t][e] = fmaf(bf16hi(ww[e]), bf16hi(xx[e]), s[t][e]);
+    }
+  }
+}
+
+// 112 registers a thread: two CTAs of 288 threads fill the SM's 64K.
+template <int NT, int C>
+__global__ void __maxnreg__(112)
+    mla_small_kernel(const DecodeArgs a, const __grid_constant__ SmallSplit split) {
+  using S = SmallSmem<NT, C>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                             ~static_cast<uintptr_t>(127));
+  uint8_t* ring = smem + S::oRing;
+  float* qv = reinterpret_cast<float*>(smem + S::oQv);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::oFull);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + S::oEmpty);
+  uint64_t* rbar = reinterpret_cast<uint64_t*>(smem + S::oRbar);
+  uint64_t* qbar = reinterpret_cast<uint64_t*>(smem + S::oQbar);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int i = blockIdx.x, P = gridDim.x;
+  const int g = i / C, rank = i % C;  // cluster (C, 1, 1): rank = blockIdx.x % C
+  const SmallSeq<C> seq{split.head[g], split.head[g + 1] - split.head[g], rank, split.rope[i],
+                        split.rope[i + 1]};
+  const int nst = seq.stages();
+
+  if (tid == 0) {
+    for (int s = 0; s < kSmSlots; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    mbar_init(&rbar[0], 1);
+    mbar_init(&rbar[1], 1);
+    mbar_init(&qbar[0], kConsumerWarps);
+    mbar_init(&qbar[1], kConsumerWarps);
+    // the peers' partials of head j land in recv[j]: armed before the
+    // cluster meets below, so no byte can arrive before its count is expected
+    for (int j = 0; j < seq.nh; ++j) mbar_arrive_expect_tx(&rbar[j], S::kRecvBytesIn);
+    mbar_fence_init();
+    pdl_launch_dependents();
+    trace_stamp(a, 0);
+  }
+  __syncthreads();
+  cluster_sync();
+  bool timed_out = false;
+
+  if (warp == kConsumerWarps) {
+    // ================= producer: weights only, no PDL wait ============
+    // A stage's copies are issued by separate lanes in one instruction (a Q_B
+    // row of 3 KiB per lane 0-7, a W_UK row of 1 KiB per lane 8-15): copies
+    // one thread issues complete one after another, copies of different
+    // threads side by side.
+    const uint64_t pol = l2_policy_evict_first();
+    if (kSmPrefetch && lane == 0)
+      for (int k = kSmSlots; k < min(nst, 2 * kSmSlots); ++k) small_prefetch_stage<C>(a, seq, k);
+    int issued = 0;
+    for (int k = 0; k < nst; ++k) {
+      const int slot = k % kSmSlots;
+      uint8_t* buf = ring + slot * kSmStage;
+      int ok = 1;
+      if (k >= kSmSlots && lane == 0)
+        ok = mbar_wait_bounded(&empty[slot], (uint32_t)(((k / kSmSlots) - 1) & 1), kWaitLimit);
+      if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
+        timed_out = true;  // the consumers stopped: issue nothing more
+        break;
+      }
+      issued = k + 1;
+      if (lane == 0 && k < 20) trace_stamp(a, 28 + k);  // stage k issued
+      if (kSmPrefetch && lane == 0 && k >= kSmSlots && k + kSmSlots < nst)
+        small_prefetch_stage<C>(a, seq, k + kSmSlots);
+      if (k < seq.nope()) {
+        const int h = seq.head(k), p0 = seq.p0(k);
+        if (lane == 0) mbar_arrive_expect_tx(&full[slot], kSmStage);
+        __syncwarp();
+        if (lane < kSmRows)
+          bulk_g2s_hint(buf + lane * kRowBytes,
+                        a.w_qb + ((int64_t)h * kHeadRows + p0 + lane) * kQLora, kRowBytes,
+                        &full[slot], pol);
+        else if (lane < 2 * kSmRows)
+          bulk_g2s_hint(buf + kSmQbBytes + (lane - kSmRows) * kKvLora * 2,
+                        a.w_uk + ((int64_t)h * kNope + p0 + lane - kSmRows) * kKvLora,
+                        kKvLora * 2, &full[slot], pol);
+      } else {
+        const int r = seq.r0 + (k - seq.nope()) * kSmRows;
+        const int n = min(kSmRows, seq.r1 - r);
+        if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)(n * kRowBytes));
+        __syncwarp();
+        if (lane < n)
+          bulk_g2s_hint(buf + lane * kRowBytes, a.w_qb + (int64_t)small_rope_row(r + lane) * kQLora,
+                        kRowBytes, &full[slot], pol);
+      }
+    }
+    // every copy issued lands before the CTA may leave
+    if (lane == 0)
+      for (int k = issued > kSmSlots ? issued - kSmSlots : 0; k < issued; ++k)
+        (void)mbar_wait_bounded(&full[k % kSmSlots], (uint32_t)((k / kSmSlots) & 1), kWaitLimit);
+  } else {
+    // ================= consumer warps 0-7 ============================
+    pdl_wait();
+    if (tid == 0) trace_stamp(a, 3);
+    // the KV rows first (CTA i inserts tokens i, i + P, ...), before the
+    // normalised q_a row takes its registers
+    if (warp == kConsumerWarps - 1)
+      for (int t = i; t < a.batch; t += P) kv_insert_warp(a, t, lane);
+    // q_a RMSNorm of every token, in every warp: lane l keeps columns
+    // 8 (l + 32 j) .. + 7, j < 6, of xq as BF16 pairs
+    uint4 xq[NT][6];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      float ss = 0.f;
+#pragma unroll
+      for (int j = 0; j < 6; ++j) {
+        xq[t][j] = t < a.batch ? *reinterpret_cast<const uint4*>(
+                                     a.q_a + (int64_t)t * a.q_a_stride + 8 * (lane + 32 * j))
+                               : make_uint4(0, 0, 0, 0);
+        const uint32_t vv[4] = {xq[t][j].x, xq[t][j].y, xq[t][j].z, xq[t][j].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          ss = fmaf(bf16lo(vv[e]), bf16lo(vv[e]), ss);
+          ss = fmaf(bf16hi(vv[e]), bf16hi(vv[e]), ss);
+        }
+      }
+      ss = warp_sum(ss);
+      const float rr = __frsqrt_rn(__fadd_rn(__fdiv_rn(ss, 1536.0f), a.eps));
+#pragma unroll
+      for (int j = 0; j < 6; ++j) {
+        const uint4 gj = *reinterpret_cast<const uint4*>(a.gamma_q + 8 * (lane + 32 * j));
+        const uint32_t gw[4] = {gj.x, gj.y, gj.z, gj.w};
+        const uint32_t vv[4] = {xq[t][j].x, xq[t][j].y, xq[t][j].z, xq[t][j].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          o[e] = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(vv[e]), rr), bf16lo(gw[e])),
+                             __fmul_rn(__fmul_rn(bf16hi(vv[e]), rr), bf16hi(gw[e])));
+        xq[t][j] = make_uint4(o[0], o[1], o[2], o[3]);
+        if constexpr (NT > 1) {
+          if (warp == 0)
+            *reinterpret_cast<uint4*>(smem + S::oXs + t * kRowBytes + 16 * (lane + 32 * j)) = xq[t][j];
+        }
+        if (i == 0 && warp == 0 && a.q_c != nullptr && t < a.batch)
+          *reinterpret_cast<uint4*>(a.q_c + (int64_t)t * kQLora + 8 * (lane + 32 * j)) = xq[t][j];
+      }
+    }
+    if constexpr (NT > 1) named_barrier(4, kConsumers);  // xq rows written (before any wait)
+    if (tid == 0) trace_stamp(a, 2);
+    const float qsi = load_qsi(a);
+
+    // Thread tid's latent columns 2 tid, 2 tid + 1 belong to rank owner.
+    const int owner = tid * C / kConsumers;
+    const int lc = 2 * tid - owner * S::kCols;  // column within the owner's range
+    float acc[NT][2];    // absorption sums of the current head
+    float keep[2][NT][2];  // owned sums of heads 0 and 1 of the cluster
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      acc[t][0] = acc[t][1] = 0.f;
+      keep[0][t][0] = keep[0][t][1] = keep[1][t][0] = keep[1][t][1] = 0.f;
+    }
+
+    for (int k = 0; k < nst; ++k) {
+      const int slot = k % kSmSlots;
+      const uint8_t* buf = ring + slot * kSmStage;
+      // a stage that never arrives ends the loop; the other warps' barrier
+      // waits below are then bounded by the same limit
+      if (!mbar_wait_bounded(&full[slot], (uint32_t)((k / kSmSlots) & 1), kWaitLimit)) {
+        timed_out = true;
+        break;
+      }
+      if (tid == 0 && k < 20) trace_stamp(a, 8 + k);  // stage k's data seen
+      const bool nope = k < seq.nope();
+      const int r = seq.r0 + (k - seq.nope()) * kSmRows;  // first rope row (rope stages)
+      const int rows = nope ? kSmRows : min(kSmRows, seq.r1 - r);
+      // ---- Q_B row `warp` of the stage: 48 products per lane, then the warp
+      float s[NT];
+#pragma unroll
+      for (int t = 0; t < NT; ++t) s[t] = 0.f;
+      if (warp < rows) {
+        const uint4* row = reinterpret_cast<const uint4*>(buf + warp * kRowBytes);
+        float s4[NT][4];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) s4[t][0] = s4[t][1] = s4[t][2] = s4[t][3] = 0.f;
+#pragma unroll
+        for (int j = 0; j < 6; ++j) {
+          uint4 xj[NT];
+#pragma unroll
+          for (int t = 0; t < NT; ++t)
+            xj[t] = NT == 1 ? xq[t][j]
+                            : *reinterpret_cast<const uint4*>(smem + S::oXs + t * kRowBytes +
+                                                               16 * (lane + 32 * j));
+          dot_chunk<NT>(row[lane + 32 * j], xj, s4);
+        }
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+          s[t] = warp_sum((s4[t][0] + s4[t][1]) + (s4[t][2] + s4[t][3]));
+      }
+      if (!nope) {
+        // ---- rope rows -> q_pe ------------------------------------------
+        if (warp < rows) {
+          const int rr_ = r + warp;
+#pragma unroll
+          for (int t = 0; t < NT; ++t)
+            if (lane == t && t < a.batch)
+              put_q(a, a.q_pe,
+                    (int64_t)t * a.qp_ts + (int64_t)(rr_ / kRope) * a.qp_hs + rr_ % kRope, s[t],
+                    qsi);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        if (tid == 0 && k < 14) trace_stamp(a, 48 + k);  // stage k done
+        continue;
+      }
+      // ---- nope rows: BF16 q of the 8 rows to every thread -------------
+      // (nope stages are k = 0 .. nope() - 1: buffer k & 1, its use k >> 1)
+      float* qk = qv + (k & 1) * kSmRows * NT;
+      if (lane == 0) {
+#pragma unroll
+        for (int t = 0; t < NT; ++t) qk[warp * NT + t] = bf_round(s[t]);
+        mbar_arrive(&qbar[k & 1]);
+      }
+      if (!mbar_wait_bounded(&qbar[k & 1], (uint32_t)((k >> 1) & 1), kWaitLimit))
+        timed_out = true;
+      // ---- absorption: W_UK rows p0..p0+7, columns 2 tid and 2 tid + 1 --
+      const uint32_t* uk = reinterpret_cast<const uint32_t*>(buf + kSmQbBytes);
+#pragma unroll
+      for (int p = 0; p < kSmRows; ++p) {
+        const uint32_t w2 = uk[p * (kKvLora / 2) + tid];
+        const float w0 = bf16lo(w2), w1 = bf16hi(w2);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const float qq = qk[p * NT + t];
+          acc[t][0] = fmaf(qq, w0, acc[t][0]);
+          acc[t][1] = fmaf(qq, w1, acc[t][1]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);  // W_QB and W_UK of the slot are read
+      if (tid == 0 && k < 14) trace_stamp(a, 48 + k);  // stage k done
+      if (k % S::kStagesPerHead == S::kStagesPerHead - 1) {
+        // the head's last stage here: columns of other ranks go to them
+        const int j = k / S::kStagesPerHead;
+        if (owner == rank) {
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            if (j == 0) {
+              keep[0][t][0] = acc[t][0];
+              keep[0][t][1] = acc[t][1];
+            } else {
+              keep[1][t][0] = acc[t][0];
+              keep[1][t][1] = acc[t][1];
+            }
+          }
+        } else {
+          // owner's recv[j][rank][lc .. lc + 1][token]
+          const uint32_t peer = (uint32_t)owner;
+          const uint32_t rb = mapa_shared(smem_u32(&rbar[j]), peer);
+          const uint32_t dst = smem_u32(smem + S::oRecv + j * S::kRecvHead +
+                                        ((rank * S::kCols + lc) * NT) * 4);
+          if constexpr (NT == 1) {
+            st_async_v2(mapa_shared(dst, peer), acc[0][0], acc[0][1], rb);
+          } else {
+            st_async_v4(mapa_shared(dst, peer), acc[0][0], acc[1][0], acc[0][1], acc[1][1], rb);
+          }
+        }
+#pragma unroll
+        for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = 0.f;
+      }
+    }
+    if (tid == 0) trace_stamp(a, 6);
+
+    // ---- owned columns: the C partials in rank order -> q_latent --------
+    // (columns 2 tid, 2 tid + 1 are the same in every CTA of the cluster;
+    // only their owner holds every partial)
+    for (int j = 0; j < seq.nh && owner == rank; ++j) {
+      if (!mbar_wait_bounded(&rbar[j], 0u, kWaitLimit)) timed_out = true;
+      const float* rv = reinterpret_cast<const float*>(smem + S::oRecv + j * S::kRecvHead);
+      float v[NT][2];
+#pragma unroll
+      for (int t = 0; t < NT; ++t) v[t][0] = v[t][1] = 0.f;
+#pragma unroll
+      for (int c = 0; c < C; ++c) {
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const float k0 = j == 0 ? keep[0][t][0] : keep[1][t][0];
+          const float k1 = j == 0 ? keep[0][t][1] : keep[1][t][1];
+          const float p0 = c == rank ? k0 : rv[((c * S::kCols + lc) * NT) + t];
+          const float p1 = c == rank ? k1 : rv[((c * S::kCols + lc + 1) * NT) + t];
+          v[t][0] = c == 0 ? p0 : v[t][0] + p0;
+          v[t][1] = c == 0 ? p1 : v[t][1] + p1;
+        }
+      }
+      const int h = seq.h0 + j;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        if (t >= a.batch) continue;
+        const int64_t idx = (int64_t)t * a.ql_ts + (int64_t)h * a.ql_hs + 2 * tid;
+        if (a.q_scale_inv == nullptr)
+          *reinterpret_cast<uint32_t*>(a.q_latent + idx) = pack_bf16x2(v[t][0], v[t][1]);
+        else
+          *reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(a.q_latent) + idx) =
+              (uint16_t)(q_fp8(v[t][0], qsi) | ((uint16_t)q_fp8(v[t][1], qsi) << 8));
+      }
+    }
+  }
+
+  if (timed_out) atomicOr(a.err, MLA_DEVERR_TIMEOUT);
+  __syncthreads();
+  cluster_sync_relaxed();
+  if (tid == 0) trace_stamp(a, 7);
+}
+
+template <int NT, int C>
+cudaLaunchConfig_t small_config(int ctas, cudaStream_t stream, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ctas, 1, 1);
+  cfg.blockDim = dim3(kSmThreads, 1, 1);
+  cfg.dynamicSmemBytes = SmallSmem<NT, C>::kAlloc;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  // one CTA of this kernel per SM: the second slot is for the next step's
+  attr[1].id = cudaLaunchAttributeClusterSchedulingPolicyPreference;
+  attr[1].val.clusterSchedulingPolicyPreference = cudaClusterSchedulingPolicySpread;
+  attr[2].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[2].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 3;
+  return cfg;
+}
+
+template <int NT, int C>
+cudaError_t prepare_small_one() {
+  // (the limit covers the one-per-SM occupancy query below; a launch asks
+  // for kAlloc)
+  cudaError_t e = cudaFuncSetAttribute(
+      mla_small_kernel<NT, C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      SmallSmem<NT, C>::kAlloc > 120 * 1024 ? SmallSmem<NT, C>::kAlloc : 120 * 1024);
+  if (e != cudaSuccess) return e;
+  // the whole unified memory as shared memory, so that two CTAs fit an SM
+  // (the default carveout measured room for one)
+  return cudaFuncSetAttribute(mla_small_kernel<NT, C>,
+                              cudaFuncAttributePreferredSharedMemoryCarveout,
+                              cudaSharedmemCarveoutMaxShared);
+}
+
+// Clusters that fit with one CTA per SM: the occupancy of a CTA asking for
+// more than half an SM's shared memory (a grid takes one CTA per SM; the
+// second slot is the next step's).
+template <int NT, int C>
+int small_max_clusters_one() {
+  cudaLaunchAttribute attr[3];
+  cudaLaunchConfig_t cfg = small_config<NT, C>(C, nullptr, attr);
+  cfg.numAttrs = 1;  // the cluster shape only
+  if (cfg.dynamicSmemBytes < 120 * 1024) cfg.dynamicSmemBytes = 120 * 1024;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, mla_small_kernel<NT, C>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return clusters;
+}
+
+template <int NT, int C>
+cudaError_t launch_small_one(const DecodeArgs& a, const SmallSplit& sp, int ctas,
+                             cudaStream_t stream) {
+  cudaLaunchAttribute attr[3];
+  cudaLaunchConfig_t cfg = small_config<NT, C>(ctas, stream, attr);
+  return cudaLaunchKernelEx(&cfg, mla_small_kernel<NT, C>, a, sp);
+}
+
+}  // namespace
+
+cudaError_t prepare_small_kernels() {
+  cudaError_t e;
+  if ((e = prepare_small_one<1, 2>()) != cudaSuccess) return e;
+  if ((e = prepare_small_one<1, 4>()) != cudaSuccess) return e;
+  if ((e = prepare_small_one<1, 8>()) != cudaSuccess) return e;
+  if ((e = prepare_small_one<2, 2>()) != cudaSuccess) return e;
+  if ((e = prepare_small_one<2, 4>()) != cudaSuccess) return e;
+  return prepare_small_one<2, 8>();
+}
+
+int small_kernel_max_clusters(int cluster, int nt) {
+  if (nt == 1)
+    return cluster == 2 ? small_max_clusters_one<1, 2>()
+           : cluster == 4 ? small_max_clusters_one<1, 4>()
+           : cluster == 8 ? small_max_clusters_one<1, 8>()
+                          : 0;
+  if (nt == 2)
+    return cluster == 2 ? small_max_clusters_one<2, 2>()
+           : cluster == 4 ? small_max_clusters_one<2, 4>()
+           : cluster == 8 ? small_max_clusters_one<2, 8>()
+                          : 0;
+  return 0;
+}
+
+cudaError_t launch_small(const DecodeArgs& a, const SmallSplit& sp, int ctas, int nt,
+                         cudaStream_t stream) {
+  const int c = sp.cluster;
+  if (nt == 1) {
+    if (c == 2) return launch_small_one<1, 2>(a, sp, ctas, stream);
+    if (c == 4) return launch_small_one<1, 4>(a, sp, ctas, stream);
+    if (c == 8) return launch_small_one<1, 8>(a, sp, ctas, stream);
+  } else if (nt == 2) {
+    if (c == 2) return launch_small_one<2, 2>(a, sp, ctas, stream);
+    if (c == 4) return launch_small_one<2, 4>(a, sp, ctas, stream);
+    if (c == 8) return launch_small_one<2, 8>(a, sp, ctas, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace mla

@@ -51,6 +51,67 @@ bool make_pair_split(int heads, int ctas, PairSplit* sp) {
   return true;
 }
 
+bool make_small_split(int heads, int ctas, int cluster, SmallSplit* sp) {
+  if (cluster != 2 && cluster != 4 && cluster != 8) return false;
+  if (ctas < cluster || ctas % cluster != 0 || ctas > kMaxCtas) return false;
+  const int groups = ctas / cluster;
+  sp->cluster = cluster;
+  for (int g = 0; g <= groups; ++g) sp->head[g] = (uint16_t)((int64_t)heads * g / groups);
+  for (int g = 0; g < groups; ++g)
+    if (sp->head[g + 1] - sp->head[g] > 2) return false;
+  // rope rows fill every CTA up to an even share of the bytes
+  const int64_t tb = (int64_t)(kNope / cluster) * (kRowBytes + kKvLora * 2);  // a head's rows
+  const int64_t rb = kRowBytes, rope = (int64_t)heads * kRope;
+  const int64_t total = (int64_t)heads * cluster * tb + rope * rb;
+  int64_t task_bytes = 0;
+  int prev = 0;
+  sp->rope[0] = 0;
+  for (int i = 0; i < ctas; ++i) {
+    task_bytes += (int64_t)(sp->head[i / cluster + 1] - sp->head[i / cluster]) * tb;
+    int64_t r = (total * (i + 1) / ctas - task_bytes + rb / 2) / rb;
+    if (r < prev) r = prev;
+    if (r > rope) r = rope;
+    if (i == ctas - 1) r = rope;
+    sp->rope[i + 1] = (uint16_t)r;
+    prev = (int)r;
+  }
+  return true;
+}
+
+int64_t small_split_max_bytes(int heads, int ctas, const SmallSplit& sp) {
+  (void)heads;
+  const int c = sp.cluster;
+  const int64_t tb = (int64_t)(kNope / c) * (kRowBytes + kKvLora * 2);
+  int64_t most = 0;
+  for (int i = 0; i < ctas; ++i) {
+    const int64_t b = (int64_t)(sp.head[i / c + 1] - sp.head[i / c]) * tb +
+                      (int64_t)(sp.rope[i + 1] - sp.rope[i]) * kRowBytes;
+    if (b > most) most = b;
+  }
+  return most;
+}
+
+int choose_small_split(int heads, int num_sms, const int* max_clusters, SmallSplit* sp) {
+  int best_ctas = 0;
+  int64_t best = 0;
+  SmallSplit trial;
+  for (int k = 0, c = 2; c <= 8; ++k, c *= 2) {
+    int groups = num_sms / c;
+    if (max_clusters != nullptr && max_clusters[k] < 0) continue;  // cannot run
+    if (max_clusters != nullptr && max_clusters[k] > 0 && max_clusters[k] < groups)
+      groups = max_clusters[k];
+    const int ctas = groups * c;
+    if (ctas < c || !make_small_split(heads, ctas, c, &trial)) continue;
+    const int64_t most = small_split_max_bytes(heads, ctas, trial);
+    if (best_ctas == 0 || most < best) {  // ties keep the smaller cluster
+      best = most;
+      best_ctas = ctas;
+      *sp = trial;
+    }
+  }
+  return best_ctas;
+}
+
 namespace {
 
 // Relative time of a single-head rope box (eight M = 64 MMAs on 16 KiB)

@@ -3,6 +3,8 @@
 //   abs  H C  task[0..C] rope[0..C]
 //   pair H C ok  head[0..C/2] rope[0..C]
 //   wide H C ok single  head[0..C/2] rope[0..C/2]
+//   small H C K ok most  head[0..C/K] rope[0..C]  (clusters of K CTAs)
+//   choose H S ctas K most  (the cluster size chosen for S SMs)
 #include <cstdio>
 
 #include "mla_internal.h"
@@ -31,6 +33,20 @@ int main() {
       for (int c = 0; c <= pairs; ++c) std::printf(" %d", wok ? ws.head[c] : 0);
       for (int c = 0; c <= pairs; ++c) std::printf(" %d", wok ? ws.rope[c] : 0);
       std::printf("\n");
+      for (int k = 2; k <= 8; k *= 2) {
+        static mla::SmallSplit ss;
+        const int sc = (ctas / k) * k;
+        const bool sok = sc >= k && mla::make_small_split(h, sc, k, &ss);
+        std::printf("small %d %d %d %d %lld", h, sc, k, sok ? 1 : 0,
+                    sok ? (long long)mla::small_split_max_bytes(h, sc, ss) : 0LL);
+        for (int g = 0; g <= sc / k; ++g) std::printf(" %d", sok ? ss.head[g] : 0);
+        for (int i = 0; i <= sc; ++i) std::printf(" %d", sok ? ss.rope[i] : 0);
+        std::printf("\n");
+      }
+      static mla::SmallSplit cs;
+      const int cc = mla::choose_small_split(h, ctas, nullptr, &cs);
+      std::printf("choose %d %d %d %d %lld\n", h, ctas, cc, cc ? cs.cluster : 0,
+                  cc ? (long long)mla::small_split_max_bytes(h, cc, cs) : 0LL);
     }
   }
   return 0;

@@ -134,13 +134,22 @@ def test_wide_kernel_head_counts(heads, batch):
     assert_parity(inp)
 
 
+@pytest.mark.parametrize("heads", [16, 32, 64, 128])
 @pytest.mark.parametrize("batch", [1, 2])
-def test_fma_and_mma_paths_agree(batch):
-    inp = S.make_inputs(batch=batch, heads=32, layout=S.LAYOUT_DS_MLA, pages=16, seed=300)
+def test_fma_and_mma_paths_agree(batch, heads):
+    """The small-batch FMA kernel (clusters of 8 at 16 heads, of 4 or 2 above)
+    and the tensor-core kernels meet the oracle on the same inputs; the q_a
+    RMSNorm and the KV insert are computed alike, bit for bit."""
+    inp = S.make_inputs(batch=batch, heads=heads, layout=S.LAYOUT_DS_MLA, pages=16,
+                        seed=300 + heads)
     fma, ref = assert_parity(inp, path=B.MLA_PATH_FMA)
     mma, _ = assert_parity(inp, path=B.MLA_PATH_MMA)
-    # the q_a RMSNorm is one code path: q_c is bit-identical across paths
-    assert np.array_equal(fma["q_c"], mma["q_c"])
+    # The two kernels add the squares of q_a in different orders, so a q_c
+    # element may take the other rounding of a tie, and only there.
+    diff = fma["q_c"] != mma["q_c"]
+    near = O.bf16_midpoint_distance(ref["xq_exact"]) <= O.XQ_TIE_REL * np.abs(ref["xq_exact"])
+    assert not (diff & ~near).any()
+    # the KV insert sums in one order on every kernel: bit-identical rows
     assert np.array_equal(fma["cache"], mma["cache"])
 
 
@@ -217,17 +226,23 @@ def test_small_head_count_repeated_calls_close_every_head():
     "batch,heads,path,want",
     [
         (1, 64, B.MLA_PATH_AUTO, "mla_absorb_pair_kernel<8>"),
+        (2, 128, B.MLA_PATH_AUTO, "mla_absorb_pair_kernel<8>"),
+        (1, 64, B.MLA_PATH_FMA, "mla_small_kernel<1,2>"),
+        (2, 128, B.MLA_PATH_FMA, "mla_small_kernel<2,2>"),
         (12, 64, B.MLA_PATH_AUTO, "mla_absorb_pair_kernel<16>"),
         (40, 64, B.MLA_PATH_AUTO, "mla_wide_norm_kernel+mla_wide_kernel"),
         (1, 16, B.MLA_PATH_AUTO, "mla_absorb_mma_kernel<8>"),
-        (2, 16, B.MLA_PATH_FMA, "mla_absorb_kernel<2>+mla_close_kernel<2>"),
+        (1, 16, B.MLA_PATH_FMA, "mla_small_kernel<1,"),
+        (2, 16, B.MLA_PATH_FMA, "mla_small_kernel<2,"),
     ],
 )
 def test_kernel_for_names_the_split(batch, heads, path, want):
     inp = S.make_inputs(batch=1, heads=heads, layout=S.LAYOUT_E4M3, pages=2, seed=720)
     st = DecodeStep(inp)
     assert st.set_path(path) == B.MLA_OK
-    assert B.mla_query_kernel_for(st.handle, batch) == want
+    got = B.mla_query_kernel_for(st.handle, batch)
+    # the small-batch kernel's cluster size depends on the device's SM groups
+    assert got == want or (want.endswith(",") and got.startswith(want)), got
     assert B.mla_query_kernel_for(st.handle, 0) is None
     st.close()
 
@@ -325,3 +340,29 @@ def test_batches_above_16_read_the_create_time_copy():
     small = st.results()
     assert not np.array_equal(small["q_pe"][:4], first["q_pe"][:4])
     st.close()
+
+
+@pytest.mark.parametrize("heads", [64, 128])
+def test_create_allocates_only_what_the_dispatch_reaches(heads):
+    """On a GB300 at 64 or 128 heads every batch takes the paired kernel (up
+    to 16 tokens, weights read in place) or the wide kernel (its tiled copies
+    of W_QB and W_UK^T, H * 704 KiB): create allocates those copies and a few
+    hundred KiB besides, not the partials buffer (H * 256 KiB), the packed
+    W_UK (H * 128 KiB) or the hand-off q buffer."""
+    inp = S.make_inputs(batch=1, heads=heads, layout=S.LAYOUT_E4M3, pages=2, seed=1020)
+    dev = torch.device("cuda", 0)
+    from mla_query_projection_gb300.runner import bf16_tensor
+
+    w = [bf16_tensor(inp[k], dev) for k in ("w_qb", "w_uk", "gamma_q", "gamma_kv")]
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    h = B.mla_query_create(heads, *w, float(inp["eps"]))
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    used = free0 - free1
+    wide = heads * 704 * 1024
+    assert B.mla_query_kernel_for(h, 1) == "mla_absorb_pair_kernel<8>"
+    assert B.mla_query_kernel_for(h, 64) == "mla_wide_norm_kernel+mla_wide_kernel"
+    # allocations are rounded to 2 MiB pages
+    assert used <= wide + 6 * 1024 * 1024, (used, wide)
+    B.mla_query_destroy(h)

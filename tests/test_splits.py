@@ -35,11 +35,12 @@ def splits(tmp_path_factory):
                     "-I", CUDA_INC, os.path.join(HERE, "split_driver.cpp"),
                     os.path.join(CSRC, "mla_split.cpp"), "-o", exe], check=True)
     out = subprocess.run([exe], check=True, capture_output=True, text=True).stdout
-    rows = {"abs": [], "pair": [], "wide": []}
+    rows = {"abs": [], "pair": [], "wide": [], "small": [], "choose": []}
     for line in out.splitlines():
         f = line.split()
         rows[f[0]].append((int(f[1]), int(f[2]), [int(x) for x in f[3:]]))
-    assert all(len(v) == 9 * 128 for v in rows.values())
+    assert all(len(rows[k]) == 9 * 128 for k in ("abs", "pair", "wide", "choose"))
+    assert len(rows["small"]) == 3 * 9 * 128
     return rows
 
 
@@ -108,3 +109,59 @@ def test_wide_split_shapes_on_76_pairs(splits):
         rb = SINGLE_BOXES if v[1] else ROPE_BOXES
         assert v[1] == single, heads
         assert max(n * HEAD_BOXES + u * rb for n, u in zip(nh, units)) == most, heads
+
+
+SMALL_ROWS = 1536 * 2 + 512 * 2  # one nope row of the small-batch kernel: Q_B row + W_UK row
+
+
+def test_small_split(splits):
+    """Clusters of K CTAs (2, 4, 8) own whole heads, at most two each; rank r
+    of a cluster takes 128/K nope rows of each; rope rows fill every CTA to
+    an even share, so no CTA is more than one rope row above the larger of
+    the share and its own nope bytes.  The reported maximum is exact."""
+    seen = 0
+    for heads, ctas, v in splits["small"]:
+        k, ok, most = v[0], v[1], v[2]
+        if ctas < k:
+            assert not ok
+            continue
+        groups = ctas // k
+        assert ok == (heads <= 2 * groups), (heads, ctas, k)
+        if not ok:
+            continue
+        seen += 1
+        head, rope = v[3:groups + 4], v[groups + 4:]
+        nh = runs(head, heads)
+        assert max(nh) <= 2
+        rows = runs(rope, 64 * heads)
+        mean = (heads * 128 * SMALL_ROWS + 64 * heads * ROW) / ctas
+        loads = []
+        for i, r in enumerate(rows):
+            own = nh[i // k] * (128 // k) * SMALL_ROWS
+            loads.append(own + r * ROW)
+            assert own + r * ROW < max(mean, own) + ROW, (heads, ctas, k, i)
+        assert max(loads) == most, (heads, ctas, k)
+    assert seen > 1000
+
+
+def test_small_split_choice(splits):
+    """The cluster size chosen is the one with the fewest bytes on the most
+    loaded CTA (ties: the smaller cluster); on 152 SMs: 64 and 128 heads take
+    pairs, 16 heads clusters of 8 (64 KiB of nope rows a CTA instead of 256)."""
+    small = {(h, c, v[0]): v for h, c, v in splits["small"]}
+    for heads, sms, v in splits["choose"]:
+        ctas, k, most = v
+        cands = []
+        for kk in (2, 4, 8):
+            row = small.get((heads, (sms // kk) * kk, kk))
+            if row is not None and row[1]:
+                cands.append((row[2], kk))
+        if not cands:
+            assert ctas == 0, (heads, sms)
+            continue
+        best = min(m for m, _ in cands)
+        assert most == best, (heads, sms)
+        assert k == min(kk for m, kk in cands if m == best), (heads, sms)
+    got = {h: v for h, s_, v in splits["choose"] if s_ == 152}
+    assert got[64][1] == 2 and got[128][1] == 2 and got[16][1] == 8
+    assert got[16][2] < 80 * 1024
