@@ -207,13 +207,27 @@ __device__ __forceinline__ void kv_group_norm(const float (&x)[8], uint4 gv, flo
 // insert_ds, insert_nvfp4), run by 64 threads (lt = 0..63, two whole warps).
 // Thread lt owns latent columns 8*lt..8*lt+7; threads 0..7 also own k_pe
 // values 8*lt..8*lt+7.  red2 holds the two warps' partial sums.
-__device__ void kv_insert(const DecodeArgs& a, int b, int lt, float* red2) {
+// The inputs of thread lt's share of token b's KV insert, loaded ahead of
+// the arithmetic (kv_insert_loaded), so a kernel can issue them together
+// with its other loads.
+struct KvLoads {
+  int64_t slot;
+  uint4 v, gv, pe;
+};
+__device__ __forceinline__ KvLoads kv_insert_load(const DecodeArgs& a, int b, int lt) {
+  KvLoads l;
+  l.slot = a.slots[b];
+  l.v = *reinterpret_cast<const uint4*>(a.kv_c + (int64_t)b * a.kv_c_stride + 8 * lt);
+  l.gv = *reinterpret_cast<const uint4*>(a.gamma_kv + 8 * lt);
+  l.pe = make_uint4(0, 0, 0, 0);
+  if (lt < 8) l.pe = *reinterpret_cast<const uint4*>(a.k_pe + (int64_t)b * a.k_pe_stride + 8 * lt);
+  return l;
+}
+
+__device__ void kv_insert_loaded(const DecodeArgs& a, int lt, float* red2, const KvLoads& l) {
   const int lane = lt & 31, w = lt >> 5;
-  const int64_t slot = a.slots[b];
-  const uint4 v = *reinterpret_cast<const uint4*>(a.kv_c + (int64_t)b * a.kv_c_stride + 8 * lt);
-  const uint4 gv = *reinterpret_cast<const uint4*>(a.gamma_kv + 8 * lt);
-  uint4 pe = make_uint4(0, 0, 0, 0);
-  if (lt < 8) pe = *reinterpret_cast<const uint4*>(a.k_pe + (int64_t)b * a.k_pe_stride + 8 * lt);
+  const int64_t slot = l.slot;
+  const uint4 v = l.v, gv = l.gv, pe = l.pe;
   const bool ds = a.layout == MLA_KV_FP8_DS_MLA;
   const bool nv = a.layout == MLA_KV_NVFP4_DS_MLA;
   const float ks = (ds || nv) ? 1.0f : *a.k_scale;
@@ -229,6 +243,10 @@ __device__ void kv_insert(const DecodeArgs& a, int b, int lt, float* red2) {
   float n[8];
   kv_group_norm(x, gv, rr, n);
   kv_store_group(a, row, n, pe, lt, ds, nv, ks);
+}
+
+__device__ void kv_insert(const DecodeArgs& a, int b, int lt, float* red2) {
+  kv_insert_loaded(a, lt, red2, kv_insert_load(a, b, lt));
 }
 
 // The same insert run by one warp: lane l takes the columns of threads l and

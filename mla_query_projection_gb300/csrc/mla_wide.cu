@@ -60,8 +60,10 @@ constexpr int kWideSlots = 5;
 // the programmatic-dependent-launch wait: the ring fills in about 2 us, and
 // the MMAs cannot start before the normalising kernel has run and xq has
 // landed, so without them the CTA's share of HBM would idle meanwhile.
+// Measured (us per step, B = 64): H = 128 21.35 / 20.95 / 20.95 with 0 / 4 /
+// 8 boxes, H = 64 14.69 / 14.55 / 15.37; 16 boxes 22.5 and 17.6.
 #ifndef MLA_WIDE_PREFETCH
-#define MLA_WIDE_PREFETCH 8
+#define MLA_WIDE_PREFETCH 4
 #endif
 constexpr int kWidePrefetch = MLA_WIDE_PREFETCH;
 constexpr int kWideBox = 128 * 128;          // one 128-row x 128 B box (16 KiB)
@@ -583,7 +585,12 @@ __global__ void __launch_bounds__(192) mla_wide_norm_kernel(const DecodeArgs a) 
   __shared__ float red2[2];
   const int t = blockIdx.x, j = threadIdx.x, lane = j & 31, warp = j >> 5;
   pdl_launch_dependents();  // the wide kernel streams weights meanwhile
+  if (j == 0) trace_stamp(a, 60);  // normalising CTA t started
   pdl_wait();
+  if (j == 0) trace_stamp(a, 61);  // its wait passed
+  // the KV insert's inputs (warps 0-1) load together with q_a, not after it
+  KvLoads kvl;
+  if (t < a.batch && warp < 2) kvl = kv_insert_load(a, t, j);
   uint4 o = make_uint4(0, 0, 0, 0);
   if (t < a.batch) {
     const uint4 v = *reinterpret_cast<const uint4*>(a.q_a + (int64_t)t * a.q_a_stride + 8 * j);
@@ -612,7 +619,9 @@ __global__ void __launch_bounds__(192) mla_wide_norm_kernel(const DecodeArgs a) 
   const int half = j / 96, cc = j % 96, at = cc >> 3, c = cc & 7;
   *reinterpret_cast<uint4*>(a.wide_xq + ((size_t)(half * kWideAtoms + at) * kWideTok) * 128 +
                             t * 128 + ((c ^ (t & 7)) << 4)) = o;
-  if (t < a.batch && warp < 2) kv_insert(a, t, j, red2);
+  if (t < a.batch && warp < 2) kv_insert_loaded(a, j, red2, kvl);
+  __syncthreads();
+  if (j == 0) trace_stamp(a, 62);  // its rows written
 }
 
 // Tiled copies for the wide kernel, each 16-byte chunk (row r, 8 K-columns
