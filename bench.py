@@ -279,7 +279,7 @@ class Workload:
     drawn on the device from a seeded torch generator with the same
     distributions, until the sets total at least 3x the L2 size."""
 
-    def __init__(self, name: str, rank: int, dev, path: int = 0):
+    def __init__(self, name: str, rank: int, dev, path: int = 0, nsets: int = 0):
         import torch
 
         from mla_query_projection_gb300 import binding as B
@@ -296,7 +296,7 @@ class Workload:
         self.hidden = hidden
         self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
         self.wbytes = H * (192 * 1536 + 128 * 512) * 2 + (QKV_ROW * HIDDEN * 2 if hidden else 0)
-        self.nsets = nsets = max(1, -(-3 * self.l2 // self.wbytes))
+        self.nsets = nsets = nsets or max(1, -(-3 * self.l2 // self.wbytes))
         gen = torch.Generator(device=dev)
         gen.manual_seed(1234 + rank)
         self.sets = []
@@ -588,7 +588,38 @@ def gpu_arm(args, rank: int, world: int, local_rank: int) -> dict | None:
         del w2
         torch.cuda.empty_cache()
     out["others"] = others
+    sweep = {}
+    for name in (SWEEP_POINTS if args.sweep else ()):
+        w2 = Workload(name, rank, dev, args.path)
+        ms2, _ = time_device(w2, args.steps, args.warmup, args.graph_steps, stream, barrier)
+        (per2,) = max_over_ranks([ms2 / args.steps], dev)
+        sweep[name] = dict(per_step_ms=per2, kernels=w2.kernels)
+        w2.close()
+        del w2
+        torch.cuda.empty_cache()
+    out["sweep"] = sweep
     return out
+
+
+def sweep_profile(args, local_rank: int) -> None:
+    """Three decode steps per sweep point with one weight set, in the order
+    of SWEEP_POINTS, for a short ncu pass (tensor-pipe utilisation and DRAM
+    bytes per point): the third launch of each point is a warm step."""
+    import torch
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    for name in SWEEP_POINTS:
+        wl = Workload(name, 0, dev, args.path, nsets=1)
+        with torch.cuda.stream(stream):
+            for j in range(3):
+                wl.decode(j, stream)
+        torch.cuda.synchronize(dev)
+        if wl.flags(stream):
+            raise RuntimeError(f"device error flags during {name}")
+        print(name, wl.kernels, flush=True)
+        wl.close()
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -758,6 +789,10 @@ KV_NAMES = {0: "fp8_e4m3_per_tensor", 1: "fp8_ds_mla", 2: "nvfp4_ds_mla"}
 L2_POLICY = ("inputs larger than L2: the weights rotate over independent sets totalling at "
              "least 3x the L2 size")
 ALSO_DEFAULT = ("tiny_b1_h16_e4m3", "latency_b1_h64_e4m3", "small_b8_h128_e4m3")
+# The sweep of the metric: B in {1, 2, 4, 8, 16, 32, 64} x H in {64, 128} x
+# the per-tensor E4M3 and fp8_ds_mla layouts (4096 pages, 1% kv_c outliers).
+SWEEP_POINTS = tuple(f"sweep_b{b}_h{h}_{lay}" for h in (64, 128) for lay in ("e4m3", "ds")
+                     for b in (1, 2, 4, 8, 16, 32, 64))
 
 
 def workload_config(name: str, world: int) -> dict:
@@ -802,11 +837,15 @@ def main():
     ap.add_argument("--e2e-bufs", type=int, default=2,
                     help="staging buffers each way in the end-to-end loop")
     ap.add_argument("--path", type=int, default=0, help="force MLA_PATH_* (0 = auto)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="also time every sweep point (B x H x layout), reported under sweep")
+    ap.add_argument("--sweep-profile", action="store_true",
+                    help="only run three decode steps per sweep point (for an ncu pass)")
     ap.add_argument("--cpu-budget", type=float, default=16.0)
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
-    args.also = [w for w in args.also.split(",") if w]
+    args.also = [w for w in args.also.split(",") if w and w != "none"]
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -845,6 +884,10 @@ def main():
         return
 
     import torch
+
+    if args.sweep_profile:
+        sweep_profile(args, local_rank)
+        return
 
     if world > 1:
         import torch.distributed as dist
@@ -901,6 +944,9 @@ def main():
                              "kernel"},
         "per_config": per_config,
     }
+    if r["sweep"]:
+        line["sweep"] = {name: config_entry(name, o["per_step_ms"], o["kernels"], world, peak)
+                         for name, o in r["sweep"].items()}
     if not args.no_cpu and world == 1:
         line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_budget)
     print(json.dumps(line), flush=True)
