@@ -68,6 +68,10 @@ extern "C" {
 #define MLA_DEVERR_BAD_SLOT 1u /* a slot >= num_pages * page_size was skipped   */
 #define MLA_DEVERR_TIMEOUT 2u  /* an internal bounded wait gave up (results of
                                   that call are not valid)                     */
+#define MLA_DEVERR_CHECK 4u    /* builds compiled with -DMLA_CHECKS only: an
+                                  index or address failed its bounds check and
+                                  the access was skipped; bit 8 + s is set for
+                                  check site s (results are not valid)        */
 
 /* Compute paths (mla_query_set_path). */
 #define MLA_PATH_AUTO 0 /* the default: MLA_PATH_MMA at every batch size

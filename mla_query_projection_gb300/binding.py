@@ -24,6 +24,7 @@ MLA_KV_FP8_DS_MLA = 1
 MLA_KV_NVFP4_DS_MLA = 2
 MLA_DEVERR_BAD_SLOT = 1
 MLA_DEVERR_TIMEOUT = 2
+MLA_DEVERR_CHECK = 4  # checks builds only: a bounds check failed (bit 8 + site names it)
 MLA_PATH_AUTO = 0
 MLA_PATH_FMA = 1
 MLA_PATH_MMA = 2

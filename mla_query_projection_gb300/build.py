@@ -42,35 +42,40 @@ def nvcc() -> str:
     return cand
 
 
-def _compile(src: str) -> tuple[str, str]:
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-    cmd = [nvcc(), *NVCC_FLAGS, "-c", src, "-o", obj]
+def _compile(src: str, build_dir: str = BUILD, extra: tuple = ()) -> tuple[str, str]:
+    obj = os.path.join(build_dir, os.path.basename(src) + ".o")
+    cmd = [nvcc(), *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
     p = subprocess.run(cmd, capture_output=True, text=True)
     if p.returncode != 0:
         raise RuntimeError(f"nvcc failed for {src}:\n{p.stdout}\n{p.stderr}")
     return obj, p.stderr
 
 
-def build(verbose: bool = False) -> str:
-    """Compile and link; returns the path of the shared library."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, out_dir: str | None = None, extra: tuple = ()) -> str:
+    """Compile and link; returns the path of the shared library.  With
+    `out_dir` and `extra` nvcc flags, a variant of the same sources goes into
+    out_dir (for instance the bounds-checked build, extra=("-DMLA_CHECKS",));
+    the in-tree library is left as it is."""
+    build_dir = BUILD if out_dir is None else out_dir
+    lib = LIB if out_dir is None else os.path.join(out_dir, "libmla_query.so")
+    os.makedirs(build_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
-        results = list(ex.map(_compile, srcs))
+        results = list(ex.map(lambda src: _compile(src, build_dir, tuple(extra)), srcs))
     objs = [o for o, _ in results]
     if verbose:
         for _, log in results:
             sys.stderr.write(log)
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
     p = subprocess.run(cmd, capture_output=True, text=True)
     if p.returncode != 0:
         raise RuntimeError(f"link failed:\n{p.stdout}\n{p.stderr}")
-    os.replace(tmp, LIB)
-    with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
+    os.replace(tmp, lib)
+    with open(os.path.join(build_dir, "ptxas.log"), "w") as f:
         for _, log in results:
             f.write(log)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

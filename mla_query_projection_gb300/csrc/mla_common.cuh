@@ -55,6 +55,26 @@ __device__ __forceinline__ void trace_stamp(const DecodeArgs& a, int slot) {
 #endif
 }
 
+// Bounds checks of a checks build (compiled with -DMLA_CHECKS, standing in
+// for a memory checker): MLA_IN_BOUNDS(a, cond, site) is cond, and a false
+// cond raises MLA_DEVERR_CHECK with bit 8 + site in the error word; the
+// caller then skips the access.  In other builds it is `true` and cond is
+// not evaluated.  Sites: 0 paired copy source, 1 paired ring slot, 2 paired
+// q_pe store, 3 paired q_latent store, 4 paired exchange offset, 5 wide tile
+// source, 6 wide ring slot or TMEM column, 7 wide output store, 8 wide
+// exchange or q tile offset, 9 normalised-row tile store, 10 small-batch copy
+// source, 11 small-batch ring slot, 12 small-batch exchange offset, 13
+// small-batch output store, 14 partials buffer, 15 partials output store,
+// 16 KV row, 17 hand-off q buffer.
+#ifdef MLA_CHECKS
+__device__ __noinline__ void check_failed(const DecodeArgs& a, int site) {
+  atomicOr(a.err, MLA_DEVERR_CHECK | (1u << (8 + site)));
+}
+#define MLA_IN_BOUNDS(a, cond, site) ((cond) ? true : (::mla::check_failed((a), (site)), false))
+#else
+#define MLA_IN_BOUNDS(a, cond, site) true
+#endif
+
 // One query output element (q_latent or q_pe) at index idx of its tensor:
 // BF16 bits, or with the per-tensor FP8 query (a.q_scale_inv set) the E4M3
 // code of bf16(v) * qsi, the product rounded to binary32 (qsi = *q_scale_inv,
@@ -189,6 +209,7 @@ __device__ __forceinline__ uint8_t* kv_row(const DecodeArgs& a, int64_t slot, bo
     return nullptr;
   }
   const bool ds = a.layout == MLA_KV_FP8_DS_MLA, nv = a.layout == MLA_KV_NVFP4_DS_MLA;
+  if (!MLA_IN_BOUNDS(a, page >= 0 && off >= 0 && off < a.page_size, 16)) return nullptr;
   return a.cache + (page * a.page_size + off) * (ds ? kRowDs : nv ? kRowNvfp4 : kRowE4m3);
 }
 

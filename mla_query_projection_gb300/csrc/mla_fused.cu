@@ -222,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total = total_stages(H);
   const int tok0 = grp * NT;
   uint16_t* qn_g = a.qn + (int64_t)grp * NT * H * kNope;
+  if (!MLA_IN_BOUNDS(a, grp >= 0 && (grp + 1) * NT <= MLA_MAX_BATCH + 16, 17)) return;
   uint32_t* ready_g = a.ready + grp * H;
 
   if (tid == 0) {
@@ -1056,8 +1057,9 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
       const int n = k, tk = seq.t0 + k;
       (void)n;
       float* part = a.partial + (int64_t)tk * NT * kKvLora;
+      const bool part_ok = MLA_IN_BOUNDS(a, tk >= 0 && tk < a.heads * kTasksPerHead, 14);
 #pragma unroll
-      for (int mt = 0; mt < 4; ++mt) {
+      for (int mt = 0; mt < 4 && part_ok; ++mt) {
         const int c = 64 * warp + 16 * mt + g;
 #pragma unroll
         for (int nt = 0; nt < NTL; ++nt) {
@@ -1245,7 +1247,9 @@ __global__ void __launch_bounds__(pair_threads<NT>(), 1)
         if (lane == 0)
           mbar_arrive_expect_tx(&full[slot], kTaskRows * kRowBytes + kTaskRows * kKvLora * 2);
         __syncwarp();
-        if (lane < kTaskRows)
+        if (!MLA_IN_BOUNDS(a, h >= 0 && h < a.heads && p0 >= 0 && p0 + kTaskRows <= kNope, 0) ||
+            !MLA_IN_BOUNDS(a, slot >= 0 && slot < ST, 1)) {
+        } else if (lane < kTaskRows)
           bulk_g2s_hint(buf + lane * kPitch,
                         a.w_qb + ((int64_t)h * kHeadRows + p0 + lane) * kQLora, kRowBytes,
                         &full[slot], pol);
@@ -1258,7 +1262,8 @@ __global__ void __launch_bounds__(pair_threads<NT>(), 1)
         const int n = min(kTaskRows, seq.r1 - r);
         if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)(n * kRowBytes));
         __syncwarp();
-        if (lane < n)
+        if (lane < n &&
+            MLA_IN_BOUNDS(a, r + lane >= 0 && r + lane < a.heads * kRope && slot < ST, 0))
           bulk_g2s_hint(buf + lane * kPitch, a.w_qb + (int64_t)rope_row(r + lane) * kQLora,
                         kRowBytes, &full[slot], pol);
       }
@@ -1409,7 +1414,8 @@ __global__ void __launch_bounds__(pair_threads<NT>(), 1)
         const int nrows = min(kTaskRows, seq.r1 - r0);
         for (int e = tid; e < kTaskRows * NT; e += kConsumers) {
           const int row = e & (kTaskRows - 1), tok = e >> 4;
-          if (row < nrows && tok < a.batch) {
+          if (row < nrows && tok < a.batch &&
+              MLA_IN_BOUNDS(a, r0 + row >= 0 && r0 + row < a.heads * kRope, 2)) {
             float v = 0.f;
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) v += red[(w * NT + tok) * kRedTok + row];
@@ -1481,7 +1487,8 @@ __global__ void __launch_bounds__(pair_threads<NT>(), 1)
                 else keep[1][mt][e] = dacc[mt][0][e];
               }
           }
-        } else {
+        } else if (MLA_IN_BOUNDS(a, j >= 0 && j < 2 && slot_off + (4 * NTL * 32 * 16) <=
+                                                               S::kRecvBytes, 4)) {
           // to the other CTA: same warp slot (w & 3), same lane, head slot j
           const uint32_t peer = (uint32_t)(rank ^ 1);
           const uint32_t rbar_remote = mapa_shared(smem_u32(&recvbar[j]), peer);
@@ -1505,6 +1512,7 @@ __global__ void __launch_bounds__(pair_threads<NT>(), 1)
       for (int j = 0; j < seq.nh; ++j) {
         if (!mbar_wait_bounded(&recvbar[j], 0u, kWaitLimit)) timed_out = true;
         const int h = seq.h0 + j;
+        if (!MLA_IN_BOUNDS(a, h >= 0 && h < a.heads && j < 2, 3)) break;
         uint8_t* slotp = smem + S::oRecv + j * S::kRecvBytes + slot_off;
         float v[4][NTL][4];
 #pragma unroll

@@ -212,7 +212,9 @@ __global__ void __maxnreg__(112)
         const int h = seq.head(k), p0 = seq.p0(k);
         if (lane == 0) mbar_arrive_expect_tx(&full[slot], kSmStage);
         __syncwarp();
-        if (lane < kSmRows)
+        if (!MLA_IN_BOUNDS(a, h >= 0 && h < a.heads && p0 >= 0 && p0 + kSmRows <= kNope, 10) ||
+            !MLA_IN_BOUNDS(a, slot >= 0 && slot < kSmSlots, 11)) {
+        } else if (lane < kSmRows)
           bulk_g2s_hint(buf + lane * kRowBytes,
                         a.w_qb + ((int64_t)h * kHeadRows + p0 + lane) * kQLora, kRowBytes,
                         &full[slot], pol);
@@ -225,7 +227,7 @@ __global__ void __maxnreg__(112)
         const int n = min(kSmRows, seq.r1 - r);
         if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)(n * kRowBytes));
         __syncwarp();
-        if (lane < n)
+        if (lane < n && MLA_IN_BOUNDS(a, r + lane >= 0 && r + lane < a.heads * kRope, 10))
           bulk_g2s_hint(buf + lane * kRowBytes, a.w_qb + (int64_t)small_rope_row(r + lane) * kQLora,
                         kRowBytes, &full[slot], pol);
       }
@@ -338,7 +340,8 @@ __global__ void __maxnreg__(112)
           const int rr_ = r + warp;
 #pragma unroll
           for (int t = 0; t < NT; ++t)
-            if (lane == t && t < a.batch)
+            if (lane == t && t < a.batch &&
+                MLA_IN_BOUNDS(a, rr_ >= 0 && rr_ < a.heads * kRope, 13))
               put_q(a, a.q_pe,
                     (int64_t)t * a.qp_ts + (int64_t)(rr_ / kRope) * a.qp_hs + rr_ % kRope, s[t],
                     qsi);
@@ -388,7 +391,8 @@ __global__ void __maxnreg__(112)
               keep[1][t][1] = acc[t][1];
             }
           }
-        } else {
+        } else if (MLA_IN_BOUNDS(a, j >= 0 && j < 2 && owner >= 0 && owner < C && lc >= 0 &&
+                                          lc + 2 <= S::kCols, 12)) {
           // owner's recv[j][rank][lc .. lc + 1][token]
           const uint32_t peer = (uint32_t)owner;
           const uint32_t rb = mapa_shared(smem_u32(&rbar[j]), peer);
@@ -428,6 +432,7 @@ __global__ void __maxnreg__(112)
         }
       }
       const int h = seq.h0 + j;
+      if (!MLA_IN_BOUNDS(a, h >= 0 && h < a.heads && 2 * tid + 2 <= kKvLora, 13)) break;
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
         if (t >= a.batch) continue;

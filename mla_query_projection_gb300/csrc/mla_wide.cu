@@ -224,6 +224,19 @@ __device__ __forceinline__ const uint8_t* wide_tile(const DecodeArgs& a, int kin
   return a.wide_ukt + ((size_t)h * 8 + 4 * half + bx) * kWideBox;  // 2 ct + pa
 }
 
+// Checks builds: whether wide_tile's box lies inside its packed copy (the
+// sizes wide_qb_bytes and wide_ukt_bytes allocate).
+__device__ __forceinline__ bool wide_tile_in_bounds(const DecodeArgs& a, int kind, int h, int half,
+                                                    int bx, int single) {
+  const int64_t H = a.heads;
+  if (kind == kUnitAbs) return h >= 0 && h < H && bx >= 0 && bx < 4 && (half == 0 || half == 1);
+  const int64_t idx =
+      kind == kUnitNope
+          ? (int64_t)(h * 2 + half) * kWideAtoms + bx
+          : H * 2 * kWideAtoms + (int64_t)(h * 2 + half) * (single ? kWideSingleBoxes : kWideAtoms) + bx;
+  return h >= 0 && bx >= 0 && idx >= 0 && idx < (H + (H + 1) / 2) * 2 * kWideAtoms;
+}
+
 __global__ void __launch_bounds__(kWideThreads, 1)
     mla_wide_kernel(const DecodeArgs a, const __grid_constant__ WideSplit split) {
   using S = WideSmem;
@@ -314,8 +327,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
               !mbar_wait_bounded(&empty[slot], (uint32_t)(((k / kWideSlots) - 1) & 1), kWaitLimit))
             timed_out = true;
           mbar_arrive_expect_tx(&full[slot], kWideBox);
-          bulk_g2s_hint(smem + S::oRing + slot * kWideBox, wide_tile(a, kind, h, rank, bx, seq.single),
-                        kWideBox, &full[slot], pol);
+          if (MLA_IN_BOUNDS(a, wide_tile_in_bounds(a, kind, h, rank, bx, seq.single), 5) &&
+              MLA_IN_BOUNDS(a, slot >= 0 && slot < kWideSlots, 6))
+            bulk_g2s_hint(smem + S::oRing + slot * kWideBox,
+                          wide_tile(a, kind, h, rank, bx, seq.single), kWideBox, &full[slot], pol);
           if (bx == 0 && u < 4) trace_stamp(a, 24 + u);  // unit u's first box issued
         }
       }
@@ -367,6 +382,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         const int half_nb = nb / 2;
         for (int bx = 0; bx < nb; ++bx) {
           if (!mbar_wait_bounded(&full[slot], fphase, kWaitLimit)) timed_out = true;
+          // TMEM: a Q_B partial at dcol + 64 * (bx >= half_nb), an absorption
+          // column tile at dcol + 64 * (bx / 2), each 64 columns wide
+          if (!MLA_IN_BOUNDS(a, dcol >= 0 && dcol + (kind == kUnitAbs ? 128 : 128) <= kWideTmemCols, 6))
+            break;
           tc_fence_after();
           const uint64_t da = dring + (uint64_t)(slot * (kWideBox >> 4));
           if (kind == kUnitAbs) {
@@ -468,7 +487,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             float v[32];
             tmem_ld32(tmem + lane_base + kWideAbsCol + 128 * ab + kWideTok * ct + t0, v);
             const int nt_here = min(kWideHalfTok, a.batch - t0);
-            if (nt_here > 0)
+            if (nt_here > 0 && MLA_IN_BOUNDS(a, h >= 0 && h < H && 256 * rank + 128 * ct + m < kKvLora, 7))
               put_q_run(a, a.q_latent,
                         (int64_t)t0 * a.ql_ts + (int64_t)h * a.ql_hs + 256 * rank + 128 * ct + m,
                         a.ql_ts, v, nt_here, qsi);
@@ -525,6 +544,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           // K-major swizzled, two atoms (each head has its own tile); this
           // CTA writes its 32 token rows and copies them into the other CTA's
           const int j = h - seq.h0;
+          if (!MLA_IN_BOUNDS(a, j == 0 || j == 1, 8)) continue;
           uint8_t* qt = smem + S::oQt + j * S::kQtBytes;
           uint8_t* qa = qt + (m >> 6) * S::kQtAtom;
 #pragma unroll
@@ -542,7 +562,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           }
         } else if (seq.single) {
           // head h: row 16 (m / 32) + m % 32 in TMEM lanes with m % 32 < 16
-          if ((m & 31) < 16) {
+          if ((m & 31) < 16 && MLA_IN_BOUNDS(a, h >= 0 && h < H, 7)) {
             const int nt_here = min(kWideHalfTok, a.batch - my0);
             put_q_run(a, a.q_pe,
                       (int64_t)my0 * a.qp_ts + (int64_t)h * a.qp_hs + 16 * (m >> 5) + (m & 15),
@@ -617,8 +637,9 @@ __global__ void __launch_bounds__(192) mla_wide_norm_kernel(const DecodeArgs a) 
   }
   // chunk j: K half j / 96, atom (j % 96) / 8, 16-byte chunk j % 8 of row t
   const int half = j / 96, cc = j % 96, at = cc >> 3, c = cc & 7;
-  *reinterpret_cast<uint4*>(a.wide_xq + ((size_t)(half * kWideAtoms + at) * kWideTok) * 128 +
-                            t * 128 + ((c ^ (t & 7)) << 4)) = o;
+  const size_t xo = ((size_t)(half * kWideAtoms + at) * kWideTok) * 128 + t * 128 + ((c ^ (t & 7)) << 4);
+  if (MLA_IN_BOUNDS(a, t < kWideTok && xo + 16 <= (size_t)2 * kWideAtoms * kWideTok * 128, 9))
+    *reinterpret_cast<uint4*>(a.wide_xq + xo) = o;
   if (t < a.batch && warp < 2) kv_insert_loaded(a, j, red2, kvl);
   __syncthreads();
   if (j == 0) trace_stamp(a, 62);  // its rows written
