@@ -78,15 +78,24 @@ int encode_uk_map(CUtensorMap* map, const void* w_uk, int heads) {
 //   hand-off kernel, tensor cores, token groups of 8 or 16 (any B).
 enum class Kernel { kSmall, kAbsorbMma, kAbsorbPair, kWide, kHandoff };
 
-// The default path takes tensor cores from one token on: measured on GB300
-// against the FP32-FMA small-batch kernel (B = 1: 8.19 against 10.6 us at 64
-// heads, 14.7 against 17.2 at 128, 5.43 against 5.56 at 16; B = 2: 8.19
-// against 14.1 us at 64 heads).  Both paths stream every weight byte once;
-// after the programmatic-dependent-launch wait a step is bound by its
-// consumers, and the per-row FMA work there is slower than the MMA tiles.
+// The default path (measured on GB300, us per step, FMA kernel against the
+// tensor-core kernel the batch would otherwise take):
+//  * one token, head counts the paired kernel does not serve (those the
+//    partials kernel would take, up to about 50 heads on 152 SMs): FP32 FMAs,
+//    8 heads 4.09 against 4.83, 16 heads 5.19 / 5.42, 32 heads 6.55 / 7.40,
+//    48 heads 8.55 / 9.90;
+//  * everything else: tensor cores.  One token where the paired kernel runs:
+//    56 heads 9.25 against 8.01, 64 heads 10.27 / 8.15, 128 heads 17.4 /
+//    14.7; two tokens: 16 heads 8.51 / 6.03, 64 heads 14.97 / 8.16.
+// Both stream every weight byte once; after the programmatic-dependent-launch
+// wait a step is bound by its consumers: the FMA kernel's clusters close each
+// head through distributed shared memory, where the partials kernel makes an
+// L2 round trip, but its per-row FMA work is slower than the paired kernel's
+// tensor-core tiles.
 int pick_kernel(const mla_query* h, int batch, Kernel* k, int* nt) {
   int path = h->path;
-  if (path == MLA_PATH_AUTO) path = MLA_PATH_MMA;
+  if (path == MLA_PATH_AUTO)
+    path = batch == 1 && h->pair_ctas == 0 && h->small_ctas > 0 ? MLA_PATH_FMA : MLA_PATH_MMA;
   if (path == MLA_PATH_FMA) {
     if (batch > 2 || h->small_ctas == 0) return MLA_EUNSUPPORTED;
     *k = Kernel::kSmall;

@@ -274,17 +274,30 @@ __device__ void kv_insert(const DecodeArgs& a, int b, int lt, float* red2) {
 // l + 32 of the 64-thread insert, and the sums are formed in the same order
 // (each group's FMA chain, each group reduced across the warp, group 0 plus
 // group 1), so the bytes written are the same.
-__device__ void kv_insert_warp(const DecodeArgs& a, int b, int lane) {
-  const int64_t slot = a.slots[b];
+// The inputs of one lane's share of the one-warp insert (kv_insert_warp),
+// loaded ahead of its arithmetic (kv_insert_warp_loaded).
+struct KvWarpLoads {
+  int64_t slot;
+  uint4 v[2], gv[2], pe;
+};
+__device__ __forceinline__ KvWarpLoads kv_insert_warp_load(const DecodeArgs& a, int b, int lane) {
+  KvWarpLoads l;
+  l.slot = a.slots[b];
   const uint16_t* kv = a.kv_c + (int64_t)b * a.kv_c_stride;
-  uint4 v[2], gv[2];
 #pragma unroll
   for (int g = 0; g < 2; ++g) {
-    v[g] = *reinterpret_cast<const uint4*>(kv + 8 * (lane + 32 * g));
-    gv[g] = *reinterpret_cast<const uint4*>(a.gamma_kv + 8 * (lane + 32 * g));
+    l.v[g] = *reinterpret_cast<const uint4*>(kv + 8 * (lane + 32 * g));
+    l.gv[g] = *reinterpret_cast<const uint4*>(a.gamma_kv + 8 * (lane + 32 * g));
   }
-  uint4 pe = make_uint4(0, 0, 0, 0);
-  if (lane < 8) pe = *reinterpret_cast<const uint4*>(a.k_pe + (int64_t)b * a.k_pe_stride + 8 * lane);
+  l.pe = make_uint4(0, 0, 0, 0);
+  if (lane < 8) l.pe = *reinterpret_cast<const uint4*>(a.k_pe + (int64_t)b * a.k_pe_stride + 8 * lane);
+  return l;
+}
+
+__device__ void kv_insert_warp_loaded(const DecodeArgs& a, int lane, const KvWarpLoads& l) {
+  const int64_t slot = l.slot;
+  const uint4 v[2] = {l.v[0], l.v[1]}, gv[2] = {l.gv[0], l.gv[1]};
+  const uint4 pe = l.pe;
   const bool ds = a.layout == MLA_KV_FP8_DS_MLA;
   const bool nv = a.layout == MLA_KV_NVFP4_DS_MLA;
   const float ks = (ds || nv) ? 1.0f : *a.k_scale;
@@ -300,6 +313,10 @@ __device__ void kv_insert_warp(const DecodeArgs& a, int b, int lane) {
     kv_group_norm(x[g], gv[g], rr, n);
     kv_store_group(a, row, n, g == 0 ? pe : make_uint4(0, 0, 0, 0), lane + 32 * g, ds, nv, ks);
   }
+}
+
+__device__ void kv_insert_warp(const DecodeArgs& a, int b, int lane) {
+  kv_insert_warp_loaded(a, lane, kv_insert_warp_load(a, b, lane));
 }
 
 }  // namespace

@@ -158,7 +158,7 @@ __global__ void __maxnreg__(112)
   uint64_t* qbar = reinterpret_cast<uint64_t*>(smem + S::oQbar);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int i = blockIdx.x, P = gridDim.x;
+  const int i = blockIdx.x;
   const int g = i / C, rank = i % C;  // cluster (C, 1, 1): rank = blockIdx.x % C
   const SmallSeq<C> seq{split.head[g], split.head[g + 1] - split.head[g], rank, split.rope[i],
                         split.rope[i + 1]};
@@ -238,12 +238,22 @@ __global__ void __maxnreg__(112)
         (void)mbar_wait_bounded(&full[k % kSmSlots], (uint32_t)((k / kSmSlots) & 1), kWaitLimit);
   } else {
     // ================= consumer warps 0-7 ============================
+    // gamma_q is a weight: one token loads it before the wait (two tokens
+    // need those registers for their second xq row)
+    uint4 gq[NT == 1 ? 6 : 1];
+    if constexpr (NT == 1) {
+#pragma unroll
+      for (int j = 0; j < 6; ++j)
+        gq[j] = *reinterpret_cast<const uint4*>(a.gamma_q + 8 * (lane + 32 * j));
+    }
     pdl_wait();
     if (tid == 0) trace_stamp(a, 3);
-    // the KV rows first (CTA i inserts tokens i, i + P, ...), before the
-    // normalised q_a row takes its registers
-    if (warp == kConsumerWarps - 1)
-      for (int t = i; t < a.batch; t += P) kv_insert_warp(a, t, lane);
+    // The KV row of token i (CTA i < B): its loads go out with the q_a row's,
+    // its arithmetic after the normalisation; a CTA inserts at most one
+    // token (B <= 2 < P).
+    const bool kv_here = warp == kConsumerWarps - 1 && i < a.batch;
+    KvWarpLoads kvl;
+    if (kv_here) kvl = kv_insert_warp_load(a, i, lane);
     // q_a RMSNorm of every token, in every warp: lane l keeps columns
     // 8 (l + 32 j) .. + 7, j < 6, of xq as BF16 pairs
     uint4 xq[NT][6];
@@ -266,7 +276,8 @@ __global__ void __maxnreg__(112)
       const float rr = __frsqrt_rn(__fadd_rn(__fdiv_rn(ss, 1536.0f), a.eps));
 #pragma unroll
       for (int j = 0; j < 6; ++j) {
-        const uint4 gj = *reinterpret_cast<const uint4*>(a.gamma_q + 8 * (lane + 32 * j));
+        const uint4 gj = NT == 1 ? gq[NT == 1 ? j : 0]
+                                 : *reinterpret_cast<const uint4*>(a.gamma_q + 8 * (lane + 32 * j));
         const uint32_t gw[4] = {gj.x, gj.y, gj.z, gj.w};
         const uint32_t vv[4] = {xq[t][j].x, xq[t][j].y, xq[t][j].z, xq[t][j].w};
         uint32_t o[4];
@@ -283,6 +294,7 @@ __global__ void __maxnreg__(112)
           *reinterpret_cast<uint4*>(a.q_c + (int64_t)t * kQLora + 8 * (lane + 32 * j)) = xq[t][j];
       }
     }
+    if (kv_here) kv_insert_warp_loaded(a, lane, kvl);
     if constexpr (NT > 1) named_barrier(4, kConsumers);  // xq rows written (before any wait)
     if (tid == 0) trace_stamp(a, 2);
     const float qsi = load_qsi(a);

@@ -231,7 +231,8 @@ def test_small_head_count_repeated_calls_close_every_head():
         (2, 128, B.MLA_PATH_FMA, "mla_small_kernel<2,2>"),
         (12, 64, B.MLA_PATH_AUTO, "mla_absorb_pair_kernel<16>"),
         (40, 64, B.MLA_PATH_AUTO, "mla_wide_norm_kernel+mla_wide_kernel"),
-        (1, 16, B.MLA_PATH_AUTO, "mla_absorb_mma_kernel<8>"),
+        (1, 16, B.MLA_PATH_AUTO, "mla_small_kernel<1,"),
+        (2, 16, B.MLA_PATH_AUTO, "mla_absorb_mma_kernel<8>"),
         (1, 16, B.MLA_PATH_FMA, "mla_small_kernel<1,"),
         (2, 16, B.MLA_PATH_FMA, "mla_small_kernel<2,"),
     ],
