@@ -82,11 +82,11 @@ enum class Kernel { kSmall, kAbsorbMma, kAbsorbPair, kWide, kHandoff };
 // tensor-core kernel the batch would otherwise take):
 //  * one token, head counts the paired kernel does not serve (those the
 //    partials kernel would take, up to about 50 heads on 152 SMs): FP32 FMAs,
-//    8 heads 4.09 against 4.83, 16 heads 5.19 / 5.42, 32 heads 6.55 / 7.40,
-//    48 heads 8.55 / 9.90;
+//    8 heads 4.10 against 4.82, 16 heads 5.14 / 5.42, 32 heads 6.01 / 7.39,
+//    48 heads 8.35 / 9.89;
 //  * everything else: tensor cores.  One token where the paired kernel runs:
-//    56 heads 9.25 against 8.01, 64 heads 10.27 / 8.15, 128 heads 17.4 /
-//    14.7; two tokens: 16 heads 8.51 / 6.03, 64 heads 14.97 / 8.16.
+//    56 heads 8.63 against 7.98, 64 heads 9.26 / 8.15; two tokens: 16 heads
+//    8.44 / 6.11.
 // Both stream every weight byte once; after the programmatic-dependent-launch
 // wait a step is bound by its consumers: the FMA kernel's clusters close each
 // head through distributed shared memory, where the partials kernel makes an

@@ -9,18 +9,17 @@
 // GB300 design.  With one or two tokens a weight element feeds one or two
 // FMAs, so the projection is no dense contraction: plain FP32 FMAs keep up
 // with the stream, and the kernel is shaped around the stream instead.
-//  * Two CTAs per SM.  A CTA holds a 96 KiB ring (three 32 KiB stages) and
-//    about 105 KiB of shared memory in all, so the CTA of the next step fits
-//    beside it.  The page's class docstring loads the static weights before
-//    the programmatic-dependent-launch wait; here that means the next step's
-//    producer fills its ring while this step computes its last stages,
-//    stores its outputs and exits, instead of after.
 //  * Clusters of C CTAs (2, 4 or 8) own whole heads (at most two per
 //    cluster); rank r takes nope rows [r 128/C, (r+1) 128/C) of each head and
 //    the same rows of W_UK, and rope rows fill every CTA to an even byte
-//    share.  A stage is 8 consecutive Q_B rows (24 KiB, contiguous in
-//    global memory) plus, for nope rows, their 8 W_UK rows (8 KiB): two 1-D
-//    bulk copies.
+//    share.  A stage is 8 consecutive Q_B rows (24 KiB) plus, for nope rows,
+//    their 8 W_UK rows (8 KiB), one 1-D bulk copy per row issued by separate
+//    lanes.  The static weights are copied before the programmatic-dependent-
+//    launch wait, as the page's class docstring has them: a 6-stage ring
+//    (192 KiB) holds a small head count's whole share (16 heads: at most
+//    128 KiB a CTA) before the wait ends.  (A 3-stage ring of about 105 KiB
+//    let the next step's CTA share the SM; that measured slower, 10.3 against
+//    9.3 us at 64 heads, and gained nothing at 16.)
 //  * Warp w computes row w of a stage: each lane dots 48 of the row's 1536
 //    values with the normalised xq it keeps in registers (BF16 pairs), then
 //    the warp adds the lanes.  The 8 BF16-rounded nope q values go through
@@ -30,6 +29,8 @@
 //    rank owns (rank r owns columns [r 512/C, (r+1) 512/C)) into that CTA's
 //    shared memory (st.async, counted on its mbarrier); each owner adds the
 //    C partials in rank order (row order of the head) and writes q_latent.
+//    No L2 round trip closes a head, which is where this kernel beats the
+//    tensor-core partials kernel at small head counts.
 // Every wait is bounded (MLA_DEVERR_TIMEOUT instead of a hang).
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -48,7 +49,7 @@ constexpr int kSmQbBytes = kSmRows * kRowBytes;    // 24 KiB
 constexpr int kSmUkBytes = kSmRows * kKvLora * 2;  // 8 KiB
 constexpr int kSmStage = kSmQbBytes + kSmUkBytes;  // 32 KiB
 #ifndef MLA_SMALL_SLOTS
-#define MLA_SMALL_SLOTS 3
+#define MLA_SMALL_SLOTS 6
 #endif
 constexpr int kSmSlots = MLA_SMALL_SLOTS;
 #ifndef MLA_SMALL_PREFETCH
@@ -142,7 +143,8 @@ __device__ __forceinline__ void dot_chunk(const uint4 w, const uint4 (&x)[NT], f
   }
 }
 
-// 112 registers a thread: two CTAs of 288 threads fill the SM's 64K.
+// 112 registers a thread (room for two CTAs of 288 threads an SM when the
+// ring is three stages deep).
 template <int NT, int C>
 __global__ void __maxnreg__(112)
     mla_small_kernel(const DecodeArgs a, const __grid_constant__ SmallSplit split) {
@@ -475,7 +477,7 @@ cudaLaunchConfig_t small_config(int ctas, cudaStream_t stream, cudaLaunchAttribu
   attr[0].val.clusterDim.x = C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  // one CTA of this kernel per SM: the second slot is for the next step's
+  // spread the clusters over the SMs, one CTA of this kernel per SM
   attr[1].id = cudaLaunchAttributeClusterSchedulingPolicyPreference;
   attr[1].val.clusterSchedulingPolicyPreference = cudaClusterSchedulingPolicySpread;
   attr[2].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -493,16 +495,15 @@ cudaError_t prepare_small_one() {
       mla_small_kernel<NT, C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
       SmallSmem<NT, C>::kAlloc > 120 * 1024 ? SmallSmem<NT, C>::kAlloc : 120 * 1024);
   if (e != cudaSuccess) return e;
-  // the whole unified memory as shared memory, so that two CTAs fit an SM
-  // (the default carveout measured room for one)
+  // the whole unified memory as shared memory (with a 3-stage ring two CTAs
+  // then fit an SM; the default carveout measured room for one)
   return cudaFuncSetAttribute(mla_small_kernel<NT, C>,
                               cudaFuncAttributePreferredSharedMemoryCarveout,
                               cudaSharedmemCarveoutMaxShared);
 }
 
 // Clusters that fit with one CTA per SM: the occupancy of a CTA asking for
-// more than half an SM's shared memory (a grid takes one CTA per SM; the
-// second slot is the next step's).
+// more than half an SM's shared memory (a grid takes one CTA per SM).
 template <int NT, int C>
 int small_max_clusters_one() {
   cudaLaunchAttribute attr[3];
