@@ -82,11 +82,11 @@ enum class Kernel { kSmall, kAbsorbMma, kAbsorbPair, kWide, kHandoff };
 // tensor-core kernel the batch would otherwise take):
 //  * one token, head counts the paired kernel does not serve (those the
 //    partials kernel would take, up to about 50 heads on 152 SMs): FP32 FMAs,
-//    8 heads 4.10 against 4.82, 16 heads 5.14 / 5.42, 32 heads 6.01 / 7.39,
-//    48 heads 8.35 / 9.89;
+//    8 heads 3.96 against 4.83, 16 heads 4.90 / 5.42, 32 heads 5.73 / 7.39,
+//    48 heads 7.50 / 9.89;
 //  * everything else: tensor cores.  One token where the paired kernel runs:
-//    56 heads 8.63 against 7.98, 64 heads 9.26 / 8.15; two tokens: 16 heads
-//    8.44 / 6.11.
+//    56 heads 8.07 against 8.01, 64 heads 8.45 / 8.17, 128 heads 14.86 /
+//    14.70; two tokens: 16 heads 7.96 / 6.11.
 // Both stream every weight byte once; after the programmatic-dependent-launch
 // wait a step is bound by its consumers: the FMA kernel's clusters close each
 // head through distributed shared memory, where the partials kernel makes an

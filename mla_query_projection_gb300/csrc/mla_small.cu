@@ -1,5 +1,4 @@
-// mla_small.cu - the decode step for one or two tokens on FP32 FMAs, shaped
-// so that the CTAs of consecutive steps share each SM.
+// mla_small.cu - the decode step for one or two tokens on FP32 FMAs.
 //
 // What it computes is the step of page "mla.query", class MlaQuery (method
 // kernel, the small-batch path, and insert / insert_ds / insert_nvfp4 /
@@ -12,19 +11,22 @@
 //  * Clusters of C CTAs (2, 4 or 8) own whole heads (at most two per
 //    cluster); rank r takes nope rows [r 128/C, (r+1) 128/C) of each head and
 //    the same rows of W_UK, and rope rows fill every CTA to an even byte
-//    share.  A stage is 8 consecutive Q_B rows (24 KiB) plus, for nope rows,
-//    their 8 W_UK rows (8 KiB), one 1-D bulk copy per row issued by separate
-//    lanes.  The static weights are copied before the programmatic-dependent-
-//    launch wait, as the page's class docstring has them: a 6-stage ring
-//    (192 KiB) holds a small head count's whole share (16 heads: at most
-//    128 KiB a CTA) before the wait ends.  (A 3-stage ring of about 105 KiB
-//    let the next step's CTA share the SM; that measured slower, 10.3 against
-//    9.3 us at 64 heads, and gained nothing at 16.)
-//  * Warp w computes row w of a stage: each lane dots 48 of the row's 1536
-//    values with the normalised xq it keeps in registers (BF16 pairs), then
-//    the warp adds the lanes.  The 8 BF16-rounded nope q values go through
-//    shared memory to all 256 threads, and thread t adds their products with
-//    W_UK columns 2t, 2t + 1 into its FP32 absorption sums.
+//    share.  A stage is 16 consecutive Q_B rows (48 KiB) plus, for nope
+//    rows, their 16 W_UK rows (16 KiB), one 1-D bulk copy per row issued by
+//    separate lanes.  The static weights are copied before the programmatic-
+//    dependent-launch wait, as the page's class docstring has them: a 3-stage
+//    ring (192 KiB, one CTA per SM) holds a small head count's whole share
+//    (16 heads: at most 128 KiB a CTA) before the wait ends.  (A ring of
+//    about 105 KiB let the next step's CTA share the SM; that measured
+//    slower, 10.3 against 9.3 us at 64 heads, and gained nothing at 16.)
+//  * Warp w computes rows w and w + 8 of a stage, their chains interleaved:
+//    each lane dots 48 of a row's 1536 values with the normalised xq it keeps
+//    in registers (BF16 pairs), then the warp adds the lanes.  The 16
+//    BF16-rounded nope q values go through shared memory to all 256 threads,
+//    and thread t adds their products with W_UK columns 2t, 2t + 1 into its
+//    FP32 absorption sums.  (Stages of 8 rows, one a warp, measured slower:
+//    the shuffles and the barrier of a stage are paid per row; 9.32 against
+//    8.45 us at 64 heads, 5.24 against 4.89 at 16.)
 //  * After a head's last stage each thread sends the sums of columns another
 //    rank owns (rank r owns columns [r 512/C, (r+1) 512/C)) into that CTA's
 //    shared memory (st.async, counted on its mbarrier); each owner adds the
@@ -44,12 +46,19 @@ namespace mla {
 
 namespace {
 
-constexpr int kSmRows = 8;                         // Q_B rows per stage: one per consumer warp
-constexpr int kSmQbBytes = kSmRows * kRowBytes;    // 24 KiB
-constexpr int kSmUkBytes = kSmRows * kKvLora * 2;  // 8 KiB
-constexpr int kSmStage = kSmQbBytes + kSmUkBytes;  // 32 KiB
+// Q_B rows per stage: MLA_SMALL_ROWS_PER_WARP (1 or 2) per consumer warp.
+#ifndef MLA_SMALL_ROWS_PER_WARP
+#define MLA_SMALL_ROWS_PER_WARP 2
+#endif
+constexpr int kSmRowsPerWarp = MLA_SMALL_ROWS_PER_WARP;
+constexpr int kSmRows = 8 * kSmRowsPerWarp;
+static_assert(kSmRowsPerWarp == 1 || kSmRowsPerWarp == 2, "rows per warp");
+static_assert(2 * kSmRows <= 32, "one producer lane per copy of a stage");
+constexpr int kSmQbBytes = kSmRows * kRowBytes;    // 24 or 48 KiB
+constexpr int kSmUkBytes = kSmRows * kKvLora * 2;  // 8 or 16 KiB
+constexpr int kSmStage = kSmQbBytes + kSmUkBytes;  // 32 or 64 KiB
 #ifndef MLA_SMALL_SLOTS
-#define MLA_SMALL_SLOTS 6
+#define MLA_SMALL_SLOTS 3
 #endif
 constexpr int kSmSlots = MLA_SMALL_SLOTS;
 #ifndef MLA_SMALL_PREFETCH
@@ -66,7 +75,7 @@ struct SmallSmem {
   static constexpr int kRecvBytesIn = (C - 1) * kCols * NT * 4;  // what the peers send
   static constexpr int oRing = 0;
   static constexpr int oRecv = kSmSlots * kSmStage;     // [2 heads][kRecvHead]
-  static constexpr int oQv = oRecv + 2 * kRecvHead;     // [2][8 rows][NT] FP32
+  static constexpr int oQv = oRecv + 2 * kRecvHead;     // [2][kSmRows][NT] FP32
   static constexpr int oFull = oQv + 2 * kSmRows * NT * 4;
   static constexpr int oEmpty = oFull + kSmSlots * 8;
   static constexpr int oRbar = oEmpty + kSmSlots * 8;   // [2] received partials
@@ -78,12 +87,11 @@ struct SmallSmem {
   static constexpr int kBytes = oXs + kXsBytes;
   static constexpr int kAlloc = kBytes + 128;
   static_assert(kStagesPerHead * kSmRows * C == kNope, "stages per head");
-  static_assert(kSmSlots != 3 || 2 * (kAlloc + 1024) <= 233472, "two CTAs per SM");
-  static_assert(kSmSlots != 3 || kAlloc <= 120 * 1024, "the one-per-SM occupancy query asks for more");
+  static_assert(kAlloc <= 227 * 1024, "shared memory of one CTA");
 };
 
 // This CTA's stages: the nope stages of each head of its cluster, then its
-// rope rows in stages of up to 8.
+// rope rows in stages of up to kSmRows.
 template <int C>
 struct SmallSeq {
   static constexpr int kPerHead = kNope / C / kSmRows;
@@ -98,8 +106,8 @@ __device__ __forceinline__ int small_rope_row(int r) {  // rope index -> W_QB ro
   return (r / kRope) * kHeadRows + kNope + (r % kRope);
 }
 
-// Stage k of a CTA into L2 (no shared memory, no completion): its 8 Q_B
-// rows and, for nope rows, their 8 W_UK rows; rope rows may span two heads.
+// Stage k of a CTA into L2 (no shared memory, no completion): its Q_B rows
+// and, for nope rows, their W_UK rows; rope rows may span two heads.
 template <int C>
 __device__ __forceinline__ void small_prefetch_stage(const DecodeArgs& a, const SmallSeq<C>& seq,
                                                      int k) {
@@ -143,10 +151,14 @@ __device__ __forceinline__ void dot_chunk(const uint4 w, const uint4 (&x)[NT], f
   }
 }
 
-// 112 registers a thread (room for two CTAs of 288 threads an SM when the
-// ring is three stages deep).
+// One CTA an SM (the ring takes most of the shared memory), so up to
+// 65536 / 288 = 227 registers a thread would fit; 112 measured faster than
+// 160 (8.45 against 8.60 us at 64 heads, one spill of 8 bytes at C = 8).
+#ifndef MLA_SMALL_MAXNREG
+#define MLA_SMALL_MAXNREG 112
+#endif
 template <int NT, int C>
-__global__ void __maxnreg__(112)
+__global__ void __maxnreg__(MLA_SMALL_MAXNREG)
     mla_small_kernel(const DecodeArgs a, const __grid_constant__ SmallSplit split) {
   using S = SmallSmem<NT, C>;
   extern __shared__ uint8_t smem_raw[];
@@ -189,7 +201,8 @@ __global__ void __maxnreg__(112)
   if (warp == kConsumerWarps) {
     // ================= producer: weights only, no PDL wait ============
     // A stage's copies are issued by separate lanes in one instruction (a Q_B
-    // row of 3 KiB per lane 0-7, a W_UK row of 1 KiB per lane 8-15): copies
+    // row of 3 KiB per lane below kSmRows, a W_UK row of 1 KiB per lane from
+    // there to 2 kSmRows): copies
     // one thread issues complete one after another, copies of different
     // threads side by side.
     const uint64_t pol = l2_policy_evict_first();
@@ -325,15 +338,15 @@ __global__ void __maxnreg__(112)
       const bool nope = k < seq.nope();
       const int r = seq.r0 + (k - seq.nope()) * kSmRows;  // first rope row (rope stages)
       const int rows = nope ? kSmRows : min(kSmRows, seq.r1 - r);
-      // ---- Q_B row `warp` of the stage: 48 products per lane, then the warp
-      float s[NT];
+      // ---- Q_B rows warp + 8 i of the stage: 48 products per lane, then
+      // the warp; the rows' chains interleave
+      float s[kSmRowsPerWarp][NT];
+      {
+        float s4[kSmRowsPerWarp][NT][4];
 #pragma unroll
-      for (int t = 0; t < NT; ++t) s[t] = 0.f;
-      if (warp < rows) {
-        const uint4* row = reinterpret_cast<const uint4*>(buf + warp * kRowBytes);
-        float s4[NT][4];
+        for (int i = 0; i < kSmRowsPerWarp; ++i)
 #pragma unroll
-        for (int t = 0; t < NT; ++t) s4[t][0] = s4[t][1] = s4[t][2] = s4[t][3] = 0.f;
+          for (int t = 0; t < NT; ++t) s4[i][t][0] = s4[i][t][1] = s4[i][t][2] = s4[i][t][3] = 0.f;
 #pragma unroll
         for (int j = 0; j < 6; ++j) {
           uint4 xj[NT];
@@ -342,40 +355,50 @@ __global__ void __maxnreg__(112)
             xj[t] = NT == 1 ? xq[t][j]
                             : *reinterpret_cast<const uint4*>(smem + S::oXs + t * kRowBytes +
                                                                16 * (lane + 32 * j));
-          dot_chunk<NT>(row[lane + 32 * j], xj, s4);
+#pragma unroll
+          for (int i = 0; i < kSmRowsPerWarp; ++i)
+            if (warp + 8 * i < rows)
+              dot_chunk<NT>(reinterpret_cast<const uint4*>(buf + (warp + 8 * i) * kRowBytes)[lane + 32 * j],
+                            xj, s4[i]);
         }
 #pragma unroll
-        for (int t = 0; t < NT; ++t)
-          s[t] = warp_sum((s4[t][0] + s4[t][1]) + (s4[t][2] + s4[t][3]));
+        for (int i = 0; i < kSmRowsPerWarp; ++i)
+#pragma unroll
+          for (int t = 0; t < NT; ++t)
+            s[i][t] = warp_sum((s4[i][t][0] + s4[i][t][1]) + (s4[i][t][2] + s4[i][t][3]));
       }
       if (!nope) {
         // ---- rope rows -> q_pe ------------------------------------------
-        if (warp < rows) {
-          const int rr_ = r + warp;
+#pragma unroll
+        for (int i = 0; i < kSmRowsPerWarp; ++i) {
+          if (warp + 8 * i >= rows) continue;
+          const int rr_ = r + warp + 8 * i;
 #pragma unroll
           for (int t = 0; t < NT; ++t)
             if (lane == t && t < a.batch &&
                 MLA_IN_BOUNDS(a, rr_ >= 0 && rr_ < a.heads * kRope, 13))
               put_q(a, a.q_pe,
-                    (int64_t)t * a.qp_ts + (int64_t)(rr_ / kRope) * a.qp_hs + rr_ % kRope, s[t],
-                    qsi);
+                    (int64_t)t * a.qp_ts + (int64_t)(rr_ / kRope) * a.qp_hs + rr_ % kRope,
+                    s[i][t], qsi);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
         if (tid == 0 && k < 14) trace_stamp(a, 48 + k);  // stage k done
         continue;
       }
-      // ---- nope rows: BF16 q of the 8 rows to every thread -------------
+      // ---- nope rows: BF16 q of the stage's rows to every thread --------
       // (nope stages are k = 0 .. nope() - 1: buffer k & 1, its use k >> 1)
       float* qk = qv + (k & 1) * kSmRows * NT;
       if (lane == 0) {
 #pragma unroll
-        for (int t = 0; t < NT; ++t) qk[warp * NT + t] = bf_round(s[t]);
+        for (int i = 0; i < kSmRowsPerWarp; ++i)
+#pragma unroll
+          for (int t = 0; t < NT; ++t) qk[(warp + 8 * i) * NT + t] = bf_round(s[i][t]);
         mbar_arrive(&qbar[k & 1]);
       }
       if (!mbar_wait_bounded(&qbar[k & 1], (uint32_t)((k >> 1) & 1), kWaitLimit))
         timed_out = true;
-      // ---- absorption: W_UK rows p0..p0+7, columns 2 tid and 2 tid + 1 --
+      // ---- absorption: W_UK rows p0.., columns 2 tid and 2 tid + 1 ------
       const uint32_t* uk = reinterpret_cast<const uint32_t*>(buf + kSmQbBytes);
 #pragma unroll
       for (int p = 0; p < kSmRows; ++p) {
