@@ -42,6 +42,27 @@ __device__ __forceinline__ void trace_add(const DecodeArgs& a, int slot, long lo
 #endif
 }
 
+// Trace builds: the time now (0 otherwise), to be stored later by trace_put.
+__device__ __forceinline__ uint64_t trace_now() {
+#ifdef MLA_TRACE
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+#else
+  return 0;
+#endif
+}
+__device__ __forceinline__ void trace_put(const DecodeArgs& a, int slot, uint64_t t) {
+#ifdef MLA_TRACE
+  if (a.trace != nullptr && slot < kTraceSlots)
+    a.trace[(int64_t)(blockIdx.y * gridDim.x + blockIdx.x) * kTraceSlots + slot] = t;
+#else
+  (void)a;
+  (void)slot;
+  (void)t;
+#endif
+}
+
 __device__ __forceinline__ void trace_stamp(const DecodeArgs& a, int slot) {
 #ifdef MLA_TRACE
   if (a.trace != nullptr && slot < kTraceSlots) {

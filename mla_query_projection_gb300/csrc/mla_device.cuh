@@ -138,6 +138,19 @@ __device__ __forceinline__ void cluster_sync() {
       "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The two halves of a cluster barrier, for work that needs no other CTA of
+// the cluster (copies into its own shared memory) and so may start before
+// the cluster has met: every thread arrives once, after its CTA's barriers
+// are initialised (relaxed: fence.mbarrier_init publishes them), and waits
+// before its first access to another CTA's shared memory (and before it
+// arrives again).  Not .aligned: the threads of a warp may reach them apart.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
 // Cluster barrier without memory ordering: only keeps every CTA of the
 // cluster resident until all have arrived.
 __device__ __forceinline__ void cluster_sync_relaxed() {

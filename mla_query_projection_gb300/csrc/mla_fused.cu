@@ -1197,6 +1197,7 @@ __global__ void __launch_bounds__(pair_threads<NT>(), 1)
   const PairSeq seq{split.head[pair], split.head[pair + 1] - split.head[pair], rank,
                     split.rope[i], split.rope[i + 1]};
   const int nst = seq.stages();
+  bool timed_out = false;
 
   if (tid == 0) {
     for (int s = 0; s < ST; ++s) {
@@ -1207,16 +1208,23 @@ __global__ void __launch_bounds__(pair_threads<NT>(), 1)
     mbar_init(&rbar[1], kConsumerWarps);
     mbar_init(&recvbar[0], 1);
     mbar_init(&recvbar[1], 1);
-    // The other CTA's sums of head j land in recv[j]: armed before the pair
-    // meets below, so no byte can arrive before its count is expected.
+    // The other CTA's sums of head j land in recv[j]: armed before this CTA
+    // arrives at the cluster barrier, so no byte can arrive before its count
+    // is expected.
     for (int j = 0; j < seq.nh; ++j) mbar_arrive_expect_tx(&recvbar[j], S::kRecvBytes);
     mbar_fence_init();
     pdl_launch_dependents();
     trace_stamp(a, 0);
   }
   __syncthreads();
-  cluster_sync();  // both CTAs' barriers are initialised and armed
-  bool timed_out = false;
+  // The cluster barrier's first phase orders the other CTA's recvbar before
+  // the first remote store: every thread arrives now (relaxed: the
+  // mbarrier-init fence publishes the barriers; a release arrive measured
+  // slower, 8.07 against 7.94 us at 64 heads), the consumers wait after the
+  // q_a prologue, the other warps at their end.  The producer starts
+  // copying without waiting for the pair.  (The producer initialising its
+  // own ring barriers and issuing before the CTA meets measured 8.18 us.)
+  cluster_arrive_relaxed();
 
   if (warp == kConsumerWarps) {
     // ================= producer: weights only, no PDL wait ============
@@ -1271,12 +1279,14 @@ __global__ void __launch_bounds__(pair_threads<NT>(), 1)
     if (lane == 0)
       for (int k = max(0, nst - ST); k < nst; ++k)
         (void)mbar_wait_bounded(&full[k % ST], (uint32_t)((k / ST) & 1), kWaitLimit);
+    cluster_wait_acquire();
   } else if (warp == kConsumerWarps + 1) {
     // ================= KV insert warp (16 tokens) ====================
     // The CTA's KV rows (kv_c and k_pe are inputs: after the PDL wait), off
     // the consumers' and the producer's paths.
     pdl_wait();
     for (int t = i; t < a.batch; t += P) kv_insert_warp(a, t, lane);
+    cluster_wait_acquire();
   } else {
     // ================= consumer warps 0-7 ============================
     const int g = lane >> 2, q = lane & 3;
@@ -1335,6 +1345,7 @@ __global__ void __launch_bounds__(pair_threads<NT>(), 1)
     if (NT == 8 && warp >= 6)
       for (int t = i; t < a.batch; t += P) kv_insert(a, t, tid - 192, ss_s + kConsumerWarps * NT);
     if (tid == 0) trace_stamp(a, 2);
+    cluster_wait_acquire();  // the other CTA's recvbar armed (long since, by now)
 
     // Columns 64 w .. 64 w + 63 belong to rank 0 for w < 4, to rank 1 else.
     // A warp's slot of a per-head buffer: [m-tile][n-tile][lane][16 B].

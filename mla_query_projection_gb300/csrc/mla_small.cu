@@ -36,6 +36,7 @@
 // Every wait is bounded (MLA_DEVERR_TIMEOUT instead of a hang).
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cstdio>
 
 #include "../../include/mla_query.h"
 #include "mla_common.cuh"
@@ -161,6 +162,7 @@ template <int NT, int C>
 __global__ void __maxnreg__(MLA_SMALL_MAXNREG)
     mla_small_kernel(const DecodeArgs a, const __grid_constant__ SmallSplit split) {
   using S = SmallSmem<NT, C>;
+  const uint64_t t_entry = trace_now();  // slot 1 of a trace build
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
                                              ~static_cast<uintptr_t>(127));
@@ -177,6 +179,7 @@ __global__ void __maxnreg__(MLA_SMALL_MAXNREG)
   const SmallSeq<C> seq{split.head[g], split.head[g + 1] - split.head[g], rank, split.rope[i],
                         split.rope[i + 1]};
   const int nst = seq.stages();
+  bool timed_out = false;
 
   if (tid == 0) {
     for (int s = 0; s < kSmSlots; ++s) {
@@ -187,16 +190,27 @@ __global__ void __maxnreg__(MLA_SMALL_MAXNREG)
     mbar_init(&rbar[1], 1);
     mbar_init(&qbar[0], kConsumerWarps);
     mbar_init(&qbar[1], kConsumerWarps);
-    // the peers' partials of head j land in recv[j]: armed before the
-    // cluster meets below, so no byte can arrive before its count is expected
+    // the peers' partials of head j land in recv[j]: armed before this CTA
+    // arrives at the cluster barrier, so no byte can arrive before its count
+    // is expected
     for (int j = 0; j < seq.nh; ++j) mbar_arrive_expect_tx(&rbar[j], S::kRecvBytesIn);
     mbar_fence_init();
     pdl_launch_dependents();
     trace_stamp(a, 0);
+    trace_put(a, 1, t_entry);
   }
   __syncthreads();
-  cluster_sync();
-  bool timed_out = false;
+  // The cluster barrier's first phase orders the peers' rbar before the
+  // first remote store: every thread arrives now (relaxed: the mbarrier-init
+  // fence publishes the barriers; a release arrive measured slower), the
+  // consumers wait after the q_a prologue, the producer after its last copy.
+  // The producer starts copying without waiting for the cluster.  (Other
+  // start-ups measured: the producer initialising its own ring barriers and
+  // issuing before the CTA meets, with or without holding its second stage
+  // until the programmatic-dependent-launch wait: 8.83 and 8.48 against
+  // 8.47 us at 64 heads, 6.14 and 5.88 against 5.72 at 32; more copies in
+  // flight when the q_a row is loaded delay the prologue.)
+  cluster_arrive_relaxed();
 
   if (warp == kConsumerWarps) {
     // ================= producer: weights only, no PDL wait ============
@@ -205,6 +219,7 @@ __global__ void __maxnreg__(MLA_SMALL_MAXNREG)
     // there to 2 kSmRows): copies
     // one thread issues complete one after another, copies of different
     // threads side by side.
+    if (lane == 0) trace_stamp(a, 4);  // the producer starts
     const uint64_t pol = l2_policy_evict_first();
     if (kSmPrefetch && lane == 0)
       for (int k = kSmSlots; k < min(nst, 2 * kSmSlots); ++k) small_prefetch_stage<C>(a, seq, k);
@@ -251,6 +266,7 @@ __global__ void __maxnreg__(MLA_SMALL_MAXNREG)
     if (lane == 0)
       for (int k = issued > kSmSlots ? issued - kSmSlots : 0; k < issued; ++k)
         (void)mbar_wait_bounded(&full[k % kSmSlots], (uint32_t)((k / kSmSlots) & 1), kWaitLimit);
+    cluster_wait_acquire();
   } else {
     // ================= consumer warps 0-7 ============================
     // gamma_q is a weight: one token loads it before the wait (two tokens
@@ -312,6 +328,7 @@ __global__ void __maxnreg__(MLA_SMALL_MAXNREG)
     if (kv_here) kv_insert_warp_loaded(a, lane, kvl);
     if constexpr (NT > 1) named_barrier(4, kConsumers);  // xq rows written (before any wait)
     if (tid == 0) trace_stamp(a, 2);
+    cluster_wait_acquire();  // every peer's rbar armed (long since, by now)
     const float qsi = load_qsi(a);
 
     // Thread tid's latent columns 2 tid, 2 tid + 1 belong to rank owner.
@@ -520,9 +537,23 @@ cudaError_t prepare_small_one() {
   if (e != cudaSuccess) return e;
   // the whole unified memory as shared memory (with a 3-stage ring two CTAs
   // then fit an SM; the default carveout measured room for one)
-  return cudaFuncSetAttribute(mla_small_kernel<NT, C>,
-                              cudaFuncAttributePreferredSharedMemoryCarveout,
-                              cudaSharedmemCarveoutMaxShared);
+  e = cudaFuncSetAttribute(mla_small_kernel<NT, C>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
+#ifdef MLA_DEBUG_SPLIT
+  if (e == cudaSuccess) {
+    int blocks = 0, clusters = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, mla_small_kernel<NT, C>, kSmThreads,
+                                                  SmallSmem<NT, C>::kAlloc);
+    cudaLaunchAttribute attr[3];
+    cudaLaunchConfig_t cfg = small_config<NT, C>(C, nullptr, attr);
+    cfg.numAttrs = 1;
+    cudaOccupancyMaxActiveClusters(&clusters, mla_small_kernel<NT, C>, &cfg);
+    cudaGetLastError();
+    fprintf(stderr, "small kernel NT %d C %d: %d bytes, %d CTAs an SM, %d clusters\n", NT, C,
+            SmallSmem<NT, C>::kAlloc, blocks, clusters);
+  }
+#endif
+  return e;
 }
 
 // Clusters that fit with one CTA per SM: the occupancy of a CTA asking for
