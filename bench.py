@@ -589,7 +589,7 @@ def gpu_arm(args, rank: int, world: int, local_rank: int) -> dict | None:
         torch.cuda.empty_cache()
     out["others"] = others
     sweep = {}
-    for name in (SWEEP_POINTS if args.sweep else ()):
+    for name in (args.points if args.sweep else ()):
         w2 = Workload(name, rank, dev, args.path)
         ms2, _ = time_device(w2, args.steps, args.warmup, args.graph_steps, stream, barrier)
         (per2,) = max_over_ranks([ms2 / args.steps], dev)
@@ -603,14 +603,15 @@ def gpu_arm(args, rank: int, world: int, local_rank: int) -> dict | None:
 
 def sweep_profile(args, local_rank: int) -> None:
     """Three decode steps per sweep point with one weight set, in the order
-    of SWEEP_POINTS, for a short ncu pass (tensor-pipe utilisation and DRAM
-    bytes per point): the third launch of each point is a warm step."""
+    of --points (the 28 sweep points by default), for a short ncu pass
+    (tensor-pipe utilisation and DRAM bytes per point): the third launch of
+    each point is a warm step."""
     import torch
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(dev)
-    for name in SWEEP_POINTS:
+    for name in args.points:
         wl = Workload(name, 0, dev, args.path, nsets=1)
         with torch.cuda.stream(stream):
             for j in range(3):
@@ -841,11 +842,15 @@ def main():
                     help="also time every sweep point (B x H x layout), reported under sweep")
     ap.add_argument("--sweep-profile", action="store_true",
                     help="only run three decode steps per sweep point (for an ncu pass)")
+    ap.add_argument("--points", default="",
+                    help="comma list of sweep points (sweep_b{B}_h{H}_{e4m3|ds|nvfp4}) for "
+                         "--sweep and --sweep-profile instead of the default 28")
     ap.add_argument("--cpu-budget", type=float, default=16.0)
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     args.also = [w for w in args.also.split(",") if w and w != "none"]
+    args.points = [w for w in args.points.split(",") if w] or list(SWEEP_POINTS)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -79,7 +79,7 @@ extern "C" {
                            serve (small counts: the FMA kernel measured
                            faster there), MLA_PATH_MMA otherwise           */
 #define MLA_PATH_FMA 1  /* FP32 FMA dot products: the small-batch kernel
-                           (batch <= 2 only; MLA_EUNSUPPORTED above)       */
+                           (batch <= 8 only; MLA_EUNSUPPORTED above)       */
 #define MLA_PATH_MMA 2  /* BF16 tensor-core tiles, FP32 accumulate           */
 
 #define MLA_MAX_BATCH 256 /* largest batch one decode call accepts           */

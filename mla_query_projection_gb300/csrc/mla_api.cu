@@ -82,11 +82,13 @@ enum class Kernel { kSmall, kAbsorbMma, kAbsorbPair, kWide, kHandoff };
 // tensor-core kernel the batch would otherwise take):
 //  * one token, head counts the paired kernel does not serve (those the
 //    partials kernel would take, up to about 50 heads on 152 SMs): FP32 FMAs,
-//    8 heads 3.96 against 4.83, 16 heads 4.90 / 5.42, 32 heads 5.73 / 7.39,
+//    8 heads 3.96 against 4.83, 16 heads 4.72 / 5.42, 32 heads 5.73 / 7.39,
 //    48 heads 7.50 / 9.89;
 //  * everything else: tensor cores.  One token where the paired kernel runs:
-//    56 heads 8.07 against 8.01, 64 heads 8.45 / 8.17, 128 heads 14.86 /
-//    14.70; two tokens: 16 heads 7.96 / 6.11.
+//    56 heads 8.07 against 8.01, 64 heads 8.48 / 7.94, 128 heads 14.72 /
+//    14.45; 2, 4 and 8 tokens: 16 heads 6.34 / 6.06, 8.74 / 6.83,
+//    13.75 / 8.16, and at 64 and 128 heads the FMA kernel is 1.4 to 3.6
+//    times slower.
 // Both stream every weight byte once; after the programmatic-dependent-launch
 // wait a step is bound by its consumers: the FMA kernel's clusters close each
 // head through distributed shared memory, where the partials kernel makes an
@@ -97,9 +99,9 @@ int pick_kernel(const mla_query* h, int batch, Kernel* k, int* nt) {
   if (path == MLA_PATH_AUTO)
     path = batch == 1 && h->pair_ctas == 0 && h->small_ctas > 0 ? MLA_PATH_FMA : MLA_PATH_MMA;
   if (path == MLA_PATH_FMA) {
-    if (batch > 2 || h->small_ctas == 0) return MLA_EUNSUPPORTED;
+    if (batch > 8 || h->small_ctas == 0) return MLA_EUNSUPPORTED;
     *k = Kernel::kSmall;
-    *nt = batch <= 1 ? 1 : 2;
+    *nt = batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 4 ? 4 : 8;
   } else if (path == MLA_PATH_MMA) {
     if (batch <= 8 && h->pair_ctas > 0) {
       *k = Kernel::kAbsorbPair;
@@ -175,16 +177,18 @@ int mla_query_create(mla_query_t* out, int num_heads, const void* w_qb, const vo
   }
   mla::make_abs_split(num_heads, h->num_sms, &h->split);
   // The small-batch FMA kernel: the cluster size whose split puts the fewest
-  // bytes on the most loaded CTA.
-  // Each grid is sized so that all its clusters can be resident at once
-  // (the occupancy counts both CTAs an SM can hold; a grid takes at most one
-  // CTA per SM, leaving the other slot to the next step).
+  // bytes on the most loaded CTA.  Each grid is sized so that all its
+  // clusters can be resident at once, one CTA per SM, for every token count
+  // (1, 2, 4, 8) the kernel is built for.
   {
     int most[3];
     for (int k = 0; k < 3; ++k) {
       const int c = 2 << k;
-      const int m1 = mla::small_kernel_max_clusters(c, 1), m2 = mla::small_kernel_max_clusters(c, 2);
-      most[k] = m1 < m2 ? m1 : m2;
+      most[k] = mla::small_kernel_max_clusters(c, 1);
+      for (int nt = 2; nt <= 8; nt *= 2) {
+        const int m = mla::small_kernel_max_clusters(c, nt);
+        if (m < most[k]) most[k] = m;
+      }
       if (most[k] <= 0) most[k] = -1;  // cannot run: no cluster of this size
     }
     h->small_ctas = 0;
@@ -557,11 +561,14 @@ const char* mla_query_kernel_for(mla_query_t h, int batch) {
   if (pick_kernel(h, batch, &kern, &nt) != MLA_OK) return nullptr;
   switch (kern) {
     case Kernel::kSmall: {
-      static const char* names[2][3] = {
+      static const char* names[4][3] = {
           {"mla_small_kernel<1,2>", "mla_small_kernel<1,4>", "mla_small_kernel<1,8>"},
-          {"mla_small_kernel<2,2>", "mla_small_kernel<2,4>", "mla_small_kernel<2,8>"}};
+          {"mla_small_kernel<2,2>", "mla_small_kernel<2,4>", "mla_small_kernel<2,8>"},
+          {"mla_small_kernel<4,2>", "mla_small_kernel<4,4>", "mla_small_kernel<4,8>"},
+          {"mla_small_kernel<8,2>", "mla_small_kernel<8,4>", "mla_small_kernel<8,8>"}};
       const int c = h->small_split.cluster;
-      return names[nt - 1][c == 2 ? 0 : c == 4 ? 1 : 2];
+      const int row = nt <= 1 ? 0 : nt == 2 ? 1 : nt == 4 ? 2 : 3;
+      return names[row][c == 2 ? 0 : c == 4 ? 1 : 2];
     }
     case Kernel::kAbsorbMma: return nt == 8 ? "mla_absorb_mma_kernel<8>" : "mla_absorb_mma_kernel<16>";
     case Kernel::kAbsorbPair: return nt == 8 ? "mla_absorb_pair_kernel<8>" : "mla_absorb_pair_kernel<16>";

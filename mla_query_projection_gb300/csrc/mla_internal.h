@@ -125,8 +125,8 @@ bool make_pair_split(int heads, int ctas, PairSplit* sp);
 // Whether `ctas` CTAs of the paired kernel (nt = 8 or 16 tokens) can all be
 // resident at once.
 bool pair_kernel_fits(int ctas, int nt);
-// Small-batch FMA kernel (1-2 tokens, clusters of `cluster` CTAs, two CTAs
-// of consecutive steps resident per SM): the heads of cluster g are
+// Small-batch FMA kernel (1, 2, 4 or 8 tokens, clusters of `cluster` CTAs,
+// one CTA per SM): the heads of cluster g are
 // [head[g], head[g + 1]) (at most two), rank r of the cluster takes nope rows
 // [r * 128 / cluster, (r + 1) * 128 / cluster) of each of them with their
 // W_UK rows, and CTA i the rope rows [rope[i], rope[i + 1]).

@@ -1,4 +1,4 @@
-// mla_small.cu - the decode step for one or two tokens on FP32 FMAs.
+// mla_small.cu - the decode step for up to eight tokens on FP32 FMAs.
 //
 // What it computes is the step of page "mla.query", class MlaQuery (method
 // kernel, the small-batch path, and insert / insert_ds / insert_nvfp4 /
@@ -7,7 +7,10 @@
 //
 // GB300 design.  With one or two tokens a weight element feeds one or two
 // FMAs, so the projection is no dense contraction: plain FP32 FMAs keep up
-// with the stream, and the kernel is shaped around the stream instead.
+// with the stream, and the kernel is shaped around the stream instead.  It
+// is built for 1, 2, 4 and 8 tokens (the last two so that the dispatch
+// between FP32 FMAs and tensor cores rests on measurements at every batch
+// up to 8).
 //  * Clusters of C CTAs (2, 4 or 8) own whole heads (at most two per
 //    cluster); rank r takes nope rows [r 128/C, (r+1) 128/C) of each head and
 //    the same rows of W_UK, and rope rows fill every CTA to an even byte
@@ -70,19 +73,22 @@ constexpr int kSmThreads = kConsumers + 32;        // 8 consumer warps + the pro
 
 template <int NT, int C>
 struct SmallSmem {
+  // ring slots: three, two at 8 tokens (their partials and xq rows take the
+  // third slot's shared memory)
+  static constexpr int kSlots = NT >= 8 ? 2 : kSmSlots;
   static constexpr int kCols = kKvLora / C;            // latent columns a rank owns
   static constexpr int kStagesPerHead = kNope / C / kSmRows;
   static constexpr int kRecvHead = C * kCols * NT * 4;  // [rank][column][token] FP32
   static constexpr int kRecvBytesIn = (C - 1) * kCols * NT * 4;  // what the peers send
   static constexpr int oRing = 0;
-  static constexpr int oRecv = kSmSlots * kSmStage;     // [2 heads][kRecvHead]
+  static constexpr int oRecv = kSlots * kSmStage;       // [2 heads][kRecvHead]
   static constexpr int oQv = oRecv + 2 * kRecvHead;     // [2][kSmRows][NT] FP32
   static constexpr int oFull = oQv + 2 * kSmRows * NT * 4;
-  static constexpr int oEmpty = oFull + kSmSlots * 8;
-  static constexpr int oRbar = oEmpty + kSmSlots * 8;   // [2] received partials
+  static constexpr int oEmpty = oFull + kSlots * 8;
+  static constexpr int oRbar = oEmpty + kSlots * 8;     // [2] received partials
   static constexpr int oQbar = oRbar + 16;              // [2] q values of a stage written
-  // two tokens: their xq rows in shared memory [NT][1536] BF16 (one token
-  // keeps its 48 values a lane in registers)
+  // two or more tokens: their xq rows in shared memory [NT][1536] BF16 (one
+  // token keeps its 48 values a lane in registers)
   static constexpr int kXsBytes = NT > 1 ? NT * kRowBytes : 0;
   static constexpr int oXs = oQbar + 16;
   static constexpr int kBytes = oXs + kXsBytes;
@@ -153,15 +159,17 @@ __device__ __forceinline__ void dot_chunk(const uint4 w, const uint4 (&x)[NT], f
 }
 
 // One CTA an SM (the ring takes most of the shared memory), so up to
-// 65536 / 288 = 227 registers a thread would fit; 112 measured faster than
-// 160 (8.45 against 8.60 us at 64 heads, one spill of 8 bytes at C = 8).
+// 65536 / 288 = 227 registers a thread would fit; for one or two tokens 112
+// measured faster than 160 (8.45 against 8.60 us at 64 heads, one spill of
+// 8 bytes at C = 8); four and eight tokens take 168 (their accumulators).
 #ifndef MLA_SMALL_MAXNREG
 #define MLA_SMALL_MAXNREG 112
 #endif
 template <int NT, int C>
-__global__ void __maxnreg__(MLA_SMALL_MAXNREG)
+__global__ void __maxnreg__(NT >= 4 ? 168 : MLA_SMALL_MAXNREG)
     mla_small_kernel(const DecodeArgs a, const __grid_constant__ SmallSplit split) {
   using S = SmallSmem<NT, C>;
+  constexpr int SL = S::kSlots;
   const uint64_t t_entry = trace_now();  // slot 1 of a trace build
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
@@ -182,7 +190,7 @@ __global__ void __maxnreg__(MLA_SMALL_MAXNREG)
   bool timed_out = false;
 
   if (tid == 0) {
-    for (int s = 0; s < kSmSlots; ++s) {
+    for (int s = 0; s < SL; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
     }
@@ -222,28 +230,28 @@ __global__ void __maxnreg__(MLA_SMALL_MAXNREG)
     if (lane == 0) trace_stamp(a, 4);  // the producer starts
     const uint64_t pol = l2_policy_evict_first();
     if (kSmPrefetch && lane == 0)
-      for (int k = kSmSlots; k < min(nst, 2 * kSmSlots); ++k) small_prefetch_stage<C>(a, seq, k);
+      for (int k = SL; k < min(nst, 2 * SL); ++k) small_prefetch_stage<C>(a, seq, k);
     int issued = 0;
     for (int k = 0; k < nst; ++k) {
-      const int slot = k % kSmSlots;
+      const int slot = k % SL;
       uint8_t* buf = ring + slot * kSmStage;
       int ok = 1;
-      if (k >= kSmSlots && lane == 0)
-        ok = mbar_wait_bounded(&empty[slot], (uint32_t)(((k / kSmSlots) - 1) & 1), kWaitLimit);
+      if (k >= SL && lane == 0)
+        ok = mbar_wait_bounded(&empty[slot], (uint32_t)(((k / SL) - 1) & 1), kWaitLimit);
       if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) {
         timed_out = true;  // the consumers stopped: issue nothing more
         break;
       }
       issued = k + 1;
       if (lane == 0 && k < 20) trace_stamp(a, 28 + k);  // stage k issued
-      if (kSmPrefetch && lane == 0 && k >= kSmSlots && k + kSmSlots < nst)
-        small_prefetch_stage<C>(a, seq, k + kSmSlots);
+      if (kSmPrefetch && lane == 0 && k >= SL && k + SL < nst)
+        small_prefetch_stage<C>(a, seq, k + SL);
       if (k < seq.nope()) {
         const int h = seq.head(k), p0 = seq.p0(k);
         if (lane == 0) mbar_arrive_expect_tx(&full[slot], kSmStage);
         __syncwarp();
         if (!MLA_IN_BOUNDS(a, h >= 0 && h < a.heads && p0 >= 0 && p0 + kSmRows <= kNope, 10) ||
-            !MLA_IN_BOUNDS(a, slot >= 0 && slot < kSmSlots, 11)) {
+            !MLA_IN_BOUNDS(a, slot >= 0 && slot < SL, 11)) {
         } else if (lane < kSmRows)
           bulk_g2s_hint(buf + lane * kRowBytes,
                         a.w_qb + ((int64_t)h * kHeadRows + p0 + lane) * kQLora, kRowBytes,
@@ -264,13 +272,13 @@ __global__ void __maxnreg__(MLA_SMALL_MAXNREG)
     }
     // every copy issued lands before the CTA may leave
     if (lane == 0)
-      for (int k = issued > kSmSlots ? issued - kSmSlots : 0; k < issued; ++k)
-        (void)mbar_wait_bounded(&full[k % kSmSlots], (uint32_t)((k / kSmSlots) & 1), kWaitLimit);
+      for (int k = issued > SL ? issued - SL : 0; k < issued; ++k)
+        (void)mbar_wait_bounded(&full[k % SL], (uint32_t)((k / SL) & 1), kWaitLimit);
     cluster_wait_acquire();
   } else {
     // ================= consumer warps 0-7 ============================
-    // gamma_q is a weight: one token loads it before the wait (two tokens
-    // need those registers for their second xq row)
+    // gamma_q is a weight: one token loads it before the wait (with more
+    // tokens each normalising warp reads it from L2 as it goes)
     uint4 gq[NT == 1 ? 6 : 1];
     if constexpr (NT == 1) {
 #pragma unroll
@@ -281,22 +289,24 @@ __global__ void __maxnreg__(MLA_SMALL_MAXNREG)
     if (tid == 0) trace_stamp(a, 3);
     // The KV row of token i (CTA i < B): its loads go out with the q_a row's,
     // its arithmetic after the normalisation; a CTA inserts at most one
-    // token (B <= 2 < P).
+    // token (B <= 8 < P).
     const bool kv_here = warp == kConsumerWarps - 1 && i < a.batch;
     KvWarpLoads kvl;
     if (kv_here) kvl = kv_insert_warp_load(a, i, lane);
-    // q_a RMSNorm of every token, in every warp: lane l keeps columns
-    // 8 (l + 32 j) .. + 7, j < 6, of xq as BF16 pairs
-    uint4 xq[NT][6];
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
+    // q_a RMSNorm: lane l holds columns 8 (l + 32 j) .. + 7, j < 6, of a
+    // token's xq as BF16 pairs.  One token: every warp normalises it and
+    // keeps it in registers.  More tokens: warp w normalises tokens w,
+    // w + 8, .. into shared memory.
+    uint4 xq1[6];  // one token: its xq
+    for (int t = NT == 1 ? 0 : warp; t < NT; t += NT == 1 ? 1 : kConsumerWarps) {
+      uint4 x[6];
       float ss = 0.f;
 #pragma unroll
       for (int j = 0; j < 6; ++j) {
-        xq[t][j] = t < a.batch ? *reinterpret_cast<const uint4*>(
-                                     a.q_a + (int64_t)t * a.q_a_stride + 8 * (lane + 32 * j))
-                               : make_uint4(0, 0, 0, 0);
-        const uint32_t vv[4] = {xq[t][j].x, xq[t][j].y, xq[t][j].z, xq[t][j].w};
+        x[j] = t < a.batch ? *reinterpret_cast<const uint4*>(a.q_a + (int64_t)t * a.q_a_stride +
+                                                             8 * (lane + 32 * j))
+                           : make_uint4(0, 0, 0, 0);
+        const uint32_t vv[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           ss = fmaf(bf16lo(vv[e]), bf16lo(vv[e]), ss);
@@ -310,19 +320,19 @@ __global__ void __maxnreg__(MLA_SMALL_MAXNREG)
         const uint4 gj = NT == 1 ? gq[NT == 1 ? j : 0]
                                  : *reinterpret_cast<const uint4*>(a.gamma_q + 8 * (lane + 32 * j));
         const uint32_t gw[4] = {gj.x, gj.y, gj.z, gj.w};
-        const uint32_t vv[4] = {xq[t][j].x, xq[t][j].y, xq[t][j].z, xq[t][j].w};
+        const uint32_t vv[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
         uint32_t o[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e)
           o[e] = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(vv[e]), rr), bf16lo(gw[e])),
                              __fmul_rn(__fmul_rn(bf16hi(vv[e]), rr), bf16hi(gw[e])));
-        xq[t][j] = make_uint4(o[0], o[1], o[2], o[3]);
-        if constexpr (NT > 1) {
-          if (warp == 0)
-            *reinterpret_cast<uint4*>(smem + S::oXs + t * kRowBytes + 16 * (lane + 32 * j)) = xq[t][j];
-        }
-        if (i == 0 && warp == 0 && a.q_c != nullptr && t < a.batch)
-          *reinterpret_cast<uint4*>(a.q_c + (int64_t)t * kQLora + 8 * (lane + 32 * j)) = xq[t][j];
+        x[j] = make_uint4(o[0], o[1], o[2], o[3]);
+        if constexpr (NT == 1)
+          xq1[j] = x[j];
+        else
+          *reinterpret_cast<uint4*>(smem + S::oXs + t * kRowBytes + 16 * (lane + 32 * j)) = x[j];
+        if (i == 0 && (NT > 1 || warp == 0) && a.q_c != nullptr && t < a.batch)
+          *reinterpret_cast<uint4*>(a.q_c + (int64_t)t * kQLora + 8 * (lane + 32 * j)) = x[j];
       }
     }
     if (kv_here) kv_insert_warp_loaded(a, lane, kvl);
@@ -343,11 +353,11 @@ __global__ void __maxnreg__(MLA_SMALL_MAXNREG)
     }
 
     for (int k = 0; k < nst; ++k) {
-      const int slot = k % kSmSlots;
+      const int slot = k % SL;
       const uint8_t* buf = ring + slot * kSmStage;
       // a stage that never arrives ends the loop; the other warps' barrier
       // waits below are then bounded by the same limit
-      if (!mbar_wait_bounded(&full[slot], (uint32_t)((k / kSmSlots) & 1), kWaitLimit)) {
+      if (!mbar_wait_bounded(&full[slot], (uint32_t)((k / SL) & 1), kWaitLimit)) {
         timed_out = true;
         break;
       }
@@ -369,7 +379,7 @@ __global__ void __maxnreg__(MLA_SMALL_MAXNREG)
           uint4 xj[NT];
 #pragma unroll
           for (int t = 0; t < NT; ++t)
-            xj[t] = NT == 1 ? xq[t][j]
+            xj[t] = NT == 1 ? xq1[j]
                             : *reinterpret_cast<const uint4*>(smem + S::oXs + t * kRowBytes +
                                                                16 * (lane + 32 * j));
 #pragma unroll
@@ -455,7 +465,14 @@ __global__ void __maxnreg__(MLA_SMALL_MAXNREG)
           if constexpr (NT == 1) {
             st_async_v2(mapa_shared(dst, peer), acc[0][0], acc[0][1], rb);
           } else {
-            st_async_v4(mapa_shared(dst, peer), acc[0][0], acc[1][0], acc[0][1], acc[1][1], rb);
+            // element e of the 2 NT: column e / NT, token e % NT
+#pragma unroll
+            for (int q = 0; q < NT / 2; ++q) {
+              float f[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) f[e] = acc[(4 * q + e) % NT][(4 * q + e) / NT];
+              st_async_v4(mapa_shared(dst + 16 * q, peer), f[0], f[1], f[2], f[3], rb);
+            }
           }
         }
 #pragma unroll
@@ -580,45 +597,62 @@ cudaError_t launch_small_one(const DecodeArgs& a, const SmallSplit& sp, int ctas
   return cudaLaunchKernelEx(&cfg, mla_small_kernel<NT, C>, a, sp);
 }
 
+template <int NT>
+cudaError_t prepare_small_nt() {
+  cudaError_t e;
+  if ((e = prepare_small_one<NT, 2>()) != cudaSuccess) return e;
+  if ((e = prepare_small_one<NT, 4>()) != cudaSuccess) return e;
+  return prepare_small_one<NT, 8>();
+}
+
+template <int NT>
+int small_max_clusters_nt(int cluster) {
+  return cluster == 2 ? small_max_clusters_one<NT, 2>()
+         : cluster == 4 ? small_max_clusters_one<NT, 4>()
+         : cluster == 8 ? small_max_clusters_one<NT, 8>()
+                        : 0;
+}
+
+template <int NT>
+cudaError_t launch_small_nt(const DecodeArgs& a, const SmallSplit& sp, int ctas,
+                            cudaStream_t stream) {
+  switch (sp.cluster) {
+    case 2: return launch_small_one<NT, 2>(a, sp, ctas, stream);
+    case 4: return launch_small_one<NT, 4>(a, sp, ctas, stream);
+    case 8: return launch_small_one<NT, 8>(a, sp, ctas, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 }  // namespace
 
 cudaError_t prepare_small_kernels() {
   cudaError_t e;
-  if ((e = prepare_small_one<1, 2>()) != cudaSuccess) return e;
-  if ((e = prepare_small_one<1, 4>()) != cudaSuccess) return e;
-  if ((e = prepare_small_one<1, 8>()) != cudaSuccess) return e;
-  if ((e = prepare_small_one<2, 2>()) != cudaSuccess) return e;
-  if ((e = prepare_small_one<2, 4>()) != cudaSuccess) return e;
-  return prepare_small_one<2, 8>();
+  if ((e = prepare_small_nt<1>()) != cudaSuccess) return e;
+  if ((e = prepare_small_nt<2>()) != cudaSuccess) return e;
+  if ((e = prepare_small_nt<4>()) != cudaSuccess) return e;
+  return prepare_small_nt<8>();
 }
 
 int small_kernel_max_clusters(int cluster, int nt) {
-  if (nt == 1)
-    return cluster == 2 ? small_max_clusters_one<1, 2>()
-           : cluster == 4 ? small_max_clusters_one<1, 4>()
-           : cluster == 8 ? small_max_clusters_one<1, 8>()
-                          : 0;
-  if (nt == 2)
-    return cluster == 2 ? small_max_clusters_one<2, 2>()
-           : cluster == 4 ? small_max_clusters_one<2, 4>()
-           : cluster == 8 ? small_max_clusters_one<2, 8>()
-                          : 0;
-  return 0;
+  switch (nt) {
+    case 1: return small_max_clusters_nt<1>(cluster);
+    case 2: return small_max_clusters_nt<2>(cluster);
+    case 4: return small_max_clusters_nt<4>(cluster);
+    case 8: return small_max_clusters_nt<8>(cluster);
+    default: return 0;
+  }
 }
 
 cudaError_t launch_small(const DecodeArgs& a, const SmallSplit& sp, int ctas, int nt,
                          cudaStream_t stream) {
-  const int c = sp.cluster;
-  if (nt == 1) {
-    if (c == 2) return launch_small_one<1, 2>(a, sp, ctas, stream);
-    if (c == 4) return launch_small_one<1, 4>(a, sp, ctas, stream);
-    if (c == 8) return launch_small_one<1, 8>(a, sp, ctas, stream);
-  } else if (nt == 2) {
-    if (c == 2) return launch_small_one<2, 2>(a, sp, ctas, stream);
-    if (c == 4) return launch_small_one<2, 4>(a, sp, ctas, stream);
-    if (c == 8) return launch_small_one<2, 8>(a, sp, ctas, stream);
+  switch (nt) {
+    case 1: return launch_small_nt<1>(a, sp, ctas, stream);
+    case 2: return launch_small_nt<2>(a, sp, ctas, stream);
+    case 4: return launch_small_nt<4>(a, sp, ctas, stream);
+    case 8: return launch_small_nt<8>(a, sp, ctas, stream);
+    default: return cudaErrorInvalidValue;
   }
-  return cudaErrorInvalidValue;
 }
 
 }  // namespace mla

@@ -38,6 +38,7 @@ CHILD = textwrap.dedent(r"""
         (3, 16, S.LAYOUT_E4M3, B.MLA_PATH_AUTO),        # partials kernel
         (1, 64, S.LAYOUT_E4M3, B.MLA_PATH_FMA),         # small-batch FMA, pairs
         (2, 16, S.LAYOUT_DS_MLA, B.MLA_PATH_FMA),       # small-batch FMA, larger clusters
+        (7, 128, S.LAYOUT_E4M3, B.MLA_PATH_FMA),        # small-batch FMA, 8 tokens a CTA
     ]
     for batch, heads, layout, path in cases:
         inp = S.make_inputs(batch=batch, heads=heads, layout=layout, pages=16, seed=3000 + batch + heads)
@@ -76,4 +77,4 @@ def test_checks_build_every_kernel(tmp_path):
     p = subprocess.run([sys.executable, "-c", CHILD, ROOT, lib], capture_output=True, text=True,
                        timeout=600)
     assert p.returncode == 0, p.stdout[-3000:] + p.stderr[-3000:]
-    assert p.stdout.count("ok") == 9, p.stdout
+    assert p.stdout.count("ok") == 10, p.stdout

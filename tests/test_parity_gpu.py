@@ -134,12 +134,13 @@ def test_wide_kernel_head_counts(heads, batch):
     assert_parity(inp)
 
 
-@pytest.mark.parametrize("heads", [16, 32, 64, 128])
-@pytest.mark.parametrize("batch", [1, 2])
+@pytest.mark.parametrize("batch,heads", [(b, h) for b in (1, 2) for h in (16, 32, 64, 128)]
+                         + [(3, 16), (4, 64), (5, 128), (8, 16), (8, 128)])
 def test_fma_and_mma_paths_agree(batch, heads):
-    """The small-batch FMA kernel (clusters of 8 at 16 heads, of 4 or 2 above)
-    and the tensor-core kernels meet the oracle on the same inputs; the q_a
-    RMSNorm and the KV insert are computed alike, bit for bit."""
+    """The small-batch FMA kernel (1, 2, 4 or 8 tokens a CTA; clusters of 4
+    at 16 heads, of 2 above) and the tensor-core kernels meet the oracle on
+    the same inputs, ragged token counts included; the KV insert is computed
+    alike, bit for bit."""
     inp = S.make_inputs(batch=batch, heads=heads, layout=S.LAYOUT_DS_MLA, pages=16,
                         seed=300 + heads)
     fma, ref = assert_parity(inp, path=B.MLA_PATH_FMA)
@@ -154,7 +155,7 @@ def test_fma_and_mma_paths_agree(batch, heads):
 
 
 def test_fma_path_refuses_large_batch():
-    inp = S.make_inputs(batch=3, heads=4, layout=S.LAYOUT_E4M3, pages=4, seed=301)
+    inp = S.make_inputs(batch=9, heads=4, layout=S.LAYOUT_E4M3, pages=4, seed=301)
     step = DecodeStep(inp)
     assert step.set_path(B.MLA_PATH_FMA) == B.MLA_OK
     assert step.decode() == B.MLA_EUNSUPPORTED
@@ -229,6 +230,8 @@ def test_small_head_count_repeated_calls_close_every_head():
         (2, 128, B.MLA_PATH_AUTO, "mla_absorb_pair_kernel<8>"),
         (1, 64, B.MLA_PATH_FMA, "mla_small_kernel<1,2>"),
         (2, 128, B.MLA_PATH_FMA, "mla_small_kernel<2,2>"),
+        (3, 64, B.MLA_PATH_FMA, "mla_small_kernel<4,2>"),
+        (8, 128, B.MLA_PATH_FMA, "mla_small_kernel<8,2>"),
         (12, 64, B.MLA_PATH_AUTO, "mla_absorb_pair_kernel<16>"),
         (40, 64, B.MLA_PATH_AUTO, "mla_wide_norm_kernel+mla_wide_kernel"),
         (1, 16, B.MLA_PATH_AUTO, "mla_small_kernel<1,"),
