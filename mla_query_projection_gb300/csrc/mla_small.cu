@@ -18,13 +18,17 @@
 //    rows, their 16 W_UK rows (16 KiB), one 1-D bulk copy per row issued by
 //    separate lanes.  The static weights are copied before the programmatic-
 //    dependent-launch wait, as the page's class docstring has them: a 3-stage
-//    ring (192 KiB, one CTA per SM) holds a small head count's whole share
-//    (16 heads: at most 128 KiB a CTA) before the wait ends.  (A ring of
-//    about 105 KiB let the next step's CTA share the SM; that measured
-//    slower, 10.3 against 9.3 us at 64 heads, and gained nothing at 16.)
+//    ring (192 KiB, one CTA per SM; two stages at 8 tokens) holds a small
+//    head count's whole share (16 heads: at most 128 KiB a CTA) before the
+//    wait ends.  (A ring of about 100 KiB measured slower, 10.3 against
+//    9.3 us at 64 heads with 8-row stages.  It does not let the next step's
+//    CTA share the SM on its own: 288 threads at 112 registers fill the
+//    register file for one CTA; capped at 96 registers two CTAs did share
+//    each SM, and the spills made it 10.7 us.)
 //  * Warp w computes rows w and w + 8 of a stage, their chains interleaved:
-//    each lane dots 48 of a row's 1536 values with the normalised xq it keeps
-//    in registers (BF16 pairs), then the warp adds the lanes.  The 16
+//    each lane dots 48 of a row's 1536 values with the normalised xq (one
+//    token: kept in registers as BF16 pairs; more tokens: each normalised
+//    by one warp into shared memory), then the warp adds the lanes.  The 16
 //    BF16-rounded nope q values go through shared memory to all 256 threads,
 //    and thread t adds their products with W_UK columns 2t, 2t + 1 into its
 //    FP32 absorption sums.  (Stages of 8 rows, one a warp, measured slower:
