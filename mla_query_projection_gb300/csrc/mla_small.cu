@@ -556,8 +556,8 @@ cudaError_t prepare_small_one() {
       mla_small_kernel<NT, C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
       SmallSmem<NT, C>::kAlloc > 120 * 1024 ? SmallSmem<NT, C>::kAlloc : 120 * 1024);
   if (e != cudaSuccess) return e;
-  // the whole unified memory as shared memory (with a 3-stage ring two CTAs
-  // then fit an SM; the default carveout measured room for one)
+  // the whole unified memory as shared memory (the ring and the partials
+  // take up to about 220 KiB)
   e = cudaFuncSetAttribute(mla_small_kernel<NT, C>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
 #ifdef MLA_DEBUG_SPLIT
