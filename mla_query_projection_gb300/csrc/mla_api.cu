@@ -275,7 +275,7 @@ int mla_query_create(mla_query_t* out, int num_heads, const void* w_qb, const vo
         goto fail;
       }
       if (mla::pack_wide_weights(h->w_qb, h->w_uk, h->wide_qb, h->wide_ukt, num_heads,
-                                 h->wide_split.single, 0) != cudaSuccess ||
+                                 h->wide_split.ndouble, 0) != cudaSuccess ||
           cudaStreamSynchronize(0) != cudaSuccess)
         goto fail;
     }

@@ -153,15 +153,20 @@ cudaError_t prepare_small_kernels();
 cudaError_t launch_small(const DecodeArgs& a, const SmallSplit& sp, int ctas, int nt,
                          cudaStream_t stream);
 // Wide kernel (17-64 tokens, tcgen05, clusters of two CTAs splitting K): the
-// heads of pair c are [head[c], head[c + 1]) (at most two), its rope units
-// [rope[c], rope[c + 1]).  A rope unit is the rope rows of two heads (2u,
-// 2u + 1: one 128-row tile), or with `single` set the rope rows of one head
-// (a 64-row tile): finer units, which even out the pairs where two-head units
-// cannot (64 heads on 76 pairs).
+// heads of pair c are [head[c], head[c + 1]) (at most two).  The rope rows
+// come in two unit shapes: a two-head unit u covers heads 2u and 2u + 1 (one
+// 128-row tile; heads 0 .. 2 ndouble - 1, a missing last head's rows zero),
+// a one-head unit v covers head 2 ndouble + v (a 64-row tile, computed as
+// M = 64: finer, but slower to issue).  Pair c takes the two-head units
+// [dbl[c], dbl[c + 1]) and the one-head units [sgl[c], sgl[c + 1]).  Mixing
+// the shapes evens out pairs that one shape alone cannot: 128 heads on 76
+// pairs, at most 44 boxes of 16 KiB per CTA with two-head units only, 40
+// with 48 of them and 32 one-head units.
 struct WideSplit {
   uint16_t head[kMaxCtas / 2 + 1];
-  uint16_t rope[kMaxCtas / 2 + 1];
-  int single;
+  uint16_t dbl[kMaxCtas / 2 + 1];
+  uint16_t sgl[kMaxCtas / 2 + 1];
+  int ndouble;
 };
 int wide_tokens();
 cudaError_t prepare_wide_kernel();
@@ -171,7 +176,7 @@ bool make_wide_split(int heads, int ctas, WideSplit* sp);
 size_t wide_qb_bytes(int heads);
 size_t wide_ukt_bytes(int heads);
 cudaError_t pack_wide_weights(const uint16_t* w_qb, const uint16_t* w_uk, uint8_t* qb_tiles,
-                              uint8_t* ukt_tiles, int heads, int single, cudaStream_t stream);
+                              uint8_t* ukt_tiles, int heads, int ndouble, cudaStream_t stream);
 // Bounded poll of a gathered query buffer [batch][q_heads][576] (mla_gather.cu):
 // returns once no element of the first wait_heads rows of every token is the
 // all-ones sentinel, or sets MLA_DEVERR_TIMEOUT in *err after limit_ns.

@@ -114,40 +114,49 @@ int choose_small_split(int heads, int num_sms, const int* max_clusters, SmallSpl
 
 namespace {
 
-// Relative time of a single-head rope box (eight M = 64 MMAs on 16 KiB)
-// against a 128-row box (four M = 128 MMAs), as a fraction.
-constexpr int kSingleCostNum = 5, kSingleCostDen = 4;
+// Estimated time of a CTA's units in quarter boxes: a 128-row box (a head's
+// NOPE / ABS box, or a two-head rope box: four M = 128 MMAs on 16 KiB) costs
+// 4, a one-head rope box (eight M = 64 MMAs on 16 KiB) 5.
+constexpr int64_t kHeadCost = (int64_t)kWideHeadBoxes * 4;   // 64
+constexpr int64_t kDoubleCost = (int64_t)kWideRopeBoxes * 4;  // 48
+constexpr int64_t kSingleCost = (int64_t)kWideSingleBoxes * 5;  // 30
 
-// Fills the split for one rope unit shape; returns the most loaded CTA's
-// estimated time in 128-row boxes x kSingleCostDen, or -1 if some pair would
-// get more than two heads.
-int64_t fill_wide_split(int heads, int pairs, int single, WideSplit* sp) {
-  sp->single = single;
+// Fills the split for `ndouble` two-head rope units (and one-head units for
+// the heads past them): each unit, two-head units first, goes to the pair
+// with the least estimated time so far (ties: the lower index).  Returns the
+// most loaded pair's estimate, or -1 if some pair would get more than two
+// heads.
+int64_t fill_wide_split(int heads, int pairs, int ndouble, WideSplit* sp) {
+  if (pairs > kMaxCtas / 2) return -1;
   for (int c = 0; c <= pairs; ++c) sp->head[c] = (uint16_t)((int64_t)heads * c / pairs);
-  for (int c = 0; c < pairs; ++c)
-    if (sp->head[c + 1] - sp->head[c] > 2) return -1;
-  // ROPE units (two heads' rope rows, 12 boxes of 16 KiB per CTA, or one
-  // head's, 6 boxes) fill every pair up to an even share of the bytes; a
-  // head's NOPE + ABS units are 16 boxes per CTA (its nope rows' K half and
-  // its half of W_UK^T).
-  const int ropes = single ? heads : (heads + 1) / 2;
-  const int64_t hb = kWideHeadBoxes, rb = single ? kWideSingleBoxes : kWideRopeBoxes;
-  const int64_t total = (int64_t)heads * hb + (int64_t)ropes * rb;
-  int64_t head_bytes = 0, most = 0;
-  int prev = 0;
-  sp->rope[0] = 0;
+  int64_t load[kMaxCtas / 2];
+  int nd[kMaxCtas / 2], ns[kMaxCtas / 2];
   for (int c = 0; c < pairs; ++c) {
     const int nh = sp->head[c + 1] - sp->head[c];
-    head_bytes += (int64_t)nh * hb;
-    int64_t r = (total * (c + 1) / pairs - head_bytes + rb / 2) / rb;
-    if (r < prev) r = prev;
-    if (r > ropes) r = ropes;
-    if (c == pairs - 1) r = ropes;
-    sp->rope[c + 1] = (uint16_t)r;
-    const int64_t cost = (int64_t)nh * hb * kSingleCostDen +
-                         (r - prev) * rb * (single ? kSingleCostNum : kSingleCostDen);
-    if (cost > most) most = cost;
-    prev = (int)r;
+    if (nh > 2) return -1;
+    load[c] = nh * kHeadCost;
+    nd[c] = ns[c] = 0;
+  }
+  const int singles = heads > 2 * ndouble ? heads - 2 * ndouble : 0;
+  for (int k = 0; k < ndouble + singles; ++k) {
+    int best = 0;
+    for (int c = 1; c < pairs; ++c)
+      if (load[c] < load[best]) best = c;
+    if (k < ndouble) {
+      load[best] += kDoubleCost;
+      ++nd[best];
+    } else {
+      load[best] += kSingleCost;
+      ++ns[best];
+    }
+  }
+  sp->ndouble = ndouble;
+  sp->dbl[0] = sp->sgl[0] = 0;
+  int64_t most = 0;
+  for (int c = 0; c < pairs; ++c) {
+    sp->dbl[c + 1] = (uint16_t)(sp->dbl[c] + nd[c]);
+    sp->sgl[c + 1] = (uint16_t)(sp->sgl[c] + ns[c]);
+    if (load[c] > most) most = load[c];
   }
   return most;
 }
@@ -156,13 +165,24 @@ int64_t fill_wide_split(int heads, int pairs, int single, WideSplit* sp) {
 
 bool make_wide_split(int heads, int ctas, WideSplit* sp) {
   const int pairs = ctas / 2;
-  sp->single = 0;
-  if (pairs < 1 || ctas > kMaxCtas) return false;
-  WideSplit one;
-  const int64_t two_cost = fill_wide_split(heads, pairs, 0, sp);
-  const int64_t one_cost = fill_wide_split(heads, pairs, 1, &one);
-  if (two_cost < 0) return false;
-  if (one_cost >= 0 && one_cost < two_cost) *sp = one;
+  if (pairs < 1 || ctas > kMaxCtas || heads < 1) return false;
+  // the fewest quarter boxes on the most loaded pair over every mix of the
+  // two rope-unit shapes; ties keep, in this order, two-head units only,
+  // one-head units only (measured: at 64 heads, 14.46 against 14.83 us at
+  // B = 64 for a mix of the same estimate), then more two-head units
+  const int most_double = (heads + 1) / 2;
+  int64_t best = -1;
+  WideSplit trial;
+  for (int k = 0; k <= most_double; ++k) {
+    const int d = k == 0 ? most_double : k == 1 ? 0 : most_double + 1 - k;
+    if (k > 0 && d == most_double) continue;
+    const int64_t cost = fill_wide_split(heads, pairs, d, &trial);
+    if (cost < 0) return false;
+    if (best < 0 || cost < best) {
+      best = cost;
+      *sp = trial;
+    }
+  }
   return true;
 }
 

@@ -188,53 +188,67 @@ __device__ __forceinline__ int sw128(int row, int col) {
 // tiles in between give the epilogue time to finish each head's q before its
 // absorption needs it, and the step ends on absorptions, whose epilogue needs
 // nothing from the other CTA.
+// A CTA's units in order: NOPE (one per head of the pair), ROPE (the pair's
+// two-head units, then its one-head units), ABS (one per head).
 struct WideSeq {
-  int h0, nh, r0, nr, single;
-  __device__ int units() const { return 2 * nh + nr; }
+  int h0, nh, d0, nd, s0, ns, ndouble;
+  __device__ int units() const { return 2 * nh + nd + ns; }
   __device__ int kind(int u) const {
     if (u < nh) return kUnitNope;
-    if (u < nh + nr) return kUnitRope;
+    if (u < nh + nd + ns) return kUnitRope;
     return kUnitAbs;
   }
-  // head of a NOPE/ABS unit, or rope unit (heads 2 r, 2 r + 1) of a ROPE unit
+  __device__ bool single(int u) const { return u >= nh + nd && u < nh + nd + ns; }
+  // head of a NOPE/ABS unit; for a ROPE unit, the two-head unit's index
+  // (heads 2 i, 2 i + 1), or the head of a one-head unit
   __device__ int head(int u) const {
     if (u < nh) return h0 + u;
-    if (u < nh + nr) return r0 + (u - nh);
-    return h0 + (u - nh - nr);
+    if (u < nh + nd) return d0 + (u - nh);
+    if (u < nh + nd + ns) return 2 * ndouble + s0 + (u - nh - nd);
+    return h0 + (u - nh - nd - ns);
   }
   __device__ int boxes(int u) const {
     const int k = kind(u);
-    return k == kUnitAbs ? 4 : k == kUnitRope && single ? kWideSingleBoxes : kWideAtoms;
+    return k == kUnitAbs ? 4 : single(u) ? kWideSingleBoxes : kWideAtoms;
   }
 };
 
-// Tile addresses in the packed copies (pack_wide_weights): NOPE tile
-// (h, K half, atom), ROPE tile (rope unit, K half, atom) or, for single-head
-// rope units, (head, K half, pair of atoms), W_UK^T tile (h, 128-column tile
-// ct, 64-row atom pa); the CTA of rank `half` takes the W_UK^T tiles of
-// latent columns 256 half.. (ct = 2 half + bx / 2, pa = bx % 2).
-__device__ __forceinline__ const uint8_t* wide_tile(const DecodeArgs& a, int kind, int h,
-                                                    int half, int bx, int single) {
-  if (kind == kUnitNope)
-    return a.wide_qb + ((size_t)(h * 2 + half) * kWideAtoms + bx) * kWideBox;
-  if (kind == kUnitRope)
-    return a.wide_qb + ((size_t)a.heads * 2 * kWideAtoms +
-                        (size_t)(h * 2 + half) * (single ? kWideSingleBoxes : kWideAtoms) + bx) *
-                           kWideBox;
-  return a.wide_ukt + ((size_t)h * 8 + 4 * half + bx) * kWideBox;  // 2 ct + pa
+// Tile index in the packed copies (pack_wide_weights): NOPE tile (h, K half,
+// atom); two-head ROPE tile (unit, K half, atom) after all NOPE tiles;
+// one-head ROPE tile (head, K half, pair of atoms) after the ndouble
+// two-head units' tiles; W_UK^T tile (h, 128-column tile ct, 64-row atom
+// pa), where the CTA of rank `half` takes latent columns 256 half.. (ct =
+// 2 half + bx / 2, pa = bx % 2).
+__device__ __forceinline__ int64_t wide_qb_tile(int heads, int ndouble, int kind, int h, int half,
+                                                int bx, bool single) {
+  if (kind == kUnitNope) return (int64_t)(h * 2 + half) * kWideAtoms + bx;
+  const int64_t rope0 = (int64_t)heads * 2 * kWideAtoms;
+  if (!single) return rope0 + (int64_t)(h * 2 + half) * kWideAtoms + bx;
+  return rope0 + (int64_t)ndouble * 2 * kWideAtoms +
+         (int64_t)((h - 2 * ndouble) * 2 + half) * kWideSingleBoxes + bx;
+}
+__device__ __forceinline__ const uint8_t* wide_tile(const DecodeArgs& a, int ndouble, int kind,
+                                                    int h, int half, int bx, bool single) {
+  if (kind == kUnitAbs) return a.wide_ukt + ((size_t)h * 8 + 4 * half + bx) * kWideBox;
+  return a.wide_qb + (size_t)wide_qb_tile(a.heads, ndouble, kind, h, half, bx, single) * kWideBox;
 }
 
 // Checks builds: whether wide_tile's box lies inside its packed copy (the
-// sizes wide_qb_bytes and wide_ukt_bytes allocate).
-__device__ __forceinline__ bool wide_tile_in_bounds(const DecodeArgs& a, int kind, int h, int half,
-                                                    int bx, int single) {
+// sizes wide_qb_bytes and wide_ukt_bytes allocate) and in its unit's range.
+__device__ __forceinline__ bool wide_tile_in_bounds(const DecodeArgs& a, int ndouble, int kind,
+                                                    int h, int half, int bx, bool single) {
   const int64_t H = a.heads;
-  if (kind == kUnitAbs) return h >= 0 && h < H && bx >= 0 && bx < 4 && (half == 0 || half == 1);
-  const int64_t idx =
-      kind == kUnitNope
-          ? (int64_t)(h * 2 + half) * kWideAtoms + bx
-          : H * 2 * kWideAtoms + (int64_t)(h * 2 + half) * (single ? kWideSingleBoxes : kWideAtoms) + bx;
-  return h >= 0 && bx >= 0 && idx >= 0 && idx < (H + (H + 1) / 2) * 2 * kWideAtoms;
+  if (half != 0 && half != 1) return false;
+  if (kind == kUnitAbs) return h >= 0 && h < H && bx >= 0 && bx < 4;
+  if (kind == kUnitNope) {
+    if (h < 0 || h >= H || bx < 0 || bx >= kWideAtoms) return false;
+  } else if (!single) {
+    if (h < 0 || h >= ndouble || bx < 0 || bx >= kWideAtoms) return false;
+  } else if (h < 2 * ndouble || h >= H || bx < 0 || bx >= kWideSingleBoxes) {
+    return false;
+  }
+  const int64_t idx = wide_qb_tile(a.heads, ndouble, kind, h, half, bx, single);
+  return idx >= 0 && idx < (H + (H + 1) / 2) * 2 * kWideAtoms;
 }
 
 __global__ void __launch_bounds__(kWideThreads, 1)
@@ -261,8 +275,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   const int pair = i >> 1, rank = i & 1;  // cluster (2, 1, 1)
   const uint32_t peer = (uint32_t)(rank ^ 1);
   const int H = a.heads;
-  const WideSeq seq{split.head[pair], split.head[pair + 1] - split.head[pair], split.rope[pair],
-                    split.rope[pair + 1] - split.rope[pair], split.single};
+  const WideSeq seq{split.head[pair],     split.head[pair + 1] - split.head[pair],
+                    split.dbl[pair],      split.dbl[pair + 1] - split.dbl[pair],
+                    split.sgl[pair],      split.sgl[pair + 1] - split.sgl[pair],
+                    split.ndouble};
   const int nu = seq.units();
 
   if (tid == 0) {
@@ -327,10 +343,11 @@ __global__ void __launch_bounds__(kWideThreads, 1)
               !mbar_wait_bounded(&empty[slot], (uint32_t)(((k / kWideSlots) - 1) & 1), kWaitLimit))
             timed_out = true;
           mbar_arrive_expect_tx(&full[slot], kWideBox);
-          if (MLA_IN_BOUNDS(a, wide_tile_in_bounds(a, kind, h, rank, bx, seq.single), 5) &&
+          if (MLA_IN_BOUNDS(a, wide_tile_in_bounds(a, seq.ndouble, kind, h, rank, bx, seq.single(u)), 5) &&
               MLA_IN_BOUNDS(a, slot >= 0 && slot < kWideSlots, 6))
             bulk_g2s_hint(smem + S::oRing + slot * kWideBox,
-                          wide_tile(a, kind, h, rank, bx, seq.single), kWideBox, &full[slot], pol);
+                          wide_tile(a, seq.ndouble, kind, h, rank, bx, seq.single(u)), kWideBox,
+                          &full[slot], pol);
           if (bx == 0 && u < 4) trace_stamp(a, 24 + u);  // unit u's first box issued
         }
       }
@@ -398,7 +415,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             umma(dt, da + 2, db + 2, idq, 1u);
             umma(dt, da + 4, db + 4, idq, 1u);
             umma(dt, da + 6, db + 6, idq, 1u);
-          } else if (kind == kUnitRope && seq.single) {
+          } else if (kind == kUnitRope && seq.single(u)) {
             // one head's 64 rope rows, K atoms 2 bx and 2 bx + 1 (8 KiB
             // each): M = 64, rows in TMEM lanes 32 (r / 16) + r % 16
             const uint64_t db = dxq + (uint64_t)(2 * bx * ((kWideTok * 128) >> 4));
@@ -446,7 +463,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         const int kind = seq.kind(u), h = seq.head(u), nb = seq.boxes(u);
         for (int bx = 0; bx < nb && k < kWideSlots + kWidePrefetch; ++bx, ++k)
           if (k >= kWideSlots)
-            bulk_prefetch_l2(wide_tile(a, kind, h, rank, bx, seq.single), kWideBox);
+            bulk_prefetch_l2(wide_tile(a, seq.ndouble, kind, h, rank, bx, seq.single(u)),
+                             kWideBox);
       }
     }
     // The normalising kernel launched just before wrote xq in this tile's
@@ -560,7 +578,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             }
             mbar_arrive(&qready[j]);
           }
-        } else if (seq.single) {
+        } else if (seq.single(u)) {
           // head h: row 16 (m / 32) + m % 32 in TMEM lanes with m % 32 < 16
           if ((m & 31) < 16 && MLA_IN_BOUNDS(a, h >= 0 && h < H, 7)) {
             const int nt_here = min(kWideHalfTok, a.batch - my0);
@@ -649,16 +667,18 @@ __global__ void __launch_bounds__(192) mla_wide_norm_kernel(const DecodeArgs a) 
 // from 8 j) at r * 128 + ((j ^ (r % 8)) * 16) of its 16 KiB tile: the K-major
 // 128-byte-swizzled layout the kernel's shared-memory descriptors read.
 //   W_QB tiles: NOPE (h, half, atom) = rows 192 h .. 192 h + 127, columns
-//   768 half + 64 atom ..; then ROPE (unit u, half, atom) = rope rows of head
-//   2u (tile rows 0..63) and 2u + 1 (rows 64..127, zeros past the last head).
+//   768 half + 64 atom ..; then two-head ROPE units (u, half, atom) = rope
+//   rows of head 2u (tile rows 0..63) and 2u + 1 (rows 64..127, zeros past
+//   the last head); then one-head ROPE units (head 2 ndouble + v, half, box)
+//   = the head's rope rows at atoms 2 box (rows 0..63) and 2 box + 1.
 //   W_UK^T tiles (h, ct, pa): row r = latent column 128 ct + r, K = W_UK row
 //   64 pa + k.
 __global__ void pack_wide_qb_kernel(const uint16_t* __restrict__ w_qb, uint8_t* __restrict__ out,
-                                    int heads, int single) {
-  const int ropes = (heads + 1) / 2;
+                                    int heads, int ndouble) {
+  const int singles = heads > 2 * ndouble ? heads - 2 * ndouble : 0;
   const int64_t nope_tiles = (int64_t)heads * 2 * kWideAtoms;
-  const int64_t tiles = nope_tiles + (single ? (int64_t)heads * 2 * kWideSingleBoxes
-                                             : (int64_t)ropes * 2 * kWideAtoms);
+  const int64_t double_tiles = (int64_t)ndouble * 2 * kWideAtoms;
+  const int64_t tiles = nope_tiles + double_tiles + (int64_t)singles * 2 * kWideSingleBoxes;
   const int64_t n = tiles * 128 * 8;  // 16-byte chunks
   for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n;
        e += (int64_t)gridDim.x * blockDim.x) {
@@ -670,18 +690,20 @@ __global__ void pack_wide_qb_kernel(const uint16_t* __restrict__ w_qb, uint8_t* 
       const int at = (int)(tile % kWideAtoms), half = (int)((tile / kWideAtoms) & 1);
       row = (tile / (2 * kWideAtoms)) * kHeadRows + r;
       col = kWideKHalf * half + 64 * at;
-    } else if (single) {
-      // (head, half, box): rows 0..63 = its rope rows at K atom 2 box,
-      // rows 64..127 of the tile = the same rows at K atom 2 box + 1
-      const int64_t t = tile - nope_tiles;
-      const int bx = (int)(t % kWideSingleBoxes), half = (int)((t / kWideSingleBoxes) & 1);
-      row = (t / (2 * kWideSingleBoxes)) * kHeadRows + kNope + (r & 63);
-      col = kWideKHalf * half + 64 * (2 * bx + (r >> 6));
-    } else {
+    } else if (tile < nope_tiles + double_tiles) {
+      // two-head unit (u, half, atom): rows 0..63 = head 2u's rope rows,
+      // 64..127 = head 2u + 1's (zeros past the last head)
       const int at = (int)(tile % kWideAtoms), half = (int)((tile / kWideAtoms) & 1);
       const int64_t hd = 2 * (tile / (2 * kWideAtoms) - heads) + (r >> 6);
       if (hd < heads) row = hd * kHeadRows + kNope + (r & 63);
       col = kWideKHalf * half + 64 * at;
+    } else {
+      // one-head unit (head 2 ndouble + v, half, box): rows 0..63 = its rope
+      // rows at K atom 2 box, rows 64..127 = the same rows at K atom 2 box + 1
+      const int64_t t = tile - nope_tiles - double_tiles;
+      const int bx = (int)(t % kWideSingleBoxes), half = (int)((t / kWideSingleBoxes) & 1);
+      row = (2 * (int64_t)ndouble + t / (2 * kWideSingleBoxes)) * kHeadRows + kNope + (r & 63);
+      col = kWideKHalf * half + 64 * (2 * bx + (r >> 6));
     }
     uint4 v = make_uint4(0, 0, 0, 0);
     if (row >= 0) v = *reinterpret_cast<const uint4*>(w_qb + row * kQLora + col + 8 * j);
@@ -756,8 +778,8 @@ size_t wide_qb_bytes(int heads) {
 size_t wide_ukt_bytes(int heads) { return (size_t)heads * 8 * kWideBox; }
 
 cudaError_t pack_wide_weights(const uint16_t* w_qb, const uint16_t* w_uk, uint8_t* qb_tiles,
-                              uint8_t* ukt_tiles, int heads, int single, cudaStream_t stream) {
-  pack_wide_qb_kernel<<<512, 256, 0, stream>>>(w_qb, qb_tiles, heads, single);
+                              uint8_t* ukt_tiles, int heads, int ndouble, cudaStream_t stream) {
+  pack_wide_qb_kernel<<<512, 256, 0, stream>>>(w_qb, qb_tiles, heads, ndouble);
   pack_wide_ukt_kernel<<<512, 256, 0, stream>>>(w_uk, ukt_tiles, heads);
   return cudaGetLastError();
 }

@@ -2,7 +2,7 @@
 // one line per (split, heads, CTAs), all integers.
 //   abs  H C  task[0..C] rope[0..C]
 //   pair H C ok  head[0..C/2] rope[0..C]
-//   wide H C ok single  head[0..C/2] rope[0..C/2]
+//   wide H C ok ndouble  head[0..C/2] dbl[0..C/2] sgl[0..C/2]
 //   small H C K ok most  head[0..C/K] rope[0..C]  (clusters of K CTAs)
 //   choose H S ctas K most  (the cluster size chosen for S SMs)
 #include <cstdio>
@@ -29,9 +29,10 @@ int main() {
       std::printf("\n");
       static mla::WideSplit ws;
       const bool wok = mla::make_wide_split(h, ctas, &ws);
-      std::printf("wide %d %d %d %d", h, ctas, wok ? 1 : 0, wok ? ws.single : 0);
+      std::printf("wide %d %d %d %d", h, ctas, wok ? 1 : 0, wok ? ws.ndouble : 0);
       for (int c = 0; c <= pairs; ++c) std::printf(" %d", wok ? ws.head[c] : 0);
-      for (int c = 0; c <= pairs; ++c) std::printf(" %d", wok ? ws.rope[c] : 0);
+      for (int c = 0; c <= pairs; ++c) std::printf(" %d", wok ? ws.dbl[c] : 0);
+      for (int c = 0; c <= pairs; ++c) std::printf(" %d", wok ? ws.sgl[c] : 0);
       std::printf("\n");
       for (int k = 2; k <= 8; k *= 2) {
         static mla::SmallSplit ss;

@@ -78,37 +78,56 @@ def test_paired_split(splits):
             assert own + r * ROW < max(mean, own) + ROW, (heads, ctas, i)
 
 
+def wide_fields(heads, ctas, v):
+    """(ok, ndouble, heads per pair, two-head units per pair, one-head units
+    per pair) of a wide split line."""
+    pairs = ctas // 2
+    ok, nd = v[0], v[1]
+    head, dbl, sgl = v[2:pairs + 3], v[pairs + 3:2 * pairs + 4], v[2 * pairs + 4:]
+    if not ok:
+        return ok, nd, None, None, None
+    singles = max(0, heads - 2 * nd)
+    return ok, nd, runs(head, heads), runs(dbl, nd), runs(sgl, singles)
+
+
+def wide_cost(nh, d, s):
+    """The planner's estimate in quarter boxes: 4 a 128-row box (16 per head,
+    12 per two-head unit), 5 a 64-row box (6 per one-head unit)."""
+    return 4 * HEAD_BOXES * nh + 4 * ROPE_BOXES * d + 5 * SINGLE_BOXES * s
+
+
 def test_wide_split(splits):
+    """Every head's rope rows are covered once: two-head units cover heads
+    0 .. 2 ndouble - 1, one-head units the rest; no pair has more than two
+    heads; and no pair's estimated time exceeds the least loaded pair's by
+    more than the largest unit (each unit went to the least loaded pair)."""
     for heads, ctas, v in splits["wide"]:
         pairs = ctas // 2
-        ok, single, head, rope = v[0], v[1], v[2:pairs + 3], v[pairs + 3:]
+        ok, nd, nh, d, s = wide_fields(heads, ctas, v)
         assert ok == (heads <= 2 * pairs), (heads, ctas)
         if not ok:
             continue
-        nh = runs(head, heads)
+        assert 0 <= nd <= (heads + 1) // 2
         assert max(nh) <= 2
-        ropes = heads if single else (heads + 1) // 2  # one head's or two heads' rope rows
-        units = runs(rope, ropes)
-        rb = SINGLE_BOXES if single else ROPE_BOXES
-        mean = (HEAD_BOXES * heads + rb * ropes) / pairs
-        for n, u in zip(nh, units):
-            own = n * HEAD_BOXES
-            assert own + u * rb < max(mean, own) + rb, (heads, ctas)
+        assert sum(d) == nd and sum(s) == max(0, heads - 2 * nd)
+        cost = [wide_cost(*x) for x in zip(nh, d, s)]
+        # a pair that got a unit was the least loaded when it did
+        for c in range(pairs):
+            if d[c] + s[c]:
+                assert cost[c] <= min(cost) + 4 * ROPE_BOXES, (heads, ctas, c)
 
 
 def test_wide_split_shapes_on_76_pairs(splits):
-    """The cases the wide kernel's measurements rest on (152 CTAs): 64 heads
-    take single-head rope units (at most 22 boxes per CTA, against 28 with
-    two-head units); 127 and 128 heads keep two-head units (at most 44)."""
+    """The cases the wide kernel's measurements rest on (152 CTAs): mixing the
+    rope-unit shapes brings 127 and 128 heads from 44 boxes on the most
+    loaded CTA (two-head units only) to 40; 64 heads stay at 22 (one-head
+    units only gave 22, two-head units 28); 16 heads at 16."""
     got = {h: v for h, c, v in splits["wide"] if c == 152}
-    for heads, single, most in ((64, 1, 22), (127, 0, 44), (128, 0, 44), (16, 0, 16)):
-        v = got[heads]
-        head, rope = v[2:79], v[79:]
-        nh = runs(head, heads)
-        units = runs(rope, heads if v[1] else (heads + 1) // 2)
-        rb = SINGLE_BOXES if v[1] else ROPE_BOXES
-        assert v[1] == single, heads
-        assert max(n * HEAD_BOXES + u * rb for n, u in zip(nh, units)) == most, heads
+    for heads, most in ((64, 22), (127, 40), (128, 40), (16, 16)):
+        ok, nd, nh, d, s = wide_fields(heads, 152, got[heads])
+        assert ok
+        boxes = [HEAD_BOXES * n + ROPE_BOXES * a + SINGLE_BOXES * b for n, a, b in zip(nh, d, s)]
+        assert max(boxes) == most, (heads, max(boxes))
 
 
 SMALL_ROWS = 1536 * 2 + 512 * 2  # one nope row of the small-batch kernel: Q_B row + W_UK row
