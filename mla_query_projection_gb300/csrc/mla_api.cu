@@ -31,6 +31,7 @@ struct mla_query {
   mla::PairSplit pair_split;  // paired absorbing kernel: per-pair heads, per-CTA rope
   int pair_ctas;              // its grid (even), 0 if it cannot run on this device
   bool pair16;                // its 16-token flavour can run too
+  bool pair_balanced;         // no CTA of it holds more than 10% above the mean bytes
   uint8_t* wide_qb;           // wide kernel: library-owned W_QB tiles
   uint8_t* wide_ukt;          // wide kernel: library-owned W_UK^T tiles
   uint8_t* wide_xq;           // wide kernel: normalised xq in tile layout
@@ -94,16 +95,31 @@ enum class Kernel { kSmall, kAbsorbMma, kAbsorbPair, kWide, kHandoff };
 // head through distributed shared memory, where the partials kernel makes an
 // L2 round trip, but its per-row FMA work is slower than the paired kernel's
 // tensor-core tiles.
+//
+// Among the tensor-core kernels up to 16 tokens: the paired kernel, even
+// where whole half-heads leave its CTAs unbalanced (its time hardly grows
+// with the tokens: 80 heads, 8 tokens 13.0 against 20.9 us for the partials
+// kernel; 96 heads 13.0 / 24.6; 48 heads 7.4 / 12.4; 16 heads and 16 tokens
+// 9.9 / 12.2), except at few heads and tokens, where the partials kernel's
+// even split wins (8 heads, 2 tokens 5.0 against 7.3; 16 heads, 4 tokens
+// 6.9 / 7.3; 32 heads, 2 tokens 8.0 / 7.3 goes to the paired kernel).
+bool partials_first(const mla_query* h, int batch) {
+  return !h->pair_balanced && h->heads <= 24 && h->heads * batch <= 64;
+}
+
 int pick_kernel(const mla_query* h, int batch, Kernel* k, int* nt) {
   int path = h->path;
   if (path == MLA_PATH_AUTO)
-    path = batch == 1 && h->pair_ctas == 0 && h->small_ctas > 0 ? MLA_PATH_FMA : MLA_PATH_MMA;
+    path = batch == 1 && !h->pair_balanced && h->small_ctas > 0 ? MLA_PATH_FMA : MLA_PATH_MMA;
   if (path == MLA_PATH_FMA) {
     if (batch > 8 || h->small_ctas == 0) return MLA_EUNSUPPORTED;
     *k = Kernel::kSmall;
     *nt = batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 4 ? 4 : 8;
   } else if (path == MLA_PATH_MMA) {
-    if (batch <= 8 && h->pair_ctas > 0) {
+    if (batch <= 16 && partials_first(h, batch)) {
+      *k = Kernel::kAbsorbMma;
+      *nt = batch <= 8 ? 8 : 16;
+    } else if (batch <= 8 && h->pair_ctas > 0) {
       *k = Kernel::kAbsorbPair;
       *nt = 8;
     } else if (batch <= 16 && h->pair_ctas > 0 && h->pair16) {
@@ -205,18 +221,19 @@ int mla_query_create(mla_query_t* out, int num_heads, const void* w_qb, const vo
 #endif
   }
   // The paired kernel gives each CTA whole half-heads (256 KiB of weights per
-  // head); it is used only where that keeps the CTAs balanced, i.e. no CTA
-  // holds more than 10% above the average bytes per CTA.
+  // head). Balanced means no CTA holds more than 10% above the average bytes
+  // per CTA; where it is not, one token takes the FMA kernel and few heads
+  // and tokens the partials kernel (pick_kernel).
   h->pair_ctas = h->num_sms & ~1;
   {
     const int pairs = h->pair_ctas / 2;
-    const int64_t most = (int64_t)((num_heads + pairs - 1) / pairs) * 4 * 65536;
-    const int64_t avg = (int64_t)num_heads * (8 * 65536 + 64 * 3072) / h->pair_ctas;
-    if (pairs < 1 || 10 * most > 11 * avg ||
-        !mla::make_pair_split(num_heads, h->pair_ctas, &h->pair_split) ||
+    if (pairs < 1 || !mla::make_pair_split(num_heads, h->pair_ctas, &h->pair_split) ||
         !mla::pair_kernel_fits(h->pair_ctas, 8))
       h->pair_ctas = 0;
     h->pair16 = h->pair_ctas > 0 && mla::pair_kernel_fits(h->pair_ctas, 16);
+    const int64_t most = (int64_t)((num_heads + pairs - 1) / (pairs > 0 ? pairs : 1)) * 4 * 65536;
+    const int64_t avg = (int64_t)num_heads * (8 * 65536 + 64 * 3072) / (h->pair_ctas > 0 ? h->pair_ctas : 1);
+    h->pair_balanced = h->pair_ctas > 0 && 10 * most <= 11 * avg;
   }
   // Wide kernel (17 tokens and more): its split decides the rope tiles' shape.
   if (mla::prepare_wide_kernel() != cudaSuccess) goto fail;
@@ -227,11 +244,12 @@ int mla_query_create(mla_query_t* out, int num_heads, const void* w_qb, const vo
   {
     // Device memory for the kernels the dispatch can reach with this head
     // count on this device, and nothing else: the partials kernel where the
-    // paired kernel cannot serve every batch of up to 16 tokens, the wide
-    // kernel's tiled weight copies where it runs, and the hand-off kernel's
-    // packed W_UK and q buffer only where neither the wide nor the 16-token
-    // paired kernel covers batches above 16.
-    const bool partials = h->pair_ctas == 0 || !h->pair16;
+    // paired kernel cannot serve every batch of up to 16 tokens or leaves it
+    // to the partials kernel (few heads and tokens), the wide kernel's tiled
+    // weight copies where it runs, and the hand-off kernel's packed W_UK and
+    // q buffer only where neither the wide nor the 16-token paired kernel
+    // covers batches above 16.
+    const bool partials = h->pair_ctas == 0 || !h->pair16 || partials_first(h, 1);
     const bool handoff = h->wide_ctas == 0 && !(h->pair_ctas > 0 && h->pair16);
     const bool wide = h->wide_ctas > 0;
     const size_t head = 256;  // err, finished

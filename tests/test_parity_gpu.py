@@ -123,6 +123,19 @@ def test_head_counts(heads, batch):
     assert_parity(inp)
 
 
+@pytest.mark.parametrize("batch,heads", [(2, 96), (8, 80), (16, 96), (16, 40), (8, 16)])
+def test_paired_kernel_unbalanced_head_counts(batch, heads):
+    """Head counts where whole half-heads leave the paired kernel's CTAs
+    unbalanced (some pairs two heads, or none) still take it for more than a
+    few tokens: it meets the oracle there."""
+    inp = S.make_inputs(batch=batch, heads=heads, layout=S.LAYOUT_DS_MLA, pages=16,
+                        seed=800 + heads + batch)
+    st = DecodeStep(inp)
+    assert B.mla_query_kernel_for(st.handle, batch).startswith("mla_absorb_pair_kernel")
+    st.close()
+    assert_parity(inp)
+
+
 @pytest.mark.parametrize("heads", [1, 3, 5, 61, 64, 113, 127])
 @pytest.mark.parametrize("batch", [24, 64])
 def test_wide_kernel_head_counts(heads, batch):
@@ -236,6 +249,11 @@ def test_small_head_count_repeated_calls_close_every_head():
         (40, 64, B.MLA_PATH_AUTO, "mla_wide_norm_kernel+mla_wide_kernel"),
         (1, 16, B.MLA_PATH_AUTO, "mla_small_kernel<1,"),
         (2, 16, B.MLA_PATH_AUTO, "mla_absorb_mma_kernel<8>"),
+        (8, 16, B.MLA_PATH_AUTO, "mla_absorb_pair_kernel<8>"),
+        (16, 16, B.MLA_PATH_AUTO, "mla_absorb_pair_kernel<16>"),
+        (1, 96, B.MLA_PATH_AUTO, "mla_small_kernel<1,"),
+        (2, 96, B.MLA_PATH_AUTO, "mla_absorb_pair_kernel<8>"),
+        (1, 96, B.MLA_PATH_MMA, "mla_absorb_pair_kernel<8>"),
         (1, 16, B.MLA_PATH_FMA, "mla_small_kernel<1,"),
         (2, 16, B.MLA_PATH_FMA, "mla_small_kernel<2,"),
     ],
