@@ -28,7 +28,8 @@ struct mla_query {
   uint8_t* w_uk_packed;  // library-owned repacked copy of W_UK
   float* partial;        // absorbing kernel: FP32 partial absorptions
   mla::AbsSplit split;   // absorbing kernel: per-CTA ranges
-  mla::PairSplit pair_split;  // paired absorbing kernel: per-pair heads, per-CTA rope
+  mla::PairSplit pair_split;    // paired absorbing kernel, up to 8 tokens: heads first
+  mla::PairSplit pair_split16;  // its 16-token flavour: heads spread evenly
   int pair_ctas;              // its grid (even), 0 if it cannot run on this device
   bool pair16;                // its 16-token flavour can run too
   bool pair_balanced;         // no CTA of it holds more than 10% above the mean bytes
@@ -227,7 +228,13 @@ int mla_query_create(mla_query_t* out, int num_heads, const void* w_qb, const vo
   h->pair_ctas = h->num_sms & ~1;
   {
     const int pairs = h->pair_ctas / 2;
-    if (pairs < 1 || !mla::make_pair_split(num_heads, h->pair_ctas, &h->pair_split) ||
+    // Where the heads do not fill every pair, one head on each of the first
+    // pairs measured faster than heads spread evenly for launches of up to 8
+    // tokens (at 64 heads on 76 pairs, one token: 7.85 against 7.92 us; 40
+    // heads, two tokens: 6.80 against 7.32), and slower for 16 tokens (11.25
+    // against 11.04 us at 64 heads); each flavour takes the faster order.
+    if (pairs < 1 || !mla::make_pair_split(num_heads, h->pair_ctas, true, &h->pair_split) ||
+        !mla::make_pair_split(num_heads, h->pair_ctas, false, &h->pair_split16) ||
         !mla::pair_kernel_fits(h->pair_ctas, 8))
       h->pair_ctas = 0;
     h->pair16 = h->pair_ctas > 0 && mla::pair_kernel_fits(h->pair_ctas, 16);
@@ -439,7 +446,7 @@ int decode_impl(mla_query_t h, int batch, const void* q_a, int64_t q_a_stride, c
       e = mla::launch_wide(s64, h->wide_split, h->wide_ctas, st);
     }
   } else if (kern == Kernel::kAbsorbPair && batch <= 16)
-    e = mla::launch_pair(a, h->pair_split, h->pair_ctas, nt, st);
+    e = mla::launch_pair(a, nt == 16 ? h->pair_split16 : h->pair_split, h->pair_ctas, nt, st);
   else if (kern == Kernel::kAbsorbPair) {
     // Batches above 16: the 16-token paired kernel once per slice of 16
     // tokens, every per-token pointer offset to the slice.  Each launch
@@ -458,7 +465,8 @@ int decode_impl(mla_query_t h, int batch, const void* q_a, int64_t q_a_stride, c
       s16.q_pe = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(a.q_pe) +
                                              (int64_t)t0 * a.qp_ts * qbytes);
       s16.q_c = a.q_c != nullptr ? a.q_c + (int64_t)t0 * mla::kQLora : nullptr;
-      e = mla::launch_pair(s16, h->pair_split, h->pair_ctas, s16.batch <= 8 ? 8 : 16, st);
+      e = s16.batch <= 8 ? mla::launch_pair(s16, h->pair_split, h->pair_ctas, 8, st)
+                         : mla::launch_pair(s16, h->pair_split16, h->pair_ctas, 16, st);
     }
   }
   else

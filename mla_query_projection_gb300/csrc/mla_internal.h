@@ -120,8 +120,10 @@ struct PairSplit {
   uint16_t rope[kMaxCtas + 1];
 };
 // Fills `sp` for `ctas` (even) CTAs; false if some pair would get more than
-// two heads.
-bool make_pair_split(int heads, int ctas, PairSplit* sp);
+// two heads.  Heads are spread evenly over the pairs, or, with `heads_first`
+// and no more heads than pairs, pair c takes head c and the pairs past the
+// last head take rope rows only.
+bool make_pair_split(int heads, int ctas, bool heads_first, PairSplit* sp);
 // Whether `ctas` CTAs of the paired kernel (nt = 8 or 16 tokens) can all be
 // resident at once.
 bool pair_kernel_fits(int ctas, int nt);

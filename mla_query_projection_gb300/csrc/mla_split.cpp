@@ -26,10 +26,12 @@ void make_abs_split(int heads, int ctas, AbsSplit* sp) {
   }
 }
 
-bool make_pair_split(int heads, int ctas, PairSplit* sp) {
+bool make_pair_split(int heads, int ctas, bool heads_first, PairSplit* sp) {
   const int pairs = ctas / 2;
   if (pairs < 1 || ctas > kMaxCtas) return false;
-  for (int c = 0; c <= pairs; ++c) sp->head[c] = (uint16_t)((int64_t)heads * c / pairs);
+  for (int c = 0; c <= pairs; ++c)
+    sp->head[c] = heads_first && heads <= pairs ? (uint16_t)(c < heads ? c : heads)
+                                                : (uint16_t)((int64_t)heads * c / pairs);
   for (int c = 0; c < pairs; ++c)
     if (sp->head[c + 1] - sp->head[c] > 2) return false;
   // rope rows fill every CTA up to an even share of the bytes

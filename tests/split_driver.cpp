@@ -1,7 +1,8 @@
 // Prints the create-time work splits of mla_split.cpp for test_splits.py:
 // one line per (split, heads, CTAs), all integers.
 //   abs  H C  task[0..C] rope[0..C]
-//   pair H C ok  head[0..C/2] rope[0..C]
+//   pair H C ok  head[0..C/2] rope[0..C]      (heads spread evenly)
+//   pairf H C ok  head[0..C/2] rope[0..C]     (heads first)
 //   wide H C ok ndouble  head[0..C/2] dbl[0..C/2] sgl[0..C/2]
 //   small H C K ok most  head[0..C/K] rope[0..C]  (clusters of K CTAs)
 //   choose H S ctas K most  (the cluster size chosen for S SMs)
@@ -21,12 +22,14 @@ int main() {
       for (int i = 0; i <= ctas; ++i) std::printf(" %d", as.task[i]);
       for (int i = 0; i <= ctas; ++i) std::printf(" %d", as.rope[i]);
       std::printf("\n");
-      static mla::PairSplit ps;
-      const bool pok = mla::make_pair_split(h, ctas, &ps);
-      std::printf("pair %d %d %d", h, ctas, pok ? 1 : 0);
-      for (int c = 0; c <= pairs; ++c) std::printf(" %d", pok ? ps.head[c] : 0);
-      for (int i = 0; i <= ctas; ++i) std::printf(" %d", pok ? ps.rope[i] : 0);
-      std::printf("\n");
+      for (int first = 0; first < 2; ++first) {
+        static mla::PairSplit ps;
+        const bool pok = mla::make_pair_split(h, ctas, first != 0, &ps);
+        std::printf("%s %d %d %d", first ? "pairf" : "pair", h, ctas, pok ? 1 : 0);
+        for (int c = 0; c <= pairs; ++c) std::printf(" %d", pok ? ps.head[c] : 0);
+        for (int i = 0; i <= ctas; ++i) std::printf(" %d", pok ? ps.rope[i] : 0);
+        std::printf("\n");
+      }
       static mla::WideSplit ws;
       const bool wok = mla::make_wide_split(h, ctas, &ws);
       std::printf("wide %d %d %d %d", h, ctas, wok ? 1 : 0, wok ? ws.ndouble : 0);

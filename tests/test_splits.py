@@ -35,11 +35,11 @@ def splits(tmp_path_factory):
                     "-I", CUDA_INC, os.path.join(HERE, "split_driver.cpp"),
                     os.path.join(CSRC, "mla_split.cpp"), "-o", exe], check=True)
     out = subprocess.run([exe], check=True, capture_output=True, text=True).stdout
-    rows = {"abs": [], "pair": [], "wide": [], "small": [], "choose": []}
+    rows = {"abs": [], "pair": [], "pairf": [], "wide": [], "small": [], "choose": []}
     for line in out.splitlines():
         f = line.split()
         rows[f[0]].append((int(f[1]), int(f[2]), [int(x) for x in f[3:]]))
-    assert all(len(rows[k]) == 9 * 128 for k in ("abs", "pair", "wide", "choose"))
+    assert all(len(rows[k]) == 9 * 128 for k in ("abs", "pair", "pairf", "wide", "choose"))
     assert len(rows["small"]) == 3 * 9 * 128
     return rows
 
@@ -61,8 +61,9 @@ def test_absorbing_split(splits):
             assert t * TASK + r * ROW < max(mean, t * TASK) + ROW, (heads, ctas)
 
 
-def test_paired_split(splits):
-    for heads, ctas, v in splits["pair"]:
+@pytest.mark.parametrize("order", ["pair", "pairf"])
+def test_paired_split(splits, order):
+    for heads, ctas, v in splits[order]:
         pairs = ctas // 2
         ok, head, rope = v[0], v[1:pairs + 2], v[pairs + 2:]
         # refused exactly when some pair would need a third head
@@ -71,6 +72,10 @@ def test_paired_split(splits):
             continue
         nh = runs(head, heads)
         assert max(nh) <= 2
+        if order == "pair" or heads > pairs:  # evenly: counts differ by one at most
+            assert max(nh) - min(nh) <= 1, (heads, ctas)
+        else:  # heads first: one head on each of the first `heads` pairs
+            assert nh == [1] * heads + [0] * (pairs - heads), (heads, ctas)
         rows = runs(rope, 64 * heads)
         mean = (heads * 8 * TASK + 64 * heads * ROW) / ctas
         for i, r in enumerate(rows):
