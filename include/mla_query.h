@@ -74,10 +74,11 @@ extern "C" {
                                   check site s (results are not valid)        */
 
 /* Compute paths (mla_query_set_path). */
-#define MLA_PATH_AUTO 0 /* the default: MLA_PATH_FMA for one token at head
-                           counts the paired tensor-core kernel does not
-                           serve (small counts: the FMA kernel measured
-                           faster there), MLA_PATH_MMA otherwise           */
+#define MLA_PATH_AUTO 0 /* the default: MLA_PATH_FMA for one token at small
+                           head counts (where the FMA kernel's most loaded
+                           CTA carries at most 80% of the paired
+                           tensor-core kernel's bytes; it measured faster
+                           there), MLA_PATH_MMA otherwise                  */
 #define MLA_PATH_FMA 1  /* FP32 FMA dot products: the small-batch kernel
                            (batch <= 8 only; MLA_EUNSUPPORTED above)       */
 #define MLA_PATH_MMA 2  /* BF16 tensor-core tiles, FP32 accumulate           */

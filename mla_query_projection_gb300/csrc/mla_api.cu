@@ -33,6 +33,7 @@ struct mla_query {
   int pair_ctas;              // its grid (even), 0 if it cannot run on this device
   bool pair16;                // its 16-token flavour can run too
   bool pair_balanced;         // no CTA of it holds more than 10% above the mean bytes
+  bool fma_first;             // one token takes the FMA kernel (pick_kernel)
   uint8_t* wide_qb;           // wide kernel: library-owned W_QB tiles
   uint8_t* wide_ukt;          // wide kernel: library-owned W_UK^T tiles
   uint8_t* wide_xq;           // wide kernel: normalised xq in tile layout
@@ -82,15 +83,18 @@ enum class Kernel { kSmall, kAbsorbMma, kAbsorbPair, kWide, kHandoff };
 
 // The default path (measured on GB300, us per step, FMA kernel against the
 // tensor-core kernel the batch would otherwise take):
-//  * one token, head counts the paired kernel does not serve (those the
-//    partials kernel would take, up to about 50 heads on 152 SMs): FP32 FMAs,
-//    8 heads 3.96 against 4.83, 16 heads 4.72 / 5.42, 32 heads 5.73 / 7.39,
-//    48 heads 7.50 / 9.89;
-//  * everything else: tensor cores.  One token where the paired kernel runs:
-//    56 heads 8.07 against 8.01, 64 heads 8.48 / 7.94, 128 heads 14.72 /
-//    14.45; 2, 4 and 8 tokens: 16 heads 6.34 / 6.06, 8.74 / 6.83,
-//    13.75 / 8.16, and at 64 and 128 heads the FMA kernel is 1.4 to 3.6
-//    times slower.
+//  * one token where the FMA kernel's most loaded CTA carries at most 80% of
+//    the paired kernel's bytes (up to 38 heads on 152 SMs: clusters of 4 or
+//    8 CTAs split a head four or eight ways, the paired kernel two ways):
+//    FP32 FMAs, 8 heads 4.00 against 4.83, 16 heads 4.73 / 5.43, 32 heads
+//    5.72 / 6.85, 36 heads 5.72 / 6.78;
+//  * everything else: tensor cores.  One token where both put the same
+//    bytes on their most loaded CTA: 40 heads 7.26 against 6.82, 48 heads
+//    7.29 / 6.98, 64 heads 8.51 / 7.85, 80 heads 13.32 / 12.98, 88 heads
+//    13.04 / 12.90, 96 heads 12.93 / 12.98, 104 heads 12.66 / 12.88, 128
+//    heads 14.59 / 14.40; 2, 4 and 8 tokens: 16 heads 6.32 / 6.11, 8.72 /
+//    6.94, 13.73 / 7.02, and at 64 and 128 heads the FMA kernel is 1.4 to
+//    3.6 times slower.
 // Both stream every weight byte once; after the programmatic-dependent-launch
 // wait a step is bound by its consumers: the FMA kernel's clusters close each
 // head through distributed shared memory, where the partials kernel makes an
@@ -111,7 +115,7 @@ bool partials_first(const mla_query* h, int batch) {
 int pick_kernel(const mla_query* h, int batch, Kernel* k, int* nt) {
   int path = h->path;
   if (path == MLA_PATH_AUTO)
-    path = batch == 1 && !h->pair_balanced && h->small_ctas > 0 ? MLA_PATH_FMA : MLA_PATH_MMA;
+    path = batch == 1 && h->fma_first ? MLA_PATH_FMA : MLA_PATH_MMA;
   if (path == MLA_PATH_FMA) {
     if (batch > 8 || h->small_ctas == 0) return MLA_EUNSUPPORTED;
     *k = Kernel::kSmall;
@@ -242,6 +246,15 @@ int mla_query_create(mla_query_t* out, int num_heads, const void* w_qb, const vo
     const int64_t avg = (int64_t)num_heads * (8 * 65536 + 64 * 3072) / (h->pair_ctas > 0 ? h->pair_ctas : 1);
     h->pair_balanced = h->pair_ctas > 0 && 10 * most <= 11 * avg;
   }
+  // One token takes the FMA kernel where its most loaded CTA carries at most
+  // 80% of the paired kernel's (clusters of 4 or 8 CTAs split a head four or
+  // eight ways where the paired kernel splits it two ways), or where the
+  // paired kernel cannot run.
+  h->fma_first =
+      h->small_ctas > 0 &&
+      (h->pair_ctas == 0 ||
+       5 * mla::small_split_max_bytes(num_heads, h->small_ctas, h->small_split) <=
+           4 * mla::pair_split_max_bytes(h->pair_ctas, h->pair_split));
   // Wide kernel (17 tokens and more): its split decides the rope tiles' shape.
   if (mla::prepare_wide_kernel() != cudaSuccess) goto fail;
   h->wide_ctas = h->num_sms & ~1;

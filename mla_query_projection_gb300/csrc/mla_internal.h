@@ -124,6 +124,8 @@ struct PairSplit {
 // and no more heads than pairs, pair c takes head c and the pairs past the
 // last head take rope rows only.
 bool make_pair_split(int heads, int ctas, bool heads_first, PairSplit* sp);
+// Weight bytes of the most loaded CTA of a paired split.
+int64_t pair_split_max_bytes(int ctas, const PairSplit& sp);
 // Whether `ctas` CTAs of the paired kernel (nt = 8 or 16 tokens) can all be
 // resident at once.
 bool pair_kernel_fits(int ctas, int nt);

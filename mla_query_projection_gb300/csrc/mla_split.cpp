@@ -53,6 +53,17 @@ bool make_pair_split(int heads, int ctas, bool heads_first, PairSplit* sp) {
   return true;
 }
 
+int64_t pair_split_max_bytes(int ctas, const PairSplit& sp) {
+  const int64_t tb = (int64_t)4 * (kTaskRows * kRowBytes + kTaskUkBytes);  // half a head
+  int64_t most = 0;
+  for (int i = 0; i < ctas; ++i) {
+    const int64_t b = (int64_t)(sp.head[i / 2 + 1] - sp.head[i / 2]) * tb +
+                      (int64_t)(sp.rope[i + 1] - sp.rope[i]) * kRowBytes;
+    if (b > most) most = b;
+  }
+  return most;
+}
+
 bool make_small_split(int heads, int ctas, int cluster, SmallSplit* sp) {
   if (cluster != 2 && cluster != 4 && cluster != 8) return false;
   if (ctas < cluster || ctas % cluster != 0 || ctas > kMaxCtas) return false;

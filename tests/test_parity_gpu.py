@@ -123,11 +123,14 @@ def test_head_counts(heads, batch):
     assert_parity(inp)
 
 
-@pytest.mark.parametrize("batch,heads", [(2, 96), (8, 80), (16, 96), (16, 40), (8, 16)])
+@pytest.mark.parametrize("batch,heads", [(1, 40), (1, 96), (2, 96), (4, 40), (8, 80), (16, 96),
+                                         (16, 40), (8, 16)])
 def test_paired_kernel_unbalanced_head_counts(batch, heads):
     """Head counts where whole half-heads leave the paired kernel's CTAs
-    unbalanced (some pairs two heads, or none) still take it for more than a
-    few tokens: it meets the oracle there."""
+    unbalanced (some pairs two heads, or none) still take it: it meets the
+    oracle there, with the heads on the first pairs (up to 8 tokens, fewer
+    heads than pairs) or spread evenly (16 tokens, or more heads than
+    pairs)."""
     inp = S.make_inputs(batch=batch, heads=heads, layout=S.LAYOUT_DS_MLA, pages=16,
                         seed=800 + heads + batch)
     st = DecodeStep(inp)
@@ -251,7 +254,9 @@ def test_small_head_count_repeated_calls_close_every_head():
         (2, 16, B.MLA_PATH_AUTO, "mla_absorb_mma_kernel<8>"),
         (8, 16, B.MLA_PATH_AUTO, "mla_absorb_pair_kernel<8>"),
         (16, 16, B.MLA_PATH_AUTO, "mla_absorb_pair_kernel<16>"),
-        (1, 96, B.MLA_PATH_AUTO, "mla_small_kernel<1,"),
+        (1, 32, B.MLA_PATH_AUTO, "mla_small_kernel<1,"),
+        (1, 40, B.MLA_PATH_AUTO, "mla_absorb_pair_kernel<8>"),
+        (1, 96, B.MLA_PATH_AUTO, "mla_absorb_pair_kernel<8>"),
         (2, 96, B.MLA_PATH_AUTO, "mla_absorb_pair_kernel<8>"),
         (1, 96, B.MLA_PATH_MMA, "mla_absorb_pair_kernel<8>"),
         (1, 16, B.MLA_PATH_FMA, "mla_small_kernel<1,"),
