@@ -225,8 +225,32 @@ __device__ __forceinline__ float bf_round(float v) {
   return __bfloat162float(__float2bfloat16_rn(v));
 }
 
+// Two FP32 values rounded to nearest-even BF16 and packed (low half from
+// `lo`) by one conversion: the same bits as two f2bf_bits, in one
+// instruction instead of two conversions, a shift and an or.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  return static_cast<uint32_t>(f2bf_bits(lo)) | (static_cast<uint32_t>(f2bf_bits(hi)) << 16);
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two FP32 products, each rounded to nearest-even (Blackwell's packed FP32
+// multiply): the same bits as two __fmul_rn.
+__device__ __forceinline__ float2 fmul2_rn(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+// RMSNorm of a BF16 pair: (x * rr) * gamma in FP32, each product rounded to
+// nearest, then rounded to a BF16 pair.
+__device__ __forceinline__ uint32_t rms_scale_bf16x2(uint32_t x, float rr, uint32_t gamma) {
+  const float2 t = fmul2_rn(fmul2_rn(make_float2(bf16lo(x), bf16hi(x)), make_float2(rr, rr)),
+                            make_float2(bf16lo(gamma), bf16hi(gamma)));
+  return pack_bf16x2(t.x, t.y);
 }
 
 // Two FP32 values -> two OCP E4M3 bytes (round to nearest even, saturate to

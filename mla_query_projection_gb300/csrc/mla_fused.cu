@@ -322,14 +322,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float rr = __frsqrt_rn(__fadd_rn(__fdiv_rn(total, 1536.0f), a.eps));
         const uint32_t ww[4] = {xv[t].x, xv[t].y, xv[t].z, xv[t].w};
         uint4 o;
-        o.x = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[0]), rr), bf16lo(gw[0])),
-                          __fmul_rn(__fmul_rn(bf16hi(ww[0]), rr), bf16hi(gw[0])));
-        o.y = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[1]), rr), bf16lo(gw[1])),
-                          __fmul_rn(__fmul_rn(bf16hi(ww[1]), rr), bf16hi(gw[1])));
-        o.z = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[2]), rr), bf16lo(gw[2])),
-                          __fmul_rn(__fmul_rn(bf16hi(ww[2]), rr), bf16hi(gw[2])));
-        o.w = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[3]), rr), bf16lo(gw[3])),
-                          __fmul_rn(__fmul_rn(bf16hi(ww[3]), rr), bf16hi(gw[3])));
+        o.x = rms_scale_bf16x2(ww[0], rr, gw[0]);
+        o.y = rms_scale_bf16x2(ww[1], rr, gw[1]);
+        o.z = rms_scale_bf16x2(ww[2], rr, gw[2]);
+        o.w = rms_scale_bf16x2(ww[3], rr, gw[3]);
         if (tok0 + t >= a.batch) o = make_uint4(0, 0, 0, 0);
         *reinterpret_cast<uint4*>(xq + t * kPitch + 16 * tid) = o;
         // q_c rows (page "mla.query", method store_qc): CTA 0 of the group.
@@ -908,8 +904,7 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
         uint32_t o[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          o[e] = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[e]), rr), bf16lo(gw[e])),
-                             __fmul_rn(__fmul_rn(bf16hi(ww[e]), rr), bf16hi(gw[e])));
+          o[e] = rms_scale_bf16x2(ww[e], rr, gw[e]);
         xb[nt][c] = make_uint4(o[0], o[1], o[2], o[3]);
         if (i == 0 && a.q_c != nullptr && tok < a.batch)
           *reinterpret_cast<uint4*>(a.q_c + (int64_t)tok * kQLora + 192 * warp + 32 * c + 8 * q) =
@@ -1334,8 +1329,7 @@ __global__ void __launch_bounds__(pair_threads<NT>(), 1)
         uint32_t o[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          o[e] = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[e]), rr), bf16lo(gw[e])),
-                             __fmul_rn(__fmul_rn(bf16hi(ww[e]), rr), bf16hi(gw[e])));
+          o[e] = rms_scale_bf16x2(ww[e], rr, gw[e]);
         xb[nt][c] = make_uint4(o[0], o[1], o[2], o[3]);
         if (i == 0 && a.q_c != nullptr && tok < a.batch)
           *reinterpret_cast<uint4*>(a.q_c + (int64_t)tok * kQLora + 192 * warp + 32 * c + 8 * q) =

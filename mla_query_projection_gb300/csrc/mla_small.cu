@@ -328,8 +328,7 @@ __global__ void __maxnreg__(NT >= 4 ? 168 : MLA_SMALL_MAXNREG)
         uint32_t o[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          o[e] = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(vv[e]), rr), bf16lo(gw[e])),
-                             __fmul_rn(__fmul_rn(bf16hi(vv[e]), rr), bf16hi(gw[e])));
+          o[e] = rms_scale_bf16x2(vv[e], rr, gw[e]);
         x[j] = make_uint4(o[0], o[1], o[2], o[3]);
         if constexpr (NT == 1)
           xq1[j] = x[j];

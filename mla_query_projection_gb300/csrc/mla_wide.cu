@@ -648,8 +648,7 @@ __global__ void __launch_bounds__(192) mla_wide_norm_kernel(const DecodeArgs a) 
     uint32_t r[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e)
-      r[e] = pack_bf16x2(__fmul_rn(__fmul_rn(bf16lo(ww[e]), rr), bf16lo(gw[e])),
-                         __fmul_rn(__fmul_rn(bf16hi(ww[e]), rr), bf16hi(gw[e])));
+      r[e] = rms_scale_bf16x2(ww[e], rr, gw[e]);
     o = make_uint4(r[0], r[1], r[2], r[3]);
     if (a.q_c != nullptr) *reinterpret_cast<uint4*>(a.q_c + (int64_t)t * kQLora + 8 * j) = o;
   }
