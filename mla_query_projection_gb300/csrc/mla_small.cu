@@ -226,13 +226,18 @@ __global__ void __maxnreg__(NT >= 4 ? 168 : MLA_SMALL_MAXNREG)
 
   if (warp == kConsumerWarps) {
     // ================= producer: weights only, no PDL wait ============
-    // A stage's copies are issued by separate lanes in one instruction (a Q_B
-    // row of 3 KiB per lane below kSmRows, a W_UK row of 1 KiB per lane from
-    // there to 2 kSmRows): copies
-    // one thread issues complete one after another, copies of different
-    // threads side by side.
+    // A stage's copies are issued by separate lanes in one instruction (Q_B
+    // rows below lane kSmRows, their W_UK rows from there): copies one
+    // thread issues complete one after another, copies of different threads
+    // side by side.  A nope stage goes out as one copy per row, or, where the
+    // CTA's whole share is at most two stages, one copy per two rows: then
+    // both stages' copies are out at once (at 16 heads the second stage's
+    // row copies left 1.15 us after the first's; 4.29 against 4.72 us a
+    // step), while a longer stream keeps more copies in flight with one row
+    // each (two rows a copy measured 9.70 against 8.30 us at 64 heads).
     if (lane == 0) trace_stamp(a, 4);  // the producer starts
     const uint64_t pol = l2_policy_evict_first();
+    const int rpc = nst <= 2 ? 2 : 1;  // nope rows per copy
     if (kSmPrefetch && lane == 0)
       for (int k = SL; k < min(nst, 2 * SL); ++k) small_prefetch_stage<C>(a, seq, k);
     int issued = 0;
@@ -256,14 +261,14 @@ __global__ void __maxnreg__(NT >= 4 ? 168 : MLA_SMALL_MAXNREG)
         __syncwarp();
         if (!MLA_IN_BOUNDS(a, h >= 0 && h < a.heads && p0 >= 0 && p0 + kSmRows <= kNope, 10) ||
             !MLA_IN_BOUNDS(a, slot >= 0 && slot < SL, 11)) {
-        } else if (lane < kSmRows)
-          bulk_g2s_hint(buf + lane * kRowBytes,
-                        a.w_qb + ((int64_t)h * kHeadRows + p0 + lane) * kQLora, kRowBytes,
-                        &full[slot], pol);
-        else if (lane < 2 * kSmRows)
-          bulk_g2s_hint(buf + kSmQbBytes + (lane - kSmRows) * kKvLora * 2,
-                        a.w_uk + ((int64_t)h * kNope + p0 + lane - kSmRows) * kKvLora,
-                        kKvLora * 2, &full[slot], pol);
+        } else if (lane < kSmRows / rpc)
+          bulk_g2s_hint(buf + lane * rpc * kRowBytes,
+                        a.w_qb + ((int64_t)h * kHeadRows + p0 + lane * rpc) * kQLora,
+                        (uint32_t)(rpc * kRowBytes), &full[slot], pol);
+        else if (lane >= kSmRows && lane < kSmRows + kSmRows / rpc)
+          bulk_g2s_hint(buf + kSmQbBytes + (lane - kSmRows) * rpc * kKvLora * 2,
+                        a.w_uk + ((int64_t)h * kNope + p0 + (lane - kSmRows) * rpc) * kKvLora,
+                        (uint32_t)(rpc * kKvLora * 2), &full[slot], pol);
       } else {
         const int r = seq.r0 + (k - seq.nope()) * kSmRows;
         const int n = min(kSmRows, seq.r1 - r);
