@@ -1291,18 +1291,26 @@ __global__ void __launch_bounds__(pair_threads<NT>(), 1)
       gam[c] = *reinterpret_cast<const uint4*>(a.gamma_q + 192 * warp + 32 * c + 8 * q);
     pdl_wait();
     if (tid == 0) trace_stamp(a, 3);
-    // q_a RMSNorm -> B fragments xb[nt][c] (token 8 nt + g, K 192 w + 32 c + 8 q + 0..7)
+    // q_a RMSNorm -> B fragments xb[nt][c] (token 8 nt + g, K 192 w + 32 c + 8 q + 0..7).
+    // Every n-tile's loads go out before the first sum of squares (one load
+    // round trip for 16 tokens: 10.51 against 10.58 us at B = 16, H = 64).
     uint4 xb[NTL][6];
+#pragma unroll
+    for (int nt = 0; nt < NTL; ++nt) {
+      const int tok = 8 * nt + g;
+#pragma unroll
+      for (int c = 0; c < 6; ++c)
+        xb[nt][c] = tok < a.batch
+                        ? *reinterpret_cast<const uint4*>(a.q_a + (int64_t)tok * a.q_a_stride +
+                                                          192 * warp + 32 * c + 8 * q)
+                        : make_uint4(0, 0, 0, 0);
+    }
 #pragma unroll
     for (int nt = 0; nt < NTL; ++nt) {
       const int tok = 8 * nt + g;
       float ss = 0.f;
 #pragma unroll
       for (int c = 0; c < 6; ++c) {
-        xb[nt][c] = tok < a.batch
-                        ? *reinterpret_cast<const uint4*>(a.q_a + (int64_t)tok * a.q_a_stride +
-                                                          192 * warp + 32 * c + 8 * q)
-                        : make_uint4(0, 0, 0, 0);
         const uint32_t ww[4] = {xb[nt][c].x, xb[nt][c].y, xb[nt][c].z, xb[nt][c].w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
