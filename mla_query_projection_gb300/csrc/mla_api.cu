@@ -84,7 +84,7 @@ enum class Kernel { kSmall, kAbsorbMma, kAbsorbPair, kWide, kHandoff };
 // The default path (measured on GB300, us per step, FMA kernel against the
 // tensor-core kernel the batch would otherwise take):
 //  * one token where the FMA kernel's most loaded CTA carries at most 80% of
-//    the paired kernel's bytes (up to 38 heads on 152 SMs: clusters of 4 or
+//    the paired kernel's bytes (up to 36 heads on GB300: clusters of 4 or
 //    8 CTAs split a head four or eight ways, the paired kernel two ways):
 //    FP32 FMAs, 8 heads 4.00 against 4.83, 16 heads 4.73 / 5.43, 32 heads
 //    5.72 / 6.85, 36 heads 5.72 / 6.78;

@@ -3,6 +3,9 @@
 //   abs  H C  task[0..C] rope[0..C]
 //   pair H C ok  head[0..C/2] rope[0..C]      (heads spread evenly)
 //   pairf H C ok  head[0..C/2] rope[0..C]     (heads first)
+//   pairmax H C most                        (most loaded CTA, heads first)
+//   fmafirst H most_fma most_pair fma         (152 SMs; at most 76, 36 and 15
+//                                              clusters of 2, 4 and 8, as on GB300)
 //   wide H C ok ndouble  head[0..C/2] dbl[0..C/2] sgl[0..C/2]
 //   small H C K ok most  head[0..C/K] rope[0..C]  (clusters of K CTAs)
 //   choose H S ctas K most  (the cluster size chosen for S SMs)
@@ -29,6 +32,16 @@ int main() {
         for (int c = 0; c <= pairs; ++c) std::printf(" %d", pok ? ps.head[c] : 0);
         for (int i = 0; i <= ctas; ++i) std::printf(" %d", pok ? ps.rope[i] : 0);
         std::printf("\n");
+        if (first && pok)
+          std::printf("pairmax %d %d %lld\n", h, ctas, (long long)mla::pair_split_max_bytes(ctas, ps));
+        if (first && pok && ctas == 152) {
+          static mla::SmallSplit fs;
+          const int gb300[3] = {76, 36, 15};
+          const int fc = mla::choose_small_split(h, 152, gb300, &fs);
+          const long long fm = fc ? (long long)mla::small_split_max_bytes(h, fc, fs) : 0;
+          const long long pm = (long long)mla::pair_split_max_bytes(ctas, ps);
+          std::printf("fmafirst %d %d %lld %lld %d\n", h, ctas, fm, pm, fc > 0 && 5 * fm <= 4 * pm);
+        }
       }
       static mla::WideSplit ws;
       const bool wok = mla::make_wide_split(h, ctas, &ws);

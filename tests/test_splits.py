@@ -35,7 +35,8 @@ def splits(tmp_path_factory):
                     "-I", CUDA_INC, os.path.join(HERE, "split_driver.cpp"),
                     os.path.join(CSRC, "mla_split.cpp"), "-o", exe], check=True)
     out = subprocess.run([exe], check=True, capture_output=True, text=True).stdout
-    rows = {"abs": [], "pair": [], "pairf": [], "wide": [], "small": [], "choose": []}
+    rows = {"abs": [], "pair": [], "pairf": [], "pairmax": [], "fmafirst": [], "wide": [],
+            "small": [], "choose": []}
     for line in out.splitlines():
         f = line.split()
         rows[f[0]].append((int(f[1]), int(f[2]), [int(x) for x in f[3:]]))
@@ -99,6 +100,36 @@ def wide_cost(nh, d, s):
     """The planner's estimate in quarter boxes: 4 a 128-row box (16 per head,
     12 per two-head unit), 5 a 64-row box (6 per one-head unit)."""
     return 4 * HEAD_BOXES * nh + 4 * ROPE_BOXES * d + 5 * SINGLE_BOXES * s
+
+
+def test_paired_split_max_bytes(splits):
+    """pair_split_max_bytes is the most loaded CTA of the heads-first split:
+    half a head's four tasks per head of its pair plus its rope rows."""
+    most = {(h, c): v[0] for h, c, v in splits["pairmax"]}
+    n = 0
+    for heads, ctas, v in splits["pairf"]:
+        if not v[0]:
+            continue
+        pairs = ctas // 2
+        nh = runs(v[1:pairs + 2], heads)
+        rows = runs(v[pairs + 2:], 64 * heads)
+        loads = [nh[i // 2] * 4 * TASK + r * ROW for i, r in enumerate(rows)]
+        assert most[(heads, ctas)] == max(loads), (heads, ctas)
+        n += 1
+    assert n > 600
+
+
+def test_one_token_dispatch_boundary(splits):
+    """One token takes the FMA kernel where its most loaded CTA carries at
+    most 80 % of the paired kernel's: on 152 SMs with GB300's cluster limits
+    that is every head count up to 36 (clusters of 8 or 4 split a head four
+    or eight ways; 37 heads no longer fit 36 clusters of four), and none
+    above (both kernels then put whole half-heads on their most loaded CTA)."""
+    got = {h: v for h, c, v in splits["fmafirst"]}
+    assert sorted(got) == list(range(1, 129))
+    for h, (fm, pm, fma) in got.items():
+        assert fma == (5 * fm <= 4 * pm), h
+        assert fma == (h <= 36), (h, fm, pm)
 
 
 def test_wide_split(splits):
