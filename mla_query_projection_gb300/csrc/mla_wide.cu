@@ -66,6 +66,7 @@ constexpr int kWideSlots = 5;
 #define MLA_WIDE_PREFETCH 4
 #endif
 constexpr int kWidePrefetch = MLA_WIDE_PREFETCH;
+constexpr int kWidePrefetch2 = 4;  // the second wave, after the wait (see the xq copies)
 constexpr int kWideBox = 128 * 128;          // one 128-row x 128 B box (16 KiB)
 constexpr int kWideThreads = 256;
 // TMEM columns: Q_B tiles [2 buffers][2 K-quarter partials][64 tokens] at
@@ -481,6 +482,29 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       if (lane < kWideAtoms) {
         const uint8_t* src = a.wide_xq + ((size_t)rank * kWideAtoms + lane) * (kWideTok * 128);
         bulk_g2s(smem + S::oXq + lane * (kWideTok * 128), src, kWideTok * 128, xqready);
+      }
+      // A second wave of kWidePrefetch2 boxes into L2 once xq is on its way:
+      // the ring and the first wave have landed by now, and the slots free
+      // only when the MMAs start.  Measured at B = 64 (us per step, waves of
+      // 3 / 4 / 5 / 6 boxes against none): H = 128 19.70 / 19.65 / 19.66 /
+      // 19.72 against 20.19, H = 96 17.31 / 17.26 / 17.24 / 17.28 against
+      // 17.56; at H = 64 (about 22 boxes a CTA) it gained nothing and lost up
+      // to 0.13 us at 24 and 32 tokens, so only CTAs with more than 28 boxes
+      // take it.
+      if (lane == 31) {
+        int total = 0;
+        for (int u = 0; u < nu; ++u) total += seq.boxes(u);
+        if (total > 28) {
+          const int k0 = kWideSlots + kWidePrefetch, k1 = k0 + kWidePrefetch2;
+          int k = 0;
+          for (int u = 0; u < nu && k < k1; ++u) {
+            const int kind = seq.kind(u), h = seq.head(u), nb = seq.boxes(u);
+            for (int bx = 0; bx < nb && k < k1; ++bx, ++k)
+              if (k >= k0)
+                bulk_prefetch_l2(wide_tile(a, seq.ndouble, kind, h, rank, bx, seq.single(u)),
+                                 kWideBox);
+          }
+        }
       }
     }
 
