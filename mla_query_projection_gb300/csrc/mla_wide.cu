@@ -508,6 +508,12 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       }
     }
 
+    // The paged KV insert of the launch's tokens, one warp a token, before
+    // the first epilogue is due (its inputs are current after the wait).
+    // In the normalising kernel it lengthened the chain before the MMAs:
+    // B = 64 H = 128 fp8_ds_mla 19.73 -> 19.05 us, H = 64 14.40 -> 13.55.
+    if (warp == 4)
+      for (int t = (int)blockIdx.x; t < a.batch; t += (int)gridDim.x) kv_insert_warp(a, t, lane);
     if (warp >= 4) {
       // ================= epilogue: TMEM lanes 0..127 ===================
       const int m = tid - 128;  // row of the tile = TMEM lane
@@ -640,19 +646,17 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 // RMSNorm of the q_a rows of up to 64 tokens for the wide kernel (page
 // "mla.query": xq = bf16((q_a * rr) * gamma_q), rr = 1/sqrt(sum q_a^2 / 1536 +
 // eps)), written as q_c and into the wide CTAs' swizzled tile layout (rows of
-// tokens beyond the batch as zeros), plus the paged KV insert of each token.
-// One CTA of 192 threads per token: thread j takes columns 8j..8j+7.
+// tokens beyond the batch as zeros).  One CTA of 192 threads per token:
+// thread j takes columns 8j..8j+7.  (The paged KV insert runs in the wide
+// kernel: every microsecond this kernel takes delays the wide kernel's
+// MMAs.)
 __global__ void __launch_bounds__(192) mla_wide_norm_kernel(const DecodeArgs a) {
   __shared__ float part[6];
-  __shared__ float red2[2];
   const int t = blockIdx.x, j = threadIdx.x, lane = j & 31, warp = j >> 5;
   pdl_launch_dependents();  // the wide kernel streams weights meanwhile
   if (j == 0) trace_stamp(a, 60);  // normalising CTA t started
   pdl_wait();
   if (j == 0) trace_stamp(a, 61);  // its wait passed
-  // the KV insert's inputs (warps 0-1) load together with q_a, not after it
-  KvLoads kvl;
-  if (t < a.batch && warp < 2) kvl = kv_insert_load(a, t, j);
   uint4 o = make_uint4(0, 0, 0, 0);
   if (t < a.batch) {
     const uint4 v = *reinterpret_cast<const uint4*>(a.q_a + (int64_t)t * a.q_a_stride + 8 * j);
@@ -681,7 +685,6 @@ __global__ void __launch_bounds__(192) mla_wide_norm_kernel(const DecodeArgs a) 
   const size_t xo = ((size_t)(half * kWideAtoms + at) * kWideTok) * 128 + t * 128 + ((c ^ (t & 7)) << 4);
   if (MLA_IN_BOUNDS(a, t < kWideTok && xo + 16 <= (size_t)2 * kWideAtoms * kWideTok * 128, 9))
     *reinterpret_cast<uint4*>(a.wide_xq + xo) = o;
-  if (t < a.batch && warp < 2) kv_insert_loaded(a, j, red2, kvl);
   __syncthreads();
   if (j == 0) trace_stamp(a, 62);  // its rows written
 }
