@@ -488,13 +488,13 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       // only when the MMAs start.  Measured at B = 64 (us per step, waves of
       // 3 / 4 / 5 / 6 boxes against none): H = 128 19.70 / 19.65 / 19.66 /
       // 19.72 against 20.19, H = 96 17.31 / 17.26 / 17.24 / 17.28 against
-      // 17.56; at H = 64 (about 22 boxes a CTA) it gained nothing and lost up
-      // to 0.13 us at 24 and 32 tokens, so only CTAs with more than 28 boxes
-      // take it.
+      // 17.56.  CTAs with more than 16 boxes take it (more than 28: H = 96
+      // 16.54, H = 64 13.57 us; more than 16: 16.38 and 13.54, 24 and 32
+      // tokens at H = 64 unchanged).
       if (lane == 31) {
         int total = 0;
         for (int u = 0; u < nu; ++u) total += seq.boxes(u);
-        if (total > 28) {
+        if (total > 16) {
           const int k0 = kWideSlots + kWidePrefetch, k1 = k0 + kWidePrefetch2;
           int k = 0;
           for (int u = 0; u < nu && k < k1; ++u) {
