@@ -1294,16 +1294,23 @@ __global__ void __launch_bounds__(pair_threads<NT>(), 1)
     // q_a RMSNorm -> B fragments xb[nt][c] (token 8 nt + g, K 192 w + 32 c + 8 q + 0..7).
     // Every n-tile's loads go out before the first sum of squares (one load
     // round trip for 16 tokens: 10.51 against 10.58 us at B = 16, H = 64).
+    // The 16-token flavour reads q_a through the read-only path (q_a is an
+    // input of the step, complete once the wait has passed): 9.73 against
+    // 10.54 us at B = 16, H = 64; the 8-token flavour keeps plain loads
+    // (7.84 against 7.79 us at B = 1 with the read-only path).
     uint4 xb[NTL][6];
 #pragma unroll
     for (int nt = 0; nt < NTL; ++nt) {
       const int tok = 8 * nt + g;
 #pragma unroll
-      for (int c = 0; c < 6; ++c)
-        xb[nt][c] = tok < a.batch
-                        ? *reinterpret_cast<const uint4*>(a.q_a + (int64_t)tok * a.q_a_stride +
-                                                          192 * warp + 32 * c + 8 * q)
-                        : make_uint4(0, 0, 0, 0);
+      for (int c = 0; c < 6; ++c) {
+        const uint4* src = reinterpret_cast<const uint4*>(a.q_a + (int64_t)tok * a.q_a_stride +
+                                                          192 * warp + 32 * c + 8 * q);
+        if constexpr (NT == 16)
+          xb[nt][c] = tok < a.batch ? __ldg(src) : make_uint4(0, 0, 0, 0);
+        else
+          xb[nt][c] = tok < a.batch ? *src : make_uint4(0, 0, 0, 0);
+      }
     }
 #pragma unroll
     for (int nt = 0; nt < NTL; ++nt) {
